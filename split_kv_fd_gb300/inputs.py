@@ -1,0 +1,95 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle.
+
+This module holds no arithmetic of the method: it only draws numbers.
+
+Recipe (one ``torch.Generator`` on the target device, seeded with the
+workload's seed; draws in this order):
+  1. lengths: ``randint(1, N + 1, (B,))`` if the workload is ragged, else N;
+  2. q: float32 N(0, 1), shape [B, H, d];
+  3. K: float32 N(0, 1) * k_scale, shape [B, H, N, d], drawn in chunks of
+     the flattened tensor;
+  4. V: float32 N(0, 1), shape [B, H, N, d], drawn the same way;
+each cast to the storage dtype with round-to-nearest-even.  Rows past a
+sequence's length are filled with NaN, so a read past the end shows up as a
+NaN in the result.
+"""
+from __future__ import annotations
+
+import torch
+
+from .workloads import Workload
+
+TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def _fill_normal(t: torch.Tensor, g: torch.Generator, factor: float, chunk: int) -> None:
+    flat = t.view(-1)
+    n = flat.numel()
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        x = torch.randn(e - s, generator=g, device=t.device, dtype=torch.float32)
+        if factor != 1.0:
+            x.mul_(factor)
+        flat[s:e].copy_(x)
+
+
+def make_lengths(w: Workload, device="cpu", seed: int | None = None) -> torch.Tensor:
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+    if w.ragged:
+        return torch.randint(1, w.N + 1, (w.B,), generator=g, device=device).to(torch.int32)
+    return torch.full((w.B,), w.N, dtype=torch.int32, device=device)
+
+
+def make_inputs(w: Workload, device="cpu", seed: int | None = None,
+                nan_pad: bool = True, chunk: int = 1 << 26):
+    """Return ``(q, K, V, lens)`` for workload ``w`` on ``device``."""
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+    dt = TORCH_DTYPES[w.dtype]
+    if w.ragged:
+        lens = torch.randint(1, w.N + 1, (w.B,), generator=g, device=device).to(torch.int32)
+    else:
+        lens = torch.full((w.B,), w.N, dtype=torch.int32, device=device)
+    q = torch.empty((w.B, w.H, w.d), dtype=dt, device=device)
+    k = torch.empty((w.B, w.H, w.N, w.d), dtype=dt, device=device)
+    v = torch.empty((w.B, w.H, w.N, w.d), dtype=dt, device=device)
+    _fill_normal(q, g, 1.0, chunk)
+    _fill_normal(k, g, w.k_scale, chunk)
+    _fill_normal(v, g, 1.0, chunk)
+    if nan_pad and w.ragged:
+        for b, n in enumerate(lens.tolist()):
+            if n < w.N:
+                k[b, :, n:, :] = float("nan")
+                v[b, :, n:, :] = float("nan")
+    return q, k, v, lens
+
+
+def random_case(B, H, N, d, dtype="bf16", lens=None, seed=0, device="cpu",
+                k_scale=1.0, nan_pad=True):
+    """A small seeded case with explicit shapes (for parity and edge tests).
+
+    ``lens``: None (all N), an int list of length B, or "ragged" (drawn
+    uniformly from [0, N] so that empty sequences occur).
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    dt = TORCH_DTYPES[dtype]
+    if lens is None:
+        lt = torch.full((B,), N, dtype=torch.int32, device=device)
+    elif isinstance(lens, str) and lens == "ragged":
+        lt = torch.randint(0, N + 1, (B,), generator=g, device=device).to(torch.int32)
+    else:
+        lt = torch.tensor(list(lens), dtype=torch.int32, device=device)
+    q = torch.empty((B, H, d), dtype=dt, device=device)
+    k = torch.empty((B, H, N, d), dtype=dt, device=device)
+    v = torch.empty((B, H, N, d), dtype=dt, device=device)
+    _fill_normal(q, g, 1.0, 1 << 24)
+    _fill_normal(k, g, k_scale, 1 << 24)
+    _fill_normal(v, g, 1.0, 1 << 24)
+    if nan_pad:
+        for b, n in enumerate(lt.tolist()):
+            if n < N:
+                k[b, :, n:, :] = float("nan")
+                v[b, :, n:, :] = float("nan")
+    return q, k, v, lt

@@ -1,0 +1,51 @@
+"""The five decode-attention workloads, as plain data.
+
+Each entry names a synthetic workload by what it is: shapes, storage dtype,
+split count (0 = automatic), the factor applied to K's draws and whether the
+lengths are ragged.  Nothing here computes anything of the method.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int            # batch (sequences)
+    H: int            # heads
+    N: int            # padded KV length per sequence
+    d: int            # head dimension
+    dtype: str        # storage dtype of q, K, V: "f32" | "f16" | "bf16"
+    out_dtype: str    # dtype of out
+    num_splits: int   # 0 => automatic decomposition
+    k_scale: float = 1.0   # K draws are N(0,1) * k_scale
+    ragged: bool = False   # lengths ~ U[1, N] per sequence, else all N
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("decode_b1_h1_n1k_d64_f32_p4", 1, 1, 1024, 64, "f32", "f32", 4),
+        Workload("decode_b1_h8_n4k_d128_f16_p4", 1, 8, 4096, 128, "f16", "f16", 4),
+        Workload("decode_b8_h32_n32k_d128_bf16", 8, 32, 32768, 128, "bf16", "bf16", 0),
+        Workload("decode_b1_h32_n128k_d128_bf16_k8", 1, 32, 131072, 128, "bf16", "bf16", 0,
+                 k_scale=8.0),
+        Workload("decode_ragged_b16_h32_n64k_d128_bf16", 16, 32, 65536, 128, "bf16", "bf16", 0,
+                 ragged=True),
+    ]
+}
+
+# in the order the workloads were specified
+ORDER = list(WORKLOADS)
+
+# the workload the benchmark times by default: uniform 32K-token sequences
+BENCH_DEFAULT = "decode_b8_h32_n32k_d128_bf16"
+
+ELEMENT_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
