@@ -1,0 +1,447 @@
+"""Benchmark of split-KV decode attention (FlashDecoding) on GB300.
+
+One step = one fused decode (split kernel + in-kernel merge, automatic
+decomposition) over the whole workload, inputs resident in HBM.  Prints ONE
+JSON line (rank 0):
+
+  value      KV-GB/s over all ranks: valid K+V bytes of every rank's step
+             divided by the max over ranks of the device time per step
+  roofline   the split kernel's achieved bytes/s (algorithmic bytes per
+             launch / mean launch time from CUDA events on its stream)
+             against the measured HBM copy bandwidth
+  e2e        the same metric through the public API from pinned host
+             buffers: every step copies q, K, V, lengths to the device,
+             decodes, and reads out and lse back
+  cpu_baseline  the float64 oracle timed on the host's cores on a bounded
+             sample of the same workload (rank 0, one GPU only)
+
+`--impl reference` times the oracle itself as the reference arm (host cores,
+bounded sample per step) and prints the same line with "impl": "reference".
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+(b, h) problems are independent; no data-path collective), weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from split_kv_fd_gb300.workloads import BENCH_DEFAULT, ELEMENT_BYTES, WORKLOADS  # noqa: E402
+
+METRIC = "split-KV decode attention KV-GB/s and % of GB300 HBM peak (~8 TB/s), 1 GPU"
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["fd_split.cuh", "fd_device.cuh", "fd_internal.h", "fd_split_bf16.cu",
+                  "fd_split_f16.cu", "fd_split_f32.cu"]
+
+
+# ----------------------------------------------------------------- helpers
+
+def kv_bytes(w, lens) -> int:
+    """Valid K and V bytes of one step: 2 * H * d * elt * sum_b len_b."""
+    return 2 * w.H * w.d * ELEMENT_BYTES[w.dtype] * int(sum(int(x) for x in lens))
+
+
+def algorithmic_bytes(w, lens) -> int:
+    """Compulsory DRAM traffic of one launch: K/V valid rows, q, out, lse, lengths."""
+    e = ELEMENT_BYTES[w.dtype]
+    out_e = ELEMENT_BYTES[w.out_dtype]
+    return kv_bytes(w, lens) + w.B * w.H * w.d * (e + out_e) + w.B * w.H * 4 + w.B * 4
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "split_kv_fd_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    from the current kernel sources on this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        ent = rec.get(workload)
+        if ent and ent.get("kernel_source_hash") == kernel_source_hash():
+            return ent.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append(dict(ts=ts, sm=float(parts[2]), smax=float(parts[3]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        win = [r for r in rows if self.t0 is not None and self.t0 - 1 <= r["ts"] <= self.t1 + 1]
+        window = "timed"
+        if not win:
+            win, window = rows, "warmup+timed"
+        reasons = set()
+        for r in win:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in win),
+                "sm_max_mhz": max(r["smax"] for r in win), "reasons": sorted(reasons),
+                "samples": len(win), "window": window}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ oracle timing
+
+def host_sample(w, rows: int, q=None, k=None, v=None, lens=None, seed=1):
+    """``rows`` (b, h) rows of the workload as host tensors [rows, 1, ...].
+
+    From the device tensors when given (the exact workload bytes), else drawn
+    on the CPU with the workload's distributions (same shapes per row)."""
+    if k is not None:
+        lens_h = lens.cpu().tolist()
+        pairs = [(i // w.H % w.B, i % w.H) for i in range(rows)]
+        n = max(lens_h[b] for b, _ in pairs)
+        qs = torch.stack([q[b, h] for b, h in pairs]).unsqueeze(1).cpu()
+        ks = torch.stack([k[b, h, :n] for b, h in pairs]).unsqueeze(1).cpu()
+        vs = torch.stack([v[b, h, :n] for b, h in pairs]).unsqueeze(1).cpu()
+        ls = torch.tensor([lens_h[b] for b, _ in pairs], dtype=torch.int32)
+        return qs, ks, vs, ls
+    from split_kv_fd_gb300.inputs import random_case
+    if w.ragged:
+        g = torch.Generator().manual_seed(w.seed)
+        lens_l = torch.randint(1, w.N + 1, (rows,), generator=g).tolist()
+    else:
+        lens_l = [w.N] * rows
+    qs, ks, vs, ls = random_case(rows, 1, max(lens_l), w.d, w.dtype, lens=lens_l, seed=seed,
+                                 k_scale=w.k_scale)
+    return qs, ks, vs, ls
+
+
+def time_oracle(w, sample, nthreads):
+    import oracle
+    qs, ks, vs, ls = sample
+    t0 = time.perf_counter()
+    oracle.attention(qs, ks, vs, lens=ls, scale=w.scale, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(w, ls) -> int:
+    return 2 * w.d * ELEMENT_BYTES[w.dtype] * int(ls.sum())
+
+
+def cpu_baseline(w, q, k, v, lens, budget_s=8.0):
+    """Oracle on a bounded sample: grow the sample until ~budget_s of wall time."""
+    import oracle
+    oracle.build()
+    cores = oracle.default_threads()
+    rows = cores
+    while True:
+        sample = host_sample(w, min(rows, w.B * w.H), q, k, v, lens)
+        dt = time_oracle(w, sample, cores)
+        if dt * 2 > budget_s or rows >= w.B * w.H:
+            break
+        rows = min(w.B * w.H, max(rows * 2, int(rows * budget_s / max(dt, 1e-3) * 0.8)))
+    nb = sample_bytes(w, sample[3])
+    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{sample[0].shape[0]} of {w.B * w.H} (b,h) rows of {w.name}, full length "
+                      f"({int(sample[3].sum())} tokens), float64 C oracle, {cores} threads, "
+                      f"{dt:.2f} s wall"}
+
+
+# --------------------------------------------------------------- the arms
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cores = oracle.default_threads()
+    rows = max(1, min(cores, w.B * w.H))
+    sample = host_sample(w, rows)
+    for _ in range(args.warmup):
+        time_oracle(w, sample, cores)
+    times = [time_oracle(w, sample, cores) for _ in range(args.steps)]
+    nb = sample_bytes(w, sample[3])
+    total = sum(times)
+    value = nb * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, "auto"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {rows} of {w.B * w.H} (b,h) rows of {w.name}, "
+                                   f"full length, drawn on the host with the workload's "
+                                   f"distributions; float64 C oracle, {cores} threads"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, num_splits):
+    return {"workload": w.name, "batch": w.B, "heads": w.H, "kv_len": w.N, "head_dim": w.d,
+            "kv_dtype": w.dtype, "out_dtype": w.out_dtype, "num_splits": num_splits,
+            "lengths": "uniform[1,N] seeded" if w.ragged else "all N",
+            "k_scale": w.k_scale,
+            "l2": ("inputs larger than L2, no flush"
+                   if 2 * w.B * w.H * w.N * w.d * ELEMENT_BYTES[w.dtype] > 4 * L2_BYTES
+                   else "L2 flushed (256 MiB write) before every step")}
+
+
+def run_ours(args, w):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import split_kv_fd_gb300 as fd
+    from split_kv_fd_gb300.inputs import make_inputs
+    from split_kv_fd_gb300.workloads import ELEMENT_BYTES as EB
+    fd.load(build_if_missing=True)
+
+    q, k, v, lens = make_inputs(w, device=dev)
+    lens_h = lens.cpu().tolist()
+    out = torch.empty((w.B, w.H, w.d), dtype=getattr(torch, {"bf16": "bfloat16", "f16": "float16",
+                                                            "f32": "float32"}[w.out_dtype]),
+                      device=dev)
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    wsbuf = fd.new_workspace(w.B, w.H, w.N, w.d, 0, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = None
+    if 2 * w.B * w.H * w.N * w.d * EB[w.dtype] <= 4 * L2_BYTES:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        if flush is not None:
+            flush.fill_(1)
+        fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse, workspace=wsbuf,
+                  stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.25)  # the sampler's first row
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    sampler.mark("t0")
+    t_start.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(1)
+        evs[i][0].record(stream)
+        fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse, workspace=wsbuf,
+                  stream=stream)
+        evs[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark("t1")
+    barrier(ws)
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = reduce_max(total_ms, ws, dev)
+    kern_ms = statistics.mean(launch_ms)
+
+    kvb = kv_bytes(w, lens_h)
+    ms_per_step = total_ms / args.steps
+    value = ws * kvb / (ms_per_step * 1e-3) / 1e9
+    peaks, peak_src = measured_peaks()
+    alg = algorithmic_bytes(w, lens_h)
+    achieved = alg / (kern_ms * 1e-3) / 1e9
+    tokens = sum(lens_h) * w.H
+
+    # end to end from pinned host buffers through the public API
+    e2e = None
+    if not args.no_e2e:
+        hq = q.cpu().pin_memory()
+        hk = k.cpu().pin_memory()
+        hv = v.cpu().pin_memory()
+        hl = lens.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            lens.copy_(hl, non_blocking=True)
+            fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
+                      workspace=wsbuf, stream=stream)
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = reduce_max(a.elapsed_time(b), ws, dev) / e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl))
+        d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+        e2e = {"value": ws * kvb / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e_ms}
+        del hq, hk, hv
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q, k, v, lens)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_of(w, "auto"),
+            "tokens_per_s": ws * tokens / (ms_per_step * 1e-3),
+            "pct_of_nominal_8tbs": 100.0 * value / ws / NOMINAL_HBM_GBS,
+            "pct_of_measured_hbm": 100.0 * value / ws / peaks["hbm_gbs"],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic(w.name), "kernel": "split_kernel",
+                         "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
+                         "algorithmic_bytes_per_launch": alg, "mean_launch_ms": kern_ms},
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=BENCH_DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    w = WORKLOADS[args.workload]
+    ws, _, _ = dist_env()
+    if args.gpus > 1 and ws == 1 and "LOCAL_RANK" not in os.environ:
+        # launch the per-GPU ranks ourselves
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               "--master-port", os.environ.get("MASTER_PORT", "29511"),
+               os.path.abspath(__file__), *(argv if argv is not None else sys.argv[1:])]
+        return subprocess.call(cmd)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

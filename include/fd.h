@@ -1,0 +1,159 @@
+/*
+ * fd.h -- C ABI of the split-KV decode attention library (FlashDecoding) for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation: for every batch row b and head h, one query row attends
+ * over the first len_b tokens of a KV cache,
+ *     out[b,h,:] = softmax(scale * q[b,h,:] . K[b,h,j,:]) . V[b,h,j,:]
+ *     lse[b,h]   = ln sum_j exp(scale * q[b,h,:] . K[b,h,j,:])
+ * ("FlashDecoding 数学推导", §2.1.1; lse as in "FlashDecoding 数学推导：
+ * 传统 m/l/o 方法与 LSE 方法", §2.3.2).  The KV cache is split along the
+ * sequence axis into tiles processed in parallel; each tile yields a partial
+ * (m, l, o) or (S, o), and an online-softmax merge combines them exactly
+ * ("FlashDecoding 数学推导", §2.4-§2.6; "...LSE 方法", §2.3.4).
+ *
+ * Conventions for every call:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller; the
+ *     library allocates no memory and keeps no reference after returning.
+ *   - Layouts are contiguous row-major:
+ *       q   [B, H, d]        K, V [B, H, N, d]      seqlens [B] int32
+ *       out [B, H, d]        lse  [B, H] float32
+ *       o_part [B, H, P, d] float32,  m_part / l_part / lse_part [B, H, P]
+ *     Tokens at index >= seqlens[b] are never read.
+ *   - q, K and V share one storage dtype; accumulation is always float32.
+ *   - Supported head dims: 64 and 128.  q, K, V, out, o_part must be 16-byte
+ *     aligned; seqlens, lse, m/l/lse partials 4-byte aligned.
+ *   - All m and lse values are natural-log quantities of the *scaled* scores.
+ *     An empty split is (o = 0, m = -inf, l = 0, lse = -inf); an empty
+ *     sequence (len 0) gives out = 0, lse = -inf.
+ *   - seqlens values are clamped to [0, N] on the device.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous and stream-ordered; nothing synchronises.
+ *   - Errors that the host can detect (null or misaligned pointers, bad
+ *     sizes, unsupported d or dtype, short workspace) are returned before
+ *     anything is launched.  A failed launch returns FD_ERR_CUDA.  Faults
+ *     during execution surface at the caller's next synchronisation.  A
+ *     kernel that gives up waiting on its own memory copies (an internal
+ *     bound, far above any real copy time) records it in a device status
+ *     word read by fd_device_status().
+ */
+#ifndef FD_H
+#define FD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FD_F32 = 0, FD_F16 = 1, FD_BF16 = 2 } fd_dtype;
+
+typedef enum {
+    FD_OK = 0,
+    FD_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, negative size   */
+    FD_ERR_UNSUPPORTED = 2,     /* head dim or dtype outside the support set  */
+    FD_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
+    FD_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed       */
+    FD_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up waiting on its own copies */
+} fd_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fd_status_str(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int fd_version(void);
+
+/* Number of SMs of the current device, or -1 on a CUDA error. */
+int fd_num_sms(void);
+
+/*
+ * Split count the two-call path (fd_decode_split + fd_combine_*) would use
+ * for this shape on a device with `sm_count` SMs, and that fd_decode uses
+ * for num_splits == 0 when the batch is too large for its balanced
+ * decomposition.  The split-count heuristic of "adv04: Flash-Decoding" (Q2:
+ * about seq/1024, capped) is replaced by one that fills every SM: enough
+ * (b, h, split) work items for several waves, splits of at least 256 tokens.
+ * Returns >= 1, or -1 for invalid sizes.
+ */
+int fd_auto_num_splits(int B, int H, int N, int d, int sm_count);
+
+/*
+ * Bytes of device workspace fd_decode needs for this shape and num_splits
+ * (0 = automatic) on the current device.  The workspace holds per-split
+ * partials and one arrival counter per (b, h).  It needs no initialisation:
+ * fd_decode clears the counters it uses, on its stream, before its kernel
+ * runs.  Two calls that overlap on the GPU must not share one workspace.
+ * Returns 0 for invalid sizes.
+ */
+size_t fd_workspace_size(int B, int H, int N, int d, int num_splits);
+
+/*
+ * Fused split-KV decode attention: split kernel plus an in-kernel merge by
+ * the last tile of each (b, h) to finish ("FlashDecoding 数学推导", §2.5,
+ * stage 1 and stage 2, in one launch).
+ *   q, k, v      inputs in `in_dtype` (layouts above)
+ *   seqlens      per-sequence lengths, or NULL for "all N"
+ *   num_splits   0 = automatic: the (b, h, token) space is divided evenly
+ *                over the SMs, so a (b, h) may be split at any token; > 0 =
+ *                each sequence is split into num_splits pieces of
+ *                ceil(len/num_splits) tokens ("adv04: Flash-Decoding" §4).
+ *                The result does not depend on the split (up to rounding).
+ *   scale        score scale (normally 1/sqrt(d))
+ *   out          [B, H, d] in `out_dtype` (round-to-nearest-even)
+ *   lse          [B, H] float32, or NULL
+ *   workspace    device buffer of at least fd_workspace_size(...) bytes,
+ *                256-byte aligned (see above)
+ */
+fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *seqlens,
+                    int B, int H, int N, int d, fd_dtype in_dtype, int num_splits,
+                    float scale, void *out, fd_dtype out_dtype, float *lse,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Stage 1 alone: per-split partials for num_splits >= 1 splits of every
+ * sequence, split p covering tokens [p*c, min((p+1)*c, len)), c =
+ * ceil(len/num_splits) ("adv04: Flash-Decoding" §4).  For each split
+ * ("FlashDecoding 数学推导", §2.4.1 direct form; "...LSE 方法", §2.3.3):
+ *   m_part   = max_j s_j,   l_part = sum_j exp(s_j - m),
+ *   o_part   = sum_j exp(s_j - m) V_j / l   (normalised, float32),
+ *   lse_part = m + ln l   (may be NULL).
+ * Empty splits get (0, -inf, 0, -inf).
+ */
+fd_status fd_decode_split(const void *q, const void *k, const void *v, const int32_t *seqlens,
+                          int B, int H, int N, int d, fd_dtype in_dtype, int num_splits,
+                          float scale, float *o_part, float *m_part, float *l_part,
+                          float *lse_part, void *stream);
+
+/*
+ * Stage 2, m/l/o form ("FlashDecoding 数学推导", §2.4.2 / §2.5 stage 2):
+ *   m_g = max_p m_p,  l_g = sum_p exp(m_p - m_g) l_p,
+ *   out = sum_p exp(m_p - m_g) l_p o_p / l_g,  lse = m_g + ln l_g.
+ * Splits with l_p == 0 get weight 0.  P >= 1.  lse may be NULL.
+ */
+fd_status fd_combine_mlo(const float *o_part, const float *m_part, const float *l_part,
+                         int B, int H, int P, int d, void *out, fd_dtype out_dtype,
+                         float *lse, void *stream);
+
+/*
+ * Stage 2, LSE form ("FlashDecoding 数学推导：传统 m/l/o 方法与 LSE 方法",
+ * §2.3.4): S_g = ln sum_p exp(S_p) (max-shifted), out = sum_p exp(S_p - S_g)
+ * o_p, lse = S_g.  Splits with S_p == -inf get weight 0.  lse may be NULL.
+ */
+fd_status fd_combine_lse(const float *o_part, const float *lse_part,
+                         int B, int H, int P, int d, void *out, fd_dtype out_dtype,
+                         float *lse, void *stream);
+
+/*
+ * Reads (and if `reset` is non-zero, clears) the current device's status
+ * word, which a kernel sets when it gives up waiting on its own copies.
+ * Synchronises the device.  Returns FD_OK, FD_ERR_DEVICE_TIMEOUT or
+ * FD_ERR_CUDA.
+ */
+fd_status fd_device_status(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_H */

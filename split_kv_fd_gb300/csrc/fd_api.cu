@@ -1,0 +1,341 @@
+// fd_api.cu -- host side of the C ABI declared in include/fd.h: argument
+// checks, the choice of decomposition and grid, workspace carving, and the
+// launches.  Nothing here computes attention; every step runs in the kernels.
+#include "fd.h"
+#include "fd_internal.h"
+#include "fd_split.cuh"
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fd {
+
+// Device status word (per device): set by a kernel that gave up waiting on
+// its own copies.
+__device__ unsigned g_status_word;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+unsigned *g_status_ptr[MAX_DEVICES];  // cached device address of g_status_word
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return -1;
+    return dev;
+}
+
+int sm_count()
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return -1;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -1;
+    return n;
+}
+
+unsigned *status_ptr()
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return nullptr;
+    if (dev < MAX_DEVICES && g_status_ptr[dev])
+        return g_status_ptr[dev];
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess)
+        return nullptr;
+    if (dev < MAX_DEVICES)
+        g_status_ptr[dev] = static_cast<unsigned *>(ptr);
+    return static_cast<unsigned *>(ptr);
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool valid_dtype(int t) { return t == FD_F32 || t == FD_F16 || t == FD_BF16; }
+
+// The plan of one fd_decode call.
+struct Plan {
+    int decomp;
+    int P;        // splits (DECOMP_SPLITS)
+    int grid;
+    long long slots;
+};
+
+Plan make_plan(int B, int H, int N, int d, int num_splits, int sms)
+{
+    Plan pl;
+    if (num_splits == 0 && B <= BALANCED_MAX_B) {
+        pl.decomp = DECOMP_BALANCED;
+        pl.P = 0;
+        pl.grid = sms;
+        pl.slots = 2LL * sms;
+    } else {
+        pl.decomp = DECOMP_SPLITS;
+        pl.P = num_splits > 0 ? num_splits : fd_auto_num_splits(B, H, N, d, sms);
+        const long long items = (long long)B * H * pl.P;
+        pl.grid = (int)(items < sms ? items : sms);
+        pl.slots = (long long)B * H * pl.P;
+    }
+    return pl;
+}
+
+struct WsLayout {
+    size_t o_off, ml_off, cnt_off, total;
+};
+
+WsLayout ws_layout(long long slots, int d, long long rows)
+{
+    WsLayout w;
+    w.o_off = 0;
+    w.ml_off = round_up((size_t)slots * d * sizeof(float), 256);
+    w.cnt_off = w.ml_off + round_up((size_t)slots * 2 * sizeof(float), 256);
+    w.total = w.cnt_off + round_up((size_t)rows * sizeof(unsigned), 256);
+    return w;
+}
+
+bool sizes_ok(int B, int H, int N, int d)
+{
+    return B >= 0 && H >= 0 && N >= 0 && d > 0 && (long long)B * H <= (1LL << 31) - 1;
+}
+
+size_t split_smem(int dtype, int d, int decomp, int B)
+{
+    if (dtype == FD_F32)
+        return d == 64 ? SplitCfg<float, 64>::smem_bytes(decomp, B) : SplitCfg<float, 128>::smem_bytes(decomp, B);
+    if (dtype == FD_F16)
+        return d == 64 ? SplitCfg<__half, 64>::smem_bytes(decomp, B) : SplitCfg<__half, 128>::smem_bytes(decomp, B);
+    return d == 64 ? SplitCfg<__nv_bfloat16, 64>::smem_bytes(decomp, B)
+                   : SplitCfg<__nv_bfloat16, 128>::smem_bytes(decomp, B);
+}
+
+fd_status launch(int dtype, int d, const SplitParams &p, int decomp, cudaStream_t s)
+{
+    const size_t smem = split_smem(dtype, d, decomp, p.B);
+    cudaError_t e;
+    if (dtype == FD_F32)
+        e = launch_split_f32(d, p, smem, s);
+    else if (dtype == FD_F16)
+        e = launch_split_f16(d, p, smem, s);
+    else
+        e = launch_split_bf16(d, p, smem, s);
+    return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fd
+
+using namespace fd;
+
+extern "C" {
+
+const char *fd_status_str(int status)
+{
+    switch (status) {
+    case FD_OK: return "FD_OK";
+    case FD_ERR_INVALID_ARG: return "FD_ERR_INVALID_ARG: null or misaligned pointer, or bad size";
+    case FD_ERR_UNSUPPORTED: return "FD_ERR_UNSUPPORTED: head dim or dtype not supported";
+    case FD_ERR_WORKSPACE: return "FD_ERR_WORKSPACE: workspace missing or too small";
+    case FD_ERR_CUDA: return "FD_ERR_CUDA: a CUDA runtime call or launch failed";
+    case FD_ERR_DEVICE_TIMEOUT: return "FD_ERR_DEVICE_TIMEOUT: a kernel gave up waiting on its copies";
+    default: return "FD_UNKNOWN_STATUS";
+    }
+}
+
+int fd_version(void) { return 100; }
+
+int fd_num_sms(void) { return sm_count(); }
+
+int fd_auto_num_splits(int B, int H, int N, int d, int sms)
+{
+    if (!sizes_ok(B, H, N, d) || sms <= 0)
+        return -1;
+    const long long bh = (long long)B * H;
+    if (bh == 0)
+        return 1;
+    // several work items per CTA so the persistent grid balances, but never
+    // splits shorter than 256 tokens
+    const long long want = (4LL * sms + bh - 1) / bh;
+    long long cap = N / 256;
+    if (cap < 1)
+        cap = 1;
+    long long P = want < cap ? want : cap;
+    if (P < 1)
+        P = 1;
+    if (P > 8192)
+        P = 8192;
+    return (int)P;
+}
+
+size_t fd_workspace_size(int B, int H, int N, int d, int num_splits)
+{
+    if (!sizes_ok(B, H, N, d) || num_splits < 0)
+        return 0;
+    const int sms = sm_count();
+    if (sms <= 0)
+        return 0;
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    return ws_layout(pl.slots, d, (long long)B * H).total;
+}
+
+fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *seqlens, int B, int H,
+                    int N, int d, fd_dtype in_dtype, int num_splits, float scale, void *out,
+                    fd_dtype out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                    void *stream)
+{
+    if (!sizes_ok(B, H, N, d) || num_splits < 0 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0)
+        return FD_OK;
+    // K and V are never read when N == 0
+    if (!q || (N > 0 && (!k || !v)) || !out || !aligned(q, 16) || !aligned(k, 16) ||
+        !aligned(v, 16) || !aligned(out, 16) || (seqlens && !aligned(seqlens, 4)) ||
+        (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    unsigned *st = status_ptr();
+    if (sms <= 0 || !st)
+        return FD_ERR_CUDA;
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    const WsLayout wl = ws_layout(pl.slots, d, (long long)B * H);
+    if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
+        return FD_ERR_WORKSPACE;
+
+    SplitParams p = {};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.lens = seqlens;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.decomp = pl.decomp;
+    p.P = pl.P;
+    p.grid = pl.grid;
+    p.out_kind = OUT_FUSED;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.lse = lse;
+    char *ws = static_cast<char *>(workspace);
+    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
+    p.status = st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the arrival counters start at zero for every call (a reused workspace
+    // may hold anything at these bytes)
+    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
+    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * H * sizeof(unsigned), cs) != cudaSuccess)
+        return FD_ERR_CUDA;
+    return launch(in_dtype, d, p, pl.decomp, cs);
+}
+
+fd_status fd_decode_split(const void *q, const void *k, const void *v, const int32_t *seqlens, int B,
+                          int H, int N, int d, fd_dtype in_dtype, int num_splits, float scale,
+                          float *o_part, float *m_part, float *l_part, float *lse_part, void *stream)
+{
+    if (!sizes_ok(B, H, N, d) || num_splits < 1 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(in_dtype) || (d != 64 && d != 128))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0)
+        return FD_OK;
+    if (!q || (N > 0 && (!k || !v)) || !o_part || !m_part || !l_part || !aligned(q, 16) || !aligned(k, 16) ||
+        !aligned(v, 16) || !aligned(o_part, 16) || !aligned(m_part, 4) || !aligned(l_part, 4) ||
+        (lse_part && !aligned(lse_part, 4)) || (seqlens && !aligned(seqlens, 4)))
+        return FD_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    unsigned *st = status_ptr();
+    if (sms <= 0 || !st)
+        return FD_ERR_CUDA;
+    const long long items = (long long)B * H * num_splits;
+
+    SplitParams p = {};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.lens = seqlens;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.decomp = DECOMP_SPLITS;
+    p.P = num_splits;
+    p.grid = (int)(items < sms ? items : sms);
+    p.out_kind = OUT_PARTIALS;
+    p.o_part = o_part;
+    p.m_part = m_part;
+    p.l_part = l_part;
+    p.lse_part = lse_part;
+    p.status = st;
+    return launch(in_dtype, d, p, DECOMP_SPLITS, static_cast<cudaStream_t>(stream));
+}
+
+static fd_status combine_common(const float *o_part, const float *a, const float *b, bool lse_form,
+                                int B, int H, int P, int d, void *out, fd_dtype out_dtype, float *lse,
+                                void *stream)
+{
+    if (B < 0 || H < 0 || P < 1 || P > 8192 || d <= 0 || (long long)B * H > (1LL << 31) - 1)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(out_dtype) || (d != 64 && d != 128))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0)
+        return FD_OK;
+    if (!o_part || !a || (!lse_form && !b) || !out || !aligned(o_part, 16) || !aligned(a, 4) ||
+        (b && !aligned(b, 4)) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    CombineParams p = {};
+    p.o_part = o_part;
+    if (lse_form) {
+        p.lse_part = a;
+    } else {
+        p.m_part = a;
+        p.l_part = b;
+    }
+    p.rows = B * H;
+    p.P = P;
+    p.d = d;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.lse = lse;
+    cudaError_t e = lse_form ? launch_combine_lse(p, static_cast<cudaStream_t>(stream))
+                             : launch_combine_mlo(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+fd_status fd_combine_mlo(const float *o_part, const float *m_part, const float *l_part, int B, int H,
+                         int P, int d, void *out, fd_dtype out_dtype, float *lse, void *stream)
+{
+    return combine_common(o_part, m_part, l_part, false, B, H, P, d, out, out_dtype, lse, stream);
+}
+
+fd_status fd_combine_lse(const float *o_part, const float *lse_part, int B, int H, int P, int d,
+                         void *out, fd_dtype out_dtype, float *lse, void *stream)
+{
+    return combine_common(o_part, lse_part, nullptr, true, B, H, P, d, out, out_dtype, lse, stream);
+}
+
+fd_status fd_device_status(int reset)
+{
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return FD_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof v) != cudaSuccess)
+        return FD_ERR_CUDA;
+    if (reset) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess)
+            return FD_ERR_CUDA;
+    }
+    return (v & STATUS_TIMEOUT) ? FD_ERR_DEVICE_TIMEOUT : FD_OK;
+}
+
+}  // extern "C"

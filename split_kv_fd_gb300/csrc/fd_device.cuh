@@ -1,0 +1,192 @@
+// fd_device.cuh -- device-side building blocks for the split-KV decode
+// kernels: shared-memory mbarriers, 1-D bulk (TMA) global->shared copies,
+// bounded waits, and 16-byte element vectors widened to float32.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace fd {
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+// Upper bound on any single wait for one of a kernel's own bulk copies.  A
+// 8 KB copy lands in microseconds; the bound only exists so that a kernel
+// can never spin forever.  After it expires the kernel records the event in
+// the device status word and stops waiting.
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;   // 1 s
+constexpr unsigned WAIT_LIMIT_POLLS = 1u << 30;
+
+// Status word bits.
+constexpr unsigned STATUS_TIMEOUT = 1u;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// One arrival that also announces `bytes` of incoming transaction data.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for phase `parity` of barrier `bar`.  Every lane polls; the
+// result is made warp-uniform (all lanes must have seen completion).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+        unsigned long long t0 = global_ns();
+        for (unsigned i = 0; i < WAIT_LIMIT_POLLS; ++i) {
+            if (mbar_try_wait(bar, parity)) {
+                ok = true;
+                break;
+            }
+            if ((i & 63u) == 63u && global_ns() - t0 > WAIT_LIMIT_NS)
+                break;
+        }
+    }
+    return __all_sync(FULL_MASK, ok);
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Same, with an L2 eviction-priority policy (streamed data is read once).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero):
+// ex2(-inf) = +0.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of the storage type, widened to float32.
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static constexpr int VEC = 4;
+    __device__ __forceinline__ static void widen(const uint4 &u, float *f)
+    {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    // bf16 is the upper half of a binary32: widening is a shift / mask.
+    __device__ __forceinline__ static void widen(const uint4 &u, float *f)
+    {
+        f[0] = __uint_as_float(u.x << 16);
+        f[1] = __uint_as_float(u.x & 0xffff0000u);
+        f[2] = __uint_as_float(u.y << 16);
+        f[3] = __uint_as_float(u.y & 0xffff0000u);
+        f[4] = __uint_as_float(u.z << 16);
+        f[5] = __uint_as_float(u.z & 0xffff0000u);
+        f[6] = __uint_as_float(u.w << 16);
+        f[7] = __uint_as_float(u.w & 0xffff0000u);
+    }
+};
+
+template <> struct Elem<__half> {
+    static constexpr int VEC = 8;
+    __device__ __forceinline__ static void widen(const uint4 &u, float *f)
+    {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h;
+            memcpy(&h, &w[i], 4);
+            float2 p = __half22float2(h);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        }
+    }
+};
+
+// Store one float as the requested output dtype (round-to-nearest-even).
+__device__ __forceinline__ void store_out(void *out, long long idx, int out_dtype, float x)
+{
+    if (out_dtype == 0)
+        static_cast<float *>(out)[idx] = x;
+    else if (out_dtype == 1)
+        static_cast<__half *>(out)[idx] = __float2half_rn(x);
+    else
+        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(x);
+}
+
+}  // namespace fd

@@ -1,0 +1,15 @@
+// fd_split_f16.cu -- split-KV decode kernel instantiated for f16 storage.
+#include "fd_split.cuh"
+
+namespace fd {
+
+cudaError_t launch_split_f16(int d, const SplitParams &p, size_t smem, cudaStream_t s)
+{
+    if (d == 64)
+        return launch_split_t<__half, 64>(p, smem, s);
+    if (d == 128)
+        return launch_split_t<__half, 128>(p, smem, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fd

@@ -1,0 +1,15 @@
+// fd_split_f32.cu -- split-KV decode kernel instantiated for f32 storage.
+#include "fd_split.cuh"
+
+namespace fd {
+
+cudaError_t launch_split_f32(int d, const SplitParams &p, size_t smem, cudaStream_t s)
+{
+    if (d == 64)
+        return launch_split_t<float, 64>(p, smem, s);
+    if (d == 128)
+        return launch_split_t<float, 128>(p, smem, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fd

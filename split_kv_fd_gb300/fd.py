@@ -1,0 +1,254 @@
+"""Python binding of the C ABI in include/fd.h (ctypes; marshalling only).
+
+Every function takes CUDA torch tensors, checks that their dtype, shape,
+contiguity and device fit the C call, passes raw device pointers and the
+current CUDA stream, and turns a non-OK status into an exception.  All the
+arithmetic runs in the CUDA kernels of ``libfd.so``; there is no fallback:
+if the library is missing or no GPU is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import _build_lib
+
+FD_OK = 0
+STATUS_NAMES = {0: "FD_OK", 1: "FD_ERR_INVALID_ARG", 2: "FD_ERR_UNSUPPORTED",
+                3: "FD_ERR_WORKSPACE", 4: "FD_ERR_CUDA", 5: "FD_ERR_DEVICE_TIMEOUT"}
+
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+# every symbol include/fd.h declares
+EXPORTS = ["fd_status_str", "fd_version", "fd_num_sms", "fd_auto_num_splits",
+           "fd_workspace_size", "fd_decode", "fd_decode_split", "fd_combine_mlo",
+           "fd_combine_lse", "fd_device_status"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FDError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)}")
+
+
+def library_path() -> str:
+    return _build_lib.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load libfd.so (no GPU needed).  Raises if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if build_if_missing and _build_lib.is_stale():
+            _build_lib.build()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fd_status_str.argtypes = [I]
+        lib.fd_status_str.restype = ctypes.c_char_p
+        lib.fd_version.argtypes = []
+        lib.fd_version.restype = I
+        lib.fd_num_sms.argtypes = []
+        lib.fd_num_sms.restype = I
+        lib.fd_auto_num_splits.argtypes = [I, I, I, I, I]
+        lib.fd_auto_num_splits.restype = I
+        lib.fd_workspace_size.argtypes = [I, I, I, I, I]
+        lib.fd_workspace_size.restype = S
+        lib.fd_decode.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, I, P, P, S, P]
+        lib.fd_decode.restype = I
+        lib.fd_decode_split.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P]
+        lib.fd_decode_split.restype = I
+        lib.fd_combine_mlo.argtypes = [P, P, P, I, I, I, I, P, I, P, P]
+        lib.fd_combine_mlo.restype = I
+        lib.fd_combine_lse.argtypes = [P, P, I, I, I, I, P, I, P, P]
+        lib.fd_combine_lse.restype = I
+        lib.fd_device_status.argtypes = [I]
+        lib.fd_device_status.restype = I
+        _lib = lib
+        return lib
+
+
+def status_str(status: int) -> str:
+    try:
+        return load().fd_status_str(int(status)).decode()
+    except Exception:  # pragma: no cover - library not loadable
+        return STATUS_NAMES.get(status, str(status))
+
+
+def _check(status: int, what: str) -> None:
+    if status != FD_OK:
+        raise FDError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor, stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (the library has no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def _check_qkv(q, k, v, seqlens):
+    _need_cuda(q, k, v, seqlens)
+    if q.dtype not in DTYPE_CODE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, K, V must share one dtype among float32/float16/bfloat16")
+    if k.dim() != 4 or v.shape != k.shape or q.shape != (k.shape[0], k.shape[1], k.shape[3]):
+        raise ValueError(f"shapes: q{tuple(q.shape)} must be [B,H,d], K/V{tuple(k.shape)} [B,H,N,d]")
+    if seqlens is not None and (seqlens.dtype != torch.int32 or seqlens.shape != (k.shape[0],)):
+        raise ValueError("seqlens must be an int32 tensor of shape [B]")
+    B, H, N, d = k.shape
+    return B, H, N, d
+
+
+def num_sms() -> int:
+    return load().fd_num_sms()
+
+
+def auto_num_splits(B, H, N, d, sm_count=None) -> int:
+    sm = num_sms() if sm_count is None else sm_count
+    return load().fd_auto_num_splits(B, H, N, d, sm)
+
+
+def workspace_size(B, H, N, d, num_splits=0) -> int:
+    return load().fd_workspace_size(B, H, N, d, num_splits)
+
+
+def new_workspace(B, H, N, d, num_splits=0, device=None) -> torch.Tensor:
+    """A workspace for fd_decode (reusable across calls on one stream)."""
+    n = workspace_size(B, H, N, d, num_splits)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+_ws_cache: dict = {}
+
+
+def _cached_workspace(device, nbytes):
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def decode(q, k, v, seqlens=None, num_splits=0, scale=None, out_dtype=None, out=None,
+           lse=None, return_lse=True, workspace=None, stream=None):
+    """Fused split-KV decode attention (fd_decode).  Returns ``(out, lse)``.
+
+    q [B,H,d], k/v [B,H,N,d] on one CUDA device; ``seqlens`` int32 [B] or
+    None; ``num_splits`` 0 = automatic.  ``workspace`` defaults to a cached
+    buffer per device (calls that overlap on the GPU need their own
+    workspaces).
+    """
+    B, H, N, d = _check_qkv(q, k, v, seqlens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, H, d), dtype=odt, device=q.device)
+    _need_cuda(out, lse)
+    if out.dtype not in DTYPE_CODE or out.shape != (B, H, d):
+        raise ValueError("out must be [B,H,d] float32/float16/bfloat16")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or lse.shape != (B, H)):
+        raise ValueError("lse must be float32 [B,H]")
+    lib = load()
+    need = lib.fd_workspace_size(B, H, N, d, int(num_splits))
+    if workspace is None:
+        workspace = _cached_workspace(q.device, need)
+    _need_cuda(workspace)
+    st = lib.fd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(seqlens), B, H, N, d, DTYPE_CODE[q.dtype],
+                       int(num_splits), float(scale), _ptr(out), DTYPE_CODE[out.dtype], _ptr(lse),
+                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                       _stream(q, stream))
+    _check(st, "fd_decode")
+    return out, lse
+
+
+def decode_split(q, k, v, num_splits, seqlens=None, scale=None, stream=None):
+    """Stage 1 alone (fd_decode_split).  Returns ``(o_part, m_part, l_part, lse_part)``."""
+    B, H, N, d = _check_qkv(q, k, v, seqlens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    P = int(num_splits)
+    dev = q.device
+    o_part = torch.empty((B, H, P, d), dtype=torch.float32, device=dev)
+    m_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
+    l_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
+    lse_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
+    st = load().fd_decode_split(_ptr(q), _ptr(k), _ptr(v), _ptr(seqlens), B, H, N, d,
+                                DTYPE_CODE[q.dtype], P, float(scale), _ptr(o_part), _ptr(m_part),
+                                _ptr(l_part), _ptr(lse_part), _stream(q, stream))
+    _check(st, "fd_decode_split")
+    return o_part, m_part, l_part, lse_part
+
+
+def _combine_out(o_part, out_dtype, out, lse, return_lse):
+    B, H, P, d = o_part.shape
+    if out is None:
+        out = torch.empty((B, H, d), dtype=out_dtype or torch.float32, device=o_part.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=o_part.device)
+    _need_cuda(out, lse)
+    return B, H, P, d, out, lse
+
+
+def combine_mlo(o_part, m_part, l_part, out_dtype=None, out=None, lse=None, return_lse=True,
+                stream=None):
+    """Stage 2, m/l/o merge (fd_combine_mlo).  Returns ``(out, lse)``."""
+    _need_cuda(o_part, m_part, l_part)
+    B, H, P, d, out, lse = _combine_out(o_part, out_dtype, out, lse, return_lse)
+    for t in (o_part, m_part, l_part):
+        if t.dtype != torch.float32:
+            raise ValueError("partials must be float32")
+    if m_part.shape != (B, H, P) or l_part.shape != (B, H, P):
+        raise ValueError("m_part/l_part must be [B,H,P]")
+    st = load().fd_combine_mlo(_ptr(o_part), _ptr(m_part), _ptr(l_part), B, H, P, d, _ptr(out),
+                               DTYPE_CODE[out.dtype], _ptr(lse), _stream(o_part, stream))
+    _check(st, "fd_combine_mlo")
+    return out, lse
+
+
+def combine_lse(o_part, lse_part, out_dtype=None, out=None, lse=None, return_lse=True,
+                stream=None):
+    """Stage 2, LSE merge (fd_combine_lse).  Returns ``(out, lse)``."""
+    _need_cuda(o_part, lse_part)
+    B, H, P, d, out, lse = _combine_out(o_part, out_dtype, out, lse, return_lse)
+    for t in (o_part, lse_part):
+        if t.dtype != torch.float32:
+            raise ValueError("partials must be float32")
+    if lse_part.shape != (B, H, P):
+        raise ValueError("lse_part must be [B,H,P]")
+    st = load().fd_combine_lse(_ptr(o_part), _ptr(lse_part), B, H, P, d, _ptr(out),
+                               DTYPE_CODE[out.dtype], _ptr(lse), _stream(o_part, stream))
+    _check(st, "fd_combine_lse")
+    return out, lse
+
+
+def device_status(reset: bool = True) -> int:
+    """FD_OK, or FD_ERR_DEVICE_TIMEOUT if a kernel gave up waiting (synchronises)."""
+    return load().fd_device_status(1 if reset else 0)

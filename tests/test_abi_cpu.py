@@ -1,0 +1,103 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol that
+include/fd.h declares, and rejects bad arguments on the host before any
+CUDA call.  Also checks the seeded input generator (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import split_kv_fd_gb300 as fd
+from split_kv_fd_gb300 import fd as fdmod
+from split_kv_fd_gb300.inputs import make_inputs, random_case
+from split_kv_fd_gb300.workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return fdmod.load(build_if_missing=True)
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fd.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fd_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert set(names) == set(fdmod.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.fd_version() >= 100
+
+
+def test_status_strings(lib):
+    for code, name in fdmod.STATUS_NAMES.items():
+        assert lib.fd_status_str(code).decode().startswith(name)
+    assert lib.fd_status_str(99).decode() == "FD_UNKNOWN_STATUS"
+
+
+def test_host_rejects_bad_arguments_without_cuda(lib):
+    P = ctypes.c_void_p
+    dummy = P(4096)  # aligned, never dereferenced: the checks fail first
+    # negative sizes
+    assert lib.fd_decode(dummy, dummy, dummy, None, -1, 1, 8, 128, 2, 0, 1.0, dummy, 2, None,
+                         dummy, 1 << 20, None) == 1
+    # unsupported head dim / dtype
+    assert lib.fd_decode(dummy, dummy, dummy, None, 1, 1, 8, 96, 2, 0, 1.0, dummy, 2, None,
+                         dummy, 1 << 20, None) == 2
+    assert lib.fd_decode(dummy, dummy, dummy, None, 1, 1, 8, 128, 7, 0, 1.0, dummy, 2, None,
+                         dummy, 1 << 20, None) == 2
+    # null and misaligned pointers
+    assert lib.fd_decode(None, dummy, dummy, None, 1, 1, 8, 128, 2, 0, 1.0, dummy, 2, None,
+                         dummy, 1 << 20, None) == 1
+    assert lib.fd_decode(dummy, P(4098), dummy, None, 1, 1, 8, 128, 2, 0, 1.0, dummy, 2, None,
+                         dummy, 1 << 20, None) == 1
+    # negative split count; split path needs >= 1
+    assert lib.fd_decode(dummy, dummy, dummy, None, 1, 1, 8, 128, 2, -1, 1.0, dummy, 2, None,
+                         dummy, 1 << 20, None) == 1
+    assert lib.fd_decode_split(dummy, dummy, dummy, None, 1, 1, 8, 128, 2, 0, 1.0, dummy, dummy,
+                               dummy, None, None) == 1
+    # combine: P out of range, unsupported d
+    assert lib.fd_combine_mlo(dummy, dummy, dummy, 1, 1, 0, 128, dummy, 0, None, None) == 1
+    assert lib.fd_combine_lse(dummy, dummy, 1, 1, 4, 80, dummy, 0, None, None) == 2
+    # an empty problem is a no-op
+    assert lib.fd_decode(None, None, None, None, 0, 4, 8, 128, 2, 0, 1.0, None, 2, None,
+                         None, 0, None) == 0
+
+
+def test_auto_num_splits_rule(lib):
+    # fills ~4 work items per SM, never splits under 256 tokens, >= 1
+    assert lib.fd_auto_num_splits(8, 32, 32768, 128, 152) == 3
+    assert lib.fd_auto_num_splits(1, 32, 131072, 128, 152) == 19
+    assert lib.fd_auto_num_splits(1, 1, 1024, 64, 152) == 4
+    assert lib.fd_auto_num_splits(1, 1, 100, 64, 152) == 1
+    assert lib.fd_auto_num_splits(0, 1, 100, 64, 152) == 1
+    assert lib.fd_auto_num_splits(1, 1, 100, 64, 0) == -1
+
+
+def test_input_generator_is_seeded_and_pads_with_nan():
+    w = WORKLOADS["decode_b1_h1_n1k_d64_f32_p4"]
+    a = make_inputs(w)
+    b = make_inputs(w)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    q, k, v, lens = random_case(3, 2, 50, 64, "bf16", lens=[50, 7, 0], seed=1)
+    assert lens.tolist() == [50, 7, 0]
+    assert torch.isnan(k[1, :, 7:].float()).all() and torch.isfinite(k[1, :, :7].float()).all()
+    assert torch.isnan(v[2].float()).all() and torch.isfinite(k[0].float()).all()
+    # K draws scaled by k_scale
+    w4 = WORKLOADS["decode_b1_h32_n128k_d128_bf16_k8"]
+    assert w4.k_scale == 8.0 and w4.scale == pytest.approx(1 / np.sqrt(128))
+
+
+def test_binding_refuses_cpu_tensors():
+    q = torch.zeros(1, 1, 64)
+    k = torch.zeros(1, 1, 4, 64)
+    with pytest.raises(ValueError):
+        fd.decode(q, k, k)
