@@ -55,7 +55,8 @@ typedef enum {
     FD_ERR_UNSUPPORTED = 2,     /* head dim or dtype outside the support set  */
     FD_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
     FD_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed       */
-    FD_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up waiting on its own copies */
+    FD_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up waiting on its own copies */
+    FD_ERR_SCRATCH_TOO_SMALL = 6 /* fd_decode_noalloc: problem exceeds its scratch */
 } fd_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -151,6 +152,49 @@ fd_status fd_combine_lse(const float *o_part, const float *lse_part,
  * FD_ERR_CUDA.
  */
 fd_status fd_device_status(int reset);
+
+/*
+ * Size of the static device scratch that fd_decode_noalloc uses: 1 MiB.
+ * Every GPU on which this library is loaded holds it until the process
+ * exits.
+ */
+#define FD_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * fd_decode_noalloc -- fd_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this call: it is an addition to
+ * the library's interface, not a step of the method.
+ *
+ * Who needs it: code that may not allocate GPU memory while it decodes, for
+ * example a serving engine that gives all device memory to its own pool at
+ * start-up and forbids allocation on the per-token path (cudaMalloc can
+ * synchronise the device and stall every stream), or a plugin slot of an
+ * inference runtime that receives only input and output pointers and a
+ * stream.  Such callers cannot provide fd_decode's workspace.
+ *
+ * What it does: exactly fd_decode (same arguments, same results, same
+ * kernels) with the workspace replaced by a static device array of
+ * FD_NOALLOC_SCRATCH_BYTES inside this library.  The caller still passes
+ * q, K, V, seqlens, out and lse.  Nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library routine is called.
+ *
+ * Limits and rules:
+ *   - A problem whose partials and counters need more than
+ *     FD_NOALLOC_SCRATCH_BYTES returns FD_ERR_SCRATCH_TOO_SMALL before
+ *     anything is launched.  With num_splits == 0 that is (about)
+ *     2*SMs*(d+2)*4 + 4*B*H bytes, e.g. B*H up to ~220,000 for d = 128 on a
+ *     152-SM GPU; with num_splits = P > 0 it is about B*H*P*(d+2)*4 bytes.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call uses the same array and it keeps the previous call's
+ *     contents; each call clears, on its stream, the counters it relies on.
+ *     Calls that overlap on the GPU (other streams, other host threads) race
+ *     on the array: the caller must serialise them.
+ */
+fd_status fd_decode_noalloc(const void *q, const void *k, const void *v, const int32_t *seqlens,
+                            int B, int H, int N, int d, fd_dtype in_dtype, int num_splits,
+                            float scale, void *out, fd_dtype out_dtype, float *lse, void *stream);
 
 #ifdef __cplusplus
 }

@@ -143,6 +143,9 @@ const char *fd_status_str(int status)
     case FD_ERR_WORKSPACE: return "FD_ERR_WORKSPACE: workspace missing or too small";
     case FD_ERR_CUDA: return "FD_ERR_CUDA: a CUDA runtime call or launch failed";
     case FD_ERR_DEVICE_TIMEOUT: return "FD_ERR_DEVICE_TIMEOUT: a kernel gave up waiting on its copies";
+    case FD_ERR_SCRATCH_TOO_SMALL:
+        return "FD_ERR_SCRATCH_TOO_SMALL: the problem needs more scratch than fd_decode_noalloc's "
+               "static buffer (FD_NOALLOC_SCRATCH_BYTES) holds; use fd_decode with a workspace";
     default: return "FD_UNKNOWN_STATUS";
     }
 }
@@ -339,3 +342,100 @@ fd_status fd_device_status(int reset)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// fd_decode_noalloc: fd_decode whose scratch is a static device array.
+//
+// Some callers cannot allocate device memory when they decode: a serving
+// engine that hands all GPU memory to its own pool at start-up and forbids
+// allocation on the per-token path (cudaMalloc may synchronise the device
+// and stall every stream), or a plugin slot of an inference runtime that is
+// given only input/output pointers and a stream.  This entry point needs no
+// workspace from them: the partials and arrival counters live in the array
+// below, which every GPU that loads this library holds until the process
+// exits.  All calls share it, so calls that overlap on the GPU (different
+// streams, or different host threads) race and must be serialised by the
+// caller.
+// ---------------------------------------------------------------------------
+namespace fd {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FD_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch, looked up once per device.  In host
+// code the array's name is only a host-side stand-in, never a device
+// address, so kernels must be given this pointer instead.
+void *g_noalloc_ptr[MAX_DEVICES];
+
+void *noalloc_scratch()
+{
+    const int dev = current_device();
+    if (dev < 0 || dev >= MAX_DEVICES)
+        return nullptr;
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess)
+            return nullptr;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace fd
+
+extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void *v,
+                                       const int32_t *seqlens, int B, int H, int N, int d,
+                                       fd_dtype in_dtype, int num_splits, float scale, void *out,
+                                       fd_dtype out_dtype, float *lse, void *stream)
+{
+    if (!sizes_ok(B, H, N, d) || num_splits < 0 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0)
+        return FD_OK;
+    if (!q || (N > 0 && (!k || !v)) || !out || !aligned(q, 16) || !aligned(k, 16) ||
+        !aligned(v, 16) || !aligned(out, 16) || (seqlens && !aligned(seqlens, 4)) ||
+        (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    unsigned *st = status_ptr();
+    if (sms <= 0 || !st)
+        return FD_ERR_CUDA;
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    const WsLayout wl = ws_layout(pl.slots, d, (long long)B * H);
+    if (wl.total > (size_t)FD_NOALLOC_SCRATCH_BYTES)
+        return FD_ERR_SCRATCH_TOO_SMALL;
+    void *scratch = noalloc_scratch();  // first call on a device: symbol lookup
+    if (!scratch)
+        return FD_ERR_CUDA;
+
+    SplitParams p = {};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.lens = seqlens;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.decomp = pl.decomp;
+    p.P = pl.P;
+    p.grid = pl.grid;
+    p.out_kind = OUT_FUSED;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.lse = lse;
+    char *ws = static_cast<char *>(scratch);
+    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
+    p.status = st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's bytes: clear the counters this call uses
+    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
+    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * H * sizeof(unsigned), cs) != cudaSuccess)
+        return FD_ERR_CUDA;
+    return launch(in_dtype, d, p, pl.decomp, cs);
+}

@@ -19,14 +19,15 @@ from . import _build_lib
 
 FD_OK = 0
 STATUS_NAMES = {0: "FD_OK", 1: "FD_ERR_INVALID_ARG", 2: "FD_ERR_UNSUPPORTED",
-                3: "FD_ERR_WORKSPACE", 4: "FD_ERR_CUDA", 5: "FD_ERR_DEVICE_TIMEOUT"}
+                3: "FD_ERR_WORKSPACE", 4: "FD_ERR_CUDA", 5: "FD_ERR_DEVICE_TIMEOUT",
+                6: "FD_ERR_SCRATCH_TOO_SMALL"}
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # every symbol include/fd.h declares
 EXPORTS = ["fd_status_str", "fd_version", "fd_num_sms", "fd_auto_num_splits",
            "fd_workspace_size", "fd_decode", "fd_decode_split", "fd_combine_mlo",
-           "fd_combine_lse", "fd_device_status"]
+           "fd_combine_lse", "fd_device_status", "fd_decode_noalloc"]
 
 _lock = threading.Lock()
 _lib = None
