@@ -45,6 +45,11 @@ WORKLOADS = {
 # in the order the workloads were specified
 ORDER = list(WORKLOADS)
 
+# a smaller case of the benchmark's kernel for detailed profiles: 256 MiB of
+# K/V (larger than the 129 MB L2, small enough for a many-pass capture)
+WORKLOADS["decode_b2_h8_n32k_d128_bf16"] = Workload(
+    "decode_b2_h8_n32k_d128_bf16", 2, 8, 32768, 128, "bf16", "bf16", 0)
+
 # the workload the benchmark times by default: uniform 32K-token sequences
 BENCH_DEFAULT = "decode_b8_h32_n32k_d128_bf16"
 
