@@ -70,16 +70,17 @@ struct Plan {
 Plan make_plan(int B, int H, int N, int d, int num_splits, int sms)
 {
     Plan pl;
+    const int ctas = sms * FD_CTAS_PER_SM;  // persistent grid
     if (num_splits == 0 && B <= BALANCED_MAX_B) {
         pl.decomp = DECOMP_BALANCED;
         pl.P = 0;
-        pl.grid = sms;
-        pl.slots = 2LL * sms;
+        pl.grid = ctas;
+        pl.slots = 2LL * ctas;
     } else {
         pl.decomp = DECOMP_SPLITS;
         pl.P = num_splits > 0 ? num_splits : fd_auto_num_splits(B, H, N, d, sms);
         const long long items = (long long)B * H * pl.P;
-        pl.grid = (int)(items < sms ? items : sms);
+        pl.grid = (int)(items < ctas ? items : ctas);
         pl.slots = (long long)B * H * pl.P;
     }
     return pl;
@@ -260,6 +261,7 @@ fd_status fd_decode_split(const void *q, const void *k, const void *v, const int
     if (sms <= 0 || !st)
         return FD_ERR_CUDA;
     const long long items = (long long)B * H * num_splits;
+    const int ctas = sms * FD_CTAS_PER_SM;
 
     SplitParams p = {};
     p.q = q;
@@ -272,7 +274,7 @@ fd_status fd_decode_split(const void *q, const void *k, const void *v, const int
     p.scale_log2 = scale * 1.4426950408889634f;
     p.decomp = DECOMP_SPLITS;
     p.P = num_splits;
-    p.grid = (int)(items < sms ? items : sms);
+    p.grid = (int)(items < ctas ? items : ctas);
     p.out_kind = OUT_PARTIALS;
     p.o_part = o_part;
     p.m_part = m_part;

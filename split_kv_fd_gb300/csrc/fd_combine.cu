@@ -78,6 +78,7 @@ template <bool LSE> __global__ void __launch_bounds__(COMBINE_THREADS) combine_k
     const float *o = p.o_part + row * P * d;
     for (int t = threadIdx.x; t < d; t += blockDim.x) {
         float acc = 0.f;
+#pragma unroll 8
         for (int i = 0; i < P; ++i)
             acc = fmaf(wgt[i], o[(long long)i * d + t], acc);
         store_out(p.out, row * d + t, p.out_dtype, nonempty ? acc / L : 0.f);

@@ -54,6 +54,15 @@ struct CombineParams {
     float *lse;
 };
 
+// Persistent CTAs launched per SM by the split kernel.
+#ifndef FD_CTAS_PER_SM
+#define FD_CTAS_PER_SM 1
+#endif
+
+// The balanced decomposition gives every CTA it uses at least this many
+// tokens (a small problem runs on fewer CTAs rather than on slivers).
+constexpr long long BALANCED_MIN_TOKENS = 128;
+
 // Largest batch the balanced decomposition keeps its length prefix sums for
 // in shared memory; larger batches use DECOMP_SPLITS.
 constexpr int BALANCED_MAX_B = 1024;

@@ -10,11 +10,16 @@
 // How (GB300): the path is bound by HBM bandwidth (every K/V byte is read
 // once; ~1 flop per byte), so there are no tensor cores.  Each CTA is
 // persistent (one per SM) and walks a contiguous list of segments.  Inside a
-// CTA every warp owns a private ring of STAGES shared-memory stages; a stage
-// holds one chunk of CT tokens of K and the same tokens of V, filled by two
-// 1-D bulk copies (cp.async.bulk, completion on an mbarrier).  Chunks of the
-// CTA's token sequence go round-robin to the warps, so the CTA streams
-// contiguous memory while warps never wait on each other inside a segment.
+// CTA the warps form groups of GW; each group owns a ring of STAGES
+// shared-memory stages.  A stage holds one chunk of CT tokens of K and the
+// same tokens of V, filled by two 1-D bulk copies (cp.async.bulk, completion
+// on a "full" mbarrier) issued by the group's first warp; each warp of the
+// group takes its own WT rows of the chunk and signals an "empty" mbarrier
+// when done, after which the stage is refilled.  Grouping keeps every copy
+// large (GW * 4 KB) and the number of copies in flight per SM moderate,
+// which the HBM/TMA path needs to stream near its peak.  Chunks of the CTA's
+// token sequence go round-robin to the groups, so the CTA streams contiguous
+// memory while groups never wait on each other inside a segment.
 // Within a warp, LPT lanes cover one token row with 16-byte loads and the
 // q.k partial sums are reduced with xor-shuffles.  The softmax state is
 // updated once per chunk in the block form of the online-softmax update
@@ -31,24 +36,45 @@ namespace fd {
 
 constexpr float LN2_F = 0.693147180559945309f;
 
+#ifndef FD_WARPS
+#define FD_WARPS 8
+#endif
+#ifndef FD_GROUP_WARPS
+#define FD_GROUP_WARPS 2
+#endif
+#ifndef FD_STAGES
+#define FD_STAGES 2
+#endif
+#ifndef FD_WARP_BYTES
+#define FD_WARP_BYTES 4096
+#endif
+// packed two-lane fp32 FMAs (same operations, half the instructions)
+#ifndef FD_NO_FMA2
+#define FD_FMA2 1
+#endif
+
 template <typename T, int D> struct SplitCfg {
     static constexpr int ESZ = sizeof(T);
     static constexpr int VEC = Elem<T>::VEC;       // elements per lane vector (16 bytes)
     static constexpr int LPT = D / VEC;            // lanes per token row
     static constexpr int TPW = 32 / LPT;           // token rows per warp-wide load
     static constexpr int ROW = D * ESZ;            // bytes per token row
-    static constexpr int WARPS = 8;
+    static constexpr int WARPS = FD_WARPS;
     static constexpr int THREADS = WARPS * 32;
-    static constexpr int STAGES = 3;
-    static constexpr int CT = 4096 / ROW;          // tokens per chunk
-    static constexpr int TOK = CT / TPW;           // tokens per lane group per chunk
+    static constexpr int GW = FD_GROUP_WARPS;      // warps sharing one ring
+    static constexpr int GROUPS = WARPS / GW;
+    static constexpr int STAGES = FD_STAGES;
+    static constexpr int WT = FD_WARP_BYTES / ROW; // tokens per warp per chunk
+    static constexpr int CT = GW * WT;             // tokens per chunk (per group)
+    static constexpr int TOK = WT / TPW;           // tokens per lane group per chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // one of K or V
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
-    static constexpr int RING_BYTES = WARPS * STAGES * STAGE_BYTES;
-    static constexpr int BAR_BYTES = WARPS * STAGES * 8;
+    static constexpr int RING_BYTES = GROUPS * STAGES * STAGE_BYTES;
+    static constexpr int BAR_BYTES = GROUPS * STAGES * 2 * 8;   // full + empty
     static constexpr int RED_BYTES = (2 * WARPS + WARPS * D) * 4 + 16;
     static_assert(LPT >= 1 && LPT <= 32 && 32 % LPT == 0, "row must map onto whole lanes");
-    static_assert(CT % TPW == 0 && TOK >= 1, "chunk must cover whole warp steps");
+    static_assert(WT % TPW == 0 && TOK >= 1, "chunk must cover whole warp steps");
+    static_assert(WARPS % GW == 0, "warps must form whole groups");
     static_assert(D <= THREADS, "one thread per output element in the merge");
 
     static size_t smem_bytes(int decomp, int B)
@@ -188,8 +214,8 @@ template <int CT> __device__ __forceinline__ long long seg_chunks(const Seg &s)
     return ((long long)(s.t1 - s.t0) + CT - 1) / CT;
 }
 
-// Producer side of a warp's ring: walks the warp's chunks (c = w, w+W, ...)
-// of the CTA's chunk sequence and issues the bulk copies for the next one.
+// Producer side of a group's ring: walks the group's chunks (c = g, g+G,
+// ...) of the CTA's chunk sequence and issues the bulk copies for the next.
 template <typename C> struct Producer {
     Seg s;
     long long base;   // chunk index of s's first chunk
@@ -212,10 +238,16 @@ template <typename C> struct Producer {
             const char *ksrc = static_cast<const char *>(p.k) + row * C::ROW;
             const char *vsrc = static_cast<const char *>(p.v) + row * C::ROW;
             mbar_arrive_expect_tx(bar, 2 * bytes);
+#ifdef FD_L2_EVICT_FIRST
+            const uint64_t pol = policy_evict_first();
+            bulk_g2s_hint(kdst, ksrc, bytes, bar, pol);
+            bulk_g2s_hint(kdst + C::CHUNK_BYTES, vsrc, bytes, bar, pol);
+#else
             bulk_g2s(kdst, ksrc, bytes, bar);
             bulk_g2s(kdst + C::CHUNK_BYTES, vsrc, bytes, bar);
+#endif
         }
-        c += C::WARPS;
+        c += C::GROUPS;
         return true;
     }
 };
@@ -236,11 +268,13 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float *a, float 
     m = M;
 }
 
-// One chunk of the warp's ring: block-wise online-softmax update of the lane
-// group's state with its TOK token rows.
+// The warp's WT rows of one chunk: block-wise online-softmax update of the
+// lane group's state with its TOK token rows (ntok valid rows from kbase /
+// vbase).
 template <typename T, int D, bool FULL>
-__device__ __forceinline__ void process_chunk(uint32_t kbase, int ntok, int grp, int col,
-                                              const float *qf, float &m, float &l, float *acc)
+__device__ __forceinline__ void process_chunk(uint32_t kbase, uint32_t vbase, int ntok, int grp,
+                                              int col, const float *qf, float &m, float &l,
+                                              float *acc)
 {
     using C = SplitCfg<T, D>;
     float s[C::TOK];
@@ -251,12 +285,21 @@ __device__ __forceinline__ void process_chunk(uint32_t kbase, int ntok, int grp,
             const uint4 u = lds128(kbase + row * C::ROW + col * 16);
             float kf[C::VEC];
             Elem<T>::widen(u, kf);
+#ifdef FD_FMA2
+            uint64_t d2 = pack2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < C::VEC; i += 2)
+                d2 = fma2(pack2(qf[i], qf[i + 1]), pack2(kf[i], kf[i + 1]), d2);
+            float d0, d1;
+            unpack2(d2, d0, d1);
+#else
             float d0 = 0.f, d1 = 0.f;
 #pragma unroll
             for (int i = 0; i < C::VEC; i += 2) {
                 d0 = fmaf(qf[i], kf[i], d0);
                 d1 = fmaf(qf[i + 1], kf[i + 1], d1);
             }
+#endif
             s[t] = d0 + d1;
         } else {
             s[t] = -INFINITY;
@@ -280,7 +323,6 @@ __device__ __forceinline__ void process_chunk(uint32_t kbase, int ntok, int grp,
 #pragma unroll
     for (int i = 0; i < C::VEC; ++i)
         acc[i] *= alpha;
-    const uint32_t vbase = kbase + C::CHUNK_BYTES;
 #pragma unroll
     for (int t = 0; t < C::TOK; ++t) {
         const int row = t * C::TPW + grp;
@@ -290,16 +332,113 @@ __device__ __forceinline__ void process_chunk(uint32_t kbase, int ntok, int grp,
             const uint4 u = lds128(vbase + row * C::ROW + col * 16);
             float vf[C::VEC];
             Elem<T>::widen(u, vf);
+#ifdef FD_FMA2
+            const uint64_t pp = pack2(pj, pj);
+#pragma unroll
+            for (int i = 0; i < C::VEC; i += 2) {
+                const uint64_t a2 = fma2(pp, pack2(vf[i], vf[i + 1]), pack2(acc[i], acc[i + 1]));
+                unpack2(a2, acc[i], acc[i + 1]);
+            }
+#else
 #pragma unroll
             for (int i = 0; i < C::VEC; ++i)
                 acc[i] = fmaf(pj, vf[i], acc[i]);
+#endif
         }
     }
     m = mnew;
 }
 
+// Block-wide max / sum over the CTA's threads (scratch: one float per warp).
+template <int WARPS>
+__device__ __forceinline__ float block_reduce(float x, bool is_max, float *scratch)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float y = __shfl_xor_sync(FULL_MASK, x, o);
+        x = is_max ? fmaxf(x, y) : x + y;
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (lane == 0)
+        scratch[w] = x;
+    __syncthreads();
+    float r = scratch[0];
+#pragma unroll
+    for (int i = 1; i < WARPS; ++i)
+        r = is_max ? fmaxf(r, scratch[i]) : r + scratch[i];
+    __syncthreads();
+    return r;
+}
+
+// Workspace slot of the i-th piece of (b, h) (see the decompositions).
+__device__ __forceinline__ long long piece_slot(const SplitParams &p, const Ctx &ctx, int bh,
+                                                unsigned i, int gf, long long off)
+{
+    if (p.decomp == DECOMP_SPLITS)
+        return (long long)bh * p.P + i;
+    const long long g = gf + (long long)i;
+    return (i == 0 && bal_bound(gf, ctx.T, ctx.Geff) != off) ? 2 * g + 1 : 2 * g;
+}
+
+// Stage 2 run by the last piece of (b, h) to arrive: the m/l/o merge of
+// "FlashDecoding 数学推导" §2.4.2 over its `target` workspace partials
+// (normalised o, m in base 2, l), read from L2.  All threads take part: the
+// max and the weights are reduced over the pieces in parallel, then each
+// (slot group, element) thread sums its share of the weighted rows.
+template <typename C, int D>
+__device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ctx, int bh,
+                                             unsigned target, int gf, long long off, int tid,
+                                             float *scratch, float *tile)
+{
+    constexpr int NSG = C::THREADS / D;        // slot groups
+    constexpr int TILE = C::WARPS * D;         // weights staged per pass
+    static_assert(C::THREADS % D == 0, "threads must cover whole rows");
+    float mx = -INFINITY;
+    for (unsigned i = tid; i < target; i += C::THREADS) {
+        const long long sl = piece_slot(p, ctx, bh, i, gf, off);
+        if (__ldcg(p.ws_ml + 2 * sl + 1) > 0.f)
+            mx = fmaxf(mx, __ldcg(p.ws_ml + 2 * sl));
+    }
+    const float M = block_reduce<C::WARPS>(mx, true, scratch);
+    const int dim = tid % D, sg = tid / D;
+    float lpart = 0.f, O = 0.f;
+    for (unsigned base = 0; base < target; base += TILE) {
+        const unsigned nt = min((unsigned)TILE, target - base);
+        for (unsigned i = tid; i < nt; i += C::THREADS) {
+            const long long sl = piece_slot(p, ctx, bh, base + i, gf, off);
+            const float ll = __ldcg(p.ws_ml + 2 * sl + 1);
+            const float e = (ll > 0.f) ? ex2(__ldcg(p.ws_ml + 2 * sl) - M) * ll : 0.f;
+            tile[i] = e;
+            lpart += e;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (unsigned i = sg; i < nt; i += NSG) {
+            const float e = tile[i];
+            if (e > 0.f) {
+                const long long sl = piece_slot(p, ctx, bh, base + i, gf, off);
+                O = fmaf(e, __ldcg(p.ws_o + sl * D + dim), O);
+            }
+        }
+        __syncthreads();
+    }
+    const float L = block_reduce<C::WARPS>(lpart, false, scratch);
+    tile[sg * D + dim] = O;
+    __syncthreads();
+    if (tid < D) {
+        float o = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < NSG; ++g2)
+            o += tile[g2 * D + tid];
+        const bool nonempty = L > 0.f;
+        store_out(p.out, (long long)bh * D + tid, p.out_dtype, nonempty ? o / L : 0.f);
+        if (tid == 0 && p.lse)
+            p.lse[bh] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+    }
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, 1) split_kernel(const SplitParams p)
+__global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split_kernel(const SplitParams p)
 {
     using C = SplitCfg<T, D>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -318,10 +457,16 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, 1) split_kernel(const
     long long *cumH = reinterpret_cast<long long *>(smem + C::RING_BYTES + C::BAR_BYTES + C::RED_BYTES);
     int *lenS = reinterpret_cast<int *>(cumH + p.B + 1);
 
-    if (lane == 0) {
+    const int grp_id = w / C::GW;     // this warp's group
+    const int gw = w % C::GW;         // its index inside the group
+    const bool issuer = (gw == 0);
+    // bars: [GROUPS][STAGES] full, then [GROUPS][STAGES] empty
+    if (issuer && lane == 0) {
 #pragma unroll
-        for (int s = 0; s < C::STAGES; ++s)
-            mbar_init(smem_addr(&bars[w * C::STAGES + s]), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_addr(&bars[grp_id * C::STAGES + s]), 1);
+            mbar_init(smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES + s]), C::GW);
+        }
     }
 
     Ctx ctx;
@@ -375,7 +520,10 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, 1) split_kernel(const
             cumH[p.B] = excl + run;
         __syncthreads();
         ctx.T = cumH[p.B];
-        ctx.Geff = (int)(ctx.T < (long long)ctx.G ? ctx.T : (long long)ctx.G);
+        // at least BALANCED_MIN_TOKENS tokens per CTA: a small problem uses
+        // fewer, fuller CTAs (fewer pieces to merge)
+        const long long want = (ctx.T + BALANCED_MIN_TOKENS - 1) / BALANCED_MIN_TOKENS;
+        ctx.Geff = (int)(want < (long long)ctx.G ? want : (long long)ctx.G);
         if (ctx.g < ctx.Geff) {
             ctx.beg = bal_bound(ctx.g, ctx.T, ctx.Geff);
             ctx.end = bal_bound(ctx.g + 1, ctx.T, ctx.Geff);
@@ -394,21 +542,25 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, 1) split_kernel(const
     fence_mbar_init();
     __syncthreads();
 
-    const uint32_t ring_base = smem_addr(ring) + (uint32_t)(w * C::STAGES * C::STAGE_BYTES);
-    const uint32_t bar_base = smem_addr(&bars[w * C::STAGES]);
+    const uint32_t ring_base = smem_addr(ring) + (uint32_t)(grp_id * C::STAGES * C::STAGE_BYTES);
+    const uint32_t bar_base = smem_addr(&bars[grp_id * C::STAGES]);                 // full
+    const uint32_t ebar_base = smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES]);  // empty
+    const uint32_t my_rows = (uint32_t)(gw * C::WT * C::ROW);  // this warp's rows in a stage
 
     Producer<C> prod;
     seg_first(p, ctx, prod.s);
     prod.base = 0;
-    prod.c = w;
-    int issued = 0;   // chunks issued by this warp
+    prod.c = grp_id;
+    int issued = 0;   // chunks issued by this warp (issuers only)
     int landed = 0;   // chunks whose copies this warp has seen complete
     bool dead = false;
+    if (issuer) {
 #pragma unroll 1
-    for (int s = 0; s < C::STAGES; ++s) {
-        if (!prod.issue(p, ctx, ring_base + s * C::STAGE_BYTES, bar_base + s * 8, lane))
-            break;
-        ++issued;
+        for (int s = 0; s < C::STAGES; ++s) {
+            if (!prod.issue(p, ctx, ring_base + s * C::STAGE_BYTES, bar_base + s * 8, lane))
+                break;
+            ++issued;
+        }
     }
 
     Seg cs;
@@ -433,9 +585,9 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, 1) split_kernel(const
         for (int i = 0; i < C::VEC; ++i)
             acc[i] = 0.f;
 
-        long long c = cbase + ((w - cbase % C::WARPS) % C::WARPS + C::WARPS) % C::WARPS;
+        long long c = cbase + ((grp_id - cbase % C::GROUPS) % C::GROUPS + C::GROUPS) % C::GROUPS;
 #pragma unroll 1
-        for (; c < cbase + nc; c += C::WARPS) {
+        for (; c < cbase + nc; c += C::GROUPS) {
             const int stage = consumed % C::STAGES;
             const uint32_t parity = (consumed / C::STAGES) & 1;
             ++consumed;
@@ -446,16 +598,26 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, 1) split_kernel(const
                     dead = true;
             }
             const int t = cs.t0 + (int)((c - cbase) * C::CT);
-            const int ntok = min(C::CT, cs.t1 - t);
+            const int ntok = min(C::CT, cs.t1 - t) - gw * C::WT;  // this warp's valid rows
             const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
-            if (!dead) {
-                if (ntok == C::CT)
-                    process_chunk<T, D, true>(kb, ntok, grp, col, qf, m, l, acc);
+            if (!dead && ntok > 0) {
+                if (ntok >= C::WT)
+                    process_chunk<T, D, true>(kb + my_rows, kb + C::CHUNK_BYTES + my_rows, C::WT,
+                                              grp, col, qf, m, l, acc);
                 else
-                    process_chunk<T, D, false>(kb, ntok, grp, col, qf, m, l, acc);
+                    process_chunk<T, D, false>(kb + my_rows, kb + C::CHUNK_BYTES + my_rows, ntok,
+                                               grp, col, qf, m, l, acc);
             }
             __syncwarp();
-            if (!dead && prod.issue(p, ctx, kb, bar_base + stage * 8, lane))
+            if (C::GW > 1) {
+                // release the stage; the issuer refills it once every warp of
+                // the group has released it
+                if (!dead && lane == 0)
+                    mbar_arrive(ebar_base + stage * 8);
+                if (issuer && !dead && !mbar_wait_bounded(ebar_base + stage * 8, parity))
+                    dead = true;
+            }
+            if (issuer && !dead && prod.issue(p, ctx, kb, bar_base + stage * 8, lane))
                 ++issued;
         }
 
@@ -553,42 +715,7 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, 1) split_kernel(const
             __syncthreads();
             if (*flag) {
                 __threadfence();
-                if (tid < D) {
-                    float M = -INFINITY;
-                    for (unsigned i = 0; i < target; ++i) {
-                        long long sl;
-                        if (p.decomp == DECOMP_SPLITS) {
-                            sl = (long long)bh * p.P + i;
-                        } else {
-                            const long long g = gf + (long long)i;
-                            sl = (i == 0 && bal_bound(gf, ctx.T, ctx.Geff) != off) ? 2 * g + 1 : 2 * g;
-                        }
-                        const float ml = __ldcg(p.ws_ml + 2 * sl);
-                        const float ll = __ldcg(p.ws_ml + 2 * sl + 1);
-                        if (ll > 0.f)
-                            M = fmaxf(M, ml);
-                    }
-                    float L = 0.f, O = 0.f;
-                    for (unsigned i = 0; i < target; ++i) {
-                        long long sl;
-                        if (p.decomp == DECOMP_SPLITS) {
-                            sl = (long long)bh * p.P + i;
-                        } else {
-                            const long long g = gf + (long long)i;
-                            sl = (i == 0 && bal_bound(gf, ctx.T, ctx.Geff) != off) ? 2 * g + 1 : 2 * g;
-                        }
-                        const float ll = __ldcg(p.ws_ml + 2 * sl + 1);
-                        if (ll > 0.f) {
-                            const float e = ex2(__ldcg(p.ws_ml + 2 * sl) - M) * ll;
-                            L += e;
-                            O = fmaf(e, __ldcg(p.ws_o + sl * D + tid), O);
-                        }
-                    }
-                    const bool nonempty = L > 0.f;
-                    store_out(p.out, (long long)bh * D + tid, p.out_dtype, nonempty ? O / L : 0.f);
-                    if (tid == 0 && p.lse)
-                        p.lse[bh] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
-                }
+                merge_pieces<C, D>(p, ctx, bh, target, gf, off, tid, red_m, red_acc);
             }
         }
         __syncthreads();
