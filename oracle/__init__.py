@@ -72,6 +72,8 @@ def _load():
         lib.or_online_softmax.restype = None
         lib.or_tile_incremental.argtypes = [P, P, I, I, P, P, P, P, P, P]
         lib.or_tile_incremental.restype = None
+        lib.or_attention_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, I64, I, D, P, P, I]
+        lib.or_attention_paged.restype = I
         lib.or_decode.argtypes = [I, P, P, I64]
         lib.or_decode.restype = None
         lib.or_f16_to_double.argtypes = [ctypes.c_uint16]
@@ -154,6 +156,45 @@ def attention(q, k, v, lens=None, scale=None, dtype=None, nthreads=None):
                           int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError("or_attention failed")
+    return out, lse
+
+
+def attention_paged(q, k_pages, v_pages, block_table, lens, scale=None, dtype=None,
+                    nthreads=None):
+    """Full attention over a paged KV cache, in float64.  Returns ``(out, lse)``.
+
+    k_pages / v_pages [num_pages, H, page_size, d]; block_table [B, max_pages]
+    int32; lens [B].  Logical token t of sequence b is row t % page_size of
+    physical page block_table[b, t // page_size] (the block-table
+    indirection of "adv04: Flash-Decoding" §5 and "从第一性原理推导 Flash
+    Attention" §7.1).
+    """
+    lib = _load()
+    qb, dq = as_bits(q, dtype)
+    kb, dk = as_bits(k_pages, dtype)
+    vb, dv = as_bits(v_pages, dtype)
+    if not (dq == dk == dv):
+        raise TypeError("q, K and V must share one dtype")
+    num_pages, H, ps, d = kb.shape
+    B = qb.shape[0]
+    if qb.shape != (B, H, d) or vb.shape != kb.shape:
+        raise ValueError("shapes")
+    if hasattr(block_table, "detach"):
+        block_table = block_table.detach().cpu().numpy()
+    if hasattr(lens, "detach"):
+        lens = lens.detach().cpu().numpy()
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    lb = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+    maxp = bt.shape[1] if bt.ndim == 2 else 0
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.empty((B, H, d), np.float64)
+    lse = np.empty((B, H), np.float64)
+    rc = lib.or_attention_paged(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), _ptr(lb), B, H, d, ps,
+                                maxp, num_pages, DTYPE_CODES[dq], float(scale), _ptr(out),
+                                _ptr(lse), int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("or_attention_paged failed (bad arguments or block-table entry)")
     return out, lse
 
 

@@ -11,7 +11,8 @@
  *   [FDD]  "FlashDecoding 数学推导"
  *   [ADV4] "adv04: Flash-Decoding（长序列 Decode 切分 + FlashInfer 简介）"
  *   [LSE]  "FlashDecoding 数学推导：传统 m/l/o 方法与 LSE 方法"
- *   [FA1P] "从第一性原理推导 Flash Attention" (its merge lemma, §3.2)
+ *   [FA1P] "从第一性原理推导 Flash Attention" (its merge lemma, §3.2; paged
+ *          KV, §7.1)
  *
  * Everything is computed in IEEE double with plain loops in index order; no
  * blocking, no fusion, no reordering beyond what the cited formulas state.
@@ -292,6 +293,145 @@ int or_split_partials(const void *q, const void *k, const void *v, const int32_t
     j.scale = scale;
     j.o_part = o_part; j.m_part = m_part; j.l_part = l_part; j.s_part = s_part;
     return run_pairs(&j, split_pair, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
+/* paged KV cache                                                      */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Full attention over a paged KV cache (the block-table indirection of
+ * [ADV4] §5 "分页 KV Cache" and [FA1P] §7.1).  Pages are laid out
+ * [num_pages, H, page_size, d]; logical token t of sequence b is row
+ * t % page_size of head h in physical page block_table[b*max_pages +
+ * t/page_size].  lens is required.  The arithmetic is or_attention's on the
+ * gathered rows.  Returns -1 on bad arguments or a table entry outside
+ * [0, num_pages).
+ */
+typedef struct {
+    const void *q, *kp, *vp;
+    const int32_t *table, *lens;
+    int B, H, d, ps, maxp, dtype;
+    int64_t num_pages;
+    double scale;
+    double *out, *lse;
+    int bad;
+} pjob_t;
+
+static size_t paged_row(const pjob_t *j, int b, int h, int t)
+{
+    int32_t pg = j->table[(int64_t)b * j->maxp + t / j->ps];
+    return (((size_t)pg * j->H + h) * j->ps + (size_t)(t % j->ps)) * j->d;
+}
+
+static void *paged_worker(void *arg)
+{
+    pjob_t **pp = (pjob_t **)arg;
+    pjob_t *j = pp[0];
+    int tid = (int)(intptr_t)pp[1], nth = (int)(intptr_t)pp[2];
+    int64_t total = (int64_t)j->B * j->H;
+    for (int64_t bh = tid; bh < total; bh += nth) {
+        int b = (int)(bh / j->H), h = (int)(bh % j->H);
+        int n = j->lens[b];
+        if (n < 0)
+            n = 0;
+        if (n > j->maxp * j->ps)
+            n = j->maxp * j->ps;
+        double *o = j->out + bh * j->d;
+        for (int i = 0; i < j->d; ++i)
+            o[i] = 0.0;
+        if (n == 0) {
+            if (j->lse)
+                j->lse[bh] = -INFINITY;
+            continue;
+        }
+        double *s = (double *)malloc(sizeof(double) * (size_t)n);
+        if (!s) {
+            j->bad = 1;
+            continue;
+        }
+        size_t qb = (size_t)bh * j->d;
+        double m = -INFINITY;
+        for (int t = 0; t < n; ++t) {
+            size_t kr = paged_row(j, b, h, t);
+            double acc = 0.0;
+            for (int i = 0; i < j->d; ++i)
+                acc += load_elem(j->q, qb + i, j->dtype) * load_elem(j->kp, kr + i, j->dtype);
+            s[t] = j->scale * acc;
+            if (s[t] > m)
+                m = s[t];
+        }
+        double l = 0.0;
+        for (int t = 0; t < n; ++t) {
+            double w = exp(s[t] - m);
+            size_t vr = paged_row(j, b, h, t);
+            l += w;
+            for (int i = 0; i < j->d; ++i)
+                o[i] += w * load_elem(j->vp, vr + i, j->dtype);
+        }
+        for (int i = 0; i < j->d; ++i)
+            o[i] /= l;
+        if (j->lse)
+            j->lse[bh] = m + log(l);
+        free(s);
+    }
+    return NULL;
+}
+
+int or_attention_paged(const void *q, const void *k_pages, const void *v_pages,
+                       const int32_t *block_table, const int32_t *lens, int B, int H, int d,
+                       int page_size, int max_pages, int64_t num_pages, int dtype, double scale,
+                       double *out, double *lse, int nthreads)
+{
+    if (B < 0 || H < 0 || d <= 0 || page_size < 1 || max_pages < 0 || num_pages < 0 ||
+        dtype < 0 || dtype > 2 || !out || !lens)
+        return -1;
+    /* every table entry a sequence uses must name an existing page */
+    for (int b = 0; b < B; ++b) {
+        int n = lens[b] < 0 ? 0 : lens[b];
+        if (n > max_pages * page_size)
+            n = max_pages * page_size;
+        for (int pgi = 0; pgi * page_size < n; ++pgi) {
+            int32_t pg = block_table[(int64_t)b * max_pages + pgi];
+            if (pg < 0 || pg >= num_pages)
+                return -1;
+        }
+    }
+    pjob_t j;
+    memset(&j, 0, sizeof j);
+    j.q = q; j.kp = k_pages; j.vp = v_pages; j.table = block_table; j.lens = lens;
+    j.B = B; j.H = H; j.d = d; j.ps = page_size; j.maxp = max_pages; j.dtype = dtype;
+    j.num_pages = num_pages; j.scale = scale; j.out = out; j.lse = lse;
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 1024)
+        nthreads = 1024;
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    void *(*args)[3] = calloc((size_t)nthreads, sizeof *args);
+    if (!th || !args) {
+        free(th);
+        free(args);
+        return -1;
+    }
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        args[t][0] = &j;
+        args[t][1] = (void *)(intptr_t)t;
+        args[t][2] = (void *)(intptr_t)nthreads;
+    }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, paged_worker, args[t]) != 0)
+            break;
+        started = t;
+    }
+    for (int t = started + 1; t < nthreads; ++t)
+        paged_worker(args[t]);
+    paged_worker(args[0]);
+    for (int t = 1; t <= started; ++t)
+        pthread_join(th[t], NULL);
+    free(th);
+    free(args);
+    return j.bad ? -1 : 0;
 }
 
 /* ------------------------------------------------------------------ */

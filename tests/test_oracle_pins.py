@@ -353,3 +353,69 @@ def test_merges_of_synthetic_partials_agree():
     r = int(np.argmax((~empty).sum(1)))
     w = np.where(empty[r], 0.0, np.exp(s[r] - np.max(s[r])))
     assert np.allclose(a[0][r], (w[:, None] * o[r]).sum(0) / w.sum(), atol=1e-13)
+
+
+# ------------------------------------------------------------ paged KV cache
+
+def _paged_from_contiguous(K, V, lens, page_size, rng, extra_pages=3):
+    """Scatter contiguous [B,H,N,d] K/V into shuffled pages [P,H,ps,d] with a
+    block table; unused pages and rows are NaN (never to be read)."""
+    B, H, N, d = K.shape
+    maxp = -(-N // page_size)
+    num_pages = B * maxp + extra_pages
+    perm = rng.permutation(num_pages)[: B * maxp].reshape(B, maxp).astype(np.int32)
+    Kp = np.full((num_pages, H, page_size, d), np.nan, dtype=K.dtype)
+    Vp = np.full((num_pages, H, page_size, d), np.nan, dtype=V.dtype)
+    for b in range(B):
+        for j in range(maxp):
+            lo, hi = j * page_size, min((j + 1) * page_size, int(lens[b]))
+            if lo >= hi:
+                continue
+            Kp[perm[b, j], :, : hi - lo] = K[b, :, lo:hi]
+            Vp[perm[b, j], :, : hi - lo] = V[b, :, lo:hi]
+    return Kp, Vp, perm
+
+
+@pytest.mark.parametrize("page_size", [1, 3, 16, 37])
+def test_paged_oracle_equals_contiguous_on_gathered_rows(page_size):
+    rng = np.random.default_rng(page_size)
+    B, H, N, d = 3, 2, 75, 8
+    q = _f32(rng.normal(size=(B, H, d)))
+    K = _f32(rng.normal(size=(B, H, N, d)) * 3)
+    V = _f32(rng.normal(size=(B, H, N, d)))
+    lens = np.array([75, 0, 41], np.int32)
+    Kp, Vp, table = _paged_from_contiguous(K, V, lens, page_size, rng)
+    out, lse = oracle.attention(q, K, V, lens=lens)
+    pout, plse = oracle.attention_paged(q, Kp, Vp, table, lens)
+    # same rows, same loop order: identical results
+    assert np.array_equal(pout, out)
+    assert np.array_equal(plse, lse)
+    assert np.all(np.isfinite(pout))  # no NaN page or row was read
+
+
+def test_paged_oracle_single_page_per_sequence_is_contiguous():
+    rng = np.random.default_rng(0)
+    B, H, N, d = 2, 3, 20, 4
+    q = _f32(rng.normal(size=(B, H, d)))
+    K = _f32(rng.normal(size=(B, H, N, d)))
+    V = _f32(rng.normal(size=(B, H, N, d)))
+    # page b holds sequence b whole: the paged layout of one page per sequence
+    Kp = np.ascontiguousarray(K)
+    Vp = np.ascontiguousarray(V)
+    table = np.arange(B, dtype=np.int32).reshape(B, 1)
+    lens = np.array([20, 7], np.int32)
+    out, lse = oracle.attention(q, K, V, lens=lens)
+    pout, plse = oracle.attention_paged(q, Kp, Vp, table, lens)
+    assert np.array_equal(pout, out) and np.array_equal(plse, lse)
+
+
+def test_paged_oracle_rejects_bad_table_entries():
+    q = _f32(np.zeros((1, 1, 4)))
+    Kp = _f32(np.zeros((2, 1, 4, 4)))
+    with pytest.raises(RuntimeError):
+        oracle.attention_paged(q, Kp, Kp, np.array([[0, 2]], np.int32), [5])
+    with pytest.raises(RuntimeError):
+        oracle.attention_paged(q, Kp, Kp, np.array([[-1, 0]], np.int32), [2])
+    # an entry past the sequence's last page is never used
+    out, _ = oracle.attention_paged(q, Kp, Kp, np.array([[1, 99]], np.int32), [4])
+    assert np.all(out == 0)
