@@ -258,7 +258,7 @@ def run_reference(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, "auto"),
+        "config": config_of(w, "auto", args.page_size),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {rows} of {w.B * w.H} (b,h) rows of {w.name}, "
                                    f"full length, drawn on the host with the workload's "
@@ -269,9 +269,11 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w, num_splits):
+def config_of(w, num_splits, page_size=0):
     return {"workload": w.name, "batch": w.B, "heads": w.H, "kv_len": w.N, "head_dim": w.d,
             "kv_dtype": w.dtype, "out_dtype": w.out_dtype, "num_splits": num_splits,
+            "kv_layout": (f"paged, {page_size}-token pages in shuffled order" if page_size
+                          else "contiguous [B,H,N,d]"),
             "lengths": "uniform[1,N] seeded" if w.ragged else "all N",
             "k_scale": w.k_scale,
             "l2": ("inputs larger than L2, no flush"
@@ -294,6 +296,19 @@ def run_ours(args, w):
 
     q, k, v, lens = make_inputs(w, device=dev)
     lens_h = lens.cpu().tolist()
+    table = None
+    if args.page_size:
+        from split_kv_fd_gb300.inputs import to_paged
+        k, v, table = to_paged(k, v, args.page_size, seed=w.seed)
+        torch.cuda.empty_cache()
+
+    def decode(out, lse, stream):
+        if table is None:
+            fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
+                      workspace=wsbuf, stream=stream)
+        else:
+            fd.decode_paged(q, k, v, table, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
+                            workspace=wsbuf, stream=stream)
     out = torch.empty((w.B, w.H, w.d), dtype=getattr(torch, {"bf16": "bfloat16", "f16": "float16",
                                                             "f32": "float32"}[w.out_dtype]),
                       device=dev)
@@ -315,8 +330,7 @@ def run_ours(args, w):
     def step():
         if flush is not None:
             do_flush()
-        fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse, workspace=wsbuf,
-                  stream=stream)
+        decode(out, lse, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -337,8 +351,7 @@ def run_ours(args, w):
         if flush is not None:
             do_flush()
         evs[i][0].record(stream)
-        fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse, workspace=wsbuf,
-                  stream=stream)
+        decode(out, lse, stream)
         evs[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -355,6 +368,8 @@ def run_ours(args, w):
     value = ws * kvb / (ms_per_step * 1e-3) / 1e9
     peaks, peak_src = measured_peaks()
     alg = algorithmic_bytes(w, lens_h)
+    if table is not None:  # the block-table entries the kernel reads
+        alg += 4 * sum(-(-int(n) // args.page_size) for n in lens_h) * w.H
     achieved = alg / (kern_ms * 1e-3) / 1e9
     tokens = sum(lens_h) * w.H
 
@@ -365,6 +380,7 @@ def run_ours(args, w):
         hk = k.cpu().pin_memory()
         hv = v.cpu().pin_memory()
         hl = lens.cpu().pin_memory()
+        ht = table.cpu().pin_memory() if table is not None else None
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -374,8 +390,9 @@ def run_ours(args, w):
             k.copy_(hk, non_blocking=True)
             v.copy_(hv, non_blocking=True)
             lens.copy_(hl, non_blocking=True)
-            fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
-                      workspace=wsbuf, stream=stream)
+            if table is not None:
+                table.copy_(ht, non_blocking=True)
+            decode(out, lse, stream)
             hout.copy_(out, non_blocking=True)
             hlse.copy_(lse, non_blocking=True)
 
@@ -390,7 +407,7 @@ def run_ours(args, w):
         b.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = reduce_max(a.elapsed_time(b), ws, dev) / e2e_steps
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl, ht) if t is not None)
         d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
         e2e = {"value": ws * kvb / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e_ms}
@@ -405,13 +422,14 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": config_of(w, "auto"),
+            "config": config_of(w, "auto", args.page_size),
             "tokens_per_s": ws * tokens / (ms_per_step * 1e-3),
             "pct_of_nominal_8tbs": 100.0 * value / ws / NOMINAL_HBM_GBS,
             "pct_of_measured_hbm": 100.0 * value / ws / peaks["hbm_gbs"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": profiled_traffic(w.name), "kernel": "split_kernel",
+                         "traffic": None if table is not None else profiled_traffic(w.name),
+                         "kernel": "split_kernel",
                          "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                          "algorithmic_bytes_per_launch": alg, "mean_launch_ms": kern_ms},
             "e2e": e2e,
@@ -434,6 +452,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=BENCH_DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="time fd_decode_paged on the workload laid out in pages of this many tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -56,7 +56,8 @@ typedef enum {
     FD_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required */
     FD_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed       */
     FD_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up waiting on its own copies */
-    FD_ERR_SCRATCH_TOO_SMALL = 6 /* fd_decode_noalloc: problem exceeds its scratch */
+    FD_ERR_SCRATCH_TOO_SMALL = 6, /* fd_decode_noalloc: problem exceeds its scratch */
+    FD_ERR_BAD_PAGE = 7         /* a block-table entry named no page (see fd_decode_paged) */
 } fd_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -112,6 +113,29 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * fd_decode over a paged KV cache: the block-table indirection of "adv04:
+ * Flash-Decoding" §5 (FlashInfer's 分页 KV Cache, block_table) and
+ * "从第一性原理推导 Flash Attention" §7.1.  Same operation and results as
+ * fd_decode on the gathered rows.
+ *   k_pages, v_pages  [num_pages, H, page_size, d] in `in_dtype`: every
+ *                     (page, head) holds page_size consecutive token rows
+ *   block_table       [B, max_pages] int32: logical page j of sequence b is
+ *                     physical page block_table[b*max_pages + j]
+ *   seqlens           [B] int32, required; clamped to [0, max_pages*page_size];
+ *                     only table entries of pages holding tokens < seqlens[b]
+ *                     are read
+ *   workspace         fd_workspace_size(B, H, max_pages*page_size, d, num_splits)
+ * A table entry outside [0, num_pages) is never dereferenced: its rows are
+ * read from page 0 instead and fd_device_status() reports FD_ERR_BAD_PAGE
+ * (the results of that sequence are then meaningless).
+ */
+fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                          const int32_t *block_table, const int32_t *seqlens, int B, int H, int d,
+                          int page_size, int max_pages, long long num_pages, fd_dtype in_dtype,
+                          int num_splits, float scale, void *out, fd_dtype out_dtype, float *lse,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Stage 1 alone: per-split partials for num_splits >= 1 splits of every
  * sequence, split p covering tokens [p*c, min((p+1)*c, len)), c =
  * ceil(len/num_splits) ("adv04: Flash-Decoding" §4).  For each split
@@ -147,9 +171,9 @@ fd_status fd_combine_lse(const float *o_part, const float *lse_part,
 
 /*
  * Reads (and if `reset` is non-zero, clears) the current device's status
- * word, which a kernel sets when it gives up waiting on its own copies.
- * Synchronises the device.  Returns FD_OK, FD_ERR_DEVICE_TIMEOUT or
- * FD_ERR_CUDA.
+ * word, which a kernel sets when it gives up waiting on its own copies or
+ * meets a block-table entry that names no page.  Synchronises the device.
+ * Returns FD_OK, FD_ERR_DEVICE_TIMEOUT, FD_ERR_BAD_PAGE or FD_ERR_CUDA.
  */
 fd_status fd_device_status(int reset);
 

@@ -144,6 +144,8 @@ const char *fd_status_str(int status)
     case FD_ERR_WORKSPACE: return "FD_ERR_WORKSPACE: workspace missing or too small";
     case FD_ERR_CUDA: return "FD_ERR_CUDA: a CUDA runtime call or launch failed";
     case FD_ERR_DEVICE_TIMEOUT: return "FD_ERR_DEVICE_TIMEOUT: a kernel gave up waiting on its copies";
+    case FD_ERR_BAD_PAGE:
+        return "FD_ERR_BAD_PAGE: a block-table entry named no page (its rows were read from page 0)";
     case FD_ERR_SCRATCH_TOO_SMALL:
         return "FD_ERR_SCRATCH_TOO_SMALL: the problem needs more scratch than fd_decode_noalloc's "
                "static buffer (FD_NOALLOC_SCRATCH_BYTES) holds; use fd_decode with a workspace";
@@ -340,7 +342,72 @@ fd_status fd_device_status(int reset)
         if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess)
             return FD_ERR_CUDA;
     }
-    return (v & STATUS_TIMEOUT) ? FD_ERR_DEVICE_TIMEOUT : FD_OK;
+    if (v & STATUS_TIMEOUT)
+        return FD_ERR_DEVICE_TIMEOUT;
+    return (v & STATUS_BAD_PAGE) ? FD_ERR_BAD_PAGE : FD_OK;
+}
+
+fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                          const int32_t *block_table, const int32_t *seqlens, int B, int H, int d,
+                          int page_size, int max_pages, long long num_pages, fd_dtype in_dtype,
+                          int num_splits, float scale, void *out, fd_dtype out_dtype, float *lse,
+                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (page_size < 1 || max_pages < 0 || num_pages < 0 ||
+        (long long)page_size * max_pages > 0x7fffffffLL)
+        return FD_ERR_INVALID_ARG;
+    const int N = page_size * max_pages;
+    if (!sizes_ok(B, H, N, d) || num_splits < 0 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0)
+        return FD_OK;
+    const bool pages = N > 0;
+    if (!q || !seqlens || !out || (pages && (!k_pages || !v_pages || !block_table || num_pages < 1)) ||
+        !aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(seqlens, 4) || !aligned(block_table, 4) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    unsigned *st = status_ptr();
+    if (sms <= 0 || !st)
+        return FD_ERR_CUDA;
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    const WsLayout wl = ws_layout(pl.slots, d, (long long)B * H);
+    if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
+        return FD_ERR_WORKSPACE;
+
+    SplitParams p = {};
+    p.q = q;
+    p.k = k_pages;
+    p.v = v_pages;
+    p.lens = seqlens;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.paged = 1;
+    p.block_table = block_table;
+    p.page_size = page_size;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.decomp = pl.decomp;
+    p.P = pl.P;
+    p.grid = pl.grid;
+    p.out_kind = OUT_FUSED;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.lse = lse;
+    char *ws = static_cast<char *>(workspace);
+    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
+    p.status = st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
+    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * H * sizeof(unsigned), cs) != cudaSuccess)
+        return FD_ERR_CUDA;
+    return launch(in_dtype, d, p, pl.decomp, cs);
 }
 
 }  // extern "C"

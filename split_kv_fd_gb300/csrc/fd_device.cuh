@@ -20,6 +20,7 @@ constexpr unsigned WAIT_LIMIT_POLLS = 1u << 30;
 
 // Status word bits.
 constexpr unsigned STATUS_TIMEOUT = 1u;
+constexpr unsigned STATUS_BAD_PAGE = 2u;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {

@@ -28,7 +28,13 @@ struct SplitParams {
     const void *k;
     const void *v;
     const int32_t *lens;  // device, may be null => all N
-    int B, H, N;
+    int B, H, N;          // N: padded length (paged: max_pages * page_size)
+    // paged KV cache: K/V are [num_pages, H, page_size, d]; logical token t
+    // of sequence b is row t % page_size of page block_table[b*max_pages + t/page_size]
+    int paged;
+    const int32_t *block_table;
+    int page_size, max_pages;
+    long long num_pages;
     float scale_log2;     // scale * log2(e): scores are kept in base 2
     int decomp;
     int P;                // splits per sequence for DECOMP_SPLITS

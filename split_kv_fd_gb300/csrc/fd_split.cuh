@@ -209,45 +209,121 @@ __device__ __forceinline__ void seg_next(const SplitParams &p, const Ctx &c, Seg
     s.t1 = (long long)len < room ? len : (int)room;
 }
 
+// Chunks lie on a fixed grid of the sequence's token index (multiples of CT),
+// so a chunk never straddles more pages than it must; a segment's first and
+// last chunks may be partial.
 template <int CT> __device__ __forceinline__ long long seg_chunks(const Seg &s)
 {
-    return ((long long)(s.t1 - s.t0) + CT - 1) / CT;
+    if (s.t1 <= s.t0)
+        return 0;
+    return (long long)((s.t1 + CT - 1) / CT - s.t0 / CT);
+}
+
+// First token and token count of chunk i of segment s.
+template <int CT>
+__device__ __forceinline__ void chunk_coords(const Seg &s, long long i, int &t, int &ntok)
+{
+    const long long blk = s.t0 / CT + i;
+    const long long lo = blk * CT;
+    t = (int)(lo > s.t0 ? lo : s.t0);
+    const long long hi = lo + CT < s.t1 ? lo + CT : s.t1;
+    ntok = (int)(hi - t);
 }
 
 // Producer side of a group's ring: walks the group's chunks (c = g, g+G,
 // ...) of the CTA's chunk sequence and issues the bulk copies for the next.
+// It always knows the coordinates of the chunk it will issue next and, for a
+// paged cache, has that chunk's block-table entries already loading into
+// registers (lane j holds pieces j and j+32), so a refill never waits on a
+// table lookup.
 template <typename C> struct Producer {
     Seg s;
     long long base;   // chunk index of s's first chunk
     long long c;      // next chunk to issue
+    bool have;        // chunk c exists
+    int t, ntok;      // its first token and token count
+    int pg0, pg1;     // prefetched page entries of its pieces lane, lane + 32
 
-    __device__ __forceinline__ bool issue(const SplitParams &p, const Ctx &ctx, uint32_t kdst,
-                                          uint32_t bar, int lane)
+    __device__ __forceinline__ void locate(const SplitParams &p, const Ctx &ctx, int lane)
     {
         while (s.valid && c >= base + seg_chunks<C::CT>(s)) {
             base += seg_chunks<C::CT>(s);
             seg_next(p, ctx, s);
         }
-        if (!s.valid)
+        have = s.valid;
+        if (!have)
+            return;
+        chunk_coords<C::CT>(s, c - base, t, ntok);
+        if (p.paged) {
+            const int ps = p.page_size;
+            const int first = t / ps;
+            const int npieces = (t + ntok - 1) / ps - first + 1;
+            const int32_t *row = p.block_table + (long long)s.b * p.max_pages + first;
+            pg0 = lane < npieces ? __ldg(row + lane) : 0;
+            pg1 = lane + 32 < npieces ? __ldg(row + lane + 32) : 0;
+        }
+    }
+
+    __device__ __forceinline__ void start(const SplitParams &p, const Ctx &ctx, int first_chunk,
+                                          int lane)
+    {
+        seg_first(p, ctx, s);
+        base = 0;
+        c = first_chunk;
+        locate(p, ctx, lane);
+    }
+
+    __device__ __forceinline__ bool issue(const SplitParams &p, const Ctx &ctx, uint32_t kdst,
+                                          uint32_t bar, int lane)
+    {
+        if (!have)
             return false;
-        const int t = s.t0 + (int)((c - base) * C::CT);
-        const int ntok = min(C::CT, s.t1 - t);
-        if (lane == 0) {
-            const uint32_t bytes = (uint32_t)ntok * C::ROW;
-            const long long row = ((long long)s.b * p.H + s.h) * p.N + t;
-            const char *ksrc = static_cast<const char *>(p.k) + row * C::ROW;
-            const char *vsrc = static_cast<const char *>(p.v) + row * C::ROW;
+        const uint32_t bytes = (uint32_t)ntok * C::ROW;
+        if (lane == 0)
             mbar_arrive_expect_tx(bar, 2 * bytes);
+        if (!p.paged) {
+            if (lane == 0) {
+                const long long row = ((long long)s.b * p.H + s.h) * p.N + t;
+                const char *ksrc = static_cast<const char *>(p.k) + row * C::ROW;
+                const char *vsrc = static_cast<const char *>(p.v) + row * C::ROW;
 #ifdef FD_L2_EVICT_FIRST
-            const uint64_t pol = policy_evict_first();
-            bulk_g2s_hint(kdst, ksrc, bytes, bar, pol);
-            bulk_g2s_hint(kdst + C::CHUNK_BYTES, vsrc, bytes, bar, pol);
+                const uint64_t pol = policy_evict_first();
+                bulk_g2s_hint(kdst, ksrc, bytes, bar, pol);
+                bulk_g2s_hint(kdst + C::CHUNK_BYTES, vsrc, bytes, bar, pol);
 #else
-            bulk_g2s(kdst, ksrc, bytes, bar);
-            bulk_g2s(kdst + C::CHUNK_BYTES, vsrc, bytes, bar);
+                bulk_g2s(kdst, ksrc, bytes, bar);
+                bulk_g2s(kdst + C::CHUNK_BYTES, vsrc, bytes, bar);
 #endif
+            }
+        } else {
+            // the chunk's rows split at page boundaries: lane j copies pieces
+            // j, j+32, ... (page entries prefetched by locate())
+            __syncwarp();
+            const int ps = p.page_size;
+            const int first = t / ps;
+            const int npieces = (t + ntok - 1) / ps - first + 1;
+            for (int j = lane; j < npieces; j += 32) {
+                const int lp = first + j;
+                const int r0 = max(t, lp * ps);
+                const int r1 = min(t + ntok, (lp + 1) * ps);
+                long long pg = j < 32 ? pg0
+                             : j < 64 ? pg1
+                                      : __ldg(p.block_table + (long long)s.b * p.max_pages + lp);
+                if (pg < 0 || pg >= p.num_pages) {
+                    // never read outside the pages: record it, read page 0
+                    atomicOr(p.status, STATUS_BAD_PAGE);
+                    pg = 0;
+                }
+                const long long row = (pg * p.H + s.h) * ps + (r0 - lp * ps);
+                const uint32_t nb = (uint32_t)(r1 - r0) * C::ROW;
+                const uint32_t off = (uint32_t)(r0 - t) * C::ROW;
+                bulk_g2s(kdst + off, static_cast<const char *>(p.k) + row * C::ROW, nb, bar);
+                bulk_g2s(kdst + C::CHUNK_BYTES + off, static_cast<const char *>(p.v) + row * C::ROW, nb,
+                         bar);
+            }
         }
         c += C::GROUPS;
+        locate(p, ctx, lane);
         return true;
     }
 };
@@ -548,9 +624,8 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split
     const uint32_t my_rows = (uint32_t)(gw * C::WT * C::ROW);  // this warp's rows in a stage
 
     Producer<C> prod;
-    seg_first(p, ctx, prod.s);
-    prod.base = 0;
-    prod.c = grp_id;
+    if (issuer)
+        prod.start(p, ctx, grp_id, lane);
     int issued = 0;   // chunks issued by this warp (issuers only)
     int landed = 0;   // chunks whose copies this warp has seen complete
     bool dead = false;
@@ -597,8 +672,9 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split
                 else
                     dead = true;
             }
-            const int t = cs.t0 + (int)((c - cbase) * C::CT);
-            const int ntok = min(C::CT, cs.t1 - t) - gw * C::WT;  // this warp's valid rows
+            int t, ntok_chunk;
+            chunk_coords<C::CT>(cs, c - cbase, t, ntok_chunk);
+            const int ntok = ntok_chunk - gw * C::WT;  // this warp's valid rows
             const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
             if (!dead && ntok > 0) {
                 if (ntok >= C::WT)

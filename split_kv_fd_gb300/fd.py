@@ -20,14 +20,14 @@ from . import _build_lib
 FD_OK = 0
 STATUS_NAMES = {0: "FD_OK", 1: "FD_ERR_INVALID_ARG", 2: "FD_ERR_UNSUPPORTED",
                 3: "FD_ERR_WORKSPACE", 4: "FD_ERR_CUDA", 5: "FD_ERR_DEVICE_TIMEOUT",
-                6: "FD_ERR_SCRATCH_TOO_SMALL"}
+                6: "FD_ERR_SCRATCH_TOO_SMALL", 7: "FD_ERR_BAD_PAGE"}
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 # every symbol include/fd.h declares
 EXPORTS = ["fd_status_str", "fd_version", "fd_num_sms", "fd_auto_num_splits",
            "fd_workspace_size", "fd_decode", "fd_decode_split", "fd_combine_mlo",
-           "fd_combine_lse", "fd_device_status", "fd_decode_noalloc"]
+           "fd_combine_lse", "fd_device_status", "fd_decode_noalloc", "fd_decode_paged"]
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,9 @@ def load(build_if_missing: bool = False):
         lib.fd_combine_mlo.restype = I
         lib.fd_combine_lse.argtypes = [P, P, I, I, I, I, P, I, P, P]
         lib.fd_combine_lse.restype = I
+        lib.fd_decode_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_longlong, I, I, F, P, I,
+                                        P, P, S, P]
+        lib.fd_decode_paged.restype = I
         lib.fd_device_status.argtypes = [I]
         lib.fd_device_status.restype = I
         _lib = lib
@@ -187,6 +190,48 @@ def decode(q, k, v, seqlens=None, num_splits=0, scale=None, out_dtype=None, out=
                        _ptr(workspace), workspace.numel() * workspace.element_size(),
                        _stream(q, stream))
     _check(st, "fd_decode")
+    return out, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seqlens, num_splits=0, scale=None,
+                 out_dtype=None, out=None, lse=None, return_lse=True, workspace=None, stream=None):
+    """fd_decode over a paged KV cache (fd_decode_paged).  Returns ``(out, lse)``.
+
+    q [B,H,d]; k_pages/v_pages [num_pages, H, page_size, d]; block_table
+    [B, max_pages] int32; seqlens [B] int32 (required).
+    """
+    _need_cuda(q, k_pages, v_pages, block_table, seqlens)
+    if q.dtype not in DTYPE_CODE or k_pages.dtype != q.dtype or v_pages.dtype != q.dtype:
+        raise ValueError("q, K, V must share one dtype among float32/float16/bfloat16")
+    if k_pages.dim() != 4 or v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages/v_pages must be [num_pages, H, page_size, d]")
+    num_pages, H, page_size, d = k_pages.shape
+    B = q.shape[0]
+    if q.shape != (B, H, d):
+        raise ValueError("q must be [B,H,d] with H, d of the pages")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be int32 [B, max_pages]")
+    if seqlens.dtype != torch.int32 or seqlens.shape != (B,):
+        raise ValueError("seqlens must be an int32 tensor of shape [B]")
+    max_pages = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, H, d), dtype=odt, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    _need_cuda(out, lse)
+    lib = load()
+    need = lib.fd_workspace_size(B, H, max_pages * page_size, d, int(num_splits))
+    if workspace is None:
+        workspace = _cached_workspace(q.device, need)
+    st = lib.fd_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seqlens),
+                             B, H, d, page_size, max_pages, num_pages, DTYPE_CODE[q.dtype],
+                             int(num_splits), float(scale), _ptr(out), DTYPE_CODE[out.dtype],
+                             _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream(q, stream))
+    _check(st, "fd_decode_paged")
     return out, lse
 
 

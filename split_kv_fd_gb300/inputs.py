@@ -93,3 +93,34 @@ def random_case(B, H, N, d, dtype="bf16", lens=None, seed=0, device="cpu",
                 k[b, :, n:, :] = float("nan")
                 v[b, :, n:, :] = float("nan")
     return q, k, v, lt
+
+
+def to_paged(k: torch.Tensor, v: torch.Tensor, page_size: int, seed: int = 0,
+             extra_pages: int = 3):
+    """Lay a contiguous [B,H,N,d] cache out as pages [num_pages, H, page_size, d]
+    in a seeded random page order, with the block table [B, ceil(N/page_size)].
+
+    Every page that holds no token and every row past N is NaN.  This only
+    moves numbers (no arithmetic of the method).
+    """
+    B, H, N, d = k.shape
+    maxp = -(-N // page_size)
+    npad = maxp * page_size
+    num_pages = B * maxp + extra_pages
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)[: B * maxp].to(k.device)
+    table = perm.view(B, maxp).to(torch.int32).contiguous()
+
+    def scatter(x):
+        if npad != N:
+            x = torch.cat([x, torch.full((B, H, npad - N, d), float("nan"), dtype=x.dtype,
+                                         device=x.device)], dim=2)
+        pages = torch.full((num_pages, H, page_size, d), float("nan"), dtype=x.dtype,
+                           device=x.device)
+        src = x.view(B, H, maxp, page_size, d).permute(0, 2, 1, 3, 4).reshape(B * maxp, H,
+                                                                             page_size, d)
+        pages[perm] = src
+        return pages
+
+    return scatter(k), scatter(v), table
