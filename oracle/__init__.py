@@ -28,7 +28,7 @@ _SRC = os.path.join(_HERE, "fd_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libfd_oracle.so")
 
-DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
 
 _lock = threading.Lock()
 _lib = None
@@ -74,6 +74,8 @@ def _load():
         lib.or_tile_incremental.restype = None
         lib.or_attention_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, I64, I, D, P, P, I]
         lib.or_attention_paged.restype = I
+        lib.or_attention_fp8.argtypes = [P, I, P, P, P, P, P, I, I, I, I, D, P, P, I]
+        lib.or_attention_fp8.restype = I
         lib.or_decode.argtypes = [I, P, P, I64]
         lib.or_decode.restype = None
         lib.or_f16_to_double.argtypes = [ctypes.c_uint16]
@@ -196,6 +198,55 @@ def attention_paged(q, k_pages, v_pages, block_table, lens, scale=None, dtype=No
     if rc != 0:
         raise RuntimeError("or_attention_paged failed (bad arguments or block-table entry)")
     return out, lse
+
+
+def _e4m3_bits(x):
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().contiguous()
+        if x.dtype == torch.float8_e4m3fn:
+            x = x.view(torch.uint8)
+        return np.ascontiguousarray(x.numpy().astype(np.uint8, copy=False))
+    return np.ascontiguousarray(np.asarray(x, dtype=np.uint8))
+
+
+def attention_fp8(q, k, v, k_scale, v_scale, lens=None, scale=None, nthreads=None):
+    """Full attention over an E4M3 KV cache with per-(b,h) scales, in float64.
+
+    k, v: [B,H,N,d] E4M3 bytes (uint8 arrays or torch float8_e4m3fn / uint8
+    tensors); k_scale, v_scale: [B,H] float32; the value of an element is
+    scale[b,h] * e4m3(byte).  q: float32 / float16 / bfloat16 [B,H,d].
+    Returns ``(out, lse)``.
+    """
+    lib = _load()
+    qb, dq = as_bits(q)
+    kb, vb = _e4m3_bits(k), _e4m3_bits(v)
+    B, H, N, d = kb.shape
+    if qb.shape != (B, H, d) or vb.shape != kb.shape:
+        raise ValueError("shapes")
+    ks = _f32_arr(k_scale).reshape(B * H)
+    vs = _f32_arr(v_scale).reshape(B * H)
+    lb = None
+    if lens is not None:
+        if hasattr(lens, "detach"):
+            lens = lens.detach().cpu().numpy()
+        lb = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.empty((B, H, d), np.float64)
+    lse = np.empty((B, H), np.float64)
+    rc = lib.or_attention_fp8(_ptr(qb), DTYPE_CODES[dq], _ptr(kb), _ptr(vb), _ptr(ks), _ptr(vs),
+                              _ptr(lb), B, H, N, d, float(scale), _ptr(out), _ptr(lse),
+                              int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("or_attention_fp8 failed")
+    return out, lse
+
+
+def _f32_arr(x):
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
 
 
 def split_partials(q, k, v, P, lens=None, scale=None, dtype=None, nthreads=None):

@@ -41,7 +41,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3 };
 
 /* ------------------------------------------------------------------ */
 /* element decoders                                                    */
@@ -74,8 +74,28 @@ double or_bf16_to_double(uint16_t h)
     return (double)f;
 }
 
+/* OCP 8-bit floating point E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits
+ * (bias 7), 3 mantissa bits, no infinities; S.1111.111 is NaN.  exponent 0
+ * => subnormal mantissa * 2^-9; otherwise (8 + mantissa) * 2^(exponent - 10). */
+double or_e4m3_to_double(uint8_t x)
+{
+    int sign = (x >> 7) & 1;
+    int e = (x >> 3) & 0xf;
+    int m = x & 0x7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(8 + m), e - 10);
+    return sign ? -v : v;
+}
+
 static double load_elem(const void *base, size_t idx, int dtype)
 {
+    if (dtype == OR_E4M3)
+        return or_e4m3_to_double(((const uint8_t *)base)[idx]);
     if (dtype == OR_F32) {
         float f;
         memcpy(&f, (const char *)base + idx * 4, 4);
@@ -101,6 +121,8 @@ typedef struct {
     const void *q, *k, *v;
     const int32_t *lens;
     int B, H, N, d, dtype, P;
+    int kvdtype;                       /* element type of K and V            */
+    const float *k_scale, *v_scale;    /* per-(b,h) dequantisation, or NULL  */
     double scale;
     double *out, *lse;                       /* full attention          */
     double *o_part, *m_part, *l_part, *s_part; /* per-split partials     */
@@ -170,14 +192,22 @@ static int seq_len(const job_t *j, int b)
     return n;
 }
 
+/* a K or V element: the stored value, times its (b,h) scale when one is given */
+static double kv_elem(const job_t *j, const void *base, size_t idx, const float *sc, size_t bh)
+{
+    double x = load_elem(base, idx, j->kvdtype);
+    return sc ? (double)sc[bh] * x : x;
+}
+
 /* score s_j = scale * sum_i q_i K_{j,i}   ([FDD] §2.2, [LSE] §2.1.1) */
 static double score(const job_t *j, int b, int h, int t)
 {
-    size_t qb = ((size_t)b * j->H + h) * j->d;
-    size_t kb = (((size_t)b * j->H + h) * j->N + t) * j->d;
+    size_t bh = (size_t)b * j->H + h;
+    size_t qb = bh * j->d;
+    size_t kb = (bh * j->N + t) * j->d;
     double acc = 0.0;
     for (int i = 0; i < j->d; ++i)
-        acc += load_elem(j->q, qb + i, j->dtype) * load_elem(j->k, kb + i, j->dtype);
+        acc += load_elem(j->q, qb + i, j->dtype) * kv_elem(j, j->k, kb + i, j->k_scale, bh);
     return j->scale * acc;
 }
 
@@ -205,12 +235,13 @@ static double direct_range(const job_t *j, int b, int h, int lo, int hi,
             m = s_scratch[t - lo];
     }
     double l = 0.0;
-    size_t vb = (((size_t)b * j->H + h) * j->N) * d;
+    size_t bh = (size_t)b * j->H + h;
+    size_t vb = (bh * j->N) * d;
     for (int t = lo; t < hi; ++t) {
         double w = exp(s_scratch[t - lo] - m);
         l += w;
         for (int i = 0; i < d; ++i)
-            o[i] += w * load_elem(j->v, vb + (size_t)t * d + i, j->dtype);
+            o[i] += w * kv_elem(j, j->v, vb + (size_t)t * d + i, j->v_scale, bh);
     }
     for (int i = 0; i < d; ++i)
         o[i] /= l;
@@ -246,7 +277,31 @@ int or_attention(const void *q, const void *k, const void *v, const int32_t *len
     job_t j;
     memset(&j, 0, sizeof j);
     j.q = q; j.k = k; j.v = v; j.lens = lens;
-    j.B = B; j.H = H; j.N = N; j.d = d; j.dtype = dtype;
+    j.B = B; j.H = H; j.N = N; j.d = d; j.dtype = dtype; j.kvdtype = dtype;
+    j.scale = scale; j.out = out; j.lse = lse;
+    return run_pairs(&j, attention_pair, nthreads);
+}
+
+/*
+ * Full attention over an FP8 (E4M3) KV cache with per-(b,h) scales: the
+ * value of K[b,h,t,i] is k_scale[b*H+h] * e4m3(k[b,h,t,i]), likewise V.  The
+ * low-precision storage is the "FP8 support" of [FA1P] §6.2 applied to the
+ * cache; the attention is exactly or_attention's on those values.  q is
+ * f32 / f16 / bf16 (q_dtype).
+ */
+int or_attention_fp8(const void *q, int q_dtype, const void *k, const void *v,
+                     const float *k_scale, const float *v_scale, const int32_t *lens,
+                     int B, int H, int N, int d, double scale, double *out, double *lse,
+                     int nthreads)
+{
+    if (B < 0 || H < 0 || N < 0 || d <= 0 || q_dtype < 0 || q_dtype > 2 || !out ||
+        !k_scale || !v_scale)
+        return -1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.q = q; j.k = k; j.v = v; j.lens = lens;
+    j.B = B; j.H = H; j.N = N; j.d = d; j.dtype = q_dtype; j.kvdtype = OR_E4M3;
+    j.k_scale = k_scale; j.v_scale = v_scale;
     j.scale = scale; j.out = out; j.lse = lse;
     return run_pairs(&j, attention_pair, nthreads);
 }
@@ -289,7 +344,7 @@ int or_split_partials(const void *q, const void *k, const void *v, const int32_t
     job_t j;
     memset(&j, 0, sizeof j);
     j.q = q; j.k = k; j.v = v; j.lens = lens;
-    j.B = B; j.H = H; j.N = N; j.d = d; j.dtype = dtype; j.P = P;
+    j.B = B; j.H = H; j.N = N; j.d = d; j.dtype = dtype; j.kvdtype = dtype; j.P = P;
     j.scale = scale;
     j.o_part = o_part; j.m_part = m_part; j.l_part = l_part; j.s_part = s_part;
     return run_pairs(&j, split_pair, nthreads);

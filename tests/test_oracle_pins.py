@@ -419,3 +419,64 @@ def test_paged_oracle_rejects_bad_table_entries():
     # an entry past the sequence's last page is never used
     out, _ = oracle.attention_paged(q, Kp, Kp, np.array([[1, 99]], np.int32), [4])
     assert np.all(out == 0)
+
+
+# ------------------------------------------------------------ FP8 (E4M3) KV cache
+
+def test_e4m3_decoder_exhaustive_vs_torch():
+    bits = np.arange(256, dtype=np.uint8)
+    ours = oracle.decode_elements(bits, "e4m3")
+    ref = torch.from_numpy(bits.copy()).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # S.1111.111 only
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+def _fp8_case(rng, B=2, H=3, N=40, d=16, pow2=True):
+    q = _f32(rng.normal(size=(B, H, d)))
+    kb = rng.integers(0, 256, size=(B, H, N, d), dtype=np.uint8)
+    vb = rng.integers(0, 256, size=(B, H, N, d), dtype=np.uint8)
+    # keep the draws finite and moderate: no NaN codes, exponents <= 9
+    kb[(kb & 0x7F) >= 0x50] &= 0xC7
+    vb[(vb & 0x7F) >= 0x50] &= 0xC7
+    if pow2:
+        ks = (2.0 ** rng.integers(-6, -2, size=(B, H))).astype(np.float32)
+        vs = (2.0 ** rng.integers(-3, 2, size=(B, H))).astype(np.float32)
+    else:
+        ks = rng.uniform(0.01, 0.2, size=(B, H)).astype(np.float32)
+        vs = rng.uniform(0.1, 3.0, size=(B, H)).astype(np.float32)
+    return q, kb, vb, ks, vs
+
+
+def test_fp8_oracle_equals_contiguous_on_exact_dequantised_values():
+    rng = np.random.default_rng(2)
+    q, kb, vb, ks, vs = _fp8_case(rng)
+    lens = np.array([40, 17], np.int32)
+    K = (oracle.decode_elements(kb, "e4m3") * ks[:, :, None, None]).astype(np.float32)
+    V = (oracle.decode_elements(vb, "e4m3") * vs[:, :, None, None]).astype(np.float32)
+    # power-of-two scales: every dequantised value is exact in float32
+    assert np.array_equal(K.astype(np.float64), oracle.decode_elements(kb, "e4m3") * ks[:, :, None, None])
+    out, lse = oracle.attention(q, K, V, lens=lens)
+    fout, flse = oracle.attention_fp8(q, kb, vb, ks, vs, lens=lens)
+    assert np.array_equal(fout, out) and np.array_equal(flse, lse)
+
+
+def test_fp8_oracle_against_numpy_float64():
+    sp = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(4)
+    q, kb, vb, ks, vs = _fp8_case(rng, pow2=False)
+    lens = np.array([40, 29], np.int32)
+    fout, flse = oracle.attention_fp8(q, kb, vb, ks, vs, lens=lens)
+    Kd = oracle.decode_elements(kb, "e4m3") * ks[:, :, None, None].astype(np.float64)
+    Vd = oracle.decode_elements(vb, "e4m3") * vs[:, :, None, None].astype(np.float64)
+    for b in range(2):
+        for h in range(3):
+            n = lens[b]
+            s = Kd[b, h, :n] @ q[b, h].astype(np.float64) / np.sqrt(q.shape[-1])
+            assert np.allclose(fout[b, h], sp.softmax(s) @ Vd[b, h, :n], atol=1e-13, rtol=0)
+            assert abs(flse[b, h] - sp.logsumexp(s)) < 1e-12
+    # out is linear in v_scale: doubling it doubles out exactly
+    fout2, flse2 = oracle.attention_fp8(q, kb, vb, ks, vs * 2, lens=lens)
+    assert np.array_equal(fout2, 2 * fout) and np.array_equal(flse2, flse)
