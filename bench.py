@@ -45,7 +45,7 @@ METRIC = "split-KV decode attention KV-GB/s and % of GB300 HBM peak (~8 TB/s), 1
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["fd_split.cuh", "fd_device.cuh", "fd_internal.h", "fd_split_bf16.cu",
-                  "fd_split_f16.cu", "fd_split_f32.cu"]
+                  "fd_split_f16.cu", "fd_split_f32.cu", "fd_split_fp8.cu"]
 
 
 # ----------------------------------------------------------------- helpers
@@ -258,7 +258,7 @@ def run_reference(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, "auto", args.page_size),
+        "config": config_of(w, "auto", args.page_size, args.kv_dtype),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {rows} of {w.B * w.H} (b,h) rows of {w.name}, "
                                    f"full length, drawn on the host with the workload's "
@@ -269,9 +269,11 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w, num_splits, page_size=0):
+def config_of(w, num_splits, page_size=0, kv_dtype="native"):
     return {"workload": w.name, "batch": w.B, "heads": w.H, "kv_len": w.N, "head_dim": w.d,
-            "kv_dtype": w.dtype, "out_dtype": w.out_dtype, "num_splits": num_splits,
+            "kv_dtype": (w.dtype if kv_dtype == "native"
+                         else f"e4m3 with per-(b,h) scales (q {w.dtype})"),
+            "out_dtype": w.out_dtype, "num_splits": num_splits,
             "kv_layout": (f"paged, {page_size}-token pages in shuffled order" if page_size
                           else "contiguous [B,H,N,d]"),
             "lengths": "uniform[1,N] seeded" if w.ragged else "all N",
@@ -297,13 +299,22 @@ def run_ours(args, w):
     q, k, v, lens = make_inputs(w, device=dev)
     lens_h = lens.cpu().tolist()
     table = None
+    k_scale = v_scale = None
+    if args.kv_dtype == "e4m3":
+        from split_kv_fd_gb300.inputs import quantize_e4m3
+        k, k_scale = quantize_e4m3(k)
+        v, v_scale = quantize_e4m3(v)
+        torch.cuda.empty_cache()
     if args.page_size:
         from split_kv_fd_gb300.inputs import to_paged
         k, v, table = to_paged(k, v, args.page_size, seed=w.seed)
         torch.cuda.empty_cache()
 
     def decode(out, lse, stream):
-        if table is None:
+        if k_scale is not None:
+            fd.decode_fp8(q, k, v, k_scale, v_scale, seqlens=lens, num_splits=0, scale=w.scale,
+                          out=out, lse=lse, workspace=wsbuf, stream=stream)
+        elif table is None:
             fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
                       workspace=wsbuf, stream=stream)
         else:
@@ -364,10 +375,14 @@ def run_ours(args, w):
     kern_ms = statistics.mean(launch_ms)
 
     kvb = kv_bytes(w, lens_h)
+    if k_scale is not None:  # one byte per element, plus the scales
+        kvb = kvb // ELEMENT_BYTES[w.dtype]
     ms_per_step = total_ms / args.steps
     value = ws * kvb / (ms_per_step * 1e-3) / 1e9
     peaks, peak_src = measured_peaks()
     alg = algorithmic_bytes(w, lens_h)
+    if k_scale is not None:
+        alg = alg - kv_bytes(w, lens_h) + kvb + 8 * w.B * w.H
     if table is not None:  # the block-table entries the kernel reads
         alg += 4 * sum(-(-int(n) // args.page_size) for n in lens_h) * w.H
     achieved = alg / (kern_ms * 1e-3) / 1e9
@@ -381,6 +396,8 @@ def run_ours(args, w):
         hv = v.cpu().pin_memory()
         hl = lens.cpu().pin_memory()
         ht = table.cpu().pin_memory() if table is not None else None
+        hks = k_scale.cpu().pin_memory() if k_scale is not None else None
+        hvs = v_scale.cpu().pin_memory() if v_scale is not None else None
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
@@ -392,6 +409,9 @@ def run_ours(args, w):
             lens.copy_(hl, non_blocking=True)
             if table is not None:
                 table.copy_(ht, non_blocking=True)
+            if k_scale is not None:
+                k_scale.copy_(hks, non_blocking=True)
+                v_scale.copy_(hvs, non_blocking=True)
             decode(out, lse, stream)
             hout.copy_(out, non_blocking=True)
             hlse.copy_(lse, non_blocking=True)
@@ -407,7 +427,8 @@ def run_ours(args, w):
         b.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = reduce_max(a.elapsed_time(b), ws, dev) / e2e_steps
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl, ht) if t is not None)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl, ht, hks, hvs)
+                  if t is not None)
         d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
         e2e = {"value": ws * kvb / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e_ms}
@@ -415,20 +436,25 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, q, k, v, lens)
+        if table is None and k_scale is None:
+            cpu = cpu_baseline(w, q, k, v, lens)
+        else:  # the oracle on host-drawn rows of the same workload in its native dtype
+            cpu = cpu_baseline(w, None, None, None, None)
+            cpu["sample"] += " (native-dtype contiguous rows drawn on the host)"
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": config_of(w, "auto", args.page_size),
+            "config": config_of(w, "auto", args.page_size, args.kv_dtype),
             "tokens_per_s": ws * tokens / (ms_per_step * 1e-3),
             "pct_of_nominal_8tbs": 100.0 * value / ws / NOMINAL_HBM_GBS,
             "pct_of_measured_hbm": 100.0 * value / ws / peaks["hbm_gbs"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": None if table is not None else profiled_traffic(w.name),
+                         "traffic": (None if table is not None or k_scale is not None
+                                     else profiled_traffic(w.name)),
                          "kernel": "split_kernel",
                          "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                          "algorithmic_bytes_per_launch": alg, "mean_launch_ms": kern_ms},
@@ -452,6 +478,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=BENCH_DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--kv-dtype", choices=["native", "e4m3"], default="native",
+                    help="e4m3: store K/V in FP8 with per-(b,h) scales and time fd_decode_fp8")
     ap.add_argument("--page-size", type=int, default=0,
                     help="time fd_decode_paged on the workload laid out in pages of this many tokens")
     ap.add_argument("--no-e2e", action="store_true")

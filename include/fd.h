@@ -47,7 +47,9 @@
 extern "C" {
 #endif
 
-typedef enum { FD_F32 = 0, FD_F16 = 1, FD_BF16 = 2 } fd_dtype;
+/* FD_E4M3 (OCP FP8 E4M3, one byte) is a KV-cache element type for
+ * fd_decode_fp8 only. */
+typedef enum { FD_F32 = 0, FD_F16 = 1, FD_BF16 = 2, FD_E4M3 = 3 } fd_dtype;
 
 typedef enum {
     FD_OK = 0,
@@ -134,6 +136,26 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
                           int page_size, int max_pages, long long num_pages, fd_dtype in_dtype,
                           int num_splits, float scale, void *out, fd_dtype out_dtype, float *lse,
                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * fd_decode over an FP8 KV cache: K and V hold OCP E4M3 bytes with one
+ * float32 dequantisation scale per (b, h); the value of K[b,h,t,i] is
+ * k_scale[b*H+h] * e4m3(k[b,h,t,i]), likewise V.  Storing the cache in FP8
+ * is the "FP8 support" of "从第一性原理推导 Flash Attention" §6.2 applied to
+ * the decode cache: half the bytes per token, so about twice the tokens per
+ * second at the same HBM bandwidth.  The attention itself is fd_decode's,
+ * in float32.
+ *   q          [B, H, d] in q_dtype (f32, f16 or bf16)
+ *   k, v       [B, H, N, d] E4M3 bytes (16-byte aligned)
+ *   k_scale, v_scale  [B, H] float32
+ * All other arguments as in fd_decode; the workspace size is
+ * fd_workspace_size(B, H, N, d, num_splits).
+ */
+fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,
+                        const float *k_scale, const float *v_scale, const int32_t *seqlens,
+                        int B, int H, int N, int d, int num_splits, float scale, void *out,
+                        fd_dtype out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                        void *stream);
 
 /*
  * Stage 1 alone: per-split partials for num_splits >= 1 splits of every

@@ -107,6 +107,9 @@ bool sizes_ok(int B, int H, int N, int d)
 
 size_t split_smem(int dtype, int d, int decomp, int B)
 {
+    if (dtype == FD_E4M3)
+        return d == 64 ? SplitCfg<__nv_fp8_e4m3, 64>::smem_bytes(decomp, B)
+                       : SplitCfg<__nv_fp8_e4m3, 128>::smem_bytes(decomp, B);
     if (dtype == FD_F32)
         return d == 64 ? SplitCfg<float, 64>::smem_bytes(decomp, B) : SplitCfg<float, 128>::smem_bytes(decomp, B);
     if (dtype == FD_F16)
@@ -121,6 +124,8 @@ fd_status launch(int dtype, int d, const SplitParams &p, int decomp, cudaStream_
     cudaError_t e;
     if (dtype == FD_F32)
         e = launch_split_f32(d, p, smem, s);
+    else if (dtype == FD_E4M3)
+        e = launch_split_fp8(d, p, smem, s);
     else if (dtype == FD_F16)
         e = launch_split_f16(d, p, smem, s);
     else
@@ -223,6 +228,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
     p.H = H;
     p.N = N;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.q_dtype = in_dtype;
     p.decomp = pl.decomp;
     p.P = pl.P;
     p.grid = pl.grid;
@@ -274,6 +280,7 @@ fd_status fd_decode_split(const void *q, const void *k, const void *v, const int
     p.H = H;
     p.N = N;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.q_dtype = in_dtype;
     p.decomp = DECOMP_SPLITS;
     p.P = num_splits;
     p.grid = (int)(items < ctas ? items : ctas);
@@ -347,6 +354,62 @@ fd_status fd_device_status(int reset)
     return (v & STATUS_BAD_PAGE) ? FD_ERR_BAD_PAGE : FD_OK;
 }
 
+fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,
+                        const float *k_scale, const float *v_scale, const int32_t *seqlens, int B,
+                        int H, int N, int d, int num_splits, float scale, void *out,
+                        fd_dtype out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    if (!sizes_ok(B, H, N, d) || num_splits < 0 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0)
+        return FD_OK;
+    if (!q || (N > 0 && (!k || !v)) || !k_scale || !v_scale || !out || !aligned(q, 16) ||
+        !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(k_scale, 4) ||
+        !aligned(v_scale, 4) || (seqlens && !aligned(seqlens, 4)) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    unsigned *st = status_ptr();
+    if (sms <= 0 || !st)
+        return FD_ERR_CUDA;
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    const WsLayout wl = ws_layout(pl.slots, d, (long long)B * H);
+    if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
+        return FD_ERR_WORKSPACE;
+
+    SplitParams p = {};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.lens = seqlens;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.q_dtype = q_dtype;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.decomp = pl.decomp;
+    p.P = pl.P;
+    p.grid = pl.grid;
+    p.out_kind = OUT_FUSED;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.lse = lse;
+    char *ws = static_cast<char *>(workspace);
+    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
+    p.status = st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
+    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * H * sizeof(unsigned), cs) != cudaSuccess)
+        return FD_ERR_CUDA;
+    return launch(FD_E4M3, d, p, pl.decomp, cs);
+}
+
 fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_pages,
                           const int32_t *block_table, const int32_t *seqlens, int B, int H, int d,
                           int page_size, int max_pages, long long num_pages, fd_dtype in_dtype,
@@ -391,6 +454,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     p.max_pages = max_pages;
     p.num_pages = num_pages;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.q_dtype = in_dtype;
     p.decomp = pl.decomp;
     p.P = pl.P;
     p.grid = pl.grid;
@@ -489,6 +553,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     p.H = H;
     p.N = N;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.q_dtype = in_dtype;
     p.decomp = pl.decomp;
     p.P = pl.P;
     p.grid = pl.grid;

@@ -5,6 +5,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace fd {
@@ -205,6 +206,70 @@ template <> struct Elem<__half> {
         }
     }
 };
+
+// OCP E4M3 bytes: each pair converts exactly to f16x2 (cvt.rn.f16x2.e4m3x2,
+// lower byte to the lower half), then to float32.
+template <> struct Elem<__nv_fp8_e4m3> {
+    static constexpr int VEC = 16;
+    __device__ __forceinline__ static void widen(const uint4 &u, float *f)
+    {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t h01, h23;
+            asm("{\n\t.reg .b16 lo, hi;\n\t"
+                "mov.b32 {lo, hi}, %2;\n\t"
+                "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+                "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+                : "=r"(h01), "=r"(h23)
+                : "r"(w[i]));
+            __half2 a, b;
+            memcpy(&a, &h01, 4);
+            memcpy(&b, &h23, 4);
+            const float2 fa = __half22float2(a), fb = __half22float2(b);
+            f[4 * i] = fa.x;
+            f[4 * i + 1] = fa.y;
+            f[4 * i + 2] = fb.x;
+            f[4 * i + 3] = fb.y;
+        }
+    }
+};
+
+// VEC elements of q starting at element `off`, widened to float32; q is
+// float32 (q_dtype 0), float16 (1) or bfloat16 (2) and 16-byte aligned.
+template <int VEC>
+__device__ __forceinline__ void load_q(const void *q, int q_dtype, long long off, float *qf)
+{
+    if (q_dtype == 0) {
+        const float4 *p4 = reinterpret_cast<const float4 *>(static_cast<const float *>(q) + off);
+#pragma unroll
+        for (int i = 0; i < VEC / 4; ++i) {
+            const float4 x = __ldg(p4 + i);
+            qf[4 * i] = x.x;
+            qf[4 * i + 1] = x.y;
+            qf[4 * i + 2] = x.z;
+            qf[4 * i + 3] = x.w;
+        }
+    } else if (VEC % 8 == 0) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(q) + off);
+#pragma unroll
+        for (int i = 0; i < VEC / 8; ++i) {
+            const uint4 u = __ldg(p + i);
+            if (q_dtype == 1)
+                Elem<__half>::widen(u, qf + 8 * i);
+            else
+                Elem<__nv_bfloat16>::widen(u, qf + 8 * i);
+        }
+    } else {
+        const uint16_t *p = static_cast<const uint16_t *>(q) + off;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const uint16_t h = __ldg(p + i);
+            qf[i] = q_dtype == 1 ? __half2float(__ushort_as_half(h))
+                                 : __uint_as_float(((uint32_t)h) << 16);
+        }
+    }
+}
 
 // Store one float as the requested output dtype (round-to-nearest-even).
 __device__ __forceinline__ void store_out(void *out, long long idx, int out_dtype, float x)

@@ -36,6 +36,9 @@ struct SplitParams {
     int page_size, max_pages;
     long long num_pages;
     float scale_log2;     // scale * log2(e): scores are kept in base 2
+    int q_dtype;          // 0 f32, 1 f16, 2 bf16 (K/V: the kernel's element type)
+    const float *k_scale; // [B*H] K dequantisation scales, or null (1)
+    const float *v_scale; // [B*H] V dequantisation scales, or null (1)
     int decomp;
     int P;                // splits per sequence for DECOMP_SPLITS
     int grid;             // number of CTAs launched (G)
@@ -84,6 +87,7 @@ cudaError_t launch_split(int dtype, int d, const SplitParams &p, cudaStream_t s)
 cudaError_t launch_split_f32(int d, const SplitParams &p, size_t smem, cudaStream_t s);
 cudaError_t launch_split_f16(int d, const SplitParams &p, size_t smem, cudaStream_t s);
 cudaError_t launch_split_bf16(int d, const SplitParams &p, size_t smem, cudaStream_t s);
+cudaError_t launch_split_fp8(int d, const SplitParams &p, size_t smem, cudaStream_t s);
 
 cudaError_t launch_combine_mlo(const CombineParams &p, cudaStream_t s);
 cudaError_t launch_combine_lse(const CombineParams &p, cudaStream_t s);

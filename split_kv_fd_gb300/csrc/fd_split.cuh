@@ -648,12 +648,12 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split
         const int bh = cs.b * p.H + cs.h;
         float qf[C::VEC];
         {
-            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
-                static_cast<const char *>(p.q) + ((long long)bh * D) * C::ESZ + col * 16));
-            Elem<T>::widen(u, qf);
+            load_q<C::VEC>(p.q, p.q_dtype, (long long)bh * D + col * C::VEC, qf);
+            // score scale, base-2 exponentials, and K's dequantisation scale
+            const float qs = p.scale_log2 * (p.k_scale ? __ldg(p.k_scale + bh) : 1.f);
 #pragma unroll
             for (int i = 0; i < C::VEC; ++i)
-                qf[i] *= p.scale_log2;
+                qf[i] *= qs;
         }
         float m = -INFINITY, l = 0.f, acc[C::VEC];
 #pragma unroll
@@ -746,7 +746,9 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split
                 }
             }
             const bool nonempty = L > 0.f;
-            const float o = nonempty ? O / L : 0.f;
+            // V's dequantisation scale is common to every row of (b, h)
+            const float vs = p.v_scale ? __ldg(p.v_scale + bh) : 1.f;
+            const float o = nonempty ? O / L * vs : 0.f;
             if (p.out_kind == OUT_PARTIALS) {
                 p.o_part[slot * D + tid] = o;
                 if (tid == 0) {

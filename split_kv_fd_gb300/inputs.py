@@ -124,3 +124,25 @@ def to_paged(k: torch.Tensor, v: torch.Tensor, page_size: int, seed: int = 0,
         return pages
 
     return scatter(k), scatter(v), table
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-(b,h) symmetric E4M3 storage of a [B,H,N,d] cache (input
+    preparation for the FP8 path, not part of the attention): scale = amax /
+    448 over the finite rows of (b, h) (1 if there are none), bytes = E4M3
+    round-to-nearest-even of x / scale.  NaN rows (past a sequence's length)
+    stay NaN.  Returns ``(x_e4m3 [B,H,N,d] float8_e4m3fn, scale [B,H] float32)``.
+    """
+    B, H, N, d = x.shape
+    out = torch.empty((B, H, N, d), dtype=torch.float8_e4m3fn, device=x.device)
+    scale = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    for b in range(B):  # one sequence at a time bounds the float32 temporaries
+        xb = x[b].float()
+        amax = torch.nan_to_num(xb, nan=0.0).abs().amax(dim=(1, 2))
+        sb = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+        scale[b] = sb
+        out[b] = (xb / sb[:, None, None]).to(torch.float8_e4m3fn)
+    return out, scale

@@ -25,7 +25,7 @@ def lib():
 def _declared():
     src = open(os.path.join(ROOT, "include", "fd.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(fd_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(fd_[a-z_0-9]+)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported(lib):
