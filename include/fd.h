@@ -192,6 +192,23 @@ fd_status fd_combine_lse(const float *o_part, const float *lse_part,
                          float *lse, void *stream);
 
 /*
+ * Merge two sets of normalised partial results, row by row, with the
+ * operator (+) of "FlashDecoding 数学推导：传统 m/l/o 方法与 LSE 方法"
+ * §2.3.5, in the safe two-term form of its §3.2.1 stage 2:
+ *   S   = max(S_a, S_b) + log1p(exp(min - max)),
+ *   out = o_a exp(S_a - S) + o_b exp(S_b - S),   lse_out = S.
+ * (+) is associative, so the partials of a sequence split across several
+ * calls, streams or devices (each one fd_decode over its range of tokens,
+ * with float32 out and lse) fold to the unsplit result in any order or tree.
+ * A row with S = -inf on one side takes the other side unchanged.
+ *   o_a, o_b, o_out      [rows, d] float32, 16-byte aligned, d % 4 == 0
+ *   lse_a, lse_b, lse_out [rows] float32 (natural log)
+ * The outputs may alias either input.
+ */
+fd_status fd_merge_lse(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                       int rows, int d, float *o_out, float *lse_out, void *stream);
+
+/*
  * Reads (and if `reset` is non-zero, clears) the current device's status
  * word, which a kernel sets when it gives up waiting on its own copies or
  * meets a block-table entry that names no page.  Synchronises the device.

@@ -337,6 +337,23 @@ fd_status fd_combine_lse(const float *o_part, const float *lse_part, int B, int 
     return combine_common(o_part, lse_part, nullptr, true, B, H, P, d, out, out_dtype, lse, stream);
 }
 
+fd_status fd_merge_lse(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                       int rows, int d, float *o_out, float *lse_out, void *stream)
+{
+    if (rows < 0 || d <= 0 || d % 4 != 0)
+        return FD_ERR_INVALID_ARG;
+    if (rows == 0)
+        return FD_OK;
+    if (!o_a || !lse_a || !o_b || !lse_b || !o_out || !lse_out || !aligned(o_a, 16) ||
+        !aligned(o_b, 16) || !aligned(o_out, 16) || !aligned(lse_a, 4) || !aligned(lse_b, 4) ||
+        !aligned(lse_out, 4))
+        return FD_ERR_INVALID_ARG;
+    return launch_merge_lse(o_a, lse_a, o_b, lse_b, rows, d, o_out, lse_out,
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FD_OK
+               : FD_ERR_CUDA;
+}
+
 fd_status fd_device_status(int reset)
 {
     if (cudaDeviceSynchronize() != cudaSuccess)

@@ -87,6 +87,60 @@ template <bool LSE> __global__ void __launch_bounds__(COMBINE_THREADS) combine_k
         p.lse[row] = lse_g;
 }
 
+// (o_a, S_a) (+) (o_b, S_b) per row: the merge operator of "FlashDecoding
+// 数学推导：传统 m/l/o 方法与 LSE 方法" §2.3.5, evaluated in the safe form of
+// §3.2.1 stage 2: S = S_max + log1p(exp(S_min - S_max)),
+// o = o_a exp(S_a - S) + o_b exp(S_b - S).  An empty side (S = -inf) leaves
+// the other unchanged; two empty sides give (0, -inf).  One warp per row:
+// every lane reads the row's S_a, S_b before lane 0 writes S, so the outputs
+// may alias either input.
+__global__ void merge_lse_kernel(const float4 *oa, const float *sa, const float4 *ob,
+                                 const float *sb, int rows, int d4, float4 *out, float *sout)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long r = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+         r += warps) {
+        const float s1 = sa[r], s2 = sb[r];
+        float w1, w2, S;
+        if (s1 == -INFINITY && s2 == -INFINITY) {
+            w1 = w2 = 0.f;
+            S = -INFINITY;
+        } else if (s2 == -INFINITY) {
+            w1 = 1.f, w2 = 0.f, S = s1;
+        } else if (s1 == -INFINITY) {
+            w1 = 0.f, w2 = 1.f, S = s2;
+        } else {
+            const float smax = fmaxf(s1, s2), smin = fminf(s1, s2);
+            S = smax + log1pf(expf(smin - smax));
+            w1 = expf(s1 - S);
+            w2 = expf(s2 - S);
+        }
+        for (int c = lane; c < d4; c += 32) {
+            const long long i = r * d4 + c;
+            const float4 a = oa[i], b = ob[i];
+            out[i] = make_float4(a.x * w1 + b.x * w2, a.y * w1 + b.y * w2, a.z * w1 + b.z * w2,
+                                 a.w * w1 + b.w * w2);
+        }
+        __syncwarp();
+        if (lane == 0)
+            sout[r] = S;
+    }
+}
+
+cudaError_t launch_merge_lse(const float *oa, const float *sa, const float *ob, const float *sb,
+                             int rows, int d, float *out, float *sout, cudaStream_t s)
+{
+    const int threads = 256;  // 8 rows per block
+    long long blocks = ((long long)rows + 7) / 8;
+    if (blocks > 65535LL * 4)
+        blocks = 65535LL * 4;
+    merge_lse_kernel<<<(unsigned)blocks, threads, 0, s>>>(
+        reinterpret_cast<const float4 *>(oa), sa, reinterpret_cast<const float4 *>(ob), sb, rows,
+        d / 4, reinterpret_cast<float4 *>(out), sout);
+    return cudaGetLastError();
+}
+
 static cudaError_t launch_combine(const CombineParams &p, bool lse_form, cudaStream_t s)
 {
     const size_t smem = (size_t)p.P * sizeof(float);

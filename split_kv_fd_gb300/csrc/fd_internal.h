@@ -91,5 +91,7 @@ cudaError_t launch_split_fp8(int d, const SplitParams &p, size_t smem, cudaStrea
 
 cudaError_t launch_combine_mlo(const CombineParams &p, cudaStream_t s);
 cudaError_t launch_combine_lse(const CombineParams &p, cudaStream_t s);
+cudaError_t launch_merge_lse(const float *oa, const float *sa, const float *ob, const float *sb,
+                             int rows, int d, float *out, float *sout, cudaStream_t s);
 
 }  // namespace fd

@@ -28,7 +28,7 @@ DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 EXPORTS = ["fd_status_str", "fd_version", "fd_num_sms", "fd_auto_num_splits",
            "fd_workspace_size", "fd_decode", "fd_decode_split", "fd_combine_mlo",
            "fd_combine_lse", "fd_device_status", "fd_decode_noalloc", "fd_decode_paged",
-           "fd_decode_fp8"]
+           "fd_decode_fp8", "fd_merge_lse"]
 
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +81,8 @@ def load(build_if_missing: bool = False):
         lib.fd_decode_paged.restype = I
         lib.fd_decode_fp8.argtypes = [P, I, P, P, P, P, P, I, I, I, I, I, F, P, I, P, P, S, P]
         lib.fd_decode_fp8.restype = I
+        lib.fd_merge_lse.argtypes = [P, P, P, P, I, I, P, P, P]
+        lib.fd_merge_lse.restype = I
         lib.fd_device_status.argtypes = [I]
         lib.fd_device_status.restype = I
         _lib = lib
@@ -336,6 +338,31 @@ def combine_lse(o_part, lse_part, out_dtype=None, out=None, lse=None, return_lse
     st = load().fd_combine_lse(_ptr(o_part), _ptr(lse_part), B, H, P, d, _ptr(out),
                                DTYPE_CODE[out.dtype], _ptr(lse), _stream(o_part, stream))
     _check(st, "fd_combine_lse")
+    return out, lse
+
+
+def merge_lse(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
+    """(o_a, lse_a) (+) (o_b, lse_b) row by row (fd_merge_lse).  Returns ``(out, lse)``.
+
+    o_*: float32 [..., d]; lse_*: float32 [...] (same leading shape).  ``out``
+    / ``lse`` may be ``o_a`` / ``lse_a`` for an in-place fold.
+    """
+    _need_cuda(o_a, lse_a, o_b, lse_b)
+    for t in (o_a, lse_a, o_b, lse_b):
+        if t.dtype != torch.float32:
+            raise ValueError("partials must be float32")
+    if o_b.shape != o_a.shape or lse_a.shape != o_a.shape[:-1] or lse_b.shape != lse_a.shape:
+        raise ValueError("shapes: o [..., d], lse [...]")
+    d = o_a.shape[-1]
+    rows = lse_a.numel()
+    if out is None:
+        out = torch.empty_like(o_a)
+    if lse is None:
+        lse = torch.empty_like(lse_a)
+    _need_cuda(out, lse)
+    st = load().fd_merge_lse(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, d, _ptr(out),
+                             _ptr(lse), _stream(o_a, stream))
+    _check(st, "fd_merge_lse")
     return out, lse
 
 
