@@ -76,6 +76,8 @@ def _load():
         lib.or_attention_paged.restype = I
         lib.or_attention_fp8.argtypes = [P, I, P, P, P, P, P, I, I, I, I, D, P, P, I]
         lib.or_attention_fp8.restype = I
+        lib.or_attention_gqa.argtypes = [P, P, P, P, I, I, I, I, I, I, D, P, P, I]
+        lib.or_attention_gqa.restype = I
         lib.or_decode.argtypes = [I, P, P, I64]
         lib.or_decode.restype = None
         lib.or_f16_to_double.argtypes = [ctypes.c_uint16]
@@ -197,6 +199,39 @@ def attention_paged(q, k_pages, v_pages, block_table, lens, scale=None, dtype=No
                                 _ptr(lse), int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError("or_attention_paged failed (bad arguments or block-table entry)")
+    return out, lse
+
+
+def attention_gqa(q, k, v, lens=None, scale=None, dtype=None, nthreads=None):
+    """Grouped-query attention in float64 ("从第一性原理推导 Flash Attention" §8).
+
+    q [B, Hq, d]; k, v [B, Hkv, N, d] with Hq a multiple of Hkv; query head h
+    uses K/V head h // (Hq // Hkv).  Returns ``(out [B,Hq,d], lse [B,Hq])``.
+    """
+    lib = _load()
+    qb, dq = as_bits(q, dtype)
+    kb, dk = as_bits(k, dtype)
+    vb, dv = as_bits(v, dtype)
+    if not (dq == dk == dv):
+        raise TypeError("q, K and V must share one dtype")
+    B, Hkv, N, d = kb.shape
+    Hq = qb.shape[1]
+    if qb.shape != (B, Hq, d) or vb.shape != kb.shape or Hq % Hkv:
+        raise ValueError("shapes: q [B,Hq,d], K/V [B,Hkv,N,d], Hq % Hkv == 0")
+    lb = None
+    if lens is not None:
+        if hasattr(lens, "detach"):
+            lens = lens.detach().cpu().numpy()
+        lb = np.ascontiguousarray(np.asarray(lens, dtype=np.int32))
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    rc = lib.or_attention_gqa(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(lb), B, Hq, Hkv, N, d,
+                              DTYPE_CODES[dq], float(scale), _ptr(out), _ptr(lse),
+                              int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("or_attention_gqa failed")
     return out, lse
 
 

@@ -122,6 +122,7 @@ typedef struct {
     const int32_t *lens;
     int B, H, N, d, dtype, P;
     int kvdtype;                       /* element type of K and V            */
+    int G;                             /* query heads per K/V head (>= 1)    */
     const float *k_scale, *v_scale;    /* per-(b,h) dequantisation, or NULL  */
     double scale;
     double *out, *lse;                       /* full attention          */
@@ -199,15 +200,23 @@ static double kv_elem(const job_t *j, const void *base, size_t idx, const float 
     return sc ? (double)sc[bh] * x : x;
 }
 
+/* the K/V head of query head h: heads come in groups of G sharing one */
+static size_t kv_row(const job_t *j, int b, int h)
+{
+    int g = j->G > 1 ? j->G : 1;
+    return (size_t)b * (size_t)(j->H / g) + (size_t)(h / g);
+}
+
 /* score s_j = scale * sum_i q_i K_{j,i}   ([FDD] §2.2, [LSE] §2.1.1) */
 static double score(const job_t *j, int b, int h, int t)
 {
     size_t bh = (size_t)b * j->H + h;
+    size_t kvh = kv_row(j, b, h);
     size_t qb = bh * j->d;
-    size_t kb = (bh * j->N + t) * j->d;
+    size_t kb = (kvh * j->N + t) * j->d;
     double acc = 0.0;
     for (int i = 0; i < j->d; ++i)
-        acc += load_elem(j->q, qb + i, j->dtype) * kv_elem(j, j->k, kb + i, j->k_scale, bh);
+        acc += load_elem(j->q, qb + i, j->dtype) * kv_elem(j, j->k, kb + i, j->k_scale, kvh);
     return j->scale * acc;
 }
 
@@ -235,13 +244,13 @@ static double direct_range(const job_t *j, int b, int h, int lo, int hi,
             m = s_scratch[t - lo];
     }
     double l = 0.0;
-    size_t bh = (size_t)b * j->H + h;
-    size_t vb = (bh * j->N) * d;
+    size_t kvh = kv_row(j, b, h);
+    size_t vb = (kvh * j->N) * d;
     for (int t = lo; t < hi; ++t) {
         double w = exp(s_scratch[t - lo] - m);
         l += w;
         for (int i = 0; i < d; ++i)
-            o[i] += w * kv_elem(j, j->v, vb + (size_t)t * d + i, j->v_scale, bh);
+            o[i] += w * kv_elem(j, j->v, vb + (size_t)t * d + i, j->v_scale, kvh);
     }
     for (int i = 0; i < d; ++i)
         o[i] /= l;
@@ -278,6 +287,28 @@ int or_attention(const void *q, const void *k, const void *v, const int32_t *len
     memset(&j, 0, sizeof j);
     j.q = q; j.k = k; j.v = v; j.lens = lens;
     j.B = B; j.H = H; j.N = N; j.d = d; j.dtype = dtype; j.kvdtype = dtype;
+    j.scale = scale; j.out = out; j.lse = lse;
+    return run_pairs(&j, attention_pair, nthreads);
+}
+
+/*
+ * Grouped-query attention (MQA / GQA, [FA1P] §8): q [B, Hq, d] and K, V
+ * [B, Hkv, N, d] with Hq = G * Hkv; query head h attends with K/V head
+ * h / G (consecutive query heads share a K/V head).  Everything else is
+ * or_attention.  out [B, Hq, d], lse [B, Hq].
+ */
+int or_attention_gqa(const void *q, const void *k, const void *v, const int32_t *lens,
+                     int B, int Hq, int Hkv, int N, int d, int dtype, double scale,
+                     double *out, double *lse, int nthreads)
+{
+    if (B < 0 || Hq < 0 || Hkv <= 0 || Hq % Hkv != 0 || N < 0 || d <= 0 || dtype < 0 ||
+        dtype > 2 || !out)
+        return -1;
+    job_t j;
+    memset(&j, 0, sizeof j);
+    j.q = q; j.k = k; j.v = v; j.lens = lens;
+    j.B = B; j.H = Hq; j.N = N; j.d = d; j.dtype = dtype; j.kvdtype = dtype;
+    j.G = Hq / Hkv;
     j.scale = scale; j.out = out; j.lse = lse;
     return run_pairs(&j, attention_pair, nthreads);
 }

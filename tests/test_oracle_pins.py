@@ -480,3 +480,24 @@ def test_fp8_oracle_against_numpy_float64():
     # out is linear in v_scale: doubling it doubles out exactly
     fout2, flse2 = oracle.attention_fp8(q, kb, vb, ks, vs * 2, lens=lens)
     assert np.array_equal(fout2, 2 * fout) and np.array_equal(flse2, flse)
+
+
+# ------------------------------------------------------ grouped-query attention
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_gqa_oracle_equals_mha_on_repeated_kv_heads(G):
+    """GQA with group size G equals multi-head attention with each K/V head
+    repeated G times (numpy repeat), bit for bit; G = 1 is plain MHA."""
+    rng = np.random.default_rng(G)
+    B, Hkv, N, d = 2, 3, 50, 16
+    q = _f32(rng.normal(size=(B, Hkv * G, d)))
+    K = _f32(rng.normal(size=(B, Hkv, N, d)) * 2)
+    V = _f32(rng.normal(size=(B, Hkv, N, d)))
+    lens = np.array([50, 23], np.int32)
+    gout, glse = oracle.attention_gqa(q, K, V, lens=lens)
+    Kr = np.repeat(K, G, axis=1)
+    Vr = np.repeat(V, G, axis=1)
+    out, lse = oracle.attention(q, Kr, Vr, lens=lens)
+    assert np.array_equal(gout, out) and np.array_equal(glse, lse)
+    with pytest.raises(ValueError):
+        oracle.attention_gqa(q[:, :-1] if G > 1 else q, K[:, :2] if G == 1 else K, V)
