@@ -51,8 +51,8 @@ KERNEL_SOURCES = ["fd_split.cuh", "fd_device.cuh", "fd_internal.h", "fd_split_bf
 # ----------------------------------------------------------------- helpers
 
 def kv_bytes(w, lens) -> int:
-    """Valid K and V bytes of one step: 2 * H * d * elt * sum_b len_b."""
-    return 2 * w.H * w.d * ELEMENT_BYTES[w.dtype] * int(sum(int(x) for x in lens))
+    """Valid K and V bytes of one step: 2 * Hkv * d * elt * sum_b len_b."""
+    return 2 * w.kv_heads * w.d * ELEMENT_BYTES[w.dtype] * int(sum(int(x) for x in lens))
 
 
 def algorithmic_bytes(w, lens) -> int:
@@ -181,20 +181,23 @@ def barrier(ws: int):
 # ------------------------------------------------------------ oracle timing
 
 def host_sample(w, rows: int, q=None, k=None, v=None, lens=None, seed=1):
-    """``rows`` (b, h) rows of the workload as host tensors [rows, 1, ...].
+    """``rows`` (b, K/V head) rows of the workload as host tensors.
 
-    From the device tensors when given (the exact workload bytes), else drawn
-    on the CPU with the workload's distributions (same shapes per row)."""
+    Each row is one sequence with one K/V head and its G query heads:
+    q [rows, G, d], K/V [rows, 1, n, d] (G = 1 unless grouped-query).  Taken
+    from the device tensors when given (the exact workload bytes), else drawn
+    on the CPU with the workload's distributions."""
+    G = w.H // w.kv_heads
     if k is not None:
         lens_h = lens.cpu().tolist()
-        pairs = [(i // w.H % w.B, i % w.H) for i in range(rows)]
+        pairs = [(i // w.kv_heads % w.B, i % w.kv_heads) for i in range(rows)]
         n = max(lens_h[b] for b, _ in pairs)
-        qs = torch.stack([q[b, h] for b, h in pairs]).unsqueeze(1).cpu()
+        qs = torch.stack([q[b, h * G:(h + 1) * G] for b, h in pairs]).cpu()
         ks = torch.stack([k[b, h, :n] for b, h in pairs]).unsqueeze(1).cpu()
         vs = torch.stack([v[b, h, :n] for b, h in pairs]).unsqueeze(1).cpu()
         ls = torch.tensor([lens_h[b] for b, _ in pairs], dtype=torch.int32)
         return qs, ks, vs, ls
-    from split_kv_fd_gb300.inputs import random_case
+    from split_kv_fd_gb300.inputs import TORCH_DTYPES, random_case
     if w.ragged:
         g = torch.Generator().manual_seed(w.seed)
         lens_l = torch.randint(1, w.N + 1, (rows,), generator=g).tolist()
@@ -202,6 +205,9 @@ def host_sample(w, rows: int, q=None, k=None, v=None, lens=None, seed=1):
         lens_l = [w.N] * rows
     qs, ks, vs, ls = random_case(rows, 1, max(lens_l), w.d, w.dtype, lens=lens_l, seed=seed,
                                  k_scale=w.k_scale)
+    if G > 1:
+        g = torch.Generator().manual_seed(seed + 1)
+        qs = torch.randn(rows, G, w.d, generator=g).to(TORCH_DTYPES[w.dtype])
     return qs, ks, vs, ls
 
 
@@ -209,7 +215,10 @@ def time_oracle(w, sample, nthreads):
     import oracle
     qs, ks, vs, ls = sample
     t0 = time.perf_counter()
-    oracle.attention(qs, ks, vs, lens=ls, scale=w.scale, nthreads=nthreads)
+    if qs.shape[1] != ks.shape[1]:
+        oracle.attention_gqa(qs, ks, vs, lens=ls, scale=w.scale, nthreads=nthreads)
+    else:
+        oracle.attention(qs, ks, vs, lens=ls, scale=w.scale, nthreads=nthreads)
     return time.perf_counter() - t0
 
 
@@ -223,15 +232,16 @@ def cpu_baseline(w, q, k, v, lens, budget_s=8.0):
     oracle.build()
     cores = oracle.default_threads()
     rows = cores
+    total = w.B * w.kv_heads
     while True:
-        sample = host_sample(w, min(rows, w.B * w.H), q, k, v, lens)
+        sample = host_sample(w, min(rows, total), q, k, v, lens)
         dt = time_oracle(w, sample, cores)
-        if dt * 2 > budget_s or rows >= w.B * w.H:
+        if dt * 2 > budget_s or rows >= total:
             break
-        rows = min(w.B * w.H, max(rows * 2, int(rows * budget_s / max(dt, 1e-3) * 0.8)))
+        rows = min(total, max(rows * 2, int(rows * budget_s / max(dt, 1e-3) * 0.8)))
     nb = sample_bytes(w, sample[3])
     return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{sample[0].shape[0]} of {w.B * w.H} (b,h) rows of {w.name}, full length "
+            "sample": f"{sample[0].shape[0]} of {total} (b, kv head) rows of {w.name}, full length "
                       f"({int(sample[3].sum())} tokens), float64 C oracle, {cores} threads, "
                       f"{dt:.2f} s wall"}
 
@@ -245,7 +255,7 @@ def run_reference(args, w):
     import oracle
     oracle.build()
     cores = oracle.default_threads()
-    rows = max(1, min(cores, w.B * w.H))
+    rows = max(1, min(cores, w.B * w.kv_heads))
     sample = host_sample(w, rows)
     for _ in range(args.warmup):
         time_oracle(w, sample, cores)
@@ -260,7 +270,7 @@ def run_reference(args, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, "auto", args.page_size, args.kv_dtype),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"each step: {rows} of {w.B * w.H} (b,h) rows of {w.name}, "
+                         "sample": f"each step: {rows} of {w.B * w.kv_heads} (b, kv head) rows of {w.name}, "
                                    f"full length, drawn on the host with the workload's "
                                    f"distributions; float64 C oracle, {cores} threads"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -270,7 +280,8 @@ def run_reference(args, w):
 
 
 def config_of(w, num_splits, page_size=0, kv_dtype="native"):
-    return {"workload": w.name, "batch": w.B, "heads": w.H, "kv_len": w.N, "head_dim": w.d,
+    return {"workload": w.name, "batch": w.B, "heads": w.H, "kv_heads": w.kv_heads,
+            "kv_len": w.N, "head_dim": w.d,
             "kv_dtype": (w.dtype if kv_dtype == "native"
                          else f"e4m3 with per-(b,h) scales (q {w.dtype})"),
             "out_dtype": w.out_dtype, "num_splits": num_splits,
@@ -279,7 +290,7 @@ def config_of(w, num_splits, page_size=0, kv_dtype="native"):
             "lengths": "uniform[1,N] seeded" if w.ragged else "all N",
             "k_scale": w.k_scale,
             "l2": ("inputs larger than L2, no flush"
-                   if 2 * w.B * w.H * w.N * w.d * ELEMENT_BYTES[w.dtype] > 4 * L2_BYTES
+                   if 2 * w.B * w.kv_heads * w.N * w.d * ELEMENT_BYTES[w.dtype] > 4 * L2_BYTES
                    else "L2 flushed before every step (256 MiB write, then 256 MiB read)")}
 
 
@@ -311,7 +322,10 @@ def run_ours(args, w):
         torch.cuda.empty_cache()
 
     def decode(out, lse, stream):
-        if k_scale is not None:
+        if w.kv_heads != w.H:
+            fd.decode_gqa(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
+                          workspace=wsbuf, stream=stream)
+        elif k_scale is not None:
             fd.decode_fp8(q, k, v, k_scale, v_scale, seqlens=lens, num_splits=0, scale=w.scale,
                           out=out, lse=lse, workspace=wsbuf, stream=stream)
         elif table is None:
@@ -324,10 +338,14 @@ def run_ours(args, w):
                                                             "f32": "float32"}[w.out_dtype]),
                       device=dev)
     lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
-    wsbuf = fd.new_workspace(w.B, w.H, w.N, w.d, 0, device=dev)
+    if w.kv_heads != w.H:
+        wsbuf = torch.empty(max(256, fd.workspace_size_gqa(w.B, w.H, w.kv_heads, w.N, w.d, 0)),
+                            dtype=torch.uint8, device=dev)
+    else:
+        wsbuf = fd.new_workspace(w.B, w.H, w.N, w.d, 0, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = None
-    if 2 * w.B * w.H * w.N * w.d * EB[w.dtype] <= 4 * L2_BYTES:
+    if 2 * w.B * w.kv_heads * w.N * w.d * EB[w.dtype] <= 4 * L2_BYTES:
         # write one buffer larger than L2, then read another, so that L2
         # holds none of the inputs and no dirty lines left to write back
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)

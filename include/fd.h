@@ -138,6 +138,25 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Grouped-query decode (MQA / GQA, "从第一性原理推导 Flash Attention" §8):
+ * Hq = G * Hkv query heads, query head h attending with K/V head h / G, so
+ * every K/V byte serves G query rows.  Same results as fd_decode with each
+ * K/V head repeated G times.
+ *   q    [B, Hq, d]          k, v [B, Hkv, N, d]      out [B, Hq, d]
+ *   lse  [B, Hq] float32 or NULL
+ * G == 1 is fd_decode.  For G = 2..16 the per-chunk contraction runs on the
+ * tensor cores, which need 16-bit operands: in_dtype f16 or bf16, and
+ * B*Hkv*N < 2^31.  The workspace size is fd_workspace_size_gqa(...).
+ * Returns FD_ERR_UNSUPPORTED for G > 16 or f32 with G > 1.
+ */
+size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_splits);
+
+fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32_t *seqlens,
+                        int B, int Hq, int Hkv, int N, int d, fd_dtype in_dtype, int num_splits,
+                        float scale, void *out, fd_dtype out_dtype, float *lse, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/*
  * fd_decode over an FP8 KV cache: K and V hold OCP E4M3 bytes with one
  * float32 dequantisation scale per (b, h); the value of K[b,h,t,i] is
  * k_scale[b*H+h] * e4m3(k[b,h,t,i]), likewise V.  Storing the cache in FP8

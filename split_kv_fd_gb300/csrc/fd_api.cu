@@ -2,8 +2,11 @@
 // checks, the choice of decomposition and grid, workspace carving, and the
 // launches.  Nothing here computes attention; every step runs in the kernels.
 #include "fd.h"
+#include "fd_gqa.cuh"
 #include "fd_internal.h"
 #include "fd_split.cuh"
+
+#include <cuda.h>
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -131,6 +134,45 @@ fd_status launch(int dtype, int d, const SplitParams &p, int decomp, cudaStream_
     else
         e = launch_split_bf16(d, p, smem, s);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime (no
+// link-time dependency on the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (fn)
+        return fn;
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    return fn;
+}
+
+// K or V [rows, d] 16-bit as the 3-D map [64 elements, d/64 lines, rows]
+// with boxes of `box_rows` rows and the 128-byte swizzle.
+bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long rows, int box_rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)(d / 64), (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)d * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)(d / 64), (cuuint32_t)box_rows};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+              const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -369,6 +411,92 @@ fd_status fd_device_status(int reset)
     if (v & STATUS_TIMEOUT)
         return FD_ERR_DEVICE_TIMEOUT;
     return (v & STATUS_BAD_PAGE) ? FD_ERR_BAD_PAGE : FD_OK;
+}
+
+size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_splits)
+{
+    if (Hkv <= 0 || Hq < 0 || Hq % Hkv != 0)
+        return 0;
+    if (Hq == Hkv)
+        return fd_workspace_size(B, Hq, N, d, num_splits);
+    if (!sizes_ok(B, Hq, N, d) || num_splits < 0)
+        return 0;
+    const int sms = sm_count();
+    if (sms <= 0)
+        return 0;
+    const Plan pl = make_plan(B, Hkv, N, d, num_splits, sms);
+    return ws_layout(pl.slots * (Hq / Hkv), d, (long long)B * Hkv).total;
+}
+
+fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32_t *seqlens, int B,
+                        int Hq, int Hkv, int N, int d, fd_dtype in_dtype, int num_splits, float scale,
+                        void *out, fd_dtype out_dtype, float *lse, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    if (Hkv <= 0 || Hq < 0 || Hq % Hkv != 0)
+        return FD_ERR_INVALID_ARG;
+    if (Hq == Hkv)
+        return fd_decode(q, k, v, seqlens, B, Hq, N, d, in_dtype, num_splits, scale, out, out_dtype,
+                         lse, workspace, workspace_bytes, stream);
+    const int G = Hq / Hkv;
+    if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(out_dtype) || (d != 64 && d != 128) || G > GqaCfg<__half, 128>::MAXG ||
+        (in_dtype != FD_F16 && in_dtype != FD_BF16))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * Hkv * N >= (1LL << 31))
+        return FD_ERR_UNSUPPORTED;  // tensor-map row coordinates are 32-bit
+    if ((long long)B * Hq == 0)
+        return FD_OK;
+    if (!q || (N > 0 && (!k || !v)) || !out || !aligned(q, 16) || !aligned(k, 16) ||
+        !aligned(v, 16) || !aligned(out, 16) || (seqlens && !aligned(seqlens, 4)) ||
+        (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    unsigned *st = status_ptr();
+    if (sms <= 0 || !st)
+        return FD_ERR_CUDA;
+    const Plan pl = make_plan(B, Hkv, N, d, num_splits, sms);
+    const WsLayout wl = ws_layout(pl.slots * G, d, (long long)B * Hkv);
+    if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
+        return FD_ERR_WORKSPACE;
+
+    GqaParams gp;
+    memset(&gp, 0, sizeof gp);
+    if (N > 0) {
+        const long long rows = (long long)B * Hkv * N;
+        if (!make_kv_map(&gp.tmk, k, in_dtype, d, rows, GqaCfg<__half, 128>::CT) ||
+            !make_kv_map(&gp.tmv, v, in_dtype, d, rows, GqaCfg<__half, 128>::CT))
+            return FD_ERR_CUDA;
+    }
+    gp.G = G;
+    SplitParams &p = gp.s;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.lens = seqlens;
+    p.B = B;
+    p.H = Hkv;
+    p.N = N;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.q_dtype = in_dtype;
+    p.decomp = pl.decomp;
+    p.P = pl.P;
+    p.grid = pl.grid;
+    p.out_kind = OUT_FUSED;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.lse = lse;
+    char *ws = static_cast<char *>(workspace);
+    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
+    p.status = st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
+    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * Hkv * sizeof(unsigned), cs) != cudaSuccess)
+        return FD_ERR_CUDA;
+    return launch_gqa(in_dtype, d, gp, cs) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
 fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,

@@ -160,6 +160,95 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
 }
 
 // ---------------------------------------------------------------------------
+// Tensor-map (tiled) TMA and warp-level tensor-core helpers.
+// ---------------------------------------------------------------------------
+
+// 3-D tiled copy global -> shared through a tensor map, completion on `bar`.
+// The innermost coordinate (x) must start on a 16-byte boundary.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Four 8x8 b16 matrices from shared memory (lane l gives the address of row
+// l % 8 of matrix l / 8), plain or transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D = A(16x16) * B(16x8) + D, fp32 accumulate; A, B both bf16 or both f16.
+template <typename T> struct Mma;
+template <> struct Mma<__nv_bfloat16> {
+    __device__ __forceinline__ static void run(float *d, const uint32_t *a, uint32_t b0, uint32_t b1)
+    {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // two floats -> one packed register (lower half = x), round-to-nearest-even
+    __device__ __forceinline__ static uint32_t pack(float x, float y)
+    {
+        __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+        uint32_t r;
+        memcpy(&r, &h, 4);
+        return r;
+    }
+    __device__ __forceinline__ static float2 unpack(uint32_t r)
+    {
+        __nv_bfloat162 h;
+        memcpy(&h, &r, 4);
+        return __bfloat1622float2(h);
+    }
+};
+template <> struct Mma<__half> {
+    __device__ __forceinline__ static void run(float *d, const uint32_t *a, uint32_t b0, uint32_t b1)
+    {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    __device__ __forceinline__ static uint32_t pack(float x, float y)
+    {
+        __half2 h = __floats2half2_rn(x, y);
+        uint32_t r;
+        memcpy(&r, &h, 4);
+        return r;
+    }
+    __device__ __forceinline__ static float2 unpack(uint32_t r)
+    {
+        __half2 h;
+        memcpy(&h, &r, 4);
+        return __half22float2(h);
+    }
+};
+
+// ---------------------------------------------------------------------------
 // 16-byte vectors of the storage type, widened to float32.
 // ---------------------------------------------------------------------------
 template <typename T> struct Elem;

@@ -209,6 +209,65 @@ __device__ __forceinline__ void seg_next(const SplitParams &p, const Ctx &c, Seg
     s.t1 = (long long)len < room ? len : (int)room;
 }
 
+// Balanced decomposition set-up, run by every thread of the CTA: clamped
+// lengths into lenS, H * exclusive prefix sums into cumH[0..B], and this
+// CTA's range of the concatenated token space in ctx.  Contains barriers.
+template <int THREADS, int WARPS>
+__device__ __forceinline__ void balanced_setup(const SplitParams &p, Ctx &ctx, long long *cumH,
+                                               int *lenS)
+{
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    constexpr int PER = (BALANCED_MAX_B + THREADS - 1) / THREADS;
+    long long v[PER];
+    long long run = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int b = tid * PER + i;
+        long long x = 0;
+        if (b < p.B) {
+            const int n = clamp_len(p, b);
+            lenS[b] = n;
+            x = (long long)n * p.H;
+        }
+        v[i] = run;
+        run += x;
+    }
+    // inclusive scan of per-thread totals across the block
+    long long incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(FULL_MASK, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    __shared__ long long warp_tot[WARPS];
+    if (lane == 31)
+        warp_tot[w] = incl;
+    __syncthreads();
+    long long wbase = 0;
+    for (int i = 0; i < w; ++i)
+        wbase += warp_tot[i];
+    const long long excl = wbase + incl - run;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int b = tid * PER + i;
+        if (b < p.B)
+            cumH[b] = excl + v[i];
+    }
+    if (tid == THREADS - 1)
+        cumH[p.B] = excl + run;
+    __syncthreads();
+    ctx.T = cumH[p.B];
+    // at least BALANCED_MIN_TOKENS tokens per CTA: a small problem uses
+    // fewer, fuller CTAs (fewer pieces to merge)
+    const long long want = (ctx.T + BALANCED_MIN_TOKENS - 1) / BALANCED_MIN_TOKENS;
+    ctx.Geff = (int)(want < (long long)ctx.G ? want : (long long)ctx.G);
+    if (ctx.g < ctx.Geff) {
+        ctx.beg = bal_bound(ctx.g, ctx.T, ctx.Geff);
+        ctx.end = bal_bound(ctx.g + 1, ctx.T, ctx.Geff);
+    }
+}
+
 // Chunks lie on a fixed grid of the sequence's token index (multiples of CT),
 // so a chunk never straddles more pages than it must; a segment's first and
 // last chunks may be partial.
@@ -554,56 +613,7 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split
     ctx.Geff = 0;
     ctx.beg = ctx.end = 0;
     if (p.decomp == DECOMP_BALANCED) {
-        // clamped lengths and H * exclusive prefix sums, by a block scan
-        constexpr int PER = (BALANCED_MAX_B + C::THREADS - 1) / C::THREADS;
-        long long v[PER];
-        long long run = 0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int b = tid * PER + i;
-            long long x = 0;
-            if (b < p.B) {
-                const int n = clamp_len(p, b);
-                lenS[b] = n;
-                x = (long long)n * p.H;
-            }
-            v[i] = run;
-            run += x;
-        }
-        // inclusive scan of per-thread totals across the block
-        long long incl = run;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long y = __shfl_up_sync(FULL_MASK, incl, o);
-            if (lane >= o)
-                incl += y;
-        }
-        __shared__ long long warp_tot[C::WARPS];
-        if (lane == 31)
-            warp_tot[w] = incl;
-        __syncthreads();
-        long long wbase = 0;
-        for (int i = 0; i < w; ++i)
-            wbase += warp_tot[i];
-        const long long excl = wbase + incl - run;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int b = tid * PER + i;
-            if (b < p.B)
-                cumH[b] = excl + v[i];
-        }
-        if (tid == C::THREADS - 1)
-            cumH[p.B] = excl + run;
-        __syncthreads();
-        ctx.T = cumH[p.B];
-        // at least BALANCED_MIN_TOKENS tokens per CTA: a small problem uses
-        // fewer, fuller CTAs (fewer pieces to merge)
-        const long long want = (ctx.T + BALANCED_MIN_TOKENS - 1) / BALANCED_MIN_TOKENS;
-        ctx.Geff = (int)(want < (long long)ctx.G ? want : (long long)ctx.G);
-        if (ctx.g < ctx.Geff) {
-            ctx.beg = bal_bound(ctx.g, ctx.T, ctx.Geff);
-            ctx.end = bal_bound(ctx.g + 1, ctx.T, ctx.Geff);
-        }
+        balanced_setup<C::THREADS, C::WARPS>(p, ctx, cumH, lenS);
         // sequences of length 0 are touched by no CTA: write their result here
         for (long long bh = (long long)ctx.g * C::THREADS + tid; bh < (long long)p.B * p.H;
              bh += (long long)ctx.G * C::THREADS) {

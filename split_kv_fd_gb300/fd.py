@@ -28,7 +28,7 @@ DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 EXPORTS = ["fd_status_str", "fd_version", "fd_num_sms", "fd_auto_num_splits",
            "fd_workspace_size", "fd_decode", "fd_decode_split", "fd_combine_mlo",
            "fd_combine_lse", "fd_device_status", "fd_decode_noalloc", "fd_decode_paged",
-           "fd_decode_fp8", "fd_merge_lse"]
+           "fd_decode_fp8", "fd_merge_lse", "fd_decode_gqa", "fd_workspace_size_gqa"]
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +83,10 @@ def load(build_if_missing: bool = False):
         lib.fd_decode_fp8.restype = I
         lib.fd_merge_lse.argtypes = [P, P, P, P, I, I, P, P, P]
         lib.fd_merge_lse.restype = I
+        lib.fd_decode_gqa.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P, I, P, P, S, P]
+        lib.fd_decode_gqa.restype = I
+        lib.fd_workspace_size_gqa.argtypes = [I, I, I, I, I, I]
+        lib.fd_workspace_size_gqa.restype = S
         lib.fd_device_status.argtypes = [I]
         lib.fd_device_status.restype = I
         _lib = lib
@@ -238,6 +242,46 @@ def decode_paged(q, k_pages, v_pages, block_table, seqlens, num_splits=0, scale=
                              _stream(q, stream))
     _check(st, "fd_decode_paged")
     return out, lse
+
+
+def decode_gqa(q, k, v, seqlens=None, num_splits=0, scale=None, out_dtype=None, out=None,
+               lse=None, return_lse=True, workspace=None, stream=None):
+    """Grouped-query decode (fd_decode_gqa).  Returns ``(out, lse)``.
+
+    q [B, Hq, d]; k, v [B, Hkv, N, d] with Hq a multiple of Hkv.
+    """
+    _need_cuda(q, k, v, seqlens)
+    if q.dtype not in DTYPE_CODE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, K, V must share one dtype among float32/float16/bfloat16")
+    if k.dim() != 4 or v.shape != k.shape or q.dim() != 3 or q.shape[0] != k.shape[0] \
+            or q.shape[2] != k.shape[3] or q.shape[1] % k.shape[1]:
+        raise ValueError("shapes: q [B,Hq,d], k/v [B,Hkv,N,d], Hq % Hkv == 0")
+    B, Hkv, N, d = k.shape
+    Hq = q.shape[1]
+    if seqlens is not None and (seqlens.dtype != torch.int32 or seqlens.shape != (B,)):
+        raise ValueError("seqlens must be an int32 tensor of shape [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=odt, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _need_cuda(out, lse)
+    lib = load()
+    need = lib.fd_workspace_size_gqa(B, Hq, Hkv, N, d, int(num_splits))
+    if workspace is None:
+        workspace = _cached_workspace(q.device, need)
+    st = lib.fd_decode_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(seqlens), B, Hq, Hkv, N, d,
+                           DTYPE_CODE[q.dtype], int(num_splits), float(scale), _ptr(out),
+                           DTYPE_CODE[out.dtype], _ptr(lse), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream(q, stream))
+    _check(st, "fd_decode_gqa")
+    return out, lse
+
+
+def workspace_size_gqa(B, Hq, Hkv, N, d, num_splits=0) -> int:
+    return load().fd_workspace_size_gqa(B, Hq, Hkv, N, d, num_splits)
 
 
 def decode_fp8(q, k, v, k_scale, v_scale, seqlens=None, num_splits=0, scale=None, out_dtype=None,

@@ -6,9 +6,9 @@ Recipe (one ``torch.Generator`` on the target device, seeded with the
 workload's seed; draws in this order):
   1. lengths: ``randint(1, N + 1, (B,))`` if the workload is ragged, else N;
   2. q: float32 N(0, 1), shape [B, H, d];
-  3. K: float32 N(0, 1) * k_scale, shape [B, H, N, d], drawn in chunks of
-     the flattened tensor;
-  4. V: float32 N(0, 1), shape [B, H, N, d], drawn the same way;
+  3. K: float32 N(0, 1) * k_scale, shape [B, Hkv, N, d] (Hkv = H unless the
+     workload is grouped-query), drawn in chunks of the flattened tensor;
+  4. V: float32 N(0, 1), shape [B, Hkv, N, d], drawn the same way;
 each cast to the storage dtype with round-to-nearest-even.  Rows past a
 sequence's length are filled with NaN, so a read past the end shows up as a
 NaN in the result.
@@ -52,8 +52,8 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None,
     else:
         lens = torch.full((w.B,), w.N, dtype=torch.int32, device=device)
     q = torch.empty((w.B, w.H, w.d), dtype=dt, device=device)
-    k = torch.empty((w.B, w.H, w.N, w.d), dtype=dt, device=device)
-    v = torch.empty((w.B, w.H, w.N, w.d), dtype=dt, device=device)
+    k = torch.empty((w.B, w.kv_heads, w.N, w.d), dtype=dt, device=device)
+    v = torch.empty((w.B, w.kv_heads, w.N, w.d), dtype=dt, device=device)
     _fill_normal(q, g, 1.0, chunk)
     _fill_normal(k, g, w.k_scale, chunk)
     _fill_normal(v, g, 1.0, chunk)

@@ -23,10 +23,15 @@ class Workload:
     k_scale: float = 1.0   # K draws are N(0,1) * k_scale
     ragged: bool = False   # lengths ~ U[1, N] per sequence, else all N
     seed: int = 0
+    Hkv: int = 0           # K/V heads (grouped-query attention); 0 => H
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv or self.H
 
 
 WORKLOADS = {
@@ -49,6 +54,11 @@ ORDER = list(WORKLOADS)
 # K/V (larger than the 129 MB L2, small enough for a many-pass capture)
 WORKLOADS["decode_b2_h8_n32k_d128_bf16"] = Workload(
     "decode_b2_h8_n32k_d128_bf16", 2, 8, 32768, 128, "bf16", "bf16", 0)
+
+# grouped-query decode: 64 query heads sharing 8 K/V heads (G = 8), 32K
+# tokens per sequence (1 GiB of K/V)
+WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"] = Workload(
+    "decode_gqa_b8_hq64_hkv8_n32k_d128_bf16", 8, 64, 32768, 128, "bf16", "bf16", 0, Hkv=8)
 
 # the workload the benchmark times by default: uniform 32K-token sequences
 BENCH_DEFAULT = "decode_b8_h32_n32k_d128_bf16"

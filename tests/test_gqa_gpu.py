@@ -1,0 +1,76 @@
+"""Grouped-query decode on the GPU (fd_decode_gqa, tensor-core path for
+G = 2..16) against the float64 GQA oracle.  Lengths include 0, shorter than
+one chunk, and ragged tails; padding rows are NaN."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_fd_gb300 as fd
+from split_kv_fd_gb300.inputs import random_case
+from parity_util import check_lse, check_out
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__ as g
+    g.build()
+    fd.load()
+    yield
+    assert fd.device_status() == 0
+
+
+def _gqa_case(B, Hq, Hkv, N, d, dtype, lens, seed, k_scale=1.0):
+    # K/V with Hkv heads; q drawn separately with Hq heads
+    _, k, v, lt = random_case(B, Hkv, N, d, dtype, lens=lens, seed=seed, k_scale=k_scale)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn(B, Hq, d, generator=g).to(DT[dtype])
+    return q, k, v, lt
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [2, 4, 8, 16])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_gqa_matches_oracle(dtype, d, G, num_splits):
+    Hkv = 2
+    q, k, v, lt = _gqa_case(3, Hkv * G, Hkv, 700, d, dtype, [700, 0, 13], seed=G + d)
+    ref_out, ref_lse = oracle.attention_gqa(q, k, v, lens=lt)
+    dev = torch.device("cuda")
+    out, lse = fd.decode_gqa(q.to(dev), k.to(dev), v.to(dev), lt.to(dev), num_splits=num_splits,
+                             out_dtype=torch.float32)
+    check_out(out, ref_out, dtype)
+    check_lse(lse, ref_lse, dtype)
+    out16, _ = fd.decode_gqa(q.to(dev), k.to(dev), v.to(dev), lt.to(dev), num_splits=num_splits,
+                             out_dtype=DT[dtype])
+    check_out(out16, ref_out, dtype)
+
+
+def test_gqa_peaked_scores_and_long_sequences():
+    """K scaled by 8 (near one-hot attention) over 20K tokens, G = 8."""
+    q, k, v, lt = _gqa_case(2, 32, 4, 20000, 128, "bf16", [20000, 7777], seed=5, k_scale=8.0)
+    ref_out, ref_lse = oracle.attention_gqa(q, k, v, lens=lt)
+    dev = torch.device("cuda")
+    out, lse = fd.decode_gqa(q.to(dev), k.to(dev), v.to(dev), lt.to(dev), out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
+
+
+def test_gqa_group_of_one_is_decode_and_errors():
+    dev = torch.device("cuda")
+    q, k, v, lt = _gqa_case(2, 4, 4, 300, 128, "bf16", [300, 100], seed=2)
+    a = fd.decode_gqa(q.to(dev), k.to(dev), v.to(dev), lt.to(dev))
+    b = fd.decode(q.to(dev), k.to(dev), v.to(dev), lt.to(dev))
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    # G > 16 and f32 with G > 1 are not supported
+    q32, k32, v32, l32 = _gqa_case(1, 34, 2, 64, 64, "bf16", None, seed=3)
+    with pytest.raises(fd.FDError):
+        fd.decode_gqa(q32.to(dev), k32.to(dev), v32.to(dev))
+    qf = torch.randn(1, 4, 64, device=dev)
+    kf = torch.randn(1, 2, 64, 64, device=dev)
+    with pytest.raises(fd.FDError):
+        fd.decode_gqa(qf, kf, kf)
