@@ -26,6 +26,10 @@
 
 namespace fd {
 
+#ifndef FD_GQA_STAGES
+#define FD_GQA_STAGES 2
+#endif
+
 template <typename T, int D> struct GqaCfg {
     static constexpr int ROW = D * 2;              // bytes per token row (16-bit types)
     static constexpr int LINES = D / 64;           // 128-byte lines per row
@@ -33,7 +37,7 @@ template <typename T, int D> struct GqaCfg {
     static constexpr int THREADS = WARPS * 32;
     static constexpr int GW = 2;                   // warps sharing one ring
     static constexpr int GROUPS = WARPS / GW;
-    static constexpr int STAGES = 2;
+    static constexpr int STAGES = FD_GQA_STAGES;
     static constexpr int WT = 16;                  // tokens per warp per chunk (one PV k-step)
     static constexpr int CT = GW * WT;             // tokens per chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // one of K or V
@@ -140,19 +144,30 @@ __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int 
                                           const uint32_t (*qa)[4], float scale_log2, int lane,
                                           GqaState<C> &st)
 {
-    // scores for 2 tiles of 8 tokens
-    float sc[2][4];
+    // scores for 2 tiles of 8 tokens; even and odd k-steps accumulate
+    // separately so the dependent MMA chains are half as long
+    float sc[2][4], sx[2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-        const int tok = row0 + 8 * j + (lane & 7);
+        sx[j][0] = sx[j][1] = sx[j][2] = sx[j][3] = 0.f;
+    }
 #pragma unroll
-        for (int s2 = 0; s2 < C::KSTEPS / 2; ++s2) {
+    for (int s2 = 0; s2 < C::KSTEPS / 2; ++s2) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int tok = row0 + 8 * j + (lane & 7);
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kstage + swz<C::LINES>(tok, 4 * s2 + (lane >> 3)), b0, b1, b2, b3);
             Mma<T>::run(sc[j], qa[2 * s2], b0, b1);
-            Mma<T>::run(sc[j], qa[2 * s2 + 1], b2, b3);
+            Mma<T>::run(sx[j], qa[2 * s2 + 1], b2, b3);
         }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sc[j][e] += sx[j][e];
     }
     // base-2 scale and the mask of rows past the last valid token
     const int colb = 2 * (lane & 3);

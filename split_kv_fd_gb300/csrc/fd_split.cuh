@@ -53,18 +53,43 @@ constexpr float LN2_F = 0.693147180559945309f;
 #define FD_FMA2 1
 #endif
 
+// Ring shape per element type.  The FP8 cache carries twice the tokens per
+// byte, so per byte it needs twice the arithmetic: it runs 16 warps (more
+// latency hiding) in groups of 4 with 3 KB per warp and stage (measured on
+// GB300: 6.97 TB/s against 6.12 TB/s with the 16-bit shape).
+#ifndef FD_FP8_WARPS
+#define FD_FP8_WARPS 16
+#endif
+#ifndef FD_FP8_GROUP_WARPS
+#define FD_FP8_GROUP_WARPS 4
+#endif
+#ifndef FD_FP8_STAGES
+#define FD_FP8_STAGES FD_STAGES
+#endif
+#ifndef FD_FP8_WARP_BYTES
+#define FD_FP8_WARP_BYTES 3072
+#endif
+template <typename T> struct RingShape {
+    static constexpr int WARPS = FD_WARPS, GW = FD_GROUP_WARPS, STAGES = FD_STAGES,
+                         WARP_BYTES = FD_WARP_BYTES;
+};
+template <> struct RingShape<__nv_fp8_e4m3> {
+    static constexpr int WARPS = FD_FP8_WARPS, GW = FD_FP8_GROUP_WARPS, STAGES = FD_FP8_STAGES,
+                         WARP_BYTES = FD_FP8_WARP_BYTES;
+};
+
 template <typename T, int D> struct SplitCfg {
     static constexpr int ESZ = sizeof(T);
     static constexpr int VEC = Elem<T>::VEC;       // elements per lane vector (16 bytes)
     static constexpr int LPT = D / VEC;            // lanes per token row
     static constexpr int TPW = 32 / LPT;           // token rows per warp-wide load
     static constexpr int ROW = D * ESZ;            // bytes per token row
-    static constexpr int WARPS = FD_WARPS;
+    static constexpr int WARPS = RingShape<T>::WARPS;
     static constexpr int THREADS = WARPS * 32;
-    static constexpr int GW = FD_GROUP_WARPS;      // warps sharing one ring
+    static constexpr int GW = RingShape<T>::GW;    // warps sharing one ring
     static constexpr int GROUPS = WARPS / GW;
-    static constexpr int STAGES = FD_STAGES;
-    static constexpr int WT = FD_WARP_BYTES / ROW; // tokens per warp per chunk
+    static constexpr int STAGES = RingShape<T>::STAGES;
+    static constexpr int WT = RingShape<T>::WARP_BYTES / ROW; // tokens per warp per chunk
     static constexpr int CT = GW * WT;             // tokens per chunk (per group)
     static constexpr int TOK = WT / TPW;           // tokens per lane group per chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // one of K or V

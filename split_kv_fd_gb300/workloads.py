@@ -55,6 +55,14 @@ ORDER = list(WORKLOADS)
 WORKLOADS["decode_b2_h8_n32k_d128_bf16"] = Workload(
     "decode_b2_h8_n32k_d128_bf16", 2, 8, 32768, 128, "bf16", "bf16", 0)
 
+# a 1 GiB case for detailed profiles of the FP8 path (512 MiB once stored in E4M3)
+WORKLOADS["decode_b4_h16_n32k_d128_bf16"] = Workload(
+    "decode_b4_h16_n32k_d128_bf16", 4, 16, 32768, 128, "bf16", "bf16", 0)
+
+# a 256 MiB grouped-query case for detailed profiles
+WORKLOADS["decode_gqa_b2_hq64_hkv8_n32k_d128_bf16"] = Workload(
+    "decode_gqa_b2_hq64_hkv8_n32k_d128_bf16", 2, 64, 32768, 128, "bf16", "bf16", 0, Hkv=8)
+
 # grouped-query decode: 64 query heads sharing 8 K/V heads (G = 8), 32K
 # tokens per sequence (1 GiB of K/V)
 WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"] = Workload(
