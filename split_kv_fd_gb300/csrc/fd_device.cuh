@@ -90,6 +90,33 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     return __all_sync(FULL_MASK, ok);
 }
 
+// Bounded wait for a phase that may take long (a whole segment of
+// streaming), for a warp that must not slow the warps doing the work: it
+// tests the phase without blocking and sleeps `sleep_ns` between tests.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity, uint32_t sleep_ns)
+{
+    const unsigned long long t0 = global_ns();
+    bool ok = false;
+    for (unsigned i = 0; i < WAIT_LIMIT_POLLS; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) {
+            ok = true;
+            break;
+        }
+        if (global_ns() - t0 > WAIT_LIMIT_NS)
+            break;
+        __nanosleep(sleep_ns);
+    }
+    return __all_sync(FULL_MASK, ok);
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
@@ -173,6 +200,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+
+// Hint: start fetching the global-memory line holding `ptr` into L1.
+__device__ __forceinline__ void prefetch_l1(const void *ptr)
+{
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(__cvta_generic_to_global(ptr)));
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)

@@ -54,14 +54,16 @@ constexpr float LN2_F = 0.693147180559945309f;
 #endif
 
 // Ring shape per element type.  The FP8 cache carries twice the tokens per
-// byte, so per byte it needs twice the arithmetic: it runs 16 warps (more
-// latency hiding) in groups of 4 with 3 KB per warp and stage (measured on
-// GB300: 6.97 TB/s against 6.12 TB/s with the 16-bit shape).
+// byte, so per byte it needs twice the arithmetic: it runs 15 streaming
+// warps (more latency hiding) in groups of 5 with 3 KB per warp and stage,
+// and 2 segment buffers to stay within shared memory (measured on GB300:
+// 7.02 TB/s, as with 12 warps of 4 KB, which spill registers; 6.55 TB/s with
+// 12 warps of 3 KB; 6.12 TB/s with the 16-bit shape).
 #ifndef FD_FP8_WARPS
-#define FD_FP8_WARPS 16
+#define FD_FP8_WARPS 15
 #endif
 #ifndef FD_FP8_GROUP_WARPS
-#define FD_FP8_GROUP_WARPS 4
+#define FD_FP8_GROUP_WARPS 5
 #endif
 #ifndef FD_FP8_STAGES
 #define FD_FP8_STAGES FD_STAGES
@@ -69,13 +71,20 @@ constexpr float LN2_F = 0.693147180559945309f;
 #ifndef FD_FP8_WARP_BYTES
 #define FD_FP8_WARP_BYTES 3072
 #endif
+// segment states in flight from the streaming warps to the merge warp
+#ifndef FD_NBUF
+#define FD_NBUF 4
+#endif
+#ifndef FD_FP8_NBUF
+#define FD_FP8_NBUF 2
+#endif
 template <typename T> struct RingShape {
     static constexpr int WARPS = FD_WARPS, GW = FD_GROUP_WARPS, STAGES = FD_STAGES,
-                         WARP_BYTES = FD_WARP_BYTES;
+                         WARP_BYTES = FD_WARP_BYTES, NBUF = FD_NBUF;
 };
 template <> struct RingShape<__nv_fp8_e4m3> {
     static constexpr int WARPS = FD_FP8_WARPS, GW = FD_FP8_GROUP_WARPS, STAGES = FD_FP8_STAGES,
-                         WARP_BYTES = FD_FP8_WARP_BYTES;
+                         WARP_BYTES = FD_FP8_WARP_BYTES, NBUF = FD_FP8_NBUF;
 };
 
 template <typename T, int D> struct SplitCfg {
@@ -84,8 +93,9 @@ template <typename T, int D> struct SplitCfg {
     static constexpr int LPT = D / VEC;            // lanes per token row
     static constexpr int TPW = 32 / LPT;           // token rows per warp-wide load
     static constexpr int ROW = D * ESZ;            // bytes per token row
-    static constexpr int WARPS = RingShape<T>::WARPS;
-    static constexpr int THREADS = WARPS * 32;
+    static constexpr int WARPS = RingShape<T>::WARPS;   // streaming warps
+    static constexpr int MW = WARPS;               // index of the merge warp
+    static constexpr int THREADS = (WARPS + 1) * 32;
     static constexpr int GW = RingShape<T>::GW;    // warps sharing one ring
     static constexpr int GROUPS = WARPS / GW;
     static constexpr int STAGES = RingShape<T>::STAGES;
@@ -95,12 +105,15 @@ template <typename T, int D> struct SplitCfg {
     static constexpr int CHUNK_BYTES = CT * ROW;   // one of K or V
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
     static constexpr int RING_BYTES = GROUPS * STAGES * STAGE_BYTES;
-    static constexpr int BAR_BYTES = GROUPS * STAGES * 2 * 8;   // full + empty
-    static constexpr int RED_BYTES = (2 * WARPS + WARPS * D) * 4 + 16;
+    static constexpr int NBUF = RingShape<T>::NBUF;   // segment states in flight to the merge warp
+    static constexpr int SEG_FLOATS = 2 * WARPS + WARPS * D;   // per warp: m, l, then acc rows
+    // ring full + empty, then segment full + free
+    static constexpr int BAR_BYTES = GROUPS * STAGES * 2 * 8 + NBUF * 2 * 8;
+    static constexpr int RED_BYTES = NBUF * SEG_FLOATS * 4;
     static_assert(LPT >= 1 && LPT <= 32 && 32 % LPT == 0, "row must map onto whole lanes");
     static_assert(WT % TPW == 0 && TOK >= 1, "chunk must cover whole warp steps");
     static_assert(WARPS % GW == 0, "warps must form whole groups");
-    static_assert(D <= THREADS, "one thread per output element in the merge");
+    static_assert(D % 32 == 0, "the merge warp holds D / 32 output elements per lane");
 
     static size_t smem_bytes(int decomp, int B)
     {
@@ -509,25 +522,20 @@ __device__ __forceinline__ void process_chunk(uint32_t kbase, uint32_t vbase, in
     m = mnew;
 }
 
-// Block-wide max / sum over the CTA's threads (scratch: one float per warp).
-template <int WARPS>
-__device__ __forceinline__ float block_reduce(float x, bool is_max, float *scratch)
+__device__ __forceinline__ float warp_max(float x)
 {
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const float y = __shfl_xor_sync(FULL_MASK, x, o);
-        x = is_max ? fmaxf(x, y) : x + y;
-    }
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    if (lane == 0)
-        scratch[w] = x;
-    __syncthreads();
-    float r = scratch[0];
+    for (int o = 16; o >= 1; o >>= 1)
+        x = fmaxf(x, __shfl_xor_sync(FULL_MASK, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
 #pragma unroll
-    for (int i = 1; i < WARPS; ++i)
-        r = is_max ? fmaxf(r, scratch[i]) : r + scratch[i];
-    __syncthreads();
-    return r;
+    for (int o = 16; o >= 1; o >>= 1)
+        x += __shfl_xor_sync(FULL_MASK, x, o);
+    return x;
 }
 
 // Workspace slot of the i-th piece of (b, h) (see the decompositions).
@@ -540,61 +548,210 @@ __device__ __forceinline__ long long piece_slot(const SplitParams &p, const Ctx 
     return (i == 0 && bal_bound(gf, ctx.T, ctx.Geff) != off) ? 2 * g + 1 : 2 * g;
 }
 
-// Stage 2 run by the last piece of (b, h) to arrive: the m/l/o merge of
-// "FlashDecoding 数学推导" §2.4.2 over its `target` workspace partials
-// (normalised o, m in base 2, l), read from L2.  All threads take part: the
-// max and the weights are reduced over the pieces in parallel, then each
-// (slot group, element) thread sums its share of the weighted rows.
-template <typename C, int D>
+// Stage 2, run by the merge warp of the last piece of (b, h) to arrive: the
+// m/l/o merge of "FlashDecoding 数学推导" §2.4.2 over its `target` workspace
+// partials (normalised o, m in base 2, l), read from L2.  Lane j owns output
+// elements j, j + 32, ...; the pieces' weights are formed 32 at a time, one
+// per lane, and broadcast by shuffles, so the merge needs no barrier.
+template <int D>
 __device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ctx, int bh,
-                                             unsigned target, int gf, long long off, int tid,
-                                             float *scratch, float *tile)
+                                             unsigned target, int gf, long long off, int lane)
 {
-    constexpr int NSG = C::THREADS / D;        // slot groups
-    constexpr int TILE = C::WARPS * D;         // weights staged per pass
-    static_assert(C::THREADS % D == 0, "threads must cover whole rows");
-    float mx = -INFINITY;
-    for (unsigned i = tid; i < target; i += C::THREADS) {
+    constexpr int DPL = D / 32;
+    // the first 32 pieces keep their slot and (m, l) in registers
+    long long s0 = 0;
+    float m0 = -INFINITY, l0 = 0.f;
+    if ((unsigned)lane < target) {
+        s0 = piece_slot(p, ctx, bh, (unsigned)lane, gf, off);
+        m0 = __ldcg(p.ws_ml + 2 * s0);
+        l0 = __ldcg(p.ws_ml + 2 * s0 + 1);
+    }
+    float mx = l0 > 0.f ? m0 : -INFINITY;
+    for (unsigned i = lane + 32; i < target; i += 32) {
         const long long sl = piece_slot(p, ctx, bh, i, gf, off);
         if (__ldcg(p.ws_ml + 2 * sl + 1) > 0.f)
             mx = fmaxf(mx, __ldcg(p.ws_ml + 2 * sl));
     }
-    const float M = block_reduce<C::WARPS>(mx, true, scratch);
-    const int dim = tid % D, sg = tid / D;
-    float lpart = 0.f, O = 0.f;
-    for (unsigned base = 0; base < target; base += TILE) {
-        const unsigned nt = min((unsigned)TILE, target - base);
-        for (unsigned i = tid; i < nt; i += C::THREADS) {
-            const long long sl = piece_slot(p, ctx, bh, base + i, gf, off);
-            const float ll = __ldcg(p.ws_ml + 2 * sl + 1);
-            const float e = (ll > 0.f) ? ex2(__ldcg(p.ws_ml + 2 * sl) - M) * ll : 0.f;
-            tile[i] = e;
-            lpart += e;
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (unsigned i = sg; i < nt; i += NSG) {
-            const float e = tile[i];
-            if (e > 0.f) {
-                const long long sl = piece_slot(p, ctx, bh, base + i, gf, off);
-                O = fmaf(e, __ldcg(p.ws_o + sl * D + dim), O);
+    const float M = warp_max(mx);
+    float L = 0.f, O[DPL];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j)
+        O[j] = 0.f;
+    for (unsigned base = 0; base < target; base += 32) {
+        long long sl = s0;
+        float m = m0, l = l0;
+        if (base > 0) {
+            sl = 0;
+            m = -INFINITY;
+            l = 0.f;
+            if (base + lane < target) {
+                sl = piece_slot(p, ctx, bh, base + lane, gf, off);
+                m = __ldcg(p.ws_ml + 2 * sl);
+                l = __ldcg(p.ws_ml + 2 * sl + 1);
             }
         }
-        __syncthreads();
-    }
-    const float L = block_reduce<C::WARPS>(lpart, false, scratch);
-    tile[sg * D + dim] = O;
-    __syncthreads();
-    if (tid < D) {
-        float o = 0.f;
+        const float e = l > 0.f ? ex2(m - M) * l : 0.f;
+        L += e;
+        const int n = (int)min(32u, target - base);
+        // 16 pieces' rows in flight at a time
+        for (int i0 = 0; i0 < n; i0 += 16) {
+            float x[16][DPL], ei[16];
 #pragma unroll
-        for (int g2 = 0; g2 < NSG; ++g2)
-            o += tile[g2 * D + tid];
-        const bool nonempty = L > 0.f;
-        store_out(p.out, (long long)bh * D + tid, p.out_dtype, nonempty ? o / L : 0.f);
-        if (tid == 0 && p.lse)
-            p.lse[bh] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+            for (int u = 0; u < 16; ++u) {
+                ei[u] = __shfl_sync(FULL_MASK, e, i0 + u);
+                const long long si = __shfl_sync(FULL_MASK, sl, i0 + u);
+#pragma unroll
+                for (int j = 0; j < DPL; ++j)
+                    x[u][j] = (i0 + u < n) ? __ldcg(p.ws_o + si * D + lane + 32 * j) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+#pragma unroll
+                for (int j = 0; j < DPL; ++j)
+                    O[j] = ei[u] > 0.f ? fmaf(ei[u], x[u][j], O[j]) : O[j];
+            }
+        }
     }
+    L = warp_sum(L);
+    const bool nonempty = L > 0.f;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j)
+        store_out(p.out, (long long)bh * D + lane + 32 * j, p.out_dtype, nonempty ? O[j] / L : 0.f);
+    if (lane == 0 && p.lse)
+        p.lse[bh] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+}
+
+// The merge warp.  It walks the CTA's segments in the streaming warps'
+// order; for segment k it waits until every streaming warp has handed over
+// its (m, l, acc) in buffer k % NBUF, merges them (the m/l/o merge of
+// "FlashDecoding 数学推导" §2.4.2), frees the buffer, and writes the result:
+// out and lse for a whole sequence, the two-call partial, or a workspace
+// partial whose arrival it counts, merging all pieces of the (b, h) if it is
+// the last to arrive.  The streaming warps never wait for any of this unless
+// all NBUF buffers are taken.
+template <typename C, int D>
+__device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx, const float *red,
+                                           uint32_t sfull, uint32_t sfree, int lane)
+{
+    constexpr int DPL = D / 32;
+    Seg s;
+    seg_first(p, ctx, s);
+    int k = 0;
+#pragma unroll 1
+    while (s.valid) {
+        // the segment's facts, worked out while its data streams
+        const int bh = s.b * p.H + s.h;
+        const int len = (p.decomp == DECOMP_BALANCED) ? ctx.lenS[s.b] : clamp_len(p, s.b);
+        bool complete;
+        long long slot;
+        if (p.decomp == DECOMP_SPLITS) {
+            complete = (p.P == 1);
+            slot = (long long)bh * p.P + s.p;
+        } else {
+            complete = (s.t0 == 0 && s.t1 == len);
+            slot = 2LL * ctx.g + (s.k == 0 ? 0 : 1);
+        }
+        // V's dequantisation scale is common to every row of (b, h)
+        const float vs = p.v_scale ? __ldg(p.v_scale + bh) : 1.f;
+
+        const int buf = k % C::NBUF;
+        if (!mbar_wait_bounded_sleep(sfull + buf * 8, (uint32_t)(k / C::NBUF) & 1, 256)) {
+            if (lane == 0)
+                atomicOr(p.status, STATUS_TIMEOUT);
+            return;
+        }
+        const float *rm = red + buf * C::SEG_FLOATS;
+        const float *rl = rm + C::WARPS;
+        const float *ra = rl + C::WARPS;
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < C::WARPS; ++i)
+            if (rl[i] > 0.f)
+                M = fmaxf(M, rm[i]);
+        float L = 0.f, O[DPL];
+#pragma unroll
+        for (int j = 0; j < DPL; ++j)
+            O[j] = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::WARPS; ++i) {
+            if (rl[i] > 0.f) {
+                const float e = ex2(rm[i] - M);
+                L = fmaf(e, rl[i], L);
+#pragma unroll
+                for (int j = 0; j < DPL; ++j)
+                    O[j] = fmaf(e, ra[i * D + lane + 32 * j], O[j]);
+            }
+        }
+        mbar_arrive(sfree + buf * 8);  // the streaming warps may refill the buffer
+        const bool nonempty = L > 0.f;
+        float o[DPL];
+#pragma unroll
+        for (int j = 0; j < DPL; ++j)
+            o[j] = nonempty ? O[j] / L * vs : 0.f;
+
+        if (p.out_kind == OUT_PARTIALS) {
+#pragma unroll
+            for (int j = 0; j < DPL; ++j)
+                p.o_part[slot * D + lane + 32 * j] = o[j];
+            if (lane == 0) {
+                p.m_part[slot] = nonempty ? M * LN2_F : -INFINITY;
+                p.l_part[slot] = L;
+                if (p.lse_part)
+                    p.lse_part[slot] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+            }
+        } else if (complete) {
+#pragma unroll
+            for (int j = 0; j < DPL; ++j)
+                store_out(p.out, (long long)bh * D + lane + 32 * j, p.out_dtype, o[j]);
+            if (lane == 0 && p.lse)
+                p.lse[bh] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+        } else {
+            // workspace partial: normalised o, m in base 2, l
+#pragma unroll
+            for (int j = 0; j < DPL; ++j)
+                p.ws_o[slot * D + lane + 32 * j] = o[j];
+            if (lane == 0) {
+                p.ws_ml[2 * slot] = nonempty ? M : -INFINITY;
+                p.ws_ml[2 * slot + 1] = L;
+            }
+            // count the arrival; the last piece of this (b, h) merges all of them
+            unsigned target;
+            int gf = 0;
+            long long off = 0;
+            if (p.decomp == DECOMP_SPLITS) {
+                target = (unsigned)p.P;
+            } else {
+                off = ctx.cumH[s.b] + (long long)s.h * len;
+                gf = bal_owner(off, ctx.T, ctx.Geff);
+                const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
+                target = (unsigned)(gl - gf + 1);
+            }
+            __threadfence();
+            __syncwarp();
+            unsigned old = 0;
+            if (lane == 0)
+                old = atomicInc(p.ws_cnt + bh, target - 1);
+            old = __shfl_sync(FULL_MASK, old, 0);
+            if (old == target - 1) {
+                __threadfence();
+                merge_pieces<D>(p, ctx, bh, target, gf, off, lane);
+            }
+        }
+        ++k;
+        seg_next(p, ctx, s);
+    }
+}
+
+// This lane's slice of the query row of (b, h) = bh, pre-multiplied by the
+// score scale in base 2 and by K's dequantisation scale.
+template <typename C, int D>
+__device__ __forceinline__ void load_q_scaled(const SplitParams &p, int bh, int col, float *qf)
+{
+    load_q<C::VEC>(p.q, p.q_dtype, (long long)bh * D + col * C::VEC, qf);
+    const float qs = p.scale_log2 * (p.k_scale ? __ldg(p.k_scale + bh) : 1.f);
+#pragma unroll
+    for (int i = 0; i < C::VEC; ++i)
+        qf[i] *= qs;
 }
 
 template <typename T, int D>
@@ -610,22 +767,23 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split
 
     unsigned char *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::RING_BYTES);
-    float *red_m = reinterpret_cast<float *>(smem + C::RING_BYTES + C::BAR_BYTES);
-    float *red_l = red_m + C::WARPS;
-    float *red_acc = red_l + C::WARPS;
-    int *flag = reinterpret_cast<int *>(red_acc + C::WARPS * D);
+    float *red = reinterpret_cast<float *>(smem + C::RING_BYTES + C::BAR_BYTES);
     long long *cumH = reinterpret_cast<long long *>(smem + C::RING_BYTES + C::BAR_BYTES + C::RED_BYTES);
     int *lenS = reinterpret_cast<int *>(cumH + p.B + 1);
 
-    const int grp_id = w / C::GW;     // this warp's group
-    const int gw = w % C::GW;         // its index inside the group
-    const bool issuer = (gw == 0);
-    // bars: [GROUPS][STAGES] full, then [GROUPS][STAGES] empty
-    if (issuer && lane == 0) {
-#pragma unroll
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(smem_addr(&bars[grp_id * C::STAGES + s]), 1);
-            mbar_init(smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES + s]), C::GW);
+    // bars: ring full [GROUPS][STAGES], ring empty [GROUPS][STAGES], then
+    // segment full [NBUF] (every streaming lane arrives) and segment free
+    // [NBUF] (the merge warp's lanes arrive)
+    const uint32_t sfull = smem_addr(&bars[2 * C::GROUPS * C::STAGES]);
+    const uint32_t sfree = sfull + C::NBUF * 8;
+    if (tid == 0) {
+        for (int i = 0; i < C::GROUPS * C::STAGES; ++i) {
+            mbar_init(smem_addr(&bars[i]), 1);
+            mbar_init(smem_addr(&bars[C::GROUPS * C::STAGES + i]), C::GW);
+        }
+        for (int i = 0; i < C::NBUF; ++i) {
+            mbar_init(sfull + i * 8, C::WARPS * 32);
+            mbar_init(sfree + i * 8, 32);
         }
     }
 
@@ -638,7 +796,7 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split
     ctx.Geff = 0;
     ctx.beg = ctx.end = 0;
     if (p.decomp == DECOMP_BALANCED) {
-        balanced_setup<C::THREADS, C::WARPS>(p, ctx, cumH, lenS);
+        balanced_setup<C::THREADS, C::WARPS + 1>(p, ctx, cumH, lenS);
         // sequences of length 0 are touched by no CTA: write their result here
         for (long long bh = (long long)ctx.g * C::THREADS + tid; bh < (long long)p.B * p.H;
              bh += (long long)ctx.G * C::THREADS) {
@@ -651,198 +809,148 @@ __global__ void __launch_bounds__(SplitCfg<T, D>::THREADS, FD_CTAS_PER_SM) split
         }
     }
     fence_mbar_init();
-    __syncthreads();
+    __syncthreads();  // the last block-wide barrier: the roles part here
 
-    const uint32_t ring_base = smem_addr(ring) + (uint32_t)(grp_id * C::STAGES * C::STAGE_BYTES);
-    const uint32_t bar_base = smem_addr(&bars[grp_id * C::STAGES]);                 // full
-    const uint32_t ebar_base = smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES]);  // empty
-    const uint32_t my_rows = (uint32_t)(gw * C::WT * C::ROW);  // this warp's rows in a stage
+    // (the streaming warps' code comes first: it is what runs at start-up)
+    if (w < C::MW) {
+        const int grp_id = w / C::GW;     // this warp's group
+        const int gw = w % C::GW;         // its index inside the group
+        const bool issuer = (gw == 0);
+        const uint32_t ring_base = smem_addr(ring) + (uint32_t)(grp_id * C::STAGES * C::STAGE_BYTES);
+        const uint32_t bar_base = smem_addr(&bars[grp_id * C::STAGES]);                 // full
+        const uint32_t ebar_base = smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES]);  // empty
+        const uint32_t my_rows = (uint32_t)(gw * C::WT * C::ROW);  // this warp's rows in a stage
 
-    Producer<C> prod;
-    if (issuer)
-        prod.start(p, ctx, grp_id, lane);
-    int issued = 0;   // chunks issued by this warp (issuers only)
-    int landed = 0;   // chunks whose copies this warp has seen complete
-    bool dead = false;
-    if (issuer) {
-#pragma unroll 1
-        for (int s = 0; s < C::STAGES; ++s) {
-            if (!prod.issue(p, ctx, ring_base + s * C::STAGE_BYTES, bar_base + s * 8, lane))
-                break;
-            ++issued;
+        // The first segment's query row is requested before any K/V copy: behind
+        // the CTAs' first burst of copies its load would wait microseconds.
+        const int qsize = p.q_dtype == 0 ? 4 : 2;
+        Seg cs;
+        seg_first(p, ctx, cs);
+        if (cs.valid) {
+            const int bh0 = cs.b * p.H + cs.h;
+            prefetch_l1(static_cast<const char *>(p.q) + ((long long)bh0 * D + col * C::VEC) * qsize);
+            if (p.k_scale && lane == 0)
+                prefetch_l1(p.k_scale + bh0);
         }
-    }
 
-    Seg cs;
-    seg_first(p, ctx, cs);
-    long long cbase = 0;
-    int consumed = 0;
+        Producer<C> prod;
+        if (issuer)
+            prod.start(p, ctx, grp_id, lane);
+        int issued = 0;   // chunks issued by this warp (issuers only)
+        int landed = 0;   // chunks whose copies this warp has seen complete
+        bool dead = false;
+        if (issuer) {
 #pragma unroll 1
-    while (cs.valid) {
-        const long long nc = seg_chunks<C::CT>(cs);
-        const int bh = cs.b * p.H + cs.h;
-        float qf[C::VEC];
-        {
-            load_q<C::VEC>(p.q, p.q_dtype, (long long)bh * D + col * C::VEC, qf);
-            // score scale, base-2 exponentials, and K's dequantisation scale
-            const float qs = p.scale_log2 * (p.k_scale ? __ldg(p.k_scale + bh) : 1.f);
-#pragma unroll
-            for (int i = 0; i < C::VEC; ++i)
-                qf[i] *= qs;
-        }
-        float m = -INFINITY, l = 0.f, acc[C::VEC];
-#pragma unroll
-        for (int i = 0; i < C::VEC; ++i)
-            acc[i] = 0.f;
-
-        long long c = cbase + ((grp_id - cbase % C::GROUPS) % C::GROUPS + C::GROUPS) % C::GROUPS;
-#pragma unroll 1
-        for (; c < cbase + nc; c += C::GROUPS) {
-            const int stage = consumed % C::STAGES;
-            const uint32_t parity = (consumed / C::STAGES) & 1;
-            ++consumed;
-            if (!dead) {
-                if (mbar_wait_bounded(bar_base + stage * 8, parity))
-                    ++landed;
-                else
-                    dead = true;
-            }
-            int t, ntok_chunk;
-            chunk_coords<C::CT>(cs, c - cbase, t, ntok_chunk);
-            const int ntok = ntok_chunk - gw * C::WT;  // this warp's valid rows
-            const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
-            if (!dead && ntok > 0) {
-                if (ntok >= C::WT)
-                    process_chunk<T, D, true>(kb + my_rows, kb + C::CHUNK_BYTES + my_rows, C::WT,
-                                              grp, col, qf, m, l, acc);
-                else
-                    process_chunk<T, D, false>(kb + my_rows, kb + C::CHUNK_BYTES + my_rows, ntok,
-                                               grp, col, qf, m, l, acc);
-            }
-            __syncwarp();
-            if (C::GW > 1) {
-                // release the stage; the issuer refills it once every warp of
-                // the group has released it
-                if (!dead && lane == 0)
-                    mbar_arrive(ebar_base + stage * 8);
-                if (issuer && !dead && !mbar_wait_bounded(ebar_base + stage * 8, parity))
-                    dead = true;
-            }
-            if (issuer && !dead && prod.issue(p, ctx, kb, bar_base + stage * 8, lane))
+            for (int s = 0; s < C::STAGES; ++s) {
+                if (!prod.issue(p, ctx, ring_base + s * C::STAGE_BYTES, bar_base + s * 8, lane))
+                    break;
                 ++issued;
+            }
         }
 
-        // ---- segment end: merge lane groups, then warps ----
-#pragma unroll
-        for (int o = C::LPT; o < 32; o <<= 1) {
-            float a2[C::VEC];
-            const float m2 = __shfl_xor_sync(FULL_MASK, m, o);
-            const float l2 = __shfl_xor_sync(FULL_MASK, l, o);
+        float qf[C::VEC];
+        if (cs.valid)
+            load_q_scaled<C, D>(p, cs.b * p.H + cs.h, col, qf);
+        long long cbase = 0;
+        int consumed = 0;
+        int k = 0;        // segment ordinal
+#pragma unroll 1
+        while (cs.valid) {
+            const long long nc = seg_chunks<C::CT>(cs);
+            Seg nx = cs;
+            seg_next(p, ctx, nx);
+            if (nx.valid) {
+                // the next segment's query row (and K scale) start loading now
+                const int nbh = nx.b * p.H + nx.h;
+                prefetch_l1(static_cast<const char *>(p.q) + ((long long)nbh * D + col * C::VEC) * qsize);
+                if (p.k_scale && lane == 0)
+                    prefetch_l1(p.k_scale + nbh);
+            }
+            float m = -INFINITY, l = 0.f, acc[C::VEC];
 #pragma unroll
             for (int i = 0; i < C::VEC; ++i)
-                a2[i] = __shfl_xor_sync(FULL_MASK, acc[i], o);
-            merge_state<C::VEC>(m, l, acc, m2, l2, a2);
-        }
-        if (grp == 0) {
-#pragma unroll
-            for (int i = 0; i < C::VEC; ++i)
-                red_acc[w * D + col * C::VEC + i] = acc[i];
-            if (col == 0) {
-                red_m[w] = m;
-                red_l[w] = l;
-            }
-        }
-        __syncthreads();
+                acc[i] = 0.f;
 
-        const int len = (p.decomp == DECOMP_BALANCED) ? lenS[cs.b] : clamp_len(p, cs.b);
-        bool complete;
-        long long slot = 0;
-        if (p.decomp == DECOMP_SPLITS) {
-            complete = (p.P == 1);
-            slot = (long long)bh * p.P + cs.p;
-        } else {
-            complete = (cs.t0 == 0 && cs.t1 == len);
-            slot = 2LL * ctx.g + (cs.k == 0 ? 0 : 1);
-        }
-
-        if (tid < D) {
-            float M = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < C::WARPS; ++i)
-                if (red_l[i] > 0.f)
-                    M = fmaxf(M, red_m[i]);
-            float L = 0.f, O = 0.f;
-#pragma unroll
-            for (int i = 0; i < C::WARPS; ++i) {
-                if (red_l[i] > 0.f) {
-                    const float e = ex2(red_m[i] - M);
-                    L = fmaf(e, red_l[i], L);
-                    O = fmaf(e, red_acc[i * D + tid], O);
+            long long c = cbase + ((grp_id - cbase % C::GROUPS) % C::GROUPS + C::GROUPS) % C::GROUPS;
+#pragma unroll 1
+            for (; c < cbase + nc; c += C::GROUPS) {
+                const int stage = consumed % C::STAGES;
+                const uint32_t parity = (consumed / C::STAGES) & 1;
+                ++consumed;
+                if (!dead) {
+                    if (mbar_wait_bounded(bar_base + stage * 8, parity))
+                        ++landed;
+                    else
+                        dead = true;
                 }
-            }
-            const bool nonempty = L > 0.f;
-            // V's dequantisation scale is common to every row of (b, h)
-            const float vs = p.v_scale ? __ldg(p.v_scale + bh) : 1.f;
-            const float o = nonempty ? O / L * vs : 0.f;
-            if (p.out_kind == OUT_PARTIALS) {
-                p.o_part[slot * D + tid] = o;
-                if (tid == 0) {
-                    p.m_part[slot] = nonempty ? M * LN2_F : -INFINITY;
-                    p.l_part[slot] = L;
-                    if (p.lse_part)
-                        p.lse_part[slot] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+                int t, ntok_chunk;
+                chunk_coords<C::CT>(cs, c - cbase, t, ntok_chunk);
+                const int ntok = ntok_chunk - gw * C::WT;  // this warp's valid rows
+                const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
+                if (!dead && ntok > 0) {
+                    if (ntok >= C::WT)
+                        process_chunk<T, D, true>(kb + my_rows, kb + C::CHUNK_BYTES + my_rows, C::WT,
+                                                  grp, col, qf, m, l, acc);
+                    else
+                        process_chunk<T, D, false>(kb + my_rows, kb + C::CHUNK_BYTES + my_rows, ntok,
+                                                   grp, col, qf, m, l, acc);
                 }
-            } else if (complete) {
-                store_out(p.out, (long long)bh * D + tid, p.out_dtype, o);
-                if (tid == 0 && p.lse)
-                    p.lse[bh] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
-            } else {
-                // workspace partial: normalised o, m in base 2, l
-                p.ws_o[slot * D + tid] = o;
-                if (tid == 0) {
-                    p.ws_ml[2 * slot] = nonempty ? M : -INFINITY;
-                    p.ws_ml[2 * slot + 1] = L;
+                __syncwarp();
+                if (C::GW > 1) {
+                    // release the stage; the issuer refills it once every warp of
+                    // the group has released it
+                    if (!dead && lane == 0)
+                        mbar_arrive(ebar_base + stage * 8);
+                    if (issuer && !dead && !mbar_wait_bounded(ebar_base + stage * 8, parity))
+                        dead = true;
                 }
+                if (issuer && !dead && prod.issue(p, ctx, kb, bar_base + stage * 8, lane))
+                    ++issued;
             }
+
+            // ---- segment end: merge the lane groups, hand the state over ----
+#pragma unroll
+            for (int o = C::LPT; o < 32; o <<= 1) {
+                float a2[C::VEC];
+                const float m2 = __shfl_xor_sync(FULL_MASK, m, o);
+                const float l2 = __shfl_xor_sync(FULL_MASK, l, o);
+#pragma unroll
+                for (int i = 0; i < C::VEC; ++i)
+                    a2[i] = __shfl_xor_sync(FULL_MASK, acc[i], o);
+                merge_state<C::VEC>(m, l, acc, m2, l2, a2);
+            }
+            const int buf = k % C::NBUF;
+            if (!dead && !mbar_wait_bounded(sfree + buf * 8, ((uint32_t)(k / C::NBUF) & 1) ^ 1))
+                dead = true;
+            if (!dead) {
+                float *rm = red + buf * C::SEG_FLOATS;
+                if (grp == 0) {
+#pragma unroll
+                    for (int i = 0; i < C::VEC; ++i)
+                        rm[2 * C::WARPS + w * D + col * C::VEC + i] = acc[i];
+                    if (col == 0) {
+                        rm[w] = m;
+                        rm[C::WARPS + w] = l;
+                    }
+                }
+                mbar_arrive(sfull + buf * 8);  // every lane: releases its own writes
+            }
+            ++k;
+            cbase += nc;
+            cs = nx;
+            if (cs.valid)
+                load_q_scaled<C, D>(p, cs.b * p.H + cs.h, col, qf);
         }
 
-        if (p.out_kind == OUT_FUSED && !complete) {
-            // last piece of this (b, h) to arrive merges all of them
-            unsigned target;
-            int gf = 0;
-            long long off = 0;
-            if (p.decomp == DECOMP_SPLITS) {
-                target = (unsigned)p.P;
-            } else {
-                off = ctx.cumH[cs.b] + (long long)cs.h * len;
-                gf = bal_owner(off, ctx.T, ctx.Geff);
-                const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
-                target = (unsigned)(gl - gf + 1);
-            }
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                const unsigned old = atomicInc(p.ws_cnt + bh, target - 1);
-                *flag = (old == target - 1);
-            }
-            __syncthreads();
-            if (*flag) {
-                __threadfence();
-                merge_pieces<C, D>(p, ctx, bh, target, gf, off, tid, red_m, red_acc);
-            }
+        if (dead) {
+            if (lane == 0)
+                atomicOr(p.status, STATUS_TIMEOUT);
+            // wait (bounded) for this warp's copies still in flight
+            for (int i = landed; i < issued; ++i)
+                mbar_wait_bounded(bar_base + (i % C::STAGES) * 8, (i / C::STAGES) & 1);
         }
-        __syncthreads();
-
-        cbase += nc;
-        seg_next(p, ctx, cs);
-    }
-
-    if (dead) {
-        if (lane == 0)
-            atomicOr(p.status, STATUS_TIMEOUT);
-        // wait (bounded) for this warp's copies still in flight
-        for (int i = landed; i < issued; ++i)
-            mbar_wait_bounded(bar_base + (i % C::STAGES) * 8, (i / C::STAGES) & 1);
+    } else {
+        merge_warp<C, D>(p, ctx, red, sfull, sfree, lane);
     }
 }
 
