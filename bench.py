@@ -79,6 +79,14 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def kernel_name(w, fp8: bool, paged: bool) -> str:
+    """The kernel that does the timed work, as ncu names it."""
+    if w.kv_heads != w.H:
+        return f"fd::gqa_kernel<{w.dtype}, {w.d}>"
+    elt = "e4m3" if fp8 else w.dtype
+    return f"fd::split_kernel<{elt}, {w.d}>" + (" (paged)" if paged else "")
+
+
 def profiled_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     from the current kernel sources on this workload; else None."""
@@ -471,9 +479,10 @@ def run_ours(args, w):
             "pct_of_measured_hbm": 100.0 * value / ws / peaks["hbm_gbs"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": (None if table is not None or k_scale is not None
-                                     else profiled_traffic(w.name)),
-                         "kernel": "split_kernel",
+                         "traffic": (None if table is not None or w.kv_heads != w.H
+                                     else profiled_traffic(w.name + ("+e4m3" if k_scale is not None
+                                                                     else ""))),
+                         "kernel": kernel_name(w, k_scale is not None, table is not None),
                          "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                          "algorithmic_bytes_per_launch": alg, "mean_launch_ms": kern_ms},
             "e2e": e2e,
