@@ -158,16 +158,17 @@ EncodeTiledFn encode_tiled()
     return fn;
 }
 
-// K or V [rows, d] 16-bit as the 3-D map [64 elements, d/64 lines, rows]
-// with boxes of `box_rows` rows and the 128-byte swizzle.
+// K or V [rows, d] 16-bit as the 3-D map [64 elements, rows, d/64 planes]
+// (strides d*2 and 128 bytes) with boxes [64, box_rows, d/64] and the
+// 128-byte swizzle: a box lands in shared memory plane by plane.
 bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long rows, int box_rows)
 {
     EncodeTiledFn fn = encode_tiled();
     if (!fn)
         return false;
-    const cuuint64_t dims[3] = {64, (cuuint64_t)(d / 64), (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {128, (cuuint64_t)d * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)(d / 64), (cuuint32_t)box_rows};
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(d / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)(d / 64)};
     const cuuint32_t es[3] = {1, 1, 1};
     return fn(m, dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,

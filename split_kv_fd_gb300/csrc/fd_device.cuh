@@ -191,7 +191,8 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
 // ---------------------------------------------------------------------------
 
 // 3-D tiled copy global -> shared through a tensor map, completion on `bar`.
-// The innermost coordinate (x) must start on a 16-byte boundary.
+// The innermost coordinate (x) times the element size must be a multiple of
+// 16 bytes.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
                                             uint32_t bar)
 {
@@ -200,6 +201,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+
+// Barrier `id` (1..15) over `count` threads (whole warps) of the block.
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Hint: start fetching the global-memory line holding `ptr` into L1.
@@ -231,12 +238,23 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                  : "r"(addr));
 }
 
+// The transpose of an 8x8 matrix of 16-bit elements held as an mma
+// fragment (lane t holds row t/4, columns 2(t%4) and 2(t%4)+1): afterwards
+// lane t holds row t/4, columns 2(t%4), 2(t%4)+1 of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
+{
+    uint32_t y;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // D = A(16x16) * B(16x8) + D, fp32 accumulate; A, B both bf16 or both f16.
+// (not volatile: a pure function of registers, free to be scheduled)
 template <typename T> struct Mma;
 template <> struct Mma<__nv_bfloat16> {
     __device__ __forceinline__ static void run(float *d, const uint32_t *a, uint32_t b0, uint32_t b1)
     {
-        asm volatile(
+        asm(
             "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
             "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -260,7 +278,7 @@ template <> struct Mma<__nv_bfloat16> {
 template <> struct Mma<__half> {
     __device__ __forceinline__ static void run(float *d, const uint32_t *a, uint32_t b0, uint32_t b1)
     {
-        asm volatile(
+        asm(
             "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
             "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

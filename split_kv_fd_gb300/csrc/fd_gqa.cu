@@ -6,10 +6,90 @@ namespace fd {
 
 // Stage 2 of a (b, kv head) for its G query rows, by the last piece to
 // arrive: the m/l/o merge ("FlashDecoding 数学推导" §2.4.2) of the `target`
-// workspace partials of each row.
+// workspace partials of each row.  All threads: the pieces' slots and (m, l)
+// are staged in shared memory (scr, at least 128 + 130 G floats), the
+// weights exp(m_p - M) l_p formed once per (piece, row), then every output
+// element sums its pieces with all its loads in flight.  Up to MERGE_PB
+// pieces; more go through gqa_merge_pieces_long.
+constexpr int MERGE_PB = 64;
+
 template <typename C, int D>
 __device__ __forceinline__ void gqa_merge_pieces(const SplitParams &p, const Ctx &ctx, int bh, int G,
-                                                 unsigned target, int gf, long long off, int tid)
+                                                 unsigned target, int gf, long long off, int tid,
+                                                 float *scr)
+{
+    constexpr int EMAX = (C::MAXG * D + C::THREADS - 1) / C::THREADS;
+    const int Hq = p.H * G;
+    const int b = bh / p.H, hk = bh % p.H;
+    const int n = (int)target;
+    long long *ss = reinterpret_cast<long long *>(scr);  // [n] workspace slots
+    float *sm = scr + 2 * MERGE_PB;                       // [n][G] m, then the weights
+    float *sw = sm + MERGE_PB * G;                        // [n][G] l
+    float *sM = sw + MERGE_PB * G;                        // [G]
+    float *sL = sM + G;                                   // [G]
+    for (int i = tid; i < n; i += C::THREADS)
+        ss[i] = piece_slot(p, ctx, bh, (unsigned)i, gf, off);
+    __syncthreads();
+    for (int i = tid; i < n * G; i += C::THREADS) {
+        const long long r = ss[i / G] * G + i % G;
+        const float l = __ldcg(p.ws_ml + 2 * r + 1);
+        sm[i] = l > 0.f ? __ldcg(p.ws_ml + 2 * r) : -INFINITY;
+        sw[i] = l;
+    }
+    __syncthreads();
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int i = 0; i < n; ++i)
+            M = fmaxf(M, sm[i * G + tid]);
+        float L = 0.f;
+        for (int i = 0; i < n; ++i) {
+            const float l = sw[i * G + tid];
+            const float e = l > 0.f ? ex2(sm[i * G + tid] - M) * l : 0.f;
+            sm[i * G + tid] = e;   // the weight replaces m
+            L += e;
+        }
+        sM[tid] = M;
+        sL[tid] = L;
+    }
+    __syncthreads();
+    float O[EMAX];
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e)
+        O[e] = 0.f;
+#pragma unroll 2
+    for (int i = 0; i < n; ++i) {
+        const long long s0 = ss[i] * G;
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            const int idx = tid + e * C::THREADS;
+            if (idx < G * D) {
+                const int g = idx / D, dim = idx % D;
+                const float w = sm[i * G + g];
+                if (w > 0.f)
+                    O[e] = fmaf(w, __ldcg(p.ws_o + (s0 + g) * D + dim), O[e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int idx = tid + e * C::THREADS;
+        if (idx < G * D) {
+            const int g = idx / D, dim = idx % D;
+            const float L = sL[g];
+            const long long qrow = (long long)b * Hq + (long long)hk * G + g;
+            const bool nonempty = L > 0.f;
+            store_out(p.out, qrow * D + dim, p.out_dtype, nonempty ? O[e] / L : 0.f);
+            if (dim == 0 && p.lse)
+                p.lse[qrow] = nonempty ? (sM[g] + log2f(L)) * LN2_F : -INFINITY;
+        }
+    }
+}
+
+// The same merge for more than MERGE_PB pieces: each thread walks the
+// pieces for its output elements.
+template <typename C, int D>
+__device__ __forceinline__ void gqa_merge_pieces_long(const SplitParams &p, const Ctx &ctx, int bh, int G,
+                                                      unsigned target, int gf, long long off, int tid)
 {
     const int Hq = p.H * G;
     const int b = bh / p.H, hk = bh % p.H;
@@ -39,7 +119,8 @@ __device__ __forceinline__ void gqa_merge_pieces(const SplitParams &p, const Ctx
     }
 }
 
-template <typename T, int D>
+// NQ: column tiles of 8 query heads (G <= 8: 1; G <= 16: 2).
+template <typename T, int D, int NQ>
 __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __grid_constant__ GqaParams gp)
 {
     using C = GqaCfg<T, D>;
@@ -58,17 +139,13 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
     long long *cumH = reinterpret_cast<long long *>(flag + 4);
     int *lenS = reinterpret_cast<int *>(cumH + p.B + 1);
 
-    const int grp_id = w / C::GW;
-    const int gw = w % C::GW;
-    const bool issuer = (gw == 0);
-    if (issuer && lane == 0) {
-#pragma unroll
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(smem_addr(&bars[grp_id * C::STAGES + s]), 1);
-            mbar_init(smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES + s]), C::GW);
-        }
-    }
+    // bars: full [GROUPS][STAGES] (the issuer's arrival plus the copies'
+    // bytes), then empty [GROUPS][STAGES] (the group's GW warps)
     if (tid == 0) {
+        for (int i = 0; i < C::GROUPS * C::STAGES; ++i) {
+            mbar_init(smem_addr(&bars[i]), 1);
+            mbar_init(smem_addr(&bars[C::GROUPS * C::STAGES + i]), C::GW);
+        }
         prefetch_tmap(&gp.tmk);
         prefetch_tmap(&gp.tmv);
     }
@@ -100,215 +177,245 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
     fence_mbar_init();
     __syncthreads();
 
-    const uint32_t ring_base = smem_addr(smem) + (uint32_t)(grp_id * C::STAGES * C::STAGE_BYTES);
-    const uint32_t bar_base = smem_addr(&bars[grp_id * C::STAGES]);
-    const uint32_t ebar_base = smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES]);
-    const int row0 = gw * C::WT;  // this warp's first row in a stage
+    {
+        const int grp_id = w / C::GW;
+        const int gw = w % C::GW;
+        const bool issuer = (gw == 0);   // the group's first warp also issues its copies
+        const uint32_t ring_base = smem_addr(smem) + (uint32_t)(grp_id * C::STAGES * C::STAGE_BYTES);
+        const uint32_t bar_base = smem_addr(&bars[grp_id * C::STAGES]);
+        const uint32_t ebar_base = smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES]);
+        const int row0 = gw * C::WT;  // this warp's first row in a stage
 
-    TmaProducer<C> prod;
-    int issued = 0, landed = 0;
-    bool dead = false;
-    if (issuer) {
-        prod.start(p, ctx, grp_id);
+        TmaProducer<C> prod;
+        int issued = 0, landed = 0;
+        bool dead = false;
+        if (issuer) {
+            prod.start(p, ctx, grp_id, C::GROUPS);
 #pragma unroll 1
-        for (int s = 0; s < C::STAGES; ++s) {
-            if (!prod.issue(gp, ctx, ring_base + s * C::STAGE_BYTES, bar_base + s * 8, lane))
-                break;
-            ++issued;
-        }
-    }
-
-    const int r0 = lane >> 2;         // this thread's rows r0, r0 + 8
-    const int cb = 2 * (lane & 3);    // and columns cb, cb + 1 of each tile
-    Seg cs;
-    seg_first(p, ctx, cs);
-    long long cbase = 0;
-    int consumed = 0;
-#pragma unroll 1
-    while (cs.valid) {
-        const long long nc = seg_chunks<C::CT>(cs);
-        const int bh = cs.b * p.H + cs.h;
-        // Q of the head group as mma A fragments (rows >= G are zero)
-        uint32_t qa[C::KSTEPS][4];
-        {
-            const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
-            const long long qbase = ((long long)cs.b * Hq + (long long)cs.h * G) * D;  // elements
-#pragma unroll
-            for (int s = 0; s < C::KSTEPS; ++s) {
-                const int col = 16 * s + cb;
-                qa[s][0] = r0 < G ? __ldg(q32 + (qbase + r0 * D + col) / 2) : 0u;
-                qa[s][1] = r0 + 8 < G ? __ldg(q32 + (qbase + (r0 + 8) * D + col) / 2) : 0u;
-                qa[s][2] = r0 < G ? __ldg(q32 + (qbase + r0 * D + col + 8) / 2) : 0u;
-                qa[s][3] = r0 + 8 < G ? __ldg(q32 + (qbase + (r0 + 8) * D + col + 8) / 2) : 0u;
-            }
-        }
-        GqaState<C> st;
-#pragma unroll
-        for (int n = 0; n < C::NT; ++n)
-            st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
-        st.m0 = st.m1 = -INFINITY;
-        st.l0 = st.l1 = 0.f;
-
-        long long c = cbase + ((grp_id - cbase % C::GROUPS) % C::GROUPS + C::GROUPS) % C::GROUPS;
-#pragma unroll 1
-        for (; c < cbase + nc; c += C::GROUPS) {
-            const int stage = consumed % C::STAGES;
-            const uint32_t parity = (consumed / C::STAGES) & 1;
-            ++consumed;
-            if (!dead) {
-                if (mbar_wait_bounded(bar_base + stage * 8, parity))
-                    ++landed;
-                else
-                    dead = true;
-            }
-            int t, ntok_chunk;
-            chunk_coords<C::CT>(cs, c - cbase, t, ntok_chunk);
-            const int nv = ntok_chunk - row0;  // this warp's valid rows
-            const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
-            if (!dead && nv > 0) {
-                if (nv < C::WT) {
-                    // rows past the last token may hold padding: zero them in V
-                    const uint32_t z0 = kb + C::CHUNK_BYTES + (uint32_t)(row0 + nv) * C::ROW;
-                    const int nbytes = (C::WT - nv) * C::ROW;
-                    for (int off = lane * 16; off < nbytes; off += 32 * 16)
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(z0 + off), "r"(0u)
-                                     : "memory");
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                }
-                gqa_chunk<T, C>(kb, kb + C::CHUNK_BYTES, row0, nv, qa, p.scale_log2, lane, st);
-            }
-            __syncwarp();
-            if (!dead && lane == 0)
-                mbar_arrive(ebar_base + stage * 8);
-            if (issuer && !dead && !mbar_wait_bounded(ebar_base + stage * 8, parity))
-                dead = true;
-            if (issuer && !dead && prod.issue(gp, ctx, kb, bar_base + stage * 8, lane))
+            for (int s = 0; s < C::STAGES; ++s) {
+                if (!prod.issue(gp, ctx, ring_base + s * C::STAGE_BYTES, bar_base + s * 8, lane))
+                    break;
                 ++issued;
-        }
-
-        // ---- segment end: full row sums, then merge the warps per row ----
-        st.l0 += __shfl_xor_sync(FULL_MASK, st.l0, 1);
-        st.l0 += __shfl_xor_sync(FULL_MASK, st.l0, 2);
-        st.l1 += __shfl_xor_sync(FULL_MASK, st.l1, 1);
-        st.l1 += __shfl_xor_sync(FULL_MASK, st.l1, 2);
-        {
-            float *rw = red + w * G * (D + 2);
-            if (r0 < G) {
-#pragma unroll
-                for (int n = 0; n < C::NT; ++n) {
-                    rw[r0 * (D + 2) + 8 * n + cb] = st.o[n][0];
-                    rw[r0 * (D + 2) + 8 * n + cb + 1] = st.o[n][1];
-                }
-                if ((lane & 3) == 0) {
-                    rw[r0 * (D + 2) + D] = st.m0;
-                    rw[r0 * (D + 2) + D + 1] = st.l0;
-                }
-            }
-            if (r0 + 8 < G) {
-#pragma unroll
-                for (int n = 0; n < C::NT; ++n) {
-                    rw[(r0 + 8) * (D + 2) + 8 * n + cb] = st.o[n][2];
-                    rw[(r0 + 8) * (D + 2) + 8 * n + cb + 1] = st.o[n][3];
-                }
-                if ((lane & 3) == 0) {
-                    rw[(r0 + 8) * (D + 2) + D] = st.m1;
-                    rw[(r0 + 8) * (D + 2) + D + 1] = st.l1;
-                }
-            }
-        }
-        __syncthreads();
-
-        const int len = (p.decomp == DECOMP_BALANCED) ? lenS[cs.b] : clamp_len(p, cs.b);
-        bool complete;
-        long long slot;
-        if (p.decomp == DECOMP_SPLITS) {
-            complete = (p.P == 1);
-            slot = (long long)bh * p.P + cs.p;
-        } else {
-            complete = (cs.t0 == 0 && cs.t1 == len);
-            slot = 2LL * ctx.g + (cs.k == 0 ? 0 : 1);
-        }
-        for (int idx = tid; idx < G * D; idx += C::THREADS) {
-            const int g = idx / D, dim = idx % D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < C::WARPS; ++i) {
-                const float *ri = red + (i * G + g) * (D + 2);
-                if (ri[D + 1] > 0.f)
-                    M = fmaxf(M, ri[D]);
-            }
-            float L = 0.f, O = 0.f;
-#pragma unroll
-            for (int i = 0; i < C::WARPS; ++i) {
-                const float *ri = red + (i * G + g) * (D + 2);
-                if (ri[D + 1] > 0.f) {
-                    const float e = ex2(ri[D] - M);
-                    L = fmaf(e, ri[D + 1], L);
-                    O = fmaf(e, ri[dim], O);
-                }
-            }
-            const bool nonempty = L > 0.f;
-            const float o = nonempty ? O / L : 0.f;
-            const long long qrow = (long long)cs.b * Hq + (long long)cs.h * G + g;
-            if (complete) {
-                store_out(p.out, qrow * D + dim, p.out_dtype, o);
-                if (dim == 0 && p.lse)
-                    p.lse[qrow] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
-            } else {
-                const long long r = slot * G + g;
-                p.ws_o[r * D + dim] = o;
-                if (dim == 0) {
-                    p.ws_ml[2 * r] = nonempty ? M : -INFINITY;
-                    p.ws_ml[2 * r + 1] = L;
-                }
             }
         }
 
-        if (!complete) {
-            unsigned target;
-            int gf = 0;
-            long long off = 0;
+        const int qn = lane >> 2;          // B fragments: head 8j + lane/4, dims 2(lane%4) (+1, +8, +9)
+        const int qk = 2 * (lane & 3);
+        Seg cs;
+        seg_first(p, ctx, cs);
+        long long cbase = 0;
+        int consumed = 0;
+#pragma unroll 1
+        while (cs.valid) {
+            const long long nc = seg_chunks<C::CT>(cs);
+            const int bh = cs.b * p.H + cs.h;
+            // Q^T of the head group as mma B fragments (heads >= G are zero)
+            uint32_t qb[NQ][C::KSTEPS][2];
+            {
+                const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
+                const long long qbase = ((long long)cs.b * Hq + (long long)cs.h * G) * D;  // elements
+#pragma unroll
+                for (int j = 0; j < NQ; ++j) {
+                    const int n = 8 * j + qn;
+#pragma unroll
+                    for (int s = 0; s < C::KSTEPS; ++s) {
+                        const long long e = qbase + (long long)n * D + 16 * s + qk;
+                        qb[j][s][0] = n < G ? __ldg(q32 + e / 2) : 0u;
+                        qb[j][s][1] = n < G ? __ldg(q32 + (e + 8) / 2) : 0u;
+                    }
+                }
+            }
+            GqaState<C, NQ> st;
+#pragma unroll
+            for (int i = 0; i < C::MT; ++i)
+#pragma unroll
+                for (int j = 0; j < NQ; ++j)
+                    st.o[i][j][0] = st.o[i][j][1] = st.o[i][j][2] = st.o[i][j][3] = 0.f;
+#pragma unroll
+            for (int j = 0; j < NQ; ++j) {
+                st.m[j][0] = st.m[j][1] = -INFINITY;
+                st.l[j][0] = st.l[j][1] = 0.f;
+            }
+
+            long long c = cbase + ((grp_id - cbase % C::GROUPS) % C::GROUPS + C::GROUPS) % C::GROUPS;
+#pragma unroll 1
+            for (; c < cbase + nc; c += C::GROUPS) {
+                const int stage = consumed % C::STAGES;
+                const uint32_t parity = (consumed / C::STAGES) & 1;
+                ++consumed;
+                if (!dead) {
+                    if (mbar_wait_bounded(bar_base + stage * 8, parity))
+                        ++landed;
+                    else
+                        dead = true;
+                }
+                int t, ntok_chunk;
+                chunk_coords<C::CT>(cs, c - cbase, t, ntok_chunk);
+                const int nv = ntok_chunk - row0;  // this warp's valid rows
+                const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
+                if (!dead && nv > 0) {
+                    if (nv < C::WT) {
+                        // rows past the last token may hold padding: zero them in
+                        // every plane of V (a row is 128 contiguous bytes of a plane)
+                        const int nbytes = (C::WT - nv) * 128;
+#pragma unroll
+                        for (int j = 0; j < C::LINES; ++j) {
+                            const uint32_t z0 =
+                                kb + C::CHUNK_BYTES + j * C::PLANE + (uint32_t)(row0 + nv) * 128;
+                            for (int off = lane * 16; off < nbytes; off += 32 * 16)
+                                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(z0 + off), "r"(0u)
+                                             : "memory");
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                    }
+                    gqa_chunk<T, C, NQ>(kb, kb + C::CHUNK_BYTES, row0, nv, qb, p.scale_log2, lane, st);
+                }
+                __syncwarp();
+                // release the stage; the issuer refills it once both warps have
+                if (!dead && lane == 0)
+                    mbar_arrive(ebar_base + stage * 8);
+                if (issuer && !dead && !mbar_wait_bounded(ebar_base + stage * 8, parity))
+                    dead = true;
+                if (issuer && !dead && prod.issue(gp, ctx, kb, bar_base + stage * 8, lane))
+                    ++issued;
+            }
+
+            // ---- segment end: full sums per head, then merge the warps per head ----
+            {
+                float *rw = red + w * G * (D + 2);
+#pragma unroll
+                for (int j = 0; j < NQ; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float l = st.l[j][e];
+                        l += __shfl_xor_sync(FULL_MASK, l, 4);
+                        l += __shfl_xor_sync(FULL_MASK, l, 8);
+                        l += __shfl_xor_sync(FULL_MASK, l, 16);
+                        const int g = 8 * j + qk + e;   // this thread's head
+                        if (g < G) {
+                            float *rg = rw + g * (D + 2);
+#pragma unroll
+                            for (int i = 0; i < C::MT; ++i) {
+                                rg[16 * i + qn] = st.o[i][j][e];
+                                rg[16 * i + qn + 8] = st.o[i][j][e + 2];
+                            }
+                            if (qn == 0) {
+                                rg[D] = st.m[j][e];
+                                rg[D + 1] = l;
+                            }
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+
+            const int len = (p.decomp == DECOMP_BALANCED) ? lenS[cs.b] : clamp_len(p, cs.b);
+            bool complete;
+            long long slot;
             if (p.decomp == DECOMP_SPLITS) {
-                target = (unsigned)p.P;
+                complete = (p.P == 1);
+                slot = (long long)bh * p.P + cs.p;
             } else {
-                off = ctx.cumH[cs.b] + (long long)cs.h * len;
-                gf = bal_owner(off, ctx.T, ctx.Geff);
-                const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
-                target = (unsigned)(gl - gf + 1);
+                complete = (cs.t0 == 0 && cs.t1 == len);
+                slot = 2LL * ctx.g + (cs.k == 0 ? 0 : 1);
             }
-            __threadfence();
+            // warp w merges heads w, w + WARPS, ...: the head's max, weights and
+            // sum once per lane, then its dims lane, lane + 32, ...
+            for (int g = w; g < G; g += C::WARPS) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < C::WARPS; ++i) {
+                    const float *ri = red + (i * G + g) * (D + 2);
+                    if (ri[D + 1] > 0.f)
+                        M = fmaxf(M, ri[D]);
+                }
+                float L = 0.f, e[C::WARPS];
+#pragma unroll
+                for (int i = 0; i < C::WARPS; ++i) {
+                    const float *ri = red + (i * G + g) * (D + 2);
+                    e[i] = ri[D + 1] > 0.f ? ex2(ri[D] - M) : 0.f;
+                    L = fmaf(e[i], ri[D + 1], L);
+                }
+                const bool nonempty = L > 0.f;
+                const long long qrow = (long long)cs.b * Hq + (long long)cs.h * G + g;
+                const long long r = slot * G + g;
+#pragma unroll
+                for (int dd = 0; dd < D / 32; ++dd) {
+                    const int dim = lane + 32 * dd;
+                    float O = 0.f;
+#pragma unroll
+                    for (int i = 0; i < C::WARPS; ++i)
+                        O = fmaf(e[i], red[(i * G + g) * (D + 2) + dim], O);
+                    const float o = nonempty ? O / L : 0.f;
+                    if (complete)
+                        store_out(p.out, qrow * D + dim, p.out_dtype, o);
+                    else
+                        p.ws_o[r * D + dim] = o;
+                }
+                if (lane == 0) {
+                    if (complete) {
+                        if (p.lse)
+                            p.lse[qrow] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+                    } else {
+                        p.ws_ml[2 * r] = nonempty ? M : -INFINITY;
+                        p.ws_ml[2 * r + 1] = L;
+                    }
+                }
+            }
+
+            if (!complete) {
+                unsigned target;
+                int gf = 0;
+                long long off = 0;
+                if (p.decomp == DECOMP_SPLITS) {
+                    target = (unsigned)p.P;
+                } else {
+                    off = ctx.cumH[cs.b] + (long long)cs.h * len;
+                    gf = bal_owner(off, ctx.T, ctx.Geff);
+                    const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
+                    target = (unsigned)(gl - gf + 1);
+                }
+                // the barrier orders every thread's partial before thread 0's
+                // fence and arrival
+                __syncthreads();
+                if (tid == 0) {
+                    __threadfence();
+                    const unsigned old = atomicInc(p.ws_cnt + bh, target - 1);
+                    *flag = (old == target - 1);
+                }
+                __syncthreads();
+                if (*flag) {
+                    __threadfence();
+                    // red is free again: every thread has passed its reads
+                    if (target <= (unsigned)MERGE_PB)
+                        gqa_merge_pieces<C, D>(p, ctx, bh, G, target, gf, off, tid, red);
+                    else
+                        gqa_merge_pieces_long<C, D>(p, ctx, bh, G, target, gf, off, tid);
+                }
+            }
             __syncthreads();
-            if (tid == 0) {
-                const unsigned old = atomicInc(p.ws_cnt + bh, target - 1);
-                *flag = (old == target - 1);
-            }
-            __syncthreads();
-            if (*flag) {
-                __threadfence();
-                gqa_merge_pieces<C, D>(p, ctx, bh, G, target, gf, off, tid);
-            }
+
+            cbase += nc;
+            seg_next(p, ctx, cs);
         }
-        __syncthreads();
 
-        cbase += nc;
-        seg_next(p, ctx, cs);
-    }
-
-    if (dead) {
-        if (lane == 0)
-            atomicOr(p.status, STATUS_TIMEOUT);
-        for (int i = landed; i < issued; ++i)
-            mbar_wait_bounded(bar_base + (i % C::STAGES) * 8, (i / C::STAGES) & 1);
+        if (dead) {
+            if (lane == 0)
+                atomicOr(p.status, STATUS_TIMEOUT);
+            // wait (bounded) for this warp's copies still in flight
+            for (int i = landed; i < issued; ++i)
+                mbar_wait_bounded(bar_base + (i % C::STAGES) * 8, (i / C::STAGES) & 1);
+        }
     }
 }
 
-template <typename T, int D>
+template <typename T, int D, int NQ>
 static cudaError_t launch_gqa_t(const GqaParams &gp, cudaStream_t s)
 {
     using C = GqaCfg<T, D>;
     const size_t smem = C::smem_bytes(gp.s.decomp, gp.s.B, gp.G);
-    auto kern = gqa_kernel<T, D>;
+    auto kern = gqa_kernel<T, D, NQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
@@ -316,11 +423,17 @@ static cudaError_t launch_gqa_t(const GqaParams &gp, cudaStream_t s)
     return cudaGetLastError();
 }
 
+template <typename T, int D>
+static cudaError_t launch_gqa_d(const GqaParams &gp, cudaStream_t s)
+{
+    return gp.G <= 8 ? launch_gqa_t<T, D, 1>(gp, s) : launch_gqa_t<T, D, 2>(gp, s);
+}
+
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s)
 {
     if (dtype == 2)
-        return d == 64 ? launch_gqa_t<__nv_bfloat16, 64>(gp, s) : launch_gqa_t<__nv_bfloat16, 128>(gp, s);
-    return d == 64 ? launch_gqa_t<__half, 64>(gp, s) : launch_gqa_t<__half, 128>(gp, s);
+        return d == 64 ? launch_gqa_d<__nv_bfloat16, 64>(gp, s) : launch_gqa_d<__nv_bfloat16, 128>(gp, s);
+    return d == 64 ? launch_gqa_d<__half, 64>(gp, s) : launch_gqa_d<__half, 128>(gp, s);
 }
 
 }  // namespace fd

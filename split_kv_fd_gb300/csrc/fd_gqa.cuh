@@ -3,16 +3,30 @@
 // ("从第一性原理推导 Flash Attention" §8).  Per (b, kv head) the work is a
 // small dense contraction: scores S[G x T] = Q[G x d] K[T x d]^T and
 // O[G x d] = P[G x T] V[T x d] over each chunk of T tokens, so it runs on the
-// tensor cores (mma.sync m16n8k16, fp32 accumulate; G padded to 16 rows).
-// The K/V bytes are still read exactly once and the path stays HBM-bound:
-// at G = 8 it needs ~8 flop per byte, far below the tensor rate.
+// tensor cores (mma.sync m16n8k16, fp32 accumulate).  The K/V bytes are still
+// read exactly once and the path stays HBM-bound: at G = 8 it needs ~8 flop
+// per byte, far below the tensor rate.
+//
+// The products are taken transposed, S^T = K Q^T and O^T = V^T P^T, so the
+// 16-row side of the MMA is tokens (for S^T) or head dimensions (for O^T)
+// and the 8-column side holds the query heads: a group of up to 8 heads (16
+// with two column tiles) wastes no MMA rows, and the accumulators are half
+// the size of the untransposed form's.  The score accumulator of S^T holds
+// P^T in the layout of an 8x8 transpose of the B operand of O^T = V^T P^T,
+// so P reaches the second product through movmatrix, without shared memory.
 //
 // Same decomposition, rings and merges as the split kernel (fd_split.cuh);
 // what differs:
 //  - K/V chunks arrive through tensor-map TMA (cp.async.bulk.tensor.3d) with
-//    the 128-byte swizzle, so ldmatrix reads them without bank conflicts.
-//    A row of d elements is viewed as d/64 lines of 128 bytes: the map is
-//    [64 elements, d/64 lines, rows], box [64, d/64, CT rows].
+//    the 128-byte swizzle.  A stage holds a chunk as d/64 planes, plane j
+//    being elements [64j, 64j + 64) of the CT rows, 128 bytes per row: the
+//    map views K (or V) as [64 elements, rows, d/64 planes] (strides d*2 and
+//    128 bytes) and one box [64, CT, d/64] fetches a whole chunk.  With
+//    128-byte rows the swizzle gives any 8 consecutive rows of a column 8
+//    different bank groups, so the ldmatrix reads are free of bank conflicts
+//    (rows of d = 128 kept whole, 256 bytes, would repeat the pattern every 4
+//    rows: 2-way conflicts).  One copy per chunk and operand keeps the TMA
+//    instruction count low: issuing a copy costs the issuing thread ~70 ns.
 //  - P is split into a bf16/f16 high part and the low part of its residual
 //    (P = P_hi + P_lo), so P.V keeps close to fp32 accuracy with 16-bit MMA
 //    operands.
@@ -29,26 +43,30 @@ namespace fd {
 #ifndef FD_GQA_STAGES
 #define FD_GQA_STAGES 2
 #endif
+#ifndef FD_GQA_GW
+#define FD_GQA_GW 2
+#endif
 
 template <typename T, int D> struct GqaCfg {
     static constexpr int ROW = D * 2;              // bytes per token row (16-bit types)
     static constexpr int LINES = D / 64;           // 128-byte lines per row
     static constexpr int WARPS = 8;
     static constexpr int THREADS = WARPS * 32;
-    static constexpr int GW = 2;                   // warps sharing one ring
+    static constexpr int GW = FD_GQA_GW;           // warps sharing one ring
     static constexpr int GROUPS = WARPS / GW;
     static constexpr int STAGES = FD_GQA_STAGES;
     static constexpr int WT = 16;                  // tokens per warp per chunk (one PV k-step)
     static constexpr int CT = GW * WT;             // tokens per chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // one of K or V
+    static constexpr int PLANE = CT * 128;         // one 64-element plane of a chunk
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
     static constexpr int RING_BYTES = GROUPS * STAGES * STAGE_BYTES;
     static constexpr int BAR_BYTES = GROUPS * STAGES * 2 * 8;
-    static constexpr int KSTEPS = D / 16;          // k-steps of Q.K^T
-    static constexpr int NT = D / 8;               // 8-wide n-tiles of O
+    static constexpr int KSTEPS = D / 16;          // k-steps of S^T = K Q^T
+    static constexpr int MT = D / 16;              // 16-row tiles of O^T
     static constexpr int MAXG = 16;
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(CHUNK_BYTES % 1024 == 0, "stages stay 1024-byte aligned for the swizzle");
+    static_assert(PLANE % 1024 == 0, "planes stay 1024-byte aligned for the swizzle");
 
     // dynamic shared memory: 1024 of alignment slack, ring, barriers, the
     // warps' (o, m, l) for the merge, a flag, and the balanced prefix sums
@@ -62,7 +80,7 @@ template <typename T, int D> struct GqaCfg {
 };
 
 struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
-    CUtensorMap tmk;   // K as [64, d/64, B*Hkv*N] 16-bit elements, 128B swizzle
+    CUtensorMap tmk;   // K as [64, B*Hkv*N, d/64] 16-bit elements, boxes [64, CT, d/64], 128B swizzle
     CUtensorMap tmv;   // V likewise
     SplitParams s;     // s.H = Hkv; s.q is [B, Hkv*G, d]; outputs [B, Hkv*G, ...]
     int G;             // query heads per K/V head, 2..16
@@ -70,22 +88,23 @@ struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
 
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s);
 
-// Byte offset of 16-byte chunk c of row r in a stage laid out by the 128B
-// swizzle (stage base 1024-aligned): line = r*LINES + c/8, and the chunk's
-// position within its 128-byte line is (c % 8) XOR (line % 8).
-template <int LINES>
+// Byte offset of 16-byte column c of row r in a stage of 64-element planes
+// written by the 128B swizzle (stage base 1024-aligned): plane c/8, and
+// within the plane's 128-byte row r, position (c % 8) XOR (r % 8).
+template <int PLANE>
 __device__ __forceinline__ uint32_t swz(int r, int c)
 {
-    const int line = r * LINES + (c >> 3);
-    return (uint32_t)(line * 128 + (((c & 7) ^ (line & 7)) << 4));
+    return (uint32_t)((c >> 3) * PLANE + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// The group's producer: the chunk walk of the split kernel's producer, with
-// each chunk fetched as one K box and one V box through the tensor maps.
+// The chunk walk of the split kernel's producer over the CTA's chunks c =
+// first, first + stride, ..., each chunk fetched as d/64 K boxes and d/64 V
+// boxes through the tensor maps.
 template <typename C> struct TmaProducer {
     Seg s;
     long long base;
     long long c;
+    int stride;
     bool have;
     int t, ntok;
 
@@ -100,11 +119,12 @@ template <typename C> struct TmaProducer {
             chunk_coords<C::CT>(s, c - base, t, ntok);
     }
 
-    __device__ __forceinline__ void start(const SplitParams &p, const Ctx &ctx, int first)
+    __device__ __forceinline__ void start(const SplitParams &p, const Ctx &ctx, int first, int step)
     {
         seg_first(p, ctx, s);
         base = 0;
         c = first;
+        stride = step;
         locate(p, ctx);
     }
 
@@ -118,115 +138,108 @@ template <typename C> struct TmaProducer {
             const SplitParams &p = gp.s;
             const int row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
             mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
-            tma_load_3d(kdst, &gp.tmk, 0, 0, row, bar);
-            tma_load_3d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, 0, row, bar);
+            tma_load_3d(kdst, &gp.tmk, 0, row, 0, bar);
+            tma_load_3d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, row, 0, bar);
         }
-        c += C::GROUPS;
+        c += stride;
         locate(gp.s, ctx);
         return true;
     }
 };
 
-// Per-warp softmax state for the 16 (padded) query rows: this thread holds
-// rows r0 = lane/4 and r1 = r0 + 8, and columns 2*(lane%4)+{0,1} of every
-// 8-wide tile of O (the mma accumulator layout).
-template <typename C> struct GqaState {
-    float o[C::NT][4];
-    float m0, m1;   // running max (base 2)
-    float l0, l1;   // this thread's share of the running sums
+// Per-warp softmax state.  Query heads are the columns of S^T and O^T: in
+// column tile j this thread has heads 8j + 2(lane%4) + {0, 1}, and of O^T
+// the head dimensions 16i + lane/4 (+ 8) of every 16-row tile i (the mma
+// accumulator layout).  m and l are per head; l is this thread's share.
+template <typename C, int NQ> struct GqaState {
+    float o[C::MT][NQ][4];
+    float m[NQ][2];   // running max (base 2)
+    float l[NQ][2];   // this thread's share of the running sums
 };
 
-// One warp's WT rows of a chunk (rows row0 .. row0+WT-1 of the stage, the
-// first `nvalid` of them real tokens): S = Q K^T on the tensor cores, the
-// block-wise online-softmax update in fp32, then O += (P_hi + P_lo) V.
-template <typename T, typename C>
+// One warp's WT = 16 rows of a chunk (rows row0 .. row0+15 of the stage, the
+// first `nvalid` of them real tokens): S^T = K Q^T on the tensor cores, the
+// block-wise online-softmax update in fp32, then O^T += V^T (P_hi + P_lo)^T.
+// qb holds Q^T as B fragments: qb[j][s] = heads of column tile j, k-step s.
+template <typename T, typename C, int NQ>
 __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int row0, int nvalid,
-                                          const uint32_t (*qa)[4], float scale_log2, int lane,
-                                          GqaState<C> &st)
+                                          const uint32_t (*qb)[C::KSTEPS][2], float scale_log2, int lane,
+                                          GqaState<C, NQ> &st)
 {
-    // scores for 2 tiles of 8 tokens; even and odd k-steps accumulate
+    // S^T for the warp's 16 tokens; even and odd k-steps accumulate
     // separately so the dependent MMA chains are half as long
-    float sc[2][4], sx[2][4];
+    float sc[NQ][4], sx[NQ][4];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < NQ; ++j) {
         sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
         sx[j][0] = sx[j][1] = sx[j][2] = sx[j][3] = 0.f;
     }
+    const int ktok = row0 + (lane & 15);
 #pragma unroll
-    for (int s2 = 0; s2 < C::KSTEPS / 2; ++s2) {
+    for (int s = 0; s < C::KSTEPS; ++s) {
+        uint32_t a[4];
+        ldsm_x4(kstage + swz<C::PLANE>(ktok, 2 * s + (lane >> 4)), a[0], a[1], a[2], a[3]);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int tok = row0 + 8 * j + (lane & 7);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kstage + swz<C::LINES>(tok, 4 * s2 + (lane >> 3)), b0, b1, b2, b3);
-            Mma<T>::run(sc[j], qa[2 * s2], b0, b1);
-            Mma<T>::run(sx[j], qa[2 * s2 + 1], b2, b3);
+        for (int j = 0; j < NQ; ++j)
+            Mma<T>::run((s & 1) ? sx[j] : sc[j], a, qb[j][s][0], qb[j][s][1]);
+    }
+    // base-2 scale; tokens lane/4 and lane/4 + 8 past the last valid one are masked
+    const int r = lane >> 2;
+    const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+        sc[j][0] = v0 ? (sc[j][0] + sx[j][0]) * scale_log2 : -INFINITY;
+        sc[j][1] = v0 ? (sc[j][1] + sx[j][1]) * scale_log2 : -INFINITY;
+        sc[j][2] = v1 ? (sc[j][2] + sx[j][2]) * scale_log2 : -INFINITY;
+        sc[j][3] = v1 ? (sc[j][3] + sx[j][3]) * scale_log2 : -INFINITY;
+    }
+    // per head: the max over the chunk's 16 tokens (a head's tokens live in
+    // the 8 lanes with the same lane % 4), the rescale, and P
+    uint32_t ph[NQ][2], pl[NQ][2];
+#pragma unroll
+    for (int j = 0; j < NQ; ++j) {
+        float x0 = fmaxf(sc[j][0], sc[j][2]), x1 = fmaxf(sc[j][1], sc[j][3]);
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+            x0 = fmaxf(x0, __shfl_xor_sync(FULL_MASK, x0, o));
+            x1 = fmaxf(x1, __shfl_xor_sync(FULL_MASK, x1, o));
         }
-    }
+        const float mn0 = fmaxf(st.m[j][0], x0), mn1 = fmaxf(st.m[j][1], x1);  // finite: nvalid >= 1
+        const float a0 = ex2(st.m[j][0] - mn0), a1 = ex2(st.m[j][1] - mn1);
+        st.m[j][0] = mn0;
+        st.m[j][1] = mn1;
+        const float p0 = ex2(sc[j][0] - mn0), p1 = ex2(sc[j][1] - mn1);
+        const float p2 = ex2(sc[j][2] - mn0), p3 = ex2(sc[j][3] - mn1);
+        st.l[j][0] = st.l[j][0] * a0 + (p0 + p2);
+        st.l[j][1] = st.l[j][1] * a1 + (p1 + p3);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            sc[j][e] += sx[j][e];
-    }
-    // base-2 scale and the mask of rows past the last valid token
-    const int colb = 2 * (lane & 3);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int tok = 8 * j + colb + (e & 1);
-            sc[j][e] = tok < nvalid ? sc[j][e] * scale_log2 : -INFINITY;
+        for (int i = 0; i < C::MT; ++i) {
+            st.o[i][j][0] *= a0;
+            st.o[i][j][1] *= a1;
+            st.o[i][j][2] *= a0;
+            st.o[i][j][3] *= a1;
         }
+        // P^T blocks (tokens 0-7 | 8-15) x (8 heads) as 16-bit pairs, high
+        // part and the low part of its residual, turned into B fragments
+        const uint32_t h0 = Mma<T>::pack(p0, p1), h1 = Mma<T>::pack(p2, p3);
+        const float2 u0 = Mma<T>::unpack(h0), u1 = Mma<T>::unpack(h1);
+        const uint32_t l0 = Mma<T>::pack(p0 - u0.x, p1 - u0.y), l1 = Mma<T>::pack(p2 - u1.x, p3 - u1.y);
+        ph[j][0] = movmatrix_t(h0);
+        ph[j][1] = movmatrix_t(h1);
+        pl[j][0] = movmatrix_t(l0);
+        pl[j][1] = movmatrix_t(l1);
     }
-    // row maxima over the chunk's 16 tokens (a row lives in a quad of lanes)
-    float x0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-    float x1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+    // O^T += V^T P^T: V^T tiles (16 dims x 16 tokens) through ldmatrix.trans
+    const int vtok = row0 + (lane & 7) + 8 * (lane >> 4);
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(FULL_MASK, x0, o));
-        x1 = fmaxf(x1, __shfl_xor_sync(FULL_MASK, x1, o));
-    }
-    const float mn0 = fmaxf(st.m0, x0), mn1 = fmaxf(st.m1, x1);  // finite: nvalid >= 1
-    const float a0 = ex2(st.m0 - mn0), a1 = ex2(st.m1 - mn1);
-    st.m0 = mn0;
-    st.m1 = mn1;
-    float pr[2][4];
+    for (int i = 0; i < C::MT; ++i) {
+        uint32_t a[4];
+        ldsm_x4_t(vstage + swz<C::PLANE>(vtok, 2 * i + ((lane >> 3) & 1)), a[0], a[1], a[2], a[3]);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        pr[j][0] = ex2(sc[j][0] - mn0);
-        pr[j][1] = ex2(sc[j][1] - mn0);
-        pr[j][2] = ex2(sc[j][2] - mn1);
-        pr[j][3] = ex2(sc[j][3] - mn1);
-    }
-    st.l0 = st.l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-    st.l1 = st.l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-#pragma unroll
-    for (int n = 0; n < C::NT; ++n) {
-        st.o[n][0] *= a0;
-        st.o[n][1] *= a0;
-        st.o[n][2] *= a1;
-        st.o[n][3] *= a1;
-    }
-    // P as the A operand of P.V: P = P_hi + P_lo, both 16-bit
-    uint32_t ph[4], pl[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int j = i >> 1, e = (i & 1) * 2;  // (tile j, rows r0 | r1)
-        ph[i] = Mma<T>::pack(pr[j][e], pr[j][e + 1]);
-        const float2 h = Mma<T>::unpack(ph[i]);
-        pl[i] = Mma<T>::pack(pr[j][e] - h.x, pr[j][e + 1] - h.y);
-    }
-    // O += P V over this warp's 16 rows: V tiles through ldmatrix.trans
-    const int vtok = row0 + 8 * ((lane >> 3) & 1) + (lane & 7);
-#pragma unroll
-    for (int n2 = 0; n2 < C::NT / 2; ++n2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vstage + swz<C::LINES>(vtok, 2 * n2 + (lane >> 4)), b0, b1, b2, b3);
-        Mma<T>::run(st.o[2 * n2], ph, b0, b1);
-        Mma<T>::run(st.o[2 * n2], pl, b0, b1);
-        Mma<T>::run(st.o[2 * n2 + 1], ph, b2, b3);
-        Mma<T>::run(st.o[2 * n2 + 1], pl, b2, b3);
+        for (int j = 0; j < NQ; ++j) {
+            Mma<T>::run(st.o[i][j], a, ph[j][0], ph[j][1]);
+            Mma<T>::run(st.o[i][j], a, pl[j][0], pl[j][1]);
+        }
     }
 }
 
