@@ -91,9 +91,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 }
 
 // Bounded wait for a phase that may take long (a whole segment of
-// streaming), for a warp that must not slow the warps doing the work: it
-// tests the phase without blocking and sleeps `sleep_ns` between tests.
-__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity, uint32_t sleep_ns)
+// streaming), for a warp that must not slow the warps doing the work: each
+// try suspends the warp in hardware for up to `hint_ns` and resumes it as
+// soon as the phase completes.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
 {
     const unsigned long long t0 = global_ns();
     bool ok = false;
@@ -101,10 +102,10 @@ __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t p
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "r"(hint_ns)
             : "memory");
         if (done) {
             ok = true;
@@ -112,7 +113,6 @@ __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t p
         }
         if (global_ns() - t0 > WAIT_LIMIT_NS)
             break;
-        __nanosleep(sleep_ns);
     }
     return __all_sync(FULL_MASK, ok);
 }

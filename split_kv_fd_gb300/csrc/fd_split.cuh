@@ -593,11 +593,12 @@ __device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ct
         const float e = l > 0.f ? ex2(m - M) * l : 0.f;
         L += e;
         const int n = (int)min(32u, target - base);
-        // 16 pieces' rows in flight at a time
-        for (int i0 = 0; i0 < n; i0 += 16) {
-            float x[16][DPL], ei[16];
+        // 4 pieces' rows in flight at a time (a larger batch only adds code,
+        // fetched cold from memory when the merge runs once per sequence)
+        for (int i0 = 0; i0 < n; i0 += 4) {
+            float x[4][DPL], ei[4];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 ei[u] = __shfl_sync(FULL_MASK, e, i0 + u);
                 const long long si = __shfl_sync(FULL_MASK, sl, i0 + u);
 #pragma unroll
@@ -605,7 +606,7 @@ __device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ct
                     x[u][j] = (i0 + u < n) ? __ldcg(p.ws_o + si * D + lane + 32 * j) : 0.f;
             }
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 4; ++u) {
 #pragma unroll
                 for (int j = 0; j < DPL; ++j)
                     O[j] = ei[u] > 0.f ? fmaf(ei[u], x[u][j], O[j]) : O[j];
@@ -655,7 +656,7 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
         const float vs = p.v_scale ? __ldg(p.v_scale + bh) : 1.f;
 
         const int buf = k % C::NBUF;
-        if (!mbar_wait_bounded_sleep(sfull + buf * 8, (uint32_t)(k / C::NBUF) & 1, 256)) {
+        if (!mbar_wait_bounded_sleep(sfull + buf * 8, (uint32_t)(k / C::NBUF) & 1, 1000000)) {
             if (lane == 0)
                 atomicOr(p.status, STATUS_TIMEOUT);
             return;
