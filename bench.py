@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -71,11 +72,17 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the split kernel's code: its sources without comments and
+    with whitespace collapsed, so that editing a comment keeps the ncu
+    records taken from the same code valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "split_kv_fd_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -25,8 +25,13 @@
 // updated once per chunk in the block form of the online-softmax update
 // (running max, rescale by exp(m_old - m_new), unnormalised accumulator),
 // with scores in base 2 (q pre-multiplied by scale*log2(e)) so that the
-// exponentials are single ex2 instructions.  At a segment end the warps'
-// states are merged through shared memory (the m/l/o merge).
+// exponentials are single ex2 instructions.  At a segment end each
+// streaming warp hands its state to the CTA's merge warp through one of
+// NBUF shared-memory buffers and goes on with the next segment; the merge
+// warp merges the warps' states (the m/l/o merge), writes the result and,
+// for a (b, h) split across CTAs, runs the last arriver's merge of the
+// pieces.  No streaming warp waits for a merge, and after the set-up there
+// is no block-wide barrier.
 #pragma once
 
 #include "fd_device.cuh"
