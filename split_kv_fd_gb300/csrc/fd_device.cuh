@@ -8,6 +8,8 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace fd {
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
