@@ -283,7 +283,7 @@ def run_reference(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, "auto", args.page_size, args.kv_dtype),
+        "config": config_of(w, w.num_splits or "auto", args.page_size, args.kv_dtype),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {rows} of {w.B * w.kv_heads} (b, kv head) rows of {w.name}, "
                                    f"full length, drawn on the host with the workload's "
@@ -294,8 +294,8 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w, num_splits, page_size=0, kv_dtype="native"):
-    return {"workload": w.name, "batch": w.B, "heads": w.H, "kv_heads": w.kv_heads,
+def config_of(w, num_splits, page_size=0, kv_dtype="native", path="fused"):
+    return {"workload": w.name, "path": path, "batch": w.B, "heads": w.H, "kv_heads": w.kv_heads,
             "kv_len": w.N, "head_dim": w.d,
             "kv_dtype": (w.dtype if kv_dtype == "native"
                          else f"e4m3 with per-(b,h) scales (q {w.dtype})"),
@@ -337,28 +337,45 @@ def run_ours(args, w):
         k, v, table = to_paged(k, v, args.page_size, seed=w.seed)
         torch.cuda.empty_cache()
 
-    def decode(out, lse, stream):
+    # the two-call form: fd_decode_split then a combine, with its own split count
+    P_split = 0
+    if args.path != "fused":
+        P_split = args.num_splits or w.num_splits or fd.auto_num_splits(w.B, w.H, w.N, w.d)
+    # fused: the workload's split count, else the automatic decomposition (0)
+    P_fused = args.num_splits or w.num_splits
+
+    def decode(out, lse, stream, mid=None):
+        if args.path != "fused":
+            o_p, m_p, l_p, s_p = fd.decode_split(q, k, v, P_split, seqlens=lens, scale=w.scale,
+                                                 stream=stream)
+            if mid is not None:
+                mid.record(stream)
+            if args.path == "split-mlo":
+                fd.combine_mlo(o_p, m_p, l_p, out=out, lse=lse, stream=stream)
+            else:
+                fd.combine_lse(o_p, s_p, out=out, lse=lse, stream=stream)
+            return
         if w.kv_heads != w.H:
-            fd.decode_gqa(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
+            fd.decode_gqa(q, k, v, lens, num_splits=P_fused, scale=w.scale, out=out, lse=lse,
                           workspace=wsbuf, stream=stream)
         elif k_scale is not None:
-            fd.decode_fp8(q, k, v, k_scale, v_scale, seqlens=lens, num_splits=0, scale=w.scale,
+            fd.decode_fp8(q, k, v, k_scale, v_scale, seqlens=lens, num_splits=P_fused, scale=w.scale,
                           out=out, lse=lse, workspace=wsbuf, stream=stream)
         elif table is None:
-            fd.decode(q, k, v, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
+            fd.decode(q, k, v, lens, num_splits=P_fused, scale=w.scale, out=out, lse=lse,
                       workspace=wsbuf, stream=stream)
         else:
-            fd.decode_paged(q, k, v, table, lens, num_splits=0, scale=w.scale, out=out, lse=lse,
+            fd.decode_paged(q, k, v, table, lens, num_splits=P_fused, scale=w.scale, out=out, lse=lse,
                             workspace=wsbuf, stream=stream)
     out = torch.empty((w.B, w.H, w.d), dtype=getattr(torch, {"bf16": "bfloat16", "f16": "float16",
                                                             "f32": "float32"}[w.out_dtype]),
                       device=dev)
     lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
     if w.kv_heads != w.H:
-        wsbuf = torch.empty(max(256, fd.workspace_size_gqa(w.B, w.H, w.kv_heads, w.N, w.d, 0)),
+        wsbuf = torch.empty(max(256, fd.workspace_size_gqa(w.B, w.H, w.kv_heads, w.N, w.d, P_fused)),
                             dtype=torch.uint8, device=dev)
     else:
-        wsbuf = fd.new_workspace(w.B, w.H, w.N, w.d, 0, device=dev)
+        wsbuf = fd.new_workspace(w.B, w.H, w.N, w.d, P_fused, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = None
     if 2 * w.B * w.kv_heads * w.N * w.d * EB[w.dtype] <= 4 * L2_BYTES:
@@ -386,6 +403,8 @@ def run_ours(args, w):
     time.sleep(0.25)  # the sampler's first row
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) if args.path != "fused" else None
+            for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(ws)
@@ -396,7 +415,7 @@ def run_ours(args, w):
         if flush is not None:
             do_flush()
         evs[i][0].record(stream)
-        decode(out, lse, stream)
+        decode(out, lse, stream, mids[i])
         evs[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -405,12 +424,17 @@ def run_ours(args, w):
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [a.elapsed_time(b) for a, b in evs]
+    combine_ms = None
+    if args.path != "fused":
+        # the dominant kernel is the split kernel; the combine is timed apart
+        combine_ms = statistics.mean(m.elapsed_time(b) for m, (_, b) in zip(mids, evs))
+        split_ms = [a.elapsed_time(m) for m, (a, _) in zip(mids, evs)]
     if flush is not None:
         # the flush runs between the steps, outside their events: a step's
         # time is its own events' interval
         total_ms = sum(launch_ms)
     total_ms = reduce_max(total_ms, ws, dev)
-    kern_ms = statistics.mean(launch_ms)
+    kern_ms = statistics.mean(launch_ms if args.path == "fused" else split_ms)
 
     kvb = kv_bytes(w, lens_h)
     if k_scale is not None:  # one byte per element, plus the scales
@@ -423,6 +447,9 @@ def run_ours(args, w):
         alg = alg - kv_bytes(w, lens_h) + kvb + 8 * w.B * w.H
     if table is not None:  # the block-table entries the kernel reads
         alg += 4 * sum(-(-int(n) // args.page_size) for n in lens_h) * w.H
+    if args.path != "fused":
+        # the split kernel also writes the partials: P (d + 3) floats per (b, h)
+        alg += 4 * w.B * w.H * P_split * (w.d + 3) - w.B * w.H * (w.d * ELEMENT_BYTES[w.out_dtype] + 4)
     achieved = alg / (kern_ms * 1e-3) / 1e9
     tokens = sum(lens_h) * w.H
 
@@ -485,7 +512,8 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": config_of(w, "auto", args.page_size, args.kv_dtype),
+            "config": config_of(w, (P_fused or "auto") if args.path == "fused" else P_split,
+                                args.page_size, args.kv_dtype, args.path),
             "tokens_per_s": ws * tokens / (ms_per_step * 1e-3),
             "pct_of_nominal_8tbs": 100.0 * value / ws / NOMINAL_HBM_GBS,
             "pct_of_measured_hbm": 100.0 * value / ws / peaks["hbm_gbs"],
@@ -498,10 +526,12 @@ def run_ours(args, w):
                          "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                          "algorithmic_bytes_per_launch": alg, "mean_launch_ms": kern_ms},
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (1 if args.path == "fused" else 2),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if combine_ms is not None:
+            line["combine_ms"] = combine_ms
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -519,12 +549,18 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--kv-dtype", choices=["native", "e4m3"], default="native",
                     help="e4m3: store K/V in FP8 with per-(b,h) scales and time fd_decode_fp8")
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="split count (0: the workload's own, else the automatic decomposition)")
+    ap.add_argument("--path", choices=["fused", "split-mlo", "split-lse"], default="fused",
+                    help="fused fd_decode, or fd_decode_split then fd_combine_mlo / fd_combine_lse")
     ap.add_argument("--page-size", type=int, default=0,
                     help="time fd_decode_paged on the workload laid out in pages of this many tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     w = WORKLOADS[args.workload]
+    if args.path != "fused" and (args.page_size or args.kv_dtype != "native" or w.kv_heads != w.H):
+        ap.error("--path split-* times the contiguous, native-dtype, one-query-per-K/V-head path")
     ws, _, _ = dist_env()
     if args.gpus > 1 and ws == 1 and "LOCAL_RANK" not in os.environ:
         # launch the per-GPU ranks ourselves

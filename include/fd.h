@@ -77,7 +77,9 @@ int fd_num_sms(void);
  * for num_splits == 0 when the batch is too large for its balanced
  * decomposition.  The split-count heuristic of "adv04: Flash-Decoding" (Q2:
  * about seq/1024, capped) is replaced by one that fills every SM: enough
- * (b, h, split) work items for several waves, splits of at least 256 tokens.
+ * (b, h, split) work items for several waves (at least 4 per SM), splits of
+ * at least 256 tokens, and among counts from that minimum up to 4 times it,
+ * the one whose items fill the last round-robin wave over the CTAs best.
  * Returns >= 1, or -1 for invalid sizes.
  */
 int fd_auto_num_splits(int B, int H, int N, int d, int sm_count);

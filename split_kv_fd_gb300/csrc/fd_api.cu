@@ -218,12 +218,29 @@ int fd_auto_num_splits(int B, int H, int N, int d, int sms)
     long long cap = N / 256;
     if (cap < 1)
         cap = 1;
-    long long P = want < cap ? want : cap;
-    if (P < 1)
-        P = 1;
-    if (P > 8192)
-        P = 8192;
-    return (int)P;
+    long long lo = want < cap ? want : cap;
+    if (lo < 1)
+        lo = 1;
+    if (lo > 8192)
+        lo = 8192;
+    // the items go round-robin to the CTAs: from lo up to 4 lo (within the
+    // cap), take the split count whose items fill the last round best; a
+    // larger count only if it fills more than 1% better
+    long long hi = 4 * lo < cap ? 4 * lo : cap;
+    if (hi > 8192)
+        hi = 8192;
+    const long long G = (long long)sms * FD_CTAS_PER_SM;
+    long long best = lo;
+    double best_fill = -1.0;
+    for (long long P = lo; P <= hi; ++P) {
+        const long long items = bh * P;
+        const double fill = (double)items / (double)(G * ((items + G - 1) / G));
+        if (fill > best_fill + 0.01) {
+            best_fill = fill;
+            best = P;
+        }
+    }
+    return (int)best;
 }
 
 size_t fd_workspace_size(int B, int H, int N, int d, int num_splits)

@@ -71,14 +71,30 @@ def test_host_rejects_bad_arguments_without_cuda(lib):
                          None, 0, None) == 0
 
 
+def _fill(bh, P, G):
+    items = bh * P
+    return items / (G * -(-items // G))
+
+
 def test_auto_num_splits_rule(lib):
-    # fills ~4 work items per SM, never splits under 256 tokens, >= 1
-    assert lib.fd_auto_num_splits(8, 32, 32768, 128, 152) == 3
-    assert lib.fd_auto_num_splits(1, 32, 131072, 128, 152) == 19
+    # >= 4 work items per SM, never splits under 256 tokens, >= 1; among
+    # counts up to 4x that minimum, the best fill of the last wave of CTAs
+    assert lib.fd_auto_num_splits(8, 32, 32768, 128, 152) == 7      # 1792 items: 11.8 per CTA
+    assert lib.fd_auto_num_splits(16, 32, 65536, 128, 152) == 5     # 2560 items: 16.8 per CTA
+    assert lib.fd_auto_num_splits(1, 32, 131072, 128, 152) == 19    # 608 items: exactly 4 per CTA
     assert lib.fd_auto_num_splits(1, 1, 1024, 64, 152) == 4
     assert lib.fd_auto_num_splits(1, 1, 100, 64, 152) == 1
     assert lib.fd_auto_num_splits(0, 1, 100, 64, 152) == 1
     assert lib.fd_auto_num_splits(1, 1, 100, 64, 0) == -1
+    # the chosen count never fills worse than the minimum one, nor splits
+    # below 256 tokens
+    for B, H, N in [(8, 32, 32768), (3, 7, 50000), (2, 8, 32768), (64, 8, 4096), (1, 5, 9000)]:
+        bh = B * H
+        lo = max(1, min(-(-4 * 152 // bh), max(1, N // 256)))
+        P = lib.fd_auto_num_splits(B, H, N, 128, 152)
+        assert lo <= P <= max(lo, 4 * lo)
+        assert P == 1 or N // P >= 256
+        assert _fill(bh, P, 152) >= _fill(bh, lo, 152)
 
 
 def test_input_generator_is_seeded_and_pads_with_nan():
