@@ -546,6 +546,13 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
+// An L2 load that a dry pass skips (its instruction still runs, predicated
+// off, so the code is the same).
+__device__ __forceinline__ float ldcg_if(bool live, const float *ptr)
+{
+    return live ? __ldcg(ptr) : 0.f;
+}
+
 // Workspace slot of the i-th piece of (b, h) (see the decompositions).
 __device__ __forceinline__ long long piece_slot(const SplitParams &p, const Ctx &ctx, int bh,
                                                 unsigned i, int gf, long long off)
@@ -563,7 +570,8 @@ __device__ __forceinline__ long long piece_slot(const SplitParams &p, const Ctx 
 // per lane, and broadcast by shuffles, so the merge needs no barrier.
 template <int D>
 __device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ctx, int bh,
-                                             unsigned target, int gf, long long off, int lane)
+                                             unsigned target, int gf, long long off, int lane,
+                                             bool live = true)
 {
     constexpr int DPL = D / 32;
     // the first 32 pieces keep their slot and (m, l) in registers
@@ -571,14 +579,14 @@ __device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ct
     float m0 = -INFINITY, l0 = 0.f;
     if ((unsigned)lane < target) {
         s0 = piece_slot(p, ctx, bh, (unsigned)lane, gf, off);
-        m0 = __ldcg(p.ws_ml + 2 * s0);
-        l0 = __ldcg(p.ws_ml + 2 * s0 + 1);
+        m0 = ldcg_if(live, p.ws_ml + 2 * s0);
+        l0 = ldcg_if(live, p.ws_ml + 2 * s0 + 1);
     }
     float mx = l0 > 0.f ? m0 : -INFINITY;
     for (unsigned i = lane + 32; i < target; i += 32) {
         const long long sl = piece_slot(p, ctx, bh, i, gf, off);
-        if (__ldcg(p.ws_ml + 2 * sl + 1) > 0.f)
-            mx = fmaxf(mx, __ldcg(p.ws_ml + 2 * sl));
+        if (ldcg_if(live, p.ws_ml + 2 * sl + 1) > 0.f)
+            mx = fmaxf(mx, ldcg_if(live, p.ws_ml + 2 * sl));
     }
     const float M = warp_max(mx);
     float L = 0.f, O[DPL];
@@ -594,8 +602,8 @@ __device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ct
             l = 0.f;
             if (base + lane < target) {
                 sl = piece_slot(p, ctx, bh, base + lane, gf, off);
-                m = __ldcg(p.ws_ml + 2 * sl);
-                l = __ldcg(p.ws_ml + 2 * sl + 1);
+                m = ldcg_if(live, p.ws_ml + 2 * sl);
+                l = ldcg_if(live, p.ws_ml + 2 * sl + 1);
             }
         }
         const float e = l > 0.f ? ex2(m - M) * l : 0.f;
@@ -611,7 +619,7 @@ __device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ct
                 const long long si = __shfl_sync(FULL_MASK, sl, i0 + u);
 #pragma unroll
                 for (int j = 0; j < DPL; ++j)
-                    x[u][j] = (i0 + u < n) ? __ldcg(p.ws_o + si * D + lane + 32 * j) : 0.f;
+                    x[u][j] = (i0 + u < n) ? ldcg_if(live, p.ws_o + si * D + lane + 32 * j) : 0.f;
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -625,8 +633,9 @@ __device__ __forceinline__ void merge_pieces(const SplitParams &p, const Ctx &ct
     const bool nonempty = L > 0.f;
 #pragma unroll
     for (int j = 0; j < DPL; ++j)
-        store_out(p.out, (long long)bh * D + lane + 32 * j, p.out_dtype, nonempty ? O[j] / L : 0.f);
-    if (lane == 0 && p.lse)
+        if (live)
+            store_out(p.out, (long long)bh * D + lane + 32 * j, p.out_dtype, nonempty ? O[j] / L : 0.f);
+    if (live && lane == 0 && p.lse)
         p.lse[bh] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
 }
 
@@ -646,6 +655,12 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
     Seg s;
     seg_first(p, ctx, s);
     int k = 0;
+    // The first pass over the first segment runs this code with every store,
+    // arrival and wait switched off: the merge warp is idle at the start, and
+    // the pass brings the code into the instruction cache, where the real
+    // merges find it (run once per segment, after an L2 flush or a long
+    // stream it would otherwise be fetched from DRAM, line by line).
+    bool live = false;
 #pragma unroll 1
     while (s.valid) {
         // the segment's facts, worked out while its data streams
@@ -664,7 +679,7 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
         const float vs = (C::FP8 && p.v_scale) ? __ldg(p.v_scale + bh) : 1.f;
 
         const int buf = k % C::NBUF;
-        if (!mbar_wait_bounded_sleep(sfull + buf * 8, (uint32_t)(k / C::NBUF) & 1, 1000000)) {
+        if (live && !mbar_wait_bounded_sleep(sfull + buf * 8, (uint32_t)(k / C::NBUF) & 1, 1000000)) {
             if (lane == 0)
                 atomicOr(p.status, STATUS_TIMEOUT);
             return;
@@ -691,7 +706,8 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
                     O[j] = fmaf(e, ra[i * D + lane + 32 * j], O[j]);
             }
         }
-        mbar_arrive(sfree + buf * 8);  // the streaming warps may refill the buffer
+        if (live)
+            mbar_arrive(sfree + buf * 8);  // the streaming warps may refill the buffer
         const bool nonempty = L > 0.f;
         float o[DPL];
 #pragma unroll
@@ -701,14 +717,15 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
         if (p.out_kind == OUT_PARTIALS) {
 #pragma unroll
             for (int j = 0; j < DPL; ++j)
-                p.o_part[slot * D + lane + 32 * j] = o[j];
-            if (lane == 0) {
+                if (live)
+                    p.o_part[slot * D + lane + 32 * j] = o[j];
+            if (live && lane == 0) {
                 p.m_part[slot] = nonempty ? M * LN2_F : -INFINITY;
                 p.l_part[slot] = L;
                 if (p.lse_part)
                     p.lse_part[slot] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
             }
-        } else if (complete) {
+        } else if (complete && live) {
 #pragma unroll
             for (int j = 0; j < DPL; ++j)
                 store_out(p.out, (long long)bh * D + lane + 32 * j, p.out_dtype, o[j]);
@@ -718,8 +735,9 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
             // workspace partial: normalised o, m in base 2, l
 #pragma unroll
             for (int j = 0; j < DPL; ++j)
-                p.ws_o[slot * D + lane + 32 * j] = o[j];
-            if (lane == 0) {
+                if (live)
+                    p.ws_o[slot * D + lane + 32 * j] = o[j];
+            if (live && lane == 0) {
                 p.ws_ml[2 * slot] = nonempty ? M : -INFINITY;
                 p.ws_ml[2 * slot + 1] = L;
             }
@@ -737,14 +755,18 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
             }
             __threadfence();
             __syncwarp();
-            unsigned old = 0;
-            if (lane == 0)
+            unsigned old = target - 1;  // the dry pass runs the merge, to no effect
+            if (live && lane == 0)
                 old = atomicInc(p.ws_cnt + bh, target - 1);
             old = __shfl_sync(FULL_MASK, old, 0);
             if (old == target - 1) {
                 __threadfence();
-                merge_pieces<D>(p, ctx, bh, target, gf, off, lane);
+                merge_pieces<D>(p, ctx, bh, target, gf, off, lane, live);
             }
+        }
+        if (!live) {
+            live = true;  // now the same segment for real
+            continue;
         }
         ++k;
         seg_next(p, ctx, s);
