@@ -238,6 +238,18 @@ fd_status fd_merge_lse(const float *o_a, const float *lse_a, const float *o_b, c
 fd_status fd_device_status(int reset);
 
 /*
+ * Test hook for the failure path (the pages have no counterpart: this checks
+ * the library's own failure reporting).  Launches, on `stream`, a one-warp
+ * kernel that waits, with the kernels' own bounded wait, on a barrier that
+ * nothing completes.  After the wait's limit (1 s) it gives up and records
+ * FD_ERR_DEVICE_TIMEOUT in the device status word, as a kernel whose copies
+ * never landed would; the kernel then ends, and the context stays usable.
+ * Read the result with fd_device_status().  Returns FD_OK when launched, else
+ * FD_ERR_CUDA.
+ */
+fd_status fd_selftest_wait_timeout(void *stream);
+
+/*
  * Size of the static device scratch that fd_decode_noalloc uses: 1 MiB.
  * Every GPU on which this library is loaded holds it until the process
  * exits.

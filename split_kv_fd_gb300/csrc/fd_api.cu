@@ -179,6 +179,11 @@ bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long r
 }  // namespace
 }  // namespace fd
 
+namespace fd {
+// the bounded-wait self-test kernel (fd_combine.cu)
+cudaError_t launch_wait_selftest(unsigned *status, cudaStream_t s);
+}  // namespace fd
+
 using namespace fd;
 
 extern "C" {
@@ -412,6 +417,15 @@ fd_status fd_merge_lse(const float *o_a, const float *lse_a, const float *o_b, c
                             static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? FD_OK
                : FD_ERR_CUDA;
+}
+
+fd_status fd_selftest_wait_timeout(void *stream)
+{
+    unsigned *st = status_ptr();
+    if (!st)
+        return FD_ERR_CUDA;
+    return launch_wait_selftest(st, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FD_OK
+                                                                                       : FD_ERR_CUDA;
 }
 
 fd_status fd_device_status(int reset)

@@ -141,6 +141,29 @@ cudaError_t launch_merge_lse(const float *oa, const float *sa, const float *ob, 
     return cudaGetLastError();
 }
 
+// Self-test of the bounded wait every kernel uses on its copies: one warp
+// waits, with that same wait, on an mbarrier that nothing completes.  The
+// wait gives up after its limit (1 s) and the kernel records a timeout in
+// the status word, as a kernel whose copies never landed would; then it
+// ends, and the context stays usable.
+__global__ void wait_selftest_kernel(unsigned *status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0)
+        mbar_init(b, 1);
+    fence_mbar_init();
+    __syncthreads();
+    if (!mbar_wait_bounded(b, 0) && threadIdx.x == 0)
+        atomicOr(status, STATUS_TIMEOUT);
+}
+
+cudaError_t launch_wait_selftest(unsigned *status, cudaStream_t s)
+{
+    wait_selftest_kernel<<<1, 32, 0, s>>>(status);
+    return cudaGetLastError();
+}
+
 static cudaError_t launch_combine(const CombineParams &p, bool lse_form, cudaStream_t s)
 {
     const size_t smem = (size_t)p.P * sizeof(float);

@@ -28,7 +28,8 @@ DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 EXPORTS = ["fd_status_str", "fd_version", "fd_num_sms", "fd_auto_num_splits",
            "fd_workspace_size", "fd_decode", "fd_decode_split", "fd_combine_mlo",
            "fd_combine_lse", "fd_device_status", "fd_decode_noalloc", "fd_decode_paged",
-           "fd_decode_fp8", "fd_merge_lse", "fd_decode_gqa", "fd_workspace_size_gqa"]
+           "fd_decode_fp8", "fd_merge_lse", "fd_decode_gqa", "fd_workspace_size_gqa",
+           "fd_selftest_wait_timeout"]
 
 _lock = threading.Lock()
 _lib = None
@@ -89,6 +90,8 @@ def load(build_if_missing: bool = False):
         lib.fd_workspace_size_gqa.restype = S
         lib.fd_device_status.argtypes = [I]
         lib.fd_device_status.restype = I
+        lib.fd_selftest_wait_timeout.argtypes = [P]
+        lib.fd_selftest_wait_timeout.restype = I
         _lib = lib
         return lib
 
@@ -408,6 +411,16 @@ def merge_lse(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
                              _ptr(lse), _stream(o_a, stream))
     _check(st, "fd_merge_lse")
     return out, lse
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait self-test (fd_selftest_wait_timeout): a kernel
+    whose wait nothing completes gives up after the kernels' wait limit (1 s)
+    and records FD_ERR_DEVICE_TIMEOUT, read back by device_status()."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = load().fd_selftest_wait_timeout(ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise FDError(rc, "fd_selftest_wait_timeout")
 
 
 def device_status(reset: bool = True) -> int:

@@ -117,3 +117,18 @@ def test_binding_refuses_cpu_tensors():
     k = torch.zeros(1, 1, 4, 64)
     with pytest.raises(ValueError):
         fd.decode(q, k, k)
+
+
+def test_library_has_no_unresolved_symbols_of_its_own():
+    """Every undefined dynamic symbol comes from another library (versioned,
+    e.g. libcudart's or libc's) or is weak: a symbol of this library that the
+    link left undefined would only fail when the library is loaded."""
+    import shutil
+    import subprocess
+    from split_kv_fd_gb300 import _build_lib as bl
+    if not shutil.which("nm"):
+        pytest.skip("nm not available")
+    out = subprocess.run(["nm", "-D", "--undefined-only", bl.LIB], capture_output=True, text=True,
+                         check=True).stdout.split("\n")
+    own = [l.split()[-1] for l in out if l.strip() and l.split()[0] == "U" and "@" not in l]
+    assert own == [], own
