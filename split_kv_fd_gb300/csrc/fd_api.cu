@@ -176,6 +176,36 @@ bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long r
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// What every fused entry point sets alike: the score scale in base 2, the
+// plan, the outputs, the workspace carve-up and the status word.
+void set_fused(SplitParams &p, const Plan &pl, const WsLayout &wl, void *workspace, float scale,
+               void *out, int out_dtype, float *lse, unsigned *status)
+{
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.decomp = pl.decomp;
+    p.P = pl.P;
+    p.grid = pl.grid;
+    p.out_kind = OUT_FUSED;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.lse = lse;
+    char *ws = static_cast<char *>(workspace);
+    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
+    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
+    p.status = status;
+}
+
+// The arrival counters of `rows` sequences start at zero on every call: a
+// reused workspace may hold anything at these bytes.  One split per
+// sequence (nothing to merge) uses none.
+bool clear_counters(const SplitParams &p, long long rows, cudaStream_t s)
+{
+    if (p.decomp == DECOMP_SPLITS && p.P == 1)
+        return true;
+    return cudaMemsetAsync(p.ws_cnt, 0, (size_t)rows * sizeof(unsigned), s) == cudaSuccess;
+}
+
 }  // namespace
 }  // namespace fd
 
@@ -292,25 +322,10 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
     p.B = B;
     p.H = H;
     p.N = N;
-    p.scale_log2 = scale * 1.4426950408889634f;
     p.q_dtype = in_dtype;
-    p.decomp = pl.decomp;
-    p.P = pl.P;
-    p.grid = pl.grid;
-    p.out_kind = OUT_FUSED;
-    p.out = out;
-    p.out_dtype = out_dtype;
-    p.lse = lse;
-    char *ws = static_cast<char *>(workspace);
-    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
-    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
-    p.status = st;
+    set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // the arrival counters start at zero for every call (a reused workspace
-    // may hold anything at these bytes)
-    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
-    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * H * sizeof(unsigned), cs) != cudaSuccess)
+    if (!clear_counters(p, (long long)B * H, cs))
         return FD_ERR_CUDA;
     return launch(in_dtype, d, p, pl.decomp, cs);
 }
@@ -510,23 +525,10 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
     p.B = B;
     p.H = Hkv;
     p.N = N;
-    p.scale_log2 = scale * 1.4426950408889634f;
     p.q_dtype = in_dtype;
-    p.decomp = pl.decomp;
-    p.P = pl.P;
-    p.grid = pl.grid;
-    p.out_kind = OUT_FUSED;
-    p.out = out;
-    p.out_dtype = out_dtype;
-    p.lse = lse;
-    char *ws = static_cast<char *>(workspace);
-    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
-    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
-    p.status = st;
+    set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
-    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * Hkv * sizeof(unsigned), cs) != cudaSuccess)
+    if (!clear_counters(p, (long long)B * Hkv, cs))
         return FD_ERR_CUDA;
     return launch_gqa(in_dtype, d, gp, cs) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
@@ -564,25 +566,12 @@ fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const vo
     p.B = B;
     p.H = H;
     p.N = N;
-    p.scale_log2 = scale * 1.4426950408889634f;
     p.q_dtype = q_dtype;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
-    p.decomp = pl.decomp;
-    p.P = pl.P;
-    p.grid = pl.grid;
-    p.out_kind = OUT_FUSED;
-    p.out = out;
-    p.out_dtype = out_dtype;
-    p.lse = lse;
-    char *ws = static_cast<char *>(workspace);
-    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
-    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
-    p.status = st;
+    set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
-    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * H * sizeof(unsigned), cs) != cudaSuccess)
+    if (!clear_counters(p, (long long)B * H, cs))
         return FD_ERR_CUDA;
     return launch(FD_E4M3, d, p, pl.decomp, cs);
 }
@@ -630,23 +619,10 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     p.page_size = page_size;
     p.max_pages = max_pages;
     p.num_pages = num_pages;
-    p.scale_log2 = scale * 1.4426950408889634f;
     p.q_dtype = in_dtype;
-    p.decomp = pl.decomp;
-    p.P = pl.P;
-    p.grid = pl.grid;
-    p.out_kind = OUT_FUSED;
-    p.out = out;
-    p.out_dtype = out_dtype;
-    p.lse = lse;
-    char *ws = static_cast<char *>(workspace);
-    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
-    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
-    p.status = st;
+    set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
-    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * H * sizeof(unsigned), cs) != cudaSuccess)
+    if (!clear_counters(p, (long long)B * H, cs))
         return FD_ERR_CUDA;
     return launch(in_dtype, d, p, pl.decomp, cs);
 }
@@ -729,24 +705,10 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     p.B = B;
     p.H = H;
     p.N = N;
-    p.scale_log2 = scale * 1.4426950408889634f;
     p.q_dtype = in_dtype;
-    p.decomp = pl.decomp;
-    p.P = pl.P;
-    p.grid = pl.grid;
-    p.out_kind = OUT_FUSED;
-    p.out = out;
-    p.out_dtype = out_dtype;
-    p.lse = lse;
-    char *ws = static_cast<char *>(scratch);
-    p.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
-    p.ws_ml = reinterpret_cast<float *>(ws + wl.ml_off);
-    p.ws_cnt = reinterpret_cast<unsigned *>(ws + wl.cnt_off);
-    p.status = st;
+    set_fused(p, pl, wl, scratch, scale, out, out_dtype, lse, st);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's bytes: clear the counters this call uses
-    const bool counters = !(pl.decomp == DECOMP_SPLITS && pl.P == 1);
-    if (counters && cudaMemsetAsync(p.ws_cnt, 0, (size_t)B * H * sizeof(unsigned), cs) != cudaSuccess)
+    if (!clear_counters(p, (long long)B * H, cs))
         return FD_ERR_CUDA;
     return launch(in_dtype, d, p, pl.decomp, cs);
 }
