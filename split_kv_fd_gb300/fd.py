@@ -92,6 +92,8 @@ def load(build_if_missing: bool = False):
         lib.fd_device_status.restype = I
         lib.fd_selftest_wait_timeout.argtypes = [P]
         lib.fd_selftest_wait_timeout.restype = I
+        lib.fd_decode_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, I, P, P]
+        lib.fd_decode_noalloc.restype = I
         _lib = lib
         return lib
 
@@ -202,6 +204,33 @@ def decode(q, k, v, seqlens=None, num_splits=0, scale=None, out_dtype=None, out=
                        _ptr(workspace), workspace.numel() * workspace.element_size(),
                        _stream(q, stream))
     _check(st, "fd_decode")
+    return out, lse
+
+
+
+def decode_noalloc(q, k, v, seqlens=None, num_splits=0, scale=None, out_dtype=None, out=None,
+                   lse=None, return_lse=True, stream=None):
+    """fd_decode on the library's own device scratch (fd_decode_noalloc):
+    nothing is allocated per call.  Returns ``(out, lse)``.  Calls on one
+    device share the scratch, so they must not overlap on the GPU; problems
+    whose workspace exceeds the scratch raise FD_ERR_SCRATCH_TOO_SMALL."""
+    B, H, N, d = _check_qkv(q, k, v, seqlens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, H, d), dtype=odt, device=q.device)
+    _need_cuda(out, lse)
+    if out.dtype not in DTYPE_CODE or out.shape != (B, H, d):
+        raise ValueError("out must be [B,H,d] float32/float16/bfloat16")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or lse.shape != (B, H)):
+        raise ValueError("lse must be float32 [B,H]")
+    st = load().fd_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(seqlens), B, H, N, d,
+                                  DTYPE_CODE[q.dtype], int(num_splits), float(scale), _ptr(out),
+                                  DTYPE_CODE[out.dtype], _ptr(lse), _stream(q, stream))
+    _check(st, "fd_decode_noalloc")
     return out, lse
 
 

@@ -132,3 +132,76 @@ def test_library_has_no_unresolved_symbols_of_its_own():
                          check=True).stdout.split("\n")
     own = [l.split()[-1] for l in out if l.strip() and l.split()[0] == "U" and "@" not in l]
     assert own == [], own
+
+
+def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
+    """GQA, FP8, paged, no-alloc and merge entry points check their arguments
+    on the host before any CUDA call (1 = invalid, 2 = unsupported, 0 = an
+    empty problem, nothing launched)."""
+    P = ctypes.c_void_p
+    dm = P(4096)
+    MB = 1 << 20
+
+    def gqa(B, Hq, Hkv, N, d, dt=2, q=dm, ns=0):
+        return lib.fd_decode_gqa(q, dm, dm, None, B, Hq, Hkv, N, d, dt, ns, 1.0, dm, 2, None, dm,
+                                 MB, None)
+    assert gqa(1, 6, 4, 64, 128) == 1            # Hq not a multiple of Hkv
+    assert gqa(1, 8, 0, 64, 128) == 1            # no K/V heads
+    assert gqa(1, 34, 2, 64, 128) == 2           # G = 17 > 16
+    assert gqa(1, 16, 2, 64, 128, dt=0) == 2     # G > 1 needs 16-bit K/V
+    assert gqa(1, 16, 2, 64, 96) == 2            # head dim
+    assert gqa(1, 8, 8, 64, 96) == 2             # G = 1 goes to fd_decode's checks
+    assert gqa(1, 16, 2, 1 << 30, 128) == 2      # 2^31 K/V rows: past 32-bit coordinates
+    assert gqa(1, 16, 2, 64, 128, q=None) == 1
+    assert gqa(1, 16, 2, 64, 128, ns=-2) == 1
+    assert gqa(0, 16, 2, 64, 128, q=None) == 0   # empty
+
+    def fp8(B=1, H=2, N=64, d=128, qdt=2, ks=dm, q=dm):
+        return lib.fd_decode_fp8(q, qdt, dm, dm, ks, dm, None, B, H, N, d, 0, 1.0, dm, 2, None, dm,
+                                 MB, None)
+    assert fp8(ks=None) == 1                     # scales are required
+    assert fp8(qdt=3) == 2                       # q stays 16/32-bit
+    assert fp8(d=80) == 2
+    assert fp8(q=P(4100)) == 1                   # misaligned q
+    assert fp8(B=0, q=None, ks=None) == 0
+
+    def paged(B=1, H=2, d=128, ps=16, mp=4, npg=8, lens=dm, table=dm):
+        return lib.fd_decode_paged(dm, dm, dm, table, lens, B, H, d, ps, mp, npg, 2, 0, 1.0, dm, 2,
+                                   None, dm, MB, None)
+    assert paged(ps=0) == 1                      # page size >= 1
+    assert paged(ps=1 << 16, mp=1 << 16) == 1    # pages x size beyond int32 tokens
+    assert paged(mp=-1) == 1
+    assert paged(lens=None) == 1                 # lengths are required
+    assert paged(npg=0) == 1                     # a table needs pages to name
+    assert paged(table=P(4098)) == 1             # misaligned block table
+    assert paged(d=72) == 2
+    assert paged(B=0, lens=None, table=None) == 0
+
+    def noalloc(B=1, H=2, N=64, d=128, q=dm, dt=2):
+        return lib.fd_decode_noalloc(q, dm, dm, None, B, H, N, d, dt, 0, 1.0, dm, 2, None, None)
+    assert noalloc(d=96) == 2
+    assert noalloc(dt=3) == 2                    # E4M3 K/V has its own entry point
+    assert noalloc(q=None) == 1
+    assert noalloc(B=0, q=None) == 0
+
+    def merge(rows=4, d=128, oa=dm):
+        return lib.fd_merge_lse(oa, dm, dm, dm, rows, d, dm, dm, None)
+    assert merge(rows=-1) == 1
+    assert merge(d=6) == 1                       # d a multiple of 4
+    assert merge(oa=None) == 1
+    assert merge(oa=P(4104)) == 1                # o rows 16-byte aligned
+    assert merge(rows=0, oa=None) == 0
+
+    assert lib.fd_workspace_size_gqa(1, 6, 4, 64, 128, 0) == 0
+    assert lib.fd_combine_mlo(dm, dm, dm, 1, 1, 4, 80, dm, 0, None, None) == 2
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the answer without a GPU")
+def test_valid_call_without_a_gpu_reports_a_cuda_error(lib):
+    """Arguments that pass every host check reach the first CUDA call, which
+    fails without a device: the call returns FD_ERR_CUDA and launches nothing."""
+    P = ctypes.c_void_p
+    dm = P(4096)
+    assert lib.fd_decode(dm, dm, dm, None, 1, 1, 8, 128, 2, 0, 1.0, dm, 2, None, P(1 << 20),
+                         1 << 20, None) == 4
+    assert lib.fd_num_sms() <= 0

@@ -3,7 +3,8 @@ memory (a serving engine whose memory pool owns the GPU, a runtime plugin
 given only pointers and a stream): it must give fd_decode's results with
 its scratch taken from the library's static device array.
 
-Called through the C ABI directly.  This file is collected last so that a
+Called through the C ABI directly and through the binding's
+decode_noalloc.  This file is collected last so that a
 run stopping at its first failure has already run every other test; it
 also passes on its own in a fresh process (it builds and loads the library
 itself).
@@ -97,3 +98,21 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
     assert "FD_NOALLOC_SCRATCH_BYTES" in fdmod.status_str(st)
     torch.cuda.synchronize()
     assert torch.all(out == 0)  # nothing was launched
+
+
+def test_binding_decode_noalloc_matches_oracle(lib):
+    """The Python binding's decode_noalloc against the float64 oracle, and its
+    error for a problem beyond the scratch."""
+    import oracle
+    from parity_util import check_lse, check_out
+    dev = torch.device("cuda")
+    q, k, v, lt = random_case(3, 8, 2500, 128, "bf16", lens=[2500, 1, 0], seed=77)
+    ref_out, ref_lse = oracle.attention(q, k, v, lens=lt)
+    out, lse = fd.decode_noalloc(q.to(dev), k.to(dev), v.to(dev), lt.to(dev), out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
+    qb = torch.zeros(4, 64, 128, device=dev, dtype=torch.bfloat16)
+    kb = torch.zeros(4, 64, 64, 128, device=dev, dtype=torch.bfloat16)
+    with pytest.raises(fd.FDError) as e:
+        fd.decode_noalloc(qb, kb, kb, num_splits=64)
+    assert e.value.status == FD_ERR_SCRATCH_TOO_SMALL
