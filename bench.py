@@ -45,8 +45,13 @@ from split_kv_fd_gb300.workloads import BENCH_DEFAULT, ELEMENT_BYTES, WORKLOADS 
 METRIC = "split-KV decode attention KV-GB/s and % of GB300 HBM peak (~8 TB/s), 1 GPU"
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCES = ["fd_split.cuh", "fd_device.cuh", "fd_internal.h", "fd_split_bf16.cu",
-                  "fd_split_f16.cu", "fd_split_f32.cu", "fd_split_fp8.cu"]
+# the sources each profiled kernel is compiled from (the hash of a kernel's
+# sources keys its committed ncu traffic record)
+KERNEL_SOURCES = {
+    "split_kernel": ["fd_split.cuh", "fd_device.cuh", "fd_internal.h", "fd_split_bf16.cu",
+                     "fd_split_f16.cu", "fd_split_f32.cu", "fd_split_fp8.cu"],
+    "gqa_kernel": ["fd_gqa.cuh", "fd_gqa.cu", "fd_split.cuh", "fd_device.cuh", "fd_internal.h"],
+}
 
 
 # ----------------------------------------------------------------- helpers
@@ -71,13 +76,13 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the split kernel's code: its sources without comments and
-    with whitespace collapsed, so that editing a comment keeps the ncu
-    records taken from the same code valid."""
+def kernel_source_hash(kernel: str = "split_kernel") -> str:
+    """Hash of a kernel's code: its sources without comments and with
+    whitespace collapsed, so that editing a comment keeps the ncu records
+    taken from the same code valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "split_kv_fd_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
@@ -94,17 +99,18 @@ def kernel_name(w, fp8: bool, paged: bool) -> str:
     return f"fd::split_kernel<{elt}, {w.d}>" + (" (paged)" if paged else "")
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    from the current kernel sources on this workload; else None."""
-    p = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+def profiled_traffic(workload: str, kernel: str = "split_kernel"):
+    """DRAM bytes per launch from the committed ncu summary of `kernel`, if
+    it was taken from the kernel's current sources on this workload; else
+    None."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
     if not os.path.exists(p):
         return None
     try:
         with open(p) as f:
             rec = json.load(f)
         ent = rec.get(workload)
-        if ent and ent.get("kernel_source_hash") == kernel_source_hash():
+        if ent and ent.get("kernel_source_hash") == kernel_source_hash(kernel):
             return ent.get("dram_bytes_per_launch")
     except Exception:
         return None
@@ -519,9 +525,11 @@ def run_ours(args, w):
             "pct_of_measured_hbm": 100.0 * value / ws / peaks["hbm_gbs"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": (None if table is not None or w.kv_heads != w.H
+                         "traffic": (None if table is not None
                                      else profiled_traffic(w.name + ("+e4m3" if k_scale is not None
-                                                                     else ""))),
+                                                                     else ""),
+                                                           "gqa_kernel" if w.kv_heads != w.H
+                                                           else "split_kernel")),
                          "kernel": kernel_name(w, k_scale is not None, table is not None),
                          "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                          "algorithmic_bytes_per_launch": alg, "mean_launch_ms": kern_ms},

@@ -21,11 +21,20 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     shutil.copytree(bench.os.path.join(bench.ROOT, "split_kv_fd_gb300", "csrc"), src)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h0 = bench.kernel_source_hash()
+    g0 = bench.kernel_source_hash("gqa_kernel")
+    assert g0 != h0
     f = src / "fd_split.cuh"
     f.write_text(f.read_text() + "\n// a comment\n/* and a block\n   comment */\n")
     assert bench.kernel_source_hash() == h0
+    assert bench.kernel_source_hash("gqa_kernel") == g0
     f.write_text(f.read_text() + "\nstatic const int fd_bench_probe = 1;\n")
     assert bench.kernel_source_hash() != h0
+    assert bench.kernel_source_hash("gqa_kernel") != g0   # the GQA kernel includes it
+    # a change to the GQA kernel alone leaves the split kernel's records valid
+    h1 = bench.kernel_source_hash()
+    g = src / "fd_gqa.cu"
+    g.write_text(g.read_text() + "\nstatic const int fd_bench_probe2 = 2;\n")
+    assert bench.kernel_source_hash() == h1
 
 
 def test_algorithmic_bytes_of_the_benchmark_workload():
@@ -37,4 +46,15 @@ def test_algorithmic_bytes_of_the_benchmark_workload():
     assert bench.algorithmic_bytes(w, lens) == kv + w.B * w.H * w.d * 4 + w.B * w.H * 4 + w.B * 4
     # the committed ncu record of this workload, when it matches the sources
     t = bench.profiled_traffic(w.name)
+    assert t is None or abs(t / bench.algorithmic_bytes(w, lens) - 1) < 0.01
+
+
+def test_algorithmic_bytes_of_the_gqa_workload():
+    """K/V counted once per K/V head; q, out and lse once per query head."""
+    w = WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]
+    lens = [w.N] * w.B
+    kv = 2 * w.kv_heads * w.d * 2 * w.N * w.B
+    assert bench.kv_bytes(w, lens) == kv == 2 ** 30
+    assert bench.algorithmic_bytes(w, lens) == kv + w.B * w.H * w.d * 4 + w.B * w.H * 4 + w.B * 4
+    t = bench.profiled_traffic(w.name, "gqa_kernel")
     assert t is None or abs(t / bench.algorithmic_bytes(w, lens) - 1) < 0.01
