@@ -94,7 +94,7 @@ def kernel_source_hash(kernel: str = "split_kernel") -> str:
 def kernel_name(w, fp8: bool, paged: bool) -> str:
     """The kernel that does the timed work, as ncu names it."""
     if w.kv_heads != w.H:
-        return f"fd::gqa_kernel<{w.dtype}, {w.d}>"
+        return f"fd::gqa_kernel<{w.dtype}, {w.d}>" + (" (paged)" if paged else "")
     elt = "e4m3" if fp8 else w.dtype
     return f"fd::split_kernel<{elt}, {w.d}>" + (" (paged)" if paged else "")
 
@@ -361,9 +361,12 @@ def run_ours(args, w):
             else:
                 fd.combine_lse(o_p, s_p, out=out, lse=lse, stream=stream)
             return
-        if w.kv_heads != w.H:
+        if w.kv_heads != w.H and table is None:
             fd.decode_gqa(q, k, v, lens, num_splits=P_fused, scale=w.scale, out=out, lse=lse,
                           workspace=wsbuf, stream=stream)
+        elif w.kv_heads != w.H:
+            fd.decode_gqa_paged(q, k, v, table, lens, num_splits=P_fused, scale=w.scale, out=out,
+                                lse=lse, workspace=wsbuf, stream=stream)
         elif k_scale is not None:
             fd.decode_fp8(q, k, v, k_scale, v_scale, seqlens=lens, num_splits=P_fused, scale=w.scale,
                           out=out, lse=lse, workspace=wsbuf, stream=stream)
@@ -451,8 +454,8 @@ def run_ours(args, w):
     alg = algorithmic_bytes(w, lens_h)
     if k_scale is not None:
         alg = alg - kv_bytes(w, lens_h) + kvb + 8 * w.B * w.H
-    if table is not None:  # the block-table entries the kernel reads
-        alg += 4 * sum(-(-int(n) // args.page_size) for n in lens_h) * w.H
+    if table is not None:  # the block-table entries of the valid pages, read once
+        alg += 4 * sum(-(-int(n) // args.page_size) for n in lens_h)
     if args.path != "fused":
         # the split kernel also writes the partials: P (d + 3) floats per (b, h)
         alg += 4 * w.B * w.H * P_split * (w.d + 3) - w.B * w.H * (w.d * ELEMENT_BYTES[w.out_dtype] + 4)
@@ -562,13 +565,16 @@ def main(argv=None):
     ap.add_argument("--path", choices=["fused", "split-mlo", "split-lse"], default="fused",
                     help="fused fd_decode, or fd_decode_split then fd_combine_mlo / fd_combine_lse")
     ap.add_argument("--page-size", type=int, default=0,
-                    help="time fd_decode_paged on the workload laid out in pages of this many tokens")
+                    help="time fd_decode_paged (fd_decode_gqa_paged for a GQA workload) on the "
+                         "workload laid out in pages of this many tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     w = WORKLOADS[args.workload]
     if args.path != "fused" and (args.page_size or args.kv_dtype != "native" or w.kv_heads != w.H):
         ap.error("--path split-* times the contiguous, native-dtype, one-query-per-K/V-head path")
+    if args.kv_dtype != "native" and (args.page_size or w.kv_heads != w.H):
+        ap.error("--kv-dtype e4m3 times the contiguous, one-query-per-K/V-head path")
     ws, _, _ = dist_env()
     if args.gpus > 1 and ws == 1 and "LOCAL_RANK" not in os.environ:
         # launch the per-GPU ranks ourselves

@@ -159,6 +159,33 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
                         size_t workspace_bytes, void *stream);
 
 /*
+ * Grouped-query decode over a paged KV cache: fd_decode_gqa with the
+ * block-table indirection of fd_decode_paged ("从第一性原理推导 Flash
+ * Attention" §7.1 and §8; "adv04: Flash-Decoding" §5).  Same results as
+ * fd_decode_gqa on the gathered rows (bit for bit: the same chunks, the same
+ * arithmetic).
+ *   q                 [B, Hq, d]; out [B, Hq, d]; lse [B, Hq] or NULL
+ *   k_pages, v_pages  [num_pages, Hkv, page_size, d] in `in_dtype` (f16 or
+ *                     bf16): every (page, K/V head) holds page_size
+ *                     consecutive token rows
+ *   block_table       [B, max_pages] int32, as in fd_decode_paged
+ *   seqlens           [B] int32, required; clamped to [0, max_pages*page_size]
+ *   workspace         fd_workspace_size_gqa(B, Hq, Hkv, max_pages*page_size,
+ *                     d, num_splits) bytes, 256-byte aligned
+ * page_size must be a multiple of 32 (the kernel's 32-token chunks then lie
+ * in one page each) and num_pages*Hkv*page_size < 2^31; otherwise
+ * FD_ERR_UNSUPPORTED.  Bad table entries are handled as in fd_decode_paged
+ * (page 0 read instead, FD_ERR_BAD_PAGE reported).  G == 1 is
+ * fd_decode_paged.
+ */
+fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_pages,
+                              const int32_t *block_table, const int32_t *seqlens, int B, int Hq,
+                              int Hkv, int d, int page_size, int max_pages, long long num_pages,
+                              fd_dtype in_dtype, int num_splits, float scale, void *out,
+                              fd_dtype out_dtype, float *lse, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/*
  * fd_decode over an FP8 KV cache: K and V hold OCP E4M3 bytes with one
  * float32 dequantisation scale per (b, h); the value of K[b,h,t,i] is
  * k_scale[b*H+h] * e4m3(k[b,h,t,i]), likewise V.  Storing the cache in FP8

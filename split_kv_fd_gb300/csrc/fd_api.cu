@@ -206,6 +206,63 @@ bool clear_counters(const SplitParams &p, long long rows, cudaStream_t s)
     return cudaMemsetAsync(p.ws_cnt, 0, (size_t)rows * sizeof(unsigned), s) == cudaSuccess;
 }
 
+// The block-table view of a paged K/V cache.
+struct PagedKV {
+    const int32_t *table;
+    int page_size, max_pages;
+    long long num_pages;
+};
+
+// The grouped-query launch once an entry point has checked its arguments:
+// plan, workspace, the K and V tensor maps over `kv_rows` rows of d
+// elements, and the kernel's parameters.  `paged` is null for contiguous
+// K/V [B, Hkv, N, d].
+fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t *seqlens, int B, int Hq,
+                     int Hkv, int N, int d, int in_dtype, int num_splits, float scale, void *out,
+                     int out_dtype, float *lse, void *workspace, size_t workspace_bytes, void *stream,
+                     long long kv_rows, const PagedKV *paged)
+{
+    const int G = Hq / Hkv;
+    const int sms = sm_count();
+    unsigned *st = status_ptr();
+    if (sms <= 0 || !st)
+        return FD_ERR_CUDA;
+    const Plan pl = make_plan(B, Hkv, N, d, num_splits, sms);
+    const WsLayout wl = ws_layout(pl.slots * G, d, (long long)B * Hkv);
+    if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
+        return FD_ERR_WORKSPACE;
+
+    GqaParams gp;
+    memset(&gp, 0, sizeof gp);
+    if (kv_rows > 0) {
+        if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_rows, GqaCfg<__half, 128>::CT) ||
+            !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, GqaCfg<__half, 128>::CT))
+            return FD_ERR_CUDA;
+    }
+    gp.G = G;
+    SplitParams &p = gp.s;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.lens = seqlens;
+    p.B = B;
+    p.H = Hkv;
+    p.N = N;
+    if (paged) {
+        p.paged = 1;
+        p.block_table = paged->table;
+        p.page_size = paged->page_size;
+        p.max_pages = paged->max_pages;
+        p.num_pages = paged->num_pages;
+    }
+    p.q_dtype = in_dtype;
+    set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (!clear_counters(p, (long long)B * Hkv, cs))
+        return FD_ERR_CUDA;
+    return launch_gqa(in_dtype, d, gp, cs) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace fd
 
@@ -499,38 +556,49 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
         !aligned(v, 16) || !aligned(out, 16) || (seqlens && !aligned(seqlens, 4)) ||
         (lse && !aligned(lse, 4)))
         return FD_ERR_INVALID_ARG;
-    const int sms = sm_count();
-    unsigned *st = status_ptr();
-    if (sms <= 0 || !st)
-        return FD_ERR_CUDA;
-    const Plan pl = make_plan(B, Hkv, N, d, num_splits, sms);
-    const WsLayout wl = ws_layout(pl.slots * G, d, (long long)B * Hkv);
-    if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
-        return FD_ERR_WORKSPACE;
+    return gqa_common(q, k, v, seqlens, B, Hq, Hkv, N, d, in_dtype, num_splits, scale, out, out_dtype,
+                      lse, workspace, workspace_bytes, stream, (long long)B * Hkv * N, nullptr);
+}
 
-    GqaParams gp;
-    memset(&gp, 0, sizeof gp);
-    if (N > 0) {
-        const long long rows = (long long)B * Hkv * N;
-        if (!make_kv_map(&gp.tmk, k, in_dtype, d, rows, GqaCfg<__half, 128>::CT) ||
-            !make_kv_map(&gp.tmv, v, in_dtype, d, rows, GqaCfg<__half, 128>::CT))
-            return FD_ERR_CUDA;
-    }
-    gp.G = G;
-    SplitParams &p = gp.s;
-    p.q = q;
-    p.k = k;
-    p.v = v;
-    p.lens = seqlens;
-    p.B = B;
-    p.H = Hkv;
-    p.N = N;
-    p.q_dtype = in_dtype;
-    set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
-    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (!clear_counters(p, (long long)B * Hkv, cs))
-        return FD_ERR_CUDA;
-    return launch_gqa(in_dtype, d, gp, cs) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_pages,
+                              const int32_t *block_table, const int32_t *seqlens, int B, int Hq, int Hkv,
+                              int d, int page_size, int max_pages, long long num_pages, fd_dtype in_dtype,
+                              int num_splits, float scale, void *out, fd_dtype out_dtype, float *lse,
+                              void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (Hkv <= 0 || Hq < 0 || Hq % Hkv != 0)
+        return FD_ERR_INVALID_ARG;
+    if (page_size < 1 || max_pages < 0 || num_pages < 0 ||
+        (long long)page_size * max_pages > 0x7fffffffLL)
+        return FD_ERR_INVALID_ARG;
+    if (Hq == Hkv)
+        return fd_decode_paged(q, k_pages, v_pages, block_table, seqlens, B, Hq, d, page_size, max_pages,
+                               num_pages, in_dtype, num_splits, scale, out, out_dtype, lse, workspace,
+                               workspace_bytes, stream);
+    const int G = Hq / Hkv;
+    const int N = page_size * max_pages;
+    if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(out_dtype) || (d != 64 && d != 128) || G > GqaCfg<__half, 128>::MAXG ||
+        (in_dtype != FD_F16 && in_dtype != FD_BF16))
+        return FD_ERR_UNSUPPORTED;
+    // a chunk of CT tokens must lie in one page, and rows are 32-bit
+    // tensor-map coordinates
+    const long long rows_per_page = (long long)Hkv * page_size;
+    if (page_size % GqaCfg<__half, 128>::CT != 0 || num_pages >= (1LL << 31) ||
+        rows_per_page >= (1LL << 31) || num_pages * rows_per_page >= (1LL << 31))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * Hq == 0)
+        return FD_OK;
+    const bool pages = N > 0;
+    if (!q || !seqlens || !out || (pages && (!k_pages || !v_pages || !block_table || num_pages < 1)) ||
+        !aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(seqlens, 4) || !aligned(block_table, 4) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    const PagedKV pk = {block_table, page_size, max_pages, num_pages};
+    return gqa_common(q, k_pages, v_pages, seqlens, B, Hq, Hkv, N, d, in_dtype, num_splits, scale, out,
+                      out_dtype, lse, workspace, workspace_bytes, stream, pages ? num_pages * rows_per_page : 0,
+                      &pk);
 }
 
 fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,

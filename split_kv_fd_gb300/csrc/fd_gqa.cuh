@@ -80,7 +80,8 @@ template <typename T, int D> struct GqaCfg {
 };
 
 struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
-    CUtensorMap tmk;   // K as [64, B*Hkv*N, d/64] 16-bit elements, boxes [64, CT, d/64], 128B swizzle
+    CUtensorMap tmk;   // K as [64, rows, d/64] 16-bit elements, boxes [64, CT, d/64], 128B swizzle;
+                       // rows = B*Hkv*N, or num_pages*Hkv*page_size when paged
     CUtensorMap tmv;   // V likewise
     SplitParams s;     // s.H = Hkv; s.q is [B, Hkv*G, d]; outputs [B, Hkv*G, ...]
     int G;             // query heads per K/V head, 2..16
@@ -98,8 +99,14 @@ __device__ __forceinline__ uint32_t swz(int r, int c)
 }
 
 // The chunk walk of the split kernel's producer over the CTA's chunks c =
-// first, first + stride, ..., each chunk fetched as d/64 K boxes and d/64 V
-// boxes through the tensor maps.
+// first, first + stride, ..., each chunk fetched as one K box and one V box
+// (d/64 planes each) through the tensor maps.
+//
+// Paged K/V ([num_pages, Hkv, page_size, d], page_size a multiple of CT):
+// a chunk's tokens lie in one aligned CT-token block of the sequence, hence
+// in one page, so its rows are consecutive rows of that page's (page, head)
+// block; the box's rows past them belong to something else and are masked
+// like the rows past a sequence's end.
 template <typename C> struct TmaProducer {
     Seg s;
     long long base;
@@ -107,6 +114,7 @@ template <typename C> struct TmaProducer {
     int stride;
     bool have;
     int t, ntok;
+    int pg;           // paged: block-table entry of chunk c (loaded a chunk ahead)
 
     __device__ __forceinline__ void locate(const SplitParams &p, const Ctx &ctx)
     {
@@ -115,8 +123,11 @@ template <typename C> struct TmaProducer {
             seg_next(p, ctx, s);
         }
         have = s.valid;
-        if (have)
+        if (have) {
             chunk_coords<C::CT>(s, c - base, t, ntok);
+            if (p.paged)
+                pg = __ldg(p.block_table + (long long)s.b * p.max_pages + t / p.page_size);
+        }
     }
 
     __device__ __forceinline__ void start(const SplitParams &p, const Ctx &ctx, int first, int step)
@@ -136,7 +147,18 @@ template <typename C> struct TmaProducer {
             return false;
         if (lane == 0) {
             const SplitParams &p = gp.s;
-            const int row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
+            int row;
+            if (p.paged) {
+                long long page = pg;
+                if (page < 0 || page >= p.num_pages) {
+                    // never read outside the pages: record it, read page 0
+                    atomicOr(p.status, STATUS_BAD_PAGE);
+                    page = 0;
+                }
+                row = (int)((page * p.H + s.h) * p.page_size + t % p.page_size);
+            } else {
+                row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
+            }
             mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
             tma_load_3d(kdst, &gp.tmk, 0, row, 0, bar);
             tma_load_3d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, row, 0, bar);

@@ -192,6 +192,22 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
     assert merge(oa=P(4104)) == 1                # o rows 16-byte aligned
     assert merge(rows=0, oa=None) == 0
 
+    def gqa_paged(B=1, Hq=16, Hkv=2, d=128, ps=64, mp=4, npg=8, dt=2, lens=dm, table=dm):
+        return lib.fd_decode_gqa_paged(dm, dm, dm, table, lens, B, Hq, Hkv, d, ps, mp, npg, dt, 0, 1.0,
+                                       dm, 2, None, dm, MB, None)
+    assert gqa_paged(Hq=6, Hkv=4) == 1            # Hq not a multiple of Hkv
+    assert gqa_paged(ps=0) == 1
+    assert gqa_paged(ps=16) == 2                  # a 32-token chunk would straddle pages
+    assert gqa_paged(ps=48) == 2
+    assert gqa_paged(dt=0) == 2                   # 16-bit K/V only
+    assert gqa_paged(Hq=34) == 2                  # G = 17
+    assert gqa_paged(npg=1 << 22, Hkv=8, ps=128) == 2   # 2^32 page rows: past 32-bit coordinates
+    assert gqa_paged(lens=None) == 1
+    assert gqa_paged(npg=0) == 1
+    assert gqa_paged(table=P(4098)) == 1
+    assert gqa_paged(Hq=2, d=96) == 2             # G = 1 goes to fd_decode_paged's checks
+    assert gqa_paged(B=0, lens=None, table=None) == 0
+
     assert lib.fd_workspace_size_gqa(1, 6, 4, 64, 128, 0) == 0
     assert lib.fd_combine_mlo(dm, dm, dm, 1, 1, 4, 80, dm, 0, None, None) == 2
 

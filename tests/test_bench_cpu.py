@@ -58,3 +58,21 @@ def test_algorithmic_bytes_of_the_gqa_workload():
     assert bench.algorithmic_bytes(w, lens) == kv + w.B * w.H * w.d * 4 + w.B * w.H * 4 + w.B * 4
     t = bench.profiled_traffic(w.name, "gqa_kernel")
     assert t is None or abs(t / bench.algorithmic_bytes(w, lens) - 1) < 0.01
+
+
+@pytest.mark.parametrize("extra", [["--page-size", "64"],
+                                   ["--workload", "decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]])
+def test_fp8_only_for_contiguous_mha(extra):
+    with pytest.raises(SystemExit) as e:
+        bench.main(["--kv-dtype", "e4m3", *extra])
+    assert e.value.code == 2
+
+
+def test_kernel_names_of_the_timed_paths():
+    w = WORKLOADS["decode_b8_h32_n32k_d128_bf16"]
+    g = WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]
+    assert bench.kernel_name(w, False, False) == "fd::split_kernel<bf16, 128>"
+    assert bench.kernel_name(w, True, False) == "fd::split_kernel<e4m3, 128>"
+    assert bench.kernel_name(w, False, True) == "fd::split_kernel<bf16, 128> (paged)"
+    assert bench.kernel_name(g, False, False) == "fd::gqa_kernel<bf16, 128>"
+    assert bench.kernel_name(g, False, True) == "fd::gqa_kernel<bf16, 128> (paged)"

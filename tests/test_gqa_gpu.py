@@ -74,3 +74,49 @@ def test_gqa_group_of_one_is_decode_and_errors():
     kf = torch.randn(1, 2, 64, 64, device=dev)
     with pytest.raises(fd.FDError):
         fd.decode_gqa(qf, kf, kf)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16",
+                                  "decode_gqa_b2_hq64_hkv8_n32k_d128_bf16"])
+def test_gqa_benchmark_workloads_sampled(name):
+    """The benchmarked GQA workloads at full size, in the launch the benchmark
+    times (automatic decomposition, the workload's own output dtype, and f32):
+    sampled query rows against the oracle, each row computed one by one as
+    plain attention of that query head over its K/V head (h // G); every
+    output finite and inside the range of its V column."""
+    from split_kv_fd_gb300.inputs import make_inputs
+    from split_kv_fd_gb300.workloads import WORKLOADS
+    w = WORKLOADS[name]
+    G = w.H // w.kv_heads
+    q, k, v, lens = make_inputs(w, device="cuda")
+    rng = np.random.default_rng(5)
+    rows = {(0, 0), (w.B - 1, w.H - 1), (0, G - 1), (w.B - 1, G)}
+    while len(rows) < 12:
+        rows.add((int(rng.integers(w.B)), int(rng.integers(w.H))))
+    rows = sorted(rows)
+    ref_o, ref_s = [], []
+    for b, h in rows:
+        o, s = oracle.attention(q[b:b + 1, h:h + 1].cpu(), k[b:b + 1, h // G:h // G + 1].cpu(),
+                                v[b:b + 1, h // G:h // G + 1].cpu(), scale=w.scale)
+        ref_o.append(o[0, 0])
+        ref_s.append(s[0, 0])
+    ref_o, ref_s = np.stack(ref_o), np.array(ref_s)
+    bi = torch.tensor([r[0] for r in rows])
+    hi = torch.tensor([r[1] for r in rows])
+    for odt in (DT[w.out_dtype], torch.float32):
+        out, lse = fd.decode_gqa(q, k, v, lens, scale=w.scale, out_dtype=odt)
+        eo = check_out(out[bi, hi], ref_o, w.dtype, what=f"{name} {odt} out")
+        el = check_lse(lse[bi, hi], ref_s, w.dtype, what=f"{name} {odt} lse")
+        print(f"PARITY {name} out={odt} rows={len(rows)} max_err_out={eo:.3e} max_err_lse={el:.3e}")
+        assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
+    # every query row is a convex combination of its K/V head's V rows
+    for b in range(w.B):
+        vb = v[b].float()                                  # [Hkv, N, d]
+        lo = vb.amin(dim=1).repeat_interleave(G, dim=0) - 1e-3
+        hi_ = vb.amax(dim=1).repeat_interleave(G, dim=0) + 1e-3
+        assert bool(torch.all(out[b] >= lo)) and bool(torch.all(out[b] <= hi_)), f"batch {b}"
+        del vb
+    del q, k, v
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
