@@ -162,8 +162,10 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
  * Grouped-query decode over a paged KV cache: fd_decode_gqa with the
  * block-table indirection of fd_decode_paged ("从第一性原理推导 Flash
  * Attention" §7.1 and §8; "adv04: Flash-Decoding" §5).  Same results as
- * fd_decode_gqa on the gathered rows (bit for bit: the same chunks, the same
- * arithmetic).
+ * fd_decode_gqa on the gathered rows: bit for bit when page_size is a
+ * multiple of 32 (the same chunks, the same arithmetic); with 16-token pages
+ * a chunk is staged from its aligned 32-token block, so its tokens may be
+ * shared between warps differently and the rounding may differ.
  *   q                 [B, Hq, d]; out [B, Hq, d]; lse [B, Hq] or NULL
  *   k_pages, v_pages  [num_pages, Hkv, page_size, d] in `in_dtype` (f16 or
  *                     bf16): every (page, K/V head) holds page_size
@@ -172,9 +174,9 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
  *   seqlens           [B] int32, required; clamped to [0, max_pages*page_size]
  *   workspace         fd_workspace_size_gqa(B, Hq, Hkv, max_pages*page_size,
  *                     d, num_splits) bytes, 256-byte aligned
- * page_size must be a multiple of 32 (the kernel's 32-token chunks then lie
- * in one page each) and num_pages*Hkv*page_size < 2^31; otherwise
- * FD_ERR_UNSUPPORTED.  Bad table entries are handled as in fd_decode_paged
+ * page_size must be 16 or a multiple of 32 (a 32-token chunk then lies in
+ * one page, or in two 16-token pages fetched one by one) and
+ * num_pages*Hkv*page_size < 2^31; otherwise FD_ERR_UNSUPPORTED.  Bad table entries are handled as in fd_decode_paged
  * (page 0 read instead, FD_ERR_BAD_PAGE reported).  G == 1 is
  * fd_decode_paged.
  */

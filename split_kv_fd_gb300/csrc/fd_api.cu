@@ -159,16 +159,17 @@ EncodeTiledFn encode_tiled()
 }
 
 // K or V [rows, d] 16-bit as the 3-D map [64 elements, rows, d/64 planes]
-// (strides d*2 and 128 bytes) with boxes [64, box_rows, d/64] and the
+// (strides d*2 and 128 bytes) with boxes [64, box_rows, box_planes] and the
 // 128-byte swizzle: a box lands in shared memory plane by plane.
-bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long rows, int box_rows)
+bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long rows, int box_rows,
+                 int box_planes)
 {
     EncodeTiledFn fn = encode_tiled();
     if (!fn)
         return false;
     const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(d / 64)};
     const cuuint64_t strides[2] = {(cuuint64_t)d * 2, 128};
-    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)(d / 64)};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_planes};
     const cuuint32_t es[3] = {1, 1, 1};
     return fn(m, dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -234,9 +235,14 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
 
     GqaParams gp;
     memset(&gp, 0, sizeof gp);
+    // boxes of one chunk (CT rows, every plane), or with 16-token pages of one
+    // page and one plane
+    gp.pages16 = (paged && paged->page_size == 16) ? 1 : 0;
+    const int box_rows = gp.pages16 ? 16 : GqaCfg<__half, 128>::CT;
+    const int box_planes = gp.pages16 ? 1 : d / 64;
     if (kv_rows > 0) {
-        if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_rows, GqaCfg<__half, 128>::CT) ||
-            !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, GqaCfg<__half, 128>::CT))
+        if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_rows, box_rows, box_planes) ||
+            !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, box_rows, box_planes))
             return FD_ERR_CUDA;
     }
     gp.G = G;
@@ -582,10 +588,10 @@ fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_
     if (!valid_dtype(out_dtype) || (d != 64 && d != 128) || G > GqaCfg<__half, 128>::MAXG ||
         (in_dtype != FD_F16 && in_dtype != FD_BF16))
         return FD_ERR_UNSUPPORTED;
-    // a chunk of CT tokens must lie in one page, and rows are 32-bit
-    // tensor-map coordinates
+    // a chunk of CT tokens lies in one page, or 16-token pages are fetched a
+    // page at a time; rows are 32-bit tensor-map coordinates
     const long long rows_per_page = (long long)Hkv * page_size;
-    if (page_size % GqaCfg<__half, 128>::CT != 0 || num_pages >= (1LL << 31) ||
+    if ((page_size % GqaCfg<__half, 128>::CT != 0 && page_size != 16) || num_pages >= (1LL << 31) ||
         rows_per_page >= (1LL << 31) || num_pages * rows_per_page >= (1LL << 31))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * Hq == 0)

@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
         int issued = 0, landed = 0;
         bool dead = false;
         if (issuer) {
-            prod.start(p, ctx, grp_id, C::GROUPS);
+            prod.start(gp, ctx, grp_id, C::GROUPS);
 #pragma unroll 1
             for (int s = 0; s < C::STAGES; ++s) {
                 if (!prod.issue(gp, ctx, ring_base + s * C::STAGE_BYTES, bar_base + s * 8, lane))
@@ -251,25 +251,33 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                 }
                 int t, ntok_chunk;
                 chunk_coords<C::CT>(cs, c - cbase, t, ntok_chunk);
-                const int nv = ntok_chunk - row0;  // this warp's valid rows
+                // stage row of the chunk's first token: 0, or with 16-token
+                // pages its place in the aligned block
+                const int lead = gp.pages16 ? (t & (C::CT - 1)) : 0;
+                const int vlo = max(lead - row0, 0);                   // this warp's valid
+                const int vhi = min(lead + ntok_chunk - row0, C::WT);  // rows [vlo, vhi)
                 const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
-                if (!dead && nv > 0) {
-                    if (nv < C::WT) {
-                        // rows past the last token may hold padding: zero them in
-                        // every plane of V (a row is 128 contiguous bytes of a plane)
-                        const int nbytes = (C::WT - nv) * 128;
+                if (!dead && vhi > vlo) {
+                    if (vlo > 0 || vhi < C::WT) {
+                        // rows outside the chunk's tokens may hold padding or other
+                        // rows: zero them in every plane of V (a row is 128
+                        // contiguous bytes of a plane)
 #pragma unroll
                         for (int j = 0; j < C::LINES; ++j) {
-                            const uint32_t z0 =
-                                kb + C::CHUNK_BYTES + j * C::PLANE + (uint32_t)(row0 + nv) * 128;
-                            for (int off = lane * 16; off < nbytes; off += 32 * 16)
-                                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(z0 + off), "r"(0u)
-                                             : "memory");
+                            const uint32_t z0 = kb + C::CHUNK_BYTES + j * C::PLANE + (uint32_t)row0 * 128;
+#pragma unroll
+                            for (int off = lane * 16; off < C::WT * 128; off += 32 * 16) {
+                                const int rr = off >> 7;
+                                if (rr < vlo || rr >= vhi)
+                                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(z0 + off),
+                                                 "r"(0u)
+                                                 : "memory");
+                            }
                         }
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
                     }
-                    gqa_chunk<T, C, NQ>(kb, kb + C::CHUNK_BYTES, row0, nv, qb, p.scale_log2, lane, st);
+                    gqa_chunk<T, C, NQ>(kb, kb + C::CHUNK_BYTES, row0, vlo, vhi, qb, p.scale_log2, lane, st);
                 }
                 __syncwarp();
                 // release the stage; the issuer refills it once both warps have

@@ -85,6 +85,7 @@ struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
     CUtensorMap tmv;   // V likewise
     SplitParams s;     // s.H = Hkv; s.q is [B, Hkv*G, d]; outputs [B, Hkv*G, ...]
     int G;             // query heads per K/V head, 2..16
+    int pages16;       // paged with 16-token pages: maps with boxes [64, 16, 1]
 };
 
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s);
@@ -102,11 +103,17 @@ __device__ __forceinline__ uint32_t swz(int r, int c)
 // first, first + stride, ..., each chunk fetched as one K box and one V box
 // (d/64 planes each) through the tensor maps.
 //
-// Paged K/V ([num_pages, Hkv, page_size, d], page_size a multiple of CT):
-// a chunk's tokens lie in one aligned CT-token block of the sequence, hence
-// in one page, so its rows are consecutive rows of that page's (page, head)
-// block; the box's rows past them belong to something else and are masked
-// like the rows past a sequence's end.
+// Paged K/V ([num_pages, Hkv, page_size, d]):
+//  - page_size a multiple of CT: a chunk's tokens lie in one aligned
+//    CT-token block of the sequence, hence in one page, so its rows are
+//    consecutive rows of that page's (page, head) block; the box's rows past
+//    them belong to something else and are masked like the rows past a
+//    sequence's end.
+//  - 16-token pages: the chunk's aligned CT-token block spans two pages.
+//    Each page that holds some of the chunk's tokens is fetched as one
+//    16-row box per plane, into rows 0-15 or 16-31 of the stage, so stage
+//    row r is token (t & ~(CT-1)) + r; the rows before the chunk's first
+//    token are masked too.
 template <typename C> struct TmaProducer {
     Seg s;
     long long base;
@@ -114,10 +121,12 @@ template <typename C> struct TmaProducer {
     int stride;
     bool have;
     int t, ntok;
-    int pg;           // paged: block-table entry of chunk c (loaded a chunk ahead)
+    int pg, pg2;      // paged: table entries of chunk c, loaded a chunk ahead
+                      // (16-token pages: of the block's first and second page)
 
-    __device__ __forceinline__ void locate(const SplitParams &p, const Ctx &ctx)
+    __device__ __forceinline__ void locate(const GqaParams &gp, const Ctx &ctx)
     {
+        const SplitParams &p = gp.s;
         while (s.valid && c >= base + seg_chunks<C::CT>(s)) {
             base += seg_chunks<C::CT>(s);
             seg_next(p, ctx, s);
@@ -125,18 +134,38 @@ template <typename C> struct TmaProducer {
         have = s.valid;
         if (have) {
             chunk_coords<C::CT>(s, c - base, t, ntok);
-            if (p.paged)
-                pg = __ldg(p.block_table + (long long)s.b * p.max_pages + t / p.page_size);
+            if (p.paged) {
+                const int32_t *row = p.block_table + (long long)s.b * p.max_pages;
+                if (gp.pages16) {
+                    const int a = t & ~(C::CT - 1);   // the aligned block
+                    pg = t < a + 16 ? __ldg(row + a / 16) : 0;
+                    pg2 = t + ntok > a + 16 ? __ldg(row + a / 16 + 1) : 0;
+                } else {
+                    pg = __ldg(row + t / p.page_size);
+                }
+            }
         }
     }
 
-    __device__ __forceinline__ void start(const SplitParams &p, const Ctx &ctx, int first, int step)
+    __device__ __forceinline__ void start(const GqaParams &gp, const Ctx &ctx, int first, int step)
     {
-        seg_first(p, ctx, s);
+        seg_first(gp.s, ctx, s);
         base = 0;
         c = first;
         stride = step;
-        locate(p, ctx);
+        locate(gp, ctx);
+    }
+
+    // A table entry checked before use: outside [0, num_pages) it is
+    // recorded and replaced by page 0, so no row outside the pages is read.
+    __device__ __forceinline__ static long long checked_page(const SplitParams &p, int entry)
+    {
+        long long page = entry;
+        if (page < 0 || page >= p.num_pages) {
+            atomicOr(p.status, STATUS_BAD_PAGE);
+            page = 0;
+        }
+        return page;
     }
 
     // Copies the full CT-row boxes (rows past the tensor end read as zeros).
@@ -147,24 +176,37 @@ template <typename C> struct TmaProducer {
             return false;
         if (lane == 0) {
             const SplitParams &p = gp.s;
-            int row;
-            if (p.paged) {
-                long long page = pg;
-                if (page < 0 || page >= p.num_pages) {
-                    // never read outside the pages: record it, read page 0
-                    atomicOr(p.status, STATUS_BAD_PAGE);
-                    page = 0;
+            if (gp.pages16) {
+                const int a = t & ~(C::CT - 1);
+                const bool first = t < a + 16, second = t + ntok > a + 16;
+                constexpr uint32_t BOX = 16 * 128;   // one plane of one page
+                mbar_arrive_expect_tx(bar, 2 * C::LINES * BOX * ((first ? 1u : 0u) + (second ? 1u : 0u)));
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (half == 0 ? !first : !second)
+                        continue;
+                    const long long page = checked_page(p, half == 0 ? pg : pg2);
+                    const int row = (int)((page * p.H + s.h) * 16);
+#pragma unroll
+                    for (int j = 0; j < C::LINES; ++j) {
+                        const uint32_t off = (uint32_t)(j * C::PLANE + half * BOX);
+                        tma_load_3d(kdst + off, &gp.tmk, 0, row, j, bar);
+                        tma_load_3d(kdst + C::CHUNK_BYTES + off, &gp.tmv, 0, row, j, bar);
+                    }
                 }
-                row = (int)((page * p.H + s.h) * p.page_size + t % p.page_size);
             } else {
-                row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
+                int row;
+                if (p.paged)
+                    row = (int)((checked_page(p, pg) * p.H + s.h) * p.page_size + t % p.page_size);
+                else
+                    row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
+                mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
+                tma_load_3d(kdst, &gp.tmk, 0, row, 0, bar);
+                tma_load_3d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, row, 0, bar);
             }
-            mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
-            tma_load_3d(kdst, &gp.tmk, 0, row, 0, bar);
-            tma_load_3d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, row, 0, bar);
         }
         c += stride;
-        locate(gp.s, ctx);
+        locate(gp, ctx);
         return true;
     }
 };
@@ -179,12 +221,13 @@ template <typename C, int NQ> struct GqaState {
     float l[NQ][2];   // this thread's share of the running sums
 };
 
-// One warp's WT = 16 rows of a chunk (rows row0 .. row0+15 of the stage, the
-// first `nvalid` of them real tokens): S^T = K Q^T on the tensor cores, the
-// block-wise online-softmax update in fp32, then O^T += V^T (P_hi + P_lo)^T.
-// qb holds Q^T as B fragments: qb[j][s] = heads of column tile j, k-step s.
+// One warp's WT = 16 rows of a chunk (rows row0 .. row0+15 of the stage,
+// rows vlo .. vhi-1 of them real tokens, vlo < vhi; V's other rows already
+// zeroed): S^T = K Q^T on the tensor cores, the block-wise online-softmax
+// update in fp32, then O^T += V^T (P_hi + P_lo)^T.  qb holds Q^T as B
+// fragments: qb[j][s] = heads of column tile j, k-step s.
 template <typename T, typename C, int NQ>
-__device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int row0, int nvalid,
+__device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int row0, int vlo, int vhi,
                                           const uint32_t (*qb)[C::KSTEPS][2], float scale_log2, int lane,
                                           GqaState<C, NQ> &st)
 {
@@ -205,9 +248,9 @@ __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int 
         for (int j = 0; j < NQ; ++j)
             Mma<T>::run((s & 1) ? sx[j] : sc[j], a, qb[j][s][0], qb[j][s][1]);
     }
-    // base-2 scale; tokens lane/4 and lane/4 + 8 past the last valid one are masked
+    // base-2 scale; tokens lane/4 and lane/4 + 8 outside the valid rows are masked
     const int r = lane >> 2;
-    const bool v0 = r < nvalid, v1 = r + 8 < nvalid;
+    const bool v0 = r >= vlo && r < vhi, v1 = r + 8 >= vlo && r + 8 < vhi;
 #pragma unroll
     for (int j = 0; j < NQ; ++j) {
         sc[j][0] = v0 ? (sc[j][0] + sx[j][0]) * scale_log2 : -INFINITY;
@@ -226,7 +269,7 @@ __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int 
             x0 = fmaxf(x0, __shfl_xor_sync(FULL_MASK, x0, o));
             x1 = fmaxf(x1, __shfl_xor_sync(FULL_MASK, x1, o));
         }
-        const float mn0 = fmaxf(st.m[j][0], x0), mn1 = fmaxf(st.m[j][1], x1);  // finite: nvalid >= 1
+        const float mn0 = fmaxf(st.m[j][0], x0), mn1 = fmaxf(st.m[j][1], x1);  // finite: vhi > vlo
         const float a0 = ex2(st.m[j][0] - mn0), a1 = ex2(st.m[j][1] - mn1);
         st.m[j][0] = mn0;
         st.m[j][1] = mn1;

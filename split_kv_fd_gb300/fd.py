@@ -322,7 +322,7 @@ def decode_gqa_paged(q, k_pages, v_pages, block_table, seqlens, num_splits=0, sc
     Returns ``(out, lse)``.
 
     q [B, Hq, d]; k_pages/v_pages [num_pages, Hkv, page_size, d] with Hq a
-    multiple of Hkv and page_size a multiple of 32; block_table [B,
+    multiple of Hkv and page_size 16 or a multiple of 32; block_table [B,
     max_pages] int32; seqlens [B] int32 (required).
     """
     _need_cuda(q, k_pages, v_pages, block_table, seqlens)

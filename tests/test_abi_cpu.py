@@ -197,7 +197,7 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
                                        dm, 2, None, dm, MB, None)
     assert gqa_paged(Hq=6, Hkv=4) == 1            # Hq not a multiple of Hkv
     assert gqa_paged(ps=0) == 1
-    assert gqa_paged(ps=16) == 2                  # a 32-token chunk would straddle pages
+    assert gqa_paged(ps=8) == 2                   # pages of 16 or a multiple of 32 tokens
     assert gqa_paged(ps=48) == 2
     assert gqa_paged(dt=0) == 2                   # 16-bit K/V only
     assert gqa_paged(Hq=34) == 2                  # G = 17
