@@ -21,8 +21,11 @@
  *       o_part [B, H, P, d] float32,  m_part / l_part / lse_part [B, H, P]
  *     Tokens at index >= seqlens[b] are never read.
  *   - q, K and V share one storage dtype; accumulation is always float32.
- *   - Supported head dims: 64 and 128.  q, K, V, out, o_part must be 16-byte
- *     aligned; seqlens, lse, m/l/lse partials 4-byte aligned.
+ *   - Supported head dims: 64 and 128; also 256 with f16, bf16 or E4M3 K/V
+ *     (fd_decode, fd_decode_split, the combines, fd_decode_paged,
+ *     fd_decode_fp8, fd_decode_noalloc; grouped-query decode with G > 1
+ *     stays at 64 and 128).  q, K, V, out, o_part must be 16-byte aligned;
+ *     seqlens, lse, m/l/lse partials 4-byte aligned.
  *   - All m and lse values are natural-log quantities of the *scaled* scores.
  *     An empty split is (o = 0, m = -inf, l = 0, lse = -inf); an empty
  *     sequence (len 0) gives out = 0, lse = -inf.

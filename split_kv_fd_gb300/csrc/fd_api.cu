@@ -108,17 +108,29 @@ bool sizes_ok(int B, int H, int N, int d)
     return B >= 0 && H >= 0 && N >= 0 && d > 0 && (long long)B * H <= (1LL << 31) - 1;
 }
 
+// Head dims of the split kernel: 64 and 128 for every storage type, 256 for
+// 16-bit and E4M3 storage (a float32 row of 256 would span 64 lanes).
+bool split_dim_ok(int dtype, int d)
+{
+    return d == 64 || d == 128 || (d == 256 && dtype != FD_F32);
+}
+
+template <typename T> size_t split_smem_t(int d, int decomp, int B)
+{
+    return d == 64    ? SplitCfg<T, 64>::smem_bytes(decomp, B)
+           : d == 128 ? SplitCfg<T, 128>::smem_bytes(decomp, B)
+                      : SplitCfg<T, 256>::smem_bytes(decomp, B);
+}
+
 size_t split_smem(int dtype, int d, int decomp, int B)
 {
     if (dtype == FD_E4M3)
-        return d == 64 ? SplitCfg<__nv_fp8_e4m3, 64>::smem_bytes(decomp, B)
-                       : SplitCfg<__nv_fp8_e4m3, 128>::smem_bytes(decomp, B);
+        return split_smem_t<__nv_fp8_e4m3>(d, decomp, B);
     if (dtype == FD_F32)
         return d == 64 ? SplitCfg<float, 64>::smem_bytes(decomp, B) : SplitCfg<float, 128>::smem_bytes(decomp, B);
     if (dtype == FD_F16)
-        return d == 64 ? SplitCfg<__half, 64>::smem_bytes(decomp, B) : SplitCfg<__half, 128>::smem_bytes(decomp, B);
-    return d == 64 ? SplitCfg<__nv_bfloat16, 64>::smem_bytes(decomp, B)
-                   : SplitCfg<__nv_bfloat16, 128>::smem_bytes(decomp, B);
+        return split_smem_t<__half>(d, decomp, B);
+    return split_smem_t<__nv_bfloat16>(d, decomp, B);
 }
 
 fd_status launch(int dtype, int d, const SplitParams &p, int decomp, cudaStream_t s)
@@ -359,7 +371,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
 {
     if (!sizes_ok(B, H, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || !split_dim_ok(in_dtype, d))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * H == 0)
         return FD_OK;
@@ -399,7 +411,7 @@ fd_status fd_decode_split(const void *q, const void *k, const void *v, const int
 {
     if (!sizes_ok(B, H, N, d) || num_splits < 1 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(in_dtype) || (d != 64 && d != 128))
+    if (!valid_dtype(in_dtype) || !split_dim_ok(in_dtype, d))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * H == 0)
         return FD_OK;
@@ -442,7 +454,7 @@ static fd_status combine_common(const float *o_part, const float *a, const float
 {
     if (B < 0 || H < 0 || P < 1 || P > 8192 || d <= 0 || (long long)B * H > (1LL << 31) - 1)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(out_dtype) || (d != 64 && d != 128))
+    if (!valid_dtype(out_dtype) || (d != 64 && d != 128 && d != 256))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * H == 0)
         return FD_OK;
@@ -615,7 +627,7 @@ fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const vo
 {
     if (!sizes_ok(B, H, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || !split_dim_ok(FD_E4M3, d))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * H == 0)
         return FD_OK;
@@ -662,7 +674,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     const int N = page_size * max_pages;
     if (!sizes_ok(B, H, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || !split_dim_ok(in_dtype, d))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * H == 0)
         return FD_OK;
@@ -751,7 +763,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
 {
     if (!sizes_ok(B, H, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || !split_dim_ok(in_dtype, d))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * H == 0)
         return FD_OK;

@@ -122,6 +122,10 @@ template <typename T, int D> struct SplitCfg {
     static_assert(WT % TPW == 0 && TOK >= 1, "chunk must cover whole warp steps");
     static_assert(WARPS % GW == 0, "warps must form whole groups");
     static_assert(D % 32 == 0, "the merge warp holds D / 32 output elements per lane");
+    static_assert(RING_BYTES + BAR_BYTES + RED_BYTES + (BALANCED_MAX_B + 1) * 8 + BALANCED_MAX_B * 4 + 1024 <=
+                      227 * 1024,
+                  "ring, barriers, segment buffers, the balanced prefix sums and the static shared "
+                  "memory fit in one CTA's 227 KB");
 
     static size_t smem_bytes(int decomp, int B)
     {

@@ -9,6 +9,8 @@ cudaError_t launch_split_f16(int d, const SplitParams &p, size_t smem, cudaStrea
         return launch_split_t<__half, 64>(p, smem, s);
     if (d == 128)
         return launch_split_t<__half, 128>(p, smem, s);
+    if (d == 256)
+        return launch_split_t<__half, 256>(p, smem, s);
     return cudaErrorInvalidValue;
 }
 

@@ -68,6 +68,10 @@ WORKLOADS["decode_gqa_b2_hq64_hkv8_n32k_d128_bf16"] = Workload(
 WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"] = Workload(
     "decode_gqa_b8_hq64_hkv8_n32k_d128_bf16", 8, 64, 32768, 128, "bf16", "bf16", 0, Hkv=8)
 
+# head dim 256: the benchmark's 4 GiB of K/V as 16 heads of 256 per sequence
+WORKLOADS["decode_b8_h16_n32k_d256_bf16"] = Workload(
+    "decode_b8_h16_n32k_d256_bf16", 8, 16, 32768, 256, "bf16", "bf16", 0)
+
 # the workload the benchmark times by default: uniform 32K-token sequences
 BENCH_DEFAULT = "decode_b8_h32_n32k_d128_bf16"
 
