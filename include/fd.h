@@ -23,9 +23,9 @@
  *   - q, K and V share one storage dtype; accumulation is always float32.
  *   - Supported head dims: 64 and 128; also 256 with f16, bf16 or E4M3 K/V
  *     (fd_decode, fd_decode_split, the combines, fd_decode_paged,
- *     fd_decode_fp8, fd_decode_noalloc; grouped-query decode with G > 1
- *     stays at 64 and 128).  q, K, V, out, o_part must be 16-byte aligned;
- *     seqlens, lse, m/l/lse partials 4-byte aligned.
+ *     fd_decode_fp8, fd_decode_noalloc; grouped-query decode with
+ *     G = 2..8).  q, K, V, out, o_part must be 16-byte aligned; seqlens,
+ *     lse, m/l/lse partials 4-byte aligned.
  *   - All m and lse values are natural-log quantities of the *scaled* scores.
  *     An empty split is (o = 0, m = -inf, l = 0, lse = -inf); an empty
  *     sequence (len 0) gives out = 0, lse = -inf.
@@ -152,7 +152,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  * G == 1 is fd_decode.  For G = 2..16 the per-chunk contraction runs on the
  * tensor cores, which need 16-bit operands: in_dtype f16 or bf16, and
  * B*Hkv*N < 2^31.  The workspace size is fd_workspace_size_gqa(...).
- * Returns FD_ERR_UNSUPPORTED for G > 16 or f32 with G > 1.
+ * Returns FD_ERR_UNSUPPORTED for G > 16 (G > 8 at d = 256) or f32 with G > 1.
  */
 size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_splits);
 

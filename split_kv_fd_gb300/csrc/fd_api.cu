@@ -115,6 +115,15 @@ bool split_dim_ok(int dtype, int d)
     return d == 64 || d == 128 || (d == 256 && dtype != FD_F32);
 }
 
+// Head dims and group sizes of the grouped-query kernel: G up to 16 at 64
+// and 128, up to 8 at 256.
+bool gqa_dim_ok(int d, int G)
+{
+    if (d == 64 || d == 128)
+        return G <= GqaCfg<__half, 128>::MAXG;
+    return d == 256 && G <= GqaCfg<__half, 256>::MAXG;
+}
+
 template <typename T> size_t split_smem_t(int d, int decomp, int B)
 {
     return d == 64    ? SplitCfg<T, 64>::smem_bytes(decomp, B)
@@ -563,7 +572,7 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
     const int G = Hq / Hkv;
     if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(out_dtype) || (d != 64 && d != 128) || G > GqaCfg<__half, 128>::MAXG ||
+    if (!valid_dtype(out_dtype) || !gqa_dim_ok(d, G) ||
         (in_dtype != FD_F16 && in_dtype != FD_BF16))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * Hkv * N >= (1LL << 31))
@@ -597,7 +606,7 @@ fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_
     const int N = page_size * max_pages;
     if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(out_dtype) || (d != 64 && d != 128) || G > GqaCfg<__half, 128>::MAXG ||
+    if (!valid_dtype(out_dtype) || !gqa_dim_ok(d, G) ||
         (in_dtype != FD_F16 && in_dtype != FD_BF16))
         return FD_ERR_UNSUPPORTED;
     // a chunk of CT tokens lies in one page, or 16-token pages are fetched a

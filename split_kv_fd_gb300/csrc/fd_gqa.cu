@@ -434,14 +434,24 @@ static cudaError_t launch_gqa_t(const GqaParams &gp, cudaStream_t s)
 template <typename T, int D>
 static cudaError_t launch_gqa_d(const GqaParams &gp, cudaStream_t s)
 {
-    return gp.G <= 8 ? launch_gqa_t<T, D, 1>(gp, s) : launch_gqa_t<T, D, 2>(gp, s);
+    if constexpr (D == 256)
+        return launch_gqa_t<T, D, 1>(gp, s);   // G <= 8
+    else
+        return gp.G <= 8 ? launch_gqa_t<T, D, 1>(gp, s) : launch_gqa_t<T, D, 2>(gp, s);
+}
+
+template <typename T> static cudaError_t launch_gqa_dt(int d, const GqaParams &gp, cudaStream_t s)
+{
+    if (d == 64)
+        return launch_gqa_d<T, 64>(gp, s);
+    if (d == 128)
+        return launch_gqa_d<T, 128>(gp, s);
+    return launch_gqa_d<T, 256>(gp, s);
 }
 
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s)
 {
-    if (dtype == 2)
-        return d == 64 ? launch_gqa_d<__nv_bfloat16, 64>(gp, s) : launch_gqa_d<__nv_bfloat16, 128>(gp, s);
-    return d == 64 ? launch_gqa_d<__half, 64>(gp, s) : launch_gqa_d<__half, 128>(gp, s);
+    return dtype == 2 ? launch_gqa_dt<__nv_bfloat16>(d, gp, s) : launch_gqa_dt<__half>(d, gp, s);
 }
 
 }  // namespace fd

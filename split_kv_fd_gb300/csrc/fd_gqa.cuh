@@ -47,10 +47,13 @@ namespace fd {
 #define FD_GQA_GW 2
 #endif
 
+// Head dim 256: 4 warps, so that two stages per group still make 128 KB in
+// flight (a 32-token chunk of K and V is then 32 KB), and G <= 8 (one column
+// tile: O^T alone takes 64 accumulator registers per thread).
 template <typename T, int D> struct GqaCfg {
     static constexpr int ROW = D * 2;              // bytes per token row (16-bit types)
     static constexpr int LINES = D / 64;           // 128-byte lines per row
-    static constexpr int WARPS = 8;
+    static constexpr int WARPS = D == 256 ? 4 : 8;
     static constexpr int THREADS = WARPS * 32;
     static constexpr int GW = FD_GQA_GW;           // warps sharing one ring
     static constexpr int GROUPS = WARPS / GW;
@@ -64,8 +67,8 @@ template <typename T, int D> struct GqaCfg {
     static constexpr int BAR_BYTES = GROUPS * STAGES * 2 * 8;
     static constexpr int KSTEPS = D / 16;          // k-steps of S^T = K Q^T
     static constexpr int MT = D / 16;              // 16-row tiles of O^T
-    static constexpr int MAXG = 16;
-    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int MAXG = D == 256 ? 8 : 16;
+    static_assert(D == 64 || D == 128 || D == 256, "head dim");
     static_assert(PLANE % 1024 == 0, "planes stay 1024-byte aligned for the swizzle");
 
     // dynamic shared memory: 1024 of alignment slack, ring, barriers, the

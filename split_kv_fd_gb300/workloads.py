@@ -72,6 +72,11 @@ WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"] = Workload(
 WORKLOADS["decode_b8_h16_n32k_d256_bf16"] = Workload(
     "decode_b8_h16_n32k_d256_bf16", 8, 16, 32768, 256, "bf16", "bf16", 0)
 
+# grouped-query decode at head dim 256: 16 query heads over 8 K/V heads
+# (G = 2), 32K tokens per sequence (2 GiB of K/V)
+WORKLOADS["decode_gqa_b8_hq16_hkv8_n32k_d256_bf16"] = Workload(
+    "decode_gqa_b8_hq16_hkv8_n32k_d256_bf16", 8, 16, 32768, 256, "bf16", "bf16", 0, Hkv=8)
+
 # the workload the benchmark times by default: uniform 32K-token sequences
 BENCH_DEFAULT = "decode_b8_h32_n32k_d128_bf16"
 

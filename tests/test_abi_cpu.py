@@ -154,7 +154,7 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
     assert gqa(1, 34, 2, 64, 128) == 2           # G = 17 > 16
     assert gqa(1, 16, 2, 64, 128, dt=0) == 2     # G > 1 needs 16-bit K/V
     assert gqa(1, 16, 2, 64, 96) == 2            # head dim
-    assert gqa(1, 16, 2, 64, 256) == 2           # 256 only through the split kernel (G = 1)
+    assert gqa(1, 32, 2, 64, 256) == 2           # G = 16 > 8 at d = 256
     assert gqa(1, 8, 8, 64, 96) == 2             # G = 1 goes to fd_decode's checks
     assert gqa(1, 16, 2, 1 << 30, 128) == 2      # 2^31 K/V rows: past 32-bit coordinates
     assert gqa(1, 16, 2, 64, 128, q=None) == 1

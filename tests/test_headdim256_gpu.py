@@ -2,7 +2,8 @@
 kernel, against the float64 oracle: fused decode with both decompositions,
 the two-call path with both merges, the paged and FP8 caches, the no-alloc
 entry point, and many short sequences (the merge warp's segment buffers
-hold 256-element rows).  GQA with G > 1 stays at 64 and 128."""
+hold 256-element rows); and grouped-query decode at d = 256 (G <= 8),
+contiguous and paged."""
 import pytest
 import torch
 
@@ -94,12 +95,48 @@ def test_many_short_sequences_d256():
     check_lse(lse, ref_lse, "bf16")
 
 
-def test_gqa_d256_only_as_one_group():
+def _gqa_case(B, Hq, Hkv, N, dtype, lens, seed):
+    _, k, v, lt = random_case(B, Hkv, N, D, dtype, lens=lens, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn(B, Hq, D, generator=g).to({"bf16": torch.bfloat16, "f16": torch.float16}[dtype])
+    return q, k, v, lt
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("G", [2, 4, 8])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_gqa_d256(dtype, G, num_splits):
+    """The tensor-core kernel at d = 256 (4 warps, G <= 8), contiguous and in
+    16- and 64-token pages."""
+    q, k, v, lt = _gqa_case(3, 2 * G, 2, 700, dtype, [700, 0, 333], seed=G + num_splits)
+    ref_out, ref_lse = oracle.attention_gqa(q, k, v, lens=lt)
+    qd, ld = q.to(DEV), lt.to(DEV)
+    out, lse = fd.decode_gqa(qd, k.to(DEV), v.to(DEV), ld, num_splits=num_splits, out_dtype=torch.float32)
+    check_out(out, ref_out, dtype)
+    check_lse(lse, ref_lse, dtype)
+    for ps in (16, 64):
+        kp, vp, table = to_paged(k, v, ps, seed=ps)
+        pout, plse = fd.decode_gqa_paged(qd, kp.to(DEV), vp.to(DEV), table.to(DEV), ld,
+                                         num_splits=num_splits, out_dtype=torch.float32)
+        check_out(pout, ref_out, dtype)
+        check_lse(plse, ref_lse, dtype)
+
+
+def test_gqa_d256_long_sequence_in_many_pieces():
+    """One 100K-token sequence (G = 8): one piece per CTA, merged by the last."""
+    q, k, v, lt = _gqa_case(1, 8, 1, 100000, "bf16", None, seed=31)
+    ref_out, ref_lse = oracle.attention_gqa(q, k, v, lens=lt)
+    out, lse = fd.decode_gqa(q.to(DEV), k.to(DEV), v.to(DEV), lt.to(DEV), out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
+
+
+def test_gqa_d256_limits():
     q, k, v, lt = random_case(2, 4, 300, D, "bf16", lens=[300, 9], seed=15)
     ref_out, ref_lse = oracle.attention(q, k, v, lens=lt)
     out, lse = fd.decode_gqa(q.to(DEV), k.to(DEV), v.to(DEV), lt.to(DEV), out_dtype=torch.float32)
     check_out(out, ref_out, "bf16")      # G = 1 is fd_decode
-    q2 = torch.randn(2, 8, D).to(torch.bfloat16)
+    q16 = torch.randn(2, 64, D).to(torch.bfloat16)
     with pytest.raises(fd.FDError) as e:
-        fd.decode_gqa(q2.to(DEV), k.to(DEV), v.to(DEV), lt.to(DEV))
-    assert e.value.status == 2           # FD_ERR_UNSUPPORTED: the tensor-core path is 64/128
+        fd.decode_gqa(q16.to(DEV), k.to(DEV), v.to(DEV), lt.to(DEV))
+    assert e.value.status == 2           # G = 16 > 8 at d = 256: FD_ERR_UNSUPPORTED
