@@ -50,7 +50,8 @@ L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {
     "split_kernel": ["fd_split.cuh", "fd_device.cuh", "fd_internal.h", "fd_split_bf16.cu",
                      "fd_split_f16.cu", "fd_split_f32.cu", "fd_split_fp8.cu"],
-    "gqa_kernel": ["fd_gqa.cuh", "fd_gqa.cu", "fd_split.cuh", "fd_device.cuh", "fd_internal.h"],
+    "gqa_kernel": ["fd_gqa.cuh", "fd_gqa_kernel.cuh", "fd_gqa_bf16.cu", "fd_gqa_f16.cu", "fd_split.cuh",
+                   "fd_device.cuh", "fd_internal.h"],
 }
 
 

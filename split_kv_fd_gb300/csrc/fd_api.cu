@@ -257,10 +257,10 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     GqaParams gp;
     memset(&gp, 0, sizeof gp);
     // boxes of one chunk (CT rows, every plane), or with 16-token pages of one
-    // page and one plane
+    // page (16 rows, every plane)
     gp.pages16 = (paged && paged->page_size == 16) ? 1 : 0;
     const int box_rows = gp.pages16 ? 16 : GqaCfg<__half, 128>::CT;
-    const int box_planes = gp.pages16 ? 1 : d / 64;
+    const int box_planes = d / 64;
     if (kv_rows > 0) {
         if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_rows, box_rows, box_planes) ||
             !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, box_rows, box_planes))

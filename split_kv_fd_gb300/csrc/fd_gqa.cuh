@@ -88,10 +88,11 @@ struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
     CUtensorMap tmv;   // V likewise
     SplitParams s;     // s.H = Hkv; s.q is [B, Hkv*G, d]; outputs [B, Hkv*G, ...]
     int G;             // query heads per K/V head, 2..16
-    int pages16;       // paged with 16-token pages: maps with boxes [64, 16, 1]
+    int pages16;       // paged with 16-token pages: boxes [64, 16, d/64], the P16 stage layout
 };
 
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s);
+cudaError_t launch_gqa_bf16(int d, const GqaParams &gp, cudaStream_t s);
 
 // Byte offset of 16-byte column c of row r in a stage of 64-element planes
 // written by the 128B swizzle (stage base 1024-aligned): plane c/8, and
@@ -100,6 +101,25 @@ template <int PLANE>
 __device__ __forceinline__ uint32_t swz(int r, int c)
 {
     return (uint32_t)((c >> 3) * PLANE + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Stage layouts.  The default one is d/64 planes of CT rows (one box per
+// chunk and operand).  With 16-token pages (P16) each 16-row half of the
+// stage is its own block of d/64 planes of 16 rows, so one box per page and
+// operand fills a half; a warp's 16 rows are one half either way, and every
+// plane starts on a 1024-byte boundary, so the swizzle phase of row r is
+// r % 8 in both.
+template <typename C, bool P16> __device__ __forceinline__ uint32_t stage_row(int r, int plane)
+{
+    if constexpr (P16)
+        return (uint32_t)((r >> 4) * (C::LINES * 2048) + plane * 2048 + (r & 15) * 128);
+    else
+        return (uint32_t)(plane * C::PLANE + r * 128);
+}
+
+template <typename C, bool P16> __device__ __forceinline__ uint32_t stage_off(int r, int c)
+{
+    return stage_row<C, P16>(r, c >> 3) + (uint32_t)((((c & 7) ^ (r & 7)) << 4));
 }
 
 // The chunk walk of the split kernel's producer over the CTA's chunks c =
@@ -112,12 +132,12 @@ __device__ __forceinline__ uint32_t swz(int r, int c)
 //    consecutive rows of that page's (page, head) block; the box's rows past
 //    them belong to something else and are masked like the rows past a
 //    sequence's end.
-//  - 16-token pages: the chunk's aligned CT-token block spans two pages.
-//    Each page that holds some of the chunk's tokens is fetched as one
-//    16-row box per plane, into rows 0-15 or 16-31 of the stage, so stage
+//  - 16-token pages (P16): the chunk's aligned CT-token block spans two
+//    pages.  Each page that holds some of the chunk's tokens is fetched as
+//    one box [64, 16, d/64] into its half of the stage (stage_row), so stage
 //    row r is token (t & ~(CT-1)) + r; the rows before the chunk's first
 //    token are masked too.
-template <typename C> struct TmaProducer {
+template <typename C, bool P16> struct TmaProducer {
     Seg s;
     long long base;
     long long c;
@@ -139,7 +159,7 @@ template <typename C> struct TmaProducer {
             chunk_coords<C::CT>(s, c - base, t, ntok);
             if (p.paged) {
                 const int32_t *row = p.block_table + (long long)s.b * p.max_pages;
-                if (gp.pages16) {
+                if constexpr (P16) {
                     const int a = t & ~(C::CT - 1);   // the aligned block
                     pg = t < a + 16 ? __ldg(row + a / 16) : 0;
                     pg2 = t + ntok > a + 16 ? __ldg(row + a / 16 + 1) : 0;
@@ -179,23 +199,19 @@ template <typename C> struct TmaProducer {
             return false;
         if (lane == 0) {
             const SplitParams &p = gp.s;
-            if (gp.pages16) {
+            if constexpr (P16) {
                 const int a = t & ~(C::CT - 1);
                 const bool first = t < a + 16, second = t + ntok > a + 16;
-                constexpr uint32_t BOX = 16 * 128;   // one plane of one page
-                mbar_arrive_expect_tx(bar, 2 * C::LINES * BOX * ((first ? 1u : 0u) + (second ? 1u : 0u)));
+                constexpr uint32_t HALF = C::LINES * 16 * 128;   // one page: 16 rows, every plane
+                mbar_arrive_expect_tx(bar, 2 * HALF * ((first ? 1u : 0u) + (second ? 1u : 0u)));
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     if (half == 0 ? !first : !second)
                         continue;
                     const long long page = checked_page(p, half == 0 ? pg : pg2);
                     const int row = (int)((page * p.H + s.h) * 16);
-#pragma unroll
-                    for (int j = 0; j < C::LINES; ++j) {
-                        const uint32_t off = (uint32_t)(j * C::PLANE + half * BOX);
-                        tma_load_3d(kdst + off, &gp.tmk, 0, row, j, bar);
-                        tma_load_3d(kdst + C::CHUNK_BYTES + off, &gp.tmv, 0, row, j, bar);
-                    }
+                    tma_load_3d(kdst + half * HALF, &gp.tmk, 0, row, 0, bar);
+                    tma_load_3d(kdst + C::CHUNK_BYTES + half * HALF, &gp.tmv, 0, row, 0, bar);
                 }
             } else {
                 int row;
@@ -229,7 +245,7 @@ template <typename C, int NQ> struct GqaState {
 // zeroed): S^T = K Q^T on the tensor cores, the block-wise online-softmax
 // update in fp32, then O^T += V^T (P_hi + P_lo)^T.  qb holds Q^T as B
 // fragments: qb[j][s] = heads of column tile j, k-step s.
-template <typename T, typename C, int NQ>
+template <typename T, typename C, int NQ, bool P16>
 __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int row0, int vlo, int vhi,
                                           const uint32_t (*qb)[C::KSTEPS][2], float scale_log2, int lane,
                                           GqaState<C, NQ> &st)
@@ -246,7 +262,7 @@ __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int 
 #pragma unroll
     for (int s = 0; s < C::KSTEPS; ++s) {
         uint32_t a[4];
-        ldsm_x4(kstage + swz<C::PLANE>(ktok, 2 * s + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        ldsm_x4(kstage + stage_off<C, P16>(ktok, 2 * s + (lane >> 4)), a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int j = 0; j < NQ; ++j)
             Mma<T>::run((s & 1) ? sx[j] : sc[j], a, qb[j][s][0], qb[j][s][1]);
@@ -302,7 +318,7 @@ __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int 
 #pragma unroll
     for (int i = 0; i < C::MT; ++i) {
         uint32_t a[4];
-        ldsm_x4_t(vstage + swz<C::PLANE>(vtok, 2 * i + ((lane >> 3) & 1)), a[0], a[1], a[2], a[3]);
+        ldsm_x4_t(vstage + stage_off<C, P16>(vtok, 2 * i + ((lane >> 3) & 1)), a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int j = 0; j < NQ; ++j) {
             Mma<T>::run(st.o[i][j], a, ph[j][0], ph[j][1]);

@@ -1,5 +1,7 @@
-// fd_gqa.cu -- the grouped-query decode kernel (see fd_gqa.cuh) and its
-// launcher.
+// fd_gqa_kernel.cuh -- the grouped-query decode kernel (see fd_gqa.cuh) and
+// its launch templates, instantiated per storage type by fd_gqa_bf16.cu and
+// fd_gqa_f16.cu (two translation units that compile in parallel).
+#pragma once
 #include "fd_gqa.cuh"
 
 namespace fd {
@@ -120,7 +122,7 @@ __device__ __forceinline__ void gqa_merge_pieces_long(const SplitParams &p, cons
 }
 
 // NQ: column tiles of 8 query heads (G <= 8: 1; G <= 16: 2).
-template <typename T, int D, int NQ>
+template <typename T, int D, int NQ, bool P16>
 __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __grid_constant__ GqaParams gp)
 {
     using C = GqaCfg<T, D>;
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
         const uint32_t ebar_base = smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES]);
         const int row0 = gw * C::WT;  // this warp's first row in a stage
 
-        TmaProducer<C> prod;
+        TmaProducer<C, P16> prod;
         int issued = 0, landed = 0;
         bool dead = false;
         if (issuer) {
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                 chunk_coords<C::CT>(cs, c - cbase, t, ntok_chunk);
                 // stage row of the chunk's first token: 0, or with 16-token
                 // pages its place in the aligned block
-                const int lead = gp.pages16 ? (t & (C::CT - 1)) : 0;
+                const int lead = P16 ? (t & (C::CT - 1)) : 0;
                 const int vlo = max(lead - row0, 0);                   // this warp's valid
                 const int vhi = min(lead + ntok_chunk - row0, C::WT);  // rows [vlo, vhi)
                 const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                         // contiguous bytes of a plane)
 #pragma unroll
                         for (int j = 0; j < C::LINES; ++j) {
-                            const uint32_t z0 = kb + C::CHUNK_BYTES + j * C::PLANE + (uint32_t)row0 * 128;
+                            const uint32_t z0 = kb + C::CHUNK_BYTES + stage_row<C, P16>(row0, j);
 #pragma unroll
                             for (int off = lane * 16; off < C::WT * 128; off += 32 * 16) {
                                 const int rr = off >> 7;
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
                     }
-                    gqa_chunk<T, C, NQ>(kb, kb + C::CHUNK_BYTES, row0, vlo, vhi, qb, p.scale_log2, lane, st);
+                    gqa_chunk<T, C, NQ, P16>(kb, kb + C::CHUNK_BYTES, row0, vlo, vhi, qb, p.scale_log2, lane, st);
                 }
                 __syncwarp();
                 // release the stage; the issuer refills it once both warps have
@@ -418,17 +420,23 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
     }
 }
 
-template <typename T, int D, int NQ>
-static cudaError_t launch_gqa_t(const GqaParams &gp, cudaStream_t s)
+template <typename T, int D, int NQ, bool P16>
+static cudaError_t launch_gqa_p(const GqaParams &gp, cudaStream_t s)
 {
     using C = GqaCfg<T, D>;
     const size_t smem = C::smem_bytes(gp.s.decomp, gp.s.B, gp.G);
-    auto kern = gqa_kernel<T, D, NQ>;
+    auto kern = gqa_kernel<T, D, NQ, P16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     kern<<<gp.s.grid, C::THREADS, smem, s>>>(gp);
     return cudaGetLastError();
+}
+
+template <typename T, int D, int NQ>
+static cudaError_t launch_gqa_t(const GqaParams &gp, cudaStream_t s)
+{
+    return gp.pages16 ? launch_gqa_p<T, D, NQ, true>(gp, s) : launch_gqa_p<T, D, NQ, false>(gp, s);
 }
 
 template <typename T, int D>
@@ -447,11 +455,6 @@ template <typename T> static cudaError_t launch_gqa_dt(int d, const GqaParams &g
     if (d == 128)
         return launch_gqa_d<T, 128>(gp, s);
     return launch_gqa_d<T, 256>(gp, s);
-}
-
-cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s)
-{
-    return dtype == 2 ? launch_gqa_dt<__nv_bfloat16>(d, gp, s) : launch_gqa_dt<__half>(d, gp, s);
 }
 
 }  // namespace fd

@@ -32,7 +32,7 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("gqa_kernel") != g0   # the GQA kernel includes it
     # a change to the GQA kernel alone leaves the split kernel's records valid
     h1 = bench.kernel_source_hash()
-    g = src / "fd_gqa.cu"
+    g = src / "fd_gqa_kernel.cuh"
     g.write_text(g.read_text() + "\nstatic const int fd_bench_probe2 = 2;\n")
     assert bench.kernel_source_hash() == h1
 
