@@ -149,10 +149,13 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  * K/V head repeated G times.
  *   q    [B, Hq, d]          k, v [B, Hkv, N, d]      out [B, Hq, d]
  *   lse  [B, Hq] float32 or NULL
- * G == 1 is fd_decode.  For G = 2..16 the per-chunk contraction runs on the
+ * G == 1 is fd_decode.  For G >= 2 the per-chunk contraction runs on the
  * tensor cores, which need 16-bit operands: in_dtype f16 or bf16, and
- * B*Hkv*N < 2^31.  The workspace size is fd_workspace_size_gqa(...).
- * Returns FD_ERR_UNSUPPORTED for G > 16 (G > 8 at d = 256) or f32 with G > 1.
+ * B*Hkv*N < 2^31.  A K/V head's query heads are processed in even slices of
+ * at most 16 (8 at d = 256), each reading that K/V head's rows (MQA with
+ * many heads included); the slices of one K/V head run side by side, so
+ * their repeated reads are mostly served from L2.  The workspace size is
+ * fd_workspace_size_gqa(...).  Returns FD_ERR_UNSUPPORTED for f32 with G > 1.
  */
 size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_splits);
 

@@ -6,6 +6,7 @@
 #include "fd_internal.h"
 #include "fd_split.cuh"
 
+#include <algorithm>
 #include <cuda.h>
 
 #include <cuda_runtime.h>
@@ -115,13 +116,35 @@ bool split_dim_ok(int dtype, int d)
     return d == 64 || d == 128 || (d == 256 && dtype != FD_F32);
 }
 
-// Head dims and group sizes of the grouped-query kernel: G up to 16 at 64
-// and 128, up to 8 at 256.
-bool gqa_dim_ok(int d, int G)
+// Head dims of the grouped-query kernel.
+bool gqa_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
+// The G query heads of a K/V head as NG virtual heads of at most Gs each:
+// the kernel holds at most MAXG heads per warp (16 at d = 64 and 128, 8 at
+// 256), so larger groups (MQA with many heads) are sliced evenly.
+void gqa_slices(int d, int G, int &NG, int &Gs)
 {
-    if (d == 64 || d == 128)
-        return G <= GqaCfg<__half, 128>::MAXG;
-    return d == 256 && G <= GqaCfg<__half, 256>::MAXG;
+    const int maxg = d == 256 ? GqaCfg<__half, 256>::MAXG : GqaCfg<__half, 128>::MAXG;
+    NG = (G + maxg - 1) / maxg;
+    Gs = (G + NG - 1) / NG;
+}
+
+// The grouped-query plan: the decomposition of the K/V heads' token space
+// over grid / NG ranges, each run by NG adjacent CTAs (one per slice of the
+// query heads); slots and arrival counters per (b, virtual head).
+Plan gqa_plan(int B, int Hkv, int N, int d, int num_splits, int sms, int NG)
+{
+    Plan pl = make_plan(B, Hkv, N, d, num_splits, sms);
+    const int ranges = std::max(1, sms * FD_CTAS_PER_SM / NG);
+    if (pl.decomp == DECOMP_BALANCED) {
+        pl.grid = ranges * NG;
+        pl.slots = 2LL * pl.grid;
+    } else {
+        const long long items = (long long)B * Hkv * pl.P;
+        pl.grid = (int)std::min<long long>(items, ranges) * NG;
+        pl.slots = (long long)B * Hkv * NG * pl.P;
+    }
+    return pl;
 }
 
 template <typename T> size_t split_smem_t(int d, int decomp, int B)
@@ -245,12 +268,15 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
                      long long kv_rows, const PagedKV *paged)
 {
     const int G = Hq / Hkv;
+    int NG, Gs;
+    gqa_slices(d, G, NG, Gs);
+    const long long Hv = (long long)Hkv * NG;   // virtual heads
     const int sms = sm_count();
     unsigned *st = status_ptr();
     if (sms <= 0 || !st)
         return FD_ERR_CUDA;
-    const Plan pl = make_plan(B, Hkv, N, d, num_splits, sms);
-    const WsLayout wl = ws_layout(pl.slots * G, d, (long long)B * Hkv);
+    const Plan pl = gqa_plan(B, Hkv, N, d, num_splits, sms, NG);
+    const WsLayout wl = ws_layout(pl.slots * Gs, d, (long long)B * Hv);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
         return FD_ERR_WORKSPACE;
 
@@ -266,7 +292,9 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
             !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, box_rows, box_planes))
             return FD_ERR_CUDA;
     }
-    gp.G = G;
+    gp.G = Gs;
+    gp.NG = NG;
+    gp.Gq = G;
     SplitParams &p = gp.s;
     p.q = q;
     p.k = k;
@@ -285,7 +313,7 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     p.q_dtype = in_dtype;
     set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (!clear_counters(p, (long long)B * Hkv, cs))
+    if (!clear_counters(p, (long long)B * Hv, cs))
         return FD_ERR_CUDA;
     return launch_gqa(in_dtype, d, gp, cs) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
@@ -550,13 +578,15 @@ size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_split
         return 0;
     if (Hq == Hkv)
         return fd_workspace_size(B, Hq, N, d, num_splits);
-    if (!sizes_ok(B, Hq, N, d) || num_splits < 0)
+    if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || !gqa_dim_ok(d))
         return 0;
     const int sms = sm_count();
     if (sms <= 0)
         return 0;
-    const Plan pl = make_plan(B, Hkv, N, d, num_splits, sms);
-    return ws_layout(pl.slots * (Hq / Hkv), d, (long long)B * Hkv).total;
+    int NG, Gs;
+    gqa_slices(d, Hq / Hkv, NG, Gs);
+    const Plan pl = gqa_plan(B, Hkv, N, d, num_splits, sms, NG);
+    return ws_layout(pl.slots * Gs, d, (long long)B * Hkv * NG).total;
 }
 
 fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32_t *seqlens, int B,
@@ -569,10 +599,9 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
     if (Hq == Hkv)
         return fd_decode(q, k, v, seqlens, B, Hq, N, d, in_dtype, num_splits, scale, out, out_dtype,
                          lse, workspace, workspace_bytes, stream);
-    const int G = Hq / Hkv;
     if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(out_dtype) || !gqa_dim_ok(d, G) ||
+    if (!valid_dtype(out_dtype) || !gqa_dim_ok(d) ||
         (in_dtype != FD_F16 && in_dtype != FD_BF16))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * Hkv * N >= (1LL << 31))
@@ -602,11 +631,10 @@ fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_
         return fd_decode_paged(q, k_pages, v_pages, block_table, seqlens, B, Hq, d, page_size, max_pages,
                                num_pages, in_dtype, num_splits, scale, out, out_dtype, lse, workspace,
                                workspace_bytes, stream);
-    const int G = Hq / Hkv;
     const int N = page_size * max_pages;
     if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(out_dtype) || !gqa_dim_ok(d, G) ||
+    if (!valid_dtype(out_dtype) || !gqa_dim_ok(d) ||
         (in_dtype != FD_F16 && in_dtype != FD_BF16))
         return FD_ERR_UNSUPPORTED;
     // a chunk of CT tokens lies in one page, or 16-token pages are fetched a

@@ -86,8 +86,10 @@ struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
     CUtensorMap tmk;   // K as [64, rows, d/64] 16-bit elements, boxes [64, CT, d/64], 128B swizzle;
                        // rows = B*Hkv*N, or num_pages*Hkv*page_size when paged
     CUtensorMap tmv;   // V likewise
-    SplitParams s;     // s.H = Hkv; s.q is [B, Hkv*G, d]; outputs [B, Hkv*G, ...]
-    int G;             // query heads per K/V head, 2..16
+    SplitParams s;     // s.H = Hkv; s.q is [B, Hkv*Gq, d]; outputs [B, Hkv*Gq, ...]
+    int G;             // query heads per slice (the last slice of a K/V head may have fewer), <= MAXG
+    int NG;            // slices per K/V head: ceil(Gq / MAXG); s.grid is a multiple of NG
+    int Gq;            // query heads per K/V head
     int pages16;       // paged with 16-token pages: boxes [64, 16, d/64], the P16 stage layout
 };
 
@@ -126,6 +128,36 @@ template <typename C, bool P16> __device__ __forceinline__ uint32_t stage_off(in
 // first, first + stride, ..., each chunk fetched as one K box and one V box
 // (d/64 planes each) through the tensor maps.
 //
+// Slices.  Query heads h*Gq .. h*Gq + Gq-1 of K/V head h are served as NG
+// slices of at most G each (virtual head v = h*NG + j holds query heads
+// h*Gq + j*G + 0..), so that a warp's accumulators stay in registers
+// whatever Gq is.  The decomposition runs over the K/V heads with
+// grid / NG ranges: CTA i takes range i / NG for slice i % NG, so the NG
+// CTAs of a range stream the same K/V rows side by side and all but the
+// first read them from L2.  Each virtual head has its own query rows,
+// arrival counter and workspace slots.
+__device__ __forceinline__ int vh_count(const GqaParams &gp, int v)
+{
+    return min(gp.G, gp.Gq - (v % gp.NG) * gp.G);
+}
+// first query row of virtual head v of sequence b in q, out and lse
+__device__ __forceinline__ long long vh_qrow0(const GqaParams &gp, int b, int v)
+{
+    return (long long)b * gp.s.H * gp.Gq + (long long)(v / gp.NG) * gp.Gq + (long long)(v % gp.NG) * gp.G;
+}
+// Workspace slot of piece i of (b, virtual head) bhv of slice `slice`: the
+// piece_slot of the K/V head's decomposition (ranges), mapped to the CTA
+// of that range and slice.
+__device__ __forceinline__ long long vh_slot(const GqaParams &gp, const Ctx &ctx, long long bhv, unsigned i,
+                                             int gf, long long off, int slice)
+{
+    const SplitParams &p = gp.s;
+    if (p.decomp == DECOMP_SPLITS)
+        return bhv * p.P + i;
+    const long long sr = piece_slot(p, ctx, 0, i, gf, off);
+    return ((sr >> 1) * gp.NG + slice) * 2 + (sr & 1);
+}
+
 // Paged K/V ([num_pages, Hkv, page_size, d]):
 //  - page_size a multiple of CT: a chunk's tokens lie in one aligned
 //    CT-token block of the sequence, hence in one page, so its rows are

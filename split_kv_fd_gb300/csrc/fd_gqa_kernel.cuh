@@ -6,9 +6,10 @@
 
 namespace fd {
 
-// Stage 2 of a (b, kv head) for its G query rows, by the last piece to
-// arrive: the m/l/o merge ("FlashDecoding 数学推导" §2.4.2) of the `target`
-// workspace partials of each row.  All threads: the pieces' slots and (m, l)
+// Stage 2 of a (b, virtual head) for its Gv query rows (first row qrow0;
+// workspace rows slot * G + g), by the last piece to arrive: the m/l/o merge
+// ("FlashDecoding 数学推导" §2.4.2) of the `target` workspace partials of
+// each row.  All threads: the pieces' slots and (m, l)
 // are staged in shared memory (scr, at least 128 + 130 G floats), the
 // weights exp(m_p - M) l_p formed once per (piece, row), then every output
 // element sums its pieces with all its loads in flight.  Up to MERGE_PB
@@ -16,13 +17,12 @@ namespace fd {
 constexpr int MERGE_PB = 64;
 
 template <typename C, int D>
-__device__ __forceinline__ void gqa_merge_pieces(const SplitParams &p, const Ctx &ctx, int bh, int G,
-                                                 unsigned target, int gf, long long off, int tid,
-                                                 float *scr)
+__device__ __forceinline__ void gqa_merge_pieces(const GqaParams &gp, const Ctx &ctx, long long bhv, int slice,
+                                                 int G, int Gv, long long qrow0, unsigned target, int gf,
+                                                 long long off, int tid, float *scr)
 {
+    const SplitParams &p = gp.s;
     constexpr int EMAX = (C::MAXG * D + C::THREADS - 1) / C::THREADS;
-    const int Hq = p.H * G;
-    const int b = bh / p.H, hk = bh % p.H;
     const int n = (int)target;
     long long *ss = reinterpret_cast<long long *>(scr);  // [n] workspace slots
     float *sm = scr + 2 * MERGE_PB;                       // [n][G] m, then the weights
@@ -30,16 +30,18 @@ __device__ __forceinline__ void gqa_merge_pieces(const SplitParams &p, const Ctx
     float *sM = sw + MERGE_PB * G;                        // [G]
     float *sL = sM + G;                                   // [G]
     for (int i = tid; i < n; i += C::THREADS)
-        ss[i] = piece_slot(p, ctx, bh, (unsigned)i, gf, off);
+        ss[i] = vh_slot(gp, ctx, bhv, (unsigned)i, gf, off, slice);
     __syncthreads();
     for (int i = tid; i < n * G; i += C::THREADS) {
+        if (i % G >= Gv)
+            continue;   // rows past this virtual head's query heads were never written
         const long long r = ss[i / G] * G + i % G;
         const float l = __ldcg(p.ws_ml + 2 * r + 1);
         sm[i] = l > 0.f ? __ldcg(p.ws_ml + 2 * r) : -INFINITY;
         sw[i] = l;
     }
     __syncthreads();
-    if (tid < G) {
+    if (tid < Gv) {
         float M = -INFINITY;
         for (int i = 0; i < n; ++i)
             M = fmaxf(M, sm[i * G + tid]);
@@ -64,7 +66,7 @@ __device__ __forceinline__ void gqa_merge_pieces(const SplitParams &p, const Ctx
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) {
             const int idx = tid + e * C::THREADS;
-            if (idx < G * D) {
+            if (idx < Gv * D) {
                 const int g = idx / D, dim = idx % D;
                 const float w = sm[i * G + g];
                 if (w > 0.f)
@@ -75,10 +77,10 @@ __device__ __forceinline__ void gqa_merge_pieces(const SplitParams &p, const Ctx
 #pragma unroll
     for (int e = 0; e < EMAX; ++e) {
         const int idx = tid + e * C::THREADS;
-        if (idx < G * D) {
+        if (idx < Gv * D) {
             const int g = idx / D, dim = idx % D;
             const float L = sL[g];
-            const long long qrow = (long long)b * Hq + (long long)hk * G + g;
+            const long long qrow = qrow0 + g;
             const bool nonempty = L > 0.f;
             store_out(p.out, qrow * D + dim, p.out_dtype, nonempty ? O[e] / L : 0.f);
             if (dim == 0 && p.lse)
@@ -90,22 +92,22 @@ __device__ __forceinline__ void gqa_merge_pieces(const SplitParams &p, const Ctx
 // The same merge for more than MERGE_PB pieces: each thread walks the
 // pieces for its output elements.
 template <typename C, int D>
-__device__ __forceinline__ void gqa_merge_pieces_long(const SplitParams &p, const Ctx &ctx, int bh, int G,
+__device__ __forceinline__ void gqa_merge_pieces_long(const GqaParams &gp, const Ctx &ctx, long long bhv,
+                                                      int slice, int G, int Gv, long long qrow0,
                                                       unsigned target, int gf, long long off, int tid)
 {
-    const int Hq = p.H * G;
-    const int b = bh / p.H, hk = bh % p.H;
-    for (int idx = tid; idx < G * D; idx += C::THREADS) {
+    const SplitParams &p = gp.s;
+    for (int idx = tid; idx < Gv * D; idx += C::THREADS) {
         const int g = idx / D, dim = idx % D;
         float M = -INFINITY;
         for (unsigned i = 0; i < target; ++i) {
-            const long long r = piece_slot(p, ctx, bh, i, gf, off) * G + g;
+            const long long r = vh_slot(gp, ctx, bhv, i, gf, off, slice) * G + g;
             if (__ldcg(p.ws_ml + 2 * r + 1) > 0.f)
                 M = fmaxf(M, __ldcg(p.ws_ml + 2 * r));
         }
         float L = 0.f, O = 0.f;
         for (unsigned i = 0; i < target; ++i) {
-            const long long r = piece_slot(p, ctx, bh, i, gf, off) * G + g;
+            const long long r = vh_slot(gp, ctx, bhv, i, gf, off, slice) * G + g;
             const float ll = __ldcg(p.ws_ml + 2 * r + 1);
             if (ll > 0.f) {
                 const float e = ex2(__ldcg(p.ws_ml + 2 * r) - M) * ll;
@@ -113,7 +115,7 @@ __device__ __forceinline__ void gqa_merge_pieces_long(const SplitParams &p, cons
                 O = fmaf(e, __ldcg(p.ws_o + r * D + dim), O);
             }
         }
-        const long long qrow = (long long)b * Hq + (long long)hk * G + g;
+        const long long qrow = qrow0 + g;
         const bool nonempty = L > 0.f;
         store_out(p.out, qrow * D + dim, p.out_dtype, nonempty ? O / L : 0.f);
         if (dim == 0 && p.lse)
@@ -121,14 +123,16 @@ __device__ __forceinline__ void gqa_merge_pieces_long(const SplitParams &p, cons
     }
 }
 
-// NQ: column tiles of 8 query heads (G <= 8: 1; G <= 16: 2).
+// NQ: column tiles of 8 query heads (G <= 8: 1; G <= 16: 2).  CTA i works
+// on range i / NG of the K/V heads' decomposition for slice i % NG of their
+// query heads (see vh_slot).
 template <typename T, int D, int NQ, bool P16>
 __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __grid_constant__ GqaParams gp)
 {
     using C = GqaCfg<T, D>;
     const SplitParams &p = gp.s;
-    const int G = gp.G;
-    const int Hq = p.H * G;
+    const int G = gp.G;            // query heads per slice (row stride of red and the workspace)
+    const int slice = (int)(blockIdx.x % gp.NG);
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -153,8 +157,8 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
     }
 
     Ctx ctx;
-    ctx.g = blockIdx.x;
-    ctx.G = p.grid;
+    ctx.g = (int)(blockIdx.x / gp.NG);   // range
+    ctx.G = p.grid / gp.NG;              // ranges
     ctx.cumH = cumH;
     ctx.lenS = lenS;
     ctx.T = 0;
@@ -162,12 +166,12 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
     ctx.beg = ctx.end = 0;
     if (p.decomp == DECOMP_BALANCED) {
         balanced_setup<C::THREADS, C::WARPS>(p, ctx, cumH, lenS);
-        // (b, kv head) of length 0 are touched by no CTA: write their G rows here
-        for (long long bh = (long long)ctx.g * C::THREADS + tid; bh < (long long)p.B * p.H;
-             bh += (long long)ctx.G * C::THREADS) {
+        // (b, K/V head) of length 0 are touched by no CTA: write their Gq rows here
+        for (long long bh = (long long)blockIdx.x * C::THREADS + tid; bh < (long long)p.B * p.H;
+             bh += (long long)gridDim.x * C::THREADS) {
             if (lenS[bh / p.H] == 0) {
-                const long long q0 = (bh / p.H) * Hq + (bh % p.H) * G;
-                for (int g = 0; g < G; ++g) {
+                const long long q0 = vh_qrow0(gp, (int)(bh / p.H), (int)(bh % p.H) * gp.NG);
+                for (int g = 0; g < gp.Gq; ++g) {
                     for (int i = 0; i < D; ++i)
                         store_out(p.out, (q0 + g) * D + i, p.out_dtype, 0.f);
                     if (p.lse)
@@ -210,20 +214,23 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
 #pragma unroll 1
         while (cs.valid) {
             const long long nc = seg_chunks<C::CT>(cs);
-            const int bh = cs.b * p.H + cs.h;
-            // Q^T of the head group as mma B fragments (heads >= G are zero)
+            const int vh = cs.h * gp.NG + slice;            // virtual head
+            const long long bhv = (long long)cs.b * p.H * gp.NG + vh;   // its counter
+            const int gv = vh_count(gp, vh);                 // its query heads
+            const long long qrow0 = vh_qrow0(gp, cs.b, vh);
+            // Q^T of the head group as mma B fragments (heads >= gv are zero)
             uint32_t qb[NQ][C::KSTEPS][2];
             {
                 const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
-                const long long qbase = ((long long)cs.b * Hq + (long long)cs.h * G) * D;  // elements
+                const long long qbase = qrow0 * D;  // elements
 #pragma unroll
                 for (int j = 0; j < NQ; ++j) {
                     const int n = 8 * j + qn;
 #pragma unroll
                     for (int s = 0; s < C::KSTEPS; ++s) {
                         const long long e = qbase + (long long)n * D + 16 * s + qk;
-                        qb[j][s][0] = n < G ? __ldg(q32 + e / 2) : 0u;
-                        qb[j][s][1] = n < G ? __ldg(q32 + (e + 8) / 2) : 0u;
+                        qb[j][s][0] = n < gv ? __ldg(q32 + e / 2) : 0u;
+                        qb[j][s][1] = n < gv ? __ldg(q32 + (e + 8) / 2) : 0u;
                     }
                 }
             }
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                         l += __shfl_xor_sync(FULL_MASK, l, 8);
                         l += __shfl_xor_sync(FULL_MASK, l, 16);
                         const int g = 8 * j + qk + e;   // this thread's head
-                        if (g < G) {
+                        if (g < gv) {
                             float *rg = rw + g * (D + 2);
 #pragma unroll
                             for (int i = 0; i < C::MT; ++i) {
@@ -325,14 +332,14 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
             long long slot;
             if (p.decomp == DECOMP_SPLITS) {
                 complete = (p.P == 1);
-                slot = (long long)bh * p.P + cs.p;
+                slot = bhv * p.P + cs.p;
             } else {
                 complete = (cs.t0 == 0 && cs.t1 == len);
-                slot = 2LL * ctx.g + (cs.k == 0 ? 0 : 1);
+                slot = 2LL * blockIdx.x + (cs.k == 0 ? 0 : 1);
             }
             // warp w merges heads w, w + WARPS, ...: the head's max, weights and
             // sum once per lane, then its dims lane, lane + 32, ...
-            for (int g = w; g < G; g += C::WARPS) {
+            for (int g = w; g < gv; g += C::WARPS) {
                 float M = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < C::WARPS; ++i) {
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                     L = fmaf(e[i], ri[D + 1], L);
                 }
                 const bool nonempty = L > 0.f;
-                const long long qrow = (long long)cs.b * Hq + (long long)cs.h * G + g;
+                const long long qrow = qrow0 + g;
                 const long long r = slot * G + g;
 #pragma unroll
                 for (int dd = 0; dd < D / 32; ++dd) {
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                 __syncthreads();
                 if (tid == 0) {
                     __threadfence();
-                    const unsigned old = atomicInc(p.ws_cnt + bh, target - 1);
+                    const unsigned old = atomicInc(p.ws_cnt + bhv, target - 1);
                     *flag = (old == target - 1);
                 }
                 __syncthreads();
@@ -399,9 +406,9 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                     __threadfence();
                     // red is free again: every thread has passed its reads
                     if (target <= (unsigned)MERGE_PB)
-                        gqa_merge_pieces<C, D>(p, ctx, bh, G, target, gf, off, tid, red);
+                        gqa_merge_pieces<C, D>(gp, ctx, bhv, slice, G, gv, qrow0, target, gf, off, tid, red);
                     else
-                        gqa_merge_pieces_long<C, D>(p, ctx, bh, G, target, gf, off, tid);
+                        gqa_merge_pieces_long<C, D>(gp, ctx, bhv, slice, G, gv, qrow0, target, gf, off, tid);
                 }
             }
             __syncthreads();

@@ -77,6 +77,11 @@ WORKLOADS["decode_b8_h16_n32k_d256_bf16"] = Workload(
 WORKLOADS["decode_gqa_b8_hq16_hkv8_n32k_d256_bf16"] = Workload(
     "decode_gqa_b8_hq16_hkv8_n32k_d256_bf16", 8, 16, 32768, 256, "bf16", "bf16", 0, Hkv=8)
 
+# multi-query decode: 64 query heads on one K/V head (served as 4 slices of
+# 16 heads), 32 sequences of 32K tokens (512 MiB of K/V)
+WORKLOADS["decode_mqa_b32_hq64_hkv1_n32k_d128_bf16"] = Workload(
+    "decode_mqa_b32_hq64_hkv1_n32k_d128_bf16", 32, 64, 32768, 128, "bf16", "bf16", 0, Hkv=1)
+
 # the workload the benchmark times by default: uniform 32K-token sequences
 BENCH_DEFAULT = "decode_b8_h32_n32k_d128_bf16"
 

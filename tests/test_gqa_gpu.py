@@ -1,5 +1,5 @@
 """Grouped-query decode on the GPU (fd_decode_gqa, tensor-core path for
-G = 2..16) against the float64 GQA oracle.  Lengths include 0, shorter than
+G >= 2, in slices of at most 16 query heads) against the float64 GQA oracle.  Lengths include 0, shorter than
 one chunk, and ragged tails; padding rows are NaN."""
 import numpy as np
 import pytest
@@ -66,10 +66,7 @@ def test_gqa_group_of_one_is_decode_and_errors():
     a = fd.decode_gqa(q.to(dev), k.to(dev), v.to(dev), lt.to(dev))
     b = fd.decode(q.to(dev), k.to(dev), v.to(dev), lt.to(dev))
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
-    # G > 16 and f32 with G > 1 are not supported
-    q32, k32, v32, l32 = _gqa_case(1, 34, 2, 64, 64, "bf16", None, seed=3)
-    with pytest.raises(fd.FDError):
-        fd.decode_gqa(q32.to(dev), k32.to(dev), v32.to(dev))
+    # f32 with G > 1 is not supported (the tensor cores take 16-bit operands)
     qf = torch.randn(1, 4, 64, device=dev)
     kf = torch.randn(1, 2, 64, 64, device=dev)
     with pytest.raises(fd.FDError):
@@ -120,3 +117,38 @@ def test_gqa_benchmark_workloads_sampled(name):
     del q, k, v
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("d,G,Hkv", [(128, 17, 2), (128, 24, 2), (128, 32, 1), (64, 48, 1), (128, 64, 1),
+                                     (256, 12, 2), (256, 32, 1)])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_gqa_large_groups_and_mqa(d, G, Hkv, num_splits):
+    """More query heads per K/V head than one warp holds (16; 8 at d = 256):
+    the heads are served as slices of at most that many, each reading the
+    same K/V rows.  Hkv = 1 is MQA.  Contiguous and in 16- and 64-token
+    pages, lengths 700/0/333."""
+    from split_kv_fd_gb300.inputs import to_paged
+    q, k, v, lt = _gqa_case(3, G * Hkv, Hkv, 700, d, "bf16", [700, 0, 333], seed=G + d + num_splits)
+    ref_out, ref_lse = oracle.attention_gqa(q, k, v, lens=lt)
+    dev = torch.device("cuda")
+    qd, ld = q.to(dev), lt.to(dev)
+    out, lse = fd.decode_gqa(qd, k.to(dev), v.to(dev), ld, num_splits=num_splits, out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
+    for ps in (16, 64):
+        kp, vp, table = to_paged(k, v, ps, seed=ps)
+        pout, plse = fd.decode_gqa_paged(qd, kp.to(dev), vp.to(dev), table.to(dev), ld,
+                                         num_splits=num_splits, out_dtype=torch.float32)
+        check_out(pout, ref_out, "bf16")
+        check_lse(plse, ref_lse, "bf16")
+
+
+def test_mqa_long_sequence_many_pieces():
+    """MQA, 64 query heads on one K/V head of 100K tokens: four slices of 16
+    heads, each cut into pieces across the CTAs and merged by the last."""
+    q, k, v, lt = _gqa_case(1, 64, 1, 100000, 128, "bf16", None, seed=41)
+    ref_out, ref_lse = oracle.attention_gqa(q, k, v, lens=lt)
+    dev = torch.device("cuda")
+    out, lse = fd.decode_gqa(q.to(dev), k.to(dev), v.to(dev), lt.to(dev), out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
