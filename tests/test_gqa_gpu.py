@@ -152,3 +152,18 @@ def test_mqa_long_sequence_many_pieces():
     out, lse = fd.decode_gqa(q.to(dev), k.to(dev), v.to(dev), lt.to(dev), out_dtype=torch.float32)
     check_out(out, ref_out, "bf16")
     check_lse(lse, ref_lse, "bf16")
+
+
+@pytest.mark.parametrize("G", [8, 24])
+def test_gqa_more_sequences_than_the_balanced_limit(G):
+    """1100 sequences (more than the balanced decomposition's 1024): the
+    automatic split count, with and without slices of the query heads."""
+    B, Hkv, N, d = 1100, 2, 96, 64
+    g = torch.Generator().manual_seed(G)
+    lens = torch.randint(0, N + 1, (B,), generator=g).tolist()
+    q, k, v, lt = _gqa_case(B, G * Hkv, Hkv, N, d, "bf16", lens, seed=50 + G)
+    ref_out, ref_lse = oracle.attention_gqa(q, k, v, lens=lt)
+    dev = torch.device("cuda")
+    out, lse = fd.decode_gqa(q.to(dev), k.to(dev), v.to(dev), lt.to(dev), out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
