@@ -30,8 +30,10 @@
 //  - P is split into a bf16/f16 high part and the low part of its residual
 //    (P = P_hi + P_lo), so P.V keeps close to fp32 accuracy with 16-bit MMA
 //    operands.
-//  - A stage's rows past the chunk's last valid token are zeroed in shared
-//    memory before P.V (those rows may hold padding).
+//  - A stage's rows outside the chunk's valid tokens are zeroed in shared
+//    memory before P.V (those rows may hold padding or other rows).
+//  - More than 16 query heads per K/V head (8 at d = 256; MQA) are served
+//    in slices run by adjacent CTAs over the same token range (see Slices).
 #pragma once
 
 #include <cuda.h>
@@ -124,10 +126,6 @@ template <typename C, bool P16> __device__ __forceinline__ uint32_t stage_off(in
     return stage_row<C, P16>(r, c >> 3) + (uint32_t)((((c & 7) ^ (r & 7)) << 4));
 }
 
-// The chunk walk of the split kernel's producer over the CTA's chunks c =
-// first, first + stride, ..., each chunk fetched as one K box and one V box
-// (d/64 planes each) through the tensor maps.
-//
 // Slices.  Query heads h*Gq .. h*Gq + Gq-1 of K/V head h are served as NG
 // slices of at most G each (virtual head v = h*NG + j holds query heads
 // h*Gq + j*G + 0..), so that a warp's accumulators stay in registers
@@ -158,6 +156,10 @@ __device__ __forceinline__ long long vh_slot(const GqaParams &gp, const Ctx &ctx
     return ((sr >> 1) * gp.NG + slice) * 2 + (sr & 1);
 }
 
+// The chunk walk of the split kernel's producer over the CTA's chunks c =
+// first, first + stride, ..., each chunk fetched as one K box and one V box
+// (d/64 planes each) through the tensor maps.
+//
 // Paged K/V ([num_pages, Hkv, page_size, d]):
 //  - page_size a multiple of CT: a chunk's tokens lie in one aligned
 //    CT-token block of the sequence, hence in one page, so its rows are
