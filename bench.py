@@ -95,7 +95,7 @@ def kernel_source_hash(kernel: str = "split_kernel") -> str:
 def kernel_name(w, fp8: bool, paged: bool) -> str:
     """The kernel that does the timed work, as ncu names it."""
     if w.kv_heads != w.H:
-        return f"fd::gqa_kernel<{w.dtype}, {w.d}>" + (" (paged)" if paged else "")
+        return f"fd::gqa_kernel<{'e4m3' if fp8 else w.dtype}, {w.d}>" + (" (paged)" if paged else "")
     elt = "e4m3" if fp8 else w.dtype
     return f"fd::split_kernel<{elt}, {w.d}>" + (" (paged)" if paged else "")
 
@@ -362,7 +362,10 @@ def run_ours(args, w):
             else:
                 fd.combine_lse(o_p, s_p, out=out, lse=lse, stream=stream)
             return
-        if w.kv_heads != w.H and table is None:
+        if w.kv_heads != w.H and k_scale is not None:
+            fd.decode_gqa_fp8(q, k, v, k_scale, v_scale, seqlens=lens, num_splits=P_fused, scale=w.scale,
+                              out=out, lse=lse, workspace=wsbuf, stream=stream)
+        elif w.kv_heads != w.H and table is None:
             fd.decode_gqa(q, k, v, lens, num_splits=P_fused, scale=w.scale, out=out, lse=lse,
                           workspace=wsbuf, stream=stream)
         elif w.kv_heads != w.H:
@@ -453,8 +456,8 @@ def run_ours(args, w):
     value = ws * kvb / (ms_per_step * 1e-3) / 1e9
     peaks, peak_src = measured_peaks()
     alg = algorithmic_bytes(w, lens_h)
-    if k_scale is not None:
-        alg = alg - kv_bytes(w, lens_h) + kvb + 8 * w.B * w.H
+    if k_scale is not None:  # one byte per element, plus the K and V scales of each (b, K/V head)
+        alg = alg - kv_bytes(w, lens_h) + kvb + 8 * w.B * w.kv_heads
     if table is not None:  # the block-table entries of the valid pages, read once
         alg += 4 * sum(-(-int(n) // args.page_size) for n in lens_h)
     if args.path != "fused":
@@ -574,8 +577,8 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.path != "fused" and (args.page_size or args.kv_dtype != "native" or w.kv_heads != w.H):
         ap.error("--path split-* times the contiguous, native-dtype, one-query-per-K/V-head path")
-    if args.kv_dtype != "native" and (args.page_size or w.kv_heads != w.H):
-        ap.error("--kv-dtype e4m3 times the contiguous, one-query-per-K/V-head path")
+    if args.kv_dtype != "native" and args.page_size:
+        ap.error("--kv-dtype e4m3 times a contiguous E4M3 cache")
     ws, _, _ = dist_env()
     if args.gpus > 1 and ws == 1 and "LOCAL_RANK" not in os.environ:
         # launch the per-GPU ranks ourselves

@@ -165,6 +165,25 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
                         size_t workspace_bytes, void *stream);
 
 /*
+ * Grouped-query decode over an E4M3 KV cache: fd_decode_gqa with the K/V
+ * storage of fd_decode_fp8 (FP8 KV cache, "从第一性原理推导 Flash
+ * Attention" §6.2 and §8).
+ *   q         [B, Hq, d] in q_dtype (f32, f16 or bf16)
+ *   k, v      [B, Hkv, N, d] OCP E4M3 bytes; K[b,h,t,i] = k_scale[b*Hkv+h] *
+ *             e4m3(byte), likewise V
+ *   k_scale, v_scale  [B*Hkv] float32, device
+ *   workspace fd_workspace_size_gqa(B, Hq, Hkv, N, d, num_splits) bytes
+ * d must be 64 or 128.  The E4M3 rows are converted exactly to f16 in
+ * shared memory and the products run on the tensor cores in f16 with fp32
+ * accumulation, q rounded to f16 (|q| < 65504).  G == 1 is fd_decode_fp8.
+ */
+fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,
+                            const float *k_scale, const float *v_scale, const int32_t *seqlens, int B,
+                            int Hq, int Hkv, int N, int d, int num_splits, float scale, void *out,
+                            fd_dtype out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
  * Grouped-query decode over a paged KV cache: fd_decode_gqa with the
  * block-table indirection of fd_decode_paged ("从第一性原理推导 Flash
  * Attention" §7.1 and §8; "adv04: Flash-Decoding" §5).  Same results as

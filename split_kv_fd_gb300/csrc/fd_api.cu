@@ -122,9 +122,10 @@ bool gqa_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
 // The G query heads of a K/V head as NG virtual heads of at most Gs each:
 // the kernel holds at most MAXG heads per warp (16 at d = 64 and 128, 8 at
 // 256), so larger groups (MQA with many heads) are sliced evenly.
-void gqa_slices(int d, int G, int &NG, int &Gs)
+void gqa_slices(int d, int G, int &NG, int &Gs, bool f8 = false)
 {
-    const int maxg = d == 256 ? GqaCfg<__half, 256>::MAXG : GqaCfg<__half, 128>::MAXG;
+    const int maxg = f8 ? GqaCfg<__half, 128, true>::MAXG
+                        : (d == 256 ? GqaCfg<__half, 256>::MAXG : GqaCfg<__half, 128>::MAXG);
     NG = (G + maxg - 1) / maxg;
     Gs = (G + NG - 1) / NG;
 }
@@ -265,11 +266,13 @@ struct PagedKV {
 fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t *seqlens, int B, int Hq,
                      int Hkv, int N, int d, int in_dtype, int num_splits, float scale, void *out,
                      int out_dtype, float *lse, void *workspace, size_t workspace_bytes, void *stream,
-                     long long kv_rows, const PagedKV *paged)
+                     long long kv_rows, const PagedKV *paged, const float *k_scale = nullptr,
+                     const float *v_scale = nullptr, int q_dtype = -1)
 {
+    const bool f8 = in_dtype == FD_E4M3;   // then q_dtype is q's own and no tensor maps are made
     const int G = Hq / Hkv;
     int NG, Gs;
-    gqa_slices(d, G, NG, Gs);
+    gqa_slices(d, G, NG, Gs, f8);
     const long long Hv = (long long)Hkv * NG;   // virtual heads
     const int sms = sm_count();
     unsigned *st = status_ptr();
@@ -287,7 +290,7 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     gp.pages16 = (paged && paged->page_size == 16) ? 1 : 0;
     const int box_rows = gp.pages16 ? 16 : GqaCfg<__half, 128>::CT;
     const int box_planes = d / 64;
-    if (kv_rows > 0) {
+    if (kv_rows > 0 && !f8) {
         if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_rows, box_rows, box_planes) ||
             !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, box_rows, box_planes))
             return FD_ERR_CUDA;
@@ -310,12 +313,15 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
         p.max_pages = paged->max_pages;
         p.num_pages = paged->num_pages;
     }
-    p.q_dtype = in_dtype;
+    p.q_dtype = f8 ? q_dtype : in_dtype;
+    gp.k_scale = k_scale;
+    gp.v_scale = v_scale;
     set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (!clear_counters(p, (long long)B * Hv, cs))
         return FD_ERR_CUDA;
-    return launch_gqa(in_dtype, d, gp, cs) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+    const cudaError_t e = f8 ? launch_gqa_f8(d, gp, cs) : launch_gqa(in_dtype, d, gp, cs);
+    return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
 }  // namespace
@@ -583,10 +589,15 @@ size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_split
     const int sms = sm_count();
     if (sms <= 0)
         return 0;
-    int NG, Gs;
-    gqa_slices(d, Hq / Hkv, NG, Gs);
-    const Plan pl = gqa_plan(B, Hkv, N, d, num_splits, sms, NG);
-    return ws_layout(pl.slots * Gs, d, (long long)B * Hkv * NG).total;
+    // the larger of the 16-bit and the E4M3 kernels' layouts (their slices differ)
+    size_t total = 0;
+    for (int f8 = 0; f8 < (d <= 128 ? 2 : 1); ++f8) {
+        int NG, Gs;
+        gqa_slices(d, Hq / Hkv, NG, Gs, f8 != 0);
+        const Plan pl = gqa_plan(B, Hkv, N, d, num_splits, sms, NG);
+        total = std::max(total, ws_layout(pl.slots * Gs, d, (long long)B * Hkv * NG).total);
+    }
+    return total;
 }
 
 fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32_t *seqlens, int B,
@@ -654,6 +665,31 @@ fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_
     return gqa_common(q, k_pages, v_pages, seqlens, B, Hq, Hkv, N, d, in_dtype, num_splits, scale, out,
                       out_dtype, lse, workspace, workspace_bytes, stream, pages ? num_pages * rows_per_page : 0,
                       &pk);
+}
+
+fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,
+                            const float *k_scale, const float *v_scale, const int32_t *seqlens, int B,
+                            int Hq, int Hkv, int N, int d, int num_splits, float scale, void *out,
+                            fd_dtype out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                            void *stream)
+{
+    if (Hkv <= 0 || Hq < 0 || Hq % Hkv != 0)
+        return FD_ERR_INVALID_ARG;
+    if (Hq == Hkv)
+        return fd_decode_fp8(q, q_dtype, k, v, k_scale, v_scale, seqlens, B, Hq, N, d, num_splits, scale, out,
+                             out_dtype, lse, workspace, workspace_bytes, stream);
+    if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * Hq == 0)
+        return FD_OK;
+    if (!q || (N > 0 && (!k || !v)) || !k_scale || !v_scale || !out || !aligned(q, 16) || !aligned(k, 16) ||
+        !aligned(v, 16) || !aligned(out, 16) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+        (seqlens && !aligned(seqlens, 4)) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    return gqa_common(q, k, v, seqlens, B, Hq, Hkv, N, d, FD_E4M3, num_splits, scale, out, out_dtype, lse,
+                      workspace, workspace_bytes, stream, 0, nullptr, k_scale, v_scale, q_dtype);
 }
 
 fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,

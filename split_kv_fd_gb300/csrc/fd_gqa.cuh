@@ -52,32 +52,46 @@ namespace fd {
 // Head dim 256: 4 warps, so that two stages per group still make 128 KB in
 // flight (a 32-token chunk of K and V is then 32 KB), and G <= 8 (one column
 // tile: O^T alone takes 64 accumulator registers per thread).
-template <typename T, int D> struct GqaCfg {
-    static constexpr int ROW = D * 2;              // bytes per token row (16-bit types)
-    static constexpr int LINES = D / 64;           // 128-byte lines per row
+//
+// F8: K/V stored as E4M3 bytes (d = 64 or 128).  The ring stages the bytes
+// as they are in memory (rows of d bytes, fetched by 1-D bulk copies), three
+// stages per group (96 KB in flight at d = 128); each warp converts its 16
+// rows to f16, exactly, into its own area (the 16-row layout of stage_row
+// with P16, K then V), frees the stage and runs the f16 products there.  A
+// slice then holds at most 8 query heads, so that the ring, the areas and the
+// merge buffer fit in one CTA's shared memory.
+template <typename T, int D, bool F8 = false> struct GqaCfg {
+    static constexpr bool F8K = F8;
+    static constexpr int ROW = F8 ? D : D * 2;     // bytes per token row in the ring
+    static constexpr int LINES = D / 64;           // 128-byte lines per 16-bit row
     static constexpr int WARPS = D == 256 ? 4 : 8;
     static constexpr int THREADS = WARPS * 32;
     static constexpr int GW = FD_GQA_GW;           // warps sharing one ring
     static constexpr int GROUPS = WARPS / GW;
-    static constexpr int STAGES = FD_GQA_STAGES;
+    static constexpr int STAGES = F8 ? 3 : FD_GQA_STAGES;
     static constexpr int WT = 16;                  // tokens per warp per chunk (one PV k-step)
     static constexpr int CT = GW * WT;             // tokens per chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // one of K or V
-    static constexpr int PLANE = CT * 128;         // one 64-element plane of a chunk
+    static constexpr int PLANE = CT * 128;         // one 64-element plane of a 16-bit chunk
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
     static constexpr int RING_BYTES = GROUPS * STAGES * STAGE_BYTES;
+    static constexpr int AREA_BYTES = F8 ? 2 * LINES * 16 * 128 : 0;   // per warp: 16 f16 rows of K and V
+    static constexpr int AREAS = WARPS * AREA_BYTES;
     static constexpr int BAR_BYTES = GROUPS * STAGES * 2 * 8;
     static constexpr int KSTEPS = D / 16;          // k-steps of S^T = K Q^T
     static constexpr int MT = D / 16;              // 16-row tiles of O^T
-    static constexpr int MAXG = D == 256 ? 8 : 16;
+    static constexpr int MAXG = (D == 256 || F8) ? 8 : 16;   // F8: the areas leave room for 8 heads' merge
     static_assert(D == 64 || D == 128 || D == 256, "head dim");
+    static_assert(!F8 || D <= 128, "E4M3 K/V: head dim 64 or 128");
     static_assert(PLANE % 1024 == 0, "planes stay 1024-byte aligned for the swizzle");
+    static_assert(RING_BYTES % 1024 == 0 && AREA_BYTES % 1024 == 0, "areas stay 1024-byte aligned");
 
-    // dynamic shared memory: 1024 of alignment slack, ring, barriers, the
-    // warps' (o, m, l) for the merge, a flag, and the balanced prefix sums
+    // dynamic shared memory: 1024 of alignment slack, ring, the F8 areas,
+    // barriers, the warps' (o, m, l) for the merge, a flag, and the balanced
+    // prefix sums
     static size_t smem_bytes(int decomp, int B, int G)
     {
-        size_t s = 1024 + RING_BYTES + BAR_BYTES + (size_t)WARPS * G * (D + 2) * 4 + 16;
+        size_t s = 1024 + RING_BYTES + AREAS + BAR_BYTES + (size_t)WARPS * G * (D + 2) * 4 + 16;
         if (decomp == DECOMP_BALANCED)
             s += (size_t)(B + 1) * 8 + (size_t)B * 4;
         return s;
@@ -93,10 +107,13 @@ struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
     int NG;            // slices per K/V head: ceil(Gq / MAXG); s.grid is a multiple of NG
     int Gq;            // query heads per K/V head
     int pages16;       // paged with 16-token pages: boxes [64, 16, d/64], the P16 stage layout
+    const float *k_scale;   // F8: [B*Hkv] dequantisation scales of K and V
+    const float *v_scale;
 };
 
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s);
 cudaError_t launch_gqa_bf16(int d, const GqaParams &gp, cudaStream_t s);
+cudaError_t launch_gqa_f8(int d, const GqaParams &gp, cudaStream_t s);   // E4M3 K/V, f16 products
 
 // Byte offset of 16-byte column c of row r in a stage of 64-element planes
 // written by the 128B swizzle (stage base 1024-aligned): plane c/8, and
@@ -233,7 +250,14 @@ template <typename C, bool P16> struct TmaProducer {
             return false;
         if (lane == 0) {
             const SplitParams &p = gp.s;
-            if constexpr (P16) {
+            if constexpr (C::F8K) {
+                // the chunk's E4M3 rows as they are in memory (contiguous K/V)
+                const long long row = ((long long)s.b * p.H + s.h) * p.N + t;
+                const uint32_t bytes = (uint32_t)ntok * C::ROW;
+                mbar_arrive_expect_tx(bar, 2 * bytes);
+                bulk_g2s(kdst, static_cast<const char *>(p.k) + row * C::ROW, bytes, bar);
+                bulk_g2s(kdst + C::CHUNK_BYTES, static_cast<const char *>(p.v) + row * C::ROW, bytes, bar);
+            } else if constexpr (P16) {
                 const int a = t & ~(C::CT - 1);
                 const bool first = t < a + 16, second = t + ntok > a + 16;
                 constexpr uint32_t HALF = C::LINES * 16 * 128;   // one page: 16 rows, every plane
@@ -263,6 +287,86 @@ template <typename C, bool P16> struct TmaProducer {
         return true;
     }
 };
+
+// Elements e and e + 1 of q (float32, float16 or bfloat16 by q_dtype; e even)
+// as an f16 pair, the B-operand word of the f16 products.
+__device__ __forceinline__ uint32_t q_pair_f16(const void *q, int q_dtype, long long e)
+{
+    float a, b;
+    if (q_dtype == 0) {
+        const float2 f = __ldg(reinterpret_cast<const float2 *>(static_cast<const float *>(q) + e));
+        a = f.x;
+        b = f.y;
+    } else {
+        const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(static_cast<const uint16_t *>(q) + e));
+        if (q_dtype == 1) {
+            __half2 h;
+            memcpy(&h, &w, 4);
+            const float2 f = __half22float2(h);
+            a = f.x;
+            b = f.y;
+        } else {
+            __nv_bfloat162 h;
+            memcpy(&h, &w, 4);
+            const float2 f = __bfloat1622float2(h);
+            a = f.x;
+            b = f.y;
+        }
+    }
+    const __half2 r = __floats2half2_rn(a, b);
+    uint32_t u;
+    memcpy(&u, &r, 4);
+    return u;
+}
+
+// 16 E4M3 bytes (elements 0..15) as 16 f16 values, exactly: elements 0..7
+// in lo, 8..15 in hi (cvt.rn.f16x2.e4m3x2 takes a byte pair, the lower byte
+// to the lower half).
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 &u, uint4 &lo, uint4 &hi)
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b16 a, b;\n\t"
+            "mov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
+            : "r"(w[i]));
+    lo = make_uint4(h[0], h[1], h[2], h[3]);
+    hi = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// A warp's 16 E4M3 rows (stage rows row0 .. row0+15, d bytes each) of K or
+// V into its f16 area (stage_row<C, true> layout, rows 0..15); rows outside
+// [vlo, vhi) become zeros.
+template <typename C>
+__device__ __forceinline__ void f8_rows_to_area(uint32_t stage, int row0, uint32_t area, int vlo, int vhi,
+                                                int lane)
+{
+    constexpr int CPR = C::ROW / 16;               // 16-byte pieces per E4M3 row
+#pragma unroll
+    for (int i = 0; i < 16 * CPR / 32; ++i) {
+        const int ci = lane + 32 * i;
+        const int r = ci / CPR, c16 = ci % CPR;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+        if (r >= vlo && r < vhi) {
+            uint4 u;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                         : "r"(stage + (uint32_t)((row0 + r) * C::ROW + c16 * 16)));
+            e4m3x16_to_f16(u, lo, hi);
+        }
+        // elements 16 c16 .. 16 c16 + 15 are 16-byte columns 2 c16 and 2 c16 + 1
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(area + stage_off<C, true>(r, 2 * c16)),
+                     "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w)
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(area + stage_off<C, true>(r, 2 * c16 + 1)),
+                     "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                     : "memory");
+    }
+}
 
 // Per-warp softmax state.  Query heads are the columns of S^T and O^T: in
 // column tile j this thread has heads 8j + 2(lane%4) + {0, 1}, and of O^T

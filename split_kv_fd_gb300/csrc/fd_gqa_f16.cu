@@ -1,8 +1,17 @@
-// fd_gqa_f16.cu -- the grouped-query decode kernel instantiated for f16 K/V,
-// and the dispatch over storage types.
+// fd_gqa_f16.cu -- the grouped-query decode kernel instantiated for f16 K/V
+// and for E4M3 K/V (converted to f16 in shared memory), and the dispatch over
+// storage types.
 #include "fd_gqa_kernel.cuh"
 
 namespace fd {
+
+cudaError_t launch_gqa_f8(int d, const GqaParams &gp, cudaStream_t s)
+{
+    // slices of at most 8 query heads: one column tile
+    if (d == 64)
+        return launch_gqa_p<__half, 64, 1, false, true>(gp, s);
+    return launch_gqa_p<__half, 128, 1, false, true>(gp, s);
+}
 
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s)
 {

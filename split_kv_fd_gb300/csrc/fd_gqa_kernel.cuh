@@ -126,10 +126,10 @@ __device__ __forceinline__ void gqa_merge_pieces_long(const GqaParams &gp, const
 // NQ: column tiles of 8 query heads (G <= 8: 1; G <= 16: 2).  CTA i works
 // on range i / NG of the K/V heads' decomposition for slice i % NG of their
 // query heads (see vh_slot).
-template <typename T, int D, int NQ, bool P16>
-__global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __grid_constant__ GqaParams gp)
+template <typename T, int D, int NQ, bool P16, bool F8>
+__global__ void __launch_bounds__(GqaCfg<T, D, F8>::THREADS, 1) gqa_kernel(const __grid_constant__ GqaParams gp)
 {
-    using C = GqaCfg<T, D>;
+    using C = GqaCfg<T, D, F8>;
     const SplitParams &p = gp.s;
     const int G = gp.G;            // query heads per slice (row stride of red and the workspace)
     const int slice = (int)(blockIdx.x % gp.NG);
@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
     const int w = tid >> 5;
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned ring
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::RING_BYTES);
-    float *red = reinterpret_cast<float *>(smem + C::RING_BYTES + C::BAR_BYTES);  // [WARPS][G][D+2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::RING_BYTES + C::AREAS);
+    float *red = reinterpret_cast<float *>(smem + C::RING_BYTES + C::AREAS + C::BAR_BYTES);  // [WARPS][G][D+2]
     int *flag = reinterpret_cast<int *>(red + C::WARPS * G * (D + 2));
     long long *cumH = reinterpret_cast<long long *>(flag + 4);
     int *lenS = reinterpret_cast<int *>(cumH + p.B + 1);
@@ -152,8 +152,10 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
             mbar_init(smem_addr(&bars[i]), 1);
             mbar_init(smem_addr(&bars[C::GROUPS * C::STAGES + i]), C::GW);
         }
-        prefetch_tmap(&gp.tmk);
-        prefetch_tmap(&gp.tmv);
+        if constexpr (!C::F8K) {   // E4M3 chunks come by 1-D bulk copies, without tensor maps
+            prefetch_tmap(&gp.tmk);
+            prefetch_tmap(&gp.tmv);
+        }
     }
 
     Ctx ctx;
@@ -191,6 +193,8 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
         const uint32_t bar_base = smem_addr(&bars[grp_id * C::STAGES]);
         const uint32_t ebar_base = smem_addr(&bars[(C::GROUPS + grp_id) * C::STAGES]);
         const int row0 = gw * C::WT;  // this warp's first row in a stage
+        // F8: this warp's f16 area (K rows, then V rows)
+        const uint32_t area = smem_addr(smem) + (uint32_t)(C::RING_BYTES + w * C::AREA_BYTES);
 
         TmaProducer<C, P16> prod;
         int issued = 0, landed = 0;
@@ -218,6 +222,14 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
             const long long bhv = (long long)cs.b * p.H * gp.NG + vh;   // its counter
             const int gv = vh_count(gp, vh);                 // its query heads
             const long long qrow0 = vh_qrow0(gp, cs.b, vh);
+            // score scale of the segment (E4M3 K: times its dequantisation
+            // scale) and V's scale, applied to the output at the segment end
+            float seg_scale = p.scale_log2;
+            float vsc = 1.f;
+            if constexpr (C::F8K) {
+                seg_scale *= __ldg(gp.k_scale + cs.b * p.H + cs.h);
+                vsc = __ldg(gp.v_scale + cs.b * p.H + cs.h);
+            }
             // Q^T of the head group as mma B fragments (heads >= gv are zero)
             uint32_t qb[NQ][C::KSTEPS][2];
             {
@@ -229,8 +241,13 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
 #pragma unroll
                     for (int s = 0; s < C::KSTEPS; ++s) {
                         const long long e = qbase + (long long)n * D + 16 * s + qk;
-                        qb[j][s][0] = n < gv ? __ldg(q32 + e / 2) : 0u;
-                        qb[j][s][1] = n < gv ? __ldg(q32 + (e + 8) / 2) : 0u;
+                        if constexpr (C::F8K) {   // q of any dtype, as f16 pairs
+                            qb[j][s][0] = n < gv ? q_pair_f16(p.q, p.q_dtype, e) : 0u;
+                            qb[j][s][1] = n < gv ? q_pair_f16(p.q, p.q_dtype, e + 8) : 0u;
+                        } else {
+                            qb[j][s][0] = n < gv ? __ldg(q32 + e / 2) : 0u;
+                            qb[j][s][1] = n < gv ? __ldg(q32 + (e + 8) / 2) : 0u;
+                        }
                     }
                 }
             }
@@ -266,6 +283,27 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                 const int vlo = max(lead - row0, 0);                   // this warp's valid
                 const int vhi = min(lead + ntok_chunk - row0, C::WT);  // rows [vlo, vhi)
                 const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
+                if constexpr (C::F8K) {
+                    // convert the warp's rows into its area, free the stage
+                    // (the issuer refills it), then compute from the area
+                    const bool work = !dead && vhi > vlo;
+                    if (work) {
+                        f8_rows_to_area<C>(kb, row0, area, vlo, vhi, lane);
+                        f8_rows_to_area<C>(kb + C::CHUNK_BYTES, row0, area + C::AREA_BYTES / 2, vlo, vhi, lane);
+                    }
+                    __syncwarp();
+                    if (!dead && lane == 0)
+                        mbar_arrive(ebar_base + stage * 8);
+                    if (issuer && !dead && !mbar_wait_bounded(ebar_base + stage * 8, parity))
+                        dead = true;
+                    if (issuer && !dead && prod.issue(gp, ctx, kb, bar_base + stage * 8, lane))
+                        ++issued;
+                    if (work)
+                        gqa_chunk<T, C, NQ, true>(area, area + C::AREA_BYTES / 2, 0, vlo, vhi, qb, seg_scale, lane,
+                                                  st);
+                    __syncwarp();   // the area is rewritten by the next chunk
+                    continue;
+                }
                 if (!dead && vhi > vlo) {
                     if (vlo > 0 || vhi < C::WT) {
                         // rows outside the chunk's tokens may hold padding or other
@@ -286,7 +324,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
                     }
-                    gqa_chunk<T, C, NQ, P16>(kb, kb + C::CHUNK_BYTES, row0, vlo, vhi, qb, p.scale_log2, lane, st);
+                    gqa_chunk<T, C, NQ, P16>(kb, kb + C::CHUNK_BYTES, row0, vlo, vhi, qb, seg_scale, lane, st);
                 }
                 __syncwarp();
                 // release the stage; the issuer refills it once both warps have
@@ -314,8 +352,8 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
                             float *rg = rw + g * (D + 2);
 #pragma unroll
                             for (int i = 0; i < C::MT; ++i) {
-                                rg[16 * i + qn] = st.o[i][j][e];
-                                rg[16 * i + qn + 8] = st.o[i][j][e + 2];
+                                rg[16 * i + qn] = st.o[i][j][e] * vsc;
+                                rg[16 * i + qn + 8] = st.o[i][j][e + 2] * vsc;
                             }
                             if (qn == 0) {
                                 rg[D] = st.m[j][e];
@@ -427,12 +465,12 @@ __global__ void __launch_bounds__(GqaCfg<T, D>::THREADS, 1) gqa_kernel(const __g
     }
 }
 
-template <typename T, int D, int NQ, bool P16>
+template <typename T, int D, int NQ, bool P16, bool F8 = false>
 static cudaError_t launch_gqa_p(const GqaParams &gp, cudaStream_t s)
 {
-    using C = GqaCfg<T, D>;
+    using C = GqaCfg<T, D, F8>;
     const size_t smem = C::smem_bytes(gp.s.decomp, gp.s.B, gp.G);
-    auto kern = gqa_kernel<T, D, NQ, P16>;
+    auto kern = gqa_kernel<T, D, NQ, P16, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;

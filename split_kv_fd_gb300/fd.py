@@ -29,7 +29,7 @@ EXPORTS = ["fd_status_str", "fd_version", "fd_num_sms", "fd_auto_num_splits",
            "fd_workspace_size", "fd_decode", "fd_decode_split", "fd_combine_mlo",
            "fd_combine_lse", "fd_device_status", "fd_decode_noalloc", "fd_decode_paged",
            "fd_decode_fp8", "fd_merge_lse", "fd_decode_gqa", "fd_workspace_size_gqa",
-           "fd_selftest_wait_timeout", "fd_decode_gqa_paged"]
+           "fd_selftest_wait_timeout", "fd_decode_gqa_paged", "fd_decode_gqa_fp8"]
 
 _lock = threading.Lock()
 _lib = None
@@ -97,6 +97,8 @@ def load(build_if_missing: bool = False):
         lib.fd_decode_gqa_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_longlong, I, I,
                                             F, P, I, P, P, S, P]
         lib.fd_decode_gqa_paged.restype = I
+        lib.fd_decode_gqa_fp8.argtypes = [P, I, P, P, P, P, P, I, I, I, I, I, I, F, P, I, P, P, S, P]
+        lib.fd_decode_gqa_fp8.restype = I
         _lib = lib
         return lib
 
@@ -402,6 +404,51 @@ def decode_fp8(q, k, v, k_scale, v_scale, seqlens=None, num_splits=0, scale=None
                            _ptr(out), DTYPE_CODE[out.dtype], _ptr(lse), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream(q, stream))
     _check(st, "fd_decode_fp8")
+    return out, lse
+
+
+
+def decode_gqa_fp8(q, k, v, k_scale, v_scale, seqlens=None, num_splits=0, scale=None, out_dtype=None,
+                   out=None, lse=None, return_lse=True, workspace=None, stream=None):
+    """Grouped-query decode over an E4M3 KV cache (fd_decode_gqa_fp8).
+
+    q: float32/float16/bfloat16 [B, Hq, d]; k, v: [B, Hkv, N, d]
+    torch.float8_e4m3fn (or uint8 E4M3 bytes) with Hq a multiple of Hkv;
+    k_scale, v_scale: float32 [B, Hkv].  Returns ``(out, lse)``.
+    """
+    _need_cuda(q, k, v, k_scale, v_scale, seqlens)
+    if q.dtype not in DTYPE_CODE:
+        raise ValueError("q must be float32, float16 or bfloat16")
+    if k.dtype not in (torch.float8_e4m3fn, torch.uint8) or v.dtype != k.dtype:
+        raise ValueError("k, v must be float8_e4m3fn (or uint8 E4M3 bytes)")
+    if k.dim() != 4 or v.shape != k.shape or q.dim() != 3 or q.shape[0] != k.shape[0] \
+            or q.shape[2] != k.shape[3] or q.shape[1] % k.shape[1]:
+        raise ValueError("shapes: q [B,Hq,d], k/v [B,Hkv,N,d], Hq % Hkv == 0")
+    B, Hkv, N, d = k.shape
+    Hq = q.shape[1]
+    for t in (k_scale, v_scale):
+        if t.dtype != torch.float32 or t.shape != (B, Hkv):
+            raise ValueError("k_scale/v_scale must be float32 [B,Hkv]")
+    if seqlens is not None and (seqlens.dtype != torch.int32 or seqlens.shape != (B,)):
+        raise ValueError("seqlens must be an int32 tensor of shape [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=odt, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _need_cuda(out, lse)
+    lib = load()
+    need = lib.fd_workspace_size_gqa(B, Hq, Hkv, N, d, int(num_splits))
+    if workspace is None:
+        workspace = _cached_workspace(q.device, need)
+    st = lib.fd_decode_gqa_fp8(_ptr(q), DTYPE_CODE[q.dtype], _ptr(k), _ptr(v), _ptr(k_scale),
+                               _ptr(v_scale), _ptr(seqlens), B, Hq, Hkv, N, d, int(num_splits),
+                               float(scale), _ptr(out), DTYPE_CODE[out.dtype], _ptr(lse),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(q, stream))
+    _check(st, "fd_decode_gqa_fp8")
     return out, lse
 
 

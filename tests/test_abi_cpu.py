@@ -210,6 +210,16 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
     assert gqa_paged(Hq=2, d=96) == 2             # G = 1 goes to fd_decode_paged's checks
     assert gqa_paged(B=0, lens=None, table=None) == 0
 
+    def gqa_fp8(B=1, Hq=16, Hkv=2, N=64, d=128, qdt=2, ks=dm, q=dm):
+        return lib.fd_decode_gqa_fp8(q, qdt, dm, dm, ks, dm, None, B, Hq, Hkv, N, d, 0, 1.0, dm, 2, None, dm,
+                                     MB, None)
+    assert gqa_fp8(Hq=6, Hkv=4) == 1             # Hq not a multiple of Hkv
+    assert gqa_fp8(ks=None) == 1                 # scales are required
+    assert gqa_fp8(d=256) == 2                   # E4M3 with G > 1: d 64 or 128
+    assert gqa_fp8(qdt=3) == 2                   # q stays 16/32-bit
+    assert gqa_fp8(q=P(4100)) == 1
+    assert gqa_fp8(B=0, q=None, ks=None) == 0
+
     assert lib.fd_workspace_size_gqa(1, 6, 4, 64, 128, 0) == 0
     assert lib.fd_combine_mlo(dm, dm, dm, 1, 1, 4, 80, dm, 0, None, None) == 2
 

@@ -61,8 +61,8 @@ def test_algorithmic_bytes_of_the_gqa_workload():
 
 
 @pytest.mark.parametrize("extra", [["--page-size", "64"],
-                                   ["--workload", "decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]])
-def test_fp8_only_for_contiguous_mha(extra):
+                                   ["--page-size", "64", "--workload", "decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]])
+def test_fp8_only_for_a_contiguous_cache(extra):
     with pytest.raises(SystemExit) as e:
         bench.main(["--kv-dtype", "e4m3", *extra])
     assert e.value.code == 2
@@ -76,3 +76,4 @@ def test_kernel_names_of_the_timed_paths():
     assert bench.kernel_name(w, False, True) == "fd::split_kernel<bf16, 128> (paged)"
     assert bench.kernel_name(g, False, False) == "fd::gqa_kernel<bf16, 128>"
     assert bench.kernel_name(g, False, True) == "fd::gqa_kernel<bf16, 128> (paged)"
+    assert bench.kernel_name(g, True, False) == "fd::gqa_kernel<e4m3, 128>"

@@ -1,0 +1,103 @@
+"""Grouped-query decode over an E4M3 KV cache (fd_decode_gqa_fp8) against the
+float64 oracle.  The reference is the FP8 oracle of one-query-per-head
+decode on the K/V heads and scales repeated G times (data movement only:
+query head h reads K/V head h / G)."""
+import pytest
+import torch
+
+import oracle
+import split_kv_fd_gb300 as fd
+from split_kv_fd_gb300.inputs import make_inputs, quantize_e4m3, random_case
+from split_kv_fd_gb300.workloads import WORKLOADS
+from parity_util import check_lse, check_out
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda")
+QT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__ as g
+    g.build()
+    fd.load()
+    yield
+    assert fd.device_status() == 0
+
+
+def _reference(q, k8, v8, ks, vs, G, lens):
+    rep = lambda t: t.repeat_interleave(G, dim=1)   # noqa: E731
+    return oracle.attention_fp8(q, rep(k8), rep(v8), rep(ks), rep(vs), lens=lens)
+
+
+@pytest.mark.parametrize("qdt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [2, 8, 16, 24])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_gqa_fp8_matches_oracle(qdt, d, G, num_splits):
+    Hkv = 2
+    _, k, v, lt = random_case(3, Hkv, 700, d, "bf16", lens=[700, 0, 333], seed=G + d, nan_pad=False)
+    q = torch.randn(3, G * Hkv, d, generator=torch.Generator().manual_seed(G)).to(QT[qdt])
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    ref_out, ref_lse = _reference(q, k8, v8, ks, vs, G, lt)
+    out, lse = fd.decode_gqa_fp8(q.to(DEV), k8.to(DEV), v8.to(DEV), ks.to(DEV), vs.to(DEV), lt.to(DEV),
+                                 num_splits=num_splits, out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
+
+
+def test_gqa_fp8_peaked_scores_and_many_pieces():
+    """K scaled by 8 (peaked softmax) over 60K tokens, one sequence cut into
+    one piece per CTA; G = 8."""
+    _, k, v, lt = random_case(1, 1, 60000, 128, "bf16", lens=None, seed=5, k_scale=8.0, nan_pad=False)
+    q = torch.randn(1, 8, 128, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    ref_out, ref_lse = _reference(q, k8, v8, ks, vs, 8, lt)
+    out, lse = fd.decode_gqa_fp8(q.to(DEV), k8.to(DEV), v8.to(DEV), ks.to(DEV), vs.to(DEV), lt.to(DEV),
+                                 out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
+
+
+def test_gqa_fp8_group_of_one_and_limits():
+    _, k, v, lt = random_case(2, 4, 300, 128, "bf16", lens=[300, 9], seed=7, nan_pad=False)
+    q = torch.randn(2, 4, 128).to(torch.bfloat16)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    args = (q.to(DEV), k8.to(DEV), v8.to(DEV), ks.to(DEV), vs.to(DEV), lt.to(DEV))
+    a = fd.decode_gqa_fp8(*args)
+    b = fd.decode_fp8(*args)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])    # G = 1 is fd_decode_fp8
+    _, k2, v2, l2 = random_case(1, 1, 64, 256, "bf16", lens=None, seed=8, nan_pad=False)
+    k82, ks2 = quantize_e4m3(k2)
+    with pytest.raises(fd.FDError) as e:
+        fd.decode_gqa_fp8(torch.randn(1, 4, 256, device=DEV).to(torch.bfloat16), k82.to(DEV), k82.to(DEV),
+                          ks2.to(DEV), ks2.to(DEV), l2.to(DEV))
+    assert e.value.status == 2   # d = 256 with E4M3 and G > 1: FD_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+def test_gqa_fp8_benchmark_workload_sampled():
+    """The 1 GiB GQA workload stored as E4M3, automatic decomposition, in the
+    launch the benchmark times; sampled rows against the oracle."""
+    import numpy as np
+    w = WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]
+    G = w.H // w.kv_heads
+    q, k, v, lens = make_inputs(w, device="cuda")
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    del k, v
+    out, lse = fd.decode_gqa_fp8(q, k8, v8, ks, vs, lens, scale=w.scale, out_dtype=torch.float32)
+    rng = np.random.default_rng(9)
+    for _ in range(8):
+        b, h = int(rng.integers(w.B)), int(rng.integers(w.H))
+        kv = h // G
+        ro, rs = oracle.attention_fp8(q[b:b + 1, h:h + 1].cpu(), k8[b:b + 1, kv:kv + 1].cpu(),
+                                      v8[b:b + 1, kv:kv + 1].cpu(), ks[b:b + 1, kv:kv + 1].cpu(),
+                                      vs[b:b + 1, kv:kv + 1].cpu(), scale=w.scale)
+        check_out(out[b:b + 1, h:h + 1], ro, "bf16")
+        check_lse(lse[b:b + 1, h:h + 1], rs, "bf16")
+    assert bool(torch.isfinite(out).all())
