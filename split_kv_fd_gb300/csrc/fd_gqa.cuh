@@ -346,10 +346,23 @@ __device__ __forceinline__ void f8_rows_to_area(uint32_t stage, int row0, uint32
                                                 int lane)
 {
     constexpr int CPR = C::ROW / 16;               // 16-byte pieces per E4M3 row
+    static_assert(CPR == 4 || CPR == 8, "d = 64 or 128");
 #pragma unroll
     for (int i = 0; i < 16 * CPR / 32; ++i) {
-        const int ci = lane + 32 * i;
-        const int r = ci / CPR, c16 = ci % CPR;
+        // Each 8-lane phase of the 16-byte accesses takes two consecutive
+        // rows: at d = 128 half a row's pieces from the first and the other
+        // half from the second.  Its loads then cover 128 contiguous bytes of
+        // staging, and its stores the two swizzle phases of adjacent rows:
+        // no bank conflicts either way.
+        int r, c16;
+        if constexpr (CPR == 8) {
+            const int q = lane >> 2, hb = q & 1;
+            r = 2 * (q >> 1) + hb + 8 * (i & 1);
+            c16 = (lane & 3) + 4 * (hb ^ (i >> 1));
+        } else {
+            r = (lane >> 2) + 8 * i;
+            c16 = lane & 3;
+        }
         uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
         if (r >= vlo && r < vhi) {
             uint4 u;
