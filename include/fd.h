@@ -20,12 +20,14 @@
  *       out [B, H, d]        lse  [B, H] float32
  *       o_part [B, H, P, d] float32,  m_part / l_part / lse_part [B, H, P]
  *     Tokens at index >= seqlens[b] are never read.
- *   - q, K and V share one storage dtype; accumulation is always float32.
+ *   - q, K and V share one storage dtype, except for E4M3 K/V, whose q is
+ *     f32, f16 or bf16; accumulation is always float32.
  *   - Supported head dims: 64 and 128; also 256 with f16, bf16 or E4M3 K/V
  *     (fd_decode, fd_decode_split, the combines, fd_decode_paged,
- *     fd_decode_fp8, fd_decode_noalloc; grouped-query decode with
- *     G = 2..8).  q, K, V, out, o_part must be 16-byte aligned; seqlens,
- *     lse, m/l/lse partials 4-byte aligned.
+ *     fd_decode_fp8, fd_decode_noalloc, and grouped-query decode with
+ *     f16/bf16 K/V; fd_decode_gqa_fp8 is 64 and 128 only).  q, K, V, out,
+ *     o_part must be 16-byte aligned; seqlens, lse, m/l/lse partials 4-byte
+ *     aligned.
  *   - All m and lse values are natural-log quantities of the *scaled* scores.
  *     An empty split is (o = 0, m = -inf, l = 0, lse = -inf); an empty
  *     sequence (len 0) gives out = 0, lse = -inf.
@@ -51,7 +53,7 @@ extern "C" {
 #endif
 
 /* FD_E4M3 (OCP FP8 E4M3, one byte) is a KV-cache element type for
- * fd_decode_fp8 only. */
+ * fd_decode_fp8 and fd_decode_gqa_fp8 only. */
 typedef enum { FD_F32 = 0, FD_F16 = 1, FD_BF16 = 2, FD_E4M3 = 3 } fd_dtype;
 
 typedef enum {
@@ -155,7 +157,9 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  * at most 16 (8 at d = 256), each reading that K/V head's rows (MQA with
  * many heads included); the slices of one K/V head run side by side, so
  * their repeated reads are mostly served from L2.  The workspace size is
- * fd_workspace_size_gqa(...).  Returns FD_ERR_UNSUPPORTED for f32 with G > 1.
+ * fd_workspace_size_gqa(...), one size for fd_decode_gqa,
+ * fd_decode_gqa_paged and fd_decode_gqa_fp8.  Returns FD_ERR_UNSUPPORTED for
+ * f32 with G > 1.
  */
 size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_splits);
 
@@ -175,7 +179,8 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
  *   workspace fd_workspace_size_gqa(B, Hq, Hkv, N, d, num_splits) bytes
  * d must be 64 or 128.  The E4M3 rows are converted exactly to f16 in
  * shared memory and the products run on the tensor cores in f16 with fp32
- * accumulation, q rounded to f16 (|q| < 65504).  G == 1 is fd_decode_fp8.
+ * accumulation, q rounded to f16 (|q| < 65504); query heads in slices of at
+ * most 8.  G == 1 is fd_decode_fp8.
  */
 fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,
                             const float *k_scale, const float *v_scale, const int32_t *seqlens, int B,
