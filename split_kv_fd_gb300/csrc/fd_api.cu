@@ -222,6 +222,22 @@ bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long r
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 K or V [rows, 128 bytes] as the 2-D map [128, rows] of bytes with
+// boxes [128, box_rows] and the 128-byte swizzle.
+bool make_f8_map(CUtensorMap *m, const void *base, long long rows, int box_rows)
+{
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // What every fused entry point sets alike: the score scale in base 2, the
 // plan, the outputs, the workspace carve-up and the status word.
 void set_fused(SplitParams &p, const Plan &pl, const WsLayout &wl, void *workspace, float scale,
@@ -293,6 +309,10 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     if (kv_rows > 0 && !f8) {
         if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_rows, box_rows, box_planes) ||
             !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, box_rows, box_planes))
+            return FD_ERR_CUDA;
+    } else if (kv_rows > 0 && d == 128) {   // E4M3 at d = 128: swizzled byte boxes
+        if (!make_f8_map(&gp.tmk, k, kv_rows, GqaCfg<__half, 128, true>::CT) ||
+            !make_f8_map(&gp.tmv, v, kv_rows, GqaCfg<__half, 128, true>::CT))
             return FD_ERR_CUDA;
     }
     gp.G = Gs;
@@ -682,6 +702,8 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
         return FD_ERR_INVALID_ARG;
     if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
         return FD_ERR_UNSUPPORTED;
+    if ((long long)B * Hkv * N >= (1LL << 31))
+        return FD_ERR_UNSUPPORTED;  // tensor-map row coordinates are 32-bit
     if ((long long)B * Hq == 0)
         return FD_OK;
     if (!q || (N > 0 && (!k || !v)) || !k_scale || !v_scale || !out || !aligned(q, 16) || !aligned(k, 16) ||
@@ -689,7 +711,8 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
         (seqlens && !aligned(seqlens, 4)) || (lse && !aligned(lse, 4)))
         return FD_ERR_INVALID_ARG;
     return gqa_common(q, k, v, seqlens, B, Hq, Hkv, N, d, FD_E4M3, num_splits, scale, out, out_dtype, lse,
-                      workspace, workspace_bytes, stream, 0, nullptr, k_scale, v_scale, q_dtype);
+                      workspace, workspace_bytes, stream, (long long)B * Hkv * N, nullptr, k_scale, v_scale,
+                      q_dtype);
 }
 
 fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,

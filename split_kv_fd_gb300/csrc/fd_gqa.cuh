@@ -62,20 +62,25 @@ namespace fd {
 // merge buffer fit in one CTA's shared memory.
 template <typename T, int D, bool F8 = false> struct GqaCfg {
     static constexpr bool F8K = F8;
+    // F8 at d = 128: K's fragments come straight from the staged bytes (a
+    // 128-byte swizzled tensor-map box per chunk) and only V goes through
+    // the f16 area; at d = 64 both do
+    static constexpr bool F8REG = F8 && D == 128;
     static constexpr int ROW = F8 ? D : D * 2;     // bytes per token row in the ring
     static constexpr int LINES = D / 64;           // 128-byte lines per 16-bit row
     static constexpr int WARPS = D == 256 ? 4 : 8;
     static constexpr int THREADS = WARPS * 32;
     static constexpr int GW = FD_GQA_GW;           // warps sharing one ring
     static constexpr int GROUPS = WARPS / GW;
-    static constexpr int STAGES = F8 ? 3 : FD_GQA_STAGES;
+    static constexpr int STAGES = F8 ? (D == 128 ? 4 : 3) : FD_GQA_STAGES;
     static constexpr int WT = 16;                  // tokens per warp per chunk (one PV k-step)
     static constexpr int CT = GW * WT;             // tokens per chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // one of K or V
     static constexpr int PLANE = CT * 128;         // one 64-element plane of a 16-bit chunk
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
     static constexpr int RING_BYTES = GROUPS * STAGES * STAGE_BYTES;
-    static constexpr int AREA_BYTES = F8 ? 2 * LINES * 16 * 128 : 0;   // per warp: 16 f16 rows of K and V
+    // per warp: 16 f16 rows of V (F8REG), or of K and V
+    static constexpr int AREA_BYTES = F8 ? (D == 128 ? 1 : 2) * LINES * 16 * 128 : 0;
     static constexpr int AREAS = WARPS * AREA_BYTES;
     static constexpr int BAR_BYTES = GROUPS * STAGES * 2 * 8;
     static constexpr int KSTEPS = D / 16;          // k-steps of S^T = K Q^T
@@ -173,6 +178,16 @@ __device__ __forceinline__ long long vh_slot(const GqaParams &gp, const Ctx &ctx
     return ((sr >> 1) * gp.NG + slice) * 2 + (sr & 1);
 }
 
+// 2-D tensor-map copy of box (x, y) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
 // The chunk walk of the split kernel's producer over the CTA's chunks c =
 // first, first + stride, ..., each chunk fetched as one K box and one V box
 // (d/64 planes each) through the tensor maps.
@@ -250,7 +265,14 @@ template <typename C, bool P16> struct TmaProducer {
             return false;
         if (lane == 0) {
             const SplitParams &p = gp.s;
-            if constexpr (C::F8K) {
+            if constexpr (C::F8REG) {
+                // a box of CT E4M3 rows (128 bytes each, 128-byte swizzle) per
+                // operand; rows past the tensor end read as zeros
+                const int row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
+                mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
+                tma_load_2d(kdst, &gp.tmk, 0, row, bar);
+                tma_load_2d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, row, bar);
+            } else if constexpr (C::F8K) {
                 // the chunk's E4M3 rows as they are in memory (contiguous K/V)
                 const long long row = ((long long)s.b * p.H + s.h) * p.N + t;
                 const uint32_t bytes = (uint32_t)ntok * C::ROW;
@@ -365,10 +387,14 @@ __device__ __forceinline__ void f8_rows_to_area(uint32_t stage, int row0, uint32
         }
         uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
         if (r >= vlo && r < vhi) {
+            const int sr = row0 + r;   // stage row
+            // at d = 128 the rows were staged with the 128-byte swizzle
+            const uint32_t src = C::F8REG ? stage + (uint32_t)(sr * 128 + ((c16 ^ (sr & 7)) << 4))
+                                          : stage + (uint32_t)(sr * C::ROW + c16 * 16);
             uint4 u;
             asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                         : "r"(stage + (uint32_t)((row0 + r) * C::ROW + c16 * 16)));
+                         : "r"(src));
             e4m3x16_to_f16(u, lo, hi);
         }
         // elements 16 c16 .. 16 c16 + 15 are 16-byte columns 2 c16 and 2 c16 + 1
@@ -396,10 +422,12 @@ template <typename C, int NQ> struct GqaState {
 // zeroed): S^T = K Q^T on the tensor cores, the block-wise online-softmax
 // update in fp32, then O^T += V^T (P_hi + P_lo)^T.  qb holds Q^T as B
 // fragments: qb[j][s] = heads of column tile j, k-step s.
-template <typename T, typename C, int NQ, bool P16>
-__device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int row0, int vlo, int vhi,
-                                          const uint32_t (*qb)[C::KSTEPS][2], float scale_log2, int lane,
-                                          GqaState<C, NQ> &st)
+// kfrag(s, a) gives K's A fragments of k-step s (the default reads the
+// stage with ldmatrix; E4M3 K converts them from registers).
+template <typename T, typename C, int NQ, bool P16, typename KF>
+__device__ __forceinline__ void gqa_chunk_kf(KF kfrag, uint32_t vstage, int row0, int vlo, int vhi,
+                                             const uint32_t (*qb)[C::KSTEPS][2], float scale_log2, int lane,
+                                             GqaState<C, NQ> &st)
 {
     // S^T for the warp's 16 tokens; even and odd k-steps accumulate
     // separately so the dependent MMA chains are half as long
@@ -409,11 +437,10 @@ __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int 
         sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
         sx[j][0] = sx[j][1] = sx[j][2] = sx[j][3] = 0.f;
     }
-    const int ktok = row0 + (lane & 15);
 #pragma unroll
     for (int s = 0; s < C::KSTEPS; ++s) {
         uint32_t a[4];
-        ldsm_x4(kstage + stage_off<C, P16>(ktok, 2 * s + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        kfrag(s, a);
 #pragma unroll
         for (int j = 0; j < NQ; ++j)
             Mma<T>::run((s & 1) ? sx[j] : sc[j], a, qb[j][s][0], qb[j][s][1]);
@@ -476,6 +503,55 @@ __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int 
             Mma<T>::run(st.o[i][j], a, pl[j][0], pl[j][1]);
         }
     }
+}
+
+// The chunk with K's fragments read from the stage.
+template <typename T, typename C, int NQ, bool P16>
+__device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int row0, int vlo, int vhi,
+                                          const uint32_t (*qb)[C::KSTEPS][2], float scale_log2, int lane,
+                                          GqaState<C, NQ> &st)
+{
+    const int ktok = row0 + (lane & 15);
+    gqa_chunk_kf<T, C, NQ, P16>(
+        [&](int s, uint32_t (&a)[4]) {
+            ldsm_x4(kstage + stage_off<C, P16>(ktok, 2 * s + (lane >> 4)), a[0], a[1], a[2], a[3]);
+        },
+        vstage, row0, vlo, vhi, qb, scale_log2, lane, st);
+}
+
+// E4M3 K at d = 128: the warp's 16 staged rows (128-byte swizzle) as raw
+// ldmatrix fragments, two k-steps (two 16-byte columns) per x4 load; the
+// stage can be freed once they and V's conversion are done.
+template <typename C>
+__device__ __forceinline__ void f8_k_raw(uint32_t stage, int row0, int lane, uint32_t (&kraw)[C::KSTEPS / 2][4])
+{
+    const int row = row0 + (lane & 15);
+#pragma unroll
+    for (int i = 0; i < C::KSTEPS / 2; ++i) {
+        const int c = 2 * i + (lane >> 4);
+        ldsm_x4(stage + (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4)), kraw[i][0], kraw[i][1], kraw[i][2],
+                kraw[i][3]);
+    }
+}
+
+// A fragments of k-step s from the raw E4M3 K: thread (g, t) holds d values
+// 16s + 4t .. 16s + 4t + 3 of rows g and g + 8; converted, they fill the
+// fragment's k slots 2t, 2t+1 (a0, a1) and 2t+8, 2t+9 (a2, a3), so q's
+// fragments take d = 16s + 4t (+1) and 16s + 4t + 2 (+3) in those slots.
+__device__ __forceinline__ void f8_k_frag(const uint32_t *kr, uint32_t (&a)[4])
+{
+    asm("{\n\t.reg .b16 x, y;\n\t"
+        "mov.b32 {x, y}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, x;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, y;\n\t}"
+        : "=r"(a[0]), "=r"(a[2])
+        : "r"(kr[0]));
+    asm("{\n\t.reg .b16 x, y;\n\t"
+        "mov.b32 {x, y}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, x;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, y;\n\t}"
+        : "=r"(a[1]), "=r"(a[3])
+        : "r"(kr[1]));
 }
 
 }  // namespace fd

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D, F8>::THREADS, 1) gqa_kernel(const
             mbar_init(smem_addr(&bars[i]), 1);
             mbar_init(smem_addr(&bars[C::GROUPS * C::STAGES + i]), C::GW);
         }
-        if constexpr (!C::F8K) {   // E4M3 chunks come by 1-D bulk copies, without tensor maps
+        if constexpr (!C::F8K || C::F8REG) {   // E4M3 at d = 64 comes by 1-D bulk copies, without maps
             prefetch_tmap(&gp.tmk);
             prefetch_tmap(&gp.tmv);
         }
@@ -241,7 +241,11 @@ __global__ void __launch_bounds__(GqaCfg<T, D, F8>::THREADS, 1) gqa_kernel(const
 #pragma unroll
                     for (int s = 0; s < C::KSTEPS; ++s) {
                         const long long e = qbase + (long long)n * D + 16 * s + qk;
-                        if constexpr (C::F8K) {   // q of any dtype, as f16 pairs
+                        if constexpr (C::F8REG) {   // d permuted as K's fragments (f8_k_frag)
+                            const long long e4 = qbase + (long long)n * D + 16 * s + 4 * (lane & 3);
+                            qb[j][s][0] = n < gv ? q_pair_f16(p.q, p.q_dtype, e4) : 0u;
+                            qb[j][s][1] = n < gv ? q_pair_f16(p.q, p.q_dtype, e4 + 2) : 0u;
+                        } else if constexpr (C::F8K) {   // q of any dtype, as f16 pairs
                             qb[j][s][0] = n < gv ? q_pair_f16(p.q, p.q_dtype, e) : 0u;
                             qb[j][s][1] = n < gv ? q_pair_f16(p.q, p.q_dtype, e + 8) : 0u;
                         } else {
@@ -283,7 +287,29 @@ __global__ void __launch_bounds__(GqaCfg<T, D, F8>::THREADS, 1) gqa_kernel(const
                 const int vlo = max(lead - row0, 0);                   // this warp's valid
                 const int vhi = min(lead + ntok_chunk - row0, C::WT);  // rows [vlo, vhi)
                 const uint32_t kb = ring_base + stage * C::STAGE_BYTES;
-                if constexpr (C::F8K) {
+                if constexpr (C::F8REG) {
+                    // V's rows into the area, K's as raw fragments; free the
+                    // stage (the issuer refills it), then compute
+                    const bool work = !dead && vhi > vlo;
+                    uint32_t kraw[C::KSTEPS / 2][4];
+                    if (work) {
+                        f8_rows_to_area<C>(kb + C::CHUNK_BYTES, row0, area, vlo, vhi, lane);
+                        f8_k_raw<C>(kb, row0, lane, kraw);
+                    }
+                    __syncwarp();
+                    if (!dead && lane == 0)
+                        mbar_arrive(ebar_base + stage * 8);
+                    if (issuer && !dead && !mbar_wait_bounded(ebar_base + stage * 8, parity))
+                        dead = true;
+                    if (issuer && !dead && prod.issue(gp, ctx, kb, bar_base + stage * 8, lane))
+                        ++issued;
+                    if (work)
+                        gqa_chunk_kf<T, C, NQ, true>(
+                            [&](int s, uint32_t (&a)[4]) { f8_k_frag(&kraw[s >> 1][2 * (s & 1)], a); }, area, 0,
+                            vlo, vhi, qb, seg_scale, lane, st);
+                    __syncwarp();   // the area is rewritten by the next chunk
+                    continue;
+                } else if constexpr (C::F8K) {
                     // convert the warp's rows into its area, free the stage
                     // (the issuer refills it), then compute from the area
                     const bool work = !dead && vhi > vlo;
