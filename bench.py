@@ -339,7 +339,12 @@ def run_ours(args, w):
         k, k_scale = quantize_e4m3(k)
         v, v_scale = quantize_e4m3(v)
         torch.cuda.empty_cache()
-    if args.page_size:
+    if args.page_size and k_scale is not None:
+        from split_kv_fd_gb300.inputs import to_paged_bytes
+        k, table = to_paged_bytes(k, args.page_size, seed=w.seed)
+        v, _ = to_paged_bytes(v, args.page_size, seed=w.seed)
+        torch.cuda.empty_cache()
+    elif args.page_size:
         from split_kv_fd_gb300.inputs import to_paged
         k, v, table = to_paged(k, v, args.page_size, seed=w.seed)
         torch.cuda.empty_cache()
@@ -362,7 +367,10 @@ def run_ours(args, w):
             else:
                 fd.combine_lse(o_p, s_p, out=out, lse=lse, stream=stream)
             return
-        if w.kv_heads != w.H and k_scale is not None:
+        if w.kv_heads != w.H and k_scale is not None and table is not None:
+            fd.decode_gqa_paged_fp8(q, k, v, k_scale, v_scale, table, lens, num_splits=P_fused, scale=w.scale,
+                                    out=out, lse=lse, workspace=wsbuf, stream=stream)
+        elif w.kv_heads != w.H and k_scale is not None:
             fd.decode_gqa_fp8(q, k, v, k_scale, v_scale, seqlens=lens, num_splits=P_fused, scale=w.scale,
                               out=out, lse=lse, workspace=wsbuf, stream=stream)
         elif w.kv_heads != w.H and table is None:
@@ -577,8 +585,8 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.path != "fused" and (args.page_size or args.kv_dtype != "native" or w.kv_heads != w.H):
         ap.error("--path split-* times the contiguous, native-dtype, one-query-per-K/V-head path")
-    if args.kv_dtype != "native" and args.page_size:
-        ap.error("--kv-dtype e4m3 times a contiguous E4M3 cache")
+    if args.kv_dtype != "native" and args.page_size and (w.kv_heads == w.H or w.d != 128):
+        ap.error("--kv-dtype e4m3 with --page-size times the paged E4M3 grouped-query path (d = 128)")
     ws, _, _ = dist_env()
     if args.gpus > 1 and ws == 1 and "LOCAL_RANK" not in os.environ:
         # launch the per-GPU ranks ourselves

@@ -53,7 +53,7 @@ extern "C" {
 #endif
 
 /* FD_E4M3 (OCP FP8 E4M3, one byte) is a KV-cache element type for
- * fd_decode_fp8 and fd_decode_gqa_fp8 only. */
+ * fd_decode_fp8, fd_decode_gqa_fp8 and fd_decode_gqa_paged_fp8 only. */
 typedef enum { FD_F32 = 0, FD_F16 = 1, FD_BF16 = 2, FD_E4M3 = 3 } fd_dtype;
 
 typedef enum {
@@ -187,6 +187,25 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
                             int Hq, int Hkv, int N, int d, int num_splits, float scale, void *out,
                             fd_dtype out_dtype, float *lse, void *workspace, size_t workspace_bytes,
                             void *stream);
+
+/*
+ * Grouped-query decode over a paged E4M3 KV cache: fd_decode_gqa_fp8 with
+ * the block-table indirection of fd_decode_gqa_paged (the layouts, table
+ * rules and bad-entry handling of fd_decode_paged; "从第一性原理推导 Flash
+ * Attention" §6.2, §7.1, §8).
+ *   k_pages, v_pages  [num_pages, Hkv, page_size, 128] E4M3 bytes
+ *   k_scale, v_scale  [B*Hkv] float32 (per sequence and K/V head)
+ *   workspace         fd_workspace_size_gqa(B, Hq, Hkv, max_pages*page_size,
+ *                     128, num_splits) bytes
+ * d must be 128 and page_size 16 or a multiple of 32; any G >= 1 (G = 1
+ * runs the same kernel).  FD_ERR_UNSUPPORTED otherwise.
+ */
+fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k_pages, const void *v_pages,
+                                  const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                  const int32_t *seqlens, int B, int Hq, int Hkv, int d, int page_size,
+                                  int max_pages, long long num_pages, int num_splits, float scale, void *out,
+                                  fd_dtype out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                                  void *stream);
 
 /*
  * Grouped-query decode over a paged KV cache: fd_decode_gqa with the

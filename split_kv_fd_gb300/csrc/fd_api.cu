@@ -311,8 +311,7 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
             !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, box_rows, box_planes))
             return FD_ERR_CUDA;
     } else if (kv_rows > 0 && d == 128) {   // E4M3 at d = 128: swizzled byte boxes
-        if (!make_f8_map(&gp.tmk, k, kv_rows, GqaCfg<__half, 128, true>::CT) ||
-            !make_f8_map(&gp.tmv, v, kv_rows, GqaCfg<__half, 128, true>::CT))
+        if (!make_f8_map(&gp.tmk, k, kv_rows, box_rows) || !make_f8_map(&gp.tmv, v, kv_rows, box_rows))
             return FD_ERR_CUDA;
     }
     gp.G = Gs;
@@ -713,6 +712,43 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
     return gqa_common(q, k, v, seqlens, B, Hq, Hkv, N, d, FD_E4M3, num_splits, scale, out, out_dtype, lse,
                       workspace, workspace_bytes, stream, (long long)B * Hkv * N, nullptr, k_scale, v_scale,
                       q_dtype);
+}
+
+fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k_pages, const void *v_pages,
+                                  const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                  const int32_t *seqlens, int B, int Hq, int Hkv, int d, int page_size,
+                                  int max_pages, long long num_pages, int num_splits, float scale, void *out,
+                                  fd_dtype out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                                  void *stream)
+{
+    if (Hkv <= 0 || Hq < 0 || Hq % Hkv != 0)
+        return FD_ERR_INVALID_ARG;
+    if (page_size < 1 || max_pages < 0 || num_pages < 0 ||
+        (long long)page_size * max_pages > 0x7fffffffLL)
+        return FD_ERR_INVALID_ARG;
+    const int N = page_size * max_pages;
+    if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
+        return FD_ERR_INVALID_ARG;
+    // E4M3 pages: the d = 128 kernel (byte boxes), G >= 1 (one query per
+    // K/V head runs it too), pages of 16 or a multiple of 32 tokens
+    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || d != 128)
+        return FD_ERR_UNSUPPORTED;
+    const long long rows_per_page = (long long)Hkv * page_size;
+    if ((page_size % GqaCfg<__half, 128>::CT != 0 && page_size != 16) || num_pages >= (1LL << 31) ||
+        rows_per_page >= (1LL << 31) || num_pages * rows_per_page >= (1LL << 31))
+        return FD_ERR_UNSUPPORTED;
+    if ((long long)B * Hq == 0)
+        return FD_OK;
+    const bool pages = N > 0;
+    if (!q || !seqlens || !out || !k_scale || !v_scale ||
+        (pages && (!k_pages || !v_pages || !block_table || num_pages < 1)) || !aligned(q, 16) ||
+        !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) || !aligned(seqlens, 4) ||
+        !aligned(block_table, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) || (lse && !aligned(lse, 4)))
+        return FD_ERR_INVALID_ARG;
+    const PagedKV pk = {block_table, page_size, max_pages, num_pages};
+    return gqa_common(q, k_pages, v_pages, seqlens, B, Hq, Hkv, N, d, FD_E4M3, num_splits, scale, out, out_dtype,
+                      lse, workspace, workspace_bytes, stream, pages ? num_pages * rows_per_page : 0, &pk, k_scale,
+                      v_scale, q_dtype);
 }
 
 fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,

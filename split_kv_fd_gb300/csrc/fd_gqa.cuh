@@ -118,7 +118,7 @@ struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
 
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s);
 cudaError_t launch_gqa_bf16(int d, const GqaParams &gp, cudaStream_t s);
-cudaError_t launch_gqa_f8(int d, const GqaParams &gp, cudaStream_t s);   // E4M3 K/V, f16 products
+cudaError_t launch_gqa_f8(int d, const GqaParams &gp, cudaStream_t s);   // E4M3 K/V, f16 products (paged: d = 128)
 
 // Byte offset of 16-byte column c of row r in a stage of 64-element planes
 // written by the 128B swizzle (stage base 1024-aligned): plane c/8, and
@@ -265,10 +265,29 @@ template <typename C, bool P16> struct TmaProducer {
             return false;
         if (lane == 0) {
             const SplitParams &p = gp.s;
-            if constexpr (C::F8REG) {
+            if constexpr (C::F8REG && P16) {
+                // 16-token pages: a box of 16 E4M3 rows per page that holds
+                // some of the chunk's tokens, into its half of the stage
+                const int a = t & ~(C::CT - 1);
+                const bool first = t < a + 16, second = t + ntok > a + 16;
+                constexpr uint32_t HALF = 16 * 128;
+                mbar_arrive_expect_tx(bar, 2 * HALF * ((first ? 1u : 0u) + (second ? 1u : 0u)));
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (half == 0 ? !first : !second)
+                        continue;
+                    const int row = (int)((checked_page(p, half == 0 ? pg : pg2) * p.H + s.h) * 16);
+                    tma_load_2d(kdst + half * HALF, &gp.tmk, 0, row, bar);
+                    tma_load_2d(kdst + C::CHUNK_BYTES + half * HALF, &gp.tmv, 0, row, bar);
+                }
+            } else if constexpr (C::F8REG) {
                 // a box of CT E4M3 rows (128 bytes each, 128-byte swizzle) per
                 // operand; rows past the tensor end read as zeros
-                const int row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
+                int row;
+                if (p.paged)
+                    row = (int)((checked_page(p, pg) * p.H + s.h) * p.page_size + t % p.page_size);
+                else
+                    row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
                 mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
                 tma_load_2d(kdst, &gp.tmk, 0, row, bar);
                 tma_load_2d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, row, bar);

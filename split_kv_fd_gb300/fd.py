@@ -29,7 +29,8 @@ EXPORTS = ["fd_status_str", "fd_version", "fd_num_sms", "fd_auto_num_splits",
            "fd_workspace_size", "fd_decode", "fd_decode_split", "fd_combine_mlo",
            "fd_combine_lse", "fd_device_status", "fd_decode_noalloc", "fd_decode_paged",
            "fd_decode_fp8", "fd_merge_lse", "fd_decode_gqa", "fd_workspace_size_gqa",
-           "fd_selftest_wait_timeout", "fd_decode_gqa_paged", "fd_decode_gqa_fp8"]
+           "fd_selftest_wait_timeout", "fd_decode_gqa_paged", "fd_decode_gqa_fp8",
+           "fd_decode_gqa_paged_fp8"]
 
 _lock = threading.Lock()
 _lib = None
@@ -99,6 +100,9 @@ def load(build_if_missing: bool = False):
         lib.fd_decode_gqa_paged.restype = I
         lib.fd_decode_gqa_fp8.argtypes = [P, I, P, P, P, P, P, I, I, I, I, I, I, F, P, I, P, P, S, P]
         lib.fd_decode_gqa_fp8.restype = I
+        lib.fd_decode_gqa_paged_fp8.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_longlong, I,
+                                                F, P, I, P, P, S, P]
+        lib.fd_decode_gqa_paged_fp8.restype = I
         _lib = lib
         return lib
 
@@ -449,6 +453,57 @@ def decode_gqa_fp8(q, k, v, k_scale, v_scale, seqlens=None, num_splits=0, scale=
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(q, stream))
     _check(st, "fd_decode_gqa_fp8")
+    return out, lse
+
+
+
+def decode_gqa_paged_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seqlens, num_splits=0,
+                         scale=None, out_dtype=None, out=None, lse=None, return_lse=True, workspace=None,
+                         stream=None):
+    """Grouped-query decode over a paged E4M3 KV cache (fd_decode_gqa_paged_fp8).
+
+    q: float32/float16/bfloat16 [B, Hq, 128]; k_pages/v_pages [num_pages, Hkv,
+    page_size, 128] torch.float8_e4m3fn (or uint8 E4M3 bytes), page_size 16 or
+    a multiple of 32; k_scale, v_scale float32 [B, Hkv]; block_table int32
+    [B, max_pages]; seqlens int32 [B].  Returns ``(out, lse)``.
+    """
+    _need_cuda(q, k_pages, v_pages, k_scale, v_scale, block_table, seqlens)
+    if q.dtype not in DTYPE_CODE:
+        raise ValueError("q must be float32, float16 or bfloat16")
+    if k_pages.dtype not in (torch.float8_e4m3fn, torch.uint8) or v_pages.dtype != k_pages.dtype:
+        raise ValueError("pages must be float8_e4m3fn (or uint8 E4M3 bytes)")
+    if k_pages.dim() != 4 or v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages/v_pages must be [num_pages, Hkv, page_size, d]")
+    num_pages, Hkv, page_size, d = k_pages.shape
+    B, Hq = q.shape[0], q.shape[1]
+    if q.dim() != 3 or q.shape[2] != d or Hq % Hkv:
+        raise ValueError("q must be [B, Hq, d] with Hq a multiple of the pages' Hkv")
+    for t in (k_scale, v_scale):
+        if t.dtype != torch.float32 or t.shape != (B, Hkv):
+            raise ValueError("k_scale/v_scale must be float32 [B,Hkv]")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be int32 [B, max_pages]")
+    if seqlens.dtype != torch.int32 or seqlens.shape != (B,):
+        raise ValueError("seqlens must be an int32 tensor of shape [B]")
+    max_pages = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    odt = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=odt, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _need_cuda(out, lse)
+    lib = load()
+    need = lib.fd_workspace_size_gqa(B, Hq, Hkv, max_pages * page_size, d, int(num_splits))
+    if workspace is None:
+        workspace = _cached_workspace(q.device, need)
+    st = lib.fd_decode_gqa_paged_fp8(_ptr(q), DTYPE_CODE[q.dtype], _ptr(k_pages), _ptr(v_pages),
+                                     _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seqlens), B, Hq,
+                                     Hkv, d, page_size, max_pages, num_pages, int(num_splits), float(scale),
+                                     _ptr(out), DTYPE_CODE[out.dtype], _ptr(lse), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(q, stream))
+    _check(st, "fd_decode_gqa_paged_fp8")
     return out, lse
 
 

@@ -146,3 +146,23 @@ def quantize_e4m3(x: torch.Tensor):
         scale[b] = sb
         out[b] = (xb / sb[:, None, None]).to(torch.float8_e4m3fn)
     return out, scale
+
+
+def to_paged_bytes(x8: torch.Tensor, page_size: int, seed: int = 0, extra_pages: int = 3):
+    """An E4M3 cache [B,H,N,d] (torch.float8_e4m3fn) laid out as pages
+    [num_pages, H, page_size, d] in the seeded page order of to_paged, with the
+    block table [B, ceil(N/page_size)].  Unused pages and rows past N hold
+    0x7F (an E4M3 NaN).  This only moves bytes."""
+    B, H, N, d = x8.shape
+    maxp = -(-N // page_size)
+    num_pages = B * maxp + extra_pages
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)[: B * maxp].to(x8.device)
+    u = x8.view(torch.uint8)
+    if maxp * page_size != N:
+        u = torch.cat([u, torch.full((B, H, maxp * page_size - N, d), 0x7F, dtype=torch.uint8,
+                                     device=x8.device)], dim=2)
+    pages = torch.full((num_pages, H, page_size, d), 0x7F, dtype=torch.uint8, device=x8.device)
+    pages[perm] = u.view(B, H, maxp, page_size, d).permute(0, 2, 1, 3, 4).reshape(B * maxp, H, page_size, d)
+    return pages.view(torch.float8_e4m3fn), perm.view(B, maxp).to(torch.int32).contiguous()

@@ -220,6 +220,15 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
     assert gqa_fp8(q=P(4100)) == 1
     assert gqa_fp8(B=0, q=None, ks=None) == 0
 
+    def gqa_paged_fp8(B=1, Hq=16, Hkv=2, d=128, ps=64, npg=8, ks=dm):
+        return lib.fd_decode_gqa_paged_fp8(dm, 2, dm, dm, ks, dm, dm, dm, B, Hq, Hkv, d, ps, 4, npg, 0, 1.0, dm,
+                                           2, None, dm, MB, None)
+    assert gqa_paged_fp8(d=64) == 2              # paged E4M3: d = 128
+    assert gqa_paged_fp8(ps=48) == 2
+    assert gqa_paged_fp8(ks=None) == 1
+    assert gqa_paged_fp8(Hq=6, Hkv=4) == 1
+    assert gqa_paged_fp8(B=0) == 0
+
     assert lib.fd_workspace_size_gqa(1, 6, 4, 64, 128, 0) == 0
     assert lib.fd_combine_mlo(dm, dm, dm, 1, 1, 4, 80, dm, 0, None, None) == 2
 

@@ -61,8 +61,8 @@ def test_algorithmic_bytes_of_the_gqa_workload():
 
 
 @pytest.mark.parametrize("extra", [["--page-size", "64"],
-                                   ["--page-size", "64", "--workload", "decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]])
-def test_fp8_only_for_a_contiguous_cache(extra):
+                                   ["--page-size", "64", "--workload", "decode_gqa_b8_hq16_hkv8_n32k_d256_bf16"]])
+def test_paged_fp8_only_for_grouped_queries_at_d128(extra):
     with pytest.raises(SystemExit) as e:
         bench.main(["--kv-dtype", "e4m3", *extra])
     assert e.value.code == 2

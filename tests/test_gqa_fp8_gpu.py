@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import split_kv_fd_gb300 as fd
-from split_kv_fd_gb300.inputs import make_inputs, quantize_e4m3, random_case
+from split_kv_fd_gb300.inputs import make_inputs, quantize_e4m3, random_case, to_paged_bytes
 from split_kv_fd_gb300.workloads import WORKLOADS
 from parity_util import check_lse, check_out
 
@@ -101,3 +101,48 @@ def test_gqa_fp8_benchmark_workload_sampled():
         check_out(out[b:b + 1, h:h + 1], ro, "bf16")
         check_lse(lse[b:b + 1, h:h + 1], rs, "bf16")
     assert bool(torch.isfinite(out).all())
+
+
+@pytest.mark.parametrize("G", [1, 4, 8, 16])
+@pytest.mark.parametrize("page_size", [16, 32, 64])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_paged_gqa_fp8_matches_oracle(G, page_size, num_splits):
+    Hkv, d = 2, 128
+    _, k, v, lt = random_case(3, Hkv, 700, d, "bf16", lens=[700, 0, 333], seed=G + page_size,
+                              nan_pad=False)
+    q = torch.randn(3, G * Hkv, d, generator=torch.Generator().manual_seed(G + 1)).to(torch.bfloat16)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    ref_out, ref_lse = _reference(q, k8, v8, ks, vs, G, lt)
+    kp, table = to_paged_bytes(k8, page_size, seed=page_size)
+    vp, _ = to_paged_bytes(v8, page_size, seed=page_size)
+    out, lse = fd.decode_gqa_paged_fp8(q.to(DEV), kp.to(DEV), vp.to(DEV), ks.to(DEV), vs.to(DEV),
+                                       table.to(DEV), lt.to(DEV), num_splits=num_splits,
+                                       out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
+    # the same cache contiguous
+    if G > 1:
+        cout, clse = fd.decode_gqa_fp8(q.to(DEV), k8.to(DEV), v8.to(DEV), ks.to(DEV), vs.to(DEV), lt.to(DEV),
+                                       num_splits=num_splits, out_dtype=torch.float32)
+        if page_size % 32 == 0:
+            assert torch.equal(out, cout) and torch.equal(lse, clse)
+
+
+def test_paged_gqa_fp8_limits_and_bad_entries():
+    _, k, v, lt = random_case(2, 2, 256, 128, "bf16", lens=[256, 256], seed=3, nan_pad=False)
+    q = torch.randn(2, 16, 128).to(torch.bfloat16)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    kp, table = to_paged_bytes(k8, 32, seed=1)
+    vp, _ = to_paged_bytes(v8, 32, seed=1)
+    bad = table.clone()
+    bad[1, 2] = 10 ** 6
+    fd.decode_gqa_paged_fp8(q.to(DEV), kp.to(DEV), vp.to(DEV), ks.to(DEV), vs.to(DEV), bad.to(DEV), lt.to(DEV))
+    assert fd.device_status(reset=True) == 7   # FD_ERR_BAD_PAGE, then cleared
+    kp8, t8 = to_paged_bytes(k8, 8, seed=1)
+    with pytest.raises(fd.FDError) as e:
+        fd.decode_gqa_paged_fp8(q.to(DEV), kp8.to(DEV), kp8.to(DEV), ks.to(DEV), vs.to(DEV), t8.to(DEV),
+                                lt.to(DEV))
+    assert e.value.status == 2   # 8-token pages: FD_ERR_UNSUPPORTED
+    assert fd.device_status() == 0
