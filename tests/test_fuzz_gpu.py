@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import split_kv_fd_gb300 as fd
-from split_kv_fd_gb300.inputs import quantize_e4m3, random_case, to_paged
+from split_kv_fd_gb300.inputs import quantize_e4m3, random_case, to_paged, to_paged_bytes
 from parity_util import check_lse, check_out
 
 pytestmark = pytest.mark.gpu
@@ -31,7 +31,11 @@ def _lib():
 def _draw(seed):
     r = np.random.default_rng(seed)
     d = int(r.choice([64, 128, 256]))
-    kind = str(r.choice(["mha", "paged", "fp8", "gqa", "gqa_paged"]))
+    kind = str(r.choice(["mha", "paged", "fp8", "gqa", "gqa_paged", "gqa_fp8", "gqa_paged_fp8"]))
+    if kind == "gqa_fp8":
+        d = int(r.choice([64, 128]))
+    elif kind == "gqa_paged_fp8":
+        d = 128
     dtype = str(r.choice(["f16", "bf16"] if (kind.startswith("gqa") or d == 256) else ["f32", "f16", "bf16"]))
     if kind == "fp8":
         dtype = str(r.choice(["f16", "bf16"]))
@@ -46,7 +50,7 @@ def _draw(seed):
     page = 0
     if kind == "paged":
         page = int(r.choice([1, 7, 16, 64, 200]))
-    elif kind == "gqa_paged":
+    elif kind in ("gqa_paged", "gqa_paged_fp8"):
         page = int(r.choice([16, 32, 64, 96]))
     return dict(d=d, kind=kind, dtype=dtype, B=B, Hkv=Hkv, G=G, N=N, lens=lens, num_splits=num_splits,
                 page=page)
@@ -60,12 +64,23 @@ def test_random_case(seed):
     _, k, v, lt = random_case(B, Hkv, N, d, dtype, lens=c["lens"], seed=seed)
     q = torch.randn(B, Hkv * G, d, generator=torch.Generator().manual_seed(seed + 7)).to(TD[dtype])
     ld = lt.to(DEV)
-    if kind == "fp8":
+    if kind in ("fp8", "gqa_fp8", "gqa_paged_fp8"):
         k8, ks = quantize_e4m3(k.nan_to_num(0.0))
         v8, vs = quantize_e4m3(v.nan_to_num(0.0))
-        ref_out, ref_lse = oracle.attention_fp8(q, k8, v8, ks, vs, lens=lt)
-        out, lse = fd.decode_fp8(q.to(DEV), k8.to(DEV), v8.to(DEV), ks.to(DEV), vs.to(DEV), ld,
-                                 num_splits=ns, out_dtype=torch.float32)
+        rep = lambda x: x.repeat_interleave(G, dim=1)   # noqa: E731  query head h reads K/V head h / G
+        ref_out, ref_lse = oracle.attention_fp8(q, rep(k8), rep(v8), rep(ks), rep(vs), lens=lt)
+        args = (ks.to(DEV), vs.to(DEV))
+        if kind == "fp8":
+            out, lse = fd.decode_fp8(q.to(DEV), k8.to(DEV), v8.to(DEV), *args, ld, num_splits=ns,
+                                     out_dtype=torch.float32)
+        elif kind == "gqa_fp8":
+            out, lse = fd.decode_gqa_fp8(q.to(DEV), k8.to(DEV), v8.to(DEV), *args, ld, num_splits=ns,
+                                         out_dtype=torch.float32)
+        else:
+            kp, table = to_paged_bytes(k8, c["page"], seed=seed)
+            vp, _ = to_paged_bytes(v8, c["page"], seed=seed)
+            out, lse = fd.decode_gqa_paged_fp8(q.to(DEV), kp.to(DEV), vp.to(DEV), *args, table.to(DEV), ld,
+                                               num_splits=ns, out_dtype=torch.float32)
     elif kind in ("gqa", "gqa_paged"):
         ref_out, ref_lse = oracle.attention_gqa(q, k, v, lens=lt)
         if kind == "gqa":
