@@ -123,3 +123,39 @@ def test_split_and_combine_graph():
     ref_out, ref_lse = oracle.attention(q2, k2, v2, lens=lt)
     check_out(out, ref_out, "f16")
     check_lse(lse, ref_lse, "f16")
+
+
+def test_paged_gqa_fp8_graph_replays_on_a_new_block_table():
+    """E4M3 pages, G = 8, 16-token pages: the captured launch holds the page
+    pools' tensor maps (by value, as kernel parameters); the replay reads
+    whatever table, lengths and page contents the captured buffers hold."""
+    from split_kv_fd_gb300.inputs import quantize_e4m3, to_paged_bytes
+    B, Hkv, G, N, d = 3, 2, 8, 640, 128
+    _, k, v, lt = random_case(B, Hkv, N, d, "bf16", lens=[640, 333, 0], seed=91, nan_pad=False)
+    q = torch.randn(B, G * Hkv, d, generator=torch.Generator().manual_seed(92)).to(torch.bfloat16)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    kp, table = to_paged_bytes(k8, 16, seed=1)
+    vp, _ = to_paged_bytes(v8, 16, seed=1)
+    qd, ld = q.to(DEV), lt.to(DEV)
+    kpd, vpd, td, ksd, vsd = kp.to(DEV), vp.to(DEV), table.to(DEV), ks.to(DEV), vs.to(DEV)
+    out = torch.empty(B, G * Hkv, d, device=DEV)
+    lse = torch.empty(B, G * Hkv, device=DEV)
+    ws = torch.empty(max(256, fd.workspace_size_gqa(B, G * Hkv, Hkv, N, d)), dtype=torch.uint8, device=DEV)
+    g = _capture(lambda s: fd.decode_gqa_paged_fp8(qd, kpd, vpd, ksd, vsd, td, ld, out=out, lse=lse,
+                                                   workspace=ws, stream=s))
+    rep = lambda x: x.repeat_interleave(G, dim=1)   # noqa: E731
+    for seed, lens in ((2, [640, 333, 0]), (3, [1, 640, 500])):
+        kp2, table2 = to_paged_bytes(k8, 16, seed=seed)
+        vp2, _ = to_paged_bytes(v8, 16, seed=seed)
+        kpd.copy_(kp2)
+        vpd.copy_(vp2)
+        td.copy_(table2)
+        l2 = torch.tensor(lens, dtype=torch.int32)
+        ld.copy_(l2)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_lse = oracle.attention_fp8(q, rep(k8), rep(v8), rep(ks), rep(vs), lens=l2)
+        check_out(out, ref_out, "bf16")
+        check_lse(lse, ref_lse, "bf16")
