@@ -146,3 +146,20 @@ def test_paged_gqa_fp8_limits_and_bad_entries():
                                 lt.to(DEV))
     assert e.value.status == 2   # 8-token pages: FD_ERR_UNSUPPORTED
     assert fd.device_status() == 0
+
+
+@pytest.mark.slow
+def test_paged_gqa_fp8_full_size_equals_contiguous():
+    """The 1 GiB GQA workload stored as E4M3 in shuffled 64-token pages:
+    bit-identical to the contiguous E4M3 kernel (the same chunks)."""
+    w = WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]
+    q, k, v, lens = make_inputs(w, device="cuda")
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    del k, v
+    cout, clse = fd.decode_gqa_fp8(q, k8, v8, ks, vs, lens, scale=w.scale, out_dtype=torch.float32)
+    kp, table = to_paged_bytes(k8, 64, seed=5)
+    vp, _ = to_paged_bytes(v8, 64, seed=5)
+    del k8, v8
+    out, lse = fd.decode_gqa_paged_fp8(q, kp, vp, ks, vs, table, lens, scale=w.scale, out_dtype=torch.float32)
+    assert torch.equal(out, cout) and torch.equal(lse, clse)

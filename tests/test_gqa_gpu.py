@@ -75,7 +75,9 @@ def test_gqa_group_of_one_is_decode_and_errors():
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16",
-                                  "decode_gqa_b2_hq64_hkv8_n32k_d128_bf16"])
+                                  "decode_gqa_b2_hq64_hkv8_n32k_d128_bf16",
+                                  "decode_gqa_b8_hq16_hkv8_n32k_d256_bf16",
+                                  "decode_mqa_b32_hq64_hkv1_n32k_d128_bf16"])
 def test_gqa_benchmark_workloads_sampled(name):
     """The benchmarked GQA workloads at full size, in the launch the benchmark
     times (automatic decomposition, the workload's own output dtype, and f32):
@@ -88,7 +90,9 @@ def test_gqa_benchmark_workloads_sampled(name):
     G = w.H // w.kv_heads
     q, k, v, lens = make_inputs(w, device="cuda")
     rng = np.random.default_rng(5)
-    rows = {(0, 0), (w.B - 1, w.H - 1), (0, G - 1), (w.B - 1, G)}
+    # the first and last query heads of the first K/V head and the first of
+    # the second (when there is one)
+    rows = {(0, 0), (w.B - 1, w.H - 1), (0, G - 1), (w.B - 1, min(G, w.H - 1))}
     while len(rows) < 12:
         rows.add((int(rng.integers(w.B)), int(rng.integers(w.H))))
     rows = sorted(rows)
