@@ -317,6 +317,75 @@ def config_of(w, num_splits, page_size=0, kv_dtype="native", path="fused"):
                         "outside the steps' CUDA events")}
 
 
+# the workloads the >= 80 %-of-HBM gate covers (uniform 32K, one 128K
+# sequence with peaked scores, ragged 16 x 32); the first is the headline
+GATED = ["decode_b8_h32_n32k_d128_bf16", "decode_b1_h32_n128k_d128_bf16_k8",
+         "decode_ragged_b16_h32_n64k_d128_bf16"]
+
+
+def time_gated(fd, name, steps, warmup, dev, ws, peaks):
+    """One gated workload through the fused call (automatic decomposition),
+    timed like the headline: `steps` launches, each inside its own CUDA
+    events on the launching stream, after `warmup` untimed ones.  The ragged
+    workload also times the two-call form with both merges (split kernel +
+    combine per step).  Inputs are larger than L2, so no flush is needed."""
+    from split_kv_fd_gb300.inputs import make_inputs
+    w = WORKLOADS[name]
+    q, k, v, lens = make_inputs(w, device=dev)
+    lens_h = lens.cpu().tolist()
+    out = torch.empty((w.B, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    wsbuf = fd.new_workspace(w.B, w.H, w.N, w.d, 0, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kvb = kv_bytes(w, lens_h)
+    alg = algorithmic_bytes(w, lens_h)
+
+    def timed(fn):
+        for _ in range(max(3, warmup)):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        ms = [a.elapsed_time(b) for a, b in evs]
+        return reduce_max(sum(ms), ws, dev) / steps, statistics.mean(ms)
+
+    step_ms, launch_ms = timed(lambda: fd.decode(q, k, v, lens, scale=w.scale, out=out, lse=lse,
+                                                 workspace=wsbuf, stream=stream))
+    ent = {"value": ws * kvb / (step_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": step_ms,
+           "pct_of_nominal_8tbs": 100.0 * kvb / (step_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
+           "roofline": {"frac": alg / (launch_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        "achieved": alg / (launch_ms * 1e-3) / 1e9,
+                        "traffic": profiled_traffic(w.name, "split_kernel")},
+           "mean_launch_ms": launch_ms, "gpu_launches": steps}
+    if w.ragged:
+        P = fd.auto_num_splits(w.B, w.H, w.N, w.d)
+        parts = fd.decode_split(q, k, v, P, seqlens=lens, scale=w.scale, stream=stream)
+        o_p, m_p, l_p, s_p = parts
+        for path, comb in (("split-mlo", lambda: fd.combine_mlo(o_p, m_p, l_p, out=out, lse=lse,
+                                                                stream=stream)),
+                           ("split-lse", lambda: fd.combine_lse(o_p, s_p, out=out, lse=lse,
+                                                                stream=stream))):
+            def two_call(comb=comb):
+                fd.decode_split(q, k, v, P, seqlens=lens, scale=w.scale, stream=stream,
+                                o_part=o_p, m_part=m_p, l_part=l_p, lse_part=s_p)
+                comb()
+            sm, _ = timed(two_call)
+            ent[path] = {"value": ws * kvb / (sm * 1e-3) / 1e9, "ms_per_step": sm,
+                         "num_splits": P, "gpu_launches": 2 * steps}
+        del parts, o_p, m_p, l_p, s_p
+    del q, k, v, lens, wsbuf
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return ent
+
+
 def run_ours(args, w):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -440,6 +509,14 @@ def run_ours(args, w):
         evs[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    # the other gated workloads, measured the same way in the same process
+    # (inside the clock sampler's window)
+    gated = None
+    if (w.name == GATED[0] and args.path == "fused" and not args.page_size
+            and args.kv_dtype == "native" and not args.num_splits and not args.no_gated):
+        gated = {}
+        for name in GATED[1:]:
+            gated[name] = time_gated(fd, name, args.steps, args.warmup, dev, ws, measured_peaks()[0])
     sampler.mark("t1")
     barrier(ws)
     clocks = sampler.stop()
@@ -532,7 +609,9 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if k_scale is not None else w.dtype, "accumulate": "f32",
+            "data": "synthetic",
             "config": config_of(w, (P_fused or "auto") if args.path == "fused" else P_split,
                                 args.page_size, args.kv_dtype, args.path),
             "tokens_per_s": ws * tokens / (ms_per_step * 1e-3),
@@ -555,6 +634,17 @@ def run_ours(args, w):
         }
         if combine_ms is not None:
             line["combine_ms"] = combine_ms
+        if gated is not None:
+            line["configs"] = {w.name: {
+                "value": value, "unit": "GB/s", "ms_per_step": ms_per_step,
+                "pct_of_nominal_8tbs": 100.0 * value / ws / NOMINAL_HBM_GBS,
+                "roofline": {k_: line["roofline"][k_] for k_ in ("frac", "achieved", "traffic")},
+                "mean_launch_ms": kern_ms, "gpu_launches": args.steps}}
+            line["configs"].update(gated)
+            line["gpu_launches"] += sum(e["gpu_launches"] + sum(e[p]["gpu_launches"]
+                                                                for p in ("split-mlo", "split-lse")
+                                                                if p in e)
+                                        for e in gated.values())
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -581,6 +671,9 @@ def main(argv=None):
                          "workload laid out in pages of this many tokens")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gated", action="store_true",
+                    help="time only the chosen workload, not the other two workloads of the "
+                         "bandwidth gate")
     args = ap.parse_args(argv)
     w = WORKLOADS[args.workload]
     if args.path != "fused" and (args.page_size or args.kv_dtype != "native" or w.kv_heads != w.H):

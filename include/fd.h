@@ -67,8 +67,9 @@ typedef enum {
     FD_ERR_BAD_PAGE = 7         /* a block-table entry named no page (see fd_decode_paged) */
 } fd_status;
 
-/* Human-readable name of a status code (static string, never NULL). */
-const char *fd_status_str(int status);
+/* Human-readable name of a status code (static string, never NULL; an
+ * unknown code gives "FD_UNKNOWN_STATUS"). */
+const char *fd_status_str(fd_status status);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int fd_version(void);
@@ -84,10 +85,22 @@ int fd_num_sms(void);
  * about seq/1024, capped) is replaced by one that fills every SM: enough
  * (b, h, split) work items for several waves (at least 4 per SM), splits of
  * at least 256 tokens, and among counts from that minimum up to 4 times it,
- * the one whose items fill the last round-robin wave over the CTAs best.
- * Returns >= 1, or -1 for invalid sizes.
+ * the one whose items fill the last round-robin wave over the CTAs best;
+ * never more than FD_MAX_COMBINE_SPLITS.
+ *   dtype  the K/V storage type (FD_F32, FD_F16, FD_BF16 or FD_E4M3).  The
+ *          rule is the same for every storage type (a split's fixed cost
+ *          is per split, its streaming cost per token), so that
+ *          fd_workspace_size, which takes no dtype, sizes every type's
+ *          workspace; the argument is checked and reserved.
+ * Returns >= 1, or -1 for invalid sizes or an unknown dtype.
  */
-int fd_auto_num_splits(int B, int H, int N, int d, int sm_count);
+int fd_auto_num_splits(int B, int H, int N, int d, fd_dtype dtype, int sm_count);
+
+/* The largest split count whose partials fd_combine_mlo / fd_combine_lse
+ * merge (their per-split weights live in shared memory), and so the largest
+ * num_splits fd_decode_split accepts.  fd_decode and its variants merge in
+ * the kernel and accept up to 65535. */
+#define FD_MAX_COMBINE_SPLITS 8192
 
 /*
  * Bytes of device workspace fd_decode needs for this shape and num_splits
@@ -264,7 +277,8 @@ fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const vo
  *   m_part   = max_j s_j,   l_part = sum_j exp(s_j - m),
  *   o_part   = sum_j exp(s_j - m) V_j / l   (normalised, float32),
  *   lse_part = m + ln l   (may be NULL).
- * Empty splits get (0, -inf, 0, -inf).
+ * Empty splits get (0, -inf, 0, -inf).  1 <= num_splits <=
+ * FD_MAX_COMBINE_SPLITS, so that the combines below can merge the result.
  */
 fd_status fd_decode_split(const void *q, const void *k, const void *v, const int32_t *seqlens,
                           int B, int H, int N, int d, fd_dtype in_dtype, int num_splits,
@@ -275,7 +289,8 @@ fd_status fd_decode_split(const void *q, const void *k, const void *v, const int
  * Stage 2, m/l/o form ("FlashDecoding 数学推导", §2.4.2 / §2.5 stage 2):
  *   m_g = max_p m_p,  l_g = sum_p exp(m_p - m_g) l_p,
  *   out = sum_p exp(m_p - m_g) l_p o_p / l_g,  lse = m_g + ln l_g.
- * Splits with l_p == 0 get weight 0.  P >= 1.  lse may be NULL.
+ * Splits with l_p == 0 get weight 0.  1 <= P <= FD_MAX_COMBINE_SPLITS.
+ * lse may be NULL.
  */
 fd_status fd_combine_mlo(const float *o_part, const float *m_part, const float *l_part,
                          int B, int H, int P, int d, void *out, fd_dtype out_dtype,
@@ -284,7 +299,8 @@ fd_status fd_combine_mlo(const float *o_part, const float *m_part, const float *
 /*
  * Stage 2, LSE form ("FlashDecoding 数学推导：传统 m/l/o 方法与 LSE 方法",
  * §2.3.4): S_g = ln sum_p exp(S_p) (max-shifted), out = sum_p exp(S_p - S_g)
- * o_p, lse = S_g.  Splits with S_p == -inf get weight 0.  lse may be NULL.
+ * o_p, lse = S_g.  Splits with S_p == -inf get weight 0.
+ * 1 <= P <= FD_MAX_COMBINE_SPLITS.  lse may be NULL.
  */
 fd_status fd_combine_lse(const float *o_part, const float *lse_part,
                          int B, int H, int P, int d, void *out, fd_dtype out_dtype,
@@ -355,12 +371,21 @@ fd_status fd_selftest_wait_timeout(void *stream);
  * Limits and rules:
  *   - A problem whose partials and counters need more than
  *     FD_NOALLOC_SCRATCH_BYTES returns FD_ERR_SCRATCH_TOO_SMALL before
- *     anything is launched.  With num_splits == 0 that is (about)
- *     2*SMs*(d+2)*4 + 4*B*H bytes, e.g. B*H up to ~220,000 for d = 128 on a
- *     152-SM GPU; with num_splits = P > 0 it is about B*H*P*(d+2)*4 bytes.
+ *     anything is launched.  The need is (each term rounded up to 256
+ *     bytes):
+ *       num_splits == 0 and B <= 1024 (the balanced decomposition):
+ *         2*SMs*(d+2)*4 + 4*B*H bytes, e.g. B*H up to ~220,000 for
+ *         d = 128 on a 152-SM GPU;
+ *       num_splits == 0 and B > 1024: the automatic split count P =
+ *         fd_auto_num_splits(B, H, N, d, in_dtype, SMs) is used, and the
+ *         need is B*H*P*(d+2)*4 + 4*B*H bytes (B = 2048, H = 1, d = 128
+ *         already exceeds 1 MiB);
+ *       num_splits = P > 0: B*H*P*(d+2)*4 + 4*B*H bytes.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The looked-up address is cached per
+ *     device; host threads that make their first calls at once may each
+ *     look it up, and store the same value (the cache is atomic).
  *   - Every call uses the same array and it keeps the previous call's
  *     contents; each call clears, on its stream, the counters it relies on.
  *     Calls that overlap on the GPU (other streams, other host threads) race

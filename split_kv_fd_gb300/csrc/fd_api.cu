@@ -7,6 +7,7 @@
 #include "fd_split.cuh"
 
 #include <algorithm>
+#include <atomic>
 #include <cuda.h>
 
 #include <cuda_runtime.h>
@@ -21,7 +22,10 @@ __device__ unsigned g_status_word;
 namespace {
 
 constexpr int MAX_DEVICES = 64;
-unsigned *g_status_ptr[MAX_DEVICES];  // cached device address of g_status_word
+// Cached device address of g_status_word, per device.  Host threads whose
+// first calls on a device coincide may each look it up; they store the same
+// value, and the atomic makes that well defined.
+std::atomic<unsigned *> g_status_ptr[MAX_DEVICES];
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -49,13 +53,16 @@ unsigned *status_ptr()
     const int dev = current_device();
     if (dev < 0)
         return nullptr;
-    if (dev < MAX_DEVICES && g_status_ptr[dev])
-        return g_status_ptr[dev];
+    if (dev < MAX_DEVICES) {
+        unsigned *cached = g_status_ptr[dev].load(std::memory_order_acquire);
+        if (cached)
+            return cached;
+    }
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess)
         return nullptr;
     if (dev < MAX_DEVICES)
-        g_status_ptr[dev] = static_cast<unsigned *>(ptr);
+        g_status_ptr[dev].store(static_cast<unsigned *>(ptr), std::memory_order_release);
     return static_cast<unsigned *>(ptr);
 }
 
@@ -71,7 +78,7 @@ struct Plan {
     long long slots;
 };
 
-Plan make_plan(int B, int H, int N, int d, int num_splits, int sms)
+Plan make_plan(int B, int H, int N, int d, int num_splits, int sms, int dtype = FD_BF16)
 {
     Plan pl;
     const int ctas = sms * FD_CTAS_PER_SM;  // persistent grid
@@ -82,7 +89,7 @@ Plan make_plan(int B, int H, int N, int d, int num_splits, int sms)
         pl.slots = 2LL * ctas;
     } else {
         pl.decomp = DECOMP_SPLITS;
-        pl.P = num_splits > 0 ? num_splits : fd_auto_num_splits(B, H, N, d, sms);
+        pl.P = num_splits > 0 ? num_splits : fd_auto_num_splits(B, H, N, d, (fd_dtype)dtype, sms);
         const long long items = (long long)B * H * pl.P;
         pl.grid = (int)(items < ctas ? items : ctas);
         pl.slots = (long long)B * H * pl.P;
@@ -190,17 +197,20 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 EncodeTiledFn encode_tiled()
 {
-    static EncodeTiledFn fn = nullptr;
-    if (fn)
-        return fn;
+    // looked up once; concurrent first calls store the same pointer
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (f)
+        return f;
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
         return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    return fn;
+    f = reinterpret_cast<EncodeTiledFn>(ptr);
+    fn.store(f, std::memory_order_release);
+    return f;
 }
 
 // K or V [rows, d] 16-bit as the 3-D map [64 elements, rows, d/64 planes]
@@ -355,9 +365,9 @@ using namespace fd;
 
 extern "C" {
 
-const char *fd_status_str(int status)
+const char *fd_status_str(fd_status status)
 {
-    switch (status) {
+    switch ((int)status) {
     case FD_OK: return "FD_OK";
     case FD_ERR_INVALID_ARG: return "FD_ERR_INVALID_ARG: null or misaligned pointer, or bad size";
     case FD_ERR_UNSUPPORTED: return "FD_ERR_UNSUPPORTED: head dim or dtype not supported";
@@ -377,9 +387,9 @@ int fd_version(void) { return 100; }
 
 int fd_num_sms(void) { return sm_count(); }
 
-int fd_auto_num_splits(int B, int H, int N, int d, int sms)
+int fd_auto_num_splits(int B, int H, int N, int d, fd_dtype dtype, int sms)
 {
-    if (!sizes_ok(B, H, N, d) || sms <= 0)
+    if (!sizes_ok(B, H, N, d) || sms <= 0 || !(valid_dtype(dtype) || dtype == FD_E4M3))
         return -1;
     const long long bh = (long long)B * H;
     if (bh == 0)
@@ -393,14 +403,14 @@ int fd_auto_num_splits(int B, int H, int N, int d, int sms)
     long long lo = want < cap ? want : cap;
     if (lo < 1)
         lo = 1;
-    if (lo > 8192)
-        lo = 8192;
+    if (lo > FD_MAX_COMBINE_SPLITS)
+        lo = FD_MAX_COMBINE_SPLITS;
     // the items go round-robin to the CTAs: from lo up to 4 lo (within the
     // cap), take the split count whose items fill the last round best; a
     // larger count only if it fills more than 1% better
     long long hi = 4 * lo < cap ? 4 * lo : cap;
-    if (hi > 8192)
-        hi = 8192;
+    if (hi > FD_MAX_COMBINE_SPLITS)
+        hi = FD_MAX_COMBINE_SPLITS;
     const long long G = (long long)sms * FD_CTAS_PER_SM;
     long long best = lo;
     double best_fill = -1.0;
@@ -446,7 +456,7 @@ fd_status fd_decode(const void *q, const void *k, const void *v, const int32_t *
     unsigned *st = status_ptr();
     if (sms <= 0 || !st)
         return FD_ERR_CUDA;
-    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms, in_dtype);
     const WsLayout wl = ws_layout(pl.slots, d, (long long)B * H);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
         return FD_ERR_WORKSPACE;
@@ -471,7 +481,7 @@ fd_status fd_decode_split(const void *q, const void *k, const void *v, const int
                           int H, int N, int d, fd_dtype in_dtype, int num_splits, float scale,
                           float *o_part, float *m_part, float *l_part, float *lse_part, void *stream)
 {
-    if (!sizes_ok(B, H, N, d) || num_splits < 1 || num_splits > 65535)
+    if (!sizes_ok(B, H, N, d) || num_splits < 1 || num_splits > FD_MAX_COMBINE_SPLITS)
         return FD_ERR_INVALID_ARG;
     if (!valid_dtype(in_dtype) || !split_dim_ok(in_dtype, d))
         return FD_ERR_UNSUPPORTED;
@@ -514,7 +524,7 @@ static fd_status combine_common(const float *o_part, const float *a, const float
                                 int B, int H, int P, int d, void *out, fd_dtype out_dtype, float *lse,
                                 void *stream)
 {
-    if (B < 0 || H < 0 || P < 1 || P > 8192 || d <= 0 || (long long)B * H > (1LL << 31) - 1)
+    if (B < 0 || H < 0 || P < 1 || P > FD_MAX_COMBINE_SPLITS || d <= 0 || (long long)B * H > (1LL << 31) - 1)
         return FD_ERR_INVALID_ARG;
     if (!valid_dtype(out_dtype) || (d != 64 && d != 128 && d != 256))
         return FD_ERR_UNSUPPORTED;
@@ -771,7 +781,7 @@ fd_status fd_decode_fp8(const void *q, fd_dtype q_dtype, const void *k, const vo
     unsigned *st = status_ptr();
     if (sms <= 0 || !st)
         return FD_ERR_CUDA;
-    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms, FD_E4M3);
     const WsLayout wl = ws_layout(pl.slots, d, (long long)B * H);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
         return FD_ERR_WORKSPACE;
@@ -819,7 +829,7 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
     unsigned *st = status_ptr();
     if (sms <= 0 || !st)
         return FD_ERR_CUDA;
-    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms, in_dtype);
     const WsLayout wl = ws_layout(pl.slots, d, (long long)B * H);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 256))
         return FD_ERR_WORKSPACE;
@@ -869,20 +879,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FD_NOALLOC_SCRA
 // Device address of g_noalloc_scratch, looked up once per device.  In host
 // code the array's name is only a host-side stand-in, never a device
 // address, so kernels must be given this pointer instead.
-void *g_noalloc_ptr[MAX_DEVICES];
+// Host threads whose first calls on a device coincide may each look it up;
+// they store the same value, and the atomic makes that well defined.
+std::atomic<void *> g_noalloc_ptr[MAX_DEVICES];
 
 void *noalloc_scratch()
 {
     const int dev = current_device();
     if (dev < 0 || dev >= MAX_DEVICES)
         return nullptr;
-    if (!g_noalloc_ptr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess)
-            return nullptr;
-        g_noalloc_ptr[dev] = ptr;
-    }
-    return g_noalloc_ptr[dev];
+    void *cached = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (cached)
+        return cached;
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess)
+        return nullptr;
+    g_noalloc_ptr[dev].store(ptr, std::memory_order_release);
+    return ptr;
 }
 
 }  // namespace
@@ -907,7 +920,7 @@ extern "C" fd_status fd_decode_noalloc(const void *q, const void *k, const void 
     unsigned *st = status_ptr();
     if (sms <= 0 || !st)
         return FD_ERR_CUDA;
-    const Plan pl = make_plan(B, H, N, d, num_splits, sms);
+    const Plan pl = make_plan(B, H, N, d, num_splits, sms, in_dtype);
     const WsLayout wl = ws_layout(pl.slots, d, (long long)B * H);
     if (wl.total > (size_t)FD_NOALLOC_SCRATCH_BYTES)
         return FD_ERR_SCRATCH_TOO_SMALL;

@@ -66,7 +66,7 @@ def load(build_if_missing: bool = False):
         lib.fd_version.restype = I
         lib.fd_num_sms.argtypes = []
         lib.fd_num_sms.restype = I
-        lib.fd_auto_num_splits.argtypes = [I, I, I, I, I]
+        lib.fd_auto_num_splits.argtypes = [I, I, I, I, I, I]
         lib.fd_auto_num_splits.restype = I
         lib.fd_workspace_size.argtypes = [I, I, I, I, I]
         lib.fd_workspace_size.restype = S
@@ -154,9 +154,15 @@ def num_sms() -> int:
     return load().fd_num_sms()
 
 
-def auto_num_splits(B, H, N, d, sm_count=None) -> int:
+KV_DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, "f32": 0, "f16": 1,
+                 "bf16": 2, "e4m3": 3}
+
+
+def auto_num_splits(B, H, N, d, dtype=torch.bfloat16, sm_count=None) -> int:
+    """fd_auto_num_splits: the split count of the two-call path for this
+    shape and K/V storage type (a torch dtype, or "f32"/"f16"/"bf16"/"e4m3")."""
     sm = num_sms() if sm_count is None else sm_count
-    return load().fd_auto_num_splits(B, H, N, d, sm)
+    return load().fd_auto_num_splits(B, H, N, d, KV_DTYPE_CODE[dtype], sm)
 
 
 def workspace_size(B, H, N, d, num_splits=0) -> int:
@@ -219,10 +225,14 @@ def decode(q, k, v, seqlens=None, num_splits=0, scale=None, out_dtype=None, out=
 
 def decode_noalloc(q, k, v, seqlens=None, num_splits=0, scale=None, out_dtype=None, out=None,
                    lse=None, return_lse=True, stream=None):
-    """fd_decode on the library's own device scratch (fd_decode_noalloc):
-    nothing is allocated per call.  Returns ``(out, lse)``.  Calls on one
-    device share the scratch, so they must not overlap on the GPU; problems
-    whose workspace exceeds the scratch raise FD_ERR_SCRATCH_TOO_SMALL."""
+    """fd_decode on the library's own device scratch (fd_decode_noalloc).
+    Returns ``(out, lse)``.
+
+    The C call allocates nothing.  This wrapper allocates only what the
+    caller leaves out: pass ``out`` (and ``lse``, or ``return_lse=False``)
+    for a call that allocates no device memory at all.  Calls on one device
+    share the scratch, so they must not overlap on the GPU; problems whose
+    partials exceed the scratch raise FD_ERR_SCRATCH_TOO_SMALL."""
     B, H, N, d = _check_qkv(q, k, v, seqlens)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -507,17 +517,32 @@ def decode_gqa_paged_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq
     return out, lse
 
 
-def decode_split(q, k, v, num_splits, seqlens=None, scale=None, stream=None):
-    """Stage 1 alone (fd_decode_split).  Returns ``(o_part, m_part, l_part, lse_part)``."""
+def decode_split(q, k, v, num_splits, seqlens=None, scale=None, stream=None, o_part=None,
+                 m_part=None, l_part=None, lse_part=None):
+    """Stage 1 alone (fd_decode_split).  Returns ``(o_part, m_part, l_part, lse_part)``.
+
+    The partial buffers may be passed in (float32, [B,H,P,d] and [B,H,P]);
+    those not given are allocated."""
     B, H, N, d = _check_qkv(q, k, v, seqlens)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     P = int(num_splits)
     dev = q.device
-    o_part = torch.empty((B, H, P, d), dtype=torch.float32, device=dev)
-    m_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
-    l_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
-    lse_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
+    if o_part is None:
+        o_part = torch.empty((B, H, P, d), dtype=torch.float32, device=dev)
+    for t in (m_part, l_part, lse_part):
+        if t is not None and (t.shape != (B, H, P) or t.dtype != torch.float32
+                              or not t.is_contiguous()):
+            raise ValueError("m_part / l_part / lse_part must be contiguous float32 [B,H,P]")
+    if o_part.shape != (B, H, P, d) or o_part.dtype != torch.float32 or not o_part.is_contiguous():
+        raise ValueError("o_part must be contiguous float32 [B,H,P,d]")
+    if m_part is None:
+        m_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
+    if l_part is None:
+        l_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((B, H, P), dtype=torch.float32, device=dev)
+    _need_cuda(o_part, m_part, l_part, lse_part)
     st = load().fd_decode_split(_ptr(q), _ptr(k), _ptr(v), _ptr(seqlens), B, H, N, d,
                                 DTYPE_CODE[q.dtype], P, float(scale), _ptr(o_part), _ptr(m_part),
                                 _ptr(l_part), _ptr(lse_part), _stream(q, stream))

@@ -15,6 +15,7 @@ from split_kv_fd_gb300.inputs import make_inputs, random_case
 from split_kv_fd_gb300.workloads import WORKLOADS
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+F32, F16, BF16, E4M3 = 0, 1, 2, 3   # fd_dtype
 
 
 @pytest.fixture(scope="module")
@@ -83,19 +84,23 @@ def _fill(bh, P, G):
 def test_auto_num_splits_rule(lib):
     # >= 4 work items per SM, never splits under 256 tokens, >= 1; among
     # counts up to 4x that minimum, the best fill of the last wave of CTAs
-    assert lib.fd_auto_num_splits(8, 32, 32768, 128, 152) == 7      # 1792 items: 11.8 per CTA
-    assert lib.fd_auto_num_splits(16, 32, 65536, 128, 152) == 5     # 2560 items: 16.8 per CTA
-    assert lib.fd_auto_num_splits(1, 32, 131072, 128, 152) == 19    # 608 items: exactly 4 per CTA
-    assert lib.fd_auto_num_splits(1, 1, 1024, 64, 152) == 4
-    assert lib.fd_auto_num_splits(1, 1, 100, 64, 152) == 1
-    assert lib.fd_auto_num_splits(0, 1, 100, 64, 152) == 1
-    assert lib.fd_auto_num_splits(1, 1, 100, 64, 0) == -1
+    assert lib.fd_auto_num_splits(8, 32, 32768, 128, BF16, 152) == 7      # 1792 items: 11.8 per CTA
+    assert lib.fd_auto_num_splits(16, 32, 65536, 128, BF16, 152) == 5     # 2560 items: 16.8 per CTA
+    assert lib.fd_auto_num_splits(1, 32, 131072, 128, BF16, 152) == 19    # 608 items: exactly 4 per CTA
+    assert lib.fd_auto_num_splits(1, 1, 1024, 64, F32, 152) == 4
+    assert lib.fd_auto_num_splits(1, 1, 100, 64, F32, 152) == 1
+    assert lib.fd_auto_num_splits(0, 1, 100, 64, F32, 152) == 1
+    assert lib.fd_auto_num_splits(1, 1, 100, 64, F32, 0) == -1
+    assert lib.fd_auto_num_splits(1, 1, 100, 64, 9, 152) == -1       # unknown storage type
+    # the same rule for every storage type (fd_workspace_size takes none)
+    for dt in (F32, F16, BF16, E4M3):
+        assert lib.fd_auto_num_splits(8, 32, 32768, 128, dt, 152) == 7
     # the chosen count never fills worse than the minimum one, nor splits
     # below 256 tokens
     for B, H, N in [(8, 32, 32768), (3, 7, 50000), (2, 8, 32768), (64, 8, 4096), (1, 5, 9000)]:
         bh = B * H
         lo = max(1, min(-(-4 * 152 // bh), max(1, N // 256)))
-        P = lib.fd_auto_num_splits(B, H, N, 128, 152)
+        P = lib.fd_auto_num_splits(B, H, N, 128, BF16, 152)
         assert lo <= P <= max(lo, 4 * lo)
         assert P == 1 or N // P >= 256
         assert _fill(bh, P, 152) >= _fill(bh, lo, 152)

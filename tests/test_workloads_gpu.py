@@ -1,12 +1,10 @@
 """Parity on the five named workloads, in the launch configuration the
 benchmark times (fused decode, automatic decomposition, default stream).
 
-The two small workloads are compared element by element with the oracle.
-The three large ones (2-16 GiB of KV) are compared on a seeded sample of
-(b, h) rows, which the oracle computes one by one, and on properties that
-hold at any size: every output is finite, every output element lies within
-the range of its V column (a softmax average is a convex combination), and
-the fused path agrees with the two-call path on every row.
+All five are compared element by element, on every (b, h) row, with the
+float64 oracle: the two small workloads through every path and both output
+dtypes, the three large ones (2-16 GiB of KV) through the fused call (the
+benchmarked configuration) and the two-call path with both merges.
 """
 import numpy as np
 import pytest
@@ -65,77 +63,49 @@ def test_small_workloads_elementwise(name):
         check_lse(lse, ref_lse, w.dtype)
 
 
-def _sample_rows(w, lens, n=12, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = {(0, 0), (w.B - 1, w.H - 1)}
-    if w.ragged:  # the shortest and the longest sequence
-        lo, hi = int(np.argmin(lens)), int(np.argmax(lens))
-        rows |= {(lo, 0), (hi, w.H - 1)}
-    while len(rows) < n:
-        rows.add((int(rng.integers(w.B)), int(rng.integers(w.H))))
-    return sorted(rows)
+def _oracle_all_rows(w, q, k, v, lens):
+    """The oracle over every (b, h) row of a full-size workload.
 
-
-def _oracle_rows(w, q, k, v, lens, rows):
-    """Oracle on the sampled rows only (each row copied to the host)."""
-    outs, lses = [], []
-    for b, h in rows:
-        n = int(lens[b])
-        qs = q[b:b + 1, h:h + 1].cpu()
-        ks = k[b:b + 1, h:h + 1, :n].cpu()
-        vs = v[b:b + 1, h:h + 1, :n].cpu()
-        o, s = oracle.attention(qs, ks, vs, scale=w.scale)
-        outs.append(o[0, 0])
-        lses.append(s[0, 0])
-    return np.stack(outs), np.array(lses)
-
-
-def _convex_bounds_ok(v, lens, out):
-    """Each output element lies within [min_j V_j, max_j V_j] of its column."""
-    for b in range(v.shape[0]):
-        n = int(lens[b])
-        vb = v[b, :, :n].float()
-        lo = vb.amin(dim=1) - 1e-3
-        hi = vb.amax(dim=1) + 1e-3
-        ob = out[b].float()
-        assert bool(torch.all(ob >= lo)) and bool(torch.all(ob <= hi)), f"row {b} outside hull"
-        del vb
+    The K/V bits are copied to the host as they are (padding included; the
+    oracle reads only the first lens[b] rows) and the float64 C oracle runs
+    threaded over all rows.
+    """
+    return oracle.attention(q.cpu(), k.cpu(), v.cpu(), lens=lens.cpu(), scale=w.scale)
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["decode_b8_h32_n32k_d128_bf16", "decode_b1_h32_n128k_d128_bf16_k8",
                                   "decode_ragged_b16_h32_n64k_d128_bf16"])
-def test_large_workloads_sampled(name):
+def test_large_workloads_every_row(name):
+    """Every element of every (b, h) row against the float64 oracle.
+
+    Split + merge equals unsplit attention on every row ("FlashDecoding 数学
+    推导" §2.6, "...传统 m/l/o 方法与 LSE 方法" §2.3.6), whatever the
+    decomposition cuts; so each path below is compared with the oracle
+    directly, never with another CUDA path.
+    """
     w = WORKLOADS[name]
     q, k, v, lens = make_inputs(w, device="cuda")
-    lens_h = lens.cpu().numpy()
-    rows = _sample_rows(w, lens_h)
-    ref_out, ref_lse = _oracle_rows(w, q, k, v, lens_h, rows)
-    bi = torch.tensor([r[0] for r in rows])
-    hi = torch.tensor([r[1] for r in rows])
+    ref_out, ref_lse = _oracle_all_rows(w, q, k, v, lens)
+    rows = w.B * w.H
 
     results = {}
-    # the benchmarked configuration: fused, automatic decomposition
-    out, lse = fd.decode(q, k, v, lens, scale=w.scale, out_dtype=OUT_DT[w.out_dtype])
-    results["fused_auto"] = (out, lse)
-    out32, lse32 = fd.decode(q, k, v, lens, scale=w.scale, out_dtype=torch.float32)
-    results["fused_auto_f32"] = (out32, lse32)
-    # the two-call path with both merges
+    # the benchmarked configuration: fused, automatic decomposition, the
+    # workload's own output dtype; then the strict bound with a float32 output
+    results[f"fused_auto_{w.out_dtype}"] = fd.decode(q, k, v, lens, scale=w.scale,
+                                                     out_dtype=OUT_DT[w.out_dtype])
+    results["fused_auto_f32"] = fd.decode(q, k, v, lens, scale=w.scale, out_dtype=torch.float32)
+    # the two-call path with both merges, each with both output dtypes
     P = fd.auto_num_splits(w.B, w.H, w.N, w.d)
     o, m, l, s = fd.decode_split(q, k, v, P, seqlens=lens, scale=w.scale)
-    results["split_mlo"] = fd.combine_mlo(o, m, l, out_dtype=torch.float32)
-    results["split_lse"] = fd.combine_lse(o, s, out_dtype=torch.float32)
+    for odt in (w.out_dtype, "f32"):
+        results[f"split{P}_mlo_{odt}"] = fd.combine_mlo(o, m, l, out_dtype=OUT_DT[odt])
+        results[f"split{P}_lse_{odt}"] = fd.combine_lse(o, s, out_dtype=OUT_DT[odt])
     del o, m, l, s
     for key, (out, lse) in results.items():
-        so = out[bi, hi]
-        sl = lse[bi, hi]
-        eo = check_out(so, ref_out, w.dtype, what=f"{key} out")
-        el = check_lse(sl, ref_lse, w.dtype, what=f"{key} lse")
-        print(f"PARITY {name} {key} rows={len(rows)} max_err_out={eo:.3e} max_err_lse={el:.3e}")
-        assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all()), key
-    # properties over every row
-    _convex_bounds_ok(v, lens_h, results["fused_auto_f32"][0])
-    a, b = results["fused_auto_f32"][0], results["split_mlo"][0]
-    assert float((a - b).abs().max()) <= 2e-3
-    del q, k, v
+        eo = check_out(out, ref_out, w.dtype, what=f"{key} out")
+        el = check_lse(lse, ref_lse, w.dtype, what=f"{key} lse")
+        print(f"PARITY {name} {key} rows={rows}/{rows} all elements "
+              f"max_err_out={eo:.3e} max_err_lse={el:.3e}")
+    del q, k, v, results
     _free()

@@ -100,6 +100,41 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
     assert torch.all(out == 0)  # nothing was launched
 
 
+def _documented_need(B, H, N, d, num_splits, sms):
+    """The scratch bytes the header documents for fd_decode_noalloc (each
+    term rounded up to 256 bytes)."""
+    r = lambda x: -(-x // 256) * 256  # noqa: E731
+    if num_splits == 0 and B <= 1024:
+        return r(2 * sms * d * 4) + r(2 * sms * 2 * 4) + r(4 * B * H)
+    P = num_splits or fd.auto_num_splits(B, H, N, d, torch.bfloat16)
+    return r(B * H * P * d * 4) + r(B * H * P * 2 * 4) + r(4 * B * H)
+
+
+@pytest.mark.parametrize("B,H,N,num_splits", [(1024, 1, 64, 0), (1025, 1, 64, 0), (2048, 1, 64, 0),
+                                              (2048, 1, 300, 0), (64, 4, 5000, 7)])
+def test_noalloc_limit_is_the_documented_one(lib, B, H, N, num_splits):
+    """Above B = 1024 the automatic mode switches to split counts, whose
+    partials grow with B*H*P: the status follows the documented bound on
+    either side of it, and a call within it matches fd_decode."""
+    dev = torch.device("cuda")
+    d = 128
+    need = _documented_need(B, H, N, d, num_splits, fd.num_sms())
+    q, k, v, lt = (t.to(dev) for t in random_case(B, H, N, d, "bf16", lens="ragged", seed=B + N))
+    out = torch.zeros(B, H, d, device=dev, dtype=torch.float32)
+    lse = torch.zeros(B, H, device=dev, dtype=torch.float32)
+    st = _noalloc(lib, q, k, v, lt, num_splits, out, lse)
+    if need > 1 << 20:
+        assert st == FD_ERR_SCRATCH_TOO_SMALL, (need, fdmod.status_str(st))
+        return
+    assert st == 0, (need, fdmod.status_str(st))
+    ref_out, ref_lse = fd.decode(q, k, v, lt, num_splits=num_splits, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert _close(out, ref_out, "bf16")
+    fin = torch.isfinite(ref_lse)
+    assert torch.equal(torch.isfinite(lse), fin)
+    assert float((lse[fin] - ref_lse[fin]).abs().max()) <= LSE_TOL["bf16"]
+
+
 def test_binding_decode_noalloc_matches_oracle(lib):
     """The Python binding's decode_noalloc against the float64 oracle, and its
     error for a problem beyond the scratch."""
