@@ -165,8 +165,10 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  *   q    [B, Hq, d]          k, v [B, Hkv, N, d]      out [B, Hq, d]
  *   lse  [B, Hq] float32 or NULL
  * G == 1 is fd_decode.  For G >= 2 the per-chunk contraction runs on the
- * tensor cores, which need 16-bit operands: in_dtype f16 or bf16, and
- * B*Hkv*N < 2^31.  A K/V head's query heads are processed in even slices of
+ * tensor cores, which need 16-bit operands: in_dtype f16 or bf16.  The
+ * cache may hold any number of rows in all (the copies address a row by its
+ * place in its (b, K/V head) block and the block's index).  A K/V head's
+ * query heads are processed in even slices of
  * at most 16 (8 at d = 256), each reading that K/V head's rows (MQA with
  * many heads included); the slices of one K/V head run side by side, so
  * their repeated reads are mostly served from L2.  The workspace size is
@@ -210,8 +212,9 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
  *   k_scale, v_scale  [B*Hkv] float32 (per sequence and K/V head)
  *   workspace         fd_workspace_size_gqa(B, Hq, Hkv, max_pages*page_size,
  *                     128, num_splits) bytes
- * d must be 128 and page_size 16 or a multiple of 32; any G >= 1 (G = 1
- * runs the same kernel).  FD_ERR_UNSUPPORTED otherwise.
+ * d must be 128, page_size 16 or a multiple of 32 and num_pages*Hkv <
+ * 2^31; any G >= 1 (G = 1 runs the same kernel).  FD_ERR_UNSUPPORTED
+ * otherwise.
  */
 fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k_pages, const void *v_pages,
                                   const float *k_scale, const float *v_scale, const int32_t *block_table,
@@ -238,7 +241,9 @@ fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k
  *                     d, num_splits) bytes, 256-byte aligned
  * page_size must be 16 or a multiple of 32 (a 32-token chunk then lies in
  * one page, or in two 16-token pages fetched one by one) and
- * num_pages*Hkv*page_size < 2^31; otherwise FD_ERR_UNSUPPORTED.  Bad table entries are handled as in fd_decode_paged
+ * num_pages*Hkv < 2^31 (a (page, K/V head) block is a 32-bit copy
+ * coordinate; the pool's total row count is not limited); otherwise
+ * FD_ERR_UNSUPPORTED.  Bad table entries are handled as in fd_decode_paged
  * (page 0 read instead, FD_ERR_BAD_PAGE reported).  G == 1 is
  * fd_decode_paged.
  */

@@ -213,37 +213,42 @@ EncodeTiledFn encode_tiled()
     return f;
 }
 
-// K or V [rows, d] 16-bit as the 3-D map [64 elements, rows, d/64 planes]
-// (strides d*2 and 128 bytes) with boxes [64, box_rows, box_planes] and the
-// 128-byte swizzle: a box lands in shared memory plane by plane.
-bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long rows, int box_rows,
-                 int box_planes)
+// K or V as `blocks` blocks of n rows of d 16-bit elements (a (b, K/V head)
+// of a contiguous cache, or a (page, K/V head) of a paged one), viewed as
+// the 4-D map [64 elements, n, blocks, d/64 planes] (strides d*2, n*d*2 and
+// 128 bytes) with boxes [64, box_rows, 1, box_planes] and the 128-byte
+// swizzle: a box lands in shared memory plane by plane.  A row is addressed
+// by (row in block, block), two coordinates below 2^31, so the cache may
+// hold any number of rows in all.
+bool make_kv_map(CUtensorMap *m, const void *base, int dtype, int d, long long n, long long blocks,
+                 int box_rows, int box_planes)
 {
     EncodeTiledFn fn = encode_tiled();
     if (!fn)
         return false;
-    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(d / 64)};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, 128};
-    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_planes};
-    const cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+    const cuuint64_t dims[4] = {64, (cuuint64_t)n, (cuuint64_t)blocks, (cuuint64_t)(d / 64)};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2, 128};
+    const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, (cuuint32_t)box_planes};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, dtype == FD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// E4M3 K or V [rows, 128 bytes] as the 2-D map [128, rows] of bytes with
-// boxes [128, box_rows] and the 128-byte swizzle.
-bool make_f8_map(CUtensorMap *m, const void *base, long long rows, int box_rows)
+// E4M3 K or V as `blocks` blocks of n rows of 128 bytes: the 3-D map [128,
+// n, blocks] of bytes (strides 128 and n*128) with boxes [128, box_rows, 1]
+// and the 128-byte swizzle.
+bool make_f8_map(CUtensorMap *m, const void *base, long long n, long long blocks, int box_rows)
 {
     EncodeTiledFn fn = encode_tiled();
     if (!fn)
         return false;
-    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
-    const cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+    const cuuint64_t dims[3] = {128, (cuuint64_t)n, (cuuint64_t)blocks};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)n * 128};
+    const cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -286,13 +291,13 @@ struct PagedKV {
 };
 
 // The grouped-query launch once an entry point has checked its arguments:
-// plan, workspace, the K and V tensor maps over `kv_rows` rows of d
-// elements, and the kernel's parameters.  `paged` is null for contiguous
-// K/V [B, Hkv, N, d].
+// plan, workspace, the K and V tensor maps over `kv_blocks` blocks of
+// `kv_n` rows of d elements (none when kv_blocks is 0), and the kernel's
+// parameters.  `paged` is null for contiguous K/V [B, Hkv, N, d].
 fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t *seqlens, int B, int Hq,
                      int Hkv, int N, int d, int in_dtype, int num_splits, float scale, void *out,
                      int out_dtype, float *lse, void *workspace, size_t workspace_bytes, void *stream,
-                     long long kv_rows, const PagedKV *paged, const float *k_scale = nullptr,
+                     long long kv_n, long long kv_blocks, const PagedKV *paged, const float *k_scale = nullptr,
                      const float *v_scale = nullptr, int q_dtype = -1)
 {
     const bool f8 = in_dtype == FD_E4M3;   // then q_dtype is q's own and no tensor maps are made
@@ -316,12 +321,14 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     gp.pages16 = (paged && paged->page_size == 16) ? 1 : 0;
     const int box_rows = gp.pages16 ? 16 : GqaCfg<__half, 128>::CT;
     const int box_planes = d / 64;
-    if (kv_rows > 0 && !f8) {
-        if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_rows, box_rows, box_planes) ||
-            !make_kv_map(&gp.tmv, v, in_dtype, d, kv_rows, box_rows, box_planes))
+    const bool maps = kv_n > 0 && kv_blocks > 0;
+    if (maps && !f8) {
+        if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_n, kv_blocks, box_rows, box_planes) ||
+            !make_kv_map(&gp.tmv, v, in_dtype, d, kv_n, kv_blocks, box_rows, box_planes))
             return FD_ERR_CUDA;
-    } else if (kv_rows > 0 && d == 128) {   // E4M3 at d = 128: swizzled byte boxes
-        if (!make_f8_map(&gp.tmk, k, kv_rows, box_rows) || !make_f8_map(&gp.tmv, v, kv_rows, box_rows))
+    } else if (maps && d == 128) {   // E4M3 at d = 128: swizzled byte boxes
+        if (!make_f8_map(&gp.tmk, k, kv_n, kv_blocks, box_rows) ||
+            !make_f8_map(&gp.tmv, v, kv_n, kv_blocks, box_rows))
             return FD_ERR_CUDA;
     }
     gp.G = Gs;
@@ -644,8 +651,6 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
     if (!valid_dtype(out_dtype) || !gqa_dim_ok(d) ||
         (in_dtype != FD_F16 && in_dtype != FD_BF16))
         return FD_ERR_UNSUPPORTED;
-    if ((long long)B * Hkv * N >= (1LL << 31))
-        return FD_ERR_UNSUPPORTED;  // tensor-map row coordinates are 32-bit
     if ((long long)B * Hq == 0)
         return FD_OK;
     if (!q || (N > 0 && (!k || !v)) || !out || !aligned(q, 16) || !aligned(k, 16) ||
@@ -653,7 +658,7 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
         (lse && !aligned(lse, 4)))
         return FD_ERR_INVALID_ARG;
     return gqa_common(q, k, v, seqlens, B, Hq, Hkv, N, d, in_dtype, num_splits, scale, out, out_dtype,
-                      lse, workspace, workspace_bytes, stream, (long long)B * Hkv * N, nullptr);
+                      lse, workspace, workspace_bytes, stream, N, (long long)B * Hkv, nullptr);
 }
 
 fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_pages,
@@ -678,10 +683,9 @@ fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_
         (in_dtype != FD_F16 && in_dtype != FD_BF16))
         return FD_ERR_UNSUPPORTED;
     // a chunk of CT tokens lies in one page, or 16-token pages are fetched a
-    // page at a time; rows are 32-bit tensor-map coordinates
-    const long long rows_per_page = (long long)Hkv * page_size;
-    if ((page_size % GqaCfg<__half, 128>::CT != 0 && page_size != 16) || num_pages >= (1LL << 31) ||
-        rows_per_page >= (1LL << 31) || num_pages * rows_per_page >= (1LL << 31))
+    // page at a time; a (page, K/V head) block is a 32-bit tensor-map
+    // coordinate
+    if ((page_size % GqaCfg<__half, 128>::CT != 0 && page_size != 16) || num_pages * Hkv >= (1LL << 31))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * Hq == 0)
         return FD_OK;
@@ -692,7 +696,7 @@ fd_status fd_decode_gqa_paged(const void *q, const void *k_pages, const void *v_
         return FD_ERR_INVALID_ARG;
     const PagedKV pk = {block_table, page_size, max_pages, num_pages};
     return gqa_common(q, k_pages, v_pages, seqlens, B, Hq, Hkv, N, d, in_dtype, num_splits, scale, out,
-                      out_dtype, lse, workspace, workspace_bytes, stream, pages ? num_pages * rows_per_page : 0,
+                      out_dtype, lse, workspace, workspace_bytes, stream, page_size, pages ? num_pages * Hkv : 0,
                       &pk);
 }
 
@@ -711,8 +715,6 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
         return FD_ERR_INVALID_ARG;
     if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
         return FD_ERR_UNSUPPORTED;
-    if ((long long)B * Hkv * N >= (1LL << 31))
-        return FD_ERR_UNSUPPORTED;  // tensor-map row coordinates are 32-bit
     if ((long long)B * Hq == 0)
         return FD_OK;
     if (!q || (N > 0 && (!k || !v)) || !k_scale || !v_scale || !out || !aligned(q, 16) || !aligned(k, 16) ||
@@ -720,7 +722,7 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
         (seqlens && !aligned(seqlens, 4)) || (lse && !aligned(lse, 4)))
         return FD_ERR_INVALID_ARG;
     return gqa_common(q, k, v, seqlens, B, Hq, Hkv, N, d, FD_E4M3, num_splits, scale, out, out_dtype, lse,
-                      workspace, workspace_bytes, stream, (long long)B * Hkv * N, nullptr, k_scale, v_scale,
+                      workspace, workspace_bytes, stream, N, (long long)B * Hkv, nullptr, k_scale, v_scale,
                       q_dtype);
 }
 
@@ -743,9 +745,7 @@ fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k
     // K/V head runs it too), pages of 16 or a multiple of 32 tokens
     if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || d != 128)
         return FD_ERR_UNSUPPORTED;
-    const long long rows_per_page = (long long)Hkv * page_size;
-    if ((page_size % GqaCfg<__half, 128>::CT != 0 && page_size != 16) || num_pages >= (1LL << 31) ||
-        rows_per_page >= (1LL << 31) || num_pages * rows_per_page >= (1LL << 31))
+    if ((page_size % GqaCfg<__half, 128>::CT != 0 && page_size != 16) || num_pages * Hkv >= (1LL << 31))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * Hq == 0)
         return FD_OK;
@@ -757,7 +757,7 @@ fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k
         return FD_ERR_INVALID_ARG;
     const PagedKV pk = {block_table, page_size, max_pages, num_pages};
     return gqa_common(q, k_pages, v_pages, seqlens, B, Hq, Hkv, N, d, FD_E4M3, num_splits, scale, out, out_dtype,
-                      lse, workspace, workspace_bytes, stream, pages ? num_pages * rows_per_page : 0, &pk, k_scale,
+                      lse, workspace, workspace_bytes, stream, page_size, pages ? num_pages * Hkv : 0, &pk, k_scale,
                       v_scale, q_dtype);
 }
 

@@ -205,6 +205,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// 4-D tiled copy global -> shared through a tensor map, completion on `bar`
+// (the same rule for x).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int x, int y, int z, int w,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
 // Barrier `id` (1..15) over `count` threads (whole warps) of the block.
 __device__ __forceinline__ void named_bar_sync(int id, int count)
 {

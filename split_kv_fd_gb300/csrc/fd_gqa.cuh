@@ -17,11 +17,12 @@
 //
 // Same decomposition, rings and merges as the split kernel (fd_split.cuh);
 // what differs:
-//  - K/V chunks arrive through tensor-map TMA (cp.async.bulk.tensor.3d) with
+//  - K/V chunks arrive through tensor-map TMA (cp.async.bulk.tensor.4d) with
 //    the 128-byte swizzle.  A stage holds a chunk as d/64 planes, plane j
 //    being elements [64j, 64j + 64) of the CT rows, 128 bytes per row: the
-//    map views K (or V) as [64 elements, rows, d/64 planes] (strides d*2 and
-//    128 bytes) and one box [64, CT, d/64] fetches a whole chunk.  With
+//    map views K (or V) as [64 elements, N rows, B*Hkv blocks, d/64 planes]
+//    (strides d*2, N*d*2 and 128 bytes) and one box [64, CT, 1, d/64]
+//    fetches a whole chunk of one (b, K/V head) block.  With
 //    128-byte rows the swizzle gives any 8 consecutive rows of a column 8
 //    different bank groups, so the ldmatrix reads are free of bank conflicts
 //    (rows of d = 128 kept whole, 256 bytes, would repeat the pattern every 4
@@ -104,8 +105,11 @@ template <typename T, int D, bool F8 = false> struct GqaCfg {
 };
 
 struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
-    CUtensorMap tmk;   // K as [64, rows, d/64] 16-bit elements, boxes [64, CT, d/64], 128B swizzle;
-                       // rows = B*Hkv*N, or num_pages*Hkv*page_size when paged
+    CUtensorMap tmk;   // K as [64, n, blocks, d/64] 16-bit elements (n = N token rows of each of
+                       // blocks = B*Hkv (b, K/V head) blocks; paged: n = page_size, blocks =
+                       // num_pages*Hkv), boxes [64, CT, 1, d/64], 128B swizzle.  E4M3 at d = 128:
+                       // [128 bytes, n, blocks], boxes [128, CT, 1].  Every coordinate stays
+                       // below 2^31 whatever the cache's total row count.
     CUtensorMap tmv;   // V likewise
     SplitParams s;     // s.H = Hkv; s.q is [B, Hkv*Gq, d]; outputs [B, Hkv*Gq, ...]
     int G;             // query heads per slice (the last slice of a K/V head may have fewer), <= MAXG
@@ -176,16 +180,6 @@ __device__ __forceinline__ long long vh_slot(const GqaParams &gp, const Ctx &ctx
         return bhv * p.P + i;
     const long long sr = piece_slot(p, ctx, 0, i, gf, off);
     return ((sr >> 1) * gp.NG + slice) * 2 + (sr & 1);
-}
-
-// 2-D tensor-map copy of box (x, y) into shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y), "r"(bar)
-        : "memory");
 }
 
 // The chunk walk of the split kernel's producer over the CTA's chunks c =
@@ -276,21 +270,24 @@ template <typename C, bool P16> struct TmaProducer {
                 for (int half = 0; half < 2; ++half) {
                     if (half == 0 ? !first : !second)
                         continue;
-                    const int row = (int)((checked_page(p, half == 0 ? pg : pg2) * p.H + s.h) * 16);
-                    tma_load_2d(kdst + half * HALF, &gp.tmk, 0, row, bar);
-                    tma_load_2d(kdst + C::CHUNK_BYTES + half * HALF, &gp.tmv, 0, row, bar);
+                    const int blk = (int)(checked_page(p, half == 0 ? pg : pg2) * p.H + s.h);
+                    tma_load_3d(kdst + half * HALF, &gp.tmk, 0, 0, blk, bar);
+                    tma_load_3d(kdst + C::CHUNK_BYTES + half * HALF, &gp.tmv, 0, 0, blk, bar);
                 }
             } else if constexpr (C::F8REG) {
                 // a box of CT E4M3 rows (128 bytes each, 128-byte swizzle) per
-                // operand; rows past the tensor end read as zeros
-                int row;
-                if (p.paged)
-                    row = (int)((checked_page(p, pg) * p.H + s.h) * p.page_size + t % p.page_size);
-                else
-                    row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
+                // operand; rows past the block's end read as zeros
+                int y, blk;
+                if (p.paged) {
+                    y = t % p.page_size;
+                    blk = (int)(checked_page(p, pg) * p.H + s.h);
+                } else {
+                    y = t;
+                    blk = s.b * p.H + s.h;
+                }
                 mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
-                tma_load_2d(kdst, &gp.tmk, 0, row, bar);
-                tma_load_2d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, row, bar);
+                tma_load_3d(kdst, &gp.tmk, 0, y, blk, bar);
+                tma_load_3d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, y, blk, bar);
             } else if constexpr (C::F8K) {
                 // the chunk's E4M3 rows as they are in memory (contiguous K/V)
                 const long long row = ((long long)s.b * p.H + s.h) * p.N + t;
@@ -307,20 +304,22 @@ template <typename C, bool P16> struct TmaProducer {
                 for (int half = 0; half < 2; ++half) {
                     if (half == 0 ? !first : !second)
                         continue;
-                    const long long page = checked_page(p, half == 0 ? pg : pg2);
-                    const int row = (int)((page * p.H + s.h) * 16);
-                    tma_load_3d(kdst + half * HALF, &gp.tmk, 0, row, 0, bar);
-                    tma_load_3d(kdst + C::CHUNK_BYTES + half * HALF, &gp.tmv, 0, row, 0, bar);
+                    const int blk = (int)(checked_page(p, half == 0 ? pg : pg2) * p.H + s.h);
+                    tma_load_4d(kdst + half * HALF, &gp.tmk, 0, 0, blk, 0, bar);
+                    tma_load_4d(kdst + C::CHUNK_BYTES + half * HALF, &gp.tmv, 0, 0, blk, 0, bar);
                 }
             } else {
-                int row;
-                if (p.paged)
-                    row = (int)((checked_page(p, pg) * p.H + s.h) * p.page_size + t % p.page_size);
-                else
-                    row = (int)(((long long)s.b * p.H + s.h) * p.N + t);
+                int y, blk;
+                if (p.paged) {
+                    y = t % p.page_size;
+                    blk = (int)(checked_page(p, pg) * p.H + s.h);
+                } else {
+                    y = t;
+                    blk = s.b * p.H + s.h;
+                }
                 mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
-                tma_load_3d(kdst, &gp.tmk, 0, row, 0, bar);
-                tma_load_3d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, row, 0, bar);
+                tma_load_4d(kdst, &gp.tmk, 0, y, blk, 0, bar);
+                tma_load_4d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, y, blk, 0, bar);
             }
         }
         c += stride;
@@ -329,36 +328,58 @@ template <typename C, bool P16> struct TmaProducer {
     }
 };
 
-// Elements e and e + 1 of q (float32, float16 or bfloat16 by q_dtype; e even)
-// as an f16 pair, the B-operand word of the f16 products.
-__device__ __forceinline__ uint32_t q_pair_f16(const void *q, int q_dtype, long long e)
+// Elements e and e + 1 of q (float32, float16 or bfloat16 by q_dtype; e
+// even) as floats.
+__device__ __forceinline__ float2 q_pair_f32(const void *q, int q_dtype, long long e)
 {
-    float a, b;
-    if (q_dtype == 0) {
-        const float2 f = __ldg(reinterpret_cast<const float2 *>(static_cast<const float *>(q) + e));
-        a = f.x;
-        b = f.y;
-    } else {
-        const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(static_cast<const uint16_t *>(q) + e));
-        if (q_dtype == 1) {
-            __half2 h;
-            memcpy(&h, &w, 4);
-            const float2 f = __half22float2(h);
-            a = f.x;
-            b = f.y;
-        } else {
-            __nv_bfloat162 h;
-            memcpy(&h, &w, 4);
-            const float2 f = __bfloat1622float2(h);
-            a = f.x;
-            b = f.y;
-        }
+    if (q_dtype == 0)
+        return __ldg(reinterpret_cast<const float2 *>(static_cast<const float *>(q) + e));
+    const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(static_cast<const uint16_t *>(q) + e));
+    if (q_dtype == 1) {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        return __half22float2(h);
     }
+    __nv_bfloat162 h;
+    memcpy(&h, &w, 4);
+    return __bfloat1622float2(h);
+}
+
+// Two floats as an f16 pair (round to nearest even), the B-operand word of
+// the f16 products.
+__device__ __forceinline__ uint32_t f16_pair(float a, float b)
+{
     const __half2 r = __floats2half2_rn(a, b);
     uint32_t u;
     memcpy(&u, &r, 4);
     return u;
 }
+
+// 2^e as a float for 0 <= e <= 127, built from its IEEE-754 bits (exact).
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// The power of two that brings a head's largest |q| (amax) below 2^14, as
+// its exponent e >= 0: q is rounded to f16 for the E4M3 products, whose
+// largest finite value is 65504, so a head with amax >= 2^14 is multiplied
+// by 2^-e first (exact) and its scores by 2^e after.  0 for amax < 2^14,
+// infinite or NaN.
+__device__ __forceinline__ int q_range_exp(float amax)
+{
+    if (!(amax >= 16384.f) || !(amax <= 3.4028235e38f))
+        return 0;
+    return (int)((__float_as_uint(amax) >> 23) & 0xff) - 127 - 13;
+}
+
+// Score scale of one head column of S^T: one value for every head, or one
+// per head column (E4M3 paths, whose heads may carry their own power of two).
+struct UniformScale {
+    float s;
+    __device__ __forceinline__ float operator()(int, int) const { return s; }
+};
+template <int NQ> struct HeadScale {
+    float s[NQ][2];   // [column tile][head 2(lane%4) + e]
+    __device__ __forceinline__ float operator()(int j, int e) const { return s[j][e]; }
+};
 
 // 16 E4M3 bytes (elements 0..15) as 16 f16 values, exactly: elements 0..7
 // in lo, 8..15 in hi (cvt.rn.f16x2.e4m3x2 takes a byte pair, the lower byte
@@ -442,10 +463,11 @@ template <typename C, int NQ> struct GqaState {
 // update in fp32, then O^T += V^T (P_hi + P_lo)^T.  qb holds Q^T as B
 // fragments: qb[j][s] = heads of column tile j, k-step s.
 // kfrag(s, a) gives K's A fragments of k-step s (the default reads the
-// stage with ldmatrix; E4M3 K converts them from registers).
-template <typename T, typename C, int NQ, bool P16, typename KF>
+// stage with ldmatrix; E4M3 K converts them from registers).  scale(j, e)
+// is the base-2 score scale of this thread's head column e of tile j.
+template <typename T, typename C, int NQ, bool P16, typename KF, typename SC>
 __device__ __forceinline__ void gqa_chunk_kf(KF kfrag, uint32_t vstage, int row0, int vlo, int vhi,
-                                             const uint32_t (*qb)[C::KSTEPS][2], float scale_log2, int lane,
+                                             const uint32_t (*qb)[C::KSTEPS][2], const SC &scale, int lane,
                                              GqaState<C, NQ> &st)
 {
     // S^T for the warp's 16 tokens; even and odd k-steps accumulate
@@ -469,10 +491,10 @@ __device__ __forceinline__ void gqa_chunk_kf(KF kfrag, uint32_t vstage, int row0
     const bool v0 = r >= vlo && r < vhi, v1 = r + 8 >= vlo && r + 8 < vhi;
 #pragma unroll
     for (int j = 0; j < NQ; ++j) {
-        sc[j][0] = v0 ? (sc[j][0] + sx[j][0]) * scale_log2 : -INFINITY;
-        sc[j][1] = v0 ? (sc[j][1] + sx[j][1]) * scale_log2 : -INFINITY;
-        sc[j][2] = v1 ? (sc[j][2] + sx[j][2]) * scale_log2 : -INFINITY;
-        sc[j][3] = v1 ? (sc[j][3] + sx[j][3]) * scale_log2 : -INFINITY;
+        sc[j][0] = v0 ? (sc[j][0] + sx[j][0]) * scale(j, 0) : -INFINITY;
+        sc[j][1] = v0 ? (sc[j][1] + sx[j][1]) * scale(j, 1) : -INFINITY;
+        sc[j][2] = v1 ? (sc[j][2] + sx[j][2]) * scale(j, 0) : -INFINITY;
+        sc[j][3] = v1 ? (sc[j][3] + sx[j][3]) * scale(j, 1) : -INFINITY;
     }
     // per head: the max over the chunk's 16 tokens (a head's tokens live in
     // the 8 lanes with the same lane % 4), the rescale, and P
@@ -525,9 +547,9 @@ __device__ __forceinline__ void gqa_chunk_kf(KF kfrag, uint32_t vstage, int row0
 }
 
 // The chunk with K's fragments read from the stage.
-template <typename T, typename C, int NQ, bool P16>
+template <typename T, typename C, int NQ, bool P16, typename SC>
 __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int row0, int vlo, int vhi,
-                                          const uint32_t (*qb)[C::KSTEPS][2], float scale_log2, int lane,
+                                          const uint32_t (*qb)[C::KSTEPS][2], const SC &scale, int lane,
                                           GqaState<C, NQ> &st)
 {
     const int ktok = row0 + (lane & 15);
@@ -535,7 +557,7 @@ __device__ __forceinline__ void gqa_chunk(uint32_t kstage, uint32_t vstage, int 
         [&](int s, uint32_t (&a)[4]) {
             ldsm_x4(kstage + stage_off<C, P16>(ktok, 2 * s + (lane >> 4)), a[0], a[1], a[2], a[3]);
         },
-        vstage, row0, vlo, vhi, qb, scale_log2, lane, st);
+        vstage, row0, vlo, vhi, qb, scale, lane, st);
 }
 
 // E4M3 K at d = 128: the warp's 16 staged rows (128-byte swizzle) as raw

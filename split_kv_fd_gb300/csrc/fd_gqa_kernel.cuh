@@ -232,23 +232,47 @@ __global__ void __launch_bounds__(GqaCfg<T, D, F8>::THREADS, 1) gqa_kernel(const
             }
             // Q^T of the head group as mma B fragments (heads >= gv are zero)
             uint32_t qb[NQ][C::KSTEPS][2];
+            // E4M3: each head's base-2 score scale, with the power of two that
+            // brought its q into the f16 range (q_range_exp)
+            HeadScale<NQ> hsc;
             {
                 const uint32_t *q32 = static_cast<const uint32_t *>(p.q);
                 const long long qbase = qrow0 * D;  // elements
 #pragma unroll
                 for (int j = 0; j < NQ; ++j) {
                     const int n = 8 * j + qn;
+                    if constexpr (C::F8K) {   // q of any dtype, as f16 pairs
+                        float2 qf[C::KSTEPS][2];
+                        float amax = 0.f;
 #pragma unroll
-                    for (int s = 0; s < C::KSTEPS; ++s) {
-                        const long long e = qbase + (long long)n * D + 16 * s + qk;
-                        if constexpr (C::F8REG) {   // d permuted as K's fragments (f8_k_frag)
-                            const long long e4 = qbase + (long long)n * D + 16 * s + 4 * (lane & 3);
-                            qb[j][s][0] = n < gv ? q_pair_f16(p.q, p.q_dtype, e4) : 0u;
-                            qb[j][s][1] = n < gv ? q_pair_f16(p.q, p.q_dtype, e4 + 2) : 0u;
-                        } else if constexpr (C::F8K) {   // q of any dtype, as f16 pairs
-                            qb[j][s][0] = n < gv ? q_pair_f16(p.q, p.q_dtype, e) : 0u;
-                            qb[j][s][1] = n < gv ? q_pair_f16(p.q, p.q_dtype, e + 8) : 0u;
-                        } else {
+                        for (int s = 0; s < C::KSTEPS; ++s) {
+                            // F8REG: d permuted as K's fragments (f8_k_frag)
+                            const long long e0 = qbase + (long long)n * D + 16 * s + (C::F8REG ? 4 * (lane & 3) : qk);
+                            const long long e1 = e0 + (C::F8REG ? 2 : 8);
+                            qf[s][0] = n < gv ? q_pair_f32(p.q, p.q_dtype, e0) : make_float2(0.f, 0.f);
+                            qf[s][1] = n < gv ? q_pair_f32(p.q, p.q_dtype, e1) : make_float2(0.f, 0.f);
+                            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(qf[s][0].x), fabsf(qf[s][0].y)),
+                                                     fmaxf(fabsf(qf[s][1].x), fabsf(qf[s][1].y))));
+                        }
+                        // the head's 4 lanes (same lane / 4) hold all its d values
+                        amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, 1));
+                        amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, 2));
+                        const int ex = q_range_exp(amax);
+                        const float down = 1.f / pow2i(ex);   // exact: a power of two
+#pragma unroll
+                        for (int s = 0; s < C::KSTEPS; ++s) {
+                            qb[j][s][0] = f16_pair(qf[s][0].x * down, qf[s][0].y * down);
+                            qb[j][s][1] = f16_pair(qf[s][1].x * down, qf[s][1].y * down);
+                        }
+                        // the accumulator's head columns 2(lane%4) + e of this
+                        // tile belong to lanes 4 (2(lane%4) + e)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            hsc.s[j][e] = seg_scale * pow2i(__shfl_sync(FULL_MASK, ex, 4 * (2 * (lane & 3) + e)));
+                    } else {
+#pragma unroll
+                        for (int s = 0; s < C::KSTEPS; ++s) {
+                            const long long e = qbase + (long long)n * D + 16 * s + qk;
                             qb[j][s][0] = n < gv ? __ldg(q32 + e / 2) : 0u;
                             qb[j][s][1] = n < gv ? __ldg(q32 + (e + 8) / 2) : 0u;
                         }
@@ -306,7 +330,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D, F8>::THREADS, 1) gqa_kernel(const
                     if (work)
                         gqa_chunk_kf<T, C, NQ, true>(
                             [&](int s, uint32_t (&a)[4]) { f8_k_frag(&kraw[s >> 1][2 * (s & 1)], a); }, area, 0,
-                            vlo, vhi, qb, seg_scale, lane, st);
+                            vlo, vhi, qb, hsc, lane, st);
                     __syncwarp();   // the area is rewritten by the next chunk
                     continue;
                 } else if constexpr (C::F8K) {
@@ -325,7 +349,7 @@ __global__ void __launch_bounds__(GqaCfg<T, D, F8>::THREADS, 1) gqa_kernel(const
                     if (issuer && !dead && prod.issue(gp, ctx, kb, bar_base + stage * 8, lane))
                         ++issued;
                     if (work)
-                        gqa_chunk<T, C, NQ, true>(area, area + C::AREA_BYTES / 2, 0, vlo, vhi, qb, seg_scale, lane,
+                        gqa_chunk<T, C, NQ, true>(area, area + C::AREA_BYTES / 2, 0, vlo, vhi, qb, hsc, lane,
                                                   st);
                     __syncwarp();   // the area is rewritten by the next chunk
                     continue;
@@ -350,7 +374,8 @@ __global__ void __launch_bounds__(GqaCfg<T, D, F8>::THREADS, 1) gqa_kernel(const
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
                     }
-                    gqa_chunk<T, C, NQ, P16>(kb, kb + C::CHUNK_BYTES, row0, vlo, vhi, qb, seg_scale, lane, st);
+                    gqa_chunk<T, C, NQ, P16>(kb, kb + C::CHUNK_BYTES, row0, vlo, vhi, qb, UniformScale{seg_scale},
+                                             lane, st);
                 }
                 __syncwarp();
                 // release the stage; the issuer refills it once both warps have

@@ -159,7 +159,9 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
     assert gqa(1, 16, 2, 64, 128, dt=0) == 2     # G > 1 needs 16-bit K/V
     assert gqa(1, 16, 2, 64, 96) == 2            # head dim
     assert gqa(1, 8, 8, 64, 96) == 2             # G = 1 goes to fd_decode's checks
-    assert gqa(1, 16, 2, 1 << 30, 128) == 2      # 2^31 K/V rows: past 32-bit coordinates
+    # 2^31 K/V rows in all is no limit (copies address (row in block, block)):
+    # only the null q is refused here
+    assert gqa(1, 16, 2, 1 << 30, 128, q=None) == 1
     assert gqa(1, 16, 2, 64, 128, q=None) == 1
     assert gqa(1, 16, 2, 64, 128, ns=-2) == 1
     assert gqa(0, 16, 2, 64, 128, q=None) == 0   # empty
@@ -208,7 +210,10 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
     assert gqa_paged(ps=8) == 2                   # pages of 16 or a multiple of 32 tokens
     assert gqa_paged(ps=48) == 2
     assert gqa_paged(dt=0) == 2                   # 16-bit K/V only
-    assert gqa_paged(npg=1 << 22, Hkv=8, ps=128) == 2   # 2^32 page rows: past 32-bit coordinates
+    assert gqa_paged(npg=1 << 28, Hkv=8) == 2     # 2^31 (page, K/V head) blocks: past 32-bit coordinates
+    # a serving-size pool (2^20 pages x 8 heads x 256 tokens = 2^31 rows) is
+    # accepted: only the missing lengths are refused here
+    assert gqa_paged(npg=1 << 20, Hkv=8, ps=256, lens=None) == 1
     assert gqa_paged(lens=None) == 1
     assert gqa_paged(npg=0) == 1
     assert gqa_paged(table=P(4098)) == 1
@@ -233,6 +238,8 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
     assert gqa_paged_fp8(ks=None) == 1
     assert gqa_paged_fp8(Hq=6, Hkv=4) == 1
     assert gqa_paged_fp8(B=0) == 0
+    assert gqa_paged_fp8(npg=1 << 28, Hkv=8) == 2   # 2^31 (page, K/V head) blocks
+    assert gqa_paged_fp8(npg=1 << 20, Hkv=8, ps=256, ks=None) == 1
 
     assert lib.fd_workspace_size_gqa(1, 6, 4, 64, 128, 0) == 0
     assert lib.fd_combine_mlo(dm, dm, dm, 1, 1, 4, 80, dm, 0, None, None) == 2
@@ -246,4 +253,12 @@ def test_valid_call_without_a_gpu_reports_a_cuda_error(lib):
     dm = P(4096)
     assert lib.fd_decode(dm, dm, dm, None, 1, 1, 8, 128, 2, 0, 1.0, dm, 2, None, P(1 << 20),
                          1 << 20, None) == 4
+    # caches of 2^31 rows and more pass every host check of the grouped-query
+    # entry points (contiguous, and a 2^20-page pool of 256-token pages)
+    assert lib.fd_decode_gqa(dm, dm, dm, None, 2, 16, 2, 1 << 30, 128, 2, 0, 1.0, dm, 2, None,
+                             P(1 << 20), 1 << 20, None) == 4
+    assert lib.fd_decode_gqa_paged(dm, dm, dm, dm, dm, 1, 16, 8, 128, 256, 4, 1 << 20, 2, 0, 1.0, dm, 2,
+                                   None, P(1 << 20), 1 << 20, None) == 4
+    assert lib.fd_decode_gqa_paged_fp8(dm, 2, dm, dm, dm, dm, dm, dm, 1, 16, 8, 128, 256, 4, 1 << 20, 0,
+                                       1.0, dm, 2, None, P(1 << 20), 1 << 20, None) == 4
     assert lib.fd_num_sms() <= 0

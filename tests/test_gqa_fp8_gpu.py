@@ -163,3 +163,35 @@ def test_paged_gqa_fp8_full_size_equals_contiguous():
     del k8, v8
     out, lse = fd.decode_gqa_paged_fp8(q, kp, vp, ks, vs, table, lens, scale=w.scale, out_dtype=torch.float32)
     assert torch.equal(out, cout) and torch.equal(lse, clse)
+
+
+@pytest.mark.parametrize("qdt", ["f32", "bf16"])
+@pytest.mark.parametrize("d,page_size", [(64, 0), (128, 0), (128, 16), (128, 64)])
+def test_gqa_fp8_q_beyond_f16_range(qdt, d, page_size):
+    """q far outside f16's range (|q| up to ~1e6 > 65504), which the E4M3
+    products take in f16: each head's q is brought into range by a power of
+    two and its scores scaled back, so the result is the oracle's.  K is
+    scaled down so that the scores stay moderate (the test is about q's
+    range, not about scores of 1e6)."""
+    Hkv, G, B = 2, 8, 2
+    _, k, v, lt = random_case(B, Hkv, 500, d, "bf16", lens=[500, 77], seed=3, nan_pad=False)
+    g = torch.Generator().manual_seed(11)
+    mag = torch.tensor([1.0, 3.0, 1e3, 7e4, 1e5, 3e5, 1e6, 2.5e5] * Hkv)   # per query head
+    q = (torch.randn(B, G * Hkv, d, generator=g) * mag[None, :, None]).to(QT[qdt])
+    assert float(q.float().abs().max()) > 65504
+    k = (k.float() * 1e-5).to(torch.bfloat16)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    ref_out, ref_lse = _reference(q, k8, v8, ks, vs, G, lt)
+    args = (q.to(DEV), None, None, ks.to(DEV), vs.to(DEV))
+    if page_size:
+        kp, table = to_paged_bytes(k8, page_size, seed=page_size)
+        vp, _ = to_paged_bytes(v8, page_size, seed=page_size)
+        out, lse = fd.decode_gqa_paged_fp8(args[0], kp.to(DEV), vp.to(DEV), args[3], args[4], table.to(DEV),
+                                           lt.to(DEV), out_dtype=torch.float32)
+    else:
+        out, lse = fd.decode_gqa_fp8(args[0], k8.to(DEV), v8.to(DEV), args[3], args[4], lt.to(DEV),
+                                     out_dtype=torch.float32)
+    check_out(out, ref_out, "bf16")
+    check_lse(lse, ref_lse, "bf16")
+    assert fd.device_status() == 0
