@@ -52,6 +52,8 @@ KERNEL_SOURCES = {
                      "fd_split_f16.cu", "fd_split_f32.cu", "fd_split_fp8.cu"],
     "gqa_kernel": ["fd_gqa.cuh", "fd_gqa_kernel.cuh", "fd_gqa_bf16.cu", "fd_gqa_f16.cu", "fd_split.cuh",
                    "fd_device.cuh", "fd_internal.h"],
+    "gqa_tc_kernel": ["fd_gqa_tc.cuh", "fd_tc.cuh", "fd_gqa_tc.cu", "fd_gqa.cuh", "fd_split.cuh",
+                      "fd_device.cuh", "fd_internal.h"],
 }
 
 
@@ -92,12 +94,25 @@ def kernel_source_hash(kernel: str = "split_kernel") -> str:
     return h.hexdigest()[:16]
 
 
+# groups of at least this many query heads per K/V head run the tcgen05
+# kernel (contiguous 16-bit K/V, head dim 64 or 128)
+GQA_TC_MIN_G = 17
+
+
+def kernel_key(w, fp8: bool, paged: bool) -> str:
+    """Which kernel does the timed work: split_kernel, gqa_kernel or gqa_tc_kernel."""
+    if w.kv_heads == w.H:
+        return "split_kernel"
+    if not fp8 and not paged and w.d <= 128 and w.H // w.kv_heads >= GQA_TC_MIN_G:
+        return "gqa_tc_kernel"
+    return "gqa_kernel"
+
+
 def kernel_name(w, fp8: bool, paged: bool) -> str:
     """The kernel that does the timed work, as ncu names it."""
-    if w.kv_heads != w.H:
-        return f"fd::gqa_kernel<{'e4m3' if fp8 else w.dtype}, {w.d}>" + (" (paged)" if paged else "")
+    key = kernel_key(w, fp8, paged)
     elt = "e4m3" if fp8 else w.dtype
-    return f"fd::split_kernel<{elt}, {w.d}>" + (" (paged)" if paged else "")
+    return f"fd::{key}<{elt}, {w.d}>" + (" (paged)" if paged else "")
 
 
 def profiled_traffic(workload: str, kernel: str = "split_kernel"):
@@ -622,8 +637,8 @@ def run_ours(args, w):
                          "traffic": (None if table is not None
                                      else profiled_traffic(w.name + ("+e4m3" if k_scale is not None
                                                                      else ""),
-                                                           "gqa_kernel" if w.kv_heads != w.H
-                                                           else "split_kernel")),
+                                                           kernel_key(w, k_scale is not None,
+                                                                      table is not None))),
                          "kernel": kernel_name(w, k_scale is not None, table is not None),
                          "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                          "algorithmic_bytes_per_launch": alg, "mean_launch_ms": kern_ms},

@@ -3,6 +3,7 @@
 // launches.  Nothing here computes attention; every step runs in the kernels.
 #include "fd.h"
 #include "fd_gqa.cuh"
+#include "fd_gqa_tc.cuh"
 #include "fd_internal.h"
 #include "fd_split.cuh"
 
@@ -133,6 +134,24 @@ void gqa_slices(int d, int G, int &NG, int &Gs, bool f8 = false)
 {
     const int maxg = f8 ? GqaCfg<__half, 128, true>::MAXG
                         : (d == 256 ? GqaCfg<__half, 256>::MAXG : GqaCfg<__half, 128>::MAXG);
+    NG = (G + maxg - 1) / maxg;
+    Gs = (G + NG - 1) / NG;
+}
+
+// Whether a grouped-query call runs the tcgen05 kernel (fd_gqa_tc.cuh): 16-bit
+// K/V in a contiguous cache, head dim 64 or 128, and groups large enough
+// that staging each chunk once per 16 heads (the mma.sync kernel) would
+// bound it.
+bool gqa_use_tc(int in_dtype, int d, int G, bool paged)
+{
+    return !paged && (in_dtype == FD_F16 || in_dtype == FD_BF16) && (d == 64 || d == 128) &&
+           G >= FD_GQA_TC_MIN_G;
+}
+
+// The tcgen05 kernel's slices: up to 128 query heads (its MMA rows) each.
+void gqa_tc_slices(int G, int &NG, int &Gs)
+{
+    constexpr int maxg = TcCfg<__half, 128>::MAXG;
     NG = (G + maxg - 1) / maxg;
     Gs = (G + NG - 1) / NG;
 }
@@ -302,8 +321,12 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
 {
     const bool f8 = in_dtype == FD_E4M3;   // then q_dtype is q's own and no tensor maps are made
     const int G = Hq / Hkv;
+    const bool tc = gqa_use_tc(in_dtype, d, G, paged != nullptr);
     int NG, Gs;
-    gqa_slices(d, G, NG, Gs, f8);
+    if (tc)
+        gqa_tc_slices(G, NG, Gs);
+    else
+        gqa_slices(d, G, NG, Gs, f8);
     const long long Hv = (long long)Hkv * NG;   // virtual heads
     const int sms = sm_count();
     unsigned *st = status_ptr();
@@ -319,7 +342,7 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     // boxes of one chunk (CT rows, every plane), or with 16-token pages of one
     // page (16 rows, every plane)
     gp.pages16 = (paged && paged->page_size == 16) ? 1 : 0;
-    const int box_rows = gp.pages16 ? 16 : GqaCfg<__half, 128>::CT;
+    const int box_rows = tc ? TcCfg<__half, 128>::CT : gp.pages16 ? 16 : GqaCfg<__half, 128>::CT;
     const int box_planes = d / 64;
     const bool maps = kv_n > 0 && kv_blocks > 0;
     if (maps && !f8) {
@@ -356,7 +379,9 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (!clear_counters(p, (long long)B * Hv, cs))
         return FD_ERR_CUDA;
-    const cudaError_t e = f8 ? launch_gqa_f8(d, gp, cs) : launch_gqa(in_dtype, d, gp, cs);
+    const cudaError_t e = tc ? launch_gqa_tc(in_dtype, d, gp, cs)
+                          : f8 ? launch_gqa_f8(d, gp, cs)
+                               : launch_gqa(in_dtype, d, gp, cs);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
@@ -625,11 +650,19 @@ size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_split
     const int sms = sm_count();
     if (sms <= 0)
         return 0;
-    // the larger of the 16-bit and the E4M3 kernels' layouts (their slices differ)
+    // the largest of the grouped-query kernels' layouts (their slices differ):
+    // mma.sync 16-bit, mma.sync E4M3 and tcgen05
     size_t total = 0;
-    for (int f8 = 0; f8 < (d <= 128 ? 2 : 1); ++f8) {
+    for (int kind = 0; kind < 3; ++kind) {
+        if (kind > 0 && d > 128)
+            continue;
+        if (kind == 2 && !gqa_use_tc(FD_BF16, d, Hq / Hkv, false))
+            continue;
         int NG, Gs;
-        gqa_slices(d, Hq / Hkv, NG, Gs, f8 != 0);
+        if (kind == 2)
+            gqa_tc_slices(Hq / Hkv, NG, Gs);
+        else
+            gqa_slices(d, Hq / Hkv, NG, Gs, kind == 1);
         const Plan pl = gqa_plan(B, Hkv, N, d, num_splits, sms, NG);
         total = std::max(total, ws_layout(pl.slots * Gs, d, (long long)B * Hkv * NG).total);
     }

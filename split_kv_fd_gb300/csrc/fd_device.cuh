@@ -73,6 +73,23 @@ __device__ __forceinline__ unsigned long long global_ns()
     return t;
 }
 
+// Bounded wait for phase `parity` of barrier `bar` by one thread on its own
+// (no warp vote: for a lane that runs a role by itself while its warp's
+// other lanes wait elsewhere).
+__device__ __forceinline__ bool mbar_wait_bounded_thread(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (unsigned i = 0; i < WAIT_LIMIT_POLLS; ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 63u) == 63u && global_ns() - t0 > WAIT_LIMIT_NS)
+            break;
+    }
+    return false;
+}
+
 // Bounded wait for phase `parity` of barrier `bar`.  Every lane polls; the
 // result is made warp-uniform (all lanes must have seen completion).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
