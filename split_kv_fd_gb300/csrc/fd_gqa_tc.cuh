@@ -1,40 +1,43 @@
 // fd_gqa_tc.cuh -- grouped-query decode for large groups (MQA and GQA with
 // many query heads per K/V head, "从第一性原理推导 Flash Attention" §8) on
-// the fifth-generation tensor cores: tcgen05.mma with operands in shared
-// memory and accumulators in tensor memory (TMEM).
+// the fifth-generation tensor cores: tcgen05.mma with accumulators in tensor
+// memory (TMEM).
 //
 // Per (b, K/V head) and chunk of CT = 64 tokens the work is two dense
 // products over all the K/V head's query heads at once (up to 128, the MMA's
 // M; more are served in slices by adjacent CTAs):
-//     S [128 x CT] = Q [128 x d] . K_chunk^T      (TMEM, fp32)
-//     O [128 x d] += P [128 x CT] . V_chunk       (TMEM, fp32, the whole segment)
+//     S [128 x CT] = Q [128 x d] . K_chunk^T     (Q and K in shared memory)
+//     O [128 x d] += P [128 x CT] . V_chunk      (P in TMEM, V in shared memory)
 // so every K/V byte enters shared memory once per CTA, whatever the number
 // of query heads (the mma.sync kernel of fd_gqa.cuh stages a chunk once per
 // 16 heads).  The online softmax between the two products runs in fp32
 // registers, one thread per query head (TMEM lane = MMA row = head):
 //  - S is read with tcgen05.ld; the scores past the chunk's tokens are
 //    masked; P = 2^(s - m_ref) is split into a 16-bit high part and the
-//    16-bit remainder, both written to shared memory (K-major, 128-byte
-//    swizzle), and the two products P_hi V + P_lo V keep P.V close to fp32
-//    accuracy with 16-bit operands.
+//    16-bit remainder, both written back into the chunk's S columns of TMEM
+//    (tcgen05.st), and the two products P_hi V + P_lo V keep P.V close to
+//    fp32 accuracy with 16-bit operands.
 //  - The rescale of the block-wise update ("FlashDecoding 数学推导" §2.4.1:
 //    acc and l times exp(m_old - m_new) when the max grows) is done lazily:
 //    the reference max m_ref moves only when a chunk's max exceeds it by
-//    more than TAU (in base 2), and only then is the head's O row in TMEM
-//    rescaled (tcgen05.ld, multiply, tcgen05.st).  In between, P may reach
-//    2^TAU, which fp32 and the 16-bit high part hold exactly enough; the
-//    result is the same quotient (o = acc / l with both relative to m_ref).
+//    more than TAU (in base 2), and only then are the head's O row in TMEM
+//    and l rescaled.  In between, P may reach 2^TAU, which fp32 and the
+//    16-bit high part hold exactly enough; the quotient o = acc / l is the
+//    same.
 //
-// Warp roles (192 threads, one CTA per SM):
-//  - warps 0-3: softmax, one query head per thread (TMEM lanes 0-127);
-//  - warp 4: the producer, K and V chunks by tensor-map TMA into a ring of
+// Warp roles (320 threads, one CTA per SM):
+//  - warps 0-3 and 4-7: two softmax warpgroups taking the chunks in turn
+//    (chunk j of the CTA goes to group j % 2), each with its own O
+//    accumulator and (m_ref, l) per head; at a segment end group 0 merges
+//    the two states ("FlashDecoding 数学推导" §2.4.2) and writes the result;
+//  - warp 8: the producer, K and V chunks by tensor-map TMA into a ring of
 //    STAGES stages (128 KB in flight, as in the other kernels);
-//  - warp 5: allocates TMEM; its lane 0 issues the MMAs.
-// Two S buffers in TMEM let the MMA warp compute S for chunk c + 1 while the
-// softmax threads work on chunk c; P.V of chunk c runs while they read S of
-// chunk c + 1.  Every hand-off is an mbarrier (the MMA warp's through
+//  - warp 9: allocates TMEM; its lane 0 issues the MMAs, S of chunk j + 1
+//    ahead of P.V of chunk j.
+// TMEM holds four S/P buffers (chunk j in buffer j % 4) and the two O
+// accumulators.  Every hand-off is an mbarrier (the MMA warp's through
 // tcgen05.commit), and every wait is bounded: on expiry a role records
-// FD_ERR_DEVICE_TIMEOUT, stops, drains what it issued and the CTA frees its
+// FD_ERR_DEVICE_TIMEOUT, stops, drains what it issued, and the CTA frees its
 // TMEM.
 //
 // The decomposition, slots, arrival counters and merges are those of the
@@ -68,36 +71,35 @@ template <typename T, int D> struct TcCfg {
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
     static constexpr int QPLANE = M * 128;         // one 64-element plane of Q
     static constexpr int Q_BYTES = LINES * QPLANE;
-    static constexpr int PHALF = M * CT * 2;       // P_hi (then P_lo): [M][CT] 16-bit, one plane
-    static constexpr int P_BYTES = 2 * PHALF;
-    static constexpr int SOFT_THREADS = 128, PROD_WARP = 4, MMA_WARP = 5, THREADS = 192;
-    // mbarriers: full[STAGES], empty[STAGES], s_full[2], s_free[2], q_full, p_full, o_full, fin,
-    // and the softmax warps' segment-end barrier
-    static constexpr int NBAR = 2 * STAGES + 9;
-    static constexpr int TMEM_O = 2 * CT;          // S buffers at columns 0 and CT, O after them
-    static constexpr uint32_t TMEM_COLS = (2 * CT + D) <= 256 ? 256u : 512u;
-    static constexpr float TAU = 8.f;              // lazy-rescale threshold (base 2)
     static constexpr int MERGE_PB = 64;            // pieces merged with weights in shared memory
+    static constexpr int SCR_BYTES = MERGE_PB * 8 + MERGE_PB * MAXG * 4 + 2 * MAXG * 4;
+    static constexpr int XCH_BYTES = 2 * M * 2 * 4;   // group 1's (m_ref, l) per head, two segments
+    static constexpr int WG_THREADS = 128, PROD_WARP = 8, MMA_WARP = 9, THREADS = 320;
+    // mbarriers: full[STAGES], empty[STAGES], s_full[4], s_free[4], p_full[2],
+    // o_full[2], q_full, fin, seg (both groups), wg0 (group 0)
+    static constexpr int NBAR = 2 * STAGES + 16;
+    static constexpr int TMEM_O = 4 * CT;          // S/P buffers at columns 0, 64, 128, 192
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr float TAU = 8.f;              // lazy-rescale threshold (base 2)
     static_assert(D == 64 || D == 128, "head dim 64 or 128");
-    static_assert(CT == 64, "P is one 128-byte plane per row");
-    static_assert(RING_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0 && PHALF % 1024 == 0, "1024-byte atoms");
-    // the last arriver's merge scratch lives in the Q and P buffers
-    static_assert(MERGE_PB * 8 + MERGE_PB * MAXG * 4 + 2 * MAXG * 4 <= Q_BYTES + P_BYTES, "merge scratch");
+    static_assert(CT == 64, "an S buffer holds P_hi and P_lo in its 64 columns");
+    static_assert(TMEM_O + 2 * D <= (int)TMEM_COLS, "TMEM columns");
+    static_assert(RING_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "1024-byte atoms");
 
     static size_t smem_bytes(int decomp, int B)
     {
-        size_t s = 1024 + RING_BYTES + Q_BYTES + P_BYTES + NBAR * 8 + 16;
+        size_t s = 1024 + RING_BYTES + Q_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16;
         if (decomp == DECOMP_BALANCED)
             s += (size_t)(B + 1) * 8 + (size_t)B * 4;
         return s;
     }
 };
 
-// A barrier of the 4 softmax warps on an mbarrier (count 4), with the
-// bounded wait: a warp whose partner gave up does not hang here.  `phase`
-// is the parity of the next completion; every softmax thread runs the same
+// A barrier of `warps` warps on an mbarrier initialised with that count,
+// with the bounded wait: a warp whose partner gave up does not hang here.
+// `phase` is the parity of the next completion; the warps run the same
 // sequence of syncs.  Returns false on expiry.
-struct SoftBar {
+struct WarpBar {
     uint32_t bar;
     uint32_t phase;
     __device__ __forceinline__ bool sync(int lane)
@@ -111,16 +113,47 @@ struct SoftBar {
     }
 };
 
-// Stage 2 of a (b, virtual head) by the last piece to arrive, on the 128
-// softmax threads: the m/l/o merge ("FlashDecoding 数学推导" §2.4.2) of the
-// `target` workspace partials of each of its Gv query rows.  With at most
-// MERGE_PB pieces the per-(piece, head) weights are formed once in `scr`
-// (the free Q and P buffers); otherwise each output element walks the
-// pieces itself.
+// Eight consecutive outputs from index idx (a multiple of 8) in out_dtype,
+// 16-byte stores for 16-bit outputs.
+__device__ __forceinline__ void store_out8(void *out, long long idx, int out_dtype, const float *x)
+{
+    if (out_dtype == 0) {
+        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + idx);
+        o[0] = make_float4(x[0], x[1], x[2], x[3]);
+        o[1] = make_float4(x[4], x[5], x[6], x[7]);
+        return;
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = out_dtype == 1 ? Mma<__half>::pack(x[2 * i], x[2 * i + 1])
+                              : Mma<__nv_bfloat16>::pack(x[2 * i], x[2 * i + 1]);
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + idx) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Four consecutive outputs from index idx (a multiple of 4).
+__device__ __forceinline__ void store_out4(void *out, long long idx, int out_dtype, float4 x)
+{
+    if (out_dtype == 0) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + idx) = x;
+        return;
+    }
+    const uint32_t a = out_dtype == 1 ? Mma<__half>::pack(x.x, x.y) : Mma<__nv_bfloat16>::pack(x.x, x.y);
+    const uint32_t b = out_dtype == 1 ? Mma<__half>::pack(x.z, x.w) : Mma<__nv_bfloat16>::pack(x.z, x.w);
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + idx) = make_uint2(a, b);
+}
+
+// Stage 2 of a (b, virtual head) by the last piece to arrive, on softmax
+// group 0: the m/l/o merge ("FlashDecoding 数学推导" §2.4.2) of the `target`
+// workspace partials of each of its Gv query rows.  With at most MERGE_PB
+// pieces the per-(piece, head) weights are formed once in `scr`, then every
+// thread sums 4 groups of 4 output elements at a time with all their loads
+// of a piece in flight; with more, each output element walks the pieces
+// itself.  Returns false if a barrier wait expired.
 template <int D, int MERGE_PB>
 __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &ctx, long long bhv, int slice,
                                                 int G, int Gv, long long qrow0, unsigned target, int gf,
-                                                long long off, int tid, unsigned char *scr, SoftBar &sb)
+                                                long long off, int tid, unsigned char *scr, WarpBar &wb)
 {
     const SplitParams &p = gp.s;
     const int n = (int)target;
@@ -156,17 +189,16 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
     float *sL = sM + G;                                              // [G]
     for (int i = tid; i < n; i += 128)
         ss[i] = vh_slot(gp, ctx, bhv, (unsigned)i, gf, off, slice);
-    if (!sb.sync(tid & 31))
+    if (!wb.sync(tid & 31))
         return false;
     if (tid < Gv) {
         float M = -INFINITY;
         for (int i = 0; i < n; ++i) {
             const long long r = ss[i] * G + tid;
             const float l = __ldcg(p.ws_ml + 2 * r + 1);
-            const float m = __ldcg(p.ws_ml + 2 * r);
             wt[i * G + tid] = l;
             if (l > 0.f)
-                M = fmaxf(M, m);
+                M = fmaxf(M, __ldcg(p.ws_ml + 2 * r));
         }
         float L = 0.f;
         for (int i = 0; i < n; ++i) {
@@ -179,22 +211,47 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
         sM[tid] = M;
         sL[tid] = L;
     }
-    if (!sb.sync(tid & 31))
+    if (!wb.sync(tid & 31))
         return false;
-    for (int idx = tid; idx < Gv * D; idx += 128) {
-        const int g = idx / D, dim = idx % D;
-        float O = 0.f;
-#pragma unroll 4
+    constexpr int GB = 4;   // groups of 4 elements per thread per pass
+    const int ngrp = Gv * D / 4;
+    for (int base = 0; base < ngrp; base += 128 * GB) {
+        float4 acc[GB];
+#pragma unroll
+        for (int e = 0; e < GB; ++e)
+            acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = 0; i < n; ++i) {
-            const float e = wt[i * G + g];
-            if (e > 0.f)
-                O = fmaf(e, __ldcg(p.ws_o + (ss[i] * G + g) * D + dim), O);
+            const long long s0 = ss[i] * G;
+#pragma unroll
+            for (int e = 0; e < GB; ++e) {
+                const int grp = base + e * 128 + tid;
+                if (grp < ngrp) {
+                    const int g = grp * 4 / D, dim = grp * 4 % D;
+                    const float w = wt[i * G + g];
+                    if (w > 0.f) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + (s0 + g) * D + dim));
+                        acc[e].x = fmaf(w, v.x, acc[e].x);
+                        acc[e].y = fmaf(w, v.y, acc[e].y);
+                        acc[e].z = fmaf(w, v.z, acc[e].z);
+                        acc[e].w = fmaf(w, v.w, acc[e].w);
+                    }
+                }
+            }
         }
-        const float L = sL[g];
-        const long long qrow = qrow0 + g;
-        store_out(p.out, qrow * D + dim, p.out_dtype, L > 0.f ? O / L : 0.f);
-        if (dim == 0 && p.lse)
-            p.lse[qrow] = L > 0.f ? (sM[g] + log2f(L)) * LN2_F : -INFINITY;
+#pragma unroll
+        for (int e = 0; e < GB; ++e) {
+            const int grp = base + e * 128 + tid;
+            if (grp < ngrp) {
+                const int g = grp * 4 / D, dim = grp * 4 % D;
+                const float L = sL[g];
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                const long long qrow = qrow0 + g;
+                store_out4(p.out, qrow * D + dim, p.out_dtype,
+                           make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv));
+                if (dim == 0 && p.lse)
+                    p.lse[qrow] = L > 0.f ? (sM[g] + log2f(L)) * LN2_F : -INFINITY;
+            }
+        }
     }
     return true;
 }
@@ -215,9 +272,9 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-aligned
     const uint32_t ring = smem_addr(smem);
     const uint32_t qbuf = ring + C::RING_BYTES;
-    const uint32_t pbuf = qbuf + C::Q_BYTES;
-    unsigned char *scratch = smem + C::RING_BYTES;   // Q and P buffers, reused by the merge
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::RING_BYTES + C::Q_BYTES + C::P_BYTES);
+    unsigned char *scratch = smem + C::RING_BYTES + C::Q_BYTES;   // the last arriver's merge
+    float *xch = reinterpret_cast<float *>(scratch + C::SCR_BYTES);   // [2][M][2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::SCR_BYTES + C::XCH_BYTES);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBAR);   // [0] TMEM base, [1] flag
     long long *cumH = reinterpret_cast<long long *>(misc + 4);
     int *lenS = reinterpret_cast<int *>(cumH + p.B + 1);
@@ -225,27 +282,31 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     auto FULL = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto EMPTY = [&](int s) { return bar0 + 8u * (uint32_t)(ST + s); };
     auto SFULL = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + b); };
-    auto SFREE = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + 2 + b); };
-    const uint32_t QFULL = bar0 + 8u * (2 * ST + 4);
-    const uint32_t PFULL = bar0 + 8u * (2 * ST + 5);
-    const uint32_t OFULL = bar0 + 8u * (2 * ST + 6);
-    const uint32_t FIN = bar0 + 8u * (2 * ST + 7);
-    const uint32_t SEGBAR = bar0 + 8u * (2 * ST + 8);
+    auto SFREE = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + 4 + b); };
+    auto PFULL = [&](int g) { return bar0 + 8u * (uint32_t)(2 * ST + 8 + g); };
+    auto OFULL = [&](int g) { return bar0 + 8u * (uint32_t)(2 * ST + 10 + g); };
+    const uint32_t QFULL = bar0 + 8u * (2 * ST + 12);
+    const uint32_t FIN = bar0 + 8u * (2 * ST + 13);
+    const uint32_t SEGBAR = bar0 + 8u * (2 * ST + 14);
+    const uint32_t WG0BAR = bar0 + 8u * (2 * ST + 15);
 
     if (tid == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(FULL(s), 1);    // the producer's arrival plus the copies' bytes
-            mbar_init(EMPTY(s), 1);   // the MMA warp's commit after P.V of the stage's chunk
+            mbar_init(EMPTY(s), 1);   // commit after P.V of the stage's chunk
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 4; ++b) {
             mbar_init(SFULL(b), 1);   // commit after S
-            mbar_init(SFREE(b), 4);   // the softmax warps have read S
+            mbar_init(SFREE(b), 4);   // the owning group's warps: P.V of the buffer's chunk is done
         }
-        mbar_init(QFULL, 4);          // the softmax warps have written Q
-        mbar_init(PFULL, 4);          // ... P (and zeroed V's rows past the chunk)
-        mbar_init(OFULL, 1);          // commit after P.V
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(PFULL(g), 4);   // the group's warps: P in TMEM, V's tail rows zeroed
+            mbar_init(OFULL(g), 1);   // commit after the group's P.V
+        }
+        mbar_init(QFULL, 4);          // group 0 has written Q
         mbar_init(FIN, 1);            // the MMA warp's last commit
-        mbar_init(SEGBAR, 4);         // the softmax warps at a segment end
+        mbar_init(SEGBAR, 8);         // both groups at a segment end
+        mbar_init(WG0BAR, 4);         // group 0 (arrival and merge)
         prefetch_tmap(&gp.tmk);
         prefetch_tmap(&gp.tmv);
     }
@@ -309,19 +370,19 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         if (lane == 0) {
             constexpr int BF = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
             constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, C::M, C::CT);   // Q K-major, K K-major
-            constexpr uint32_t ID_O = idesc_f16(BF, 0, 1, C::M, D);       // P K-major, V MN-major
-            long long i = 0;   // chunks of this CTA so far
-            int k = 0;         // non-empty segments so far
-            // S of chunk j (global index) into S buffer j % 2
+            constexpr uint32_t ID_O = idesc_f16(BF, 0, 1, C::M, D);       // P (TMEM) K-major, V MN-major
+            long long pw[2] = {0, 0};   // P.V handed by each softmax group so far
+            int k = 0;                  // non-empty segments so far
+            // S of chunk j into S/P buffer j % 4
             auto issue_s = [&](long long j) -> bool {
                 const int s = (int)(j % ST);
                 if (!mbar_wait_bounded_thread(FULL(s), (uint32_t)((j / ST) & 1)))
                     return false;
-                if (j >= 2 && !mbar_wait_bounded_thread(SFREE((int)(j & 1)), (uint32_t)(((j >> 1) - 1) & 1)))
+                if (j >= 4 && !mbar_wait_bounded_thread(SFREE((int)(j & 3)), (uint32_t)(((j >> 2) - 1) & 1)))
                     return false;
                 tc_fence_after();
                 const uint32_t kb = ring + (uint32_t)(s * C::STAGE_BYTES);
-                const uint32_t ds = tmem + (uint32_t)((j & 1) * C::CT);
+                const uint32_t ds = tmem + (uint32_t)((j & 3) * C::CT);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t col = (uint32_t)((ks & 3) * 32);   // 16 elements = 32 bytes per k-step
@@ -329,9 +390,10 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     const uint64_t b = smem_desc_sw128(kb + (uint32_t)((ks >> 2) * C::PLANE) + col, 16, 1024);
                     tc_mma_ss(ds, a, b, ID_S, ks > 0 ? 1u : 0u);
                 }
-                tc_commit(SFULL((int)(j & 1)));
+                tc_commit(SFULL((int)(j & 3)));
                 return true;
             };
+            long long j = 0;   // chunks of this CTA so far
             Seg cs;
             seg_first(p, ctx, cs);
 #pragma unroll 1
@@ -344,35 +406,38 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     }
                     ++k;
                     tc_fence_after();
-                    if (!issue_s(i)) {
+                    if (!issue_s(j)) {
                         dead = true;
                         break;
                     }
 #pragma unroll 1
-                    for (long long c = 0; c < n; ++c, ++i) {
-                        if (c + 1 < n && !issue_s(i + 1)) {
+                    for (long long c = 0; c < n; ++c, ++j) {
+                        if (c + 1 < n && !issue_s(j + 1)) {
                             dead = true;
                             break;
                         }
-                        if (!mbar_wait_bounded_thread(PFULL, (uint32_t)(i & 1))) {
+                        const int g = (int)(j & 1);
+                        if (!mbar_wait_bounded_thread(PFULL(g), (uint32_t)(pw[g] & 1))) {
                             dead = true;
                             break;
                         }
+                        ++pw[g];
                         tc_fence_after();
-                        const uint32_t vb = ring + (uint32_t)((i % ST) * C::STAGE_BYTES + C::CHUNK_BYTES);
+                        const uint32_t vb = ring + (uint32_t)((j % ST) * C::STAGE_BYTES + C::CHUNK_BYTES);
+                        const uint32_t pa = tmem + (uint32_t)((j & 3) * C::CT);
 #pragma unroll
                         for (int ks = 0; ks < C::CT / 16; ++ks) {
 #pragma unroll
                             for (int hl = 0; hl < 2; ++hl) {
-                                const uint64_t a =
-                                    smem_desc_sw128(pbuf + (uint32_t)(hl * C::PHALF + ks * 32), 16, 1024);
+                                // P_hi in columns 0-31 of the buffer, P_lo in 32-63; 8 columns per k-step
                                 const uint64_t b =
                                     smem_desc_sw128(vb + (uint32_t)(ks * 2048), (uint32_t)C::PLANE, 1024);
-                                tc_mma_ss(tmem + C::TMEM_O, a, b, ID_O, (c > 0 || ks > 0 || hl > 0) ? 1u : 0u);
+                                tc_mma_ts(tmem + (uint32_t)(C::TMEM_O + g * D), pa + (uint32_t)(hl * 32 + ks * 8), b,
+                                          ID_O, (c >= 2 || ks > 0 || hl > 0) ? 1u : 0u);
                             }
                         }
-                        tc_commit(OFULL);
-                        tc_commit(EMPTY((int)(i % ST)));
+                        tc_commit(OFULL(g));
+                        tc_commit(EMPTY((int)(j % ST)));
                     }
                 }
                 seg_next(p, ctx, cs);
@@ -384,11 +449,15 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax
-        const int row = tid;   // query head within the slice = TMEM lane
-        const uint32_t tl = tmem + ((uint32_t)(w * 32) << 16);
-        SoftBar sb{SEGBAR, 0u};
-        long long i = 0;
+        // ------------------------------------------------------------ softmax groups
+        const int wg = w >> 2;             // softmax group
+        const int row = tid & 127;         // query head within the slice = TMEM lane
+        const uint32_t tl = tmem + ((uint32_t)((w & 3) * 32) << 16);
+        const uint32_t ocol = (uint32_t)(C::TMEM_O + wg * D);
+        WarpBar sb{SEGBAR, 0u}, wb{WG0BAR, 0u};
+        long long nw = 0;   // chunks this group has handed to P.V
+        long long j0 = 0;   // the CTA's chunk index of the segment's first chunk
+        int k = 0;          // segments so far
         Seg cs;
         seg_first(p, ctx, cs);
 #pragma unroll 1
@@ -400,215 +469,270 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             const long long qrow0 = vh_qrow0(gp, cs.b, vh);
             const bool live = row < gv;
             float m_ref = -INFINITY, l = 0.f;
-            if (n > 0) {
-                // this head's q row into the Q buffer (K-major, 128-byte swizzle)
-                {
-                    const uint4 *qs = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
-                                                                      (qrow0 + row) * D);
+            if (n > 0 && wg == 0) {
+                // the query rows into the Q buffer (K-major, 128-byte swizzle)
+                const uint4 *qs = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
+                                                                  (qrow0 + row) * D);
 #pragma unroll
-                    for (int pl = 0; pl < C::LINES; ++pl)
+                for (int pl = 0; pl < C::LINES; ++pl)
 #pragma unroll
-                        for (int c16 = 0; c16 < 8; ++c16) {
-                            const uint4 v = live ? __ldg(qs + pl * 8 + c16) : make_uint4(0, 0, 0, 0);
-                            const uint32_t a = qbuf + (uint32_t)(pl * C::QPLANE + row * 128 +
-                                                                 ((c16 ^ (row & 7)) << 4));
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x),
-                                         "r"(v.y), "r"(v.z), "r"(v.w)
-                                         : "memory");
-                        }
-                }
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const uint4 v = live ? __ldg(qs + pl * 8 + c16) : make_uint4(0, 0, 0, 0);
+                        const uint32_t a =
+                            qbuf + (uint32_t)(pl * C::QPLANE + row * 128 + ((c16 ^ (row & 7)) << 4));
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                                     "r"(v.z), "r"(v.w)
+                                     : "memory");
+                    }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(QFULL);
+            }
+            bool had = false;
+            long long jprev = 0;
 #pragma unroll 1
-                for (long long c = 0; c < n; ++c, ++i) {
-                    if (!mbar_wait_bounded(SFULL((int)(i & 1)), (uint32_t)((i >> 1) & 1))) {
-                        dead = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    float s0[32], s1[32];   // the head's scores of the chunk's 64 tokens
-                    tmem_ld32(tl + (uint32_t)((i & 1) * C::CT), s0);
-                    tmem_ld32(tl + (uint32_t)((i & 1) * C::CT + 32), s1);
-                    tmem_wait_ld();
-                    auto S = [&](int j) -> float & { return j < 32 ? s0[j] : s1[j - 32]; };
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(SFREE((int)(i & 1)));
-                    int t, ntok;
-                    chunk_coords<C::CT>(cs, c, t, ntok);
-                    float mc = -INFINITY;
-#pragma unroll
-                    for (int j = 0; j < C::CT; ++j) {
-                        S(j) = j < ntok ? S(j) * p.scale_log2 : -INFINITY;
-                        mc = fmaxf(mc, S(j));
-                    }
-                    // P.V of the previous chunk is done: its P buffer is free and O is final
-                    if (c > 0) {
-                        if (!mbar_wait_bounded(OFULL, (uint32_t)((i - 1) & 1))) {
-                            dead = true;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    // lazy rescale: the reference max moves only when the
-                    // chunk's max exceeds it by more than TAU
-                    const bool grow = mc > m_ref + C::TAU;
-                    float a = 1.f;
-                    if (grow) {
-                        a = ex2(m_ref - mc);   // 0 on the first chunk
-                        l *= a;
-                        m_ref = mc;
-                    }
-                    // the O rows in TMEM: the tcgen05 loads and stores are
-                    // warp-wide, so the whole warp runs them when any of its
-                    // heads grew (a = 1 for the others)
-                    if (c > 0 && __any_sync(FULL_MASK, grow)) {
-#pragma unroll 1
-                        for (int q4 = 0; q4 < D / 32; ++q4) {
-                            float o[32];
-                            tmem_ld32(tl + (uint32_t)(C::TMEM_O + 32 * q4), o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                o[e] *= a;
-                            tmem_st32(tl + (uint32_t)(C::TMEM_O + 32 * q4), o);
-                        }
-                        tmem_wait_st();
-                    }
-                    // P = 2^(s - m_ref), high part and remainder, into the P buffer
-                    float ls = 0.f;
-#pragma unroll
-                    for (int c16 = 0; c16 < 8; ++c16) {
-                        uint32_t hi[4], lo[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int j = c16 * 8 + 2 * e;
-                            const float p0 = live ? ex2(S(j) - m_ref) : 0.f;
-                            const float p1 = live ? ex2(S(j + 1) - m_ref) : 0.f;
-                            ls += p0 + p1;
-                            hi[e] = Mma<T>::pack(p0, p1);
-                            const float2 u = Mma<T>::unpack(hi[e]);
-                            lo[e] = Mma<T>::pack(p0 - u.x, p1 - u.y);
-                        }
-                        const uint32_t off = (uint32_t)(row * 128 + ((c16 ^ (row & 7)) << 4));
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pbuf + off), "r"(hi[0]),
-                                     "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
-                                     : "memory");
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(pbuf + C::PHALF + off),
-                                     "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
-                                     : "memory");
-                    }
-                    l += ls;
-                    // V's rows past the chunk's tokens may hold padding (NaN * 0 is NaN)
-                    if (ntok < C::CT) {
-                        const uint32_t vb = ring + (uint32_t)((i % ST) * C::STAGE_BYTES + C::CHUNK_BYTES);
-                        const int pieces = (C::CT - ntok) * C::LINES * 8;
-                        for (int x = tid; x < pieces; x += 128) {
-                            const int r = ntok + x / (C::LINES * 8);
-                            const int rem = x % (C::LINES * 8);
-                            const uint32_t a = vb + (uint32_t)((rem >> 3) * C::PLANE + r * 128 + (rem & 7) * 16);
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(PFULL);
-                }
-                if (dead)
-                    break;
-                if (!mbar_wait_bounded(OFULL, (uint32_t)((i - 1) & 1))) {
+            for (long long c = (long long)(wg ^ (int)(j0 & 1)); c < n; c += 2) {
+                const long long j = j0 + c;
+                const int b = (int)(j & 3);
+                if (!mbar_wait_bounded(SFULL(b), (uint32_t)((j >> 2) & 1))) {
                     dead = true;
                     break;
                 }
                 tc_fence_after();
-            }
-
-            // ---- segment end: this head's (o, m, l) ----
-            const int len = (p.decomp == DECOMP_BALANCED) ? lenS[cs.b] : clamp_len(p, cs.b);
-            bool complete;
-            long long slot;
-            if (p.decomp == DECOMP_SPLITS) {
-                complete = (p.P == 1);
-                slot = bhv * p.P + cs.p;
-            } else {
-                complete = (cs.t0 == 0 && cs.t1 == len);
-                slot = 2LL * blockIdx.x + (cs.k == 0 ? 0 : 1);
-            }
-            const bool nonempty = l > 0.f;
-            const float inv = nonempty ? 1.f / l : 0.f;
-            const long long qrow = qrow0 + row;
-            const long long r = slot * G + row;
-#pragma unroll 1
-            for (int q4 = 0; q4 < D / 32; ++q4) {
-                float o[32];
-                if (n > 0) {
-                    tmem_ld32(tl + (uint32_t)(C::TMEM_O + 32 * q4), o);
-                    tmem_wait_ld();
-                }
-                if (live) {
+                // the chunk's max over its valid tokens (base-2 scores), 32
+                // columns at a time; the scores are read again for P below
+                int t, ntok;
+                chunk_coords<C::CT>(cs, c, t, ntok);
+                const float sc = p.scale_log2;
+                float mc = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float x = (n > 0 && nonempty) ? o[e] * inv : 0.f;
-                        if (complete)
-                            store_out(p.out, qrow * D + 32 * q4 + e, p.out_dtype, x);
-                        else
-                            p.ws_o[r * D + 32 * q4 + e] = x;
-                    }
+                for (int h = 0; h < 2; ++h) {
+                    float sv[32];
+                    tmem_ld32(tl + (uint32_t)(b * C::CT + 32 * h), sv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * h + i < ntok)
+                            mc = fmaxf(mc, sv[i] * sc);
                 }
-            }
-            tc_fence_before();
-            if (live) {
-                if (complete) {
-                    if (p.lse)
-                        p.lse[qrow] = nonempty ? (m_ref + log2f(l)) * LN2_F : -INFINITY;
-                } else {
-                    p.ws_ml[2 * r] = nonempty ? m_ref : -INFINITY;
-                    p.ws_ml[2 * r + 1] = l;
-                }
-            }
-            if (!complete) {
-                unsigned target;
-                int gf = 0;
-                long long off = 0;
-                if (p.decomp == DECOMP_SPLITS) {
-                    target = (unsigned)p.P;
-                } else {
-                    off = ctx.cumH[cs.b] + (long long)cs.h * len;
-                    gf = bal_owner(off, ctx.T, ctx.Geff);
-                    const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
-                    target = (unsigned)(gl - gf + 1);
-                }
-                // the barrier orders every thread's partial before thread 0's
-                // fence and arrival
-                if (!sb.sync(lane)) {
-                    dead = true;
-                    break;
-                }
-                if (tid == 0) {
-                    __threadfence();
-                    const unsigned old = atomicInc(p.ws_cnt + bhv, target - 1);
-                    misc[1] = (old == target - 1) ? 1u : 0u;
-                }
-                if (!sb.sync(lane)) {
-                    dead = true;
-                    break;
-                }
-                if (misc[1]) {
-                    __threadfence();
-                    if (!tc_merge_pieces<D, C::MERGE_PB>(gp, ctx, bhv, slice, G, gv, qrow0, target, gf, off,
-                                                         tid, scratch, sb)) {
+                // the group's previous chunk: its P.V is done, so O is final
+                // and its S/P buffer free for the chunk four ahead
+                if (had) {
+                    if (!mbar_wait_bounded(OFULL(wg), (uint32_t)((nw - 1) & 1))) {
                         dead = true;
                         break;
                     }
+                    tc_fence_after();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(SFREE((int)(jprev & 3)));
                 }
-                if (!sb.sync(lane)) {   // the flag and the scratch are reused
+                // lazy rescale: the reference max moves only when the
+                // chunk's max exceeds it by more than TAU
+                const bool grow = mc > m_ref + C::TAU;
+                float a = 1.f;
+                if (grow) {
+                    a = ex2(m_ref - mc);   // 0 on the group's first chunk
+                    l *= a;
+                    m_ref = mc;
+                }
+                // the O rows in TMEM: the tcgen05 loads and stores are
+                // warp-wide, so the whole warp runs them when any of its
+                // heads grew (a = 1 for the others)
+                if (had && __any_sync(FULL_MASK, grow)) {
+#pragma unroll 1
+                    for (int q = 0; q < D / 16; ++q) {
+                        float o[16];
+                        tmem_ld16(tl + ocol + (uint32_t)(16 * q), o);
+                        tmem_wait_ld();
+                        uint32_t u[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            u[e] = __float_as_uint(o[e] * a);
+                        tmem_st16u(tl + ocol + (uint32_t)(16 * q), u);
+                    }
+                }
+                // P = 2^(s - m_ref): the 16-bit high part and its remainder,
+                // packed pairs, into the chunk's S columns (0-31 and 32-63),
+                // 32 tokens at a time (P of tokens 32h.. overwrites columns
+                // 16h.. and 32 + 16h.., which hold scores already read)
+                const uint64_t sc2 = pack2(sc, sc), nm2 = pack2(-m_ref, -m_ref), one2 = pack2(1.f, 1.f);
+                uint64_t ls2 = pack2(0.f, 0.f);
+                float sv1[32];   // scores of tokens 32..63, read before their columns are overwritten
+                tmem_ld32(tl + (uint32_t)(b * C::CT + 32), sv1);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float sv[32];
+                    if (h == 0) {
+                        tmem_ld32(tl + (uint32_t)(b * C::CT), sv);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            sv[i] = sv1[i];
+                    }
+                    uint32_t ph[16], plo[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int tk = 32 * h + 2 * i;
+                        float x0, x1;
+                        unpack2(fma2(pack2(sv[2 * i], sv[2 * i + 1]), sc2, nm2), x0, x1);
+                        const float p0 = (live && tk < ntok) ? ex2(x0) : 0.f;
+                        const float p1 = (live && tk + 1 < ntok) ? ex2(x1) : 0.f;
+                        ls2 = fma2(pack2(p0, p1), one2, ls2);
+                        ph[i] = Mma<T>::pack(p0, p1);
+                        const float2 u = Mma<T>::unpack(ph[i]);
+                        plo[i] = Mma<T>::pack(p0 - u.x, p1 - u.y);
+                    }
+                    tmem_st16u(tl + (uint32_t)(b * C::CT + 16 * h), ph);
+                    tmem_st16u(tl + (uint32_t)(b * C::CT + 32 + 16 * h), plo);
+                }
+                float lsa, lsb;
+                unpack2(ls2, lsa, lsb);
+                l += lsa + lsb;
+                // V's rows past the chunk's tokens may hold padding (NaN * 0 is NaN)
+                if (ntok < C::CT) {
+                    const uint32_t vb = ring + (uint32_t)((j % ST) * C::STAGE_BYTES + C::CHUNK_BYTES);
+                    const int pieces = (C::CT - ntok) * C::LINES * 8;
+                    for (int x = row; x < pieces; x += 128) {
+                        const int r = ntok + x / (C::LINES * 8);
+                        const int rem = x % (C::LINES * 8);
+                        const uint32_t va = vb + (uint32_t)((rem >> 3) * C::PLANE + r * 128 + (rem & 7) * 16);
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(va), "r"(0u) : "memory");
+                    }
+                    fence_proxy_async_smem();
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(PFULL(wg));
+                ++nw;
+                had = true;
+                jprev = j;
+            }
+            if (dead)
+                break;
+            if (had) {
+                if (!mbar_wait_bounded(OFULL(wg), (uint32_t)((nw - 1) & 1))) {
                     dead = true;
                     break;
+                }
+                tc_fence_after();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(SFREE((int)(jprev & 3)));
+            }
+            j0 += n;
+
+            // ---- segment end: group 1 hands over its (m_ref, l), group 0 merges ----
+            float *xk = xch + (k & 1) * C::M * 2;
+            if (wg == 1) {
+                xk[2 * row] = had ? m_ref : -INFINITY;
+                xk[2 * row + 1] = had ? l : 0.f;
+            }
+            ++k;
+            if (!sb.sync(lane)) {
+                dead = true;
+                break;
+            }
+            if (wg == 0) {
+                const float m1 = xk[2 * row], l1 = xk[2 * row + 1];
+                const float m0 = had ? m_ref : -INFINITY, l0 = had ? l : 0.f;
+                const float M = fmaxf(l0 > 0.f ? m0 : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
+                const float a0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
+                const float a1 = l1 > 0.f ? ex2(m1 - M) : 0.f;
+                const float L = a0 * l0 + a1 * l1;
+                const bool nonempty = L > 0.f;
+                const float f0 = nonempty ? a0 / L : 0.f, f1 = nonempty ? a1 / L : 0.f;
+                const bool need0 = __any_sync(FULL_MASK, l0 > 0.f), need1 = __any_sync(FULL_MASK, l1 > 0.f);
+                const int len = (p.decomp == DECOMP_BALANCED) ? lenS[cs.b] : clamp_len(p, cs.b);
+                bool complete;
+                long long slot;
+                if (p.decomp == DECOMP_SPLITS) {
+                    complete = (p.P == 1);
+                    slot = bhv * p.P + cs.p;
+                } else {
+                    complete = (cs.t0 == 0 && cs.t1 == len);
+                    slot = 2LL * blockIdx.x + (cs.k == 0 ? 0 : 1);
+                }
+                const long long qrow = qrow0 + row;
+                const long long r = slot * G + row;
+#pragma unroll 1
+                for (int q = 0; q < D / 16; ++q) {
+                    float o0[16], o1[16];
+                    if (need0)
+                        tmem_ld16(tl + (uint32_t)(C::TMEM_O + 16 * q), o0);
+                    if (need1)
+                        tmem_ld16(tl + (uint32_t)(C::TMEM_O + D + 16 * q), o1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        o0[e] = (need0 ? f0 * o0[e] : 0.f) + (need1 ? f1 * o1[e] : 0.f);
+                    if (live) {
+                        if (complete) {
+                            store_out8(p.out, qrow * D + 16 * q, p.out_dtype, o0);
+                            store_out8(p.out, qrow * D + 16 * q + 8, p.out_dtype, o0 + 8);
+                        } else {
+                            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + r * D + 16 * q);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                dst[e] = make_float4(o0[4 * e], o0[4 * e + 1], o0[4 * e + 2], o0[4 * e + 3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                if (live) {
+                    if (complete) {
+                        if (p.lse)
+                            p.lse[qrow] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+                    } else {
+                        p.ws_ml[2 * r] = nonempty ? M : -INFINITY;
+                        p.ws_ml[2 * r + 1] = L;
+                    }
+                }
+                if (!complete) {
+                    unsigned target;
+                    int gf = 0;
+                    long long off = 0;
+                    if (p.decomp == DECOMP_SPLITS) {
+                        target = (unsigned)p.P;
+                    } else {
+                        off = ctx.cumH[cs.b] + (long long)cs.h * len;
+                        gf = bal_owner(off, ctx.T, ctx.Geff);
+                        const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
+                        target = (unsigned)(gl - gf + 1);
+                    }
+                    // the barrier orders every thread's partial before thread 0's
+                    // fence and arrival
+                    if (!wb.sync(lane)) {
+                        dead = true;
+                        break;
+                    }
+                    if (tid == 0) {
+                        __threadfence();
+                        const unsigned old = atomicInc(p.ws_cnt + bhv, target - 1);
+                        misc[1] = (old == target - 1) ? 1u : 0u;
+                    }
+                    if (!wb.sync(lane)) {
+                        dead = true;
+                        break;
+                    }
+                    if (misc[1]) {
+                        __threadfence();
+                        if (!tc_merge_pieces<D, C::MERGE_PB>(gp, ctx, bhv, slice, G, gv, qrow0, target, gf, off,
+                                                             tid, scratch, wb)) {
+                            dead = true;
+                            break;
+                        }
+                    }
+                    if (!wb.sync(lane)) {   // the flag and the scratch are reused
+                        dead = true;
+                        break;
+                    }
                 }
             }
             seg_next(p, ctx, cs);

@@ -82,6 +82,10 @@ WORKLOADS["decode_gqa_b8_hq16_hkv8_n32k_d256_bf16"] = Workload(
 WORKLOADS["decode_mqa_b32_hq64_hkv1_n32k_d128_bf16"] = Workload(
     "decode_mqa_b32_hq64_hkv1_n32k_d128_bf16", 32, 64, 32768, 128, "bf16", "bf16", 0, Hkv=1)
 
+# a 256 MiB multi-query case for detailed profiles of the tcgen05 kernel
+WORKLOADS["decode_mqa_b16_hq64_hkv1_n32k_d128_bf16"] = Workload(
+    "decode_mqa_b16_hq64_hkv1_n32k_d128_bf16", 16, 64, 32768, 128, "bf16", "bf16", 0, Hkv=1)
+
 # the workload the benchmark times by default: uniform 32K-token sequences
 BENCH_DEFAULT = "decode_b8_h32_n32k_d128_bf16"
 
