@@ -143,97 +143,90 @@ __device__ __forceinline__ void store_out4(void *out, long long idx, int out_dty
     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + idx) = make_uint2(a, b);
 }
 
-// Stage 2 of a (b, virtual head) by the last piece to arrive, on softmax
-// group 0: the m/l/o merge ("FlashDecoding 数学推导" §2.4.2) of the `target`
-// workspace partials of each of its Gv query rows.  With at most MERGE_PB
-// pieces the per-(piece, head) weights are formed once in `scr`, then every
-// thread sums 4 groups of 4 output elements at a time with all their loads
-// of a piece in flight; with more, each output element walks the pieces
-// itself.  Returns false if a barrier wait expired.
-template <int D, int MERGE_PB>
-__device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &ctx, long long bhv, int slice,
-                                                int G, int Gv, long long qrow0, unsigned target, int gf,
-                                                long long off, int tid, unsigned char *scr, WarpBar &wb)
+// One batch of the last arriver's merge, on softmax group 0: the m/l/o
+// merge ("FlashDecoding 数学推导" §2.4.2) of the n <= MERGE_PB workspace
+// partials whose slots are in ss[0..n-1], for each of the Gv query rows.
+// The per-(piece, head) weights are formed once in `wt` (shared memory);
+// then every output element sums its pieces, with 16 loads in flight per
+// thread (the merge sits on the CTA's critical path: the next segment waits
+// for it).  The result goes to out/lse, or, when `into` >= 0, back into the
+// workspace slot `into` as a normalised partial (o, m, l) that a later batch
+// merges.  Returns false if a barrier wait expired.
+template <int D>
+__device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int Gv, long long qrow0, const long long *ss,
+                                               int n, long long into, float *wt, float *sM, float *sL, int tid,
+                                               WarpBar &wb)
 {
-    const SplitParams &p = gp.s;
-    const int n = (int)target;
-    if (n > MERGE_PB) {
-        for (int idx = tid; idx < Gv * D; idx += 128) {
-            const int g = idx / D, dim = idx % D;
-            float M = -INFINITY;
-            for (int i = 0; i < n; ++i) {
-                const long long r = vh_slot(gp, ctx, bhv, (unsigned)i, gf, off, slice) * G + g;
-                if (__ldcg(p.ws_ml + 2 * r + 1) > 0.f)
-                    M = fmaxf(M, __ldcg(p.ws_ml + 2 * r));
-            }
-            float L = 0.f, O = 0.f;
-            for (int i = 0; i < n; ++i) {
-                const long long r = vh_slot(gp, ctx, bhv, (unsigned)i, gf, off, slice) * G + g;
-                const float l = __ldcg(p.ws_ml + 2 * r + 1);
-                if (l > 0.f) {
-                    const float e = ex2(__ldcg(p.ws_ml + 2 * r) - M) * l;
-                    L += e;
-                    O = fmaf(e, __ldcg(p.ws_o + r * D + dim), O);
-                }
-            }
-            const long long qrow = qrow0 + g;
-            store_out(p.out, qrow * D + dim, p.out_dtype, L > 0.f ? O / L : 0.f);
-            if (dim == 0 && p.lse)
-                p.lse[qrow] = L > 0.f ? (M + log2f(L)) * LN2_F : -INFINITY;
-        }
-        return true;
-    }
-    long long *ss = reinterpret_cast<long long *>(scr);            // [n] slots
-    float *wt = reinterpret_cast<float *>(scr + MERGE_PB * 8);      // [n][G] weights
-    float *sM = wt + MERGE_PB * G;                                   // [G]
-    float *sL = sM + G;                                              // [G]
-    for (int i = tid; i < n; i += 128)
-        ss[i] = vh_slot(gp, ctx, bhv, (unsigned)i, gf, off, slice);
-    if (!wb.sync(tid & 31))
-        return false;
     if (tid < Gv) {
+        // the head's max over the pieces, then its weights; 8 loads in flight
         float M = -INFINITY;
-        for (int i = 0; i < n; ++i) {
-            const long long r = ss[i] * G + tid;
-            const float l = __ldcg(p.ws_ml + 2 * r + 1);
-            wt[i * G + tid] = l;
-            if (l > 0.f)
-                M = fmaxf(M, __ldcg(p.ws_ml + 2 * r));
+        for (int i0 = 0; i0 < n; i0 += 8) {
+            float mv[8], lv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const long long r = ss[min(i0 + u, n - 1)] * G + tid;
+                mv[u] = __ldcg(p.ws_ml + 2 * r);
+                lv[u] = __ldcg(p.ws_ml + 2 * r + 1);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u < n && lv[u] > 0.f)
+                    M = fmaxf(M, mv[u]);
         }
         float L = 0.f;
-        for (int i = 0; i < n; ++i) {
-            const long long r = ss[i] * G + tid;
-            const float l = wt[i * G + tid];
-            const float e = l > 0.f ? ex2(__ldcg(p.ws_ml + 2 * r) - M) * l : 0.f;
-            wt[i * G + tid] = e;
-            L += e;
+        for (int i0 = 0; i0 < n; i0 += 8) {
+            float mv[8], lv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const long long r = ss[min(i0 + u, n - 1)] * G + tid;
+                mv[u] = __ldcg(p.ws_ml + 2 * r);
+                lv[u] = __ldcg(p.ws_ml + 2 * r + 1);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (i0 + u < n) {
+                    const float e = lv[u] > 0.f ? ex2(mv[u] - M) * lv[u] : 0.f;
+                    wt[(i0 + u) * G + tid] = e;
+                    L += e;
+                }
+            }
         }
         sM[tid] = M;
         sL[tid] = L;
     }
     if (!wb.sync(tid & 31))
         return false;
-    constexpr int GB = 4;   // groups of 4 elements per thread per pass
+    constexpr int GB = 2, PB = 8;   // groups of 4 elements, pieces per round
     const int ngrp = Gv * D / 4;
     for (int base = 0; base < ngrp; base += 128 * GB) {
         float4 acc[GB];
+        int gg[GB], dd[GB];
 #pragma unroll
-        for (int e = 0; e < GB; ++e)
+        for (int e = 0; e < GB; ++e) {
             acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < n; ++i) {
-            const long long s0 = ss[i] * G;
+            const int grp = min(base + e * 128 + tid, ngrp - 1);
+            gg[e] = grp * 4 / D;
+            dd[e] = grp * 4 % D;
+        }
+        for (int i0 = 0; i0 < n; i0 += PB) {
+            float4 v[GB][PB];
 #pragma unroll
-            for (int e = 0; e < GB; ++e) {
-                const int grp = base + e * 128 + tid;
-                if (grp < ngrp) {
-                    const int g = grp * 4 / D, dim = grp * 4 % D;
-                    const float w = wt[i * G + g];
+            for (int u = 0; u < PB; ++u) {
+                const long long s0 = ss[min(i0 + u, n - 1)] * G;
+#pragma unroll
+                for (int e = 0; e < GB; ++e)
+                    v[e][u] = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + (s0 + gg[e]) * D + dd[e]));
+            }
+#pragma unroll
+            for (int u = 0; u < PB; ++u) {
+#pragma unroll
+                for (int e = 0; e < GB; ++e) {
+                    const float w = (i0 + u < n) ? wt[(i0 + u) * G + gg[e]] : 0.f;
                     if (w > 0.f) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + (s0 + g) * D + dim));
-                        acc[e].x = fmaf(w, v.x, acc[e].x);
-                        acc[e].y = fmaf(w, v.y, acc[e].y);
-                        acc[e].z = fmaf(w, v.z, acc[e].z);
-                        acc[e].w = fmaf(w, v.w, acc[e].w);
+                        acc[e].x = fmaf(w, v[e][u].x, acc[e].x);
+                        acc[e].y = fmaf(w, v[e][u].y, acc[e].y);
+                        acc[e].z = fmaf(w, v[e][u].z, acc[e].z);
+                        acc[e].w = fmaf(w, v[e][u].w, acc[e].w);
                     }
                 }
             }
@@ -242,16 +235,159 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
         for (int e = 0; e < GB; ++e) {
             const int grp = base + e * 128 + tid;
             if (grp < ngrp) {
-                const int g = grp * 4 / D, dim = grp * 4 % D;
+                const int g = gg[e], dim = dd[e];
                 const float L = sL[g];
                 const float inv = L > 0.f ? 1.f / L : 0.f;
-                const long long qrow = qrow0 + g;
-                store_out4(p.out, qrow * D + dim, p.out_dtype,
-                           make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv));
-                if (dim == 0 && p.lse)
-                    p.lse[qrow] = L > 0.f ? (sM[g] + log2f(L)) * LN2_F : -INFINITY;
+                const float4 o = make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv);
+                if (into >= 0) {
+                    // this thread alone reads and writes these four elements
+                    *reinterpret_cast<float4 *>(p.ws_o + (into * G + g) * D + dim) = o;
+                } else {
+                    const long long qrow = qrow0 + g;
+                    store_out4(p.out, qrow * D + dim, p.out_dtype, o);
+                    if (dim == 0 && p.lse)
+                        p.lse[qrow] = L > 0.f ? (sM[g] + log2f(L)) * LN2_F : -INFINITY;
+                }
             }
         }
+    }
+    if (into >= 0 && tid < Gv) {   // every read of (m, l) was before the barrier above
+        const long long r = into * G + tid;
+        p.ws_ml[2 * r] = sL[tid] > 0.f ? sM[tid] : -INFINITY;
+        p.ws_ml[2 * r + 1] = sL[tid];
+    }
+    return wb.sync(tid & 31);
+}
+
+// Stage 2 of a (b, virtual head) by the last piece to arrive, on softmax
+// group 0: the merge of its `target` workspace partials, in batches of at
+// most MERGE_PB pieces; each batch but the last leaves its result in its
+// last piece's slot, which starts the next batch.  Returns false if a
+// barrier wait expired.
+template <int D, int MERGE_PB>
+__device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &ctx, long long bhv, int slice,
+                                                int G, int Gv, long long qrow0, unsigned target, int gf,
+                                                long long off, int tid, unsigned char *scr, WarpBar &wb)
+{
+    const SplitParams &p = gp.s;
+    long long *ss = reinterpret_cast<long long *>(scr);            // [MERGE_PB] slots
+    float *wt = reinterpret_cast<float *>(scr + MERGE_PB * 8);      // [MERGE_PB][G] weights
+    float *sM = wt + MERGE_PB * G;                                   // [G]
+    float *sL = sM + G;                                              // [G]
+    const int n = (int)target;
+    int first = 0;
+    for (;;) {
+        const int cnt = min(n - first, MERGE_PB);
+        for (int i = tid; i < cnt; i += 128)
+            ss[i] = vh_slot(gp, ctx, bhv, (unsigned)(first + i), gf, off, slice);
+        if (!wb.sync(tid & 31))
+            return false;
+        const bool last = first + cnt == n;
+        if (!tc_merge_batch<D>(p, G, Gv, qrow0, ss, cnt, last ? -1 : ss[cnt - 1], wt, sM, sL, tid, wb))
+            return false;
+        if (last)
+            return true;
+        first += cnt - 1;   // the batch's result, in its last slot, opens the next batch
+    }
+}
+
+// Segment end on softmax group 0 (out of line, so that its registers do not
+// crowd the chunk loop): merges the two groups' (m_ref, l, O) per head
+// ("FlashDecoding 数学推导" §2.4.2), then writes out/lse for a whole (b, h),
+// or a workspace partial and, for the last piece to arrive, runs the merge
+// of the pieces.  Returns false if a barrier wait expired.
+template <typename C, int D>
+__device__ __noinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int G, int gv,
+                                            long long qrow0, long long bhv, bool had, float m_ref, float l, float m1,
+                                            float l1, int row, int lane, int tid, uint32_t tl, uint32_t *misc,
+                                            unsigned char *scratch, WarpBar &wb)
+{
+    const SplitParams &p = gp.s;
+    const bool live = row < gv;
+    const float m0 = had ? m_ref : -INFINITY, l0 = had ? l : 0.f;
+    const float M = fmaxf(l0 > 0.f ? m0 : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
+    const float a0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
+    const float a1 = l1 > 0.f ? ex2(m1 - M) : 0.f;
+    const float L = a0 * l0 + a1 * l1;
+    const bool nonempty = L > 0.f;
+    const float f0 = nonempty ? a0 / L : 0.f, f1 = nonempty ? a1 / L : 0.f;
+    const bool need0 = __any_sync(FULL_MASK, l0 > 0.f), need1 = __any_sync(FULL_MASK, l1 > 0.f);
+    const int len = (p.decomp == DECOMP_BALANCED) ? ctx.lenS[cs.b] : clamp_len(p, cs.b);
+    bool complete;
+    long long slot;
+    if (p.decomp == DECOMP_SPLITS) {
+        complete = (p.P == 1);
+        slot = bhv * p.P + cs.p;
+    } else {
+        complete = (cs.t0 == 0 && cs.t1 == len);
+        slot = 2LL * blockIdx.x + (cs.k == 0 ? 0 : 1);
+    }
+    const long long qrow = qrow0 + row;
+    const long long r = slot * G + row;
+#pragma unroll 1
+    for (int q = 0; q < D / 16; ++q) {
+        float o0[16], o1[16];
+        if (need0)
+            tmem_ld16(tl + (uint32_t)(C::TMEM_O + 16 * q), o0);
+        if (need1)
+            tmem_ld16(tl + (uint32_t)(C::TMEM_O + D + 16 * q), o1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            o0[e] = (need0 ? f0 * o0[e] : 0.f) + (need1 ? f1 * o1[e] : 0.f);
+        if (live) {
+            if (complete) {
+                store_out8(p.out, qrow * D + 16 * q, p.out_dtype, o0);
+                store_out8(p.out, qrow * D + 16 * q + 8, p.out_dtype, o0 + 8);
+            } else {
+                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + r * D + 16 * q);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(o0[4 * e], o0[4 * e + 1], o0[4 * e + 2], o0[4 * e + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    if (live) {
+        if (complete) {
+            if (p.lse)
+                p.lse[qrow] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+        } else {
+            p.ws_ml[2 * r] = nonempty ? M : -INFINITY;
+            p.ws_ml[2 * r + 1] = L;
+        }
+    }
+    if (!complete) {
+        unsigned target;
+        int gf = 0;
+        long long off = 0;
+        if (p.decomp == DECOMP_SPLITS) {
+            target = (unsigned)p.P;
+        } else {
+            off = ctx.cumH[cs.b] + (long long)cs.h * len;
+            gf = bal_owner(off, ctx.T, ctx.Geff);
+            const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
+            target = (unsigned)(gl - gf + 1);
+        }
+        // the barrier orders every thread's partial before thread 0's
+        // fence and arrival
+        if (!wb.sync(lane))
+            return false;
+        if (tid == 0) {
+            __threadfence();
+            const unsigned old = atomicInc(p.ws_cnt + bhv, target - 1);
+            misc[1] = (old == target - 1) ? 1u : 0u;
+        }
+        if (!wb.sync(lane))
+            return false;
+        if (misc[1]) {
+            __threadfence();
+            if (!tc_merge_pieces<D, C::MERGE_PB>(gp, ctx, bhv, slice, G, gv, qrow0, target, gf, off, tid,
+                                                 scratch, wb))
+                return false;
+        }
+        if (!wb.sync(lane))   // the flag and the scratch are reused
+            return false;
     }
     return true;
 }
@@ -639,101 +775,10 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 dead = true;
                 break;
             }
-            if (wg == 0) {
-                const float m1 = xk[2 * row], l1 = xk[2 * row + 1];
-                const float m0 = had ? m_ref : -INFINITY, l0 = had ? l : 0.f;
-                const float M = fmaxf(l0 > 0.f ? m0 : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
-                const float a0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
-                const float a1 = l1 > 0.f ? ex2(m1 - M) : 0.f;
-                const float L = a0 * l0 + a1 * l1;
-                const bool nonempty = L > 0.f;
-                const float f0 = nonempty ? a0 / L : 0.f, f1 = nonempty ? a1 / L : 0.f;
-                const bool need0 = __any_sync(FULL_MASK, l0 > 0.f), need1 = __any_sync(FULL_MASK, l1 > 0.f);
-                const int len = (p.decomp == DECOMP_BALANCED) ? lenS[cs.b] : clamp_len(p, cs.b);
-                bool complete;
-                long long slot;
-                if (p.decomp == DECOMP_SPLITS) {
-                    complete = (p.P == 1);
-                    slot = bhv * p.P + cs.p;
-                } else {
-                    complete = (cs.t0 == 0 && cs.t1 == len);
-                    slot = 2LL * blockIdx.x + (cs.k == 0 ? 0 : 1);
-                }
-                const long long qrow = qrow0 + row;
-                const long long r = slot * G + row;
-#pragma unroll 1
-                for (int q = 0; q < D / 16; ++q) {
-                    float o0[16], o1[16];
-                    if (need0)
-                        tmem_ld16(tl + (uint32_t)(C::TMEM_O + 16 * q), o0);
-                    if (need1)
-                        tmem_ld16(tl + (uint32_t)(C::TMEM_O + D + 16 * q), o1);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        o0[e] = (need0 ? f0 * o0[e] : 0.f) + (need1 ? f1 * o1[e] : 0.f);
-                    if (live) {
-                        if (complete) {
-                            store_out8(p.out, qrow * D + 16 * q, p.out_dtype, o0);
-                            store_out8(p.out, qrow * D + 16 * q + 8, p.out_dtype, o0 + 8);
-                        } else {
-                            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + r * D + 16 * q);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                dst[e] = make_float4(o0[4 * e], o0[4 * e + 1], o0[4 * e + 2], o0[4 * e + 3]);
-                        }
-                    }
-                }
-                tc_fence_before();
-                if (live) {
-                    if (complete) {
-                        if (p.lse)
-                            p.lse[qrow] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
-                    } else {
-                        p.ws_ml[2 * r] = nonempty ? M : -INFINITY;
-                        p.ws_ml[2 * r + 1] = L;
-                    }
-                }
-                if (!complete) {
-                    unsigned target;
-                    int gf = 0;
-                    long long off = 0;
-                    if (p.decomp == DECOMP_SPLITS) {
-                        target = (unsigned)p.P;
-                    } else {
-                        off = ctx.cumH[cs.b] + (long long)cs.h * len;
-                        gf = bal_owner(off, ctx.T, ctx.Geff);
-                        const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
-                        target = (unsigned)(gl - gf + 1);
-                    }
-                    // the barrier orders every thread's partial before thread 0's
-                    // fence and arrival
-                    if (!wb.sync(lane)) {
-                        dead = true;
-                        break;
-                    }
-                    if (tid == 0) {
-                        __threadfence();
-                        const unsigned old = atomicInc(p.ws_cnt + bhv, target - 1);
-                        misc[1] = (old == target - 1) ? 1u : 0u;
-                    }
-                    if (!wb.sync(lane)) {
-                        dead = true;
-                        break;
-                    }
-                    if (misc[1]) {
-                        __threadfence();
-                        if (!tc_merge_pieces<D, C::MERGE_PB>(gp, ctx, bhv, slice, G, gv, qrow0, target, gf, off,
-                                                             tid, scratch, wb)) {
-                            dead = true;
-                            break;
-                        }
-                    }
-                    if (!wb.sync(lane)) {   // the flag and the scratch are reused
-                        dead = true;
-                        break;
-                    }
-                }
+            if (wg == 0 && !tc_segment_end<C, D>(gp, ctx, cs, slice, G, gv, qrow0, bhv, had, m_ref, l, xk[2 * row],
+                                                   xk[2 * row + 1], row, lane, tid, tl, misc, scratch, wb)) {
+                dead = true;
+                break;
             }
             seg_next(p, ctx, cs);
         }
