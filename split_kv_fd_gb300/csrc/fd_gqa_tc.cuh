@@ -636,21 +636,35 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     break;
                 }
                 tc_fence_after();
-                // the chunk's max over its valid tokens (base-2 scores), 32
-                // columns at a time; the scores are read again for P below
+                // the head's 64 scores in one TMEM round trip
+                float s0[32], s1[32];
+                tmem_ld32(tl + (uint32_t)(b * C::CT), s0);
+                tmem_ld32(tl + (uint32_t)(b * C::CT + 32), s1);
                 int t, ntok;
                 chunk_coords<C::CT>(cs, c, t, ntok);
+                tmem_wait_ld();
+                auto S = [&](int i) -> float & { return i < 32 ? s0[i] : s1[i - 32]; };
+                // the tokens past the chunk's (a partial chunk only) become -inf
+                if (ntok < C::CT) {
+#pragma unroll
+                    for (int i = 0; i < C::CT; ++i)
+                        S(i) = i < ntok ? S(i) : -INFINITY;
+                }
+                // the chunk's max of the base-2 scores s * sc: the max of the
+                // raw scores times sc (sc > 0, the normal case), else the min
                 const float sc = p.scale_log2;
-                float mc = -INFINITY;
+                float mc;
+                if (sc > 0.f) {
+                    float x = S(0);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float sv[32];
-                    tmem_ld32(tl + (uint32_t)(b * C::CT + 32 * h), sv);
-                    tmem_wait_ld();
+                    for (int i = 1; i < C::CT; ++i)
+                        x = fmaxf(x, S(i));
+                    mc = x * sc;
+                } else {
+                    mc = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (32 * h + i < ntok)
-                            mc = fmaxf(mc, sv[i] * sc);
+                    for (int i = 0; i < C::CT; ++i)
+                        mc = fmaxf(mc, S(i) * sc);
                 }
                 // the group's previous chunk: its P.V is done, so O is final
                 // and its S/P buffer free for the chunk four ahead
@@ -690,33 +704,22 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                         tmem_st16u(tl + ocol + (uint32_t)(16 * q), u);
                     }
                 }
-                // P = 2^(s - m_ref): the 16-bit high part and its remainder,
-                // packed pairs, into the chunk's S columns (0-31 and 32-63),
-                // 32 tokens at a time (P of tokens 32h.. overwrites columns
-                // 16h.. and 32 + 16h.., which hold scores already read)
+                // P = 2^(s sc - m_ref): the 16-bit high part and its
+                // remainder, packed pairs, into the chunk's S columns (P_hi
+                // in 0-31, P_lo in 32-63; the scores are all in registers).
+                // Heads past the slice's (zero q rows) get P = 1 and are
+                // never written out.
                 const uint64_t sc2 = pack2(sc, sc), nm2 = pack2(-m_ref, -m_ref), one2 = pack2(1.f, 1.f);
                 uint64_t ls2 = pack2(0.f, 0.f);
-                float sv1[32];   // scores of tokens 32..63, read before their columns are overwritten
-                tmem_ld32(tl + (uint32_t)(b * C::CT + 32), sv1);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    float sv[32];
-                    if (h == 0) {
-                        tmem_ld32(tl + (uint32_t)(b * C::CT), sv);
-                        tmem_wait_ld();
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            sv[i] = sv1[i];
-                    }
                     uint32_t ph[16], plo[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int tk = 32 * h + 2 * i;
                         float x0, x1;
-                        unpack2(fma2(pack2(sv[2 * i], sv[2 * i + 1]), sc2, nm2), x0, x1);
-                        const float p0 = (live && tk < ntok) ? ex2(x0) : 0.f;
-                        const float p1 = (live && tk + 1 < ntok) ? ex2(x1) : 0.f;
+                        unpack2(fma2(pack2(S(tk), S(tk + 1)), sc2, nm2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
                         ls2 = fma2(pack2(p0, p1), one2, ls2);
                         ph[i] = Mma<T>::pack(p0, p1);
                         const float2 u = Mma<T>::unpack(ph[i]);
