@@ -6,7 +6,7 @@
 // Per (b, K/V head) and chunk of CT = 64 tokens the work is two dense
 // products over all the K/V head's query heads at once (up to 128, the MMA's
 // M; more are served in slices by adjacent CTAs):
-//     S [128 x CT] = Q [128 x d] . K_chunk^T     (Q and K in shared memory)
+//     S [128 x CT] = Q [128 x d] . K_chunk^T     (Q in TMEM, K in shared memory)
 //     O [128 x d] += P [128 x CT] . V_chunk      (P in TMEM, V in shared memory)
 // so every K/V byte enters shared memory once per CTA, whatever the number
 // of query heads (the mma.sync kernel of fd_gqa.cuh stages a chunk once per
@@ -31,11 +31,14 @@
 //    accumulator and (m_ref, l) per head; at a segment end group 0 merges
 //    the two states ("FlashDecoding 数学推导" §2.4.2) and writes the result;
 //  - warp 8: the producer, K and V chunks by tensor-map TMA into a ring of
-//    STAGES stages (128 KB in flight, as in the other kernels);
+//    STAGES stages (192 KB);
 //  - warp 9: allocates TMEM; its lane 0 issues the MMAs, S of chunk j + 1
 //    ahead of P.V of chunk j.
-// TMEM holds four S/P buffers (chunk j in buffer j % 4) and the two O
-// accumulators.  Every hand-off is an mbarrier (the MMA warp's through
+// TMEM holds the S/P buffers (chunk j in buffer j % NSB), Q (the A
+// operand of S, written by group 0 at a segment start) and the two O
+// accumulators; with Q there, shared memory holds a 192 KB ring: a stage
+// stays taken from its copy until P.V of its chunk is done, and the copies
+// take ~3 us to land at full load.  Every hand-off is an mbarrier (the MMA warp's through
 // tcgen05.commit), and every wait is bounded: on expiry a role records
 // FD_ERR_DEVICE_TIMEOUT, stops, drains what it issued, and the CTA frees its
 // TMEM.
@@ -67,28 +70,34 @@ template <typename T, int D> struct TcCfg {
     static constexpr int PLANE = CT * 128;         // one 64-element plane of a chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // K or V of one chunk
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
-    static constexpr int STAGES = (128 * 1024) / STAGE_BYTES;
+    // a stage stays taken from its copy until P.V of its chunk is done, so
+    // the ring is deeper than the other kernels' 128 KB in flight
+    // a stage stays taken from its copy until P.V of its chunk is done, so
+    // the ring is deeper than the other kernels' 128 KB in flight
+    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int QPLANE = M * 128;         // one 64-element plane of Q
-    static constexpr int Q_BYTES = LINES * QPLANE;
-    static constexpr int MERGE_PB = 64;            // pieces merged with weights in shared memory
-    static constexpr int SCR_BYTES = MERGE_PB * 8 + MERGE_PB * MAXG * 4 + 2 * MAXG * 4;
+    static constexpr int MERGE_PB = 64;            // pieces per batch of the last arriver's merge
+    static constexpr int SCR_BYTES = MERGE_PB * 8 + 2 * MAXG * 4;   // their slots, then M and L per head
     static constexpr int XCH_BYTES = 2 * M * 2 * 4;   // group 1's (m_ref, l) per head, two segments
     static constexpr int WG_THREADS = 128, PROD_WARP = 8, MMA_WARP = 9, THREADS = 320;
-    // mbarriers: full[STAGES], empty[STAGES], s_full[4], s_free[4], p_full[2],
-    // o_full[2], q_full, fin, seg (both groups), wg0 (group 0)
-    static constexpr int NBAR = 2 * STAGES + 16;
-    static constexpr int TMEM_O = 4 * CT;          // S/P buffers at columns 0, 64, 128, 192
+    // TMEM: NSB S/P buffers of CT columns (chunk j in buffer j % NSB), then Q
+    // (d/2 columns of 16-bit pairs), then the two groups' O accumulators
+    static constexpr int NSB = D == 128 ? 3 : 4;
+    static constexpr int TMEM_Q = NSB * CT;
+    static constexpr int TMEM_O = (TMEM_Q + D / 2 + 63) / 64 * 64;   // accumulators on a 64-column boundary
     static constexpr uint32_t TMEM_COLS = 512;
+    // mbarriers: full[STAGES], empty[STAGES], s_full[NSB], s_free[NSB],
+    // p_full[2], o_full[2], q_full, fin, seg (both groups), wg0 (group 0)
+    static constexpr int NBAR = 2 * STAGES + 2 * NSB + 8;
     static constexpr float TAU = 8.f;              // lazy-rescale threshold (base 2)
     static_assert(D == 64 || D == 128, "head dim 64 or 128");
     static_assert(CT == 64, "an S buffer holds P_hi and P_lo in its 64 columns");
     static_assert(TMEM_O + 2 * D <= (int)TMEM_COLS, "TMEM columns");
-    static_assert(RING_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "1024-byte atoms");
+    static_assert(RING_BYTES % 1024 == 0, "1024-byte atoms");
 
     static size_t smem_bytes(int decomp, int B)
     {
-        size_t s = 1024 + RING_BYTES + Q_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16;
+        size_t s = 1024 + RING_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16;
         if (decomp == DECOMP_BALANCED)
             s += (size_t)(B + 1) * 8 + (size_t)B * 4;
         return s;
@@ -146,50 +155,39 @@ __device__ __forceinline__ void store_out4(void *out, long long idx, int out_dty
 // One batch of the last arriver's merge, on softmax group 0: the m/l/o
 // merge ("FlashDecoding 数学推导" §2.4.2) of the n <= MERGE_PB workspace
 // partials whose slots are in ss[0..n-1], for each of the Gv query rows.
-// The per-(piece, head) weights are formed once in `wt` (shared memory);
-// then every output element sums its pieces, with 16 loads in flight per
-// thread (the merge sits on the CTA's critical path: the next segment waits
-// for it).  The result goes to out/lse, or, when `into` >= 0, back into the
-// workspace slot `into` as a normalised partial (o, m, l) that a later batch
-// merges.  Returns false if a barrier wait expired.
+// First each head's max M and sum L over the pieces, then every output
+// element sums its pieces with their weights exp(m_i - M) l_i formed on the
+// fly, many loads in flight (the merge sits on the CTA's critical path: the
+// next segment waits for it).  The result goes to out/lse, or, when `into`
+// >= 0, back into the workspace slot `into` as a normalised partial (o, m,
+// l) that a later batch merges.  Returns false if a barrier wait expired.
 template <int D>
 __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int Gv, long long qrow0, const long long *ss,
-                                               int n, long long into, float *wt, float *sM, float *sL, int tid,
-                                               WarpBar &wb)
+                                               int n, long long into, float *sM, float *sL, int tid, WarpBar &wb)
 {
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);   // (m, l) per workspace row
     if (tid < Gv) {
-        // the head's max over the pieces, then its weights; 8 loads in flight
         float M = -INFINITY;
         for (int i0 = 0; i0 < n; i0 += 8) {
-            float mv[8], lv[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const long long r = ss[min(i0 + u, n - 1)] * G + tid;
-                mv[u] = __ldcg(p.ws_ml + 2 * r);
-                lv[u] = __ldcg(p.ws_ml + 2 * r + 1);
-            }
+            float2 v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (i0 + u < n && lv[u] > 0.f)
-                    M = fmaxf(M, mv[u]);
+                v[u] = __ldcg(ml + ss[min(i0 + u, n - 1)] * G + tid);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u < n && v[u].y > 0.f)
+                    M = fmaxf(M, v[u].x);
         }
         float L = 0.f;
         for (int i0 = 0; i0 < n; i0 += 8) {
-            float mv[8], lv[8];
+            float2 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const long long r = ss[min(i0 + u, n - 1)] * G + tid;
-                mv[u] = __ldcg(p.ws_ml + 2 * r);
-                lv[u] = __ldcg(p.ws_ml + 2 * r + 1);
-            }
+            for (int u = 0; u < 8; ++u)
+                v[u] = __ldcg(ml + ss[min(i0 + u, n - 1)] * G + tid);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (i0 + u < n) {
-                    const float e = lv[u] > 0.f ? ex2(mv[u] - M) * lv[u] : 0.f;
-                    wt[(i0 + u) * G + tid] = e;
-                    L += e;
-                }
-            }
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u < n && v[u].y > 0.f)
+                    L += ex2(v[u].x - M) * v[u].y;
         }
         sM[tid] = M;
         sL[tid] = L;
@@ -201,32 +199,37 @@ __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int 
     for (int base = 0; base < ngrp; base += 128 * GB) {
         float4 acc[GB];
         int gg[GB], dd[GB];
+        float Mg[GB];
 #pragma unroll
         for (int e = 0; e < GB; ++e) {
             acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
             const int grp = min(base + e * 128 + tid, ngrp - 1);
             gg[e] = grp * 4 / D;
             dd[e] = grp * 4 % D;
+            Mg[e] = sM[gg[e]];
         }
         for (int i0 = 0; i0 < n; i0 += PB) {
             float4 v[GB][PB];
+            float2 w[GB][PB];
 #pragma unroll
             for (int u = 0; u < PB; ++u) {
                 const long long s0 = ss[min(i0 + u, n - 1)] * G;
 #pragma unroll
-                for (int e = 0; e < GB; ++e)
+                for (int e = 0; e < GB; ++e) {
                     v[e][u] = __ldcg(reinterpret_cast<const float4 *>(p.ws_o + (s0 + gg[e]) * D + dd[e]));
+                    w[e][u] = __ldcg(ml + s0 + gg[e]);
+                }
             }
 #pragma unroll
             for (int u = 0; u < PB; ++u) {
 #pragma unroll
                 for (int e = 0; e < GB; ++e) {
-                    const float w = (i0 + u < n) ? wt[(i0 + u) * G + gg[e]] : 0.f;
-                    if (w > 0.f) {
-                        acc[e].x = fmaf(w, v[e][u].x, acc[e].x);
-                        acc[e].y = fmaf(w, v[e][u].y, acc[e].y);
-                        acc[e].z = fmaf(w, v[e][u].z, acc[e].z);
-                        acc[e].w = fmaf(w, v[e][u].w, acc[e].w);
+                    if (i0 + u < n && w[e][u].y > 0.f) {
+                        const float wt = ex2(w[e][u].x - Mg[e]) * w[e][u].y;
+                        acc[e].x = fmaf(wt, v[e][u].x, acc[e].x);
+                        acc[e].y = fmaf(wt, v[e][u].y, acc[e].y);
+                        acc[e].z = fmaf(wt, v[e][u].z, acc[e].z);
+                        acc[e].w = fmaf(wt, v[e][u].w, acc[e].w);
                     }
                 }
             }
@@ -251,7 +254,10 @@ __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int 
             }
         }
     }
-    if (into >= 0 && tid < Gv) {   // every read of (m, l) was before the barrier above
+    // every read of the batch's (m, l) is done before the slot's are replaced
+    if (!wb.sync(tid & 31))
+        return false;
+    if (into >= 0 && tid < Gv) {
         const long long r = into * G + tid;
         p.ws_ml[2 * r] = sL[tid] > 0.f ? sM[tid] : -INFINITY;
         p.ws_ml[2 * r + 1] = sL[tid];
@@ -271,8 +277,7 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
 {
     const SplitParams &p = gp.s;
     long long *ss = reinterpret_cast<long long *>(scr);            // [MERGE_PB] slots
-    float *wt = reinterpret_cast<float *>(scr + MERGE_PB * 8);      // [MERGE_PB][G] weights
-    float *sM = wt + MERGE_PB * G;                                   // [G]
+    float *sM = reinterpret_cast<float *>(scr + MERGE_PB * 8);      // [G]
     float *sL = sM + G;                                              // [G]
     const int n = (int)target;
     int first = 0;
@@ -283,7 +288,7 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
         if (!wb.sync(tid & 31))
             return false;
         const bool last = first + cnt == n;
-        if (!tc_merge_batch<D>(p, G, Gv, qrow0, ss, cnt, last ? -1 : ss[cnt - 1], wt, sM, sL, tid, wb))
+        if (!tc_merge_batch<D>(p, G, Gv, qrow0, ss, cnt, last ? -1 : ss[cnt - 1], sM, sL, tid, wb))
             return false;
         if (last)
             return true;
@@ -407,8 +412,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-aligned
     const uint32_t ring = smem_addr(smem);
-    const uint32_t qbuf = ring + C::RING_BYTES;
-    unsigned char *scratch = smem + C::RING_BYTES + C::Q_BYTES;   // the last arriver's merge
+    unsigned char *scratch = smem + C::RING_BYTES;   // the last arriver's merge
     float *xch = reinterpret_cast<float *>(scratch + C::SCR_BYTES);   // [2][M][2]
     uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::SCR_BYTES + C::XCH_BYTES);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBAR);   // [0] TMEM base, [1] flag
@@ -417,21 +421,23 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     const uint32_t bar0 = smem_addr(bars);
     auto FULL = [&](int s) { return bar0 + 8u * (uint32_t)s; };
     auto EMPTY = [&](int s) { return bar0 + 8u * (uint32_t)(ST + s); };
+    constexpr int NSB = C::NSB;
+    constexpr int B0 = 2 * ST + 2 * NSB;   // the barriers after the ring's and the S buffers'
     auto SFULL = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + b); };
-    auto SFREE = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + 4 + b); };
-    auto PFULL = [&](int g) { return bar0 + 8u * (uint32_t)(2 * ST + 8 + g); };
-    auto OFULL = [&](int g) { return bar0 + 8u * (uint32_t)(2 * ST + 10 + g); };
-    const uint32_t QFULL = bar0 + 8u * (2 * ST + 12);
-    const uint32_t FIN = bar0 + 8u * (2 * ST + 13);
-    const uint32_t SEGBAR = bar0 + 8u * (2 * ST + 14);
-    const uint32_t WG0BAR = bar0 + 8u * (2 * ST + 15);
+    auto SFREE = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + NSB + b); };
+    auto PFULL = [&](int g) { return bar0 + 8u * (uint32_t)(B0 + g); };
+    auto OFULL = [&](int g) { return bar0 + 8u * (uint32_t)(B0 + 2 + g); };
+    const uint32_t QFULL = bar0 + 8u * (B0 + 4);
+    const uint32_t FIN = bar0 + 8u * (B0 + 5);
+    const uint32_t SEGBAR = bar0 + 8u * (B0 + 6);
+    const uint32_t WG0BAR = bar0 + 8u * (B0 + 7);
 
     if (tid == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(FULL(s), 1);    // the producer's arrival plus the copies' bytes
             mbar_init(EMPTY(s), 1);   // commit after P.V of the stage's chunk
         }
-        for (int b = 0; b < 4; ++b) {
+        for (int b = 0; b < NSB; ++b) {
             mbar_init(SFULL(b), 1);   // commit after S
             mbar_init(SFREE(b), 4);   // the owning group's warps: P.V of the buffer's chunk is done
         }
@@ -505,28 +511,30 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr int BF = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
-            constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, C::M, C::CT);   // Q K-major, K K-major
+            constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, C::M, C::CT);   // Q (TMEM) K-major, K K-major
             constexpr uint32_t ID_O = idesc_f16(BF, 0, 1, C::M, D);       // P (TMEM) K-major, V MN-major
             long long pw[2] = {0, 0};   // P.V handed by each softmax group so far
             int k = 0;                  // non-empty segments so far
-            // S of chunk j into S/P buffer j % 4
+            // S of chunk j into S/P buffer j % NSB
             auto issue_s = [&](long long j) -> bool {
                 const int s = (int)(j % ST);
+                const int sb = (int)(j % NSB);
                 if (!mbar_wait_bounded_thread(FULL(s), (uint32_t)((j / ST) & 1)))
                     return false;
-                if (j >= 4 && !mbar_wait_bounded_thread(SFREE((int)(j & 3)), (uint32_t)(((j >> 2) - 1) & 1)))
+                if (j >= NSB && !mbar_wait_bounded_thread(SFREE(sb), (uint32_t)(((j / NSB) - 1) & 1)))
                     return false;
                 tc_fence_after();
                 const uint32_t kb = ring + (uint32_t)(s * C::STAGE_BYTES);
-                const uint32_t ds = tmem + (uint32_t)((j & 3) * C::CT);
+                const uint32_t ds = tmem + (uint32_t)(sb * C::CT);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t col = (uint32_t)((ks & 3) * 32);   // 16 elements = 32 bytes per k-step
-                    const uint64_t a = smem_desc_sw128(qbuf + (uint32_t)((ks >> 2) * C::QPLANE) + col, 16, 1024);
+                    // Q's 16 elements of this k-step: 8 columns of 16-bit pairs;
+                    // K's: 32 bytes of each 128-byte row of plane ks / 4
+                    const uint32_t col = (uint32_t)((ks & 3) * 32);
                     const uint64_t b = smem_desc_sw128(kb + (uint32_t)((ks >> 2) * C::PLANE) + col, 16, 1024);
-                    tc_mma_ss(ds, a, b, ID_S, ks > 0 ? 1u : 0u);
+                    tc_mma_ts(ds, tmem + (uint32_t)(C::TMEM_Q + ks * 8), b, ID_S, ks > 0 ? 1u : 0u);
                 }
-                tc_commit(SFULL((int)(j & 3)));
+                tc_commit(SFULL(sb));
                 return true;
             };
             long long j = 0;   // chunks of this CTA so far
@@ -560,7 +568,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                         ++pw[g];
                         tc_fence_after();
                         const uint32_t vb = ring + (uint32_t)((j % ST) * C::STAGE_BYTES + C::CHUNK_BYTES);
-                        const uint32_t pa = tmem + (uint32_t)((j & 3) * C::CT);
+                        const uint32_t pa = tmem + (uint32_t)((j % NSB) * C::CT);
 #pragma unroll
                         for (int ks = 0; ks < C::CT / 16; ++ks) {
 #pragma unroll
@@ -606,21 +614,25 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             const bool live = row < gv;
             float m_ref = -INFINITY, l = 0.f;
             if (n > 0 && wg == 0) {
-                // the query rows into the Q buffer (K-major, 128-byte swizzle)
+                // this head's q row into TMEM (its lane; d/2 columns of 16-bit
+                // pairs, the A operand of S = Q K^T); zero for heads past the slice's
                 const uint4 *qs = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
                                                                   (qrow0 + row) * D);
 #pragma unroll
-                for (int pl = 0; pl < C::LINES; ++pl)
+                for (int h = 0; h < D / 32; ++h) {   // 16 columns (32 elements) at a time
+                    uint32_t wv[16];
 #pragma unroll
-                    for (int c16 = 0; c16 < 8; ++c16) {
-                        const uint4 v = live ? __ldg(qs + pl * 8 + c16) : make_uint4(0, 0, 0, 0);
-                        const uint32_t a =
-                            qbuf + (uint32_t)(pl * C::QPLANE + row * 128 + ((c16 ^ (row & 7)) << 4));
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
-                                     "r"(v.z), "r"(v.w)
-                                     : "memory");
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 v = live ? __ldg(qs + 4 * h + i) : make_uint4(0, 0, 0, 0);
+                        wv[4 * i] = v.x;
+                        wv[4 * i + 1] = v.y;
+                        wv[4 * i + 2] = v.z;
+                        wv[4 * i + 3] = v.w;
                     }
-                fence_proxy_async_smem();
+                    tmem_st16u(tl + (uint32_t)(C::TMEM_Q + 16 * h), wv);
+                }
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(QFULL);
@@ -630,8 +642,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
 #pragma unroll 1
             for (long long c = (long long)(wg ^ (int)(j0 & 1)); c < n; c += 2) {
                 const long long j = j0 + c;
-                const int b = (int)(j & 3);
-                if (!mbar_wait_bounded(SFULL(b), (uint32_t)((j >> 2) & 1))) {
+                const int b = (int)(j % NSB);
+                if (!mbar_wait_bounded(SFULL(b), (uint32_t)((j / NSB) & 1))) {
                     dead = true;
                     break;
                 }
@@ -677,7 +689,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(SFREE((int)(jprev & 3)));
+                        mbar_arrive(SFREE((int)(jprev % NSB)));
                 }
                 // lazy rescale: the reference max moves only when the
                 // chunk's max exceeds it by more than TAU
@@ -763,7 +775,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(SFREE((int)(jprev & 3)));
+                    mbar_arrive(SFREE((int)(jprev % NSB)));
             }
             j0 += n;
 
