@@ -343,7 +343,7 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     // page (16 rows, every plane)
     gp.pages16 = (paged && paged->page_size == 16) ? 1 : 0;
     const int box_rows = tc ? TcCfg<__half, 128>::CT : gp.pages16 ? 16 : GqaCfg<__half, 128>::CT;
-    const int box_planes = tc ? TcCfg<__half, 128>::BOX_PLANES : d / 64;
+    const int box_planes = d / 64;
     const bool maps = kv_n > 0 && kv_blocks > 0;
     if (maps && !f8) {
         if (!make_kv_map(&gp.tmk, k, in_dtype, d, kv_n, kv_blocks, box_rows, box_planes) ||

@@ -87,7 +87,6 @@ template <typename T, int D, bool F8 = false> struct GqaCfg {
     static constexpr int KSTEPS = D / 16;          // k-steps of S^T = K Q^T
     static constexpr int MT = D / 16;              // 16-row tiles of O^T
     static constexpr int MAXG = (D == 256 || F8) ? 8 : 16;   // F8: the areas leave room for 8 heads' merge
-    static constexpr int BOX_PLANES = LINES;       // a chunk's box covers every plane
     static_assert(D == 64 || D == 128 || D == 256, "head dim");
     static_assert(!F8 || D <= 128, "E4M3 K/V: head dim 64 or 128");
     static_assert(PLANE % 1024 == 0, "planes stay 1024-byte aligned for the swizzle");
@@ -320,13 +319,8 @@ template <typename C, bool P16> struct TmaProducer {
                     blk = s.b * p.H + s.h;
                 }
                 mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
-                // one box per operand, or (BOX_PLANES < LINES) one per group of planes
-#pragma unroll
-                for (int pl = 0; pl < C::LINES; pl += C::BOX_PLANES) {
-                    const uint32_t o = (uint32_t)(pl * C::CT * 128);
-                    tma_load_4d(kdst + o, &gp.tmk, 0, y, blk, pl, bar);
-                    tma_load_4d(kdst + C::CHUNK_BYTES + o, &gp.tmv, 0, y, blk, pl, bar);
-                }
+                tma_load_4d(kdst, &gp.tmk, 0, y, blk, 0, bar);
+                tma_load_4d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, y, blk, 0, bar);
             }
         }
         c += stride;

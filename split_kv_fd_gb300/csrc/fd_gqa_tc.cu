@@ -5,17 +5,11 @@
 
 namespace fd {
 
-template <int MM> static cudaError_t launch_mm(int dtype, int d, const GqaParams &gp, cudaStream_t s)
-{
-    if (dtype == FD_BF16)
-        return d == 64 ? launch_gqa_tc_t<__nv_bfloat16, 64, MM>(gp, s) : launch_gqa_tc_t<__nv_bfloat16, 128, MM>(gp, s);
-    return d == 64 ? launch_gqa_tc_t<__half, 64, MM>(gp, s) : launch_gqa_tc_t<__half, 128, MM>(gp, s);
-}
-
-// Slices of at most 64 query heads run the M = 64 products.
 cudaError_t launch_gqa_tc(int dtype, int d, const GqaParams &gp, cudaStream_t s)
 {
-    return gp.G <= 64 ? launch_mm<64>(dtype, d, gp, s) : launch_mm<128>(dtype, d, gp, s);
+    if (dtype == FD_BF16)
+        return d == 64 ? launch_gqa_tc_t<__nv_bfloat16, 64>(gp, s) : launch_gqa_tc_t<__nv_bfloat16, 128>(gp, s);
+    return d == 64 ? launch_gqa_tc_t<__half, 64>(gp, s) : launch_gqa_tc_t<__half, 128>(gp, s);
 }
 
 }  // namespace fd

@@ -5,8 +5,7 @@
 //
 // Per (b, K/V head) and chunk of CT = 64 tokens the work is two dense
 // products over all the K/V head's query heads at once (up to 128, the MMA's
-// M, which is 64 for groups of at most 64; more are served in slices by
-// adjacent CTAs):
+// M; more are served in slices by adjacent CTAs):
 //     S [128 x CT] = Q [128 x d] . K_chunk^T     (Q in TMEM, K in shared memory)
 //     O [128 x d] += P [128 x CT] . V_chunk      (P in TMEM, V in shared memory)
 // so every K/V byte enters shared memory once per CTA, whatever the number
@@ -67,7 +66,6 @@ template <typename T, int D> struct TcCfg {
     static constexpr int M = 128;                  // query-head rows of the MMAs (TMEM lanes)
     static constexpr int MAXG = M;
     static constexpr int LINES = D / 64;           // 128-byte planes of a row
-    static constexpr int BOX_PLANES = 1;           // one 8 KB box per plane and operand
     static constexpr int ROW = D * 2;
     static constexpr int PLANE = CT * 128;         // one 64-element plane of a chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // K or V of one chunk
@@ -306,11 +304,11 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
 template <typename C, int D>
 __device__ __noinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int G, int gv,
                                             long long qrow0, long long bhv, bool had, float m_ref, float l, float m1,
-                                            float l1, bool real, int row, int lane, int tid, uint32_t tl, uint32_t *misc,
+                                            float l1, int row, int lane, int tid, uint32_t tl, uint32_t *misc,
                                             unsigned char *scratch, WarpBar &wb)
 {
     const SplitParams &p = gp.s;
-    const bool live = real && row < gv;
+    const bool live = row < gv;
     const float m0 = had ? m_ref : -INFINITY, l0 = had ? l : 0.f;
     const float M = fmaxf(l0 > 0.f ? m0 : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
     const float a0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
@@ -399,10 +397,7 @@ __device__ __noinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, 
     return true;
 }
 
-// MM: rows of the MMAs, 128, or 64 for slices of at most 64 query heads
-// (half the tensor work; an M = 64 result puts rows 16i..16i+15 in lanes
-// 32i..32i+15 of TMEM, so in each warp only lanes 0-15 hold heads).
-template <typename T, int D, int MM>
+template <typename T, int D>
 __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const __grid_constant__ GqaParams gp)
 {
     using C = TcCfg<T, D>;
@@ -516,8 +511,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr int BF = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
-            constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, MM, C::CT);   // Q (TMEM) K-major, K K-major
-            constexpr uint32_t ID_O = idesc_f16(BF, 0, 1, MM, D);       // P (TMEM) K-major, V MN-major
+            constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, C::M, C::CT);   // Q (TMEM) K-major, K K-major
+            constexpr uint32_t ID_O = idesc_f16(BF, 0, 1, C::M, D);       // P (TMEM) K-major, V MN-major
             long long pw[2] = {0, 0};   // P.V handed by each softmax group so far
             int k = 0;                  // non-empty segments so far
             // S of chunk j into S/P buffer j % NSB
@@ -600,10 +595,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     } else {
         // ------------------------------------------------------------ softmax groups
         const int wg = w >> 2;             // softmax group
-        // the query head of this thread's TMEM lane (MM = 64: lanes 16-31 of
-        // each warp hold none; they run along and write nothing)
-        const bool real = MM == 128 || lane < 16;
-        const int row = MM == 128 ? (tid & 127) : (w & 3) * 16 + (lane & 15);
+        const int row = tid & 127;         // query head within the slice = TMEM lane
         const uint32_t tl = tmem + ((uint32_t)((w & 3) * 32) << 16);
         const uint32_t ocol = (uint32_t)(C::TMEM_O + wg * D);
         WarpBar sb{SEGBAR, 0u}, wb{WG0BAR, 0u};
@@ -619,7 +611,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             const long long bhv = (long long)cs.b * p.H * gp.NG + vh;
             const int gv = vh_count(gp, vh);
             const long long qrow0 = vh_qrow0(gp, cs.b, vh);
-            const bool live = real && row < gv;
+            const bool live = row < gv;
             float m_ref = -INFINITY, l = 0.f;
             if (n > 0 && wg == 0) {
                 // this head's q row into TMEM (its lane; d/2 columns of 16-bit
@@ -701,7 +693,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 }
                 // lazy rescale: the reference max moves only when the
                 // chunk's max exceeds it by more than TAU
-                const bool grow = real && mc > m_ref + C::TAU;   // lanes without a head never grow
+                const bool grow = mc > m_ref + C::TAU;
                 float a = 1.f;
                 if (grow) {
                     a = ex2(m_ref - mc);   // 0 on the group's first chunk
@@ -755,7 +747,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 if (ntok < C::CT) {
                     const uint32_t vb = ring + (uint32_t)((j % ST) * C::STAGE_BYTES + C::CHUNK_BYTES);
                     const int pieces = (C::CT - ntok) * C::LINES * 8;
-                    for (int x = tid & 127; x < pieces; x += 128) {
+                    for (int x = row; x < pieces; x += 128) {
                         const int r = ntok + x / (C::LINES * 8);
                         const int rem = x % (C::LINES * 8);
                         const uint32_t va = vb + (uint32_t)((rem >> 3) * C::PLANE + r * 128 + (rem & 7) * 16);
@@ -789,7 +781,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
 
             // ---- segment end: group 1 hands over its (m_ref, l), group 0 merges ----
             float *xk = xch + (k & 1) * C::M * 2;
-            if (wg == 1 && real) {
+            if (wg == 1) {
                 xk[2 * row] = had ? m_ref : -INFINITY;
                 xk[2 * row + 1] = had ? l : 0.f;
             }
@@ -799,7 +791,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 break;
             }
             if (wg == 0 && !tc_segment_end<C, D>(gp, ctx, cs, slice, G, gv, qrow0, bhv, had, m_ref, l, xk[2 * row],
-                                                   xk[2 * row + 1], real, row, lane, tid, tl, misc, scratch, wb)) {
+                                                   xk[2 * row + 1], row, lane, tid, tl, misc, scratch, wb)) {
                 dead = true;
                 break;
             }
@@ -816,11 +808,11 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <typename T, int D, int MM> static cudaError_t launch_gqa_tc_t(const GqaParams &gp, cudaStream_t s)
+template <typename T, int D> static cudaError_t launch_gqa_tc_t(const GqaParams &gp, cudaStream_t s)
 {
     using C = TcCfg<T, D>;
     const size_t smem = C::smem_bytes(gp.s.decomp, gp.s.B);
-    auto kern = gqa_tc_kernel<T, D, MM>;
+    auto kern = gqa_tc_kernel<T, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
