@@ -6,7 +6,7 @@
 // Per (b, K/V head) and chunk of CT = 64 tokens the work is two dense
 // products over all the K/V head's query heads at once (up to 128, the MMA's
 // M; more are served in slices by adjacent CTAs):
-//     S [128 x CT] = Q [128 x d] . K_chunk^T     (Q in TMEM, K in shared memory)
+//     S [128 x CT] = Q [128 x d] . K_chunk^T     (Q and K in shared memory)
 //     O [128 x d] += P [128 x CT] . V_chunk      (P in TMEM, V in shared memory)
 // so every K/V byte enters shared memory once per CTA, whatever the number
 // of query heads (the mma.sync kernel of fd_gqa.cuh stages a chunk once per
@@ -31,14 +31,13 @@
 //    accumulator and (m_ref, l) per head; at a segment end group 0 merges
 //    the two states ("FlashDecoding 数学推导" §2.4.2) and writes the result;
 //  - warp 8: the producer, K and V chunks by tensor-map TMA into a ring of
-//    STAGES stages (192 KB);
-//  - warp 9: allocates TMEM; its lane 0 issues the MMAs, S of chunk j + 1
+//    STAGES stages;
+//  - warp 9: allocates TMEM; its lane 0 issues the MMAs, S of chunk j + 2
 //    ahead of P.V of chunk j.
-// TMEM holds the S/P buffers (chunk j in buffer j % NSB), Q (the A
-// operand of S, written by group 0 at a segment start) and the two O
-// accumulators; with Q there, shared memory holds a 192 KB ring: a stage
-// stays taken from its copy until P.V of its chunk is done, and the copies
-// take ~3 us to land at full load.  Every hand-off is an mbarrier (the MMA warp's through
+// TMEM holds four S/P buffers (chunk j in buffer j % 4) and the two O
+// accumulators.  A stage of the ring stays taken from its copy until P.V of
+// its chunk is done, and the copies take ~3 us to land at full load, so the
+// ring takes the shared memory left beside Q (160 KB at d = 128).  Every hand-off is an mbarrier (the MMA warp's through
 // tcgen05.commit), and every wait is bounded: on expiry a role records
 // FD_ERR_DEVICE_TIMEOUT, stops, drains what it issued, and the CTA frees its
 // TMEM.
@@ -71,20 +70,20 @@ template <typename T, int D> struct TcCfg {
     static constexpr int CHUNK_BYTES = CT * ROW;   // K or V of one chunk
     static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
     // a stage stays taken from its copy until P.V of its chunk is done, so
-    // the ring is deeper than the other kernels' 128 KB in flight
-    // a stage stays taken from its copy until P.V of its chunk is done, so
-    // the ring is deeper than the other kernels' 128 KB in flight
-    static constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
+    // the ring is deeper than the other kernels' 128 KB in flight: all the
+    // shared memory left beside Q, the merge scratch and the barriers
+    static constexpr int STAGES = ((D == 128 ? 160 : 192) * 1024) / STAGE_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int QPLANE = M * 128;         // one 64-element plane of Q
+    static constexpr int Q_BYTES = LINES * QPLANE;
     static constexpr int MERGE_PB = 64;            // pieces per batch of the last arriver's merge
     static constexpr int SCR_BYTES = MERGE_PB * 8 + 2 * MAXG * 4;   // their slots, then M and L per head
     static constexpr int XCH_BYTES = 2 * M * 2 * 4;   // group 1's (m_ref, l) per head, two segments
     static constexpr int WG_THREADS = 128, PROD_WARP = 8, MMA_WARP = 9, THREADS = 320;
-    // TMEM: NSB S/P buffers of CT columns (chunk j in buffer j % NSB), then Q
-    // (d/2 columns of 16-bit pairs), then the two groups' O accumulators
-    static constexpr int NSB = D == 128 ? 3 : 4;
-    static constexpr int TMEM_Q = NSB * CT;
-    static constexpr int TMEM_O = (TMEM_Q + D / 2 + 63) / 64 * 64;   // accumulators on a 64-column boundary
+    // TMEM: NSB S/P buffers of CT columns (chunk j in buffer j % NSB), then
+    // the two groups' O accumulators
+    static constexpr int NSB = 4;
+    static constexpr int TMEM_O = NSB * CT;
     static constexpr uint32_t TMEM_COLS = 512;
     // mbarriers: full[STAGES], empty[STAGES], s_full[NSB], s_free[NSB],
     // p_full[2], o_full[2], q_full, fin, seg (both groups), wg0 (group 0)
@@ -93,11 +92,11 @@ template <typename T, int D> struct TcCfg {
     static_assert(D == 64 || D == 128, "head dim 64 or 128");
     static_assert(CT == 64, "an S buffer holds P_hi and P_lo in its 64 columns");
     static_assert(TMEM_O + 2 * D <= (int)TMEM_COLS, "TMEM columns");
-    static_assert(RING_BYTES % 1024 == 0, "1024-byte atoms");
+    static_assert(RING_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "1024-byte atoms");
 
     static size_t smem_bytes(int decomp, int B)
     {
-        size_t s = 1024 + RING_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16;
+        size_t s = 1024 + RING_BYTES + Q_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16;
         if (decomp == DECOMP_BALANCED)
             s += (size_t)(B + 1) * 8 + (size_t)B * 4;
         return s;
@@ -412,7 +411,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-aligned
     const uint32_t ring = smem_addr(smem);
-    unsigned char *scratch = smem + C::RING_BYTES;   // the last arriver's merge
+    const uint32_t qbuf = ring + C::RING_BYTES;
+    unsigned char *scratch = smem + C::RING_BYTES + C::Q_BYTES;   // the last arriver's merge
     float *xch = reinterpret_cast<float *>(scratch + C::SCR_BYTES);   // [2][M][2]
     uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::SCR_BYTES + C::XCH_BYTES);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBAR);   // [0] TMEM base, [1] flag
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr int BF = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
-            constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, C::M, C::CT);   // Q (TMEM) K-major, K K-major
+            constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, C::M, C::CT);   // Q K-major, K K-major
             constexpr uint32_t ID_O = idesc_f16(BF, 0, 1, C::M, D);       // P (TMEM) K-major, V MN-major
             long long pw[2] = {0, 0};   // P.V handed by each softmax group so far
             int k = 0;                  // non-empty segments so far
@@ -528,11 +528,11 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 const uint32_t ds = tmem + (uint32_t)(sb * C::CT);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    // Q's 16 elements of this k-step: 8 columns of 16-bit pairs;
-                    // K's: 32 bytes of each 128-byte row of plane ks / 4
+                    // 16 elements = 32 bytes of each 128-byte row of plane ks / 4
                     const uint32_t col = (uint32_t)((ks & 3) * 32);
+                    const uint64_t a = smem_desc_sw128(qbuf + (uint32_t)((ks >> 2) * C::QPLANE) + col, 16, 1024);
                     const uint64_t b = smem_desc_sw128(kb + (uint32_t)((ks >> 2) * C::PLANE) + col, 16, 1024);
-                    tc_mma_ts(ds, tmem + (uint32_t)(C::TMEM_Q + ks * 8), b, ID_S, ks > 0 ? 1u : 0u);
+                    tc_mma_ss(ds, a, b, ID_S, ks > 0 ? 1u : 0u);
                 }
                 tc_commit(SFULL(sb));
                 return true;
@@ -550,13 +550,15 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     }
                     ++k;
                     tc_fence_after();
-                    if (!issue_s(j)) {
+                    // S runs two chunks ahead of P.V, so that the tensor pipe
+                    // has work while a group computes its P
+                    if (!issue_s(j) || (n > 1 && !issue_s(j + 1))) {
                         dead = true;
                         break;
                     }
 #pragma unroll 1
                     for (long long c = 0; c < n; ++c, ++j) {
-                        if (c + 1 < n && !issue_s(j + 1)) {
+                        if (c + 2 < n && !issue_s(j + 2)) {
                             dead = true;
                             break;
                         }
@@ -614,25 +616,22 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             const bool live = row < gv;
             float m_ref = -INFINITY, l = 0.f;
             if (n > 0 && wg == 0) {
-                // this head's q row into TMEM (its lane; d/2 columns of 16-bit
-                // pairs, the A operand of S = Q K^T); zero for heads past the slice's
+                // the query rows into the Q buffer (K-major, 128-byte swizzle);
+                // zero for heads past the slice's
                 const uint4 *qs = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
                                                                   (qrow0 + row) * D);
 #pragma unroll
-                for (int h = 0; h < D / 32; ++h) {   // 16 columns (32 elements) at a time
-                    uint32_t wv[16];
+                for (int pl = 0; pl < C::LINES; ++pl)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint4 v = live ? __ldg(qs + 4 * h + i) : make_uint4(0, 0, 0, 0);
-                        wv[4 * i] = v.x;
-                        wv[4 * i + 1] = v.y;
-                        wv[4 * i + 2] = v.z;
-                        wv[4 * i + 3] = v.w;
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const uint4 v = live ? __ldg(qs + pl * 8 + c16) : make_uint4(0, 0, 0, 0);
+                        const uint32_t a =
+                            qbuf + (uint32_t)(pl * C::QPLANE + row * 128 + ((c16 ^ (row & 7)) << 4));
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                                     "r"(v.z), "r"(v.w)
+                                     : "memory");
                     }
-                    tmem_st16u(tl + (uint32_t)(C::TMEM_Q + 16 * h), wv);
-                }
-                tmem_wait_st();
-                tc_fence_before();
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(QFULL);
