@@ -32,8 +32,8 @@
 //    the two states ("FlashDecoding 数学推导" §2.4.2) and writes the result;
 //  - warp 8: the producer, K and V chunks by tensor-map TMA into a ring of
 //    STAGES stages;
-//  - warp 9: allocates TMEM; its lane 0 issues the MMAs, S of chunk j + 2
-//    ahead of P.V of chunk j.
+//  - warp 9: allocates TMEM; its lane 0 issues the MMAs, S of chunk j + 1
+//    ahead of P.V of chunk j (measured: two ahead was no faster).
 // TMEM holds four S/P buffers (chunk j in buffer j % 4) and the two O
 // accumulators.  A stage of the ring stays taken from its copy until P.V of
 // its chunk is done, and the copies take ~3 us to land at full load, so the
@@ -54,6 +54,10 @@
 // (16-bit K/V, contiguous cache, head dim 64 or 128).
 #ifndef FD_GQA_TC_MIN_G
 #define FD_GQA_TC_MIN_G 17
+#endif
+// S products issued ahead of the P.V products (chunks)
+#ifndef FD_TC_LOOKAHEAD
+#define FD_TC_LOOKAHEAD 1
 #endif
 
 namespace fd {
@@ -550,15 +554,19 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     }
                     ++k;
                     tc_fence_after();
-                    // S runs two chunks ahead of P.V, so that the tensor pipe
+                    // S runs LOOK chunks ahead of P.V, so that the tensor pipe
                     // has work while a group computes its P
-                    if (!issue_s(j) || (n > 1 && !issue_s(j + 1))) {
+                    constexpr int LOOK = FD_TC_LOOKAHEAD;
+                    bool ok = true;
+                    for (int c = 0; c < LOOK && c < n; ++c)
+                        ok = ok && issue_s(j + c);
+                    if (!ok) {
                         dead = true;
                         break;
                     }
 #pragma unroll 1
                     for (long long c = 0; c < n; ++c, ++j) {
-                        if (c + 2 < n && !issue_s(j + 2)) {
+                        if (c + LOOK < n && !issue_s(j + LOOK)) {
                             dead = true;
                             break;
                         }

@@ -82,6 +82,13 @@ WORKLOADS["decode_gqa_b8_hq16_hkv8_n32k_d256_bf16"] = Workload(
 WORKLOADS["decode_mqa_b32_hq64_hkv1_n32k_d128_bf16"] = Workload(
     "decode_mqa_b32_hq64_hkv1_n32k_d128_bf16", 32, 64, 32768, 128, "bf16", "bf16", 0, Hkv=1)
 
+# grouped-query decode with larger groups on the same 1 GiB cache: 128 and
+# 256 query heads over 8 K/V heads (G = 16, 32)
+WORKLOADS["decode_gqa_b8_hq128_hkv8_n32k_d128_bf16"] = Workload(
+    "decode_gqa_b8_hq128_hkv8_n32k_d128_bf16", 8, 128, 32768, 128, "bf16", "bf16", 0, Hkv=8)
+WORKLOADS["decode_gqa_b8_hq256_hkv8_n32k_d128_bf16"] = Workload(
+    "decode_gqa_b8_hq256_hkv8_n32k_d128_bf16", 8, 256, 32768, 128, "bf16", "bf16", 0, Hkv=8)
+
 # a 256 MiB multi-query case for detailed profiles of the tcgen05 kernel
 WORKLOADS["decode_mqa_b16_hq64_hkv1_n32k_d128_bf16"] = Workload(
     "decode_mqa_b16_hq64_hkv1_n32k_d128_bf16", 16, 64, 32768, 128, "bf16", "bf16", 0, Hkv=1)
