@@ -7,8 +7,9 @@ Covers groups from 33 to 256 (two slices of 128), head dims 64 and 128,
 bf16 and f16, the automatic decomposition and explicit splits, lengths 0,
 shorter than one 64-token chunk and ragged, peaked scores (the lazy
 rescale of the O rows in TMEM), one long sequence cut into many pieces
-(the merges with weights in shared memory and, past 64 pieces, the
-per-element one), and both output dtypes.  Padding rows are NaN.
+(the last arriver's merge in one batch and, past 64 pieces, in batches
+whose results are written back as partials), and both output dtypes.
+Padding rows are NaN.
 """
 import pytest
 import torch
@@ -79,9 +80,9 @@ def test_peaked_scores_rescale_o_in_tmem():
 
 @pytest.mark.parametrize("num_splits", [0, 40, 100])
 def test_long_sequence_many_pieces(num_splits):
-    """One 150K-token sequence: cut into one piece per CTA (automatic), into
-    40 explicit splits (weights in shared memory) and into 100 (the
-    per-element merge)."""
+    """One 150K-token sequence: cut into one piece per CTA (automatic: 152
+    pieces, three merge batches), into 40 explicit splits (one batch) and
+    into 100 (two batches)."""
     q, k, v, lt = _gqa_case(1, 64, 1, 150000, 128, "bf16", None, seed=11)
     _run(q, k, v, lt, "bf16", num_splits)
 
