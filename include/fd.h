@@ -167,11 +167,15 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  * G == 1 is fd_decode.  For G >= 2 the per-chunk contraction runs on the
  * tensor cores, which need 16-bit operands: in_dtype f16 or bf16.  The
  * cache may hold any number of rows in all (the copies address a row by its
- * place in its (b, K/V head) block and the block's index).  A K/V head's
- * query heads are processed in even slices of
- * at most 16 (8 at d = 256), each reading that K/V head's rows (MQA with
- * many heads included); the slices of one K/V head run side by side, so
- * their repeated reads are mostly served from L2.  The workspace size is
+ * place in its (b, K/V head) block and the block's index).  Up to 32
+ * query heads per K/V head (and any group with d = 256 or a paged cache),
+ * the products are mma.sync and a K/V head's query heads are processed in
+ * even slices of at most 16 (8 at d = 256), each reading that K/V head's
+ * rows, side by side so that the repeated reads are mostly served from L2.
+ * From 33 query heads per K/V head (MQA included; contiguous cache, d = 64
+ * or 128) they are tcgen05 products with accumulators in tensor memory, all
+ * of a K/V head's query heads (slices of at most 128) served from one copy
+ * of each K/V chunk.  The workspace size is
  * fd_workspace_size_gqa(...), one size for fd_decode_gqa,
  * fd_decode_gqa_paged and fd_decode_gqa_fp8.  Returns FD_ERR_UNSUPPORTED for
  * f32 with G > 1.
