@@ -693,8 +693,8 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.path != "fused" and (args.page_size or args.kv_dtype != "native" or w.kv_heads != w.H):
         ap.error("--path split-* times the contiguous, native-dtype, one-query-per-K/V-head path")
-    if args.kv_dtype != "native" and args.page_size and (w.kv_heads == w.H or w.d != 128):
-        ap.error("--kv-dtype e4m3 with --page-size times the paged E4M3 grouped-query path (d = 128)")
+    if args.kv_dtype != "native" and args.page_size and w.kv_heads == w.H:
+        ap.error("--kv-dtype e4m3 with --page-size times the paged E4M3 grouped-query path")
     ws, _, _ = dist_env()
     if args.gpus > 1 and ws == 1 and "LOCAL_RANK" not in os.environ:
         # launch the per-GPU ranks ourselves

@@ -24,8 +24,8 @@
  *     f32, f16 or bf16; accumulation is always float32.
  *   - Supported head dims: 64 and 128; also 256 with f16, bf16 or E4M3 K/V
  *     (fd_decode, fd_decode_split, the combines, fd_decode_paged,
- *     fd_decode_fp8, fd_decode_noalloc, and grouped-query decode with
- *     f16/bf16 K/V; fd_decode_gqa_fp8 is 64 and 128 only).  q, K, V, out,
+ *     fd_decode_fp8, fd_decode_noalloc, and grouped-query decode, paged
+ *     or not, with f16, bf16 or E4M3 K/V).  q, K, V, out,
  *     o_part must be 16-byte aligned; seqlens, lse, m/l/lse partials 4-byte
  *     aligned.
  *   - All m and lse values are natural-log quantities of the *scaled* scores.
@@ -196,10 +196,11 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
  *             e4m3(byte), likewise V
  *   k_scale, v_scale  [B*Hkv] float32, device
  *   workspace fd_workspace_size_gqa(B, Hq, Hkv, N, d, num_splits) bytes
- * d must be 64 or 128.  The E4M3 rows are converted exactly to f16 in
+ * d must be 64, 128 or 256.  The E4M3 rows are converted exactly to f16 in
  * shared memory and the products run on the tensor cores in f16 with fp32
- * accumulation, q rounded to f16 (|q| < 65504); query heads in slices of at
- * most 8.  G == 1 is fd_decode_fp8.
+ * accumulation, q brought into the f16 range per query head by a power of
+ * two that the scores undo; query heads in slices of at most 8.  G == 1 is
+ * fd_decode_fp8.
  */
 fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,
                             const float *k_scale, const float *v_scale, const int32_t *seqlens, int B,
@@ -212,13 +213,13 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
  * the block-table indirection of fd_decode_gqa_paged (the layouts, table
  * rules and bad-entry handling of fd_decode_paged; "从第一性原理推导 Flash
  * Attention" §6.2, §7.1, §8).
- *   k_pages, v_pages  [num_pages, Hkv, page_size, 128] E4M3 bytes
+ *   k_pages, v_pages  [num_pages, Hkv, page_size, d] E4M3 bytes
  *   k_scale, v_scale  [B*Hkv] float32 (per sequence and K/V head)
  *   workspace         fd_workspace_size_gqa(B, Hq, Hkv, max_pages*page_size,
- *                     128, num_splits) bytes
- * d must be 128, page_size 16 or a multiple of 32 and num_pages*Hkv <
- * 2^31; any G >= 1 (G = 1 runs the same kernel).  FD_ERR_UNSUPPORTED
- * otherwise.
+ *                     d, num_splits) bytes
+ * d must be 64, 128 or 256, page_size 16 or a multiple of 32 and
+ * num_pages*Hkv < 2^31; any G >= 1 (G = 1 runs the same kernel).
+ * FD_ERR_UNSUPPORTED otherwise.
  */
 fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k_pages, const void *v_pages,
                                   const float *k_scale, const float *v_scale, const int32_t *block_table,

@@ -654,7 +654,7 @@ size_t fd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, int num_split
     // mma.sync 16-bit, mma.sync E4M3 and tcgen05
     size_t total = 0;
     for (int kind = 0; kind < 3; ++kind) {
-        if (kind > 0 && d > 128)
+        if (kind == 2 && d > 128)
             continue;
         if (kind == 2 && !gqa_use_tc(FD_BF16, d, Hq / Hkv, false))
             continue;
@@ -746,7 +746,7 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
                              out_dtype, lse, workspace, workspace_bytes, stream);
     if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || (d != 64 && d != 128))
+    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || !gqa_dim_ok(d))
         return FD_ERR_UNSUPPORTED;
     if ((long long)B * Hq == 0)
         return FD_OK;
@@ -774,9 +774,10 @@ fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k
     const int N = page_size * max_pages;
     if (!sizes_ok(B, Hq, N, d) || num_splits < 0 || num_splits > 65535)
         return FD_ERR_INVALID_ARG;
-    // E4M3 pages: the d = 128 kernel (byte boxes), G >= 1 (one query per
-    // K/V head runs it too), pages of 16 or a multiple of 32 tokens
-    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || d != 128)
+    // E4M3 pages: the grouped-query kernel at d = 64, 128 or 256, G >= 1
+    // (one query per K/V head runs it too), pages of 16 or a multiple of 32
+    // tokens
+    if (!valid_dtype(q_dtype) || !valid_dtype(out_dtype) || !gqa_dim_ok(d))
         return FD_ERR_UNSUPPORTED;
     if ((page_size % GqaCfg<__half, 128>::CT != 0 && page_size != 16) || num_pages * Hkv >= (1LL << 31))
         return FD_ERR_UNSUPPORTED;

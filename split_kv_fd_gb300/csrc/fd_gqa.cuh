@@ -54,13 +54,15 @@ namespace fd {
 // flight (a 32-token chunk of K and V is then 32 KB), and G <= 8 (one column
 // tile: O^T alone takes 64 accumulator registers per thread).
 //
-// F8: K/V stored as E4M3 bytes (d = 64 or 128).  The ring stages the bytes
-// as they are in memory (rows of d bytes, fetched by 1-D bulk copies), three
-// stages per group (96 KB in flight at d = 128); each warp converts its 16
-// rows to f16, exactly, into its own area (the 16-row layout of stage_row
-// with P16, K then V), frees the stage and runs the f16 products there.  A
-// slice then holds at most 8 query heads, so that the ring, the areas and the
-// merge buffer fit in one CTA's shared memory.
+// F8: K/V stored as E4M3 bytes (d = 64, 128 or 256).  The ring stages the
+// bytes as they are in memory (rows of d bytes; at d = 64 and 256 fetched by
+// 1-D bulk copies, a page at a time when a chunk spans two 16-token pages),
+// three stages per group at d = 64 and 256, four at d = 128; each warp
+// converts its 16 rows to f16, exactly, into its own area (the 16-row layout
+// of stage_row with P16, K then V), frees the stage and runs the f16
+// products there.  A slice then holds at most 8 query heads, so that the
+// ring, the areas and the merge buffer fit in one CTA's shared memory (at
+// d = 256: 96 KB of ring, 64 KB of areas, 33 KB of merge buffer).
 template <typename T, int D, bool F8 = false> struct GqaCfg {
     static constexpr bool F8K = F8;
     // F8 at d = 128: K's fragments come straight from the staged bytes (a
@@ -88,7 +90,6 @@ template <typename T, int D, bool F8 = false> struct GqaCfg {
     static constexpr int MT = D / 16;              // 16-row tiles of O^T
     static constexpr int MAXG = (D == 256 || F8) ? 8 : 16;   // F8: the areas leave room for 8 heads' merge
     static_assert(D == 64 || D == 128 || D == 256, "head dim");
-    static_assert(!F8 || D <= 128, "E4M3 K/V: head dim 64 or 128");
     static_assert(PLANE % 1024 == 0, "planes stay 1024-byte aligned for the swizzle");
     static_assert(RING_BYTES % 1024 == 0 && AREA_BYTES % 1024 == 0, "areas stay 1024-byte aligned");
 
@@ -122,7 +123,7 @@ struct GqaParams {  // CUtensorMap carries its own 64-byte (or wider) alignment
 
 cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s);
 cudaError_t launch_gqa_bf16(int d, const GqaParams &gp, cudaStream_t s);
-cudaError_t launch_gqa_f8(int d, const GqaParams &gp, cudaStream_t s);   // E4M3 K/V, f16 products (paged: d = 128)
+cudaError_t launch_gqa_f8(int d, const GqaParams &gp, cudaStream_t s);   // E4M3 K/V, f16 products
 cudaError_t launch_gqa_tc(int dtype, int d, const GqaParams &gp, cudaStream_t s);   // tcgen05, large groups
 
 // Byte offset of 16-byte column c of row r in a stage of 64-element planes
@@ -289,9 +290,34 @@ template <typename C, bool P16> struct TmaProducer {
                 mbar_arrive_expect_tx(bar, 2 * C::CHUNK_BYTES);
                 tma_load_3d(kdst, &gp.tmk, 0, y, blk, bar);
                 tma_load_3d(kdst + C::CHUNK_BYTES, &gp.tmv, 0, y, blk, bar);
+            } else if constexpr (C::F8K && P16) {
+                // 16-token pages: the chunk's rows in each of its (at most
+                // two) pages, to the stage rows of their place in the
+                // aligned block
+                const int a = t & ~(C::CT - 1);
+                const int t1 = t + ntok, mid = a + 16;
+                const int n0 = t < mid ? min(t1, mid) - t : 0;   // tokens in the first page
+                const int n1 = t1 > mid ? t1 - max(t, mid) : 0;  // and in the second
+                mbar_arrive_expect_tx(bar, 2 * (uint32_t)(n0 + n1) * C::ROW);
+                if (n0 > 0) {
+                    const long long row = (checked_page(p, pg) * p.H + s.h) * 16 + (t - a);
+                    const uint32_t dst = (uint32_t)(t - a) * C::ROW, bytes = (uint32_t)n0 * C::ROW;
+                    bulk_g2s(kdst + dst, static_cast<const char *>(p.k) + row * C::ROW, bytes, bar);
+                    bulk_g2s(kdst + C::CHUNK_BYTES + dst, static_cast<const char *>(p.v) + row * C::ROW, bytes, bar);
+                }
+                if (n1 > 0) {
+                    const int r1 = max(t, mid) - mid;            // first row in the second page
+                    const long long row = (checked_page(p, pg2) * p.H + s.h) * 16 + r1;
+                    const uint32_t dst = (uint32_t)(16 + r1) * C::ROW, bytes = (uint32_t)n1 * C::ROW;
+                    bulk_g2s(kdst + dst, static_cast<const char *>(p.k) + row * C::ROW, bytes, bar);
+                    bulk_g2s(kdst + C::CHUNK_BYTES + dst, static_cast<const char *>(p.v) + row * C::ROW, bytes, bar);
+                }
             } else if constexpr (C::F8K) {
-                // the chunk's E4M3 rows as they are in memory (contiguous K/V)
-                const long long row = ((long long)s.b * p.H + s.h) * p.N + t;
+                // the chunk's E4M3 rows as they are in memory: of the
+                // sequence's (b, K/V head) block, or of the one page that
+                // holds them (pages of a multiple of CT tokens)
+                const long long row = p.paged ? (checked_page(p, pg) * p.H + s.h) * p.page_size + t % p.page_size
+                                              : ((long long)s.b * p.H + s.h) * p.N + t;
                 const uint32_t bytes = (uint32_t)ntok * C::ROW;
                 mbar_arrive_expect_tx(bar, 2 * bytes);
                 bulk_g2s(kdst, static_cast<const char *>(p.k) + row * C::ROW, bytes, bar);
@@ -409,16 +435,17 @@ __device__ __forceinline__ void f8_rows_to_area(uint32_t stage, int row0, uint32
                                                 int lane)
 {
     constexpr int CPR = C::ROW / 16;               // 16-byte pieces per E4M3 row
-    static_assert(CPR == 4 || CPR == 8, "d = 64 or 128");
+    static_assert(CPR == 4 || CPR == 8 || CPR == 16, "d = 64, 128 or 256");
 #pragma unroll
     for (int i = 0; i < 16 * CPR / 32; ++i) {
         // Each 8-lane phase of the 16-byte accesses takes two consecutive
-        // rows: at d = 128 half a row's pieces from the first and the other
-        // half from the second.  Its loads then cover 128 contiguous bytes of
-        // staging, and its stores the two swizzle phases of adjacent rows:
-        // no bank conflicts either way.
+        // rows, four pieces (64 bytes) of each: at d = 128 half a row's
+        // pieces from the first and the other half from the second, at
+        // d = 256 quarters of opposite parity.  Its loads then fall on all
+        // 32 banks, and its stores on the two swizzle phases of adjacent
+        // rows: no bank conflicts either way.
         int r, c16;
-        if constexpr (CPR == 8) {
+        if constexpr (CPR >= 8) {
             const int q = lane >> 2, hb = q & 1;
             r = 2 * (q >> 1) + hb + 8 * (i & 1);
             c16 = (lane & 3) + 4 * (hb ^ (i >> 1));

@@ -9,7 +9,11 @@ cudaError_t launch_gqa_f8(int d, const GqaParams &gp, cudaStream_t s)
 {
     // slices of at most 8 query heads: one column tile
     if (d == 64)
-        return launch_gqa_p<__half, 64, 1, false, true>(gp, s);
+        return gp.pages16 ? launch_gqa_p<__half, 64, 1, true, true>(gp, s)
+                          : launch_gqa_p<__half, 64, 1, false, true>(gp, s);
+    if (d == 256)
+        return gp.pages16 ? launch_gqa_p<__half, 256, 1, true, true>(gp, s)
+                          : launch_gqa_p<__half, 256, 1, false, true>(gp, s);
     return gp.pages16 ? launch_gqa_p<__half, 128, 1, true, true>(gp, s)
                       : launch_gqa_p<__half, 128, 1, false, true>(gp, s);
 }

@@ -427,8 +427,8 @@ def decode_gqa_fp8(q, k, v, k_scale, v_scale, seqlens=None, num_splits=0, scale=
     """Grouped-query decode over an E4M3 KV cache (fd_decode_gqa_fp8).
 
     q: float32/float16/bfloat16 [B, Hq, d]; k, v: [B, Hkv, N, d]
-    torch.float8_e4m3fn (or uint8 E4M3 bytes) with Hq a multiple of Hkv;
-    k_scale, v_scale: float32 [B, Hkv].  Returns ``(out, lse)``.
+    torch.float8_e4m3fn (or uint8 E4M3 bytes) with Hq a multiple of Hkv, d
+    64, 128 or 256; k_scale, v_scale: float32 [B, Hkv].  Returns ``(out, lse)``.
     """
     _need_cuda(q, k, v, k_scale, v_scale, seqlens)
     if q.dtype not in DTYPE_CODE:
@@ -472,9 +472,9 @@ def decode_gqa_paged_fp8(q, k_pages, v_pages, k_scale, v_scale, block_table, seq
                          stream=None):
     """Grouped-query decode over a paged E4M3 KV cache (fd_decode_gqa_paged_fp8).
 
-    q: float32/float16/bfloat16 [B, Hq, 128]; k_pages/v_pages [num_pages, Hkv,
-    page_size, 128] torch.float8_e4m3fn (or uint8 E4M3 bytes), page_size 16 or
-    a multiple of 32; k_scale, v_scale float32 [B, Hkv]; block_table int32
+    q: float32/float16/bfloat16 [B, Hq, d]; k_pages/v_pages [num_pages, Hkv,
+    page_size, d] torch.float8_e4m3fn (or uint8 E4M3 bytes), d 64, 128 or
+    256, page_size 16 or a multiple of 32; k_scale, v_scale float32 [B, Hkv]; block_table int32
     [B, max_pages]; seqlens int32 [B].  Returns ``(out, lse)``.
     """
     _need_cuda(q, k_pages, v_pages, k_scale, v_scale, block_table, seqlens)

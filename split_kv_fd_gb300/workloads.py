@@ -89,6 +89,11 @@ WORKLOADS["decode_gqa_b8_hq128_hkv8_n32k_d128_bf16"] = Workload(
 WORKLOADS["decode_gqa_b8_hq256_hkv8_n32k_d128_bf16"] = Workload(
     "decode_gqa_b8_hq256_hkv8_n32k_d128_bf16", 8, 256, 32768, 128, "bf16", "bf16", 0, Hkv=8)
 
+# grouped-query decode at head dim 64: 64 query heads over 8 K/V heads
+# (G = 8), 16 sequences of 32K tokens (1 GiB of K/V in bf16, 512 MiB in E4M3)
+WORKLOADS["decode_gqa_b16_hq64_hkv8_n32k_d64_bf16"] = Workload(
+    "decode_gqa_b16_hq64_hkv8_n32k_d64_bf16", 16, 64, 32768, 64, "bf16", "bf16", 0, Hkv=8)
+
 # a 256 MiB multi-query case for detailed profiles of the tcgen05 kernel
 WORKLOADS["decode_mqa_b16_hq64_hkv1_n32k_d128_bf16"] = Workload(
     "decode_mqa_b16_hq64_hkv1_n32k_d128_bf16", 16, 64, 32768, 128, "bf16", "bf16", 0, Hkv=1)

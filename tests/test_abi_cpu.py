@@ -225,7 +225,7 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
                                      MB, None)
     assert gqa_fp8(Hq=6, Hkv=4) == 1             # Hq not a multiple of Hkv
     assert gqa_fp8(ks=None) == 1                 # scales are required
-    assert gqa_fp8(d=256) == 2                   # E4M3 with G > 1: d 64 or 128
+    assert gqa_fp8(d=96) == 2                    # head dims 64, 128 and 256
     assert gqa_fp8(qdt=3) == 2                   # q stays 16/32-bit
     assert gqa_fp8(q=P(4100)) == 1
     assert gqa_fp8(B=0, q=None, ks=None) == 0
@@ -233,7 +233,7 @@ def test_other_entry_points_reject_bad_arguments_without_cuda(lib):
     def gqa_paged_fp8(B=1, Hq=16, Hkv=2, d=128, ps=64, npg=8, ks=dm):
         return lib.fd_decode_gqa_paged_fp8(dm, 2, dm, dm, ks, dm, dm, dm, B, Hq, Hkv, d, ps, 4, npg, 0, 1.0, dm,
                                            2, None, dm, MB, None)
-    assert gqa_paged_fp8(d=64) == 2              # paged E4M3: d = 128
+    assert gqa_paged_fp8(d=96) == 2              # paged E4M3: d 64, 128 or 256
     assert gqa_paged_fp8(ps=48) == 2
     assert gqa_paged_fp8(ks=None) == 1
     assert gqa_paged_fp8(Hq=6, Hkv=4) == 1
@@ -261,4 +261,11 @@ def test_valid_call_without_a_gpu_reports_a_cuda_error(lib):
                                    None, P(1 << 20), 1 << 20, None) == 4
     assert lib.fd_decode_gqa_paged_fp8(dm, 2, dm, dm, dm, dm, dm, dm, 1, 16, 8, 128, 256, 4, 1 << 20, 0,
                                        1.0, dm, 2, None, P(1 << 20), 1 << 20, None) == 4
+    # E4M3 grouped-query decode at head dims 64 and 256, paged (16-token
+    # pages) and contiguous
+    for d in (64, 256):
+        assert lib.fd_decode_gqa_paged_fp8(dm, 2, dm, dm, dm, dm, dm, dm, 1, 16, 2, d, 16, 4, 8, 0, 1.0, dm, 2,
+                                           None, P(1 << 20), 1 << 20, None) == 4
+        assert lib.fd_decode_gqa_fp8(dm, 2, dm, dm, dm, dm, None, 1, 16, 2, 64, d, 0, 1.0, dm, 2, None,
+                                     P(1 << 20), 1 << 20, None) == 4
     assert lib.fd_num_sms() <= 0

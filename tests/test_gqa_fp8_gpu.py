@@ -32,7 +32,7 @@ def _reference(q, k8, v8, ks, vs, G, lens):
 
 
 @pytest.mark.parametrize("qdt", ["bf16", "f16", "f32"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("G", [2, 8, 16, 24])
 @pytest.mark.parametrize("num_splits", [0, 3])
 def test_gqa_fp8_matches_oracle(qdt, d, G, num_splits):
@@ -71,12 +71,12 @@ def test_gqa_fp8_group_of_one_and_limits():
     a = fd.decode_gqa_fp8(*args)
     b = fd.decode_fp8(*args)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])    # G = 1 is fd_decode_fp8
-    _, k2, v2, l2 = random_case(1, 1, 64, 256, "bf16", lens=None, seed=8, nan_pad=False)
+    _, k2, v2, l2 = random_case(1, 1, 64, 96, "bf16", lens=None, seed=8, nan_pad=False)
     k82, ks2 = quantize_e4m3(k2)
     with pytest.raises(fd.FDError) as e:
-        fd.decode_gqa_fp8(torch.randn(1, 4, 256, device=DEV).to(torch.bfloat16), k82.to(DEV), k82.to(DEV),
+        fd.decode_gqa_fp8(torch.randn(1, 4, 96, device=DEV).to(torch.bfloat16), k82.to(DEV), k82.to(DEV),
                           ks2.to(DEV), ks2.to(DEV), l2.to(DEV))
-    assert e.value.status == 2   # d = 256 with E4M3 and G > 1: FD_ERR_UNSUPPORTED
+    assert e.value.status == 2   # d = 96: FD_ERR_UNSUPPORTED
 
 
 @pytest.mark.slow
@@ -103,12 +103,13 @@ def test_gqa_fp8_benchmark_workload_sampled():
     assert bool(torch.isfinite(out).all())
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("G", [1, 4, 8, 16])
 @pytest.mark.parametrize("page_size", [16, 32, 64])
 @pytest.mark.parametrize("num_splits", [0, 3])
-def test_paged_gqa_fp8_matches_oracle(G, page_size, num_splits):
-    Hkv, d = 2, 128
-    _, k, v, lt = random_case(3, Hkv, 700, d, "bf16", lens=[700, 0, 333], seed=G + page_size,
+def test_paged_gqa_fp8_matches_oracle(d, G, page_size, num_splits):
+    Hkv = 2
+    _, k, v, lt = random_case(3, Hkv, 700, d, "bf16", lens=[700, 0, 333], seed=G + page_size + d,
                               nan_pad=False)
     q = torch.randn(3, G * Hkv, d, generator=torch.Generator().manual_seed(G + 1)).to(torch.bfloat16)
     k8, ks = quantize_e4m3(k)
@@ -165,8 +166,49 @@ def test_paged_gqa_fp8_full_size_equals_contiguous():
     assert torch.equal(out, cout) and torch.equal(lse, clse)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("name,page_size", [("decode_gqa_b8_hq16_hkv8_n32k_d256_bf16", 0),
+                                            ("decode_gqa_b8_hq16_hkv8_n32k_d256_bf16", 16),
+                                            ("decode_gqa_b16_hq64_hkv8_n32k_d64_bf16", 16),
+                                            ("decode_gqa_b16_hq64_hkv8_n32k_d64_bf16", 64)])
+def test_gqa_fp8_full_size_head_dims(name, page_size):
+    """The 2 GiB head-dim-256 (G = 2) and 1 GiB head-dim-64 (G = 8) GQA
+    workloads stored as E4M3, contiguous or in shuffled pages, automatic
+    decomposition: sampled rows against the oracle; 64-token pages are
+    bit-identical to the contiguous kernel (the same chunks)."""
+    import numpy as np
+    w = WORKLOADS[name]
+    G = w.H // w.kv_heads
+    q, k, v, lens = make_inputs(w, device="cuda")
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    del k, v
+    cout, clse = fd.decode_gqa_fp8(q, k8, v8, ks, vs, lens, scale=w.scale, out_dtype=torch.float32)
+    out, lse = cout, clse
+    if page_size:
+        kp, table = to_paged_bytes(k8, page_size, seed=5)
+        vp, _ = to_paged_bytes(v8, page_size, seed=5)
+        out, lse = fd.decode_gqa_paged_fp8(q, kp, vp, ks, vs, table, lens, scale=w.scale,
+                                           out_dtype=torch.float32)
+        del kp, vp
+        if page_size % 32 == 0:
+            assert torch.equal(out, cout) and torch.equal(lse, clse)
+    rng = np.random.default_rng(13)
+    for _ in range(8):
+        b, h = int(rng.integers(w.B)), int(rng.integers(w.H))
+        kv = h // G
+        ro, rs = oracle.attention_fp8(q[b:b + 1, h:h + 1].cpu(), k8[b:b + 1, kv:kv + 1].cpu(),
+                                      v8[b:b + 1, kv:kv + 1].cpu(), ks[b:b + 1, kv:kv + 1].cpu(),
+                                      vs[b:b + 1, kv:kv + 1].cpu(), scale=w.scale)
+        check_out(out[b:b + 1, h:h + 1], ro, "bf16")
+        check_lse(lse[b:b + 1, h:h + 1], rs, "bf16")
+    assert bool(torch.isfinite(out).all())
+    assert fd.device_status() == 0
+
+
 @pytest.mark.parametrize("qdt", ["f32", "bf16"])
-@pytest.mark.parametrize("d,page_size", [(64, 0), (128, 0), (128, 16), (128, 64)])
+@pytest.mark.parametrize("d,page_size", [(64, 0), (128, 0), (256, 0), (64, 16), (128, 16), (128, 64),
+                                         (256, 32)])
 def test_gqa_fp8_q_beyond_f16_range(qdt, d, page_size):
     """q far outside f16's range (|q| up to ~1e6 > 65504), which the E4M3
     products take in f16: each head's q is brought into range by a power of
