@@ -54,6 +54,8 @@ KERNEL_SOURCES = {
                    "fd_device.cuh", "fd_internal.h"],
     "gqa_tc_kernel": ["fd_gqa_tc.cuh", "fd_tc.cuh", "fd_gqa_tc.cu", "fd_gqa.cuh", "fd_split.cuh",
                       "fd_device.cuh", "fd_internal.h"],
+    "gqa_tc8_kernel": ["fd_gqa_tc8.cuh", "fd_gqa_tc8.cu", "fd_gqa_tc.cuh", "fd_tc.cuh", "fd_gqa.cuh",
+                       "fd_split.cuh", "fd_device.cuh", "fd_internal.h"],
 }
 
 
@@ -99,18 +101,21 @@ def kernel_source_hash(kernel: str = "split_kernel") -> str:
 GQA_TC_MIN_G = 33
 
 
-def kernel_key(w, fp8: bool, paged: bool) -> str:
-    """Which kernel does the timed work: split_kernel, gqa_kernel or gqa_tc_kernel."""
+def kernel_key(w, fp8: bool, paged: bool, page_size: int = 0) -> str:
+    """Which kernel does the timed work: split_kernel, gqa_kernel,
+    gqa_tc_kernel or gqa_tc8_kernel."""
     if w.kv_heads == w.H:
         return "split_kernel"
     if not fp8 and not paged and w.d <= 128 and w.H // w.kv_heads >= GQA_TC_MIN_G:
         return "gqa_tc_kernel"
+    if fp8 and w.d == 128 and (not paged or page_size % 128 == 0):
+        return "gqa_tc8_kernel"
     return "gqa_kernel"
 
 
-def kernel_name(w, fp8: bool, paged: bool) -> str:
+def kernel_name(w, fp8: bool, paged: bool, page_size: int = 0) -> str:
     """The kernel that does the timed work, as ncu names it."""
-    key = kernel_key(w, fp8, paged)
+    key = kernel_key(w, fp8, paged, page_size)
     elt = "e4m3" if fp8 else w.dtype
     return f"fd::{key}<{elt}, {w.d}>" + (" (paged)" if paged else "")
 
@@ -338,6 +343,13 @@ GATED = ["decode_b8_h32_n32k_d128_bf16", "decode_b1_h32_n128k_d128_bf16_k8",
          "decode_ragged_b16_h32_n64k_d128_bf16"]
 
 
+def check_device_status(fd):
+    """A timed run counts only if no kernel gave up a bounded wait in it."""
+    st = fd.device_status()
+    if st != 0:
+        raise SystemExit(f"bench: a kernel reported device status {st} during the timed steps")
+
+
 def time_gated(fd, name, steps, warmup, dev, ws, peaks):
     """One gated workload through the fused call (automatic decomposition),
     timed like the headline: `steps` launches, each inside its own CUDA
@@ -373,6 +385,7 @@ def time_gated(fd, name, steps, warmup, dev, ws, peaks):
 
     step_ms, launch_ms = timed(lambda: fd.decode(q, k, v, lens, scale=w.scale, out=out, lse=lse,
                                                  workspace=wsbuf, stream=stream))
+    check_device_status(fd)
     ent = {"value": ws * kvb / (step_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": step_ms,
            "pct_of_nominal_8tbs": 100.0 * kvb / (step_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
            "roofline": {"frac": alg / (launch_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -535,6 +548,7 @@ def run_ours(args, w):
     sampler.mark("t1")
     barrier(ws)
     clocks = sampler.stop()
+    check_device_status(fd)
     total_ms = t_start.elapsed_time(t_end)
     launch_ms = [a.elapsed_time(b) for a, b in evs]
     combine_ms = None
@@ -638,8 +652,8 @@ def run_ours(args, w):
                                      else profiled_traffic(w.name + ("+e4m3" if k_scale is not None
                                                                      else ""),
                                                            kernel_key(w, k_scale is not None,
-                                                                      table is not None))),
-                         "kernel": kernel_name(w, k_scale is not None, table is not None),
+                                                                      table is not None, args.page_size))),
+                         "kernel": kernel_name(w, k_scale is not None, table is not None, args.page_size),
                          "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                          "algorithmic_bytes_per_launch": alg, "mean_launch_ms": kern_ms},
             "e2e": e2e,

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfd.so")
 
 SOURCES = ["fd_api.cu", "fd_combine.cu", "fd_split_f32.cu", "fd_split_f16.cu", "fd_split_bf16.cu",
-           "fd_split_fp8.cu", "fd_gqa_bf16.cu", "fd_gqa_f16.cu", "fd_gqa_tc.cu"]
+           "fd_split_fp8.cu", "fd_gqa_bf16.cu", "fd_gqa_f16.cu", "fd_gqa_tc.cu", "fd_gqa_tc8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

@@ -3,7 +3,7 @@
 // launches.  Nothing here computes attention; every step runs in the kernels.
 #include "fd.h"
 #include "fd_gqa.cuh"
-#include "fd_gqa_tc.cuh"
+#include "fd_gqa_tc8.cuh"
 #include "fd_internal.h"
 #include "fd_split.cuh"
 
@@ -146,6 +146,22 @@ bool gqa_use_tc(int in_dtype, int d, int G, bool paged)
 {
     return !paged && (in_dtype == FD_F16 || in_dtype == FD_BF16) && (d == 64 || d == 128) &&
            G >= FD_GQA_TC_MIN_G;
+}
+
+// The block-table view of a paged K/V cache.
+struct PagedKV {
+    const int32_t *table;
+    int page_size, max_pages;
+    long long num_pages;
+};
+
+// Whether an E4M3 grouped-query call runs the FP8 tcgen05 kernel
+// (fd_gqa_tc8.cuh): head dim 128, a contiguous cache or pages of a multiple
+// of its 128-token chunk, two or more query heads per K/V head.
+bool gqa_use_tc8(int in_dtype, int d, int G, const PagedKV *paged)
+{
+    return in_dtype == FD_E4M3 && d == 128 && G >= 2 &&
+           (!paged || paged->page_size % Tc8Cfg<128>::CT == 0);
 }
 
 // The tcgen05 kernel's slices: up to 128 query heads (its MMA rows) each.
@@ -302,13 +318,6 @@ bool clear_counters(const SplitParams &p, long long rows, cudaStream_t s)
     return cudaMemsetAsync(p.ws_cnt, 0, (size_t)rows * sizeof(unsigned), s) == cudaSuccess;
 }
 
-// The block-table view of a paged K/V cache.
-struct PagedKV {
-    const int32_t *table;
-    int page_size, max_pages;
-    long long num_pages;
-};
-
 // The grouped-query launch once an entry point has checked its arguments:
 // plan, workspace, the K and V tensor maps over `kv_blocks` blocks of
 // `kv_n` rows of d elements (none when kv_blocks is 0), and the kernel's
@@ -322,11 +331,12 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     const bool f8 = in_dtype == FD_E4M3;   // then q_dtype is q's own and no tensor maps are made
     const int G = Hq / Hkv;
     const bool tc = gqa_use_tc(in_dtype, d, G, paged != nullptr);
+    const bool tc8 = gqa_use_tc8(in_dtype, d, G, paged);
     int NG, Gs;
     if (tc)
         gqa_tc_slices(G, NG, Gs);
     else
-        gqa_slices(d, G, NG, Gs, f8);
+        gqa_slices(d, G, NG, Gs, f8);   // the FP8 tcgen05 kernel's slices are the E4M3 kernel's
     const long long Hv = (long long)Hkv * NG;   // virtual heads
     const int sms = sm_count();
     unsigned *st = status_ptr();
@@ -342,7 +352,10 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     // boxes of one chunk (CT rows, every plane), or with 16-token pages of one
     // page (16 rows, every plane)
     gp.pages16 = (paged && paged->page_size == 16) ? 1 : 0;
-    const int box_rows = tc ? TcCfg<__half, 128>::CT : gp.pages16 ? 16 : GqaCfg<__half, 128>::CT;
+    const int box_rows = tc ? TcCfg<__half, 128>::CT
+                         : tc8        ? Tc8Cfg<128>::CT
+                         : gp.pages16 ? 16
+                                      : GqaCfg<__half, 128>::CT;
     const int box_planes = d / 64;
     const bool maps = kv_n > 0 && kv_blocks > 0;
     if (maps && !f8) {
@@ -379,9 +392,10 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (!clear_counters(p, (long long)B * Hv, cs))
         return FD_ERR_CUDA;
-    const cudaError_t e = tc ? launch_gqa_tc(in_dtype, d, gp, cs)
-                          : f8 ? launch_gqa_f8(d, gp, cs)
-                               : launch_gqa(in_dtype, d, gp, cs);
+    const cudaError_t e = tc    ? launch_gqa_tc(in_dtype, d, gp, cs)
+                          : tc8 ? launch_gqa_tc8(d, gp, cs)
+                          : f8  ? launch_gqa_f8(d, gp, cs)
+                                : launch_gqa(in_dtype, d, gp, cs);
     return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 

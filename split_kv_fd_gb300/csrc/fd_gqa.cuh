@@ -125,6 +125,7 @@ cudaError_t launch_gqa(int dtype, int d, const GqaParams &gp, cudaStream_t s);
 cudaError_t launch_gqa_bf16(int d, const GqaParams &gp, cudaStream_t s);
 cudaError_t launch_gqa_f8(int d, const GqaParams &gp, cudaStream_t s);   // E4M3 K/V, f16 products
 cudaError_t launch_gqa_tc(int dtype, int d, const GqaParams &gp, cudaStream_t s);   // tcgen05, large groups
+cudaError_t launch_gqa_tc8(int d, const GqaParams &gp, cudaStream_t s);   // tcgen05 FP8 products, E4M3 K/V
 
 // Byte offset of 16-byte column c of row r in a stage of 64-element planes
 // written by the 128B swizzle (stage base 1024-aligned): plane c/8, and

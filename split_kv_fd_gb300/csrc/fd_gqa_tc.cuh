@@ -299,6 +299,60 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
     }
 }
 
+// Where a segment's result goes: `complete` when the segment is its whole
+// (b, virtual head), then to out/lse; else to workspace slot `slot`.
+__device__ __forceinline__ void tc_seg_dest(const SplitParams &p, const Seg &cs, long long bhv, int len, bool &complete,
+                                            long long &slot)
+{
+    if (p.decomp == DECOMP_SPLITS) {
+        complete = (p.P == 1);
+        slot = bhv * p.P + cs.p;
+    } else {
+        complete = (cs.t0 == 0 && cs.t1 == len);
+        slot = 2LL * blockIdx.x + (cs.k == 0 ? 0 : 1);
+    }
+}
+
+// After a segment's partial is in the workspace, on softmax group 0: the
+// arrival on the (b, virtual head)'s counter and, for the last piece to
+// arrive, the merge of the pieces.  Returns false if a barrier wait expired.
+template <int D, int MERGE_PB>
+__device__ __noinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int gv,
+                                             long long qrow0, long long bhv, int len, int lane, int tid,
+                                             uint32_t *misc, unsigned char *scratch, WarpBar &wb)
+{
+    const SplitParams &p = gp.s;
+    unsigned target;
+    int gf = 0;
+    long long off = 0;
+    if (p.decomp == DECOMP_SPLITS) {
+        target = (unsigned)p.P;
+    } else {
+        off = ctx.cumH[cs.b] + (long long)cs.h * len;
+        gf = bal_owner(off, ctx.T, ctx.Geff);
+        const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
+        target = (unsigned)(gl - gf + 1);
+    }
+    // the barrier orders every thread's partial before thread 0's fence and
+    // arrival
+    if (!wb.sync(lane))
+        return false;
+    if (tid == 0) {
+        __threadfence();
+        const unsigned old = atomicInc(p.ws_cnt + bhv, target - 1);
+        misc[1] = (old == target - 1) ? 1u : 0u;
+    }
+    if (!wb.sync(lane))
+        return false;
+    if (misc[1]) {
+        __threadfence();
+        if (!tc_merge_pieces<D, MERGE_PB>(gp, ctx, bhv, slice, gp.G, gv, qrow0, target, gf, off, tid, scratch,
+                                          wb))
+            return false;
+    }
+    return wb.sync(lane);   // the flag and the scratch are reused
+}
+
 // Segment end on softmax group 0 (out of line, so that its registers do not
 // crowd the chunk loop): merges the two groups' (m_ref, l, O) per head
 // ("FlashDecoding 数学推导" §2.4.2), then writes out/lse for a whole (b, h),
@@ -323,13 +377,7 @@ __device__ __noinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, 
     const int len = (p.decomp == DECOMP_BALANCED) ? ctx.lenS[cs.b] : clamp_len(p, cs.b);
     bool complete;
     long long slot;
-    if (p.decomp == DECOMP_SPLITS) {
-        complete = (p.P == 1);
-        slot = bhv * p.P + cs.p;
-    } else {
-        complete = (cs.t0 == 0 && cs.t1 == len);
-        slot = 2LL * blockIdx.x + (cs.k == 0 ? 0 : 1);
-    }
+    tc_seg_dest(p, cs, bhv, len, complete, slot);
     const long long qrow = qrow0 + row;
     const long long r = slot * G + row;
 #pragma unroll 1
@@ -365,38 +413,8 @@ __device__ __noinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, 
             p.ws_ml[2 * r + 1] = L;
         }
     }
-    if (!complete) {
-        unsigned target;
-        int gf = 0;
-        long long off = 0;
-        if (p.decomp == DECOMP_SPLITS) {
-            target = (unsigned)p.P;
-        } else {
-            off = ctx.cumH[cs.b] + (long long)cs.h * len;
-            gf = bal_owner(off, ctx.T, ctx.Geff);
-            const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
-            target = (unsigned)(gl - gf + 1);
-        }
-        // the barrier orders every thread's partial before thread 0's
-        // fence and arrival
-        if (!wb.sync(lane))
-            return false;
-        if (tid == 0) {
-            __threadfence();
-            const unsigned old = atomicInc(p.ws_cnt + bhv, target - 1);
-            misc[1] = (old == target - 1) ? 1u : 0u;
-        }
-        if (!wb.sync(lane))
-            return false;
-        if (misc[1]) {
-            __threadfence();
-            if (!tc_merge_pieces<D, C::MERGE_PB>(gp, ctx, bhv, slice, G, gv, qrow0, target, gf, off, tid,
-                                                 scratch, wb))
-                return false;
-        }
-        if (!wb.sync(lane))   // the flag and the scratch are reused
-            return false;
-    }
+    if (!complete)
+        return tc_arrive_merge<D, C::MERGE_PB>(gp, ctx, cs, slice, gv, qrow0, bhv, len, lane, tid, misc, scratch, wb);
     return true;
 }
 

@@ -91,6 +91,21 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem] with 8-bit floating-point operands
+// (kind::f8f6f4; the instruction descriptor's format fields 0 = E4M3, so
+// idesc_f16(0, ...) describes E4M3 x E4M3 with an fp32 accumulator), 32
+// elements of K per instruction.
+__device__ __forceinline__ void tc_mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]: A read from tensor memory (M lanes, its K
 // elements packed two 16-bit values per 32-bit column, the lower half the
 // even element), B by descriptor.

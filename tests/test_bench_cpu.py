@@ -74,4 +74,6 @@ def test_kernel_names_of_the_timed_paths():
     assert bench.kernel_name(w, False, True) == "fd::split_kernel<bf16, 128> (paged)"
     assert bench.kernel_name(g, False, False) == "fd::gqa_kernel<bf16, 128>"
     assert bench.kernel_name(g, False, True) == "fd::gqa_kernel<bf16, 128> (paged)"
-    assert bench.kernel_name(g, True, False) == "fd::gqa_kernel<e4m3, 128>"
+    assert bench.kernel_name(g, True, False) == "fd::gqa_tc8_kernel<e4m3, 128>"
+    assert bench.kernel_name(g, True, True, 64) == "fd::gqa_kernel<e4m3, 128> (paged)"
+    assert bench.kernel_name(g, True, True, 256) == "fd::gqa_tc8_kernel<e4m3, 128> (paged)"

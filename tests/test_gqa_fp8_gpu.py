@@ -105,7 +105,7 @@ def test_gqa_fp8_benchmark_workload_sampled():
 
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("G", [1, 4, 8, 16])
-@pytest.mark.parametrize("page_size", [16, 32, 64])
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
 @pytest.mark.parametrize("num_splits", [0, 3])
 def test_paged_gqa_fp8_matches_oracle(d, G, page_size, num_splits):
     Hkv = 2
@@ -126,7 +126,10 @@ def test_paged_gqa_fp8_matches_oracle(d, G, page_size, num_splits):
     if G > 1:
         cout, clse = fd.decode_gqa_fp8(q.to(DEV), k8.to(DEV), v8.to(DEV), ks.to(DEV), vs.to(DEV), lt.to(DEV),
                                        num_splits=num_splits, out_dtype=torch.float32)
-        if page_size % 32 == 0:
+        # the same kernel on the same chunks: at d = 128 the tcgen05 kernel
+        # (128-token chunks) serves contiguous caches and pages of a
+        # multiple of 128 tokens, the mma.sync kernel smaller pages
+        if page_size % (128 if d == 128 else 32) == 0:
             assert torch.equal(out, cout) and torch.equal(lse, clse)
 
 
@@ -151,16 +154,16 @@ def test_paged_gqa_fp8_limits_and_bad_entries():
 
 @pytest.mark.slow
 def test_paged_gqa_fp8_full_size_equals_contiguous():
-    """The 1 GiB GQA workload stored as E4M3 in shuffled 64-token pages:
-    bit-identical to the contiguous E4M3 kernel (the same chunks)."""
+    """The 1 GiB GQA workload stored as E4M3 in shuffled 128-token pages:
+    bit-identical to the contiguous E4M3 kernel (the same kernel and chunks)."""
     w = WORKLOADS["decode_gqa_b8_hq64_hkv8_n32k_d128_bf16"]
     q, k, v, lens = make_inputs(w, device="cuda")
     k8, ks = quantize_e4m3(k)
     v8, vs = quantize_e4m3(v)
     del k, v
     cout, clse = fd.decode_gqa_fp8(q, k8, v8, ks, vs, lens, scale=w.scale, out_dtype=torch.float32)
-    kp, table = to_paged_bytes(k8, 64, seed=5)
-    vp, _ = to_paged_bytes(v8, 64, seed=5)
+    kp, table = to_paged_bytes(k8, 128, seed=5)
+    vp, _ = to_paged_bytes(v8, 128, seed=5)
     del k8, v8
     out, lse = fd.decode_gqa_paged_fp8(q, kp, vp, ks, vs, table, lens, scale=w.scale, out_dtype=torch.float32)
     assert torch.equal(out, cout) and torch.equal(lse, clse)
