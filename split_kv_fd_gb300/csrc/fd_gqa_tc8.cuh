@@ -59,23 +59,33 @@ template <int D> struct Tc8Cfg {
     static constexpr int LINES = 1;
     static constexpr int CHUNK_BYTES = CT * ROW;   // K or V of one chunk
     static constexpr int QP_BYTES = NC * D;        // q parts: NC rows of d bytes
-    static constexpr int NPB = 4;                  // Pp^T buffers (chunk j in j % NPB; even: a group's own)
+    static constexpr int NWG = 2;                  // softmax groups (4 warps each), pairs of chunks in turn
+    static constexpr int NPB = 2 * NWG;            // Pp^T buffers (chunk j in j % NPB)
     static constexpr int PT_BYTES = NC * CT;       // one Pp^T: NC rows of CT bytes
-    static constexpr int NSB = 8;                  // S^T buffers in TMEM (chunk j in j % NSB)
-    static constexpr int TMEM_O = NSB * NC;        // then the two groups' O^T
+    static constexpr int NSB = 12;                 // S^T buffers in TMEM (chunk j in j % NSB)
+    static constexpr int TMEM_O = NSB * NC;        // then the groups' O^T
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int MERGE_PB = 64;
     static constexpr int SCR_BYTES = MERGE_PB * 8 + 2 * MAXG * 4;
     // per group: vote flags [2][4], chunk maxima [4][8]; per segment parity:
-    // l sums [2][4][8] and m [2][8]; the heads' score scales [8]
-    static constexpr int XCH_FLOATS = 2 * 2 * 4 + 2 * 4 * 8 + 2 * (2 * 4 * 8 + 2 * 8) + 8;
+    // l sums [NWG][4][8] and m [NWG][8]; the heads' score scales [8]
+    static constexpr int SEGX = NWG * 4 * 8 + NWG * 8;
+    static constexpr int XCH_FLOATS = NWG * 2 * 4 + NWG * 4 * 8 + 2 * SEGX + 8;
     static constexpr int XCH_BYTES = (XCH_FLOATS * 4 + 15) / 16 * 16;
-    // warps 0-7: two softmax groups; 8, 9: the K and V producers; 10: the
-    // S^T issuer (it allocates TMEM); 11: the P.V issuer
-    static constexpr int WG_THREADS = 128, KPROD_WARP = 8, VPROD_WARP = 9, S_WARP = 10, PV_WARP = 11;
-    static constexpr int THREADS = 384;
+    // warps 0 .. 4 NWG - 1: the softmax groups; then four epilogue warps,
+    // the K and V producers, the S^T issuer (it allocates TMEM) and the P.V
+    // issuer
+    static constexpr int WG_THREADS = 128, EPI_WARP = 4 * NWG, KPROD_WARP = EPI_WARP + 4;
+    static constexpr int VPROD_WARP = KPROD_WARP + 1;
+    static constexpr int S_WARP = KPROD_WARP + 2, PV_WARP = KPROD_WARP + 3;
+    static constexpr int THREADS = 32 * (4 * NWG + 8);
+    // staging of a segment's result for the epilogue (two, by segment
+    // parity): 8 heads x d outputs, then 8 maxima and 8 sums
+    static constexpr int STG_FLOATS = 8 * D + 16;
+    static constexpr int STG_BYTES = 2 * STG_FLOATS * 4;
     // mbarriers: full/empty of the K and V buffers, s_full[NSB],
-    // s_free[NSB], p_full[NPB], pv_done[NPB], q_full, fin (2), seg, wg0, wg[2]
+    // s_free[NSB], p_full[NPB], pv_done[NPB], q_full, fin (2), seg, epi,
+    // wg[NWG], stg_full[2], stg_free[2]
     static constexpr float TAU = 2.f;              // lazy-rescale threshold (base 2)
     static constexpr float PEXP = 8.f - TAU;       // P is taken times 2^PEXP: at most 2^8
     // K and V have rings of their own: a K buffer is free again once S^T of
@@ -84,23 +94,23 @@ template <int D> struct Tc8Cfg {
     // KST K buffers and the rest, the prefix sums of up to BALANCED_MAX_B
     // sequences included (two barriers per buffer)
     static constexpr int KST = 4;
-    static constexpr int NBAR_FIXED = 2 * KST + 2 * NSB + 2 * NPB + 7;
-    static constexpr int FIXED = 1024 + KST * CHUNK_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES +
+    static constexpr int NBAR_FIXED = 2 * KST + 2 * NSB + 2 * NPB + 5 + NWG + 4;
+    static constexpr int FIXED = 1024 + KST * CHUNK_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + STG_BYTES +
                                  NBAR_FIXED * 8 + 16 + (BALANCED_MAX_B + 1) * 8 + BALANCED_MAX_B * 4;
     static constexpr int VST = (227 * 1024 - FIXED) / (CHUNK_BYTES + 16);
     static constexpr int RING_BYTES = (KST + VST) * CHUNK_BYTES;   // K buffers, then V buffers
     static constexpr int NBAR = 2 * VST + NBAR_FIXED;
     static_assert(D == 128, "head dim 128");
     static_assert(VST >= 4, "ring depth");
-    static_assert(1024 + RING_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16 +
+    static_assert(1024 + RING_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + STG_BYTES + NBAR * 8 + 16 +
                           (BALANCED_MAX_B + 1) * 8 + BALANCED_MAX_B * 4 <= 227 * 1024,
                   "shared memory");
-    static_assert(TMEM_O + 2 * NC <= (int)TMEM_COLS, "TMEM columns");
+    static_assert(TMEM_O + NWG * NC <= (int)TMEM_COLS, "TMEM columns");
     static_assert(RING_BYTES % 1024 == 0 && QP_BYTES % 1024 == 0 && PT_BYTES % 1024 == 0, "1024-byte atoms");
 
     static size_t smem_bytes(int decomp, int B)
     {
-        size_t s = 1024 + RING_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16;
+        size_t s = 1024 + RING_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + STG_BYTES + NBAR * 8 + 16;
         if (decomp == DECOMP_BALANCED)
             s += (size_t)(B + 1) * 8 + (size_t)B * 4;
         return s;
@@ -172,64 +182,65 @@ __device__ __forceinline__ void tc8_issue(TmaProducer<C, false> &pr, const GqaPa
     pr.locate(gp, ctx);
 }
 
-// Segment end on softmax group 0: merges the two groups' states per head,
-// then writes out/lse for a whole (b, h), or a workspace partial and, for
-// the last piece to arrive, runs the merge of the pieces.  Thread `row` is
-// TMEM lane row of O^T, i.e. head dimension row.  Returns false if a
-// barrier wait expired.
+// Segment end on softmax group 0 ("FlashDecoding 数学推导" §2.4.2): merges
+// the groups' states per head (l summed over each group's warps at lsum
+// [g][4][8], its reference max at mseg[g][8]) into the staging buffer: the
+// normalised output of head h at stg_o[h * D + row] (thread `row` = TMEM
+// lane of O^T = head dimension), and the head's base-2 max and sum at
+// stg_ml[h], stg_ml[8 + h].  The epilogue warps take it from there.
 template <int D>
-__device__ __noinline__ bool tc8_segment_end(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int gv,
-                                             long long qrow0, long long bhv, const float *lsum, const float *mseg,
-                                             float vsc, int row, int lane, int tid, uint32_t tl, uint32_t *misc,
-                                             unsigned char *scratch, WarpBar &wb)
+__device__ __forceinline__ void tc8_seg_merge(const float *lsum, const float *mseg, float vsc, int row, uint32_t tl,
+                                              float *stg_o, float *stg_ml)
 {
     using C = Tc8Cfg<D>;
-    const SplitParams &p = gp.s;
-    const int G = gp.G;
-    float f0[8], f1[8], Mh[8], Lh[8];
-    bool need0 = false, need1 = false;
+    constexpr int NWG = C::NWG;
+    float Mh[8], Lh[8], oh[8];
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
-        const float l0 = lsum[h] + lsum[8 + h] + lsum[16 + h] + lsum[24 + h];
-        const float l1 = lsum[32 + h] + lsum[40 + h] + lsum[48 + h] + lsum[56 + h];
-        const float m0 = mseg[h], m1 = mseg[8 + h];
-        const float M = fmaxf(l0 > 0.f ? m0 : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
-        const float a0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
-        const float a1 = l1 > 0.f ? ex2(m1 - M) : 0.f;
-        const float L = a0 * l0 + a1 * l1;
-        f0[h] = L > 0.f ? a0 / L * vsc : 0.f;
-        f1[h] = L > 0.f ? a1 / L * vsc : 0.f;
-        need0 = need0 || l0 > 0.f;
-        need1 = need1 || l1 > 0.f;
-        Mh[h] = M;
-        Lh[h] = L * pow2i(-(int)C::PEXP);   // P was taken times 2^PEXP
-    }
-    float o0[32], o1[32];
-    if (need0)
-        tmem_ld32(tl + (uint32_t)C::TMEM_O, o0);
-    if (need1)
-        tmem_ld32(tl + (uint32_t)(C::TMEM_O + C::NC), o1);
-    tmem_wait_ld();
-    tc_fence_before();
-    const int len = (p.decomp == DECOMP_BALANCED) ? ctx.lenS[cs.b] : clamp_len(p, cs.b);
-    bool complete;
-    long long slot;
-    tc_seg_dest(p, cs, bhv, len, complete, slot);
+        float M = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-        if (h < gv) {
-            float o = 0.f;
-            if (need0 && f0[h] != 0.f)
-                o += f0[h] * (o0[h] + 0.0625f * o0[8 + h] + 0.00390625f * o0[16 + h]);
-            if (need1 && f1[h] != 0.f)
-                o += f1[h] * (o1[h] + 0.0625f * o1[8 + h] + 0.00390625f * o1[16 + h]);
-            if (complete)
-                store_out(p.out, (qrow0 + h) * D + row, p.out_dtype, o);
-            else
-                p.ws_o[(slot * G + h) * D + row] = o;
+        for (int g = 0; g < NWG; ++g) {
+            const float lg = lsum[g * 32 + h] + lsum[g * 32 + 8 + h] + lsum[g * 32 + 16 + h] + lsum[g * 32 + 24 + h];
+            if (lg > 0.f)
+                M = fmaxf(M, mseg[g * 8 + h]);
         }
+        float L = 0.f;
+#pragma unroll
+        for (int g = 0; g < NWG; ++g) {
+            const float lg = lsum[g * 32 + h] + lsum[g * 32 + 8 + h] + lsum[g * 32 + 16 + h] + lsum[g * 32 + 24 + h];
+            if (lg > 0.f)
+                L += ex2(mseg[g * 8 + h] - M) * lg;
+        }
+        Mh[h] = M;
+        Lh[h] = L;
+        oh[h] = 0.f;
     }
-    if (row < gv) {
+    // each group's O^T (one TMEM load per group), weighted into oh
+#pragma unroll 1
+    for (int g = 0; g < NWG; ++g) {
+        bool need = false;
+        float f[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            const float lg = lsum[g * 32 + h] + lsum[g * 32 + 8 + h] + lsum[g * 32 + 16 + h] + lsum[g * 32 + 24 + h];
+            f[h] = (lg > 0.f && Lh[h] > 0.f) ? ex2(mseg[g * 8 + h] - Mh[h]) / Lh[h] * vsc : 0.f;
+            need = need || f[h] != 0.f;
+        }
+        if (!need)   // the same for every thread: the values come from shared memory
+            continue;
+        float o[32];
+        tmem_ld32(tl + (uint32_t)(C::TMEM_O + g * C::NC), o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+            if (f[h] != 0.f)
+                oh[h] += f[h] * (o[h] + 0.0625f * o[8 + h] + 0.00390625f * o[16 + h]);
+    }
+    tc_fence_before();
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+        stg_o[h * D + row] = oh[h];
+    if (row < 8) {
         float M = Mh[0], L = Lh[0];
 #pragma unroll
         for (int h = 1; h < 8; ++h)
@@ -237,12 +248,47 @@ __device__ __noinline__ bool tc8_segment_end(const GqaParams &gp, const Ctx ctx,
                 M = Mh[h];
                 L = Lh[h];
             }
+        stg_ml[row] = M;
+        stg_ml[8 + row] = L * pow2i(-(int)C::PEXP);   // P was taken times 2^PEXP
+    }
+}
+
+// The epilogue of a segment, on the epilogue warps (tid 0..127), from the
+// staging buffer: out/lse for a whole (b, h), or a workspace partial and,
+// for the last piece to arrive, the merge of the pieces.  Its global-memory
+// round trips (the arrival counter, the pieces' partials) overlap the next
+// segment's streaming.  Returns false if a barrier wait expired.
+template <int D>
+__device__ __noinline__ bool tc8_epilogue(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice,
+                                          const float *stg_o, const float *stg_ml, int lane, int tid, uint32_t *misc,
+                                          unsigned char *scratch, WarpBar &wb)
+{
+    using C = Tc8Cfg<D>;
+    const SplitParams &p = gp.s;
+    const int G = gp.G;
+    const int vh = cs.h * gp.NG + slice;
+    const long long bhv = (long long)cs.b * p.H * gp.NG + vh;
+    const int gv = vh_count(gp, vh);
+    const long long qrow0 = vh_qrow0(gp, cs.b, vh);
+    const int len = (p.decomp == DECOMP_BALANCED) ? ctx.lenS[cs.b] : clamp_len(p, cs.b);
+    bool complete;
+    long long slot;
+    tc_seg_dest(p, cs, bhv, len, complete, slot);
+    for (int h = 0; h < gv; ++h) {
+        const float o = stg_o[h * D + tid];
+        if (complete)
+            store_out(p.out, (qrow0 + h) * D + tid, p.out_dtype, o);
+        else
+            p.ws_o[(slot * G + h) * D + tid] = o;
+    }
+    if (tid < gv) {
+        const float M = stg_ml[tid], L = stg_ml[8 + tid];
         const bool nonempty = L > 0.f;
         if (complete) {
             if (p.lse)
-                p.lse[qrow0 + row] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
+                p.lse[qrow0 + tid] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
         } else {
-            const long long r = slot * G + row;
+            const long long r = slot * G + tid;
             p.ws_ml[2 * r] = nonempty ? M : -INFINITY;
             p.ws_ml[2 * r + 1] = L;
         }
@@ -271,11 +317,13 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
     const uint32_t pbuf = qbuf + C::QP_BYTES;
     unsigned char *scratch = smem + C::RING_BYTES + C::QP_BYTES + C::NPB * C::PT_BYTES;
     float *xch = reinterpret_cast<float *>(scratch + C::SCR_BYTES);
-    int *flg = reinterpret_cast<int *>(xch);      // [2 groups][2][4 warps]
-    float *red = xch + 16;                        // [2 groups][4 warps][8 heads]
-    float *segx = red + 64;                       // [2 parities][l sums [2][4][8], m [2][8]]
-    float *fhs = segx + 2 * 80;                   // [8] score scales of the segment's heads
-    uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::SCR_BYTES + C::XCH_BYTES);
+    constexpr int NWG = C::NWG;
+    int *flg = reinterpret_cast<int *>(xch);      // [NWG groups][2][4 warps]
+    float *red = xch + NWG * 8;                   // [NWG groups][4 warps][8 heads]
+    float *segx = red + NWG * 32;                 // [2 parities][l sums [NWG][4][8], m [NWG][8]]
+    float *fhs = segx + 2 * C::SEGX;              // [8] score scales of the segment's heads
+    float *stg = reinterpret_cast<float *>(scratch + C::SCR_BYTES + C::XCH_BYTES);   // [2][STG_FLOATS]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::SCR_BYTES + C::XCH_BYTES + C::STG_BYTES);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBAR);   // [0] TMEM base, [1] flag
     long long *cumH = reinterpret_cast<long long *>(misc + 4);
     int *lenS = reinterpret_cast<int *>(cumH + p.B + 1);
@@ -301,7 +349,9 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
     const uint32_t SEGBAR = bar0 + 8u * (B1 + 3);
     const uint32_t WG0BAR = bar0 + 8u * (B1 + 4);
     auto WGBAR = [&](int g) { return bar0 + 8u * (uint32_t)(B1 + 5 + g); };
-    static_assert(B1 + 7 == C::NBAR, "barrier count");
+    auto STGF = [&](int i) { return bar0 + 8u * (uint32_t)(B1 + 5 + NWG + i); };
+    auto STGE = [&](int i) { return bar0 + 8u * (uint32_t)(B1 + 7 + NWG + i); };
+    static_assert(B1 + 9 + NWG == C::NBAR, "barrier count");
 
     if (tid == 0) {
         for (int s = 0; s < KST; ++s) {
@@ -323,10 +373,14 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         mbar_init(QFULL, 4);          // group 0 has written the q parts and score scales
         mbar_init(FINS, 1);           // the MMA issuers' last commits
         mbar_init(FINP, 1);
-        mbar_init(SEGBAR, 8);         // both groups at a segment end
-        mbar_init(WG0BAR, 4);         // group 0 (arrival and merge)
-        mbar_init(WGBAR(0), 4);       // each group's vote and max exchange
-        mbar_init(WGBAR(1), 4);
+        mbar_init(SEGBAR, 4 * NWG);   // every softmax group at a segment end
+        mbar_init(WG0BAR, 4);         // the epilogue warps (arrival and merge)
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(STGF(i), 4);    // group 0's warps have staged a segment's result
+            mbar_init(STGE(i), 4);    // the epilogue warps are done with it
+        }
+        for (int g = 0; g < NWG; ++g)
+            mbar_init(WGBAR(g), 4);   // each group's vote and max exchange
         prefetch_tmap(&gp.tmk);
         prefetch_tmap(&gp.tmv);
     }
@@ -466,8 +520,8 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                     }
                     tc_fence_after();
                     // the pair's group; its first chunk of the segment overwrites O^T
-                    const int g = (int)((pp0 + c / 2) & 1);
-                    const bool first = c < 4 && (c & 1) == 0;
+                    const int g = (int)((pp0 + c / 2) % NWG);
+                    const bool first = c < 2 * NWG && (c & 1) == 0;
                     const uint32_t vb = ring + (uint32_t)((KST + jp % VST) * C::CHUNK_BYTES);
                     const uint32_t pb = pbuf + (uint32_t)((jp % NPB) * C::PT_BYTES);
 #pragma unroll
@@ -490,6 +544,32 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 dead = true;
         }
         __syncwarp();
+    } else if (w >= C::EPI_WARP) {
+        // ------------------------------------------------------------ epilogue
+        // each segment's staged result to out/lse or the workspace, the
+        // arrival and, for the last piece, the merge of the pieces
+        const int etid = tid - 32 * C::EPI_WARP;
+        WarpBar wb{WG0BAR, 0u};
+        int si = 0;
+        Seg cs;
+        seg_first(p, ctx, cs);
+#pragma unroll 1
+        while (cs.valid && !dead) {
+            const float *sg = stg + (si & 1) * C::STG_FLOATS;
+            if (!mbar_wait_bounded(STGF(si & 1), (uint32_t)((si >> 1) & 1))) {
+                dead = true;
+                break;
+            }
+            if (!tc8_epilogue<D>(gp, ctx, cs, slice, sg, sg + 8 * D, lane, etid, misc, scratch, wb)) {
+                dead = true;
+                break;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(STGE(si & 1));
+            ++si;
+            seg_next(p, ctx, cs);
+        }
     } else {
         // ------------------------------------------------------------ softmax groups
         const int wg = w >> 2;             // softmax group
@@ -497,7 +577,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         const int row = tid & 127;         // token of the chunk (S^T) = head dim (O^T) = TMEM lane
         const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
         const uint32_t ocol = (uint32_t)(C::TMEM_O + wg * NC);
-        WarpBar sb{SEGBAR, 0u}, wb{WG0BAR, 0u}, gb{WGBAR(wg), 0u};
+        WarpBar sb{SEGBAR, 0u}, gb{WGBAR(wg), 0u};
         long long nw = 0;   // chunks this group has handed to P.V
         long long j0 = 0;   // the CTA's chunk index of the segment's first chunk
         long long p0 = 0;   // pairs of chunks before the segment
@@ -509,9 +589,10 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         while (cs.valid && !dead) {
             const long long n = seg_chunks<C::CT>(cs);
             const int vh = cs.h * gp.NG + slice;
-            const long long bhv = (long long)cs.b * p.H * gp.NG + vh;
             const int gv = vh_count(gp, vh);
             const long long qrow0 = vh_qrow0(gp, cs.b, vh);
+            // V's dequantisation scale, applied at the segment end
+            const float vsc = wg == 0 ? __ldg(gp.v_scale + cs.b * p.H + cs.h) : 0.f;
             float m[8], l[8], fh[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
@@ -578,9 +659,9 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             long long jprev = 0;
             const long long npairs = (n + 1) / 2;
             // the segment's chunks in pairs (2i, 2i + 1), pair i to group
-            // (pairs before the segment + i) % 2; both chunks share one vote
+            // (pairs before the segment + i) % NWG; both chunks share one vote
 #pragma unroll 1
-            for (long long pi = (long long)((wg - (int)(p0 & 1)) & 1); pi < npairs; pi += 2) {
+            for (long long pi = (long long)(((wg - (int)(p0 % NWG)) % NWG + NWG) % NWG); pi < npairs; pi += NWG) {
                 const long long c0 = 2 * pi;
                 const bool two = c0 + 1 < n;
                 const long long j = j0 + c0;
@@ -750,8 +831,9 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             p0 += (n + 1) / 2;
 
             // ---- segment end: each group's l per head over its 128 tokens,
-            // then group 0 merges the two states ----
-            float *sx = segx + (k & 1) * 80;   // l sums [2][4][8], then m [2][8]
+            // then group 0 merges the groups' states into a staging buffer
+            // for the epilogue warps and goes on ----
+            float *sx = segx + (k & 1) * C::SEGX;   // l sums [NWG][4][8], then m [NWG][8]
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
                 float v = had ? l[h] : 0.f;
@@ -761,7 +843,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 if (lane == 0)
                     sx[(wg * 4 + wq) * 8 + h] = v;
                 if (wq == 0 && lane == 0)
-                    sx[64 + wg * 8 + h] = had ? m[h] : -INFINITY;
+                    sx[NWG * 32 + wg * 8 + h] = had ? m[h] : -INFINITY;
             }
             ++k;
             if (!sb.sync(lane)) {
@@ -769,12 +851,16 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 break;
             }
             if (wg == 0) {
-                const float vsc = __ldg(gp.v_scale + cs.b * p.H + cs.h);
-                if (!tc8_segment_end<D>(gp, ctx, cs, slice, gv, qrow0, bhv, sx, sx + 64, vsc, row, lane, tid, tl,
-                                        misc, scratch, wb)) {
+                const int si = k - 1;   // this segment's staging buffer: si % 2
+                if (si >= 2 && !mbar_wait_bounded(STGE(si & 1), (uint32_t)(((si >> 1) - 1) & 1))) {
                     dead = true;
                     break;
                 }
+                tc8_seg_merge<D>(sx, sx + NWG * 32, vsc, row, tl, stg + (si & 1) * C::STG_FLOATS,
+                                 stg + (si & 1) * C::STG_FLOATS + 8 * D);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(STGF(si & 1));
             }
             seg_next(p, ctx, cs);
         }
