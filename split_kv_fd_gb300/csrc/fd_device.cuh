@@ -109,6 +109,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     return __all_sync(FULL_MASK, ok);
 }
 
+// One try at phase `parity` of barrier `bar` that may suspend the thread in
+// hardware for up to `hint_ns`; it resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Bounded wait for a phase that may take long (a whole segment of
 // streaming), for a warp that must not slow the warps doing the work: each
 // try suspends the warp in hardware for up to `hint_ns` and resumes it as
@@ -118,15 +133,7 @@ __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t p
     const unsigned long long t0 = global_ns();
     bool ok = false;
     for (unsigned i = 0; i < WAIT_LIMIT_POLLS; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity), "r"(hint_ns)
-            : "memory");
-        if (done) {
+        if (mbar_try_wait_hint(bar, parity, hint_ns)) {
             ok = true;
             break;
         }
@@ -134,6 +141,21 @@ __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t p
             break;
     }
     return __all_sync(FULL_MASK, ok);
+}
+
+// The same for one thread on its own (no warp vote).
+__device__ __forceinline__ bool mbar_wait_bounded_sleep_thread(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    if (mbar_try_wait_hint(bar, parity, hint_ns))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (unsigned i = 0; i < WAIT_LIMIT_POLLS; ++i) {
+        if (mbar_try_wait_hint(bar, parity, hint_ns))
+            return true;
+        if (global_ns() - t0 > WAIT_LIMIT_NS)
+            break;
+    }
+    return false;
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.

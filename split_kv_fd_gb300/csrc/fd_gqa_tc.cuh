@@ -114,12 +114,13 @@ template <typename T, int D> struct TcCfg {
 struct WarpBar {
     uint32_t bar;
     uint32_t phase;
+    uint32_t hint_ns = 0;   // > 0: the waiting warps are suspended in hardware meanwhile
     __device__ __forceinline__ bool sync(int lane)
     {
         __syncwarp();
         if (lane == 0)
             mbar_arrive(bar);
-        const bool ok = mbar_wait_bounded(bar, phase);
+        const bool ok = hint_ns ? mbar_wait_bounded_sleep(bar, phase, hint_ns) : mbar_wait_bounded(bar, phase);
         phase ^= 1u;
         return ok;
     }

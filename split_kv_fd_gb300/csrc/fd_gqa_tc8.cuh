@@ -86,6 +86,10 @@ template <int D> struct Tc8Cfg {
     // mbarriers: full/empty of the K and V buffers, s_full[NSB],
     // s_free[NSB], p_full[NPB], pv_done[NPB], q_full, fin (2), seg, epi,
     // wg[NWG], stg_full[2], stg_free[2]
+    // every wait suspends the waiting thread in hardware (woken when the
+    // phase completes) rather than polling, so that waiting warps leave the
+    // issue slots to the working ones
+    static constexpr uint32_t SLEEP_NS = 100000;
     static constexpr float TAU = 2.f;              // lazy-rescale threshold (base 2)
     static constexpr float PEXP = 8.f - TAU;       // P is taken times 2^PEXP: at most 2^8
     // K and V have rings of their own: a K buffer is free again once S^T of
@@ -439,7 +443,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             while (pr.have) {
                 const int b = issued % nb;
                 if (issued >= nb &&
-                    !mbar_wait_bounded_thread(isk ? EMPTYK(b) : EMPTYV(b), (uint32_t)(((issued / nb) - 1) & 1))) {
+                    !mbar_wait_bounded_sleep_thread(isk ? EMPTYK(b) : EMPTYV(b), (uint32_t)(((issued / nb) - 1) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             }
             // no copy may be in flight when the CTA ends: the last fill of each buffer
             for (int i = max(0, issued - nb); i < issued; ++i)
-                mbar_wait_bounded_thread(isk ? FULLK(i % nb) : FULLV(i % nb), (uint32_t)((i / nb) & 1));
+                mbar_wait_bounded_sleep_thread(isk ? FULLK(i % nb) : FULLV(i % nb), (uint32_t)((i / nb) & 1), C::SLEEP_NS);
         }
         __syncwarp();
     } else if (w == C::S_WARP) {
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             while (ss.valid && !dead) {
                 const long long n = seg_chunks<C::CT>(ss);
                 if (n > 0) {
-                    if (!mbar_wait_bounded_thread(QFULL, (uint32_t)(kq & 1))) {
+                    if (!mbar_wait_bounded_sleep_thread(QFULL, (uint32_t)(kq & 1), C::SLEEP_NS)) {
                         dead = true;
                         break;
                     }
@@ -476,8 +480,8 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
 #pragma unroll 1
                 for (long long c = 0; c < n; ++c, ++js) {
                     const int st = (int)(js % KST), sb = (int)(js % NSB);
-                    if (!mbar_wait_bounded_thread(FULLK(st), (uint32_t)((js / KST) & 1)) ||
-                        (js >= NSB && !mbar_wait_bounded_thread(SFREE(sb), (uint32_t)(((js / NSB) - 1) & 1)))) {
+                    if (!mbar_wait_bounded_sleep_thread(FULLK(st), (uint32_t)((js / KST) & 1), C::SLEEP_NS) ||
+                        (js >= NSB && !mbar_wait_bounded_sleep_thread(SFREE(sb), (uint32_t)(((js / NSB) - 1) & 1), C::SLEEP_NS))) {
                         dead = true;
                         break;
                     }
@@ -497,7 +501,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             }
             // every MMA this thread issued has completed before TMEM is freed
             tc_commit(FINS);
-            if (!mbar_wait_bounded_thread(FINS, 0))
+            if (!mbar_wait_bounded_sleep_thread(FINS, 0, C::SLEEP_NS))
                 dead = true;
         }
         __syncwarp();
@@ -513,8 +517,8 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 const long long n = seg_chunks<C::CT>(sp);
 #pragma unroll 1
                 for (long long c = 0; c < n; ++c, ++jp) {
-                    if (!mbar_wait_bounded_thread(PFULL((int)(jp % NPB)), (uint32_t)((jp / NPB) & 1)) ||
-                        !mbar_wait_bounded_thread(FULLV((int)(jp % VST)), (uint32_t)((jp / VST) & 1))) {
+                    if (!mbar_wait_bounded_sleep_thread(PFULL((int)(jp % NPB)), (uint32_t)((jp / NPB) & 1), C::SLEEP_NS) ||
+                        !mbar_wait_bounded_sleep_thread(FULLV((int)(jp % VST)), (uint32_t)((jp / VST) & 1), C::SLEEP_NS)) {
                         dead = true;
                         break;
                     }
@@ -540,7 +544,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 seg_next(p, ctx, sp);
             }
             tc_commit(FINP);
-            if (!mbar_wait_bounded_thread(FINP, 0))
+            if (!mbar_wait_bounded_sleep_thread(FINP, 0, C::SLEEP_NS))
                 dead = true;
         }
         __syncwarp();
@@ -549,14 +553,14 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         // each segment's staged result to out/lse or the workspace, the
         // arrival and, for the last piece, the merge of the pieces
         const int etid = tid - 32 * C::EPI_WARP;
-        WarpBar wb{WG0BAR, 0u};
+        WarpBar wb{WG0BAR, 0u, C::SLEEP_NS};
         int si = 0;
         Seg cs;
         seg_first(p, ctx, cs);
 #pragma unroll 1
         while (cs.valid && !dead) {
             const float *sg = stg + (si & 1) * C::STG_FLOATS;
-            if (!mbar_wait_bounded(STGF(si & 1), (uint32_t)((si >> 1) & 1))) {
+            if (!mbar_wait_bounded_sleep(STGF(si & 1), (uint32_t)((si >> 1) & 1), C::SLEEP_NS)) {
                 dead = true;
                 break;
             }
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         const int row = tid & 127;         // token of the chunk (S^T) = head dim (O^T) = TMEM lane
         const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
         const uint32_t ocol = (uint32_t)(C::TMEM_O + wg * NC);
-        WarpBar sb{SEGBAR, 0u}, gb{WGBAR(wg), 0u};
+        WarpBar sb{SEGBAR, 0u, C::SLEEP_NS}, gb{WGBAR(wg), 0u, C::SLEEP_NS};
         long long nw = 0;   // chunks this group has handed to P.V
         long long j0 = 0;   // the CTA's chunk index of the segment's first chunk
         long long p0 = 0;   // pairs of chunks before the segment
@@ -646,7 +650,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                     if (lane == 0)
                         mbar_arrive(QFULL);
                 }
-                if (!mbar_wait_bounded(QFULL, (uint32_t)(kq & 1))) {
+                if (!mbar_wait_bounded_sleep(QFULL, (uint32_t)(kq & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
@@ -666,8 +670,8 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 const bool two = c0 + 1 < n;
                 const long long j = j0 + c0;
                 const int b0 = (int)(j % NSB), b1 = (int)((j + 1) % NSB);
-                if (!mbar_wait_bounded(SFULL(b0), (uint32_t)((j / NSB) & 1)) ||
-                    (two && !mbar_wait_bounded(SFULL(b1), (uint32_t)(((j + 1) / NSB) & 1)))) {
+                if (!mbar_wait_bounded_sleep(SFULL(b0), (uint32_t)((j / NSB) & 1), C::SLEEP_NS) ||
+                    (two && !mbar_wait_bounded_sleep(SFULL(b1), (uint32_t)(((j + 1) / NSB) & 1), C::SLEEP_NS))) {
                     dead = true;
                     break;
                 }
@@ -743,7 +747,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                     // the group's O^T columns of the heads that moved, once
                     // its previous P.V is done (every warp its 32 lanes)
                     if (had && grow) {
-                        if (!mbar_wait_bounded(PVD((int)(jprev % NPB)), (uint32_t)((jprev / NPB) & 1))) {
+                        if (!mbar_wait_bounded_sleep(PVD((int)(jprev % NPB)), (uint32_t)((jprev / NPB) & 1), C::SLEEP_NS)) {
                             dead = true;
                             break;
                         }
@@ -761,7 +765,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 // the Pp^T buffers of the pair are free once P.V of chunk
                 // j + 1 - NPB (or j - NPB) is done: P.V completes in order
                 const long long jw = j + (two ? 1 : 0) - NPB;
-                if (jw >= 0 && !mbar_wait_bounded(PVD((int)(jw % NPB)), (uint32_t)((jw / NPB) & 1))) {
+                if (jw >= 0 && !mbar_wait_bounded_sleep(PVD((int)(jw % NPB)), (uint32_t)((jw / NPB) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
@@ -792,7 +796,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                     // refilled before P.V of the chunk)
                     const int ntq = q ? ntok1 : ntok0;
                     if (ntq < C::CT &&
-                        !mbar_wait_bounded(FULLV((int)(jq % VST)), (uint32_t)((jq / VST) & 1))) {
+                        !mbar_wait_bounded_sleep(FULLV((int)(jq % VST)), (uint32_t)((jq / VST) & 1), C::SLEEP_NS)) {
                         dead = true;
                         break;
                     }
@@ -821,7 +825,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 break;
             if (had) {
                 // the group's last P.V: its O^T is final
-                if (!mbar_wait_bounded(PVD((int)(jprev % NPB)), (uint32_t)((jprev / NPB) & 1))) {
+                if (!mbar_wait_bounded_sleep(PVD((int)(jprev % NPB)), (uint32_t)((jprev / NPB) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
@@ -852,7 +856,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             }
             if (wg == 0) {
                 const int si = k - 1;   // this segment's staging buffer: si % 2
-                if (si >= 2 && !mbar_wait_bounded(STGE(si & 1), (uint32_t)(((si >> 1) - 1) & 1))) {
+                if (si >= 2 && !mbar_wait_bounded_sleep(STGE(si & 1), (uint32_t)(((si >> 1) - 1) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
