@@ -93,6 +93,9 @@ template <typename T, int D> struct TcCfg {
     // p_full[2], o_full[2], q_full, fin, seg (both groups), wg0 (group 0)
     static constexpr int NBAR = 2 * STAGES + 2 * NSB + 8;
     static constexpr float TAU = 8.f;              // lazy-rescale threshold (base 2)
+    // every wait suspends the waiting thread in hardware (woken when the
+    // phase completes) rather than polling
+    static constexpr uint32_t SLEEP_NS = 100000;
     static_assert(D == 64 || D == 128, "head dim 64 or 128");
     static_assert(CT == 64, "an S buffer holds P_hi and P_lo in its 64 columns");
     static_assert(TMEM_O + 2 * D <= (int)TMEM_COLS, "TMEM columns");
@@ -519,7 +522,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
 #pragma unroll 1
         for (;;) {
             const int s = issued % ST;
-            if (issued >= ST && !mbar_wait_bounded(EMPTY(s), ((issued / ST) - 1) & 1)) {
+            if (issued >= ST && !mbar_wait_bounded_sleep(EMPTY(s), ((issued / ST) - 1) & 1, C::SLEEP_NS)) {
                 dead = true;
                 break;
             }
@@ -529,7 +532,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         }
         // no copy may be in flight when the CTA ends: the last fill of each stage
         for (int i = max(0, issued - ST); i < issued; ++i)
-            mbar_wait_bounded(FULL(i % ST), (i / ST) & 1);
+            mbar_wait_bounded_sleep(FULL(i % ST), (i / ST) & 1, C::SLEEP_NS);
     } else if (w == C::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -542,9 +545,9 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             auto issue_s = [&](long long j) -> bool {
                 const int s = (int)(j % ST);
                 const int sb = (int)(j % NSB);
-                if (!mbar_wait_bounded_thread(FULL(s), (uint32_t)((j / ST) & 1)))
+                if (!mbar_wait_bounded_sleep_thread(FULL(s), (uint32_t)((j / ST) & 1), C::SLEEP_NS))
                     return false;
-                if (j >= NSB && !mbar_wait_bounded_thread(SFREE(sb), (uint32_t)(((j / NSB) - 1) & 1)))
+                if (j >= NSB && !mbar_wait_bounded_sleep_thread(SFREE(sb), (uint32_t)(((j / NSB) - 1) & 1), C::SLEEP_NS))
                     return false;
                 tc_fence_after();
                 const uint32_t kb = ring + (uint32_t)(s * C::STAGE_BYTES);
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             while (cs.valid && !dead) {
                 const long long n = seg_chunks<C::CT>(cs);
                 if (n > 0) {
-                    if (!mbar_wait_bounded_thread(QFULL, (uint32_t)(k & 1))) {
+                    if (!mbar_wait_bounded_sleep_thread(QFULL, (uint32_t)(k & 1), C::SLEEP_NS)) {
                         dead = true;
                         break;
                     }
@@ -590,7 +593,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                             break;
                         }
                         const int g = (int)(j & 1);
-                        if (!mbar_wait_bounded_thread(PFULL(g), (uint32_t)(pw[g] & 1))) {
+                        if (!mbar_wait_bounded_sleep_thread(PFULL(g), (uint32_t)(pw[g] & 1), C::SLEEP_NS)) {
                             dead = true;
                             break;
                         }
@@ -617,7 +620,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             }
             // every MMA this thread issued has completed before TMEM is freed
             tc_commit(FIN);
-            if (!mbar_wait_bounded_thread(FIN, 0))
+            if (!mbar_wait_bounded_sleep_thread(FIN, 0, C::SLEEP_NS))
                 dead = true;
         }
         __syncwarp();
@@ -627,7 +630,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         const int row = tid & 127;         // query head within the slice = TMEM lane
         const uint32_t tl = tmem + ((uint32_t)((w & 3) * 32) << 16);
         const uint32_t ocol = (uint32_t)(C::TMEM_O + wg * D);
-        WarpBar sb{SEGBAR, 0u}, wb{WG0BAR, 0u};
+        WarpBar sb{SEGBAR, 0u, C::SLEEP_NS}, wb{WG0BAR, 0u, C::SLEEP_NS};
         long long nw = 0;   // chunks this group has handed to P.V
         long long j0 = 0;   // the CTA's chunk index of the segment's first chunk
         int k = 0;          // segments so far
@@ -669,7 +672,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             for (long long c = (long long)(wg ^ (int)(j0 & 1)); c < n; c += 2) {
                 const long long j = j0 + c;
                 const int b = (int)(j % NSB);
-                if (!mbar_wait_bounded(SFULL(b), (uint32_t)((j / NSB) & 1))) {
+                if (!mbar_wait_bounded_sleep(SFULL(b), (uint32_t)((j / NSB) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
@@ -707,7 +710,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 // the group's previous chunk: its P.V is done, so O is final
                 // and its S/P buffer free for the chunk four ahead
                 if (had) {
-                    if (!mbar_wait_bounded(OFULL(wg), (uint32_t)((nw - 1) & 1))) {
+                    if (!mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
                         dead = true;
                         break;
                     }
@@ -793,7 +796,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             if (dead)
                 break;
             if (had) {
-                if (!mbar_wait_bounded(OFULL(wg), (uint32_t)((nw - 1) & 1))) {
+                if (!mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
