@@ -159,61 +159,36 @@ __device__ __forceinline__ void store_out4(void *out, long long idx, int out_dty
     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + idx) = make_uint2(a, b);
 }
 
-// One batch of the last arriver's merge, on softmax group 0: the m/l/o
-// merge ("FlashDecoding 数学推导" §2.4.2) of the n <= MERGE_PB workspace
-// partials whose slots are in ss[0..n-1], for each of the Gv query rows.
-// First each head's max M and sum L over the pieces, then every output
-// element sums its pieces with their weights exp(m_i - M) l_i formed on the
-// fly, many loads in flight (the merge sits on the CTA's critical path: the
-// next segment waits for it).  The result goes to out/lse, or, when `into`
-// >= 0, back into the workspace slot `into` as a normalised partial (o, m,
-// l) that a later batch merges.  Returns false if a barrier wait expired.
+// One batch of the last arriver's merge, on 128 threads: the m/l/o merge
+// ("FlashDecoding 数学推导" §2.4.2) of the n <= MERGE_PB workspace partials
+// whose slots are in ss[0..n-1], for each of the Gv query rows.  Each thread
+// takes four elements of a head at a time and the pieces' partials and
+// (m, l) together, many loads in flight, with a running max and sum for its
+// head: acc and L scaled by exp2(M_old - M_new) when the max grows, so one
+// round trip to memory serves the batch (the merge sits on the CTA's
+// critical path).  The result goes to out/lse, or, when `into` >= 0, back
+// into the workspace slot `into` as a normalised partial (o, m, l) that a
+// later batch merges (each head's (m, l) through sM, sL, written once every
+// thread has read the slot's).  Returns false if a barrier wait expired.
 template <int D>
 __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int Gv, long long qrow0, const long long *ss,
                                                int n, long long into, float *sM, float *sL, int tid, WarpBar &wb)
 {
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);   // (m, l) per workspace row
-    if (tid < Gv) {
-        float M = -INFINITY;
-        for (int i0 = 0; i0 < n; i0 += 8) {
-            float2 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                v[u] = __ldcg(ml + ss[min(i0 + u, n - 1)] * G + tid);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (i0 + u < n && v[u].y > 0.f)
-                    M = fmaxf(M, v[u].x);
-        }
-        float L = 0.f;
-        for (int i0 = 0; i0 < n; i0 += 8) {
-            float2 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                v[u] = __ldcg(ml + ss[min(i0 + u, n - 1)] * G + tid);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (i0 + u < n && v[u].y > 0.f)
-                    L += ex2(v[u].x - M) * v[u].y;
-        }
-        sM[tid] = M;
-        sL[tid] = L;
-    }
-    if (!wb.sync(tid & 31))
-        return false;
     constexpr int GB = 2, PB = 8;   // groups of 4 elements, pieces per round
     const int ngrp = Gv * D / 4;
     for (int base = 0; base < ngrp; base += 128 * GB) {
         float4 acc[GB];
         int gg[GB], dd[GB];
-        float Mg[GB];
+        float Mr[GB], Lr[GB];
 #pragma unroll
         for (int e = 0; e < GB; ++e) {
             acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
             const int grp = min(base + e * 128 + tid, ngrp - 1);
             gg[e] = grp * 4 / D;
             dd[e] = grp * 4 % D;
-            Mg[e] = sM[gg[e]];
+            Mr[e] = -INFINITY;
+            Lr[e] = 0.f;
         }
         for (int i0 = 0; i0 < n; i0 += PB) {
             float4 v[GB][PB];
@@ -232,11 +207,15 @@ __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int 
 #pragma unroll
                 for (int e = 0; e < GB; ++e) {
                     if (i0 + u < n && w[e][u].y > 0.f) {
-                        const float wt = ex2(w[e][u].x - Mg[e]) * w[e][u].y;
-                        acc[e].x = fmaf(wt, v[e][u].x, acc[e].x);
-                        acc[e].y = fmaf(wt, v[e][u].y, acc[e].y);
-                        acc[e].z = fmaf(wt, v[e][u].z, acc[e].z);
-                        acc[e].w = fmaf(wt, v[e][u].w, acc[e].w);
+                        const float mn = fmaxf(Mr[e], w[e][u].x);
+                        const float a = ex2(Mr[e] - mn);   // 0 for the first piece
+                        const float b = ex2(w[e][u].x - mn) * w[e][u].y;
+                        acc[e].x = fmaf(b, v[e][u].x, acc[e].x * a);
+                        acc[e].y = fmaf(b, v[e][u].y, acc[e].y * a);
+                        acc[e].z = fmaf(b, v[e][u].z, acc[e].z * a);
+                        acc[e].w = fmaf(b, v[e][u].w, acc[e].w * a);
+                        Lr[e] = fmaf(Lr[e], a, b);
+                        Mr[e] = mn;
                     }
                 }
             }
@@ -244,11 +223,12 @@ __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int 
 #pragma unroll
         for (int e = 0; e < GB; ++e) {
             const int grp = base + e * 128 + tid;
-            if (grp < ngrp) {
-                const int g = gg[e], dim = dd[e];
-                const float L = sL[g];
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                const float4 o = make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv);
+            const bool mine = grp < ngrp;
+            const int g = gg[e], dim = dd[e];
+            const float L = Lr[e];
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const float4 o = make_float4(acc[e].x * inv, acc[e].y * inv, acc[e].z * inv, acc[e].w * inv);
+            if (mine) {
                 if (into >= 0) {
                     // this thread alone reads and writes these four elements
                     *reinterpret_cast<float4 *>(p.ws_o + (into * G + g) * D + dim) = o;
@@ -256,15 +236,21 @@ __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int 
                     const long long qrow = qrow0 + g;
                     store_out4(p.out, qrow * D + dim, p.out_dtype, o);
                     if (dim == 0 && p.lse)
-                        p.lse[qrow] = L > 0.f ? (sM[g] + log2f(L)) * LN2_F : -INFINITY;
+                        p.lse[qrow] = L > 0.f ? (Mr[e] + log2f(L)) * LN2_F : -INFINITY;
                 }
+            }
+            if (mine && dim == 0 && into >= 0) {
+                sM[g] = Mr[e];
+                sL[g] = L;
             }
         }
     }
+    if (into < 0)
+        return true;
     // every read of the batch's (m, l) is done before the slot's are replaced
     if (!wb.sync(tid & 31))
         return false;
-    if (into >= 0 && tid < Gv) {
+    if (tid < Gv) {
         const long long r = into * G + tid;
         p.ws_ml[2 * r] = sL[tid] > 0.f ? sM[tid] : -INFINITY;
         p.ws_ml[2 * r + 1] = sL[tid];

@@ -58,19 +58,19 @@ template <int D> struct Tc8Cfg {
     static constexpr int ROW = D;                  // bytes per token row
     static constexpr int LINES = 1;
     static constexpr int CHUNK_BYTES = CT * ROW;   // K or V of one chunk
-    static constexpr int QP_BYTES = NC * D;        // q parts: NC rows of d bytes
+    static constexpr int QP_BYTES = NC * D;        // q parts: NC rows of d bytes (two buffers, by segment)
     static constexpr int NWG = 2;                  // softmax groups (4 warps each), pairs of chunks in turn
     static constexpr int NPB = 2 * NWG;            // Pp^T buffers (chunk j in j % NPB)
     static constexpr int PT_BYTES = NC * CT;       // one Pp^T: NC rows of CT bytes
     static constexpr int NSB = 12;                 // S^T buffers in TMEM (chunk j in j % NSB)
-    static constexpr int TMEM_O = NSB * NC;        // then the groups' O^T
+    static constexpr int TMEM_O = NSB * NC;        // then the groups' O^T, two sets (by segment)
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int MERGE_PB = 64;
     static constexpr int SCR_BYTES = MERGE_PB * 8 + 2 * MAXG * 4;
     // per group: vote flags [2][4], chunk maxima [4][8]; per segment parity:
-    // l sums [NWG][4][8] and m [NWG][8]; the heads' score scales [8]
+    // l sums [NWG][4][8] and m [NWG][8], and the heads' score scales [8]
     static constexpr int SEGX = NWG * 4 * 8 + NWG * 8;
-    static constexpr int XCH_FLOATS = NWG * 2 * 4 + NWG * 4 * 8 + 2 * SEGX + 8;
+    static constexpr int XCH_FLOATS = NWG * 2 * 4 + NWG * 4 * 8 + 2 * SEGX + 2 * 8;
     static constexpr int XCH_BYTES = (XCH_FLOATS * 4 + 15) / 16 * 16;
     // warps 0 .. 4 NWG - 1: the softmax groups; then four epilogue warps,
     // the K and V producers, the S^T issuer (it allocates TMEM) and the P.V
@@ -79,13 +79,9 @@ template <int D> struct Tc8Cfg {
     static constexpr int VPROD_WARP = KPROD_WARP + 1;
     static constexpr int S_WARP = KPROD_WARP + 2, PV_WARP = KPROD_WARP + 3;
     static constexpr int THREADS = 32 * (4 * NWG + 8);
-    // staging of a segment's result for the epilogue (two, by segment
-    // parity): 8 heads x d outputs, then 8 maxima and 8 sums
-    static constexpr int STG_FLOATS = 8 * D + 16;
-    static constexpr int STG_BYTES = 2 * STG_FLOATS * 4;
     // mbarriers: full/empty of the K and V buffers, s_full[NSB],
-    // s_free[NSB], p_full[NPB], pv_done[NPB], q_full, fin (2), seg, epi,
-    // wg[NWG], stg_full[2], stg_free[2]
+    // s_free[NSB], p_full[NPB], pv_done[NPB], fin (2), epi, wg[NWG], and by
+    // segment parity q_full, seg_done, o_free
     // every wait suspends the waiting thread in hardware (woken when the
     // phase completes) rather than polling, so that waiting warps leave the
     // issue slots to the working ones
@@ -98,23 +94,23 @@ template <int D> struct Tc8Cfg {
     // KST K buffers and the rest, the prefix sums of up to BALANCED_MAX_B
     // sequences included (two barriers per buffer)
     static constexpr int KST = 4;
-    static constexpr int NBAR_FIXED = 2 * KST + 2 * NSB + 2 * NPB + 5 + NWG + 4;
-    static constexpr int FIXED = 1024 + KST * CHUNK_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + STG_BYTES +
+    static constexpr int NBAR_FIXED = 2 * KST + 2 * NSB + 2 * NPB + 3 + NWG + 6;
+    static constexpr int FIXED = 1024 + KST * CHUNK_BYTES + 2 * QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES +
                                  NBAR_FIXED * 8 + 16 + (BALANCED_MAX_B + 1) * 8 + BALANCED_MAX_B * 4;
     static constexpr int VST = (227 * 1024 - FIXED) / (CHUNK_BYTES + 16);
     static constexpr int RING_BYTES = (KST + VST) * CHUNK_BYTES;   // K buffers, then V buffers
     static constexpr int NBAR = 2 * VST + NBAR_FIXED;
     static_assert(D == 128, "head dim 128");
     static_assert(VST >= 4, "ring depth");
-    static_assert(1024 + RING_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + STG_BYTES + NBAR * 8 + 16 +
+    static_assert(1024 + RING_BYTES + 2 * QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16 +
                           (BALANCED_MAX_B + 1) * 8 + BALANCED_MAX_B * 4 <= 227 * 1024,
                   "shared memory");
-    static_assert(TMEM_O + NWG * NC <= (int)TMEM_COLS, "TMEM columns");
+    static_assert(TMEM_O + 2 * NWG * NC <= (int)TMEM_COLS, "TMEM columns");
     static_assert(RING_BYTES % 1024 == 0 && QP_BYTES % 1024 == 0 && PT_BYTES % 1024 == 0, "1024-byte atoms");
 
     static size_t smem_bytes(int decomp, int B)
     {
-        size_t s = 1024 + RING_BYTES + QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + STG_BYTES + NBAR * 8 + 16;
+        size_t s = 1024 + RING_BYTES + 2 * QP_BYTES + NPB * PT_BYTES + SCR_BYTES + XCH_BYTES + NBAR * 8 + 16;
         if (decomp == DECOMP_BALANCED)
             s += (size_t)(B + 1) * 8 + (size_t)B * 4;
         return s;
@@ -186,35 +182,87 @@ __device__ __forceinline__ void tc8_issue(TmaProducer<C, false> &pr, const GqaPa
     pr.locate(gp, ctx);
 }
 
-// Segment end on softmax group 0 ("FlashDecoding 数学推导" §2.4.2): merges
-// the groups' states per head (l summed over each group's warps at lsum
-// [g][4][8], its reference max at mseg[g][8]) into the staging buffer: the
-// normalised output of head h at stg_o[h * D + row] (thread `row` = TMEM
-// lane of O^T = head dimension), and the head's base-2 max and sum at
-// stg_ml[h], stg_ml[8 + h].  The epilogue warps take it from there.
+// The q parts of segment qs's slice of heads (K-major, 128-byte swizzle,
+// row 8p + h for part p of head h; rows of heads past the slice stay zero)
+// into the buffer at qb, and the heads' base-2 score scales into fh[8], on
+// 128 threads (tid): 16 per head, 8 head dimensions each.  Each head's q is
+// first brought to amax in [128, 256) by a power of two 2^e, and its score
+// scale carries 2^-e.
 template <int D>
-__device__ __forceinline__ void tc8_seg_merge(const float *lsum, const float *mseg, float vsc, int row, uint32_t tl,
-                                              float *stg_o, float *stg_ml)
+__device__ __forceinline__ void tc8_prep_q(const GqaParams &gp, const Seg &qs, int slice, uint32_t qb, float *fh,
+                                           int tid)
+{
+    const SplitParams &p = gp.s;
+    const int vh = qs.h * gp.NG + slice;
+    const int gv = vh_count(gp, vh);
+    const long long qrow0 = vh_qrow0(gp, qs.b, vh);
+    const int h = tid >> 4, sub = tid & 15;
+    const bool live = h < gv;
+    float qv[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = live ? q_pair_f32(p.q, p.q_dtype, (qrow0 + h) * D + sub * 8 + 2 * i) : make_float2(0.f, 0.f);
+        qv[2 * i] = f.x;
+        qv[2 * i + 1] = f.y;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        amax = fmaxf(amax, fabsf(qv[i]));
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, o));
+    const int eb = (int)((__float_as_uint(amax) >> 23) & 0xff);
+    // amax in [2^(eb-127), 2^(eb-126)): times 2^(134-eb); zero, subnormal,
+    // infinite or NaN amax: unscaled
+    const int e = (eb >= 8 && eb <= 254) ? 134 - eb : 0;
+    const float up = pow2i(e);
+    uint32_t pr[3][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        e4m3_parts2(qv[2 * i] * up, qv[2 * i + 1] * up, pr[0][i], pr[1][i], pr[2][i]);
+#pragma unroll
+    for (int pp = 0; pp < 3; ++pp) {
+        const uint32_t lo = pr[pp][0] | (pr[pp][1] << 16), hi = pr[pp][2] | (pr[pp][3] << 16);
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(qb + sw128_byte(pp * 8 + h, sub * 8)), "r"(lo),
+                     "r"(hi)
+                     : "memory");
+    }
+    if (sub == 0)
+        fh[h] = p.scale_log2 * __ldg(gp.k_scale + qs.b * p.H + qs.h) * pow2i(-e);
+    fence_proxy_async_smem();
+}
+
+// A segment's result, on the epilogue warps ("FlashDecoding 数学推导"
+// §2.4.2): the groups' states per head (l summed over each group's warps at
+// lsum[g][4][8], its reference max at mseg[g][8]) merged into this thread's
+// output of every head, oh[h] (thread `row` = TMEM lane of O^T = head
+// dimension; the groups' O^T at columns ocols + g NC), and each head's
+// base-2 max Mh and sum Lh.
+template <int D>
+__device__ __forceinline__ void tc8_seg_merge(const float *lsum, const float *mseg, float vsc, uint32_t ocols,
+                                              float (&oh)[8], float (&Mh)[8], float (&Lh)[8])
 {
     using C = Tc8Cfg<D>;
     constexpr int NWG = C::NWG;
-    float Mh[8], Lh[8], oh[8];
+    float lg[NWG][8];
+#pragma unroll
+    for (int g = 0; g < NWG; ++g)
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+            lg[g][h] = lsum[g * 32 + h] + lsum[g * 32 + 8 + h] + lsum[g * 32 + 16 + h] + lsum[g * 32 + 24 + h];
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
         float M = -INFINITY;
 #pragma unroll
-        for (int g = 0; g < NWG; ++g) {
-            const float lg = lsum[g * 32 + h] + lsum[g * 32 + 8 + h] + lsum[g * 32 + 16 + h] + lsum[g * 32 + 24 + h];
-            if (lg > 0.f)
+        for (int g = 0; g < NWG; ++g)
+            if (lg[g][h] > 0.f)
                 M = fmaxf(M, mseg[g * 8 + h]);
-        }
         float L = 0.f;
 #pragma unroll
-        for (int g = 0; g < NWG; ++g) {
-            const float lg = lsum[g * 32 + h] + lsum[g * 32 + 8 + h] + lsum[g * 32 + 16 + h] + lsum[g * 32 + 24 + h];
-            if (lg > 0.f)
-                L += ex2(mseg[g * 8 + h] - M) * lg;
-        }
+        for (int g = 0; g < NWG; ++g)
+            if (lg[g][h] > 0.f)
+                L += ex2(mseg[g * 8 + h] - M) * lg[g][h];
         Mh[h] = M;
         Lh[h] = L;
         oh[h] = 0.f;
@@ -226,46 +274,64 @@ __device__ __forceinline__ void tc8_seg_merge(const float *lsum, const float *ms
         float f[8];
 #pragma unroll
         for (int h = 0; h < 8; ++h) {
-            const float lg = lsum[g * 32 + h] + lsum[g * 32 + 8 + h] + lsum[g * 32 + 16 + h] + lsum[g * 32 + 24 + h];
-            f[h] = (lg > 0.f && Lh[h] > 0.f) ? ex2(mseg[g * 8 + h] - Mh[h]) / Lh[h] * vsc : 0.f;
+            f[h] = (lg[g][h] > 0.f && Lh[h] > 0.f) ? ex2(mseg[g * 8 + h] - Mh[h]) / Lh[h] * vsc : 0.f;
             need = need || f[h] != 0.f;
         }
         if (!need)   // the same for every thread: the values come from shared memory
             continue;
         float o[32];
-        tmem_ld32(tl + (uint32_t)(C::TMEM_O + g * C::NC), o);
+        tmem_ld32(ocols + (uint32_t)(g * C::NC), o);
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < 8; ++h)
             if (f[h] != 0.f)
                 oh[h] += f[h] * (o[h] + 0.0625f * o[8 + h] + 0.00390625f * o[16 + h]);
     }
-    tc_fence_before();
 #pragma unroll
     for (int h = 0; h < 8; ++h)
-        stg_o[h * D + row] = oh[h];
-    if (row < 8) {
-        float M = Mh[0], L = Lh[0];
-#pragma unroll
-        for (int h = 1; h < 8; ++h)
-            if (row == h) {
-                M = Mh[h];
-                L = Lh[h];
-            }
-        stg_ml[row] = M;
-        stg_ml[8 + row] = L * pow2i(-(int)C::PEXP);   // P was taken times 2^PEXP
+        Lh[h] *= pow2i(-(int)C::PEXP);   // P was taken times 2^PEXP
+}
+
+// Warms the lines (and their address translations) that the epilogue of
+// segment cs will write, on 128 threads: its out rows, or its workspace
+// rows and (m, l); called while the segment streams.
+template <int D>
+__device__ __forceinline__ void tc8_prefetch_dest(const GqaParams &gp, const Ctx &ctx, const Seg &cs, int slice,
+                                                  int tid)
+{
+    const SplitParams &p = gp.s;
+    const int vh = cs.h * gp.NG + slice;
+    const long long bhv = (long long)cs.b * p.H * gp.NG + vh;
+    const int gv = vh_count(gp, vh);
+    const int len = (p.decomp == DECOMP_BALANCED) ? ctx.lenS[cs.b] : clamp_len(p, cs.b);
+    bool complete;
+    long long slot;
+    tc_seg_dest(p, cs, bhv, len, complete, slot);
+    const char *a;
+    if (complete) {
+        const int es = p.out_dtype == 0 ? 4 : 2;
+        a = static_cast<const char *>(p.out) + vh_qrow0(gp, cs.b, vh) * D * es + tid * 128;
+        if (tid * 128 < gv * D * es)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    } else {
+        const long long r0 = slot * gp.G;
+        a = reinterpret_cast<const char *>(p.ws_o + r0 * D) + tid * 128;
+        if (tid * 128 < gv * D * 4)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        if (tid == 0)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.ws_ml + 2 * r0));
     }
 }
 
-// The epilogue of a segment, on the epilogue warps (tid 0..127), from the
-// staging buffer: out/lse for a whole (b, h), or a workspace partial and,
-// for the last piece to arrive, the merge of the pieces.  Its global-memory
-// round trips (the arrival counter, the pieces' partials) overlap the next
-// segment's streaming.  Returns false if a barrier wait expired.
+// The rest of a segment's epilogue (tid 0..127 = head dimension): out/lse
+// for a whole (b, h), or a workspace partial and, for the last piece to
+// arrive, the merge of the pieces.  Its global-memory round trips (the
+// arrival counter, the pieces' partials) overlap the next segments'
+// streaming.  Returns false if a barrier wait expired.
 template <int D>
 __device__ __noinline__ bool tc8_epilogue(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice,
-                                          const float *stg_o, const float *stg_ml, int lane, int tid, uint32_t *misc,
-                                          unsigned char *scratch, WarpBar &wb)
+                                          const float (&oh)[8], const float (&Mh)[8], const float (&Lh)[8], int lane,
+                                          int tid, uint32_t *misc, unsigned char *scratch, WarpBar &wb)
 {
     using C = Tc8Cfg<D>;
     const SplitParams &p = gp.s;
@@ -278,15 +344,23 @@ __device__ __noinline__ bool tc8_epilogue(const GqaParams &gp, const Ctx ctx, co
     bool complete;
     long long slot;
     tc_seg_dest(p, cs, bhv, len, complete, slot);
-    for (int h = 0; h < gv; ++h) {
-        const float o = stg_o[h * D + tid];
-        if (complete)
-            store_out(p.out, (qrow0 + h) * D + tid, p.out_dtype, o);
-        else
-            p.ws_o[(slot * G + h) * D + tid] = o;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+        if (h < gv) {
+            if (complete)
+                store_out(p.out, (qrow0 + h) * D + tid, p.out_dtype, oh[h]);
+            else
+                p.ws_o[(slot * G + h) * D + tid] = oh[h];
+        }
     }
     if (tid < gv) {
-        const float M = stg_ml[tid], L = stg_ml[8 + tid];
+        float M = Mh[0], L = Lh[0];
+#pragma unroll
+        for (int h = 1; h < 8; ++h)
+            if (tid == h) {
+                M = Mh[h];
+                L = Lh[h];
+            }
         const bool nonempty = L > 0.f;
         if (complete) {
             if (p.lse)
@@ -317,17 +391,16 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 1024-aligned
     const uint32_t ring = smem_addr(smem);
-    const uint32_t qbuf = ring + C::RING_BYTES;
-    const uint32_t pbuf = qbuf + C::QP_BYTES;
-    unsigned char *scratch = smem + C::RING_BYTES + C::QP_BYTES + C::NPB * C::PT_BYTES;
+    const uint32_t qbuf = ring + C::RING_BYTES;   // two q-part buffers
+    const uint32_t pbuf = qbuf + 2 * C::QP_BYTES;
+    unsigned char *scratch = smem + C::RING_BYTES + 2 * C::QP_BYTES + C::NPB * C::PT_BYTES;
     float *xch = reinterpret_cast<float *>(scratch + C::SCR_BYTES);
     constexpr int NWG = C::NWG;
     int *flg = reinterpret_cast<int *>(xch);      // [NWG groups][2][4 warps]
     float *red = xch + NWG * 8;                   // [NWG groups][4 warps][8 heads]
     float *segx = red + NWG * 32;                 // [2 parities][l sums [NWG][4][8], m [NWG][8]]
-    float *fhs = segx + 2 * C::SEGX;              // [8] score scales of the segment's heads
-    float *stg = reinterpret_cast<float *>(scratch + C::SCR_BYTES + C::XCH_BYTES);   // [2][STG_FLOATS]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::SCR_BYTES + C::XCH_BYTES + C::STG_BYTES);
+    float *fhs = segx + 2 * C::SEGX;              // [2][8] score scales of the segment's heads
+    uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::SCR_BYTES + C::XCH_BYTES);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBAR);   // [0] TMEM base, [1] flag
     long long *cumH = reinterpret_cast<long long *>(misc + 4);
     int *lenS = reinterpret_cast<int *>(cumH + p.B + 1);
@@ -347,15 +420,15 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
     auto PFULL = [&](int b) { return bar0 + 8u * (uint32_t)(B0 + b); };
     auto PVD = [&](int b) { return bar0 + 8u * (uint32_t)(B0 + NPB + b); };
     constexpr int B1 = B0 + 2 * NPB;
-    const uint32_t QFULL = bar0 + 8u * B1;
-    const uint32_t FINS = bar0 + 8u * (B1 + 1);
-    const uint32_t FINP = bar0 + 8u * (B1 + 2);
-    const uint32_t SEGBAR = bar0 + 8u * (B1 + 3);
-    const uint32_t WG0BAR = bar0 + 8u * (B1 + 4);
-    auto WGBAR = [&](int g) { return bar0 + 8u * (uint32_t)(B1 + 5 + g); };
-    auto STGF = [&](int i) { return bar0 + 8u * (uint32_t)(B1 + 5 + NWG + i); };
-    auto STGE = [&](int i) { return bar0 + 8u * (uint32_t)(B1 + 7 + NWG + i); };
-    static_assert(B1 + 9 + NWG == C::NBAR, "barrier count");
+    const uint32_t FINS = bar0 + 8u * B1;
+    const uint32_t FINP = bar0 + 8u * (B1 + 1);
+    const uint32_t WG0BAR = bar0 + 8u * (B1 + 2);
+    auto WGBAR = [&](int g) { return bar0 + 8u * (uint32_t)(B1 + 3 + g); };
+    constexpr int B2 = B1 + 3 + NWG;   // then five pairs, by segment parity
+    auto QFULL = [&](int i) { return bar0 + 8u * (uint32_t)(B2 + i); };
+    auto SEGDONE = [&](int i) { return bar0 + 8u * (uint32_t)(B2 + 2 + i); };
+    auto OFREE = [&](int i) { return bar0 + 8u * (uint32_t)(B2 + 4 + i); };
+    static_assert(B2 + 6 == C::NBAR, "barrier count");
 
     if (tid == 0) {
         for (int s = 0; s < KST; ++s) {
@@ -374,14 +447,17 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             mbar_init(PFULL(b), 4);   // the owning group's warps: Pp^T written, V's tail rows zeroed, O^T rescaled
             mbar_init(PVD(b), 1);     // commit after P.V of the buffer's chunk
         }
-        mbar_init(QFULL, 4);          // group 0 has written the q parts and score scales
         mbar_init(FINS, 1);           // the MMA issuers' last commits
         mbar_init(FINP, 1);
-        mbar_init(SEGBAR, 4 * NWG);   // every softmax group at a segment end
         mbar_init(WG0BAR, 4);         // the epilogue warps (arrival and merge)
         for (int i = 0; i < 2; ++i) {
-            mbar_init(STGF(i), 4);    // group 0's warps have staged a segment's result
-            mbar_init(STGE(i), 4);    // the epilogue warps are done with it
+            // by parity of the non-empty segments: the epilogue warps have
+            // written a q buffer and its score scales
+            mbar_init(QFULL(i), 4);
+            // by parity of all segments: every softmax warp has left its
+            // (m, l) and its group's final O^T; the epilogue has read them
+            mbar_init(SEGDONE(i), 4 * NWG);
+            mbar_init(OFREE(i), 4);
         }
         for (int g = 0; g < NWG; ++g)
             mbar_init(WGBAR(g), 4);   // each group's vote and max exchange
@@ -389,7 +465,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         prefetch_tmap(&gp.tmv);
     }
     // the q-part rows past 3 x 8 stay zero
-    for (int i = tid; i < C::QP_BYTES / 16; i += C::THREADS)
+    for (int i = tid; i < 2 * C::QP_BYTES / 16; i += C::THREADS)
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(qbuf + 16u * (uint32_t)i), "r"(0u) : "memory");
     if (w == C::S_WARP) {
         tmem_alloc(smem_addr(misc), C::TMEM_COLS);
@@ -469,8 +545,10 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
 #pragma unroll 1
             while (ss.valid && !dead) {
                 const long long n = seg_chunks<C::CT>(ss);
+                const int qp = kq & 1;   // this segment's q buffer (non-empty segments alternate)
+                const uint32_t qb = qbuf + (uint32_t)(qp * C::QP_BYTES);
                 if (n > 0) {
-                    if (!mbar_wait_bounded_sleep_thread(QFULL, (uint32_t)(kq & 1), C::SLEEP_NS)) {
+                    if (!mbar_wait_bounded_sleep_thread(QFULL(qp), (uint32_t)((kq >> 1) & 1), C::SLEEP_NS)) {
                         dead = true;
                         break;
                     }
@@ -491,7 +569,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                     for (int ks = 0; ks < D / 32; ++ks) {
                         // 32 E4M3 values = 32 bytes of each 128-byte row
                         const uint64_t a = smem_desc_sw128(kb + (uint32_t)(ks * 32), 16, 1024);
-                        const uint64_t b = smem_desc_sw128(qbuf + (uint32_t)(ks * 32), 16, 1024);
+                        const uint64_t b = smem_desc_sw128(qb + (uint32_t)(ks * 32), 16, 1024);
                         tc_mma_f8_ss(tmem + (uint32_t)(sb * NC), a, b, ID_S, ks > 0 ? 1u : 0u);
                     }
                     tc_commit(SFULL(sb));
@@ -510,11 +588,19 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         if (lane == 0) {
             constexpr uint32_t ID_O = idesc_f16(0, 1, 0, D, NC);      // V^T MN-major, Pp^T K-major
             long long jp = 0, pp0 = 0;   // chunks, and pairs before the segment
+            int ks_ = 0;                 // segments so far: their O^T sets alternate
             Seg sp;
             seg_first(p, ctx, sp);
 #pragma unroll 1
             while (sp.valid && !dead) {
                 const long long n = seg_chunks<C::CT>(sp);
+                const uint32_t oset = (uint32_t)(C::TMEM_O + (ks_ & 1) * NWG * NC);
+                // the set was read by the epilogue for segment ks_ - 2
+                if (n > 0 && ks_ >= 2 &&
+                    !mbar_wait_bounded_sleep_thread(OFREE(ks_ & 1), (uint32_t)(((ks_ >> 1) - 1) & 1), C::SLEEP_NS)) {
+                    dead = true;
+                    break;
+                }
 #pragma unroll 1
                 for (long long c = 0; c < n; ++c, ++jp) {
                     if (!mbar_wait_bounded_sleep_thread(PFULL((int)(jp % NPB)), (uint32_t)((jp / NPB) & 1), C::SLEEP_NS) ||
@@ -534,13 +620,13 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                         // 32 bytes of each Pp^T row
                         const uint64_t a = smem_desc_sw128(vb + (uint32_t)(ks * 4096), 16, 1024);
                         const uint64_t b = smem_desc_sw128(pb + (uint32_t)(ks * 32), 16, 1024);
-                        tc_mma_f8_ss(tmem + (uint32_t)(C::TMEM_O + g * NC), a, b, ID_O,
-                                     (!first || ks > 0) ? 1u : 0u);
+                        tc_mma_f8_ss(tmem + oset + (uint32_t)(g * NC), a, b, ID_O, (!first || ks > 0) ? 1u : 0u);
                     }
                     tc_commit(EMPTYV((int)(jp % VST)));
                     tc_commit(PVD((int)(jp % NPB)));
                 }
                 pp0 += (n + 1) / 2;
+                ++ks_;
                 seg_next(p, ctx, sp);
             }
             tc_commit(FINP);
@@ -550,28 +636,61 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         __syncwarp();
     } else if (w >= C::EPI_WARP) {
         // ------------------------------------------------------------ epilogue
-        // each segment's staged result to out/lse or the workspace, the
-        // arrival and, for the last piece, the merge of the pieces
+        // each segment's state (the softmax warps' (m, l), the groups' O^T)
+        // merged, released, and written to out/lse or the workspace, with
+        // the arrival and, for the last piece, the merge of the pieces
         const int etid = tid - 32 * C::EPI_WARP;
-        WarpBar wb{WG0BAR, 0u, C::SLEEP_NS};
-        int si = 0;
+        const uint32_t etl = tmem + ((uint32_t)((w & 3) * 32) << 16);   // this warp's TMEM lanes
+        WarpBar wb{WG0BAR, 0u, 0u};   // busy warps: no sleep between their syncs
+        // the q parts of the non-empty segments, two ahead: the first two
+        // now, each further one as soon as the segment two before it is done
+        Seg qs;
+        seg_first(p, ctx, qs);
+        int kqp = 0;
+        auto prep_next = [&]() {
+            while (qs.valid && seg_chunks<C::CT>(qs) == 0)
+                seg_next(p, ctx, qs);
+            if (!qs.valid)
+                return;
+            tc8_prep_q<D>(gp, qs, slice, qbuf + (uint32_t)((kqp & 1) * C::QP_BYTES), fhs + (kqp & 1) * 8, etid);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(QFULL(kqp & 1));
+            ++kqp;
+            seg_next(p, ctx, qs);
+        };
+        prep_next();
+        prep_next();
+        int k = 0;
         Seg cs;
         seg_first(p, ctx, cs);
 #pragma unroll 1
         while (cs.valid && !dead) {
-            const float *sg = stg + (si & 1) * C::STG_FLOATS;
-            if (!mbar_wait_bounded_sleep(STGF(si & 1), (uint32_t)((si >> 1) & 1), C::SLEEP_NS)) {
+            const long long n = seg_chunks<C::CT>(cs);
+            const float vsc = __ldg(gp.v_scale + cs.b * p.H + cs.h);   // V's dequantisation scale
+            tc8_prefetch_dest<D>(gp, ctx, cs, slice, etid);
+            const float *sx = segx + (k & 1) * C::SEGX;
+            if (!mbar_wait_bounded_sleep(SEGDONE(k & 1), (uint32_t)((k >> 1) & 1), C::SLEEP_NS)) {
                 dead = true;
                 break;
             }
-            if (!tc8_epilogue<D>(gp, ctx, cs, slice, sg, sg + 8 * D, lane, etid, misc, scratch, wb)) {
-                dead = true;
-                break;
-            }
+            tc_fence_after();
+            float oh[8], Mh[8], Lh[8];
+            tc8_seg_merge<D>(sx, sx + NWG * 32, vsc, etl + (uint32_t)(C::TMEM_O + (k & 1) * NWG * NC), oh, Mh, Lh);
+            // the (m, l) and the O^T set are free for segment k + 2
+            tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(STGE(si & 1));
-            ++si;
+                mbar_arrive(OFREE(k & 1));
+            // this segment's q buffer is free (its S^T are done, its score
+            // scales read): the next q parts into it
+            if (n > 0)
+                prep_next();
+            if (!tc8_epilogue<D>(gp, ctx, cs, slice, oh, Mh, Lh, lane, etid, misc, scratch, wb)) {
+                dead = true;
+                break;
+            }
+            ++k;
             seg_next(p, ctx, cs);
         }
     } else {
@@ -580,8 +699,7 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
         const int wq = w & 3;              // warp within the group
         const int row = tid & 127;         // token of the chunk (S^T) = head dim (O^T) = TMEM lane
         const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
-        const uint32_t ocol = (uint32_t)(C::TMEM_O + wg * NC);
-        WarpBar sb{SEGBAR, 0u, C::SLEEP_NS}, gb{WGBAR(wg), 0u, C::SLEEP_NS};
+        WarpBar gb{WGBAR(wg), 0u, C::SLEEP_NS};
         long long nw = 0;   // chunks this group has handed to P.V
         long long j0 = 0;   // the CTA's chunk index of the segment's first chunk
         long long p0 = 0;   // pairs of chunks before the segment
@@ -595,8 +713,9 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             const int vh = cs.h * gp.NG + slice;
             const int gv = vh_count(gp, vh);
             const long long qrow0 = vh_qrow0(gp, cs.b, vh);
-            // V's dequantisation scale, applied at the segment end
-            const float vsc = wg == 0 ? __ldg(gp.v_scale + cs.b * p.H + cs.h) : 0.f;
+            // this group's O^T in the segment's set (segments alternate)
+            const uint32_t ocol = (uint32_t)(C::TMEM_O + ((k & 1) * NWG + wg) * NC);
+            const int qp = kq & 1;   // the q buffer of a non-empty segment
             float m[8], l[8], fh[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
@@ -604,60 +723,14 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 l[h] = 0.f;
             }
             if (n > 0) {
-                if (wg == 0) {
-                    // q parts: 16 threads per head, 8 dims each; the head's
-                    // amax to [128, 256) by a power of two
-                    const int h = row >> 4, sub = row & 15;
-                    const bool live = h < gv;
-                    float qv[8];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = live ? q_pair_f32(p.q, p.q_dtype, (qrow0 + h) * D + sub * 8 + 2 * i)
-                                              : make_float2(0.f, 0.f);
-                        qv[2 * i] = f.x;
-                        qv[2 * i + 1] = f.y;
-                    }
-                    float amax = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        amax = fmaxf(amax, fabsf(qv[i]));
-#pragma unroll
-                    for (int o = 1; o < 16; o <<= 1)
-                        amax = fmaxf(amax, __shfl_xor_sync(FULL_MASK, amax, o));
-                    const int eb = (int)((__float_as_uint(amax) >> 23) & 0xff);
-                    // amax in [2^(eb-127), 2^(eb-126)): times 2^(134-eb); zero,
-                    // subnormal, infinite or NaN amax: unscaled
-                    const int e = (eb >= 8 && eb <= 254) ? 134 - eb : 0;
-                    const float up = pow2i(e);
-                    uint32_t pr[3][4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        e4m3_parts2(qv[2 * i] * up, qv[2 * i + 1] * up, pr[0][i], pr[1][i], pr[2][i]);
-#pragma unroll
-                    for (int pp = 0; pp < 3; ++pp) {
-                        const int nrow = pp * 8 + h;
-                        const uint32_t lo = pr[pp][0] | (pr[pp][1] << 16), hi = pr[pp][2] | (pr[pp][3] << 16);
-                        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(qbuf + sw128_byte(nrow, sub * 8)),
-                                     "r"(lo), "r"(hi)
-                                     : "memory");
-                    }
-                    if (sub == 0) {
-                        float sc = p.scale_log2 * __ldg(gp.k_scale + cs.b * p.H + cs.h);
-                        fhs[h] = sc * pow2i(-e);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(QFULL);
-                }
-                if (!mbar_wait_bounded_sleep(QFULL, (uint32_t)(kq & 1), C::SLEEP_NS)) {
+                if (!mbar_wait_bounded_sleep(QFULL(qp), (uint32_t)((kq >> 1) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
                 ++kq;
 #pragma unroll
                 for (int h = 0; h < 8; ++h)
-                    fh[h] = fhs[h];
+                    fh[h] = fhs[qp * 8 + h];
             }
             bool had = false;
             long long jprev = 0;
@@ -834,9 +907,14 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
             j0 += n;
             p0 += (n + 1) / 2;
 
-            // ---- segment end: each group's l per head over its 128 tokens,
-            // then group 0 merges the groups' states into a staging buffer
-            // for the epilogue warps and goes on ----
+            // ---- segment end: each warp's l per head over its 32 tokens and
+            // its group's m, for the epilogue warps (the buffer of segment
+            // k - 2 once they have read it), which merge the groups' states
+            // while the softmax groups go on ----
+            if (k >= 2 && !mbar_wait_bounded_sleep(OFREE(k & 1), (uint32_t)(((k >> 1) - 1) & 1), C::SLEEP_NS)) {
+                dead = true;
+                break;
+            }
             float *sx = segx + (k & 1) * C::SEGX;   // l sums [NWG][4][8], then m [NWG][8]
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
@@ -849,23 +927,11 @@ __global__ void __launch_bounds__(Tc8Cfg<D>::THREADS, 1) gqa_tc8_kernel(const __
                 if (wq == 0 && lane == 0)
                     sx[NWG * 32 + wg * 8 + h] = had ? m[h] : -INFINITY;
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(SEGDONE(k & 1));
             ++k;
-            if (!sb.sync(lane)) {
-                dead = true;
-                break;
-            }
-            if (wg == 0) {
-                const int si = k - 1;   // this segment's staging buffer: si % 2
-                if (si >= 2 && !mbar_wait_bounded_sleep(STGE(si & 1), (uint32_t)(((si >> 1) - 1) & 1), C::SLEEP_NS)) {
-                    dead = true;
-                    break;
-                }
-                tc8_seg_merge<D>(sx, sx + NWG * 32, vsc, row, tl, stg + (si & 1) * C::STG_FLOATS,
-                                 stg + (si & 1) * C::STG_FLOATS + 8 * D);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(STGF(si & 1));
-            }
             seg_next(p, ctx, cs);
         }
     }
