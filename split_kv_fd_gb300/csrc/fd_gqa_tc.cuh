@@ -307,7 +307,7 @@ __device__ __forceinline__ void tc_seg_dest(const SplitParams &p, const Seg &cs,
 // arrival on the (b, virtual head)'s counter and, for the last piece to
 // arrive, the merge of the pieces.  Returns false if a barrier wait expired.
 template <int D, int MERGE_PB>
-__device__ __noinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int gv,
+__device__ __forceinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int gv,
                                              long long qrow0, long long bhv, int len, int lane, int tid,
                                              uint32_t *misc, unsigned char *scratch, WarpBar &wb)
 {

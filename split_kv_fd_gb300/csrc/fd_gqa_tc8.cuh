@@ -329,7 +329,7 @@ __device__ __forceinline__ void tc8_prefetch_dest(const GqaParams &gp, const Ctx
 // arrival counter, the pieces' partials) overlap the next segments'
 // streaming.  Returns false if a barrier wait expired.
 template <int D>
-__device__ __noinline__ bool tc8_epilogue(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice,
+__device__ __forceinline__ bool tc8_epilogue(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice,
                                           const float (&oh)[8], const float (&Mh)[8], const float (&Lh)[8], int lane,
                                           int tid, uint32_t *misc, unsigned char *scratch, WarpBar &wb)
 {
