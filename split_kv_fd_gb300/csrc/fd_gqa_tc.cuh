@@ -349,7 +349,7 @@ __device__ __forceinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx c
 // or a workspace partial and, for the last piece to arrive, runs the merge
 // of the pieces.  Returns false if a barrier wait expired.
 template <typename C, int D>
-__device__ __noinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int G, int gv,
+__device__ __forceinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int G, int gv,
                                             long long qrow0, long long bhv, bool had, float m_ref, float l, float m1,
                                             float l1, int row, int lane, int tid, uint32_t tl, uint32_t *misc,
                                             unsigned char *scratch, WarpBar &wb)
