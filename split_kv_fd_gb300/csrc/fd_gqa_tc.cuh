@@ -55,10 +55,6 @@
 #ifndef FD_GQA_TC_MIN_G
 #define FD_GQA_TC_MIN_G 33
 #endif
-// S products issued ahead of the P.V products (chunks)
-#ifndef FD_TC_LOOKAHEAD
-#define FD_TC_LOOKAHEAD 1
-#endif
 
 namespace fd {
 
@@ -72,26 +68,31 @@ template <typename T, int D> struct TcCfg {
     static constexpr int ROW = D * 2;
     static constexpr int PLANE = CT * 128;         // one 64-element plane of a chunk
     static constexpr int CHUNK_BYTES = CT * ROW;   // K or V of one chunk
-    static constexpr int STAGE_BYTES = 2 * CHUNK_BYTES;
-    // a stage stays taken from its copy until P.V of its chunk is done, so
-    // the ring is deeper than the other kernels' 128 KB in flight: all the
+    // K and V have rings of their own: a K buffer is free once S of its
+    // chunk is done, a V buffer only once P.V is; together they take the
     // shared memory left beside Q, the merge scratch and the barriers
-    static constexpr int STAGES = ((D == 128 ? 160 : 192) * 1024) / STAGE_BYTES;
-    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int RING_BUFS = ((D == 128 ? 160 : 192) * 1024) / CHUNK_BYTES;
+    static constexpr int KST = RING_BUFS / 3 > 4 ? RING_BUFS / 3 : 4;
+    static constexpr int VST = RING_BUFS - KST;
+    static constexpr int RING_BYTES = RING_BUFS * CHUNK_BYTES;   // K buffers, then V buffers
     static constexpr int QPLANE = M * 128;         // one 64-element plane of Q
     static constexpr int Q_BYTES = LINES * QPLANE;
     static constexpr int MERGE_PB = 64;            // pieces per batch of the last arriver's merge
     static constexpr int SCR_BYTES = MERGE_PB * 8 + 2 * MAXG * 4;   // their slots, then M and L per head
     static constexpr int XCH_BYTES = 2 * M * 2 * 4;   // group 1's (m_ref, l) per head, two segments
-    static constexpr int WG_THREADS = 128, PROD_WARP = 8, MMA_WARP = 9, THREADS = 320;
+    // warps 0-7: the two softmax groups; 8, 9: the K and V producers; 10:
+    // the S issuer (it allocates TMEM); 11: the P.V issuer
+    static constexpr int WG_THREADS = 128, KPROD_WARP = 8, VPROD_WARP = 9, S_WARP = 10, PV_WARP = 11;
+    static constexpr int THREADS = 384;
     // TMEM: NSB S/P buffers of CT columns (chunk j in buffer j % NSB), then
     // the two groups' O accumulators
     static constexpr int NSB = 4;
     static constexpr int TMEM_O = NSB * CT;
     static constexpr uint32_t TMEM_COLS = 512;
-    // mbarriers: full[STAGES], empty[STAGES], s_full[NSB], s_free[NSB],
-    // p_full[2], o_full[2], q_full, fin, seg (both groups), wg0 (group 0)
-    static constexpr int NBAR = 2 * STAGES + 2 * NSB + 8;
+    // mbarriers: full/empty of the K and V buffers, s_full[NSB],
+    // s_free[NSB], p_full[NSB], o_full[2], q_full, fin (2), seg (both
+    // groups), wg0 (group 0)
+    static constexpr int NBAR = 2 * RING_BUFS + 3 * NSB + 7;
     static constexpr float TAU = 8.f;              // lazy-rescale threshold (base 2)
     // every wait suspends the waiting thread in hardware (woken when the
     // phase completes) rather than polling
@@ -99,7 +100,8 @@ template <typename T, int D> struct TcCfg {
     static_assert(D == 64 || D == 128, "head dim 64 or 128");
     static_assert(CT == 64, "an S buffer holds P_hi and P_lo in its 64 columns");
     static_assert(TMEM_O + 2 * D <= (int)TMEM_COLS, "TMEM columns");
-    static_assert(RING_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "1024-byte atoms");
+    static_assert(RING_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0 && CHUNK_BYTES % 1024 == 0, "1024-byte atoms");
+    static_assert(VST >= 4, "ring depth");
 
     static size_t smem_bytes(int decomp, int B)
     {
@@ -412,7 +414,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const __grid_constant__ GqaParams gp)
 {
     using C = TcCfg<T, D>;
-    constexpr int ST = C::STAGES;
+    constexpr int KST = C::KST, VST = C::VST;
     const SplitParams &p = gp.s;
     const int G = gp.G;   // query heads per slice (<= 128): row stride of the workspace
     const int slice = (int)(blockIdx.x % gp.NG);
@@ -431,40 +433,52 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     long long *cumH = reinterpret_cast<long long *>(misc + 4);
     int *lenS = reinterpret_cast<int *>(cumH + p.B + 1);
     const uint32_t bar0 = smem_addr(bars);
-    auto FULL = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-    auto EMPTY = [&](int s) { return bar0 + 8u * (uint32_t)(ST + s); };
+    auto FULLK = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+    auto EMPTYK = [&](int s) { return bar0 + 8u * (uint32_t)(KST + s); };
+    auto FULLV = [&](int s) { return bar0 + 8u * (uint32_t)(2 * KST + s); };
+    auto EMPTYV = [&](int s) { return bar0 + 8u * (uint32_t)(2 * KST + VST + s); };
     constexpr int NSB = C::NSB;
-    constexpr int B0 = 2 * ST + 2 * NSB;   // the barriers after the ring's and the S buffers'
-    auto SFULL = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + b); };
-    auto SFREE = [&](int b) { return bar0 + 8u * (uint32_t)(2 * ST + NSB + b); };
-    auto PFULL = [&](int g) { return bar0 + 8u * (uint32_t)(B0 + g); };
-    auto OFULL = [&](int g) { return bar0 + 8u * (uint32_t)(B0 + 2 + g); };
-    const uint32_t QFULL = bar0 + 8u * (B0 + 4);
-    const uint32_t FIN = bar0 + 8u * (B0 + 5);
-    const uint32_t SEGBAR = bar0 + 8u * (B0 + 6);
-    const uint32_t WG0BAR = bar0 + 8u * (B0 + 7);
+    constexpr int BS = 2 * (KST + VST);
+    auto SFULL = [&](int b) { return bar0 + 8u * (uint32_t)(BS + b); };
+    auto SFREE = [&](int b) { return bar0 + 8u * (uint32_t)(BS + NSB + b); };
+    // P of chunk j is handed over on p_full[j % NSB]: a group arrives there
+    // again (chunk j + NSB) only after S of that chunk, which waits for P.V
+    // of chunk j, so no phase is missed
+    auto PFULL = [&](int b) { return bar0 + 8u * (uint32_t)(BS + 2 * NSB + b); };
+    constexpr int B0 = BS + 3 * NSB;
+    auto OFULL = [&](int g) { return bar0 + 8u * (uint32_t)(B0 + g); };
+    const uint32_t QFULL = bar0 + 8u * (B0 + 2);
+    const uint32_t FINS = bar0 + 8u * (B0 + 3);
+    const uint32_t FINP = bar0 + 8u * (B0 + 4);
+    const uint32_t SEGBAR = bar0 + 8u * (B0 + 5);
+    const uint32_t WG0BAR = bar0 + 8u * (B0 + 6);
+    static_assert(B0 + 7 == C::NBAR, "barrier count");
 
     if (tid == 0) {
-        for (int s = 0; s < ST; ++s) {
-            mbar_init(FULL(s), 1);    // the producer's arrival plus the copies' bytes
-            mbar_init(EMPTY(s), 1);   // commit after P.V of the stage's chunk
+        for (int s = 0; s < KST; ++s) {
+            mbar_init(FULLK(s), 1);   // the producer's arrival plus the copy's bytes
+            mbar_init(EMPTYK(s), 1);  // commit after S of the buffer's chunk
+        }
+        for (int s = 0; s < VST; ++s) {
+            mbar_init(FULLV(s), 1);
+            mbar_init(EMPTYV(s), 1);  // commit after P.V of the buffer's chunk
         }
         for (int b = 0; b < NSB; ++b) {
             mbar_init(SFULL(b), 1);   // commit after S
-            mbar_init(SFREE(b), 4);   // the owning group's warps: P.V of the buffer's chunk is done
+            mbar_init(SFREE(b), 1);   // commit after P.V of the buffer's chunk
+            mbar_init(PFULL(b), 4);   // the owning group's warps: P in TMEM, V's tail rows zeroed
         }
-        for (int g = 0; g < 2; ++g) {
-            mbar_init(PFULL(g), 4);   // the group's warps: P in TMEM, V's tail rows zeroed
+        for (int g = 0; g < 2; ++g)
             mbar_init(OFULL(g), 1);   // commit after the group's P.V
-        }
         mbar_init(QFULL, 4);          // group 0 has written Q
-        mbar_init(FIN, 1);            // the MMA warp's last commit
+        mbar_init(FINS, 1);           // the MMA issuers' last commits
+        mbar_init(FINP, 1);
         mbar_init(SEGBAR, 8);         // both groups at a segment end
         mbar_init(WG0BAR, 4);         // group 0 (arrival and merge)
         prefetch_tmap(&gp.tmk);
         prefetch_tmap(&gp.tmv);
     }
-    if (w == C::MMA_WARP) {
+    if (w == C::S_WARP) {
         tmem_alloc(smem_addr(misc), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -500,56 +514,51 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     const uint32_t tmem = misc[0];
     bool dead = false;
 
-    if (w == C::PROD_WARP) {
-        // ------------------------------------------------------------ producer
-        TmaProducer<C, false> prod;
-        prod.start(gp, ctx, 0, 1);
-        int issued = 0;
+    if (w == C::KPROD_WARP || w == C::VPROD_WARP) {
+        // ------------------------------------------------------------ producers
+        // one warp per ring (lane 0): K refills a buffer once S of its chunk
+        // is done, V once P.V is
+        if (lane == 0) {
+            const bool isk = w == C::KPROD_WARP;
+            const int nb = isk ? KST : VST;
+            const uint32_t base = ring + (uint32_t)(isk ? 0 : KST * C::CHUNK_BYTES);
+            TmaProducer<C, false> pr;
+            pr.start(gp, ctx, 0, 1);
+            int issued = 0;
 #pragma unroll 1
-        for (;;) {
-            const int s = issued % ST;
-            if (issued >= ST && !mbar_wait_bounded_sleep(EMPTY(s), ((issued / ST) - 1) & 1, C::SLEEP_NS)) {
-                dead = true;
-                break;
+            while (pr.have) {
+                const int b = issued % nb;
+                if (issued >= nb && !mbar_wait_bounded_sleep_thread(isk ? EMPTYK(b) : EMPTYV(b),
+                                                                    (uint32_t)(((issued / nb) - 1) & 1), C::SLEEP_NS)) {
+                    dead = true;
+                    break;
+                }
+                // one box of the chunk's CT rows, every plane; rows past the
+                // block's end read as zeros
+                const int y = pr.t, blk = pr.s.b * p.H + pr.s.h;
+                const uint32_t bar = isk ? FULLK(b) : FULLV(b);
+                mbar_arrive_expect_tx(bar, C::CHUNK_BYTES);
+                tma_load_4d(base + (uint32_t)(b * C::CHUNK_BYTES), isk ? &gp.tmk : &gp.tmv, 0, y, blk, 0, bar);
+                pr.c += pr.stride;
+                pr.locate(gp, ctx);
+                ++issued;
             }
-            if (!prod.issue(gp, ctx, ring + (uint32_t)(s * C::STAGE_BYTES), FULL(s), lane))
-                break;
-            ++issued;
+            // no copy may be in flight when the CTA ends: the last fill of each buffer
+            for (int i = max(0, issued - nb); i < issued; ++i)
+                mbar_wait_bounded_sleep_thread(isk ? FULLK(i % nb) : FULLV(i % nb), (uint32_t)((i / nb) & 1),
+                                               C::SLEEP_NS);
         }
-        // no copy may be in flight when the CTA ends: the last fill of each stage
-        for (int i = max(0, issued - ST); i < issued; ++i)
-            mbar_wait_bounded_sleep(FULL(i % ST), (i / ST) & 1, C::SLEEP_NS);
-    } else if (w == C::MMA_WARP) {
-        // ------------------------------------------------------------ MMA issuer
+        __syncwarp();
+    } else if (w == C::S_WARP) {
+        // ------------------------------------------------------------ S issuer
+        // S of each chunk as soon as its K has landed and its S/P buffer is
+        // free (P.V of chunk j - NSB done); the first S of a segment once
+        // group 0 has written the segment's Q
         if (lane == 0) {
             constexpr int BF = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
             constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, C::M, C::CT);   // Q K-major, K K-major
-            constexpr uint32_t ID_O = idesc_f16(BF, 0, 1, C::M, D);       // P (TMEM) K-major, V MN-major
-            long long pw[2] = {0, 0};   // P.V handed by each softmax group so far
-            int k = 0;                  // non-empty segments so far
-            // S of chunk j into S/P buffer j % NSB
-            auto issue_s = [&](long long j) -> bool {
-                const int s = (int)(j % ST);
-                const int sb = (int)(j % NSB);
-                if (!mbar_wait_bounded_sleep_thread(FULL(s), (uint32_t)((j / ST) & 1), C::SLEEP_NS))
-                    return false;
-                if (j >= NSB && !mbar_wait_bounded_sleep_thread(SFREE(sb), (uint32_t)(((j / NSB) - 1) & 1), C::SLEEP_NS))
-                    return false;
-                tc_fence_after();
-                const uint32_t kb = ring + (uint32_t)(s * C::STAGE_BYTES);
-                const uint32_t ds = tmem + (uint32_t)(sb * C::CT);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    // 16 elements = 32 bytes of each 128-byte row of plane ks / 4
-                    const uint32_t col = (uint32_t)((ks & 3) * 32);
-                    const uint64_t a = smem_desc_sw128(qbuf + (uint32_t)((ks >> 2) * C::QPLANE) + col, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(kb + (uint32_t)((ks >> 2) * C::PLANE) + col, 16, 1024);
-                    tc_mma_ss(ds, a, b, ID_S, ks > 0 ? 1u : 0u);
-                }
-                tc_commit(SFULL(sb));
-                return true;
-            };
             long long j = 0;   // chunks of this CTA so far
+            int k = 0;         // non-empty segments so far
             Seg cs;
             seg_first(p, ctx, cs);
 #pragma unroll 1
@@ -562,51 +571,79 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     }
                     ++k;
                     tc_fence_after();
-                    // S runs LOOK chunks ahead of P.V, so that the tensor pipe
-                    // has work while a group computes its P
-                    constexpr int LOOK = FD_TC_LOOKAHEAD;
-                    bool ok = true;
-                    for (int c = 0; c < LOOK && c < n; ++c)
-                        ok = ok && issue_s(j + c);
-                    if (!ok) {
+                }
+#pragma unroll 1
+                for (long long c = 0; c < n; ++c, ++j) {
+                    const int st = (int)(j % KST), sb = (int)(j % NSB);
+                    if (!mbar_wait_bounded_sleep_thread(FULLK(st), (uint32_t)((j / KST) & 1), C::SLEEP_NS) ||
+                        (j >= NSB &&
+                         !mbar_wait_bounded_sleep_thread(SFREE(sb), (uint32_t)(((j / NSB) - 1) & 1), C::SLEEP_NS))) {
                         dead = true;
                         break;
                     }
-#pragma unroll 1
-                    for (long long c = 0; c < n; ++c, ++j) {
-                        if (c + LOOK < n && !issue_s(j + LOOK)) {
-                            dead = true;
-                            break;
-                        }
-                        const int g = (int)(j & 1);
-                        if (!mbar_wait_bounded_sleep_thread(PFULL(g), (uint32_t)(pw[g] & 1), C::SLEEP_NS)) {
-                            dead = true;
-                            break;
-                        }
-                        ++pw[g];
-                        tc_fence_after();
-                        const uint32_t vb = ring + (uint32_t)((j % ST) * C::STAGE_BYTES + C::CHUNK_BYTES);
-                        const uint32_t pa = tmem + (uint32_t)((j % NSB) * C::CT);
+                    tc_fence_after();
+                    const uint32_t kb = ring + (uint32_t)(st * C::CHUNK_BYTES);
+                    const uint32_t ds = tmem + (uint32_t)(sb * C::CT);
 #pragma unroll
-                        for (int ks = 0; ks < C::CT / 16; ++ks) {
-#pragma unroll
-                            for (int hl = 0; hl < 2; ++hl) {
-                                // P_hi in columns 0-31 of the buffer, P_lo in 32-63; 8 columns per k-step
-                                const uint64_t b =
-                                    smem_desc_sw128(vb + (uint32_t)(ks * 2048), (uint32_t)C::PLANE, 1024);
-                                tc_mma_ts(tmem + (uint32_t)(C::TMEM_O + g * D), pa + (uint32_t)(hl * 32 + ks * 8), b,
-                                          ID_O, (c >= 2 || ks > 0 || hl > 0) ? 1u : 0u);
-                            }
-                        }
-                        tc_commit(OFULL(g));
-                        tc_commit(EMPTY((int)(j % ST)));
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        // 16 elements = 32 bytes of each 128-byte row of plane ks / 4
+                        const uint32_t col = (uint32_t)((ks & 3) * 32);
+                        const uint64_t a = smem_desc_sw128(qbuf + (uint32_t)((ks >> 2) * C::QPLANE) + col, 16, 1024);
+                        const uint64_t b = smem_desc_sw128(kb + (uint32_t)((ks >> 2) * C::PLANE) + col, 16, 1024);
+                        tc_mma_ss(ds, a, b, ID_S, ks > 0 ? 1u : 0u);
                     }
+                    tc_commit(SFULL(sb));
+                    tc_commit(EMPTYK(st));
                 }
                 seg_next(p, ctx, cs);
             }
             // every MMA this thread issued has completed before TMEM is freed
-            tc_commit(FIN);
-            if (!mbar_wait_bounded_sleep_thread(FIN, 0, C::SLEEP_NS))
+            tc_commit(FINS);
+            if (!mbar_wait_bounded_sleep_thread(FINS, 0, C::SLEEP_NS))
+                dead = true;
+        }
+        __syncwarp();
+    } else if (w == C::PV_WARP) {
+        // ------------------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            constexpr int BF = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+            constexpr uint32_t ID_O = idesc_f16(BF, 0, 1, C::M, D);       // P (TMEM) K-major, V MN-major
+            long long j = 0;
+            Seg cs;
+            seg_first(p, ctx, cs);
+#pragma unroll 1
+            while (cs.valid && !dead) {
+                const long long n = seg_chunks<C::CT>(cs);
+#pragma unroll 1
+                for (long long c = 0; c < n; ++c, ++j) {
+                    const int sb = (int)(j % NSB), vs = (int)(j % VST);
+                    if (!mbar_wait_bounded_sleep_thread(PFULL(sb), (uint32_t)((j / NSB) & 1), C::SLEEP_NS) ||
+                        !mbar_wait_bounded_sleep_thread(FULLV(vs), (uint32_t)((j / VST) & 1), C::SLEEP_NS)) {
+                        dead = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int g = (int)(j & 1);
+                    const uint32_t vb = ring + (uint32_t)((KST + vs) * C::CHUNK_BYTES);
+                    const uint32_t pa = tmem + (uint32_t)(sb * C::CT);
+#pragma unroll
+                    for (int ks = 0; ks < C::CT / 16; ++ks) {
+#pragma unroll
+                        for (int hl = 0; hl < 2; ++hl) {
+                            // P_hi in columns 0-31 of the buffer, P_lo in 32-63; 8 columns per k-step
+                            const uint64_t b = smem_desc_sw128(vb + (uint32_t)(ks * 2048), (uint32_t)C::PLANE, 1024);
+                            tc_mma_ts(tmem + (uint32_t)(C::TMEM_O + g * D), pa + (uint32_t)(hl * 32 + ks * 8), b,
+                                      ID_O, (c >= 2 || ks > 0 || hl > 0) ? 1u : 0u);
+                        }
+                    }
+                    tc_commit(OFULL(g));
+                    tc_commit(EMPTYV(vs));
+                    tc_commit(SFREE(sb));
+                }
+                seg_next(p, ctx, cs);
+            }
+            tc_commit(FINP);
+            if (!mbar_wait_bounded_sleep_thread(FINP, 0, C::SLEEP_NS))
                 dead = true;
         }
         __syncwarp();
@@ -653,7 +690,6 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     mbar_arrive(QFULL);
             }
             bool had = false;
-            long long jprev = 0;
 #pragma unroll 1
             for (long long c = (long long)(wg ^ (int)(j0 & 1)); c < n; c += 2) {
                 const long long j = j0 + c;
@@ -693,19 +729,6 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                     for (int i = 0; i < C::CT; ++i)
                         mc = fmaxf(mc, S(i) * sc);
                 }
-                // the group's previous chunk: its P.V is done, so O is final
-                // and its S/P buffer free for the chunk four ahead
-                if (had) {
-                    if (!mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
-                        dead = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(SFREE((int)(jprev % NSB)));
-                }
                 // lazy rescale: the reference max moves only when the
                 // chunk's max exceeds it by more than TAU
                 const bool grow = mc > m_ref + C::TAU;
@@ -719,6 +742,14 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 // warp-wide, so the whole warp runs them when any of its
                 // heads grew (a = 1 for the others)
                 if (had && __any_sync(FULL_MASK, grow)) {
+                    // once the group's previous P.V is done (P.V of its chunk
+                    // before that is: S of this chunk waited for it, so the
+                    // phase is unambiguous)
+                    if (!mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
+                        dead = true;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll 1
                     for (int q = 0; q < D / 16; ++q) {
                         float o[16];
@@ -758,9 +789,15 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 float lsa, lsb;
                 unpack2(ls2, lsa, lsb);
                 l += lsa + lsb;
-                // V's rows past the chunk's tokens may hold padding (NaN * 0 is NaN)
+                // V's rows past the chunk's tokens may hold padding (NaN * 0 is
+                // NaN): zeroed once V's copy has landed (its buffer is not
+                // refilled before P.V of the chunk)
                 if (ntok < C::CT) {
-                    const uint32_t vb = ring + (uint32_t)((j % ST) * C::STAGE_BYTES + C::CHUNK_BYTES);
+                    if (!mbar_wait_bounded_sleep(FULLV((int)(j % VST)), (uint32_t)((j / VST) & 1), C::SLEEP_NS)) {
+                        dead = true;
+                        break;
+                    }
+                    const uint32_t vb = ring + (uint32_t)((KST + j % VST) * C::CHUNK_BYTES);
                     const int pieces = (C::CT - ntok) * C::LINES * 8;
                     for (int x = row; x < pieces; x += 128) {
                         const int r = ntok + x / (C::LINES * 8);
@@ -774,23 +811,19 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(PFULL(wg));
+                    mbar_arrive(PFULL((int)(j % NSB)));
                 ++nw;
                 had = true;
-                jprev = j;
             }
             if (dead)
                 break;
             if (had) {
+                // the group's last P.V: its O is final
                 if (!mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
                 tc_fence_after();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(SFREE((int)(jprev % NSB)));
             }
             j0 += n;
 
@@ -819,7 +852,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (w == C::MMA_WARP)
+    if (w == C::S_WARP)
         tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
