@@ -98,7 +98,7 @@ def kernel_source_hash(kernel: str = "split_kernel") -> str:
 
 # groups of at least this many query heads per K/V head run the tcgen05
 # kernel (contiguous 16-bit K/V, head dim 64 or 128)
-GQA_TC_MIN_G = 33
+GQA_TC_MIN_G = 17
 
 
 def kernel_key(w, fp8: bool, paged: bool, page_size: int = 0) -> str:

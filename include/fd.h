@@ -167,12 +167,12 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  * G == 1 is fd_decode.  For G >= 2 the per-chunk contraction runs on the
  * tensor cores, which need 16-bit operands: in_dtype f16 or bf16.  The
  * cache may hold any number of rows in all (the copies address a row by its
- * place in its (b, K/V head) block and the block's index).  Up to 32
+ * place in its (b, K/V head) block and the block's index).  Up to 16
  * query heads per K/V head (and any group with d = 256 or a paged cache),
  * the products are mma.sync and a K/V head's query heads are processed in
  * even slices of at most 16 (8 at d = 256), each reading that K/V head's
  * rows, side by side so that the repeated reads are mostly served from L2.
- * From 33 query heads per K/V head (MQA included; contiguous cache, d = 64
+ * From 17 query heads per K/V head (MQA included; contiguous cache, d = 64
  * or 128) they are tcgen05 products with accumulators in tensor memory, all
  * of a K/V head's query heads (slices of at most 128) served from one copy
  * of each K/V chunk.  The workspace size is

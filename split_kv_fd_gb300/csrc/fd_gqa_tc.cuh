@@ -53,7 +53,7 @@
 // Groups of at least this many query heads per K/V head run this kernel
 // (16-bit K/V, contiguous cache, head dim 64 or 128).
 #ifndef FD_GQA_TC_MIN_G
-#define FD_GQA_TC_MIN_G 33
+#define FD_GQA_TC_MIN_G 17
 #endif
 
 namespace fd {
