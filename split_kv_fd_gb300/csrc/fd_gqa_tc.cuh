@@ -25,19 +25,23 @@
 //    16-bit high part hold exactly enough; the quotient o = acc / l is the
 //    same.
 //
-// Warp roles (320 threads, one CTA per SM):
+// Warp roles (384 threads, one CTA per SM):
 //  - warps 0-3 and 4-7: two softmax warpgroups taking the chunks in turn
 //    (chunk j of the CTA goes to group j % 2), each with its own O
 //    accumulator and (m_ref, l) per head; at a segment end group 0 merges
 //    the two states ("FlashDecoding 数学推导" §2.4.2) and writes the result;
-//  - warp 8: the producer, K and V chunks by tensor-map TMA into a ring of
-//    STAGES stages;
-//  - warp 9: allocates TMEM; its lane 0 issues the MMAs, S of chunk j + 1
-//    ahead of P.V of chunk j (measured: two ahead was no faster).
-// TMEM holds four S/P buffers (chunk j in buffer j % 4) and the two O
-// accumulators.  A stage of the ring stays taken from its copy until P.V of
-// its chunk is done, and the copies take ~3 us to land at full load, so the
-// ring takes the shared memory left beside Q (160 KB at d = 128).  Every hand-off is an mbarrier (the MMA warp's through
+//  - warps 8 and 9: the K and V producers (lane 0 each), chunks by
+//    tensor-map TMA into rings of their own: a K buffer is refilled once S
+//    of its chunk is done, a V buffer once P.V is;
+//  - warp 10: allocates TMEM; its lane 0 issues S = Q K^T, up to NSB chunks
+//    ahead of P.V;
+//  - warp 11: lane 0 issues P.V and frees the chunk's V and S buffers by
+//    its commits.
+// TMEM holds NSB S/P buffers (chunk j in buffer j % NSB) and the two O
+// accumulators.  The copies take ~3 us to land at full load, so the two
+// rings take the shared memory left beside Q (160 KB at d = 128); after
+// the CTA's last segment the idle rings stage the pieces of a last
+// arriver's merge.  Every hand-off is an mbarrier (the MMA warps' through
 // tcgen05.commit), and every wait is bounded: on expiry a role records
 // FD_ERR_DEVICE_TIMEOUT, stops, drains what it issued, and the CTA frees its
 // TMEM.
@@ -91,8 +95,8 @@ template <typename T, int D> struct TcCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     // mbarriers: full/empty of the K and V buffers, s_full[NSB],
     // s_free[NSB], p_full[NSB], o_full[2], q_full, fin (2), seg (both
-    // groups), wg0 (group 0)
-    static constexpr int NBAR = 2 * RING_BUFS + 3 * NSB + 7;
+    // groups), wg0 (group 0), the two of a merge staged in the ring
+    static constexpr int NBAR = 2 * RING_BUFS + 3 * NSB + 9;
     static constexpr float TAU = 8.f;              // lazy-rescale threshold (base 2)
     // every wait suspends the waiting thread in hardware (woken when the
     // phase completes) rather than polling
@@ -260,6 +264,131 @@ __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int 
     return wb.sync(tid & 31);
 }
 
+// Shared memory a merge may stage the pieces in: the CTA's K/V ring once its
+// last segment is done (no copy in flight, no MMA reading it), with two
+// mbarriers of its own.  p == nullptr: none (the merge reads the pieces
+// from global memory).
+struct MergeStage {
+    unsigned char *p = nullptr;
+    uint32_t a = 0;       // shared-space address of p
+    int bytes = 0;
+    uint32_t mb[2] = {0u, 0u};
+};
+
+// The same batch as tc_merge_batch, with the pieces' o rows staged in
+// shared memory: first the weights, one thread per head (each piece's
+// 2^(m_i - M) l_i / L, M the max over the pieces that hold tokens, L the sum
+// of 2^(m_i - M) l_i: the merge of "FlashDecoding 数学推导" §2.4.2 with the
+// normalisation folded in), while bulk copies bring a block of HB heads of
+// every piece into one of two buffers; then each block is summed while the
+// next one lands.  Every load of the batch is in flight at once, where the
+// loop of tc_merge_batch waits for a round trip per 256 groups of 4
+// elements.  The results differ from tc_merge_batch's only in the order of
+// the fp32 operations.  `mph` holds the two mbarriers' phases.  Returns
+// false if a wait expired.
+template <int D>
+__device__ __forceinline__ bool tc_merge_staged(const SplitParams &p, int G, int Gv, long long qrow0,
+                                                const long long *ss, int n, long long into, int tid, WarpBar &wb,
+                                                const MergeStage &st, uint32_t &mph)
+{
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);
+    float2 *wml = reinterpret_cast<float2 *>(st.p);   // [n][Gv]: (m, l), then (weight, -)
+    const int wml_bytes = (n * Gv * 8 + 127) & ~127;
+    const int buf_bytes = ((st.bytes - wml_bytes) / 2) & ~127;
+    const int head_bytes = n * D * 4;                  // one head of every piece
+    int hb = min(Gv, buf_bytes / head_bytes);
+    const int nblk = (Gv + hb - 1) / hb;
+    hb = (Gv + nblk - 1) / nblk;                       // blocks of even size
+    auto issue = [&](int blk) {
+        const int h0 = blk * hb, nh = min(hb, Gv - h0);
+        const uint32_t bytes = (uint32_t)(nh * D * 4), bar = st.mb[blk & 1];
+        const uint32_t dst = st.a + (uint32_t)(wml_bytes + (blk & 1) * buf_bytes);
+        mbar_arrive_expect_tx(bar, bytes * (uint32_t)n);
+        for (int i = 0; i < n; ++i)
+            bulk_g2s(dst + (uint32_t)i * bytes, p.ws_o + (ss[i] * G + h0) * D, bytes, bar);
+    };
+    if (tid == 0) {
+        fence_proxy_async_global();   // the pieces' writers' stores, acquired by the arrival
+        issue(0);
+        if (nblk > 1)
+            issue(1);
+    }
+    if (tid < Gv) {
+        float M = -INFINITY;
+        for (int i0 = 0; i0 < n; i0 += 8) {
+            float2 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = __ldcg(ml + ss[min(i0 + u, n - 1)] * G + tid);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u < n) {
+                    if (v[u].y > 0.f)
+                        M = fmaxf(M, v[u].x);
+                    wml[(i0 + u) * Gv + tid] = v[u];
+                }
+        }
+        float L = 0.f;
+        for (int i = 0; i < n; ++i) {
+            const float2 v = wml[i * Gv + tid];
+            const float wgt = v.y > 0.f ? ex2(v.x - M) * v.y : 0.f;
+            wml[i * Gv + tid].x = wgt;
+            L += wgt;
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int i = 0; i < n; ++i)
+            wml[i * Gv + tid].x *= inv;
+        if (into >= 0) {
+            // this thread alone read the slot's (m, l) for this head
+            const long long r = into * G + tid;
+            p.ws_ml[2 * r] = L > 0.f ? M : -INFINITY;
+            p.ws_ml[2 * r + 1] = L;
+        } else if (p.lse) {
+            p.lse[qrow0 + tid] = L > 0.f ? (M + log2f(L)) * LN2_F : -INFINITY;
+        }
+    }
+    if (!wb.sync(tid & 31))
+        return false;
+#pragma unroll 1
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int h0 = blk * hb, nh = min(hb, Gv - h0);
+        const uint32_t par = (mph >> (blk & 1)) & 1u;
+        mph ^= 1u << (blk & 1);
+        if (!mbar_wait_bounded(st.mb[blk & 1], par))
+            return false;
+        const float *buf = reinterpret_cast<const float *>(st.p + wml_bytes + (blk & 1) * buf_bytes);
+        const int ngrp = nh * D / 4;
+        for (int grp = tid; grp < ngrp; grp += 128) {
+            const int g = h0 + grp * 4 / D, dim = grp * 4 % D;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int i = 0; i < n; ++i) {
+                const float wgt = wml[i * Gv + g].x;
+                const float4 v = *reinterpret_cast<const float4 *>(buf + i * nh * D + grp * 4);
+                acc.x = fmaf(wgt, v.x, acc.x);
+                acc.y = fmaf(wgt, v.y, acc.y);
+                acc.z = fmaf(wgt, v.z, acc.z);
+                acc.w = fmaf(wgt, v.w, acc.w);
+            }
+            if (into >= 0)
+                *reinterpret_cast<float4 *>(p.ws_o + (into * G + g) * D + dim) = acc;
+            else
+                store_out4(p.out, (qrow0 + g) * D + dim, p.out_dtype, acc);
+        }
+        if (blk + 2 < nblk) {
+            // every thread is done with the buffer before it is refilled
+            if (!wb.sync(tid & 31))
+                return false;
+            if (tid == 0)
+                issue(blk + 2);
+        }
+    }
+    if (into < 0)
+        return true;
+    fence_proxy_async_global();   // the next batch copies this slot back in
+    return wb.sync(tid & 31);
+}
+
 // Stage 2 of a (b, virtual head) by the last piece to arrive, on softmax
 // group 0: the merge of its `target` workspace partials, in batches of at
 // most MERGE_PB pieces; each batch but the last leaves its result in its
@@ -268,7 +397,8 @@ __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int 
 template <int D, int MERGE_PB>
 __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &ctx, long long bhv, int slice,
                                                 int G, int Gv, long long qrow0, unsigned target, int gf,
-                                                long long off, int tid, unsigned char *scr, WarpBar &wb)
+                                                long long off, int tid, unsigned char *scr, WarpBar &wb,
+                                                const MergeStage &st)
 {
     const SplitParams &p = gp.s;
     long long *ss = reinterpret_cast<long long *>(scr);            // [MERGE_PB] slots
@@ -276,6 +406,7 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
     float *sL = sM + G;                                              // [G]
     const int n = (int)target;
     int first = 0;
+    uint32_t mph = 0;   // the staging mbarriers' phases (one staged merge per CTA)
     for (;;) {
         const int cnt = min(n - first, MERGE_PB);
         for (int i = tid; i < cnt; i += 128)
@@ -283,7 +414,13 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
         if (!wb.sync(tid & 31))
             return false;
         const bool last = first + cnt == n;
-        if (!tc_merge_batch<D>(p, G, Gv, qrow0, ss, cnt, last ? -1 : ss[cnt - 1], sM, sL, tid, wb))
+        // staged when the ring is idle and a block of one head of every
+        // piece fits beside the weights
+        const int wml_bytes = (cnt * Gv * 8 + 127) & ~127;
+        const bool staged = st.p != nullptr && ((st.bytes - wml_bytes) / 2 & ~127) >= cnt * D * 4;
+        const long long into = last ? -1 : ss[cnt - 1];
+        if (!(staged ? tc_merge_staged<D>(p, G, Gv, qrow0, ss, cnt, into, tid, wb, st, mph)
+                     : tc_merge_batch<D>(p, G, Gv, qrow0, ss, cnt, into, sM, sL, tid, wb)))
             return false;
         if (last)
             return true;
@@ -311,7 +448,8 @@ __device__ __forceinline__ void tc_seg_dest(const SplitParams &p, const Seg &cs,
 template <int D, int MERGE_PB>
 __device__ __forceinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int gv,
                                              long long qrow0, long long bhv, int len, int lane, int tid,
-                                             uint32_t *misc, unsigned char *scratch, WarpBar &wb)
+                                             uint32_t *misc, unsigned char *scratch, WarpBar &wb,
+                                             const MergeStage st = MergeStage())
 {
     const SplitParams &p = gp.s;
     unsigned target;
@@ -339,7 +477,7 @@ __device__ __forceinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx c
     if (misc[1]) {
         __threadfence();
         if (!tc_merge_pieces<D, MERGE_PB>(gp, ctx, bhv, slice, gp.G, gv, qrow0, target, gf, off, tid, scratch,
-                                          wb))
+                                          wb, st))
             return false;
     }
     return wb.sync(lane);   // the flag and the scratch are reused
@@ -354,7 +492,7 @@ template <typename C, int D>
 __device__ __forceinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int G, int gv,
                                             long long qrow0, long long bhv, bool had, float m_ref, float l, float m1,
                                             float l1, int row, int lane, int tid, uint32_t tl, uint32_t *misc,
-                                            unsigned char *scratch, WarpBar &wb)
+                                            unsigned char *scratch, WarpBar &wb, const MergeStage &st)
 {
     const SplitParams &p = gp.s;
     const bool live = row < gv;
@@ -405,8 +543,11 @@ __device__ __forceinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ct
             p.ws_ml[2 * r + 1] = L;
         }
     }
-    if (!complete)
-        return tc_arrive_merge<D, C::MERGE_PB>(gp, ctx, cs, slice, gv, qrow0, bhv, len, lane, tid, misc, scratch, wb);
+    if (!complete) {
+        fence_proxy_async_global();   // the last arriver may bulk-copy this partial
+        return tc_arrive_merge<D, C::MERGE_PB>(gp, ctx, cs, slice, gv, qrow0, bhv, len, lane, tid, misc, scratch, wb,
+                                               st);
+    }
     return true;
 }
 
@@ -452,7 +593,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     const uint32_t FINP = bar0 + 8u * (B0 + 4);
     const uint32_t SEGBAR = bar0 + 8u * (B0 + 5);
     const uint32_t WG0BAR = bar0 + 8u * (B0 + 6);
-    static_assert(B0 + 7 == C::NBAR, "barrier count");
+    const uint32_t MRG0 = bar0 + 8u * (B0 + 7), MRG1 = bar0 + 8u * (B0 + 8);
+    static_assert(B0 + 9 == C::NBAR, "barrier count");
 
     if (tid == 0) {
         for (int s = 0; s < KST; ++s) {
@@ -475,6 +617,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         mbar_init(FINP, 1);
         mbar_init(SEGBAR, 8);         // both groups at a segment end
         mbar_init(WG0BAR, 4);         // group 0 (arrival and merge)
+        mbar_init(MRG0, 1);           // a merge's bulk copies into the idle ring
+        mbar_init(MRG1, 1);
         prefetch_tmap(&gp.tmk);
         prefetch_tmap(&gp.tmv);
     }
@@ -838,12 +982,24 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 dead = true;
                 break;
             }
+            Seg nx = cs;
+            seg_next(p, ctx, nx);
+            // after the CTA's last segment no copy is in flight into the
+            // ring and no MMA reads it: a merge may stage its pieces there
+            MergeStage st;
+            if (!nx.valid) {
+                st.p = smem;
+                st.a = ring;
+                st.bytes = C::RING_BYTES;
+                st.mb[0] = MRG0;
+                st.mb[1] = MRG1;
+            }
             if (wg == 0 && !tc_segment_end<C, D>(gp, ctx, cs, slice, G, gv, qrow0, bhv, had, m_ref, l, xk[2 * row],
-                                                   xk[2 * row + 1], row, lane, tid, tl, misc, scratch, wb)) {
+                                                   xk[2 * row + 1], row, lane, tid, tl, misc, scratch, wb, st)) {
                 dead = true;
                 break;
             }
-            seg_next(p, ctx, cs);
+            cs = nx;
         }
     }
 

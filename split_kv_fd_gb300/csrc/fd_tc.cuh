@@ -44,6 +44,13 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same for global memory: generic-proxy writes (or, after an acquire,
+// those of other threads) against bulk copies that read them.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05): start address, leading- and
 // stride-dimension byte offsets (all in 16-byte units), the fixed version

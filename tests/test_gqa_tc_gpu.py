@@ -78,12 +78,15 @@ def test_peaked_scores_rescale_o_in_tmem():
     _run(q, k, v, lt, "bf16")
 
 
+@pytest.mark.parametrize("G,d", [(64, 128), (128, 64), (128, 128)])
 @pytest.mark.parametrize("num_splits", [0, 40, 100])
-def test_long_sequence_many_pieces(num_splits):
-    """One 150K-token sequence: cut into one piece per CTA (automatic: 152
-    pieces, three merge batches), into 40 explicit splits (one batch) and
-    into 100 (two batches)."""
-    q, k, v, lt = _gqa_case(1, 64, 1, 150000, 128, "bf16", None, seed=11)
+def test_long_sequence_many_pieces(G, d, num_splits):
+    """One long sequence: cut into one piece per CTA (automatic: 152 pieces,
+    three merge batches), into 40 explicit splits (one batch) and into 100
+    (two batches).  The last arriver is at its last segment, so it stages
+    the pieces in its idle ring: blocks of 16 heads (40 pieces of 64 heads)
+    down to one head per block (64 pieces of 128 heads at d = 128)."""
+    q, k, v, lt = _gqa_case(1, G, 1, 150000 if G == 64 else 60000, d, "bf16", None, seed=11 + G + d)
     _run(q, k, v, lt, "bf16", num_splits)
 
 
