@@ -148,6 +148,19 @@ bool gqa_use_tc(int in_dtype, int d, int G, bool paged)
            G >= FD_GQA_TC_MIN_G;
 }
 
+// What the balanced decomposition charges the tcgen05 kernel for each (b, K/V
+// head) sequence a CTA starts, in tokens: measured at full load, a CTA's
+// switch of sequences (the segment end with its partial's stores and
+// arrival, the query reload, the pipeline's refill) takes about as long as
+// streaming FD_TC_SEG_COST_KB of K and V.
+#ifndef FD_TC_SEG_COST_KB
+#define FD_TC_SEG_COST_KB 768
+#endif
+int tc_seg_cost(int d)
+{
+    return (int)(FD_TC_SEG_COST_KB * 1024LL / (2LL * 2 * d));   // K and V rows of 16-bit elements
+}
+
 // The block-table view of a paged K/V cache.
 struct PagedKV {
     const int32_t *table;
@@ -389,6 +402,8 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     gp.k_scale = k_scale;
     gp.v_scale = v_scale;
     set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
+    if (tc && pl.decomp == DECOMP_BALANCED)
+        p.seg_cost = tc_seg_cost(d);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (!clear_counters(p, (long long)B * Hv, cs))
         return FD_ERR_CUDA;

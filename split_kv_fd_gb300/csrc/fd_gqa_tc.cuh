@@ -437,7 +437,7 @@ __device__ __forceinline__ void tc_seg_dest(const SplitParams &p, const Seg &cs,
         complete = (p.P == 1);
         slot = bhv * p.P + cs.p;
     } else {
-        complete = (cs.t0 == 0 && cs.t1 == len);
+        complete = seg_whole(p, cs, len);
         slot = 2LL * blockIdx.x + (cs.k == 0 ? 0 : 1);
     }
 }
@@ -458,9 +458,9 @@ __device__ __forceinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx c
     if (p.decomp == DECOMP_SPLITS) {
         target = (unsigned)p.P;
     } else {
-        off = ctx.cumH[cs.b] + (long long)cs.h * len;
+        off = bal_offset(p, ctx, cs.b, cs.h, len);
         gf = bal_owner(off, ctx.T, ctx.Geff);
-        const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
+        const int gl = bal_owner(off + bal_span(p, len) - 1, ctx.T, ctx.Geff);
         target = (unsigned)(gl - gf + 1);
     }
     // the barrier orders every thread's partial before thread 0's fence and

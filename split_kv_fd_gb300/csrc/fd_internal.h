@@ -40,6 +40,7 @@ struct SplitParams {
     const float *k_scale; // [B*H] K dequantisation scales, or null (1)
     const float *v_scale; // [B*H] V dequantisation scales, or null (1)
     int decomp;
+    int seg_cost;         // DECOMP_BALANCED: tokens charged for starting each (b, h) sequence
     int P;                // splits per sequence for DECOMP_SPLITS
     int grid;             // number of CTAs launched (G)
     int out_kind;

@@ -143,6 +143,7 @@ struct Seg {
     int k;            // ordinal of the segment within the CTA's list
     int p;            // split index (DECOMP_SPLITS)
     long long pos;    // start in the concatenated token space (DECOMP_BALANCED)
+    int span;         // its extent there (DECOMP_BALANCED)
     bool valid;
 };
 
@@ -153,9 +154,43 @@ struct Ctx {
     int Geff;         // CTAs with work (balanced: min(G, T))
     long long T;      // total tokens over all (b, h) (balanced)
     long long beg, end;  // this CTA's range in the concatenated space
-    const long long *cumH;  // [B+1] H * prefix sum of lengths (balanced)
+    const long long *cumH;  // [B+1] H * prefix sum of spans (balanced)
     const int *lenS;        // [B] clamped lengths (balanced)
 };
+
+// Extent of a (b, h) sequence of n tokens in the balanced decomposition's
+// concatenated space: its tokens after a charge of seg_cost for starting it
+// (the segment end before it, the query reload, the pipeline's refill), so
+// that a CTA that switches sequences is given fewer tokens.  A segment
+// covering [v0, v1) of that extent holds tokens [v0 - c, v1 - c) clamped at
+// 0; one that falls inside the charge holds none and still counts as a
+// piece.
+__device__ __forceinline__ int bal_span(const SplitParams &p, int n)
+{
+    return n > 0 ? n + p.seg_cost : 0;
+}
+
+__device__ __forceinline__ void bal_tokens(const SplitParams &p, Seg &s, int v0, int v1)
+{
+    s.t0 = v0 > p.seg_cost ? v0 - p.seg_cost : 0;
+    s.t1 = v1 > p.seg_cost ? v1 - p.seg_cost : 0;
+    s.span = v1 - v0;
+}
+
+// Whether segment s is its whole (b, h) sequence of `len` tokens (its
+// result then goes straight to the output).
+__device__ __forceinline__ bool seg_whole(const SplitParams &p, const Seg &s, int len)
+{
+    if (p.decomp == DECOMP_SPLITS)
+        return p.P == 1;
+    return s.span == bal_span(p, len);
+}
+
+// Offset of (b, h) in the concatenated space.
+__device__ __forceinline__ long long bal_offset(const SplitParams &p, const Ctx &c, int b, int h, int len)
+{
+    return c.cumH[b] + (long long)h * bal_span(p, len);
+}
 
 __device__ __forceinline__ int clamp_len(const SplitParams &p, int b)
 {
@@ -222,12 +257,12 @@ __device__ __forceinline__ void seg_first(const SplitParams &p, const Ctx &c, Se
         return;
     s.pos = c.beg;
     s.b = find_batch(c.cumH, p.B, s.pos);
-    const int len = c.lenS[s.b];
+    const int span = bal_span(p, c.lenS[s.b]);
     const long long rel = s.pos - c.cumH[s.b];
-    s.h = (int)(rel / len);
-    s.t0 = (int)(rel % len);
+    s.h = (int)(rel / span);
+    const int v0 = (int)(rel % span);
     const long long room = c.end - s.pos;
-    s.t1 = (long long)(len - s.t0) < room ? len : (int)(s.t0 + room);
+    bal_tokens(p, s, v0, (long long)(span - v0) < room ? span : (int)(v0 + room));
 }
 
 __device__ __forceinline__ void seg_next(const SplitParams &p, const Ctx &c, Seg &s)
@@ -240,7 +275,7 @@ __device__ __forceinline__ void seg_next(const SplitParams &p, const Ctx &c, Seg
             split_item(p, item, s);
         return;
     }
-    s.pos += s.t1 - s.t0;
+    s.pos += s.span;
     if (s.pos >= c.end) {
         s.valid = false;
         return;
@@ -253,10 +288,9 @@ __device__ __forceinline__ void seg_next(const SplitParams &p, const Ctx &c, Seg
             s.b += 1;
         } while (c.lenS[s.b] == 0);
     }
-    const int len = c.lenS[s.b];
-    s.t0 = 0;
+    const int span = bal_span(p, c.lenS[s.b]);
     const long long room = c.end - s.pos;
-    s.t1 = (long long)len < room ? len : (int)room;
+    bal_tokens(p, s, 0, (long long)span < room ? span : (int)room);
 }
 
 // Balanced decomposition set-up, run by every thread of the CTA: clamped
@@ -277,7 +311,7 @@ __device__ __forceinline__ void balanced_setup(const SplitParams &p, Ctx &ctx, l
         if (b < p.B) {
             const int n = clamp_len(p, b);
             lenS[b] = n;
-            x = (long long)n * p.H;
+            x = (long long)bal_span(p, n) * p.H;
         }
         v[i] = run;
         run += x;
@@ -676,7 +710,7 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
             complete = (p.P == 1);
             slot = (long long)bh * p.P + s.p;
         } else {
-            complete = (s.t0 == 0 && s.t1 == len);
+            complete = seg_whole(p, s, len);
             slot = 2LL * ctx.g + (s.k == 0 ? 0 : 1);
         }
         // V's dequantisation scale is common to every row of (b, h)
@@ -752,9 +786,9 @@ __device__ __forceinline__ void merge_warp(const SplitParams &p, const Ctx &ctx,
             if (p.decomp == DECOMP_SPLITS) {
                 target = (unsigned)p.P;
             } else {
-                off = ctx.cumH[s.b] + (long long)s.h * len;
+                off = bal_offset(p, ctx, s.b, s.h, len);
                 gf = bal_owner(off, ctx.T, ctx.Geff);
-                const int gl = bal_owner(off + len - 1, ctx.T, ctx.Geff);
+                const int gl = bal_owner(off + bal_span(p, len) - 1, ctx.T, ctx.Geff);
                 target = (unsigned)(gl - gf + 1);
             }
             __threadfence();
