@@ -83,7 +83,7 @@ template <typename T, int D> struct TcCfg {
     static constexpr int Q_BYTES = LINES * QPLANE;
     static constexpr int MERGE_PB = 64;            // pieces per batch of the last arriver's merge
     static constexpr int SCR_BYTES = MERGE_PB * 8 + 2 * MAXG * 4;   // their slots, then M and L per head
-    static constexpr int XCH_BYTES = 2 * M * 2 * 4;   // group 1's (m_ref, l) per head, two segments
+    static constexpr int XCH_BYTES = 2 * 2 * M * 2 * 4;   // both groups' (m_ref, l) per head, two segments
     // warps 0-7: the two softmax groups; 8, 9: the K and V producers; 10:
     // the S issuer (it allocates TMEM); 11: the P.V issuer
     static constexpr int WG_THREADS = 128, KPROD_WARP = 8, VPROD_WARP = 9, S_WARP = 10, PV_WARP = 11;
@@ -95,8 +95,8 @@ template <typename T, int D> struct TcCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     // mbarriers: full/empty of the K and V buffers, s_full[NSB],
     // s_free[NSB], p_full[NSB], o_full[2], q_full, fin (2), seg (both
-    // groups), wg0 (group 0), the two of a merge staged in the ring
-    static constexpr int NBAR = 2 * RING_BUFS + 3 * NSB + 9;
+    // groups), the two of a merge staged in the ring
+    static constexpr int NBAR = 2 * RING_BUFS + 3 * NSB + 8;
     static constexpr float TAU = 8.f;              // lazy-rescale threshold (base 2)
     // every wait suspends the waiting thread in hardware (woken when the
     // phase completes) rather than polling
@@ -176,21 +176,21 @@ __device__ __forceinline__ void store_out4(void *out, long long idx, int out_dty
 // into the workspace slot `into` as a normalised partial (o, m, l) that a
 // later batch merges (each head's (m, l) through sM, sL, written once every
 // thread has read the slot's).  Returns false if a barrier wait expired.
-template <int D>
+template <int D, int NT>
 __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int Gv, long long qrow0, const long long *ss,
                                                int n, long long into, float *sM, float *sL, int tid, WarpBar &wb)
 {
     const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml);   // (m, l) per workspace row
     constexpr int GB = 2, PB = 8;   // groups of 4 elements, pieces per round
     const int ngrp = Gv * D / 4;
-    for (int base = 0; base < ngrp; base += 128 * GB) {
+    for (int base = 0; base < ngrp; base += NT * GB) {
         float4 acc[GB];
         int gg[GB], dd[GB];
         float Mr[GB], Lr[GB];
 #pragma unroll
         for (int e = 0; e < GB; ++e) {
             acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-            const int grp = min(base + e * 128 + tid, ngrp - 1);
+            const int grp = min(base + e * NT + tid, ngrp - 1);
             gg[e] = grp * 4 / D;
             dd[e] = grp * 4 % D;
             Mr[e] = -INFINITY;
@@ -228,7 +228,7 @@ __device__ __forceinline__ bool tc_merge_batch(const SplitParams &p, int G, int 
         }
 #pragma unroll
         for (int e = 0; e < GB; ++e) {
-            const int grp = base + e * 128 + tid;
+            const int grp = base + e * NT + tid;
             const bool mine = grp < ngrp;
             const int g = gg[e], dim = dd[e];
             const float L = Lr[e];
@@ -286,7 +286,7 @@ struct MergeStage {
 // elements.  The results differ from tc_merge_batch's only in the order of
 // the fp32 operations.  `mph` holds the two mbarriers' phases.  Returns
 // false if a wait expired.
-template <int D>
+template <int D, int NT>
 __device__ __forceinline__ bool tc_merge_staged(const SplitParams &p, int G, int Gv, long long qrow0,
                                                 const long long *ss, int n, long long into, int tid, WarpBar &wb,
                                                 const MergeStage &st, uint32_t &mph)
@@ -358,7 +358,7 @@ __device__ __forceinline__ bool tc_merge_staged(const SplitParams &p, int G, int
             return false;
         const float *buf = reinterpret_cast<const float *>(st.p + wml_bytes + (blk & 1) * buf_bytes);
         const int ngrp = nh * D / 4;
-        for (int grp = tid; grp < ngrp; grp += 128) {
+        for (int grp = tid; grp < ngrp; grp += NT) {
             const int g = h0 + grp * 4 / D, dim = grp * 4 % D;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
@@ -394,7 +394,7 @@ __device__ __forceinline__ bool tc_merge_staged(const SplitParams &p, int G, int
 // most MERGE_PB pieces; each batch but the last leaves its result in its
 // last piece's slot, which starts the next batch.  Returns false if a
 // barrier wait expired.
-template <int D, int MERGE_PB>
+template <int D, int MERGE_PB, int NT>
 __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &ctx, long long bhv, int slice,
                                                 int G, int Gv, long long qrow0, unsigned target, int gf,
                                                 long long off, int tid, unsigned char *scr, WarpBar &wb,
@@ -409,7 +409,7 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
     uint32_t mph = 0;   // the staging mbarriers' phases (one staged merge per CTA)
     for (;;) {
         const int cnt = min(n - first, MERGE_PB);
-        for (int i = tid; i < cnt; i += 128)
+        for (int i = tid; i < cnt; i += NT)
             ss[i] = vh_slot(gp, ctx, bhv, (unsigned)(first + i), gf, off, slice);
         if (!wb.sync(tid & 31))
             return false;
@@ -419,8 +419,8 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
         const int wml_bytes = (cnt * Gv * 8 + 127) & ~127;
         const bool staged = st.p != nullptr && ((st.bytes - wml_bytes) / 2 & ~127) >= cnt * D * 4;
         const long long into = last ? -1 : ss[cnt - 1];
-        if (!(staged ? tc_merge_staged<D>(p, G, Gv, qrow0, ss, cnt, into, tid, wb, st, mph)
-                     : tc_merge_batch<D>(p, G, Gv, qrow0, ss, cnt, into, sM, sL, tid, wb)))
+        if (!(staged ? tc_merge_staged<D, NT>(p, G, Gv, qrow0, ss, cnt, into, tid, wb, st, mph)
+                     : tc_merge_batch<D, NT>(p, G, Gv, qrow0, ss, cnt, into, sM, sL, tid, wb)))
             return false;
         if (last)
             return true;
@@ -442,10 +442,11 @@ __device__ __forceinline__ void tc_seg_dest(const SplitParams &p, const Seg &cs,
     }
 }
 
-// After a segment's partial is in the workspace, on softmax group 0: the
-// arrival on the (b, virtual head)'s counter and, for the last piece to
-// arrive, the merge of the pieces.  Returns false if a barrier wait expired.
-template <int D, int MERGE_PB>
+// After a segment's partial is in the workspace, on the NT threads that
+// wrote it (barrier `wb`): the arrival on the (b, virtual head)'s counter
+// and, for the last piece to arrive, the merge of the pieces.  Returns
+// false if a barrier wait expired.
+template <int D, int MERGE_PB, int NT>
 __device__ __forceinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int gv,
                                              long long qrow0, long long bhv, int len, int lane, int tid,
                                              uint32_t *misc, unsigned char *scratch, WarpBar &wb,
@@ -476,33 +477,35 @@ __device__ __forceinline__ bool tc_arrive_merge(const GqaParams &gp, const Ctx c
         return false;
     if (misc[1]) {
         __threadfence();
-        if (!tc_merge_pieces<D, MERGE_PB>(gp, ctx, bhv, slice, gp.G, gv, qrow0, target, gf, off, tid, scratch,
-                                          wb, st))
+        if (!tc_merge_pieces<D, MERGE_PB, NT>(gp, ctx, bhv, slice, gp.G, gv, qrow0, target, gf, off, tid, scratch,
+                                              wb, st))
             return false;
     }
     return wb.sync(lane);   // the flag and the scratch are reused
 }
 
-// Segment end on softmax group 0 (out of line, so that its registers do not
-// crowd the chunk loop): merges the two groups' (m_ref, l, O) per head
-// ("FlashDecoding 数学推导" §2.4.2), then writes out/lse for a whole (b, h),
-// or a workspace partial and, for the last piece to arrive, runs the merge
-// of the pieces.  Returns false if a barrier wait expired.
+// Segment end on both softmax groups (256 threads, barrier `sb`): merges
+// the two groups' (m_ref, l, O) per head ("FlashDecoding 数学推导" §2.4.2),
+// group g reading and writing columns [g d/2, (g+1) d/2) of both O
+// accumulators, then writes out/lse for a whole (b, h), or a workspace
+// partial and, for the last piece to arrive, runs the merge of the pieces
+// on all 256 threads.  (m0, l0) and (m1, l1) are the groups' states
+// (l = 0: the group had no chunk).  Returns false if a barrier wait expired.
 template <typename C, int D>
 __device__ __forceinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ctx, const Seg cs, int slice, int G, int gv,
-                                            long long qrow0, long long bhv, bool had, float m_ref, float l, float m1,
-                                            float l1, int row, int lane, int tid, uint32_t tl, uint32_t *misc,
-                                            unsigned char *scratch, WarpBar &wb, const MergeStage &st)
+                                            long long qrow0, long long bhv, float m0, float l0, float m1, float l1,
+                                            int wg, int row, int lane, int tid, uint32_t tl, uint32_t *misc,
+                                            unsigned char *scratch, WarpBar &sb, const MergeStage &st)
 {
     const SplitParams &p = gp.s;
     const bool live = row < gv;
-    const float m0 = had ? m_ref : -INFINITY, l0 = had ? l : 0.f;
     const float M = fmaxf(l0 > 0.f ? m0 : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
     const float a0 = l0 > 0.f ? ex2(m0 - M) : 0.f;
     const float a1 = l1 > 0.f ? ex2(m1 - M) : 0.f;
     const float L = a0 * l0 + a1 * l1;
     const bool nonempty = L > 0.f;
     const float f0 = nonempty ? a0 / L : 0.f, f1 = nonempty ? a1 / L : 0.f;
+    // warps w and w + 4 hold the same rows: the same votes
     const bool need0 = __any_sync(FULL_MASK, l0 > 0.f), need1 = __any_sync(FULL_MASK, l1 > 0.f);
     const int len = (p.decomp == DECOMP_BALANCED) ? ctx.lenS[cs.b] : clamp_len(p, cs.b);
     bool complete;
@@ -510,8 +513,9 @@ __device__ __forceinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ct
     tc_seg_dest(p, cs, bhv, len, complete, slot);
     const long long qrow = qrow0 + row;
     const long long r = slot * G + row;
+    constexpr int QH = D / 32;   // 16-column slices per group
 #pragma unroll 1
-    for (int q = 0; q < D / 16; ++q) {
+    for (int q = wg * QH; q < (wg + 1) * QH; ++q) {
         float o0[16], o1[16];
         if (need0)
             tmem_ld16(tl + (uint32_t)(C::TMEM_O + 16 * q), o0);
@@ -534,7 +538,7 @@ __device__ __forceinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ct
         }
     }
     tc_fence_before();
-    if (live) {
+    if (live && wg == 0) {
         if (complete) {
             if (p.lse)
                 p.lse[qrow] = nonempty ? (M + log2f(L)) * LN2_F : -INFINITY;
@@ -545,8 +549,8 @@ __device__ __forceinline__ bool tc_segment_end(const GqaParams &gp, const Ctx ct
     }
     if (!complete) {
         fence_proxy_async_global();   // the last arriver may bulk-copy this partial
-        return tc_arrive_merge<D, C::MERGE_PB>(gp, ctx, cs, slice, gv, qrow0, bhv, len, lane, tid, misc, scratch, wb,
-                                               st);
+        return tc_arrive_merge<D, C::MERGE_PB, 2 * C::WG_THREADS>(gp, ctx, cs, slice, gv, qrow0, bhv, len, lane, tid,
+                                                                  misc, scratch, sb, st);
     }
     return true;
 }
@@ -568,7 +572,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     const uint32_t ring = smem_addr(smem);
     const uint32_t qbuf = ring + C::RING_BYTES;
     unsigned char *scratch = smem + C::RING_BYTES + C::Q_BYTES;   // the last arriver's merge
-    float *xch = reinterpret_cast<float *>(scratch + C::SCR_BYTES);   // [2][M][2]
+    float *xch = reinterpret_cast<float *>(scratch + C::SCR_BYTES);   // [2][2][M][2]
     uint64_t *bars = reinterpret_cast<uint64_t *>(scratch + C::SCR_BYTES + C::XCH_BYTES);
     uint32_t *misc = reinterpret_cast<uint32_t *>(bars + C::NBAR);   // [0] TMEM base, [1] flag
     long long *cumH = reinterpret_cast<long long *>(misc + 4);
@@ -592,9 +596,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     const uint32_t FINS = bar0 + 8u * (B0 + 3);
     const uint32_t FINP = bar0 + 8u * (B0 + 4);
     const uint32_t SEGBAR = bar0 + 8u * (B0 + 5);
-    const uint32_t WG0BAR = bar0 + 8u * (B0 + 6);
-    const uint32_t MRG0 = bar0 + 8u * (B0 + 7), MRG1 = bar0 + 8u * (B0 + 8);
-    static_assert(B0 + 9 == C::NBAR, "barrier count");
+    const uint32_t MRG0 = bar0 + 8u * (B0 + 6), MRG1 = bar0 + 8u * (B0 + 7);
+    static_assert(B0 + 8 == C::NBAR, "barrier count");
 
     if (tid == 0) {
         for (int s = 0; s < KST; ++s) {
@@ -612,11 +615,10 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         }
         for (int g = 0; g < 2; ++g)
             mbar_init(OFULL(g), 1);   // commit after the group's P.V
-        mbar_init(QFULL, 4);          // group 0 has written Q
+        mbar_init(QFULL, 8);          // both groups have written their halves of Q
         mbar_init(FINS, 1);           // the MMA issuers' last commits
         mbar_init(FINP, 1);
-        mbar_init(SEGBAR, 8);         // both groups at a segment end
-        mbar_init(WG0BAR, 4);         // group 0 (arrival and merge)
+        mbar_init(SEGBAR, 8);         // both groups: segment ends, arrivals, merges
         mbar_init(MRG0, 1);           // a merge's bulk copies into the idle ring
         mbar_init(MRG1, 1);
         prefetch_tmap(&gp.tmk);
@@ -797,7 +799,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         const int row = tid & 127;         // query head within the slice = TMEM lane
         const uint32_t tl = tmem + ((uint32_t)((w & 3) * 32) << 16);
         const uint32_t ocol = (uint32_t)(C::TMEM_O + wg * D);
-        WarpBar sb{SEGBAR, 0u, C::SLEEP_NS}, wb{WG0BAR, 0u, C::SLEEP_NS};
+        WarpBar sb{SEGBAR, 0u, C::SLEEP_NS};
         long long nw = 0;   // chunks this group has handed to P.V
         long long j0 = 0;   // the CTA's chunk index of the segment's first chunk
         int k = 0;          // segments so far
@@ -812,15 +814,16 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             const long long qrow0 = vh_qrow0(gp, cs.b, vh);
             const bool live = row < gv;
             float m_ref = -INFINITY, l = 0.f;
-            if (n > 0 && wg == 0) {
-                // the query rows into the Q buffer (K-major, 128-byte swizzle);
+            if (n > 0) {
+                // the query rows into the Q buffer (K-major, 128-byte swizzle),
+                // group g the 16-byte pieces 4g..4g+3 of each 128-byte line;
                 // zero for heads past the slice's
                 const uint4 *qs = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) +
                                                                   (qrow0 + row) * D);
 #pragma unroll
                 for (int pl = 0; pl < C::LINES; ++pl)
 #pragma unroll
-                    for (int c16 = 0; c16 < 8; ++c16) {
+                    for (int c16 = 4 * wg; c16 < 4 * wg + 4; ++c16) {
                         const uint4 v = live ? __ldg(qs + pl * 8 + c16) : make_uint4(0, 0, 0, 0);
                         const uint32_t a =
                             qbuf + (uint32_t)(pl * C::QPLANE + row * 128 + ((c16 ^ (row & 7)) << 4));
@@ -971,17 +974,17 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             }
             j0 += n;
 
-            // ---- segment end: group 1 hands over its (m_ref, l), group 0 merges ----
-            float *xk = xch + (k & 1) * C::M * 2;
-            if (wg == 1) {
-                xk[2 * row] = had ? m_ref : -INFINITY;
-                xk[2 * row + 1] = had ? l : 0.f;
-            }
+            // ---- segment end: the groups swap their (m_ref, l) and share the work ----
+            float *xk = xch + (k & 1) * 2 * C::M * 2;   // [group][row][2]
+            xk[(wg * C::M + row) * 2] = had ? m_ref : -INFINITY;
+            xk[(wg * C::M + row) * 2 + 1] = had ? l : 0.f;
             ++k;
+            tc_fence_before();
             if (!sb.sync(lane)) {
                 dead = true;
                 break;
             }
+            tc_fence_after();
             Seg nx = cs;
             seg_next(p, ctx, nx);
             // after the CTA's last segment no copy is in flight into the
@@ -994,8 +997,13 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 st.mb[0] = MRG0;
                 st.mb[1] = MRG1;
             }
-            if (wg == 0 && !tc_segment_end<C, D>(gp, ctx, cs, slice, G, gv, qrow0, bhv, had, m_ref, l, xk[2 * row],
-                                                   xk[2 * row + 1], row, lane, tid, tl, misc, scratch, wb, st)) {
+            // its syncs spin: both groups are in it, nothing else to run
+            WarpBar se{SEGBAR, sb.phase, 0u};
+            const bool ok = tc_segment_end<C, D>(gp, ctx, cs, slice, G, gv, qrow0, bhv, xk[2 * row], xk[2 * row + 1],
+                                                 xk[(C::M + row) * 2], xk[(C::M + row) * 2 + 1], wg, row, lane, tid,
+                                                 tl, misc, scratch, se, st);
+            sb.phase = se.phase;
+            if (!ok) {
                 dead = true;
                 break;
             }

@@ -372,7 +372,7 @@ __device__ __forceinline__ bool tc8_epilogue(const GqaParams &gp, const Ctx ctx,
         }
     }
     if (!complete)
-        return tc_arrive_merge<D, C::MERGE_PB>(gp, ctx, cs, slice, gv, qrow0, bhv, len, lane, tid, misc, scratch, wb);
+        return tc_arrive_merge<D, C::MERGE_PB, 128>(gp, ctx, cs, slice, gv, qrow0, bhv, len, lane, tid, misc, scratch, wb);
     return true;
 }
 
