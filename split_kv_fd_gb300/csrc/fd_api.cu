@@ -156,9 +156,14 @@ bool gqa_use_tc(int in_dtype, int d, int G, bool paged)
 #ifndef FD_TC_SEG_COST_KB
 #define FD_TC_SEG_COST_KB 768
 #endif
-int tc_seg_cost(int d)
+// The same for the FP8 tcgen05 kernel (fd_gqa_tc8.cuh).
+#ifndef FD_TC8_SEG_COST_KB
+#define FD_TC8_SEG_COST_KB 256
+#endif
+// In tokens of K and V rows of d elements of `es` bytes.
+int seg_cost_tokens(long long kb, int d, int es)
 {
-    return (int)(FD_TC_SEG_COST_KB * 1024LL / (2LL * 2 * d));   // K and V rows of 16-bit elements
+    return (int)(kb * 1024LL / (2LL * es * d));
 }
 
 // The block-table view of a paged K/V cache.
@@ -402,8 +407,8 @@ fd_status gqa_common(const void *q, const void *k, const void *v, const int32_t 
     gp.k_scale = k_scale;
     gp.v_scale = v_scale;
     set_fused(p, pl, wl, workspace, scale, out, out_dtype, lse, st);
-    if (tc && pl.decomp == DECOMP_BALANCED)
-        p.seg_cost = tc_seg_cost(d);
+    if (pl.decomp == DECOMP_BALANCED && (tc || tc8))
+        p.seg_cost = tc ? seg_cost_tokens(FD_TC_SEG_COST_KB, d, 2) : seg_cost_tokens(FD_TC8_SEG_COST_KB, d, 1);
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (!clear_counters(p, (long long)B * Hv, cs))
         return FD_ERR_CUDA;
