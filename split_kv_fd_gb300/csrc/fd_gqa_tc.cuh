@@ -385,7 +385,11 @@ __device__ __forceinline__ bool tc_merge_staged(const SplitParams &p, int G, int
     }
     if (into < 0)
         return true;
-    fence_proxy_async_global();   // the next batch copies this slot back in
+    // the next batch copies this slot back in through the async proxy, which
+    // reads L2: the stores must have reached it (a barrier orders them only
+    // within the CTA)
+    __threadfence();
+    fence_proxy_async_global();
     return wb.sync(tid & 31);
 }
 
@@ -965,8 +969,13 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             if (dead)
                 break;
             if (had) {
-                // the group's last P.V: its O is final
-                if (!mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
+                // the group's last P.V: its O is final.  A parity wait is
+                // unambiguous only once the phase before it is complete: S of
+                // the group's last chunk waited for P.V of its chunk three
+                // back (NSB = 4 ahead), not for the one before the last, so
+                // that phase is waited for first.
+                if ((nw >= 2 && !mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 2) & 1), C::SLEEP_NS)) ||
+                    !mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }

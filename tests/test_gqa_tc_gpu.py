@@ -96,3 +96,22 @@ def test_many_short_sequences():
     lens = [(37 * i) % 301 for i in range(96)]
     q, k, v, lt = _gqa_case(96, 128, 2, 300, 128, "f16", lens, seed=3)
     _run(q, k, v, lt, "f16")
+
+
+def test_alternating_queries_reuse_the_workspace():
+    """Two query sets in turn, eight launches through the same workspace,
+    with 152 pieces merged in three batches: the last arriver reads the
+    other pieces' partials and its own intermediate batches back from the
+    workspace, so a read that saw the previous launch's data (the same
+    slots, the other query set) would show against each set's oracle."""
+    _, k, v, lt = random_case(1, 1, 60000, 128, "bf16", lens=None, seed=21)
+    qs = [torch.randn(1, 128, 128, generator=torch.Generator().manual_seed(s)).to(torch.bfloat16) for s in (1, 2)]
+    refs = [oracle.attention_gqa(q, k, v, lens=lt) for q in qs]
+    kd, vd, ld = k.to(DEV), v.to(DEV), lt.to(DEV)
+    for r in range(8):
+        i = r % 2
+        od = torch.float32 if r < 4 else torch.bfloat16
+        out, lse = fd.decode_gqa(qs[i].to(DEV), kd, vd, ld, out_dtype=od)
+        check_out(out, refs[i][0], "bf16")
+        check_lse(lse, refs[i][1], "bf16")
+    assert fd.device_status() == 0
