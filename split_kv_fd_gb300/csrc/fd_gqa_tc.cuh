@@ -94,9 +94,9 @@ template <typename T, int D> struct TcCfg {
     static constexpr int TMEM_O = NSB * CT;
     static constexpr uint32_t TMEM_COLS = 512;
     // mbarriers: full/empty of the K and V buffers, s_full[NSB],
-    // s_free[NSB], p_full[NSB], o_full[2], q_full, fin (2), seg (both
+    // s_free[NSB], p_full[NSB], o_full[2][2], q_full, fin (2), seg (both
     // groups), the two of a merge staged in the ring
-    static constexpr int NBAR = 2 * RING_BUFS + 3 * NSB + 8;
+    static constexpr int NBAR = 2 * RING_BUFS + 3 * NSB + 10;
     static constexpr float TAU = 8.f;              // lazy-rescale threshold (base 2)
     // every wait suspends the waiting thread in hardware (woken when the
     // phase completes) rather than polling
@@ -595,13 +595,19 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
     // of chunk j, so no phase is missed
     auto PFULL = [&](int b) { return bar0 + 8u * (uint32_t)(BS + 2 * NSB + b); };
     constexpr int B0 = BS + 3 * NSB;
-    auto OFULL = [&](int g) { return bar0 + 8u * (uint32_t)(B0 + g); };
-    const uint32_t QFULL = bar0 + 8u * (B0 + 2);
-    const uint32_t FINS = bar0 + 8u * (B0 + 3);
-    const uint32_t FINP = bar0 + 8u * (B0 + 4);
-    const uint32_t SEGBAR = bar0 + 8u * (B0 + 5);
-    const uint32_t MRG0 = bar0 + 8u * (B0 + 6), MRG1 = bar0 + 8u * (B0 + 7);
-    static_assert(B0 + 8 == C::NBAR, "barrier count");
+    // P.V of chunk j (group j % 2) commits o_full[j % 2][(j / 2) % 2]: a
+    // barrier per group and parity of the group's chunk count, so that one
+    // phase there is chunk j and the one before it chunk j - 4, which S of
+    // chunk j waited for (P.V completes in order); a wait for a chunk's P.V
+    // is then never two phases away from the barrier's
+    auto OFULL = [&](int g, int b) { return bar0 + 8u * (uint32_t)(B0 + 2 * g + b); };
+    auto OFULL_J = [&](long long j) { return OFULL((int)(j & 1), (int)((j >> 1) & 1)); };
+    const uint32_t QFULL = bar0 + 8u * (B0 + 4);
+    const uint32_t FINS = bar0 + 8u * (B0 + 5);
+    const uint32_t FINP = bar0 + 8u * (B0 + 6);
+    const uint32_t SEGBAR = bar0 + 8u * (B0 + 7);
+    const uint32_t MRG0 = bar0 + 8u * (B0 + 8), MRG1 = bar0 + 8u * (B0 + 9);
+    static_assert(B0 + 10 == C::NBAR, "barrier count");
 
     if (tid == 0) {
         for (int s = 0; s < KST; ++s) {
@@ -617,8 +623,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
             mbar_init(SFREE(b), 1);   // commit after P.V of the buffer's chunk
             mbar_init(PFULL(b), 4);   // the owning group's warps: P in TMEM, V's tail rows zeroed
         }
-        for (int g = 0; g < 2; ++g)
-            mbar_init(OFULL(g), 1);   // commit after the group's P.V
+        for (int g = 0; g < 4; ++g)
+            mbar_init(OFULL(g >> 1, g & 1), 1);   // commit after P.V of the group's chunk
         mbar_init(QFULL, 8);          // both groups have written their halves of Q
         mbar_init(FINS, 1);           // the MMA issuers' last commits
         mbar_init(FINP, 1);
@@ -786,7 +792,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                                       ID_O, (c >= 2 || ks > 0 || hl > 0) ? 1u : 0u);
                         }
                     }
-                    tc_commit(OFULL(g));
+                    tc_commit(OFULL_J(j));
                     tc_commit(EMPTYV(vs));
                     tc_commit(SFREE(sb));
                 }
@@ -804,7 +810,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         const uint32_t tl = tmem + ((uint32_t)((w & 3) * 32) << 16);
         const uint32_t ocol = (uint32_t)(C::TMEM_O + wg * D);
         WarpBar sb{SEGBAR, 0u, C::SLEEP_NS};
-        long long nw = 0;   // chunks this group has handed to P.V
+        long long jl = -1;  // the CTA's chunk index of the last chunk this group handed to P.V
         long long j0 = 0;   // the CTA's chunk index of the segment's first chunk
         int k = 0;          // segments so far
         Seg cs;
@@ -893,10 +899,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 // warp-wide, so the whole warp runs them when any of its
                 // heads grew (a = 1 for the others)
                 if (had && __any_sync(FULL_MASK, grow)) {
-                    // once the group's previous P.V is done (P.V of its chunk
-                    // before that is: S of this chunk waited for it, so the
-                    // phase is unambiguous)
-                    if (!mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
+                    // once the group's previous P.V (chunk jl = j - 2) is done
+                    if (!mbar_wait_bounded_sleep(OFULL_J(jl), (uint32_t)((jl >> 2) & 1), C::SLEEP_NS)) {
                         dead = true;
                         break;
                     }
@@ -963,19 +967,14 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(PFULL((int)(j % NSB)));
-                ++nw;
+                jl = j;
                 had = true;
             }
             if (dead)
                 break;
             if (had) {
-                // the group's last P.V: its O is final.  A parity wait is
-                // unambiguous only once the phase before it is complete: S of
-                // the group's last chunk waited for P.V of its chunk three
-                // back (NSB = 4 ahead), not for the one before the last, so
-                // that phase is waited for first.
-                if ((nw >= 2 && !mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 2) & 1), C::SLEEP_NS)) ||
-                    !mbar_wait_bounded_sleep(OFULL(wg), (uint32_t)((nw - 1) & 1), C::SLEEP_NS)) {
+                // the group's last P.V: its O is final
+                if (!mbar_wait_bounded_sleep(OFULL_J(jl), (uint32_t)((jl >> 2) & 1), C::SLEEP_NS)) {
                     dead = true;
                     break;
                 }
