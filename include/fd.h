@@ -175,7 +175,11 @@ fd_status fd_decode_paged(const void *q, const void *k_pages, const void *v_page
  * From 17 query heads per K/V head (MQA included; contiguous cache, d = 64
  * or 128) they are tcgen05 products with accumulators in tensor memory, all
  * of a K/V head's query heads (slices of at most 128) served from one copy
- * of each K/V chunk.  The workspace size is
+ * of each K/V chunk.  With num_splits == 0 the tcgen05 kernels divide the
+ * (b, K/V head, token) space after charging every (b, K/V head) a fixed
+ * start cost (the segment end and the reload that switching sequences
+ * takes), so a CTA that starts a sequence streams fewer tokens; the result
+ * does not depend on the division (up to rounding).  The workspace size is
  * fd_workspace_size_gqa(...), one size for fd_decode_gqa,
  * fd_decode_gqa_paged and fd_decode_gqa_fp8.  Returns FD_ERR_UNSUPPORTED for
  * f32 with G > 1.
@@ -196,10 +200,14 @@ fd_status fd_decode_gqa(const void *q, const void *k, const void *v, const int32
  *             e4m3(byte), likewise V
  *   k_scale, v_scale  [B*Hkv] float32, device
  *   workspace fd_workspace_size_gqa(B, Hq, Hkv, N, d, num_splits) bytes
- * d must be 64, 128 or 256.  The E4M3 rows are converted exactly to f16 in
- * shared memory and the products run on the tensor cores in f16 with fp32
- * accumulation, q brought into the f16 range per query head by a power of
- * two that the scores undo; query heads in slices of at most 8.  G == 1 is
+ * d must be 64, 128 or 256.  At d = 128 (G >= 2) both products run in FP8
+ * on the tcgen05 tensor cores straight from the cache bytes: q and P are
+ * each split into three E4M3 parts of weights 1, 2^-4 and 2^-8 (about 12
+ * significant bits), q brought to amax in [128, 256) per query head by a
+ * power of two that the scores undo.  At d = 64 and 256 the E4M3 rows are
+ * converted exactly to f16 in shared memory and the products run on the
+ * tensor cores in f16 with fp32 accumulation, q brought into the f16 range
+ * the same way.  Query heads in slices of at most 8.  G == 1 is
  * fd_decode_fp8.
  */
 fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, const void *v,
@@ -218,8 +226,10 @@ fd_status fd_decode_gqa_fp8(const void *q, fd_dtype q_dtype, const void *k, cons
  *   workspace         fd_workspace_size_gqa(B, Hq, Hkv, max_pages*page_size,
  *                     d, num_splits) bytes
  * d must be 64, 128 or 256, page_size 16 or a multiple of 32 and
- * num_pages*Hkv < 2^31; any G >= 1 (G = 1 runs the same kernel).
- * FD_ERR_UNSUPPORTED otherwise.
+ * num_pages*Hkv < 2^31; any G >= 1 (G = 1 runs the same kernel).  At
+ * d = 128 with G >= 2 and pages of a multiple of 128 tokens the FP8
+ * tcgen05 products of fd_decode_gqa_fp8 run, else the f16 conversion.
+ * Other head dims or page sizes return FD_ERR_UNSUPPORTED.
  */
 fd_status fd_decode_gqa_paged_fp8(const void *q, fd_dtype q_dtype, const void *k_pages, const void *v_pages,
                                   const float *k_scale, const float *v_scale, const int32_t *block_table,
