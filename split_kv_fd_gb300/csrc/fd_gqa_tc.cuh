@@ -28,8 +28,9 @@
 // Warp roles (384 threads, one CTA per SM):
 //  - warps 0-3 and 4-7: two softmax warpgroups taking the chunks in turn
 //    (chunk j of the CTA goes to group j % 2), each with its own O
-//    accumulator and (m_ref, l) per head; at a segment end group 0 merges
-//    the two states ("FlashDecoding 数学推导" §2.4.2) and writes the result;
+//    accumulator and (m_ref, l) per head; at a segment end both merge the
+//    two states ("FlashDecoding 数学推导" §2.4.2), each for half of the
+//    columns, and write the result;
 //  - warps 8 and 9: the K and V producers (lane 0 each), chunks by
 //    tensor-map TMA into rings of their own: a K buffer is refilled once S
 //    of its chunk is done, a V buffer once P.V is;
@@ -165,7 +166,7 @@ __device__ __forceinline__ void store_out4(void *out, long long idx, int out_dty
     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + idx) = make_uint2(a, b);
 }
 
-// One batch of the last arriver's merge, on 128 threads: the m/l/o merge
+// One batch of the last arriver's merge, on NT threads: the m/l/o merge
 // ("FlashDecoding 数学推导" §2.4.2) of the n <= MERGE_PB workspace partials
 // whose slots are in ss[0..n-1], for each of the Gv query rows.  Each thread
 // takes four elements of a head at a time and the pieces' partials and
@@ -393,11 +394,12 @@ __device__ __forceinline__ bool tc_merge_staged(const SplitParams &p, int G, int
     return wb.sync(tid & 31);
 }
 
-// Stage 2 of a (b, virtual head) by the last piece to arrive, on softmax
-// group 0: the merge of its `target` workspace partials, in batches of at
-// most MERGE_PB pieces; each batch but the last leaves its result in its
-// last piece's slot, which starts the next batch.  Returns false if a
-// barrier wait expired.
+// Stage 2 of a (b, virtual head) by the last piece to arrive, on the NT
+// threads of barrier `wb`: the merge of its `target` workspace partials, in
+// batches of at most MERGE_PB pieces; each batch but the last leaves its
+// result in its last piece's slot, which starts the next batch.  Staged in
+// shared memory when `st` gives the idle ring.  Returns false if a barrier
+// wait expired.
 template <int D, int MERGE_PB, int NT>
 __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &ctx, long long bhv, int slice,
                                                 int G, int Gv, long long qrow0, unsigned target, int gf,
@@ -410,7 +412,7 @@ __device__ __forceinline__ bool tc_merge_pieces(const GqaParams &gp, const Ctx &
     float *sL = sM + G;                                              // [G]
     const int n = (int)target;
     int first = 0;
-    uint32_t mph = 0;   // the staging mbarriers' phases (one staged merge per CTA)
+    uint32_t mph = 0;   // the staging mbarriers' phases (a CTA stages one merge, at its last segment)
     for (;;) {
         const int cnt = min(n - first, MERGE_PB);
         for (int i = tid; i < cnt; i += NT)
@@ -709,7 +711,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::THREADS, 1) gqa_tc_kernel(const _
         // ------------------------------------------------------------ S issuer
         // S of each chunk as soon as its K has landed and its S/P buffer is
         // free (P.V of chunk j - NSB done); the first S of a segment once
-        // group 0 has written the segment's Q
+        // both groups have written the segment's Q
         if (lane == 0) {
             constexpr int BF = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
             constexpr uint32_t ID_S = idesc_f16(BF, 0, 0, C::M, C::CT);   // Q K-major, K K-major
