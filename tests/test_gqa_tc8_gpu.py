@@ -128,3 +128,9 @@ def test_large_pages_equal_contiguous(page_size):
                                        lt.to(DEV), out_dtype=torch.float32)
     assert torch.equal(out, cout) and torch.equal(lse, clse)
     assert fd.device_status() == 0
+
+
+def test_start_charge_empty_pieces():
+    """Sequences of 1, 2 and 3000 tokens with 4 K/V heads: the start charge
+    per sequence makes most of the short sequences' spans empty pieces."""
+    _check(*_case(3, 4, 8, 3000, [1, 2, 3000], seed=9), G=8)

@@ -115,3 +115,14 @@ def test_alternating_queries_reuse_the_workspace():
         check_out(out, refs[i][0], "bf16")
         check_lse(lse, refs[i][1], "bf16")
     assert fd.device_status() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_start_charge_empty_pieces(d):
+    """Sequences of 1, 2 and 5000 tokens: the automatic decomposition charges
+    every sequence a start cost in the space the CTAs divide, so the short
+    sequences' spans are mostly charge, and a dozen CTAs each hold an empty
+    piece (no tokens) of the same sequence next to the one that holds its
+    tokens; the merge gives the empty pieces weight 0."""
+    q, k, v, lt = _gqa_case(3, 64, 1, 5000, d, "bf16", [1, 2, 5000], seed=31 + d)
+    _run(q, k, v, lt, "bf16")
